@@ -1,0 +1,266 @@
+/*
+ * ss_oracle.c -- plain, slow CPU oracle for sampled-softmax cross-entropy over
+ * a shared candidate set.
+ *
+ * TEST INFRASTRUCTURE. Only the test suite, the smoke check and the CPU
+ * baseline / reference arms of the benchmark load this library. The CUDA
+ * library never calls it, and the two share no code, headers or tables.
+ *
+ * What is computed, and where it comes from:
+ *   - "KellerJordan/modded-nanogpt" README, technique list: the training loss
+ *     is a sampled softmax over ONE candidate set shared by the whole batch.
+ *   - "NanoGPT Training Record: Technical Optimizations & Speed", section "Key
+ *     Optimizations and Ablation Table Results" (and "Technical Architecture
+ *     and Implementation Details"): only the candidate rows of the vocabulary
+ *     are scored, in both the forward and the backward pass; the candidate
+ *     count follows a schedule that ends at the full vocabulary (C = V).
+ *   - the record tweet quoted on the airebao page: a token that occurs in the
+ *     batch is always scored, a token that does not is scored only sometimes.
+ *     Reading: every batch target is a candidate; the rest of the set is
+ *     filled with sampled non-target ids.
+ * The pages give no formula. The textbook softmax cross-entropy restricted to
+ * the candidate rows is written out below, step by step, in the pages' terms:
+ *
+ *   candidates  u = sorted unique targets (U of them); k = C - U negatives =
+ *               the k non-target ids with the smallest keys, sorted by id;
+ *               cand = u ++ negatives; slot[t] = position of target[t] in u.
+ *   forward     s[t][j] = sum_d H[t][d] * W[cand[j]][d]           (d ascending)
+ *               lse[t]  = m + log(sum_j exp(s[t][j] - m)), m = max_j s[t][j]
+ *               loss[t] = lse[t] - s[t][slot[t]]
+ *   backward    G[t][j] = scale * (exp(s[t][j] - lse[t]) - [j == slot[t]])
+ *               dH[t]   = sum_j G[t][j] * W[cand[j]]               (j ascending)
+ *               dW[cand[j]] = sum_t G[t][j] * H[t]                 (t ascending)
+ *
+ * Negative-sampling key (the pages name no sampler; reading: uniform without
+ * replacement over the non-targets, driven by a counter-based generator so
+ * that a CPU and a GPU implementation can agree bit for bit):
+ *   key(v) = (high 32 bits of SplitMix64 output number v of a stream whose
+ *             state starts at `seed`) * 2^32 + v
+ *   where output number i (0-based) of SplitMix64 (Steele, Lea and Flood,
+ *   "Fast splittable pseudorandom number generators", OOPSLA 2014; the
+ *   splitmix64.c reference by S. Vigna) is mix(seed + (i + 1) * 0x9E3779B97F4A7C15).
+ *
+ * Precision: the definition is fp32. Its inputs are bf16 bit patterns widened
+ * exactly to float. An fp64 instantiation of the same loops, on double inputs,
+ * exists for the finite-difference and library cross-checks. Build with
+ * -ffp-contract=off so that x86-64 and aarch64 round identically.
+ *
+ * Parallelism: OpenMP over independent output rows only (tokens for the
+ * forward and dH, candidate rows for dW); every sum keeps the order above.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+enum {
+  ORC_OK = 0,
+  ORC_ERR_INVALID = 1,
+  ORC_ERR_CAPACITY = 3,     /* more unique targets than candidate slots */
+  ORC_ERR_TARGET_RANGE = 4, /* a target id outside [0, V) */
+  ORC_ERR_NOMEM = 8
+};
+
+static float bf16_to_float(uint16_t b) {
+  uint32_t u = (uint32_t)b << 16;
+  float f;
+  memcpy(&f, &u, sizeof f);
+  return f;
+}
+
+/* ---------------------------------------------------------------- SplitMix64 */
+
+uint64_t orc_splitmix64_output(uint64_t seed, uint64_t i) {
+  uint64_t z = seed + (i + 1u) * 0x9E3779B97F4A7C15ull;
+  z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+  z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+  return z ^ (z >> 31);
+}
+
+uint64_t orc_negative_key(uint64_t seed, int64_t v) {
+  uint64_t hi = orc_splitmix64_output(seed, (uint64_t)v) >> 32;
+  return (hi << 32) | (uint64_t)(uint32_t)v;
+}
+
+/* ---------------------------------------------------------- candidate build */
+
+static int cmp_i32(const void* a, const void* b) {
+  int32_t x = *(const int32_t*)a, y = *(const int32_t*)b;
+  return (x > y) - (x < y);
+}
+
+static int cmp_u64(const void* a, const void* b) {
+  uint64_t x = *(const uint64_t*)a, y = *(const uint64_t*)b;
+  return (x > y) - (x < y);
+}
+
+/* index of v in the sorted array u[0..n), or -1 */
+static int64_t find_sorted(const int32_t* u, int64_t n, int32_t v) {
+  int64_t lo = 0, hi = n;
+  while (lo < hi) {
+    int64_t mid = lo + (hi - lo) / 2;
+    if (u[mid] < v) lo = mid + 1;
+    else hi = mid;
+  }
+  return (lo < n && u[lo] == v) ? lo : -1;
+}
+
+/*
+ * Build the shared candidate set of one batch.
+ *   targets[T] in [0, V); cand[C] and slot[T] are written; *U_out = U.
+ * Returns ORC_ERR_TARGET_RANGE if a target is outside [0, V) and
+ * ORC_ERR_CAPACITY if U > C (then *U_out is still set and cand/slot are not).
+ */
+int orc_build_candidates(const int32_t* targets, int64_t T, int64_t V, int64_t C,
+                         uint64_t seed, int32_t* cand, int32_t* slot, int64_t* U_out) {
+  if (T < 0 || V <= 0 || C <= 0 || C > V) return ORC_ERR_INVALID;
+  for (int64_t t = 0; t < T; ++t)
+    if (targets[t] < 0 || targets[t] >= V) return ORC_ERR_TARGET_RANGE;
+
+  /* u = sorted unique targets */
+  int32_t* u = (int32_t*)malloc(sizeof(int32_t) * (size_t)(T > 0 ? T : 1));
+  if (!u) return ORC_ERR_NOMEM;
+  memcpy(u, targets, sizeof(int32_t) * (size_t)T);
+  qsort(u, (size_t)T, sizeof(int32_t), cmp_i32);
+  int64_t U = 0;
+  for (int64_t i = 0; i < T; ++i)
+    if (U == 0 || u[U - 1] != u[i]) u[U++] = u[i];
+  *U_out = U;
+  if (U > C) { free(u); return ORC_ERR_CAPACITY; }
+
+  /* negatives: the k non-targets with the smallest keys, then sorted by id */
+  int64_t k = C - U;
+  int64_t n_non = V - U;
+  uint64_t* keys = (uint64_t*)malloc(sizeof(uint64_t) * (size_t)(n_non > 0 ? n_non : 1));
+  if (!keys) { free(u); return ORC_ERR_NOMEM; }
+  int64_t n = 0;
+  for (int64_t v = 0; v < V; ++v)
+    if (find_sorted(u, U, (int32_t)v) < 0) keys[n++] = orc_negative_key(seed, v);
+  qsort(keys, (size_t)n, sizeof(uint64_t), cmp_u64);
+  int32_t* neg = (int32_t*)malloc(sizeof(int32_t) * (size_t)(k > 0 ? k : 1));
+  if (!neg) { free(keys); free(u); return ORC_ERR_NOMEM; }
+  for (int64_t i = 0; i < k; ++i) neg[i] = (int32_t)(keys[i] & 0xFFFFFFFFull);
+  qsort(neg, (size_t)k, sizeof(int32_t), cmp_i32);
+
+  for (int64_t i = 0; i < U; ++i) cand[i] = u[i];
+  for (int64_t i = 0; i < k; ++i) cand[U + i] = neg[i];
+  for (int64_t t = 0; t < T; ++t) slot[t] = (int32_t)find_sorted(u, U, targets[t]);
+
+  free(neg);
+  free(keys);
+  free(u);
+  return ORC_OK;
+}
+
+/* ------------------------------------------------------ forward / backward */
+/*
+ * The loops below are written once as a macro and instantiated twice:
+ *   f32: inputs are bf16 bit patterns, arithmetic in float (the definition);
+ *   f64: inputs are doubles, arithmetic in double (finite differences and
+ *        library cross-checks, which need inputs that are not on the bf16 grid).
+ * Row subsets: `rows` (token indices, nrows of them) or NULL for all T rows;
+ * `cols` (candidate indices j, ncols of them) or NULL for all C candidates.
+ * Outputs for a subset are packed in subset order.
+ */
+#define LOAD_BF16(x) bf16_to_float(x)
+#define LOAD_REAL(x) (x)
+
+#define ORC_DEFINE(REAL, SUF, IN_T, LOAD, EXP, LOG)                                          \
+  /* logits of token t against every candidate: s[j], j = 0..C-1 */                         \
+  static void logits_##SUF(const IN_T* H, const IN_T* W, const int32_t* cand, int64_t C,    \
+                           int64_t D, int64_t t, REAL* s) {                                 \
+    const IN_T* h = H + t * D;                                                               \
+    for (int64_t j = 0; j < C; ++j) {                                                        \
+      const IN_T* w = W + (int64_t)cand[j] * D;                                              \
+      REAL acc = 0;                                                                          \
+      for (int64_t d = 0; d < D; ++d) acc += (REAL)LOAD(h[d]) * (REAL)LOAD(w[d]);            \
+      s[j] = acc;                                                                            \
+    }                                                                                        \
+  }                                                                                          \
+                                                                                             \
+  void orc_forward_##SUF(const IN_T* H, const IN_T* W, const int32_t* cand,                  \
+                         const int32_t* slot, int64_t T, int64_t C, int64_t D,               \
+                         const int64_t* rows, int64_t nrows, REAL* loss, REAL* lse) {        \
+    int64_t n = rows ? nrows : T;                                                            \
+    _Pragma("omp parallel")                                                                  \
+    {                                                                                        \
+      REAL* s = (REAL*)malloc(sizeof(REAL) * (size_t)C);                                     \
+      _Pragma("omp for schedule(dynamic, 1)")                                                \
+      for (int64_t i = 0; i < n; ++i) {                                                      \
+        int64_t t = rows ? rows[i] : i;                                                      \
+        logits_##SUF(H, W, cand, C, D, t, s);                                                \
+        REAL m = s[0];                                                                       \
+        for (int64_t j = 1; j < C; ++j)                                                      \
+          if (s[j] > m) m = s[j];                                                            \
+        REAL sum = 0;                                                                        \
+        for (int64_t j = 0; j < C; ++j) sum += EXP(s[j] - m);                                \
+        REAL l = m + LOG(sum);                                                               \
+        lse[i] = l;                                                                          \
+        loss[i] = l - s[slot[t]];                                                            \
+      }                                                                                      \
+      free(s);                                                                               \
+    }                                                                                        \
+  }                                                                                          \
+                                                                                             \
+  /* dH rows: needs lse of those tokens (lse_rows packed like rows) */                       \
+  void orc_backward_dH_##SUF(const IN_T* H, const IN_T* W, const int32_t* cand,              \
+                             const int32_t* slot, const REAL* lse_rows, int64_t T,           \
+                             int64_t C, int64_t D, REAL scale, const int64_t* rows,          \
+                             int64_t nrows, REAL* dH) {                                      \
+    int64_t n = rows ? nrows : T;                                                            \
+    _Pragma("omp parallel")                                                                  \
+    {                                                                                        \
+      REAL* s = (REAL*)malloc(sizeof(REAL) * (size_t)C);                                     \
+      _Pragma("omp for schedule(dynamic, 1)")                                                \
+      for (int64_t i = 0; i < n; ++i) {                                                      \
+        int64_t t = rows ? rows[i] : i;                                                      \
+        logits_##SUF(H, W, cand, C, D, t, s);                                                \
+        REAL* out = dH + i * D;                                                              \
+        for (int64_t d = 0; d < D; ++d) out[d] = 0;                                          \
+        for (int64_t j = 0; j < C; ++j) {                                                    \
+          REAL y = (j == slot[t]) ? (REAL)1 : (REAL)0;                                       \
+          REAL g = scale * (EXP(s[j] - lse_rows[i]) - y);                                    \
+          const IN_T* w = W + (int64_t)cand[j] * D;                                          \
+          for (int64_t d = 0; d < D; ++d) out[d] += g * (REAL)LOAD(w[d]);                    \
+        }                                                                                    \
+      }                                                                                      \
+      free(s);                                                                               \
+    }                                                                                        \
+  }                                                                                          \
+                                                                                             \
+  /* dW_c rows (candidate index j): needs lse of ALL T tokens */                             \
+  void orc_backward_dW_##SUF(const IN_T* H, const IN_T* W, const int32_t* cand,              \
+                             const int32_t* slot, const REAL* lse, int64_t T, int64_t C,     \
+                             int64_t D, REAL scale, const int64_t* cols, int64_t ncols,      \
+                             REAL* dWc) {                                                    \
+    int64_t n = cols ? ncols : C;                                                            \
+    _Pragma("omp parallel for schedule(dynamic, 1)")                                         \
+    for (int64_t i = 0; i < n; ++i) {                                                        \
+      int64_t j = cols ? cols[i] : i;                                                        \
+      const IN_T* w = W + (int64_t)cand[j] * D;                                              \
+      REAL* out = dWc + i * D;                                                               \
+      for (int64_t d = 0; d < D; ++d) out[d] = 0;                                            \
+      for (int64_t t = 0; t < T; ++t) {                                                      \
+        const IN_T* h = H + t * D;                                                           \
+        REAL st = 0;                                                                         \
+        for (int64_t d = 0; d < D; ++d) st += (REAL)LOAD(h[d]) * (REAL)LOAD(w[d]);           \
+        REAL y = (j == slot[t]) ? (REAL)1 : (REAL)0;                                         \
+        REAL g = scale * (EXP(st - lse[t]) - y);                                             \
+        for (int64_t d = 0; d < D; ++d) out[d] += g * (REAL)LOAD(h[d]);                      \
+      }                                                                                      \
+    }                                                                                        \
+  }
+
+ORC_DEFINE(float, f32, uint16_t, LOAD_BF16, expf, logf)
+ORC_DEFINE(double, f64, double, LOAD_REAL, exp, log)
+
+int orc_num_threads(void) {
+#ifdef _OPENMP
+  return omp_get_max_threads();
+#else
+  return 1;
+#endif
+}

@@ -1,0 +1,430 @@
+"""Pins for the CPU oracle, against facts that do not come from the oracle itself.
+
+* candidate set: published SplitMix64 outputs, set invariants, brute force over
+  every k-subset on tiny vocabularies, and a chi-square test of uniformity;
+* forward: the full-vocabulary case equals dense cross-entropy (torch), any
+  candidate set equals torch's cross-entropy on the candidate columns, zero
+  logits give ln C, and a two-candidate case has a closed form;
+* backward: torch autograd in fp64, central finite differences in fp64, closed
+  forms with H = 0 and with W = 0, and the invariants of P - Y;
+* a mutation check: planting plausible mistakes in the oracle's C source makes
+  at least one of these checks fail.
+"""
+import itertools
+import json
+import math
+import os
+import subprocess
+import sys
+
+import numpy as np
+import pytest
+import torch
+import torch.nn.functional as F
+
+import synth
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def _f64(bits):
+    return synth.bf16_bits_to_f32(bits).astype(np.float64)
+
+
+def _vectors():
+    out = []
+    with open(os.path.join(GOLDEN, "splitmix64_vectors.txt")) as f:
+        for line in f:
+            if line.strip() and not line.startswith("#"):
+                s, i, o = (int(x) for x in line.split())
+                out.append((s, i, o))
+    return out
+
+
+# ----------------------------------------------------------------- generator
+
+def test_splitmix64_published_vectors(orc):
+    vec = _vectors()
+    assert len(vec) >= 6
+    for seed, i, out in vec:
+        assert orc.splitmix64_output(seed, i) == out
+
+
+def test_negative_key_layout(orc):
+    # high half = high 32 bits of the published output number v; low half = v
+    for seed, i, out in _vectors():
+        key = orc.negative_key(seed, i)
+        assert key >> 32 == out >> 32
+        assert key & 0xFFFFFFFF == i
+
+
+# ------------------------------------------------------------ candidate set
+
+def check_candidates(targets, V, C, cand, slot, U):
+    t = np.asarray(targets)
+    u = np.unique(t)
+    assert U == len(u)
+    assert cand.shape == (C,) and cand.dtype == np.int32
+    assert np.array_equal(cand[:U], u), "targets first, ascending"
+    neg = cand[U:]
+    assert np.all(np.diff(neg) > 0), "negatives ascending and distinct"
+    assert not np.isin(neg, u).any(), "no target among negatives"
+    assert np.all((neg >= 0) & (neg < V))
+    assert np.array_equal(cand[slot], t), "cand[slot[t]] == target[t]"
+    assert np.all((slot >= 0) & (slot < U))
+
+
+@pytest.mark.parametrize("T,V,C,s,seed", [
+    (1, 10, 1, 1.1, 0),
+    (1, 10, 10, 1.1, 1),
+    (64, 300, 64, 1.1, 2),
+    (256, 50304, 4096, 1.1, 0),
+    (2000, 5000, 5000, 1.0, 5),     # full vocabulary
+    (5000, 700, 700, 0.5, 6),       # nearly every id is a target
+])
+def test_candidate_invariants(orc, T, V, C, s, seed):
+    rng = np.random.default_rng(seed)
+    targets = synth.zipf_targets(rng, T, V, s)
+    U = len(np.unique(targets))
+    if U > C:
+        C = U
+    cand, slot, U2 = orc.build_candidates(targets, V, C, seed)
+    check_candidates(targets, V, C, cand, slot, U2)
+    if C == V:
+        assert np.array_equal(np.sort(cand), np.arange(V))
+
+
+def test_candidates_exact_fill(orc):
+    # U == C: no negatives at all
+    targets = np.array([5, 3, 3, 9, 0, 5], np.int32)
+    cand, slot, U = orc.build_candidates(targets, 12, 4, 1)
+    assert U == 4 and list(cand) == [0, 3, 5, 9]
+    assert list(slot) == [2, 1, 1, 3, 0, 2]
+
+
+def test_candidates_bruteforce_tiny(orc):
+    # the chosen negatives are the k-subset of non-targets whose sorted key
+    # tuple is smallest, found by enumerating every k-subset
+    rng = np.random.default_rng(11)
+    cases = 0
+    for V in range(2, 10):
+        for _ in range(6):
+            T = int(rng.integers(1, V + 1))
+            targets = rng.integers(0, V, size=T).astype(np.int32)
+            U = len(np.unique(targets))
+            for C in range(U, V + 1):
+                seed = int(rng.integers(0, 2**63))
+                cand, slot, U2 = orc.build_candidates(targets, V, C, seed)
+                non = [v for v in range(V) if v not in set(targets.tolist())]
+                k = C - U
+                best = None
+                for sub in itertools.combinations(non, k):
+                    key = tuple(sorted(orc.negative_key(seed, v) for v in sub))
+                    if best is None or key < best[0]:
+                        best = (key, sorted(sub))
+                assert list(cand[U:]) == best[1]
+                check_candidates(targets, V, C, cand, slot, U2)
+                cases += 1
+    assert cases > 100
+
+
+def test_candidates_uniform_chi2(orc):
+    # V = 6, targets {0, 2}: 4 non-targets, k = 2 -> 6 equally likely subsets
+    targets = np.array([0, 2, 2], np.int32)
+    counts = {}
+    n = 6000
+    for seed in range(n):
+        cand, _, U = orc.build_candidates(targets, 6, 4, seed)
+        counts[tuple(cand[U:])] = counts.get(tuple(cand[U:]), 0) + 1
+    assert len(counts) == 6
+    exp = n / 6
+    chi2 = sum((c - exp) ** 2 / exp for c in counts.values())
+    assert chi2 < 20.52  # 5 degrees of freedom, p = 0.001
+
+
+def test_candidates_errors(orc):
+    with pytest.raises(orc.OracleError) as e:
+        orc.build_candidates(np.array([1, 10], np.int32), 10, 5, 0)
+    assert e.value.code == 4
+    with pytest.raises(orc.OracleError) as e:
+        orc.build_candidates(np.array([1, -1], np.int32), 10, 5, 0)
+    assert e.value.code == 4
+    with pytest.raises(orc.OracleError) as e:
+        orc.build_candidates(np.array([1, 2, 3, 4], np.int32), 10, 3, 0)
+    assert e.value.code == 3 and e.value.U == 4
+
+
+def test_seed_changes_negatives(orc):
+    targets = np.array([1, 2, 3], np.int32)
+    a, _, _ = orc.build_candidates(targets, 1000, 50, 1)
+    b, _, _ = orc.build_candidates(targets, 1000, 50, 2)
+    assert np.array_equal(a[:3], b[:3]) and not np.array_equal(a[3:], b[3:])
+
+
+# ------------------------------------------------------------------ forward
+
+def _case(T, V, D, C, seed, w_std=0.3, s=1.1):
+    x = synth.make_inputs(T, V, D, s, seed, w_std=w_std)
+    U = len(np.unique(x["targets"]))
+    C = max(C, U)
+    return x, C
+
+
+def _torch_ref(H64, W64, cand, slot, scale=1.0):
+    Ht = torch.tensor(H64, requires_grad=True)
+    Wt = torch.tensor(W64, requires_grad=True)
+    logits = Ht @ Wt[torch.from_numpy(cand.astype(np.int64))].T
+    y = torch.from_numpy(slot.astype(np.int64))
+    loss = F.cross_entropy(logits, y, reduction="none")
+    (scale * loss.sum()).backward()
+    return (loss.detach().numpy(), torch.logsumexp(logits, 1).detach().numpy(),
+            Ht.grad.numpy(), Wt.grad.numpy())
+
+
+def test_forward_full_vocab_equals_dense_ce(orc):
+    T, V, D = 40, 300, 32
+    x = synth.make_inputs(T, V, D, 1.1, 3, w_std=0.3)
+    cand, slot, U = orc.build_candidates(x["targets"], V, V, 3)
+    H64, W64 = _f64(x["H"]), _f64(x["W"])
+    dense = F.cross_entropy(torch.tensor(H64 @ W64.T), torch.from_numpy(x["targets"].astype(np.int64)),
+                            reduction="none").numpy()
+    l64, _ = orc.forward(x["H"], x["W"], cand, slot, dtype=np.float64)
+    l32, _ = orc.forward(x["H"], x["W"], cand, slot)
+    np.testing.assert_allclose(l64, dense, rtol=1e-12, atol=0)
+    np.testing.assert_allclose(l32, dense, rtol=2e-5, atol=0)
+
+
+@pytest.mark.parametrize("T,V,D,C,seed", [(33, 200, 24, 50, 1), (7, 64, 8, 9, 2), (100, 1000, 64, 300, 3)])
+def test_forward_equals_ce_on_candidate_columns(orc, T, V, D, C, seed):
+    x, C = _case(T, V, D, C, seed)
+    cand, slot, U = orc.build_candidates(x["targets"], V, C, seed)
+    loss, lse, _, _ = _torch_ref(_f64(x["H"]), _f64(x["W"]), cand, slot)
+    l64, s64 = orc.forward(x["H"], x["W"], cand, slot, dtype=np.float64)
+    np.testing.assert_allclose(l64, loss, rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(s64, lse, rtol=1e-12, atol=1e-13)
+    l32, s32 = orc.forward(x["H"], x["W"], cand, slot)
+    np.testing.assert_allclose(l32, loss, rtol=1e-5, atol=1e-6)
+    assert np.all(l64 >= 0)
+
+
+@pytest.mark.parametrize("C", [1, 5, 4096, 10240])
+def test_uniform_logits_give_ln_C(orc, C):
+    T, V, D = 6, max(C, 16), 16
+    x = synth.make_inputs(T, V, D, 1.1, 4)
+    cand, slot, U = orc.build_candidates(x["targets"] % C if C < 16 else x["targets"], V, C, 4)
+    for H, W in ((np.zeros_like(x["H"]), x["W"]), (x["H"], np.zeros_like(x["W"]))):
+        loss, lse = orc.forward(H, W, cand, slot)
+        assert np.all(np.abs(loss - math.log(C)) <= 2e-7 * max(1.0, math.log(C)))
+        np.testing.assert_array_equal(loss, lse)
+
+
+def test_two_candidate_closed_form(orc):
+    # every target is id 1 of V = 3, C = 2: one negative n; with logits a (target)
+    # and b (negative), loss = log(1 + e^(b - a)) and dL/dh = sigmoid(b - a) (w_n - w_1)
+    W = synth.f32_to_bf16_bits(np.array([[0.5, -1.25], [2.0, 0.75], [-0.5, 1.5]], np.float32))
+    H = synth.f32_to_bf16_bits(np.array([[1.0, 0.0], [0.0, 1.0], [2.0, -1.0], [0.25, 0.5]], np.float32))
+    targets = np.ones(4, np.int32)
+    cand, slot, U = orc.build_candidates(targets, 3, 2, 9)
+    assert U == 1 and cand[0] == 1 and cand[1] in (0, 2)
+    w = synth.bf16_bits_to_f32(W).astype(np.float64)
+    h = synth.bf16_bits_to_f32(H).astype(np.float64)
+    a, b = h @ w[1], h @ w[cand[1]]
+    loss = np.log1p(np.exp(b - a))
+    sig = 1 / (1 + np.exp(-(b - a)))
+    l, lse = orc.forward(H, W, cand, slot, dtype=np.float64)
+    np.testing.assert_allclose(l, loss, rtol=1e-12, atol=1e-15)
+    np.testing.assert_allclose(lse, a + loss, rtol=1e-14)
+    dH = orc.backward_dH(H, W, cand, slot, lse, dtype=np.float64)
+    np.testing.assert_allclose(dH, sig[:, None] * (w[cand[1]] - w[1])[None, :], rtol=1e-13, atol=1e-15)
+    dWc = orc.backward_dWc(H, W, cand, slot, lse, dtype=np.float64)
+    np.testing.assert_allclose(dWc[0], -(sig[:, None] * h).sum(0), rtol=1e-13)
+    np.testing.assert_allclose(dWc[1], (sig[:, None] * h).sum(0), rtol=1e-13)
+
+
+# ----------------------------------------------------------------- backward
+
+@pytest.mark.parametrize("T,V,D,C,seed,scale", [(33, 200, 24, 50, 1, 1.0), (50, 120, 16, 120, 2, 0.02),
+                                                (100, 1000, 64, 300, 3, 1.0 / 100)])
+def test_backward_matches_torch_autograd(orc, T, V, D, C, seed, scale):
+    x, C = _case(T, V, D, C, seed)
+    cand, slot, U = orc.build_candidates(x["targets"], V, C, seed)
+    _, _, gH, gW = _torch_ref(_f64(x["H"]), _f64(x["W"]), cand, slot, scale)
+    r64 = orc.loss_and_grads(x["H"], x["W"], x["targets"], C, seed, scale, dtype=np.float64)
+    np.testing.assert_allclose(r64["dH"], gH, rtol=1e-10, atol=1e-13)
+    np.testing.assert_allclose(r64["dW"], gW, rtol=1e-10, atol=1e-13)
+    r32 = orc.loss_and_grads(x["H"], x["W"], x["targets"], C, seed, scale)
+    for k, ref in (("dH", gH), ("dW", gW)):
+        err = np.linalg.norm(r32[k] - ref) / np.linalg.norm(ref)
+        assert err < 1e-5, (k, err)
+
+
+def test_backward_finite_differences(orc):
+    rng = np.random.default_rng(21)
+    T, V, D, C, scale = 3, 9, 6, 5, 0.7
+    H = rng.standard_normal((T, D))
+    W = rng.standard_normal((V, D)) * 0.8
+    targets = np.array([4, 1, 4], np.int32)
+    cand, slot, U = orc.build_candidates(targets, V, C, 5)
+
+    def L(H_, W_):
+        loss, _ = orc.forward(H_, W_, cand, slot, dtype=np.float64)
+        return scale * loss.sum()
+
+    _, lse = orc.forward(H, W, cand, slot, dtype=np.float64)
+    dH = orc.backward_dH(H, W, cand, slot, lse, scale, dtype=np.float64)
+    dWc = orc.backward_dWc(H, W, cand, slot, lse, scale, dtype=np.float64)
+    dW = np.zeros_like(W)
+    dW[cand] = dWc
+    eps = 1e-6
+    for M, G in ((H, dH), (W, dW)):
+        num = np.zeros_like(M)
+        for idx in np.ndindex(M.shape):
+            keep = M[idx]
+            M[idx] = keep + eps
+            lp = L(H, W)
+            M[idx] = keep - eps
+            lm = L(H, W)
+            M[idx] = keep
+            num[idx] = (lp - lm) / (2 * eps)
+        assert np.linalg.norm(num - G) <= 1e-6 * np.linalg.norm(G) + 1e-9
+    # rows of W outside the candidate set carry no gradient
+    outside = np.setdiff1d(np.arange(V), cand)
+    assert outside.size == V - C and np.all(dW[outside] == 0)
+
+
+def test_backward_W_zero_closed_form(orc):
+    # W = 0: P is uniform 1/C, so dH = 0 and dWc[j] = scale * sum_t (1/C - [slot_t == j]) H[t]
+    T, V, D, C, scale = 20, 50, 8, 12, 0.5
+    x, C = _case(T, V, D, C, 8, w_std=0.02)
+    W0 = np.zeros_like(x["W"])
+    r = orc.loss_and_grads(x["H"], W0, x["targets"], C, 8, scale, dtype=np.float64)
+    assert np.all(r["dH"] == 0)
+    Y = np.zeros((T, C))
+    Y[np.arange(T), r["slot"]] = 1
+    ref = scale * (1.0 / C - Y).T @ _f64(x["H"])
+    np.testing.assert_allclose(r["dWc"], ref, rtol=1e-12, atol=1e-14)
+
+
+def test_backward_H_zero_closed_form(orc):
+    # H = 0: dWc = 0 and dH[t] = scale * (mean_j W[cand[j]] - W[target_t])
+    T, V, D, C, scale = 20, 50, 8, 12, 2.0
+    x, C = _case(T, V, D, C, 9, w_std=0.5)
+    H0 = np.zeros_like(x["H"])
+    r = orc.loss_and_grads(H0, x["W"], x["targets"], C, 9, scale, dtype=np.float64)
+    assert np.all(r["dWc"] == 0)
+    W64 = _f64(x["W"])
+    ref = scale * (W64[r["cand"]].mean(0)[None, :] - W64[x["targets"]])
+    np.testing.assert_allclose(r["dH"], ref, rtol=1e-12, atol=1e-14)
+
+
+def test_backward_invariants(orc):
+    T, V, D, C = 64, 500, 32, 100
+    x, C = _case(T, V, D, C, 12, w_std=0.2)
+    rng = np.random.default_rng(0)
+    dW0 = rng.standard_normal((V, D)).astype(np.float32)
+    r = orc.loss_and_grads(x["H"], x["W"], x["targets"], C, 12, dW_init=dW0)
+    # rows of P - Y sum to zero -> candidate-row gradients sum to zero
+    colsum = np.abs(r["dWc"].astype(np.float64).sum(0)).max()
+    assert colsum <= 1e-5 * np.abs(r["dWc"]).max()
+    # <dWc, W_c> = sum G*S = <dH, H>
+    lhs = float((r["dWc"].astype(np.float64) * _f64(x["W"])[r["cand"]]).sum())
+    rhs = float((r["dH"].astype(np.float64) * _f64(x["H"])).sum())
+    assert abs(lhs - rhs) <= 1e-4 * (abs(lhs) + 1e-3)
+    # rows outside the candidate set are left as given
+    outside = np.setdiff1d(np.arange(V), r["cand"])
+    assert np.array_equal(r["dW"][outside], dW0[outside])
+    # accumulate adds instead of overwriting
+    ra = orc.loss_and_grads(x["H"], x["W"], x["targets"], C, 12, dW_init=dW0, accumulate=True)
+    np.testing.assert_allclose(ra["dW"][r["cand"]], dW0[r["cand"]] + r["dWc"], rtol=1e-6, atol=1e-7)
+    assert np.array_equal(ra["dW"][outside], dW0[outside])
+
+
+def test_row_subsets_match_full(orc):
+    T, V, D, C = 40, 400, 32, 90
+    x, C = _case(T, V, D, C, 13)
+    cand, slot, U = orc.build_candidates(x["targets"], V, C, 13)
+    loss, lse = orc.forward(x["H"], x["W"], cand, slot)
+    rows = np.array([39, 0, 17, 17, 5])
+    l2, s2 = orc.forward(x["H"], x["W"], cand, slot, rows=rows)
+    assert np.array_equal(l2, loss[rows]) and np.array_equal(s2, lse[rows])
+    dH = orc.backward_dH(x["H"], x["W"], cand, slot, lse)
+    dH2 = orc.backward_dH(x["H"], x["W"], cand, slot, lse[rows], rows=rows)
+    assert np.array_equal(dH2, dH[rows])
+    dWc = orc.backward_dWc(x["H"], x["W"], cand, slot, lse)
+    cols = np.array([C - 1, 0, 3])
+    assert np.array_equal(orc.backward_dWc(x["H"], x["W"], cand, slot, lse, cols=cols), dWc[cols])
+
+
+# ------------------------------------------------------ planted mistakes
+
+MUTATIONS = [
+    ("drop one-hot term in dH", "REAL g = scale * (EXP(s[j] - lse_rows[i]) - y);",
+     "REAL g = scale * (EXP(s[j] - lse_rows[i]));"),
+    ("sign of the log-sum", "REAL l = m + LOG(sum);", "REAL l = m - LOG(sum);"),
+    ("transposed operand in dW", "for (int64_t d = 0; d < D; ++d) out[d] += g * (REAL)LOAD(h[d]);",
+     "for (int64_t d = 0; d < D; ++d) out[d] += g * (REAL)LOAD(w[d]);"),
+    ("wrong target index", "loss[i] = l - s[slot[t]];", "loss[i] = l - s[0];"),
+    ("dropped term of the dot product", "for (int64_t d = 0; d < D; ++d) acc +=",
+     "for (int64_t d = 1; d < D; ++d) acc +="),
+    ("negatives left in key order", "qsort(neg, (size_t)k, sizeof(int32_t), cmp_i32);", ""),
+    ("targets not deduplicated", "if (U == 0 || u[U - 1] != u[i]) u[U++] = u[i];", "u[U++] = u[i];"),
+    ("wrong hash constant", "0xBF58476D1CE4E5B9ull", "0xBF58476D1CE4E5B8ull"),
+]
+
+
+def _battery(orc):
+    """Run a compact set of the pins above; return the names of those that fail."""
+    failed = []
+    try:
+        for seed, i, out in _vectors():
+            assert orc.splitmix64_output(seed, i) == out
+    except AssertionError:
+        failed.append("vectors")
+    T, V, D, C = 30, 150, 16, 40
+    x, C = _case(T, V, D, C, 31)
+    try:
+        cand, slot, U = orc.build_candidates(x["targets"], V, C, 31)
+        check_candidates(x["targets"], V, C, cand, slot, U)
+    except (AssertionError, Exception):
+        failed.append("candidates")
+        return failed
+    _, _, gH, gW = _torch_ref(_f64(x["H"]), _f64(x["W"]), cand, slot)
+    loss, lse, _, _ = _torch_ref(_f64(x["H"]), _f64(x["W"]), cand, slot)
+    l64, s64 = orc.forward(x["H"], x["W"], cand, slot, dtype=np.float64)
+    if not np.allclose(l64, loss, rtol=1e-10):
+        failed.append("forward")
+    dH = orc.backward_dH(x["H"], x["W"], cand, slot, s64, dtype=np.float64)
+    dWc = orc.backward_dWc(x["H"], x["W"], cand, slot, s64, dtype=np.float64)
+    if not np.allclose(dH, gH, rtol=1e-8, atol=1e-12):
+        failed.append("dH")
+    if not np.allclose(dWc, gW[cand], rtol=1e-8, atol=1e-12):
+        failed.append("dW")
+    return failed
+
+
+def _battery_in_subprocess(so_path):
+    """Run the battery against another build of the oracle in a child process, so
+    that a planted mistake which corrupts memory cannot take the test run down."""
+    here = os.path.dirname(os.path.abspath(__file__))
+    code = ("import json, sys; sys.path[:0] = [%r, %r]; import oracle, test_oracle as t; "
+            "oracle._lib = oracle.load(%r); print('BATTERY', json.dumps(t._battery(oracle)))"
+            % (os.path.dirname(here), here, str(so_path)))
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, timeout=300)
+    for line in r.stdout.splitlines():
+        if line.startswith("BATTERY "):
+            return json.loads(line[len("BATTERY "):])
+    return [f"crashed (exit {r.returncode})"]
+
+
+def test_pins_catch_planted_mistakes(orc, tmp_path):
+    src = open(orc._SRC).read()
+    assert _battery(orc) == []
+    for i, (name, old, new) in enumerate(MUTATIONS):
+        assert src.count(old) >= 1, name
+        mut = tmp_path / f"mut{i}.c"
+        mut.write_text(src.replace(old, new))
+        so = tmp_path / f"mut{i}.so"
+        subprocess.run(["gcc", "-O1", "-std=c11", "-fopenmp", "-ffp-contract=off", "-fPIC", "-shared",
+                        "-o", str(so), str(mut), "-lm"], check=True)
+        failed = _battery_in_subprocess(so)
+        assert failed, f"planted mistake not caught: {name}"
