@@ -1,0 +1,442 @@
+#!/usr/bin/env python
+"""Benchmark of the sampled-softmax CE hot path on GB300.
+
+One step = one pass of the whole path over one synthetic batch: candidate
+build, forward (loss + saved lse) and backward (dH, dW candidate rows), i.e.
+ss_build_candidates + ss_forward + ss_backward through the C ABI.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 2]
+                    [--impl native|reference] [--no-cpu-baseline]
+
+Prints ONE JSON line on rank 0. `value` is tokens/s of the whole job with the
+inputs resident in device memory (device-timed with CUDA events, L2 flushed by
+a 256 MB write between steps, outside the timed events). `e2e` is the same
+metric through the public Python API with the step's inputs (H, targets)
+copied from pinned host memory and the per-token loss read back, every step.
+`roofline` is for the kernel with the largest share of the step, timed live
+with CUDA events on its launch stream. `cpu_baseline` / `--impl reference`
+time the CPU oracle (the plain definition, not tuned) on a bounded sample of
+the same workload on this machine's host cores.
+
+Multi-GPU: the path does not shard across GPUs in this library (one GPU, no
+collectives), so N > 1 runs N independent replicas, one per rank (weak
+scaling), with a barrier around the timed region and the max time over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "sampled-softmax CE fwd+bwd tokens/s; % of GB300 bf16 tensor peak"
+UNIT = "tokens/s"
+L2_FLUSH_BYTES = 256 << 20
+GEMM_KERNELS = ("gemm_forward_lse", "gemm_softmax_grad", "gemm_grad_h", "gemm_grad_w_scatter")
+CSRC = os.path.join(ROOT, "sampled_softmax_output_gb300", "csrc")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=None,
+                    help="timed steps (default: enough for ~3 s of device time)")
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", type=int, default=2, choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="target CPU seconds of the oracle sample")
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------------ helpers
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {"bf16_tflops": float(p["bf16_tflops"]),
+                "bf16_tflops_sustained": float(p["bf16_tflops_sustained"]),
+                "hbm_gbs": float(p["hbm_gbs"]), "source": "measured"}
+    except Exception:
+        return {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0,
+                "source": "fallback"}
+
+
+def csrc_sha() -> str:
+    h = hashlib.sha256()
+    for name in sorted(os.listdir(CSRC)):
+        with open(os.path.join(CSRC, name), "rb") as f:
+            h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()[:16]
+
+
+def load_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, or None
+    if there is none or the kernel sources changed since it was captured."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            lines = [ln.strip() for ln in f if ln.strip() and not ln.startswith("#")]
+    except OSError:
+        return None
+    sha = csrc_sha()
+    for ln in lines:
+        parts = dict(kv.split("=", 1) for kv in ln.split())
+        if parts.get("kernel") == kernel and parts.get("workload") == workload:
+            if parts.get("src_sha") != sha:
+                return None
+            return float(parts["dram_bytes_per_launch"])
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons while it runs."""
+
+    QUERY = ("index,uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid: str | None):
+        self.uuid = uuid
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.out = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=self.out, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+            return
+        t0 = time.time()
+        while time.time() - t0 < 10:  # wait for the first sample
+            if os.path.getsize(self.path) > 0:
+                break
+            time.sleep(0.02)
+
+    def stop(self):
+        if self.proc is None:
+            return {"samples": 0, "sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.out.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                c = [x.strip() for x in line.split(",")]
+                if len(c) < 10:
+                    continue
+                if self.uuid and self.uuid not in c[1]:
+                    continue
+                rows.append(c)
+        os.unlink(self.path)
+        if not rows:
+            return {"samples": 0, "sm_mhz": None, "sm_max_mhz": None, "reasons": []}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[2]) for r in rows if num(r[2]) is not None]
+        mx = [num(r[3]) for r in rows if num(r[3]) is not None]
+        pw = [num(r[4]) for r in rows if num(r[4]) is not None]
+        reasons = set()
+        for r in rows:
+            for name, col in (("hw_slowdown", 6), ("hw_thermal_slowdown", 7),
+                              ("sw_thermal_slowdown", 8), ("sw_power_cap", 9)):
+                if r[col].lower().startswith("active"):
+                    reasons.add(name)
+        return {"samples": len(rows), "sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "power_w_max": max(pw) if pw else None, "reasons": sorted(reasons)}
+
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        backend = "nccl" if (args.impl == "native" and torch.cuda.is_available()) else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ------------------------------------------------------------- CPU oracle
+
+def oracle_sample(x: dict, w, T_s: int, scale: float):
+    """One oracle pass over a bounded sample: the full-batch candidate build,
+    then forward + backward for the first T_s tokens against that candidate
+    set. Returns seconds."""
+    import oracle
+    t0 = time.perf_counter()
+    cand, slot, U = oracle.build_candidates(x["targets"], w.V, w.C, w.seed)
+    Hs = x["H"][:T_s]
+    ss_ = slot[:T_s]
+    loss, lse = oracle.forward(Hs, x["W"], cand, ss_)
+    oracle.backward_dH(Hs, x["W"], cand, ss_, lse, scale)
+    oracle.backward_dWc(Hs, x["W"], cand, ss_, lse, scale)
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(x: dict, w, target_s: float) -> dict:
+    import oracle
+    oracle.build()
+    scale = 1.0 / w.T
+    t_small = oracle_sample(x, w, 16, scale)
+    T_s = int(max(16, min(w.T, 16 * target_s / max(t_small, 1e-3))))
+    dt = oracle_sample(x, w, T_s, scale)
+    return {"value": T_s / dt, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": (f"{w.name}: full-batch candidate build (T={w.T}) + forward/backward of the "
+                       f"first {T_s} tokens against all C={w.C} candidates; {dt:.1f} s"),
+            "seconds": dt, "tokens": T_s}
+
+
+# ------------------------------------------------------------ native arm
+
+def run_native(args, world, rank, local):
+    import torch
+
+    import sampled_softmax_output_gb300 as ss
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    w = synth.WORKLOADS[args.workload]
+    T, V, C, D = w.T, w.V, w.C, w.D
+    x = synth.workload_inputs(w)
+    H = torch.from_numpy(x["H"].view(np.int16)).to(dev).view(torch.bfloat16)
+    W = torch.from_numpy(x["W"].view(np.int16)).to(dev).view(torch.bfloat16)
+    targets = torch.from_numpy(x["targets"]).to(dev)
+    ws = ss.workspace(T, V, C, D, device=dev)
+    cand = torch.empty(C, dtype=torch.int32, device=dev)
+    slot = torch.empty(T, dtype=torch.int32, device=dev)
+    loss = torch.empty(T, dtype=torch.float32, device=dev)
+    lse = torch.empty(T, dtype=torch.float32, device=dev)
+    dH = torch.empty(T, D, dtype=torch.bfloat16, device=dev)
+    dW = torch.zeros(V, D, dtype=torch.float32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    scale = 1.0 / T
+
+    def step(h=H, tg=targets):
+        ss.build_candidates(tg, V, C, w.seed, ws, cand=cand, slot=slot)
+        ss.forward(h, W, cand, slot, ws, loss=loss, lse=lse)
+        ss.backward(h, W, cand, slot, lse, ws, scale=scale, dH=dH, dW=dW)
+
+    for _ in range(max(args.warmup, 1)):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    st, _ = ss.read_status(ws)
+    if st != 0:
+        raise RuntimeError(f"device status {st} after warm-up")
+
+    # size the timed region: ~3 s of device time unless --steps is given
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    step()
+    e1.record()
+    torch.cuda.synchronize()
+    est_ms = e0.elapsed_time(e1)
+    K = args.steps if args.steps is not None else int(min(3000, max(20, 3000.0 / max(est_ms, 1e-3))))
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    uuid = None
+    try:
+        uuid = str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        pass
+    sampler = ClockSampler(uuid)
+    barrier(world)
+    torch.cuda.synchronize()
+    sampler.start()
+    trace = ss.KernelTrace(capacity=16 * K)
+    with trace:
+        for k in range(K):
+            flush.zero_()
+            starts[k].record()
+            step()
+            ends[k].record()
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    barrier(world)
+    total_ms = sum(s.elapsed_time(e) for s, e in zip(starts, ends))
+    total_ms_max = max_over_ranks(total_ms, world, dev)
+    st, _ = ss.read_status(ws)
+    if st != 0:
+        raise RuntimeError(f"device status {st} after the timed region")
+
+    # per-kernel times from the trace
+    per = {}
+    for name, ms in trace.timings():
+        per.setdefault(name, []).append(ms)
+    launches = trace.count
+    kern = {n: {"launches": len(v), "avg_ms": sum(v) / len(v), "total_ms": sum(v)}
+            for n, v in per.items()}
+    traced_total = sum(k["total_ms"] for k in kern.values())
+    for k in kern.values():
+        k["share"] = k["total_ms"] / traced_total if traced_total > 0 else None
+    dom = max(kern, key=lambda n: kern[n]["total_ms"])
+    peaks = load_peaks()
+    flops = 2.0 * T * C * D
+    if dom in GEMM_KERNELS:
+        achieved = flops / (kern[dom]["avg_ms"] * 1e-3) / 1e12
+        peak = peaks["bf16_tflops"]
+        roof = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak,
+                "unit": "TFLOP/s", "frac": achieved / peak,
+                "traffic": load_traffic(dom, w.name),
+                "peak_source": f"{peaks['source']} bf16 burst (MEASURED_PEAKS.json)"
+                if peaks["source"] == "measured" else "fallback",
+                "frac_of_sustained": achieved / peaks["bf16_tflops_sustained"],
+                "algorithmic_flops_per_launch": flops}
+    else:
+        roof = {"bound": "hbm", "kernel": dom, "achieved": None, "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "frac": None, "traffic": None}
+
+    tokens_per_s = world * T * K / (total_ms_max * 1e-3)
+    ms_per_step = total_ms_max / K
+    step_tflops = 6.0 * T * C * D / (ms_per_step * 1e-3) / 1e12
+
+    # end to end through the public API: H2D of H and targets from pinned
+    # memory, the three calls, D2H of the per-token loss, every step
+    H_pin = torch.from_numpy(x["H"].view(np.int16)).pin_memory()
+    tg_pin = torch.from_numpy(x["targets"]).pin_memory()
+    loss_pin = torch.empty(T, dtype=torch.float32).pin_memory()
+    H_dev = torch.empty(T, D, dtype=torch.int16, device=dev)
+    tg_dev = torch.empty(T, dtype=torch.int32, device=dev)
+    Ke = max(3, min(K, 50))
+    es = [torch.cuda.Event(enable_timing=True) for _ in range(Ke)]
+    ee = [torch.cuda.Event(enable_timing=True) for _ in range(Ke)]
+    barrier(world)
+    for k in range(Ke):
+        flush.zero_()
+        es[k].record()
+        H_dev.copy_(H_pin, non_blocking=True)
+        tg_dev.copy_(tg_pin, non_blocking=True)
+        step(H_dev.view(torch.bfloat16), tg_dev)
+        loss_pin.copy_(loss, non_blocking=True)
+        ee[k].record()
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in zip(es, ee)), world, dev)
+    e2e = {"value": world * T * Ke / (e2e_ms * 1e-3), "unit": UNIT,
+           "h2d_bytes_per_step": int(H_pin.numel() * 2 + tg_pin.numel() * 4),
+           "d2h_bytes_per_step": int(loss_pin.numel() * 4), "steps": Ke}
+
+    line = {
+        "metric": METRIC, "value": tokens_per_s, "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.name, "T": T, "V": V, "C": C, "D": D, "zipf_s": w.zipf_s,
+                   "seed": w.seed, "parallelism": f"replicas x{world}" if world > 1 else "single",
+                   "l2": "flushed between steps (256 MB write, outside the timed events)",
+                   "step": "ss_build_candidates + ss_forward + ss_backward",
+                   "step_tflops_algorithmic_6TCD": step_tflops,
+                   "pct_bf16_peak_algorithmic": 100.0 * step_tflops / peaks["bf16_tflops"]},
+        "roofline": roof,
+        "kernels": kern,
+        "gpu_launches": launches,
+        "e2e": e2e,
+        "clocks": clocks,
+    }
+    return line, x, w
+
+
+def run_reference(args, world, rank):
+    """The CPU oracle as it stands on this machine's host cores, rank 0 only."""
+    if rank != 0:
+        return None
+    import oracle
+    oracle.build()
+    w = synth.WORKLOADS[args.workload]
+    x = synth.workload_inputs(w)
+    K = args.steps if args.steps is not None else 3
+    W_ = max(args.warmup, 0)
+    per_step_s = min(5.0, 150.0 / max(K + W_, 1))
+    scale = 1.0 / w.T
+    t_small = oracle_sample(x, w, 8, scale)
+    T_s = int(max(1, min(w.T, 8 * per_step_s / max(t_small, 1e-3))))
+    for _ in range(W_):
+        oracle_sample(x, w, T_s, scale)
+    dt = 0.0
+    for _ in range(K):
+        dt += oracle_sample(x, w, T_s, scale)
+    value = T_s * K / dt
+    cores = oracle.num_threads()
+    sample = (f"{w.name}: per step, full-batch candidate build (T={w.T}) + forward/backward of "
+              f"the first {T_s} tokens against all C={w.C} candidates")
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": K, "warmup": W_, "ms_per_step": 1e3 * dt / K, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": w.name, "T": w.T, "V": w.V, "C": w.C, "D": w.D,
+                       "sample_tokens_per_step": T_s},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    args = parse_args()
+    world, rank, local = dist_setup(args)
+    if args.impl == "reference":
+        line = run_reference(args, world, rank)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return
+    line, x, w = run_native(args, world, rank, local)
+    if rank == 0:
+        if world == 1 and not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline(x, w, args.cpu_seconds)
+        else:
+            line["cpu_baseline"] = None
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

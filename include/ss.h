@@ -1,0 +1,177 @@
+/*
+ * ss.h -- C ABI of libss, sampled-softmax cross-entropy over a shared candidate
+ * set, forward and backward, as hand-written CUDA for GB300 (sm_103a).
+ *
+ * The method. The lm_head of a language model scores every vocabulary row for
+ * every token; sampled softmax scores only a candidate subset of the rows, in
+ * the forward and in the backward pass, with one candidate set shared by the
+ * whole batch:
+ *   - "KellerJordan/modded-nanogpt" README, technique list (sampled softmax
+ *     over a shared candidate set for most of training);
+ *   - "NanoGPT Training Record: Technical Optimizations & Speed", section "Key
+ *     Optimizations and Ablation Table Results" (fewer vocabulary elements
+ *     scored in forward and backward; candidate counts 10,240, 14,336 and
+ *     24,576, then all 50,304 rows for the final steps), and section
+ *     "Technical Architecture and Implementation Details";
+ *   - the record tweet quoted on the airebao page (a token present in the
+ *     batch is always scored; absent tokens only some of the time).
+ * Definitions used here (textbook softmax cross-entropy restricted to the
+ * candidate rows; notation: T tokens, D model width, V vocabulary rows,
+ * C candidates, U distinct targets):
+ *   cand   = the sorted distinct targets, then C - U non-target ids chosen
+ *            uniformly without replacement (seeded; see ss_build_candidates),
+ *            sorted by id;        slot[t] = index of target[t] in cand.
+ *   S      = H . W[cand]^T                         (T x C logits, fp32)
+ *   lse[t] = log sum_j exp(S[t,j]);   loss[t] = lse[t] - S[t, slot[t]]
+ *   G      = scale * (exp(S - lse) - onehot(slot))
+ *   dH     = G . W[cand];             dW[cand[j]] = (G^T . H)[j]
+ *
+ * Conventions for every entry point:
+ *   - Every pointer argument except U_host / device_status_host / U_status_host
+ *     is a DEVICE pointer on the current CUDA device. The caller owns every
+ *     buffer; the library allocates no device memory and keeps no state
+ *     between calls other than what it writes into the caller's workspace.
+ *   - bf16 tensors are passed as uint16_t bit patterns. Matrices are
+ *     row-major and dense: H [T, D], W [V, D], dH [T, D], dW [V, D].
+ *   - H, W, dH, dW and the workspace must be 16-byte aligned; targets, cand,
+ *     slot, loss, lse 4-byte aligned. Misaligned pointers -> SS_ERR_INVALID.
+ *   - Work is enqueued asynchronously on `stream` (a cudaStream_t; NULL means
+ *     the legacy default stream). Only ss_build_candidates with a non-NULL
+ *     U_host, and ss_read_status, synchronise that stream.
+ *   - Argument errors are returned before anything is enqueued. Errors found
+ *     on the device (a target id outside [0, V), more distinct targets than
+ *     C, a cand or slot entry out of range, a device wait that timed out) are
+ *     recorded in a status word inside the workspace: the first error wins,
+ *     later kernels of any call that shares the workspace see it and do no
+ *     work, and ss_read_status returns it. ss_build_candidates clears it.
+ *   - Limits: 1 <= C <= V <= SS_MAX_V; 0 <= T < 2^31; D % 64 == 0 and
+ *     64 <= D <= SS_MAX_D. Out of range -> SS_ERR_UNSUPPORTED (or
+ *     SS_ERR_INVALID for values that can never be valid).
+ *   - No C++ exception crosses this boundary.
+ */
+#ifndef SS_H_
+#define SS_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define SS_MAX_V 524288
+#define SS_MAX_D 16384
+
+typedef enum ss_status {
+  SS_OK = 0,
+  SS_ERR_INVALID = 1,      /* bad argument: null pointer, bad size, misalignment */
+  SS_ERR_UNSUPPORTED = 2,  /* valid in principle, outside this library's limits */
+  SS_ERR_CAPACITY = 3,     /* U > C: more distinct targets than candidate slots */
+  SS_ERR_TARGET_RANGE = 4, /* a target id outside [0, V) */
+  SS_ERR_WORKSPACE = 5,    /* workspace smaller than ss_workspace_size() */
+  SS_ERR_CUDA = 6,         /* a CUDA runtime/driver call or launch failed */
+  SS_ERR_TIMEOUT = 7,      /* a device-side wait gave up (kernel returned early) */
+  SS_ERR_INDEX = 8         /* a cand entry outside [0, V) or slot outside [0, C) */
+} ss_status;
+
+typedef void* ss_stream; /* cudaStream_t */
+
+/*
+ * Bytes of device workspace that ss_build_candidates, ss_forward and
+ * ss_backward need for problem size (T, V, C, D); 0 if the sizes are invalid.
+ * One workspace serves all three calls of a batch. Contents: a status header,
+ * the gathered candidate rows W[cand] (C x D bf16), per-tile softmax partials
+ * of the forward pass, and the bf16 softmax-gradient matrix G (T x C) of the
+ * backward pass.
+ */
+size_t ss_workspace_size(int64_t T, int64_t V, int64_t C, int64_t D);
+
+/*
+ * Build the shared candidate set of one batch
+ * ("KellerJordan/modded-nanogpt" README, technique list; airebao page, the
+ * quoted record tweet: every in-batch target is scored).
+ *   targets [T] int32, device: token ids, each in [0, V).
+ *   seed        : selects the negatives. Non-target id v gets the key
+ *                 (high 32 bits of SplitMix64 output number v of the stream
+ *                 seeded with `seed`) * 2^32 + v; the C - U non-targets with
+ *                 the smallest keys are the negatives (a uniform sample
+ *                 without replacement when the keys behave as random).
+ *   cand [C] int32, device, out: sorted distinct targets in [0, U), then the
+ *                 negatives in ascending id order in [U, C).
+ *   slot [T] int32, device, out: cand[slot[t]] == targets[t].
+ *   U_host      : NULL, or a host int32 that receives U after the stream is
+ *                 synchronised; with it the call also returns the device
+ *                 status (SS_ERR_TARGET_RANGE, SS_ERR_CAPACITY).
+ * Clears the workspace status word first. On a device-side error cand and
+ * slot are left unspecified and the status word holds the error.
+ */
+ss_status ss_build_candidates(const int32_t* targets, int64_t T, int64_t V, int64_t C,
+                              uint64_t seed, int32_t* cand, int32_t* slot, int32_t* U_host,
+                              void* workspace, size_t workspace_bytes, ss_stream stream);
+
+/*
+ * Forward pass over the candidate rows ("NanoGPT Training Record: Technical
+ * Optimizations & Speed", "Key Optimizations and Ablation Table Results":
+ * only candidates are scored). The T x C logits never reach device memory:
+ * tensor-core tiles are reduced to per-row log-sum-exp partials on chip.
+ *   H [T, D] bf16, W [V, D] bf16, cand [C], slot [T]: inputs (device).
+ *   loss [T] fp32 out: lse[t] - S[t, slot[t]].
+ *   lse  [T] fp32 out: log-sum-exp over the C candidates; ss_backward needs it.
+ */
+ss_status ss_forward(const uint16_t* H, const uint16_t* W, const int32_t* cand,
+                     const int32_t* slot, int64_t T, int64_t V, int64_t C, int64_t D,
+                     float* loss, float* lse, void* workspace, size_t workspace_bytes,
+                     ss_stream stream);
+
+/*
+ * Backward pass over the candidate rows (same sections as ss_forward: the
+ * backward pass also scores only candidates). Recomputes the logits tile by
+ * tile from H, W[cand] and the saved lse, forms G = scale * (P - Y) in bf16,
+ * then dH = G . W[cand] and dW[cand] = G^T . H with fp32 accumulation.
+ *   lse [T] fp32: from ss_forward on the same inputs.
+ *   scale      : d(objective)/d(loss[t]); 1 for the sum over tokens, 1/T for
+ *                the mean.
+ *   accumulate : 0 -> dW[cand[j]] = dW_c[j]; 1 -> dW[cand[j]] += dW_c[j]
+ *                (gradient accumulation over steps). Rows of dW that are not
+ *                candidates are never read or written; cand must hold
+ *                distinct ids (as ss_build_candidates makes them), which is
+ *                what makes this write-back race-free without atomics.
+ *   dH [T, D] bf16 out (overwritten), dW [V, D] fp32 in/out.
+ */
+ss_status ss_backward(const uint16_t* H, const uint16_t* W, const int32_t* cand,
+                      const int32_t* slot, const float* lse, int64_t T, int64_t V, int64_t C,
+                      int64_t D, float scale, int accumulate, uint16_t* dH, float* dW,
+                      void* workspace, size_t workspace_bytes, ss_stream stream);
+
+/*
+ * Synchronise `stream` and read the workspace status word (one of ss_status)
+ * into *device_status_host and the last U written by ss_build_candidates into
+ * *U_status_host (either may be NULL). Returns SS_ERR_CUDA if the
+ * synchronisation fails, else the device status.
+ */
+ss_status ss_read_status(const void* workspace, size_t workspace_bytes, ss_stream stream,
+                         int32_t* device_status_host, int32_t* U_status_host);
+
+/* Static English text for a status code. */
+const char* ss_status_string(ss_status status);
+
+/*
+ * Diagnostics: per-kernel timing with CUDA events, for benchmarks.
+ * Between ss_trace_begin and ss_trace_end, on the calling host thread, every
+ * kernel that libss launches is bracketed by cudaEventRecord(events[2k]) and
+ * cudaEventRecord(events[2k + 1]) on the launch stream, for k = 0, 1, ...
+ * while k < capacity; later launches are counted but not recorded.
+ *   events   : host array of 2 * capacity cudaEvent_t created by the caller.
+ * ss_trace_end returns the number of launches since ss_trace_begin;
+ * ss_trace_kernel_name(k) is the static name of launch k (k < capacity and
+ * k < that count), or NULL. Tracing adds only the event records.
+ */
+ss_status ss_trace_begin(void** events, int capacity);
+int ss_trace_end(void);
+const char* ss_trace_kernel_name(int k);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SS_H_ */

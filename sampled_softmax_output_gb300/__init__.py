@@ -1,0 +1,267 @@
+"""GB300 sampled-softmax cross-entropy: Python binding of libss (include/ss.h).
+
+Sampled softmax scores only a candidate subset of the vocabulary rows, shared
+by the whole batch, in the forward and the backward pass of the lm_head
+("KellerJordan/modded-nanogpt" README, technique list; "NanoGPT Training
+Record: Technical Optimizations & Speed", section "Key Optimizations and
+Ablation Table Results").
+
+This module is argument marshalling only: every step of the computation runs in
+the CUDA kernels of ``_build/libss.so``. PyTorch provides device memory and the
+current CUDA stream. If the library has not been built, importing the binding
+raises -- there is no fallback.
+
+    import sampled_softmax_output_gb300 as ss
+    ws = ss.workspace(T, V, C, D)                       # device bytes, reusable
+    cand, slot, U = ss.build_candidates(targets, V, C, seed, ws, return_U=True)
+    loss, lse = ss.forward(H, W, cand, slot, ws)        # per-token loss, saved lse
+    dH, dW = ss.backward(H, W, cand, slot, lse, ws, scale=1.0 / T, dW=dW)
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libss.so")
+HEADER = os.path.join(os.path.dirname(_HERE), "include", "ss.h")
+
+STATUS = {
+    0: "SS_OK", 1: "SS_ERR_INVALID", 2: "SS_ERR_UNSUPPORTED", 3: "SS_ERR_CAPACITY",
+    4: "SS_ERR_TARGET_RANGE", 5: "SS_ERR_WORKSPACE", 6: "SS_ERR_CUDA", 7: "SS_ERR_TIMEOUT",
+    8: "SS_ERR_INDEX",
+}
+MAX_V = 524288
+MAX_D = 16384
+
+
+class SSError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = int(code)
+        self.name = STATUS.get(self.code, str(code))
+        msg = _lib.ss_status_string(self.code).decode() if _lib is not None else self.name
+        super().__init__(f"{where}: {self.name} ({msg})")
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(
+            f"libss.so is not built ({LIB_PATH}); run `python -m sampled_softmax_output_gb300.build` "
+            "(or __graft_entry__.build()). There is no non-CUDA fallback.")
+    L = ctypes.CDLL(LIB_PATH)
+    p, i64, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_size_t
+    L.ss_workspace_size.restype = sz
+    L.ss_workspace_size.argtypes = [i64, i64, i64, i64]
+    L.ss_build_candidates.restype = ctypes.c_int
+    L.ss_build_candidates.argtypes = [p, i64, i64, i64, ctypes.c_uint64, p, p, p, p, sz, p]
+    L.ss_forward.restype = ctypes.c_int
+    L.ss_forward.argtypes = [p, p, p, p, i64, i64, i64, i64, p, p, p, sz, p]
+    L.ss_backward.restype = ctypes.c_int
+    L.ss_backward.argtypes = [p, p, p, p, p, i64, i64, i64, i64, ctypes.c_float, ctypes.c_int,
+                              p, p, p, sz, p]
+    L.ss_read_status.restype = ctypes.c_int
+    L.ss_read_status.argtypes = [p, sz, p, p, p]
+    L.ss_status_string.restype = ctypes.c_char_p
+    L.ss_status_string.argtypes = [ctypes.c_int]
+    L.ss_trace_begin.restype = ctypes.c_int
+    L.ss_trace_begin.argtypes = [p, ctypes.c_int]
+    L.ss_trace_end.restype = ctypes.c_int
+    L.ss_trace_end.argtypes = []
+    L.ss_trace_kernel_name.restype = ctypes.c_char_p
+    L.ss_trace_kernel_name.argtypes = [ctypes.c_int]
+    return L
+
+
+_lib = None
+_lib = _load()
+
+
+def lib():
+    return _lib
+
+
+def header_symbols(path: str = HEADER) -> list[str]:
+    """Names of the functions include/ss.h declares."""
+    text = open(path).read()
+    return sorted(set(re.findall(r"^\s*(?:[A-Za-z_][\w\s\*]*?)\b(ss_\w+)\s*\(", text, re.M)))
+
+
+# ----------------------------------------------------------------- helpers
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(device) -> ctypes.c_void_p:
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _need(t: torch.Tensor, name: str, dtype, device=None, shape=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+
+
+def _check(code: int, where: str):
+    if code != 0:
+        raise SSError(code, where)
+
+
+def _bits(t: torch.Tensor) -> torch.Tensor:
+    """bf16 tensor -> the same memory as int16 bit patterns (no copy)."""
+    return t.view(torch.int16) if t.dtype == torch.bfloat16 else t
+
+
+# --------------------------------------------------------------- public API
+
+def workspace_size(T: int, V: int, C: int, D: int) -> int:
+    n = _lib.ss_workspace_size(T, V, C, D)
+    if n == 0:
+        raise SSError(1, "ss_workspace_size")
+    return int(n)
+
+
+def workspace(T: int, V: int, C: int, D: int, device=None) -> torch.Tensor:
+    """A device byte buffer large enough for one batch of size (T, V, C, D)."""
+    return torch.empty(workspace_size(T, V, C, D), dtype=torch.uint8,
+                       device=device if device is not None else "cuda")
+
+
+def build_candidates(targets: torch.Tensor, V: int, C: int, seed: int, ws: torch.Tensor,
+                     cand: torch.Tensor | None = None, slot: torch.Tensor | None = None,
+                     return_U: bool = False):
+    """cand [C] int32 (sorted distinct targets, then seeded negatives by id),
+    slot [T] int32 (cand[slot[t]] == targets[t]); U if return_U (synchronises)."""
+    _need(targets, "targets", torch.int32)
+    dev = targets.device
+    T = targets.numel()
+    _need(ws, "workspace", torch.uint8, dev)
+    if cand is None:
+        cand = torch.empty(C, dtype=torch.int32, device=dev)
+    if slot is None:
+        slot = torch.empty(T, dtype=torch.int32, device=dev)
+    _need(cand, "cand", torch.int32, dev, (C,))
+    _need(slot, "slot", torch.int32, dev, (T,))
+    U = ctypes.c_int32(-1)
+    code = _lib.ss_build_candidates(_ptr(targets), T, V, C, seed & (2**64 - 1), _ptr(cand),
+                                    _ptr(slot), ctypes.byref(U) if return_U else None, _ptr(ws),
+                                    ws.numel(), _stream(dev))
+    _check(code, "ss_build_candidates")
+    return (cand, slot, int(U.value)) if return_U else (cand, slot)
+
+
+def forward(H: torch.Tensor, W: torch.Tensor, cand: torch.Tensor, slot: torch.Tensor,
+            ws: torch.Tensor, loss: torch.Tensor | None = None, lse: torch.Tensor | None = None):
+    """Per-token loss [T] and log-sum-exp [T] (fp32) over the candidate rows."""
+    _need(H, "H", torch.bfloat16)
+    dev = H.device
+    T, D = H.shape
+    _need(W, "W", torch.bfloat16, dev)
+    V = W.shape[0]
+    C = cand.numel()
+    _need(W, "W", torch.bfloat16, dev, (V, D))
+    _need(cand, "cand", torch.int32, dev, (C,))
+    _need(slot, "slot", torch.int32, dev, (T,))
+    _need(ws, "workspace", torch.uint8, dev)
+    if loss is None:
+        loss = torch.empty(T, dtype=torch.float32, device=dev)
+    if lse is None:
+        lse = torch.empty(T, dtype=torch.float32, device=dev)
+    _need(loss, "loss", torch.float32, dev, (T,))
+    _need(lse, "lse", torch.float32, dev, (T,))
+    code = _lib.ss_forward(_ptr(H), _ptr(W), _ptr(cand), _ptr(slot), T, V, C, D, _ptr(loss),
+                           _ptr(lse), _ptr(ws), ws.numel(), _stream(dev))
+    _check(code, "ss_forward")
+    return loss, lse
+
+
+def backward(H: torch.Tensor, W: torch.Tensor, cand: torch.Tensor, slot: torch.Tensor,
+             lse: torch.Tensor, ws: torch.Tensor, scale: float = 1.0, accumulate: bool = False,
+             dH: torch.Tensor | None = None, dW: torch.Tensor | None = None):
+    """dH [T, D] bf16 and dW [V, D] fp32 (only candidate rows written / added to).
+    A new dW is zero-filled, so that it is the dense gradient."""
+    _need(H, "H", torch.bfloat16)
+    dev = H.device
+    T, D = H.shape
+    _need(W, "W", torch.bfloat16, dev)
+    V = W.shape[0]
+    C = cand.numel()
+    _need(W, "W", torch.bfloat16, dev, (V, D))
+    _need(cand, "cand", torch.int32, dev, (C,))
+    _need(slot, "slot", torch.int32, dev, (T,))
+    _need(lse, "lse", torch.float32, dev, (T,))
+    _need(ws, "workspace", torch.uint8, dev)
+    if dH is None:
+        dH = torch.empty(T, D, dtype=torch.bfloat16, device=dev)
+    if dW is None:
+        dW = torch.zeros(V, D, dtype=torch.float32, device=dev)
+    _need(dH, "dH", torch.bfloat16, dev, (T, D))
+    _need(dW, "dW", torch.float32, dev, (V, D))
+    code = _lib.ss_backward(_ptr(H), _ptr(W), _ptr(cand), _ptr(slot), _ptr(lse), T, V, C, D,
+                            float(scale), 1 if accumulate else 0, _ptr(dH), _ptr(dW), _ptr(ws),
+                            ws.numel(), _stream(dev))
+    _check(code, "ss_backward")
+    return dH, dW
+
+
+def read_status(ws: torch.Tensor) -> tuple[int, int]:
+    """(device status code, last U) after synchronising the current stream."""
+    _need(ws, "workspace", torch.uint8)
+    st = ctypes.c_int32(0)
+    U = ctypes.c_int32(0)
+    _lib.ss_read_status(_ptr(ws), ws.numel(), _stream(ws.device), ctypes.byref(st), ctypes.byref(U))
+    return int(st.value), int(U.value)
+
+
+class KernelTrace:
+    """Per-kernel CUDA-event timing of libss launches on this host thread.
+
+        with ss.KernelTrace(capacity=64) as tr:
+            ...calls...
+        torch.cuda.synchronize()
+        for name, ms in tr.timings(): ...
+    """
+
+    def __init__(self, capacity: int = 256):
+        self.capacity = capacity
+        self.events = [torch.cuda.Event(enable_timing=True) for _ in range(2 * capacity)]
+        self._handles = (ctypes.c_void_p * (2 * capacity))(
+            *[ctypes.c_void_p(e.cuda_event) for e in self.events])
+        self.count = 0
+
+    def __enter__(self):
+        _check(_lib.ss_trace_begin(ctypes.cast(self._handles, ctypes.c_void_p), self.capacity),
+               "ss_trace_begin")
+        return self
+
+    def __exit__(self, *exc):
+        self.count = int(_lib.ss_trace_end())
+        self.names = [(_lib.ss_trace_kernel_name(k) or b"?").decode()
+                      for k in range(min(self.count, self.capacity))]
+        return False
+
+    def timings(self) -> list[tuple[str, float]]:
+        """(kernel name, milliseconds) per recorded launch; call after synchronising."""
+        return [(self.names[k], self.events[2 * k].elapsed_time(self.events[2 * k + 1]))
+                for k in range(min(self.count, self.capacity))]
+
+
+def step(H, W, targets, C: int, seed: int, ws, scale: float = 1.0, dW=None, accumulate=False):
+    """One full pass of the path: candidates, forward, backward."""
+    V = W.shape[0]
+    cand, slot = build_candidates(targets, V, C, seed, ws)
+    loss, lse = forward(H, W, cand, slot, ws)
+    dH, dW = backward(H, W, cand, slot, lse, ws, scale=scale, accumulate=accumulate, dW=dW)
+    return {"cand": cand, "slot": slot, "loss": loss, "lse": lse, "dH": dH, "dW": dW}

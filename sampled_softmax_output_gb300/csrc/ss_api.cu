@@ -1,0 +1,409 @@
+// ss_api.cu -- the C ABI declared in include/ss.h: argument checks, the
+// workspace layout, TMA tensor maps, and the launch sequence of each call.
+// Also holds the three small memory-bound kernels of the path: the candidate
+// row gather W_c = W[cand], the log-sum-exp merge of the forward partials, and
+// the zeroing of candidate rows for an empty batch.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <atomic>
+#include <mutex>
+
+#include "ss.h"
+#include "ss_internal.h"
+#include "ss_ptx.cuh"
+
+namespace ss {
+namespace {
+
+// ------------------------------------------------------------ workspace
+
+struct Layout {
+  size_t hdr, wc, part, tgt, g, total;
+  int64_t ldG, n_ct;
+};
+
+constexpr size_t kHdrBytes = 1024;  // int32 status, int32 U, padding
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+Layout make_layout(int64_t T, int64_t C, int64_t D) {
+  Layout L;
+  L.ldG = (C + 63) / 64 * 64;
+  L.n_ct = (C + kBnLogits - 1) / kBnLogits;
+  size_t off = 0;
+  L.hdr = off;
+  off += kHdrBytes;
+  L.wc = off;
+  off = align_up(off + static_cast<size_t>(C) * D * 2, 1024);
+  L.part = off;
+  off = align_up(off + static_cast<size_t>(L.n_ct) * T * sizeof(float2), 1024);
+  L.tgt = off;
+  off = align_up(off + static_cast<size_t>(T) * sizeof(float), 1024);
+  L.g = off;
+  off = align_up(off + static_cast<size_t>(T) * L.ldG * 2, 1024);
+  L.total = off;
+  return L;
+}
+
+ss_status check_sizes(int64_t T, int64_t V, int64_t C, int64_t D) {
+  if (T < 0 || V <= 0 || C <= 0 || D <= 0 || C > V) return SS_ERR_INVALID;
+  if (T >= (int64_t(1) << 31) || V > SS_MAX_V || D > SS_MAX_D || D % 64 != 0 || D < 64)
+    return SS_ERR_UNSUPPORTED;
+  return SS_OK;
+}
+
+bool aligned(const void* p, size_t a) { return reinterpret_cast<uintptr_t>(p) % a == 0; }
+
+// ------------------------------------------------------------ device info
+
+constexpr int kMaxDevices = 64;
+std::atomic<int> g_num_sms[kMaxDevices];
+
+int num_sms_current() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return -1;
+  int n = g_num_sms[dev].load(std::memory_order_relaxed);
+  if (n > 0) return n;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
+  g_num_sms[dev].store(n, std::memory_order_relaxed);
+  return n;
+}
+
+// ------------------------------------------------------------ tensor maps
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// Row-major bf16 matrix [outer, inner] with `row_bytes` between rows, read in
+// boxes of box_outer rows x box_inner elements with the 128-byte swizzle.
+bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
+              uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {row_bytes};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t es[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// ------------------------------------------------------------ small kernels
+
+// W_c[j, :] = W[cand[j], :]; one warp per row, 16-byte vectors.
+__global__ void __launch_bounds__(256) k_gather_rows(const uint16_t* __restrict__ W,
+                                                     const int32_t* __restrict__ cand, int C,
+                                                     int V, int D, uint16_t* __restrict__ Wc,
+                                                     int* status) {
+  if (read_status(status) != 0) return;
+  const int lane = threadIdx.x & 31;
+  const int n16 = D / 8;
+  const int warps = gridDim.x * (blockDim.x / 32);
+  for (int j = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32; j < C; j += warps) {
+    const int v = __ldg(cand + j);
+    uint4* dst = reinterpret_cast<uint4*>(Wc + static_cast<size_t>(j) * D);
+    if (static_cast<unsigned>(v) >= static_cast<unsigned>(V)) {
+      if (lane == 0) set_status(status, SS_ERR_INDEX);
+      for (int i = lane; i < n16; i += 32) dst[i] = make_uint4(0, 0, 0, 0);
+      continue;
+    }
+    const uint4* src = reinterpret_cast<const uint4*>(W + static_cast<size_t>(v) * D);
+    for (int i = lane; i < n16; i += 32) dst[i] = __ldg(src + i);
+  }
+}
+
+// lse[t] = log sum over tiles of s_c * exp(m_c); loss[t] = lse[t] - tgt[t].
+__global__ void __launch_bounds__(256) k_lse_merge(const float2* __restrict__ part,
+                                                   const float* __restrict__ tgt,
+                                                   const int32_t* __restrict__ slot, int T, int C,
+                                                   int n_ct, float* __restrict__ loss,
+                                                   float* __restrict__ lse, int* status) {
+  if (read_status(status) != 0) return;
+  const int t = blockIdx.x * blockDim.x + threadIdx.x;
+  if (t >= T) return;
+  if (static_cast<unsigned>(__ldg(slot + t)) >= static_cast<unsigned>(C)) {
+    set_status(status, SS_ERR_INDEX);
+    return;
+  }
+  float M = -INFINITY;
+  for (int c = 0; c < n_ct; ++c) M = fmaxf(M, part[static_cast<size_t>(c) * T + t].x);
+  float S = 0.f;
+  for (int c = 0; c < n_ct; ++c) {
+    const float2 q = part[static_cast<size_t>(c) * T + t];
+    S += q.y * expf(q.x - M);
+  }
+  const float l = M + logf(S);
+  lse[t] = l;
+  loss[t] = l - tgt[t];
+}
+
+// dW[cand[j], :] = 0 (the gradient of an empty batch).
+__global__ void __launch_bounds__(256) k_zero_rows(const int32_t* __restrict__ cand, int C, int V,
+                                                   int D, float* __restrict__ dW, int* status) {
+  if (read_status(status) != 0) return;
+  const int lane = threadIdx.x & 31;
+  const int warps = gridDim.x * (blockDim.x / 32);
+  for (int j = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32; j < C; j += warps) {
+    const int v = __ldg(cand + j);
+    if (static_cast<unsigned>(v) >= static_cast<unsigned>(V)) {
+      if (lane == 0) set_status(status, SS_ERR_INDEX);
+      continue;
+    }
+    float4* dst = reinterpret_cast<float4*>(dW + static_cast<size_t>(v) * D);
+    for (int i = lane; i < D / 4; i += 32) dst[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+}
+
+int rows_grid(int64_t rows, int num_sms) {
+  const int64_t want = (rows + 7) / 8;
+  const int64_t cap = static_cast<int64_t>(num_sms) * 8;
+  return static_cast<int>(want < cap ? (want > 0 ? want : 1) : cap);
+}
+
+ss_status cuda_status(cudaError_t e) { return e == cudaSuccess ? SS_OK : SS_ERR_CUDA; }
+
+// ------------------------------------------------------------ launch trace
+
+constexpr int kTraceNames = 4096;
+
+struct Trace {
+  bool on = false;
+  cudaEvent_t* events = nullptr;
+  int capacity = 0;
+  int count = 0;
+  const char* names[kTraceNames];
+};
+thread_local Trace g_trace;
+
+void trace_pre(cudaStream_t s, const char* name) {
+  Trace& t = g_trace;
+  if (!t.on) return;
+  if (t.count < t.capacity) {
+    cudaEventRecord(t.events[2 * t.count], s);
+    if (t.count < kTraceNames) t.names[t.count] = name;
+  }
+}
+
+void trace_post(cudaStream_t s) {
+  Trace& t = g_trace;
+  if (!t.on) return;
+  if (t.count < t.capacity) cudaEventRecord(t.events[2 * t.count + 1], s);
+  ++t.count;
+}
+
+}  // namespace
+}  // namespace ss
+
+using namespace ss;
+
+extern "C" {
+
+size_t ss_workspace_size(int64_t T, int64_t V, int64_t C, int64_t D) {
+  if (check_sizes(T, V, C, D) != SS_OK) return 0;
+  return make_layout(T, C, D).total;
+}
+
+ss_status ss_build_candidates(const int32_t* targets, int64_t T, int64_t V, int64_t C,
+                              uint64_t seed, int32_t* cand, int32_t* slot, int32_t* U_host,
+                              void* workspace, size_t workspace_bytes, ss_stream stream) {
+  const ss_status st = check_sizes(T, V, C, 64);
+  if (st != SS_OK) return st;
+  if ((T > 0 && (!targets || !slot)) || !cand || !workspace) return SS_ERR_INVALID;
+  if (!aligned(targets, 4) || !aligned(cand, 4) || !aligned(slot, 4) || !aligned(workspace, 16))
+    return SS_ERR_INVALID;
+  if (workspace_bytes < kHdrBytes) return SS_ERR_WORKSPACE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int* hdr = static_cast<int*>(workspace);
+  if (cudaMemsetAsync(hdr, 0, 2 * sizeof(int), s) != cudaSuccess) return SS_ERR_CUDA;
+  trace_pre(s, "build_candidates");
+  const cudaError_t e = launch_build_candidates(targets, static_cast<int>(T), static_cast<int>(V),
+                                                static_cast<int>(C), seed, cand, slot, hdr, s);
+  trace_post(s);
+  if (e != cudaSuccess) return SS_ERR_CUDA;
+  if (U_host) {
+    int32_t h[2] = {0, 0};
+    if (cudaMemcpyAsync(h, hdr, sizeof h, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+      return SS_ERR_CUDA;
+    *U_host = h[1];
+    return static_cast<ss_status>(h[0]);
+  }
+  return SS_OK;
+}
+
+ss_status ss_forward(const uint16_t* H, const uint16_t* W, const int32_t* cand,
+                     const int32_t* slot, int64_t T, int64_t V, int64_t C, int64_t D,
+                     float* loss, float* lse, void* workspace, size_t workspace_bytes,
+                     ss_stream stream) {
+  const ss_status st = check_sizes(T, V, C, D);
+  if (st != SS_OK) return st;
+  if (!W || !cand || !workspace || (T > 0 && (!H || !slot || !loss || !lse)))
+    return SS_ERR_INVALID;
+  if (!aligned(H, 16) || !aligned(W, 16) || !aligned(workspace, 16) || !aligned(cand, 4) ||
+      !aligned(slot, 4) || !aligned(loss, 4) || !aligned(lse, 4))
+    return SS_ERR_INVALID;
+  const Layout L = make_layout(T, C, D);
+  if (workspace_bytes < L.total) return SS_ERR_WORKSPACE;
+  if (T == 0) return SS_OK;
+  const int nsm = num_sms_current();
+  if (nsm <= 0) return SS_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  char* ws = static_cast<char*>(workspace);
+  int* status = reinterpret_cast<int*>(ws + L.hdr);
+  uint16_t* Wc = reinterpret_cast<uint16_t*>(ws + L.wc);
+  float2* part = reinterpret_cast<float2*>(ws + L.part);
+  float* tgt = reinterpret_cast<float*>(ws + L.tgt);
+
+  trace_pre(s, "gather_rows");
+  k_gather_rows<<<rows_grid(C, nsm), 256, 0, s>>>(W, cand, static_cast<int>(C),
+                                                   static_cast<int>(V), static_cast<int>(D), Wc,
+                                                   status);
+  trace_post(s);
+  if (cudaGetLastError() != cudaSuccess) return SS_ERR_CUDA;
+
+  CUtensorMap tH, tWc;
+  if (!make_map(&tH, H, D, T, D * 2, 64, 128) || !make_map(&tWc, Wc, D, C, D * 2, 64, kBnLogits))
+    return SS_ERR_CUDA;
+  trace_pre(s, "gemm_forward_lse");
+  const cudaError_t e = launch_forward_logits(tH, tWc, static_cast<int>(T), static_cast<int>(C),
+                                              static_cast<int>(D), slot, part, tgt, status, nsm,
+                                              s);
+  trace_post(s);
+  if (e != cudaSuccess) return SS_ERR_CUDA;
+  const int blocks = static_cast<int>((T + 255) / 256);
+  trace_pre(s, "lse_merge");
+  k_lse_merge<<<blocks, 256, 0, s>>>(part, tgt, slot, static_cast<int>(T), static_cast<int>(C),
+                                     static_cast<int>(L.n_ct), loss, lse, status);
+  trace_post(s);
+  return cuda_status(cudaGetLastError());
+}
+
+ss_status ss_backward(const uint16_t* H, const uint16_t* W, const int32_t* cand,
+                      const int32_t* slot, const float* lse, int64_t T, int64_t V, int64_t C,
+                      int64_t D, float scale, int accumulate, uint16_t* dH, float* dW,
+                      void* workspace, size_t workspace_bytes, ss_stream stream) {
+  const ss_status st = check_sizes(T, V, C, D);
+  if (st != SS_OK) return st;
+  if (!W || !cand || !dW || !workspace || (T > 0 && (!H || !slot || !lse || !dH)))
+    return SS_ERR_INVALID;
+  if (!aligned(H, 16) || !aligned(W, 16) || !aligned(dH, 16) || !aligned(dW, 16) ||
+      !aligned(workspace, 16) || !aligned(cand, 4) || !aligned(slot, 4) || !aligned(lse, 4))
+    return SS_ERR_INVALID;
+  if (accumulate != 0 && accumulate != 1) return SS_ERR_INVALID;
+  const Layout L = make_layout(T, C, D);
+  if (workspace_bytes < L.total) return SS_ERR_WORKSPACE;
+  const int nsm = num_sms_current();
+  if (nsm <= 0) return SS_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  char* ws = static_cast<char*>(workspace);
+  int* status = reinterpret_cast<int*>(ws + L.hdr);
+  const int iT = static_cast<int>(T), iV = static_cast<int>(V), iC = static_cast<int>(C),
+            iD = static_cast<int>(D);
+
+  if (T == 0) {
+    if (!accumulate) {
+      trace_pre(s, "zero_rows");
+      k_zero_rows<<<rows_grid(C, nsm), 256, 0, s>>>(cand, iC, iV, iD, dW, status);
+      trace_post(s);
+      return cuda_status(cudaGetLastError());
+    }
+    return SS_OK;
+  }
+  uint16_t* Wc = reinterpret_cast<uint16_t*>(ws + L.wc);
+  uint16_t* G = reinterpret_cast<uint16_t*>(ws + L.g);
+
+  trace_pre(s, "gather_rows");
+  k_gather_rows<<<rows_grid(C, nsm), 256, 0, s>>>(W, cand, iC, iV, iD, Wc, status);
+  trace_post(s);
+  if (cudaGetLastError() != cudaSuccess) return SS_ERR_CUDA;
+
+  CUtensorMap tH, tWc, tGk, tWcMn, tGmn, tHmn;
+  const uint64_t gRow = static_cast<uint64_t>(L.ldG) * 2;
+  if (!make_map(&tH, H, D, T, D * 2, 64, 128) || !make_map(&tWc, Wc, D, C, D * 2, 64, kBnLogits) ||
+      !make_map(&tGk, G, C, T, gRow, 64, 128) || !make_map(&tWcMn, Wc, D, C, D * 2, 64, 64) ||
+      !make_map(&tGmn, G, C, T, gRow, 64, 64) || !make_map(&tHmn, H, D, T, D * 2, 64, 64))
+    return SS_ERR_CUDA;
+
+  trace_pre(s, "gemm_softmax_grad");
+  cudaError_t e = launch_softmax_grad(tH, tWc, iT, iC, iD, static_cast<int>(L.ldG), slot, lse,
+                                      scale, G, status, nsm, s);
+  trace_post(s);
+  if (e != cudaSuccess) return SS_ERR_CUDA;
+  trace_pre(s, "gemm_grad_h");
+  e = launch_grad_h(tGk, tWcMn, iT, iC, iD, dH, status, nsm, s);
+  trace_post(s);
+  if (e != cudaSuccess) return SS_ERR_CUDA;
+  trace_pre(s, "gemm_grad_w_scatter");
+  e = launch_grad_w(tGmn, tHmn, iT, iC, iD, iV, accumulate, cand, dW, status, nsm, s);
+  trace_post(s);
+  if (e != cudaSuccess) return SS_ERR_CUDA;
+  return SS_OK;
+}
+
+ss_status ss_read_status(const void* workspace, size_t workspace_bytes, ss_stream stream,
+                         int32_t* device_status_host, int32_t* U_status_host) {
+  if (!workspace || !aligned(workspace, 16)) return SS_ERR_INVALID;
+  if (workspace_bytes < kHdrBytes) return SS_ERR_WORKSPACE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int32_t h[2] = {0, 0};
+  if (cudaMemcpyAsync(h, workspace, sizeof h, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+      cudaStreamSynchronize(s) != cudaSuccess)
+    return SS_ERR_CUDA;
+  if (device_status_host) *device_status_host = h[0];
+  if (U_status_host) *U_status_host = h[1];
+  return static_cast<ss_status>(h[0]);
+}
+
+ss_status ss_trace_begin(void** events, int capacity) {
+  if (capacity < 0 || (capacity > 0 && !events)) return SS_ERR_INVALID;
+  Trace& t = g_trace;
+  t.on = true;
+  t.events = reinterpret_cast<cudaEvent_t*>(events);
+  t.capacity = capacity;
+  t.count = 0;
+  return SS_OK;
+}
+
+int ss_trace_end(void) {
+  Trace& t = g_trace;
+  t.on = false;
+  return t.count;
+}
+
+const char* ss_trace_kernel_name(int k) {
+  const Trace& t = g_trace;
+  if (k < 0 || k >= t.count || k >= t.capacity || k >= kTraceNames) return nullptr;
+  return t.names[k];
+}
+
+const char* ss_status_string(ss_status status) {
+  switch (status) {
+    case SS_OK: return "ok";
+    case SS_ERR_INVALID: return "invalid argument";
+    case SS_ERR_UNSUPPORTED: return "unsupported size";
+    case SS_ERR_CAPACITY: return "more distinct targets than candidate slots (U > C)";
+    case SS_ERR_TARGET_RANGE: return "target id outside [0, V)";
+    case SS_ERR_WORKSPACE: return "workspace too small";
+    case SS_ERR_CUDA: return "CUDA error";
+    case SS_ERR_TIMEOUT: return "device wait timed out";
+    case SS_ERR_INDEX: return "cand entry outside [0, V) or slot outside [0, C)";
+  }
+  return "unknown status";
+}
+
+}  // extern "C"

@@ -1,0 +1,440 @@
+// ss_gemm.cuh -- persistent, warp-specialised bf16 GEMM on the 5th-generation
+// tensor cores of sm_103a, with the sampled-softmax epilogues fused in.
+//
+// One CTA per SM walks a static round-robin list of 128 x BN output tiles
+// ("units"). Roles:
+//   warp 0, one lane : TMA producer -- loads 128 x 64 A and BN x 64 B blocks
+//                      (128-byte swizzle) into a STAGES-deep ring.
+//   warp 1, one lane : MMA issuer  -- tcgen05.mma 128 x BN x 16 into one of two
+//                      TMEM accumulators (2 x BN fp32 columns), commits to
+//                      mbarriers to free ring slots and to hand tiles over.
+//   warps 2-5        : epilogue    -- tcgen05.ld the accumulator (warp w owns
+//                      TMEM lanes 32*(w%4)..+31, one output row per thread),
+//                      apply the fused epilogue, release the accumulator.
+// The epilogue of tile i overlaps the MMAs of tile i+1.
+//
+// Operand layouts (A is M x K, B is N x K in the MMA's terms):
+//   K-major : the K index is contiguous in memory; one TMA box of 64 (K) x rows.
+//   MN-major: the M/N index is contiguous; boxes of 64 (M/N) x 64 (K), one per
+//             64-wide M/N chunk, laid out 8 KB apart.
+// Out-of-range rows/columns of a box are zero-filled by TMA, so ragged M, N
+// and K edges need no special casing in the main loop.
+#pragma once
+
+#include <math.h>
+
+#include "ss_ptx.cuh"
+
+namespace ss {
+
+constexpr int BM = 128;          // tile rows = TMEM lanes
+constexpr int BK = 64;           // 64 bf16 = one 128-byte swizzle row
+constexpr int UMMA_K = 16;       // K of one tcgen05.mma kind::f16
+constexpr int GEMM_THREADS = 192;
+constexpr float kLog2e = 1.4426950408889634f;
+
+template <int BN, int STAGES>
+struct GemmSmem {
+  static constexpr int A_BYTES = BM * BK * 2;
+  static constexpr int B_BYTES = BN * BK * 2;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int TILES_BYTES = STAGES * STAGE_BYTES;
+  static constexpr int CTRL_BYTES = 256;
+  static constexpr int TOTAL = TILES_BYTES + CTRL_BYTES + 1024;  // + 1024-byte alignment slack
+};
+
+struct GemmCtrl {
+  uint64_t full[8];
+  uint64_t empty[8];
+  uint64_t tfull[2];
+  uint64_t tempty[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+// Units are (m_tile, n_tile) pairs numbered m-major: u = m_tile * n_tiles + n_tile.
+struct GemmShape {
+  int m_tiles;
+  int n_tiles;
+  int k_blocks;
+};
+
+// ----------------------------------------------------------------- epilogues
+
+// Forward: per-row softmax partials of one 128 x BN logit tile.
+//   part[n_tile][t] = (max_j S[t,j], sum_j exp(S[t,j] - max)) over the tile's
+//   valid columns; tgt[t] = S[t, slot[t]] from the tile that holds slot[t].
+struct EpiFwd {
+  struct Params {
+    int T, C;
+    const int32_t* slot;
+    float2* part;
+    float* tgt;
+    int* status;
+  };
+  template <int BN>
+  __device__ static void apply(const Params& p, int mt, int nt, int row, uint32_t taddr) {
+    const int t = mt * BM + row;
+    const bool valid = t < p.T;
+    const int sl = valid ? __ldg(p.slot + t) : -1;
+    const int j0 = nt * BN;
+    const int ncols = min(BN, p.C - j0);
+    float m = -INFINITY, s = 0.f, tg = 0.f;
+    bool has_t = false;
+#pragma unroll 1
+    for (int c = 0; c < BN / 32; ++c) {
+      const int jc = c * 32;
+      if (jc >= ncols) break;  // uniform: depends on the tile only
+      uint32_t r[32];
+      tmem_ld32(taddr + jc, r);
+      tmem_ld_wait();
+      const int nv = min(32, ncols - jc);
+      float cm = -INFINITY;
+#pragma unroll
+      for (int i = 0; i < 32; ++i)
+        if (i < nv) cm = fmaxf(cm, __uint_as_float(r[i]));
+      const float nm = fmaxf(m, cm);
+      const float nm2 = nm * kLog2e;
+      float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll
+      for (int i = 0; i < 32; i += 4) {
+        if (i + 0 < nv) a0 += ex2_approx(fmaf(__uint_as_float(r[i + 0]), kLog2e, -nm2));
+        if (i + 1 < nv) a1 += ex2_approx(fmaf(__uint_as_float(r[i + 1]), kLog2e, -nm2));
+        if (i + 2 < nv) a2 += ex2_approx(fmaf(__uint_as_float(r[i + 2]), kLog2e, -nm2));
+        if (i + 3 < nv) a3 += ex2_approx(fmaf(__uint_as_float(r[i + 3]), kLog2e, -nm2));
+      }
+      s = s * ex2_approx((m - nm) * kLog2e) + ((a0 + a1) + (a2 + a3));
+      m = nm;
+      const int off = sl - j0 - jc;
+      if (static_cast<unsigned>(off) < static_cast<unsigned>(nv)) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          if (i == off) tg = __uint_as_float(r[i]);
+        has_t = true;
+      }
+    }
+    if (valid) {
+      p.part[static_cast<size_t>(nt) * p.T + t] = make_float2(m, s);
+      if (has_t) p.tgt[t] = tg;
+    }
+  }
+};
+
+// Backward, step 1: G[t, j] = scale * (exp(S[t,j] - lse[t]) - [j == slot[t]]), bf16.
+struct EpiG {
+  struct Params {
+    int T, C, ldG;
+    const int32_t* slot;
+    const float* lse;
+    float scale;
+    uint16_t* G;
+    int* status;
+  };
+  template <int BN>
+  __device__ static void apply(const Params& p, int mt, int nt, int row, uint32_t taddr) {
+    const int t = mt * BM + row;
+    const bool valid = t < p.T;
+    const int sl = valid ? __ldg(p.slot + t) : -1;
+    if (valid && nt == 0 && static_cast<unsigned>(sl) >= static_cast<unsigned>(p.C))
+      set_status(p.status, SS_ERR_INDEX);
+    const float l2 = valid ? __ldg(p.lse + t) * kLog2e : 0.f;
+    const float sc = p.scale;
+    const int j0 = nt * BN;
+    const int ncols = min(BN, p.C - j0);
+    uint16_t* grow = p.G + static_cast<size_t>(valid ? t : 0) * p.ldG + j0;
+#pragma unroll 1
+    for (int c = 0; c < BN / 32; ++c) {
+      const int jc = c * 32;
+      if (jc >= ncols) break;
+      uint32_t r[32];
+      tmem_ld32(taddr + jc, r);
+      tmem_ld_wait();
+      const int off = sl - j0 - jc;
+      uint32_t pk[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        float g0 = ex2_approx(fmaf(__uint_as_float(r[2 * i]), kLog2e, -l2));
+        float g1 = ex2_approx(fmaf(__uint_as_float(r[2 * i + 1]), kLog2e, -l2));
+        if (off == 2 * i) g0 -= 1.f;
+        if (off == 2 * i + 1) g1 -= 1.f;
+        pk[i] = pack_bf16x2(sc * g0, sc * g1);
+      }
+      if (valid) {
+        uint4* dst = reinterpret_cast<uint4*>(grow + jc);
+#pragma unroll
+        for (int v = 0; v < 4; ++v)
+          if (jc + 8 * v < ncols)
+            dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+      }
+    }
+  }
+};
+
+// Backward, step 2: dH tile -> bf16.
+struct EpiDh {
+  struct Params {
+    int T, D;
+    uint16_t* dH;
+  };
+  template <int BN>
+  __device__ static void apply(const Params& p, int mt, int nt, int row, uint32_t taddr) {
+    const int t = mt * BM + row;
+    const bool valid = t < p.T;
+    const int n0 = nt * BN;
+    const int ncols = min(BN, p.D - n0);
+    uint16_t* drow = p.dH + static_cast<size_t>(valid ? t : 0) * p.D + n0;
+#pragma unroll 1
+    for (int c = 0; c < BN / 32; ++c) {
+      const int jc = c * 32;
+      if (jc >= ncols) break;
+      uint32_t r[32];
+      tmem_ld32(taddr + jc, r);
+      tmem_ld_wait();
+      if (valid) {
+        uint4* dst = reinterpret_cast<uint4*>(drow + jc);
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+          uint32_t q0 = pack_bf16x2(__uint_as_float(r[8 * v + 0]), __uint_as_float(r[8 * v + 1]));
+          uint32_t q1 = pack_bf16x2(__uint_as_float(r[8 * v + 2]), __uint_as_float(r[8 * v + 3]));
+          uint32_t q2 = pack_bf16x2(__uint_as_float(r[8 * v + 4]), __uint_as_float(r[8 * v + 5]));
+          uint32_t q3 = pack_bf16x2(__uint_as_float(r[8 * v + 6]), __uint_as_float(r[8 * v + 7]));
+          dst[v] = make_uint4(q0, q1, q2, q3);
+        }
+      }
+    }
+  }
+};
+
+// Backward, step 3: dW_c tile scattered into the owning rows dW[cand[j]]
+// (= or +=). Candidate ids are distinct, so no two threads write one row.
+struct EpiDw {
+  struct Params {
+    int C, D, V, accumulate;
+    const int32_t* cand;
+    float* dW;
+    int* status;
+  };
+  template <int BN>
+  __device__ static void apply(const Params& p, int mt, int nt, int row, uint32_t taddr) {
+    const int j = mt * BM + row;
+    bool valid = j < p.C;
+    const int v = valid ? __ldg(p.cand + j) : 0;
+    if (valid && static_cast<unsigned>(v) >= static_cast<unsigned>(p.V)) {
+      set_status(p.status, SS_ERR_INDEX);
+      valid = false;
+    }
+    const int n0 = nt * BN;
+    const int ncols = min(BN, p.D - n0);
+    float* drow = p.dW + static_cast<size_t>(valid ? v : 0) * p.D + n0;
+#pragma unroll 1
+    for (int c = 0; c < BN / 32; ++c) {
+      const int jc = c * 32;
+      if (jc >= ncols) break;
+      uint32_t r[32];
+      tmem_ld32(taddr + jc, r);
+      tmem_ld_wait();
+      if (valid) {
+        float4* dst = reinterpret_cast<float4*>(drow + jc);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          float4 o = make_float4(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]),
+                                 __uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3]));
+          if (p.accumulate) {
+            const float4 old = dst[i];
+            o.x += old.x;
+            o.y += old.y;
+            o.z += old.z;
+            o.w += old.w;
+          }
+          dst[i] = o;
+        }
+      }
+    }
+  }
+};
+
+// -------------------------------------------------------------------- kernel
+
+template <int BN, int STAGES, bool A_MN, bool B_MN, class Epi>
+__global__ void __launch_bounds__(GEMM_THREADS, 1)
+    k_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+           GemmShape shp, typename Epi::Params ep, int* status) {
+  static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "BN");
+  static_assert(STAGES >= 2 && STAGES <= 8, "STAGES");
+  using L = GemmSmem<BN, STAGES>;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ int s_go;
+
+  const uint32_t raw = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+  GemmCtrl* ctrl = reinterpret_cast<GemmCtrl*>(smem + L::TILES_BYTES);
+  const uint32_t tiles = smem_u32(smem);
+  const int warp = threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+
+  // An earlier error of this batch: do nothing (decided once for the CTA).
+  if (threadIdx.x == 0) s_go = (read_status(status) == 0);
+  __syncthreads();
+  if (!s_go) return;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&ctrl->full[s], 1);
+      mbar_init(&ctrl->empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&ctrl->tfull[b], 1);
+      mbar_init(&ctrl->tempty[b], 4 * 32);
+    }
+    mbar_init(&ctrl->drain, 1);
+    ctrl->abort_flag = 0;
+    fence_mbar_init();
+    tma_prefetch_map(&tmA);
+    tma_prefetch_map(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc(&ctrl->tmem_base, 2 * BN);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = ctrl->tmem_base;
+  volatile int* abort_flag = &ctrl->abort_flag;
+  const int num_units = shp.m_tiles * shp.n_tiles;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int s = 0;
+      uint32_t ph = 0, issued = 0, issued_ph = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; ok && u < num_units; u += gridDim.x) {
+        const int mt = u / shp.n_tiles, nt = u % shp.n_tiles;
+        for (int kb = 0; kb < shp.k_blocks; ++kb) {
+          if (!mbar_wait(&ctrl->empty[s], ph ^ 1u, abort_flag, status)) {
+            ok = false;
+            break;
+          }
+          uint64_t* fb = &ctrl->full[s];
+          mbar_arrive_expect_tx(fb, L::STAGE_BYTES);
+          const uint32_t a_dst = tiles + s * L::STAGE_BYTES;
+          const uint32_t b_dst = a_dst + L::A_BYTES;
+          if (A_MN) {
+#pragma unroll
+            for (int i = 0; i < BM / 64; ++i)
+              tma_load_2d(a_dst + i * 8192, &tmA, fb, mt * BM + 64 * i, kb * BK);
+          } else {
+            tma_load_2d(a_dst, &tmA, fb, kb * BK, mt * BM);
+          }
+          if (B_MN) {
+#pragma unroll
+            for (int i = 0; i < BN / 64; ++i)
+              tma_load_2d(b_dst + i * 8192, &tmB, fb, nt * BN + 64 * i, kb * BK);
+          } else {
+            tma_load_2d(b_dst, &tmB, fb, kb * BK, nt * BN);
+          }
+          issued |= 1u << s;
+          issued_ph = (issued_ph & ~(1u << s)) | (ph << s);
+          if (++s == STAGES) {
+            s = 0;
+            ph ^= 1u;
+          }
+        }
+      }
+      // Every issued copy must land before the CTA may exit.
+      for (int i = 0; i < STAGES; ++i)
+        if ((issued >> i) & 1u) mbar_drain(&ctrl->full[i], (issued_ph >> i) & 1u, status);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ---------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16_f32(BM, BN, A_MN, B_MN);
+      int s = 0, b = 0;
+      uint32_t ph = 0, aph = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; ok && u < num_units; u += gridDim.x) {
+        if (!mbar_wait(&ctrl->tempty[b], aph ^ 1u, abort_flag, status)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(b * BN);
+        for (int kb = 0; kb < shp.k_blocks; ++kb) {
+          if (!mbar_wait(&ctrl->full[s], ph, abort_flag, status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_addr = tiles + s * L::STAGE_BYTES;
+          const uint32_t b_addr = a_addr + L::A_BYTES;
+#pragma unroll
+          for (int k = 0; k < BK / UMMA_K; ++k) {
+            const uint64_t ad = A_MN ? sdesc_sw128(a_addr + k * 2048, 8192, 1024)
+                                     : sdesc_sw128(a_addr + k * 32, 16, 1024);
+            const uint64_t bd = B_MN ? sdesc_sw128(b_addr + k * 2048, 8192, 1024)
+                                     : sdesc_sw128(b_addr + k * 32, 16, 1024);
+            mma_bf16(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+          }
+          mma_commit(&ctrl->empty[s]);
+          if (++s == STAGES) {
+            s = 0;
+            ph ^= 1u;
+          }
+        }
+        if (!ok) break;
+        mma_commit(&ctrl->tfull[b]);
+        if (++b == 2) {
+          b = 0;
+          aph ^= 1u;
+        }
+      }
+      // Every issued MMA must finish before TMEM is released.
+      mma_commit(&ctrl->drain);
+      mbar_drain(&ctrl->drain, 0, status);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;
+    const int row = q * 32 + lane;
+    const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+    int b = 0;
+    uint32_t aph = 0;
+    for (int u = blockIdx.x; u < num_units; u += gridDim.x) {
+      const bool ok = mbar_wait(&ctrl->tfull[b], aph, abort_flag, status);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      tc_fence_after();
+      const int mt = u / shp.n_tiles, nt = u % shp.n_tiles;
+      Epi::template apply<BN>(ep, mt, nt, row, lane_addr + static_cast<uint32_t>(b * BN));
+      tc_fence_before();
+      mbar_arrive(&ctrl->tempty[b]);
+      if (++b == 2) {
+        b = 0;
+        aph ^= 1u;
+      }
+    }
+  }
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, 2 * BN);
+  }
+}
+
+// Host-side launcher: grid = min(units, SMs), one CTA per SM.
+template <int BN, int STAGES, bool A_MN, bool B_MN, class Epi>
+cudaError_t launch_gemm(const CUtensorMap& tA, const CUtensorMap& tB, GemmShape shp,
+                        const typename Epi::Params& ep, int* status, int num_sms,
+                        cudaStream_t stream) {
+  auto kern = k_gemm<BN, STAGES, A_MN, B_MN, Epi>;
+  constexpr int smem = GemmSmem<BN, STAGES>::TOTAL;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  const int units = shp.m_tiles * shp.n_tiles;
+  if (units <= 0) return cudaSuccess;
+  const int grid = units < num_sms ? units : num_sms;
+  kern<<<grid, GEMM_THREADS, smem, stream>>>(tA, tB, shp, ep, status);
+  return cudaGetLastError();
+}
+
+}  // namespace ss

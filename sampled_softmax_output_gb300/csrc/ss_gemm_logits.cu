@@ -1,0 +1,30 @@
+// ss_gemm_logits.cu -- the two GEMMs over the T x C logit matrix S = H . W_c^T
+// (K = D): the forward pass (log-sum-exp partials, target logit) and the
+// backward recompute (softmax gradient G in bf16). Neither writes S itself.
+#include "ss_gemm.cuh"
+#include "ss_internal.h"
+
+namespace ss {
+
+constexpr int kStagesLogits = 4;
+
+cudaError_t launch_forward_logits(const CUtensorMap& tH, const CUtensorMap& tWc, int T, int C,
+                                  int D, const int32_t* slot, float2* part, float* tgt,
+                                  int* status, int num_sms, cudaStream_t stream) {
+  GemmShape shp{(T + BM - 1) / BM, (C + kBnLogits - 1) / kBnLogits, D / BK};
+  EpiFwd::Params ep{T, C, slot, part, tgt, status};
+  return launch_gemm<kBnLogits, kStagesLogits, false, false, EpiFwd>(tH, tWc, shp, ep, status,
+                                                                     num_sms, stream);
+}
+
+cudaError_t launch_softmax_grad(const CUtensorMap& tH, const CUtensorMap& tWc, int T, int C,
+                                int D, int ldG, const int32_t* slot, const float* lse,
+                                float scale, uint16_t* G, int* status, int num_sms,
+                                cudaStream_t stream) {
+  GemmShape shp{(T + BM - 1) / BM, (C + kBnLogits - 1) / kBnLogits, D / BK};
+  EpiG::Params ep{T, C, ldG, slot, lse, scale, G, status};
+  return launch_gemm<kBnLogits, kStagesLogits, false, false, EpiG>(tH, tWc, shp, ep, status,
+                                                                   num_sms, stream);
+}
+
+}  // namespace ss

@@ -1,0 +1,40 @@
+// ss_internal.h -- declarations shared by the translation units of libss.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace ss {
+
+// Tile widths of the GEMMs (output columns per tile).
+constexpr int kBnLogits = 256;  // logit tiles: forward and softmax-gradient
+constexpr int kBnGrad = 256;    // dH and dW tiles along D
+
+struct GemmShape;
+
+// ---- candidate build (ss_candidates.cu)
+size_t build_candidates_smem_bytes(int64_t V);
+cudaError_t launch_build_candidates(const int32_t* targets, int T, int V, int C, uint64_t seed,
+                                    int32_t* cand, int32_t* slot, int* hdr, cudaStream_t stream);
+
+// ---- logit GEMMs (ss_gemm_logits.cu): A = H [T, D] (K-major), B = W_c [C, D] (K-major)
+cudaError_t launch_forward_logits(const CUtensorMap& tH, const CUtensorMap& tWc, int T, int C,
+                                  int D, const int32_t* slot, float2* part, float* tgt,
+                                  int* status, int num_sms, cudaStream_t stream);
+cudaError_t launch_softmax_grad(const CUtensorMap& tH, const CUtensorMap& tWc, int T, int C,
+                                int D, int ldG, const int32_t* slot, const float* lse,
+                                float scale, uint16_t* G, int* status, int num_sms,
+                                cudaStream_t stream);
+
+// ---- gradient GEMMs (ss_gemm_grads.cu)
+// dH = G . W_c : A = G [T, C] (K-major), B = W_c [C, D] (MN-major)
+cudaError_t launch_grad_h(const CUtensorMap& tG_kmaj, const CUtensorMap& tWc_mn, int T, int C,
+                          int D, uint16_t* dH, int* status, int num_sms, cudaStream_t stream);
+// dW[cand] (=|+=) G^T . H : A = G (MN-major), B = H [T, D] (MN-major)
+cudaError_t launch_grad_w(const CUtensorMap& tG_mn, const CUtensorMap& tH_mn, int T, int C, int D,
+                          int V, int accumulate, const int32_t* cand, float* dW, int* status,
+                          int num_sms, cudaStream_t stream);
+
+}  // namespace ss

@@ -1,0 +1,130 @@
+"""Host-side checks of the C ABI: the library loads without a GPU, exports every
+function include/ss.h declares, sizes its workspace, and rejects bad arguments
+before it touches the device (these paths make no CUDA call, so they run on a
+machine without a GPU; the fake device addresses below are never dereferenced)."""
+import ctypes
+
+import pytest
+
+import sampled_softmax_output_gb300 as ss  # noqa: E402  (fails loudly if libss.so is missing)
+
+OK, INVALID, UNSUPPORTED, WORKSPACE = 0, 1, 2, 5
+FAKE = 0x7F0000000000  # 4 KB-aligned address, never dereferenced
+p = ctypes.c_void_p
+
+
+def test_exports_every_declared_symbol():
+    names = ss.header_symbols()
+    assert set(names) == {"ss_workspace_size", "ss_build_candidates", "ss_forward",
+                          "ss_backward", "ss_read_status", "ss_status_string",
+                          "ss_trace_begin", "ss_trace_end", "ss_trace_kernel_name"}
+    for n in names:
+        assert hasattr(ss.lib(), n), n
+
+
+def test_status_strings():
+    L = ss.lib()
+    for code in range(9):
+        s = L.ss_status_string(code)
+        assert s and s != b"unknown status"
+    assert L.ss_status_string(99) == b"unknown status"
+
+
+def test_workspace_size():
+    L = ss.lib()
+    T, V, C, D = 16384, 50304, 10240, 768
+    n = L.ss_workspace_size(T, V, C, D)
+    # at least the bf16 softmax-gradient matrix and the gathered candidate rows
+    assert n >= T * C * 2 + C * D * 2
+    assert n % 1024 == 0
+    assert L.ss_workspace_size(0, V, C, D) > 0             # empty batch is valid
+    assert L.ss_workspace_size(T, V, V + 1, D) == 0        # C > V
+    assert L.ss_workspace_size(T, V, 0, D) == 0            # C = 0
+    assert L.ss_workspace_size(T, V, C, 100) == 0          # D % 64 != 0
+    assert L.ss_workspace_size(T, ss.MAX_V + 1, C, D) == 0
+    assert L.ss_workspace_size(-1, V, C, D) == 0
+    # monotone in every size
+    assert L.ss_workspace_size(2 * T, V, C, D) > n and L.ss_workspace_size(T, V, 2 * C, D) > n
+
+
+def _fwd(**kw):
+    a = dict(H=FAKE, W=FAKE, cand=FAKE, slot=FAKE, T=256, V=50304, C=4096, D=768, loss=FAKE,
+             lse=FAKE, ws=FAKE, wsb=1 << 40)
+    a.update(kw)
+    return ss.lib().ss_forward(p(a["H"]), p(a["W"]), p(a["cand"]), p(a["slot"]), a["T"], a["V"],
+                               a["C"], a["D"], p(a["loss"]), p(a["lse"]), p(a["ws"]), a["wsb"],
+                               None)
+
+
+def _bwd(**kw):
+    a = dict(H=FAKE, W=FAKE, cand=FAKE, slot=FAKE, lse=FAKE, T=256, V=50304, C=4096, D=768,
+             scale=1.0, acc=0, dH=FAKE, dW=FAKE, ws=FAKE, wsb=1 << 40)
+    a.update(kw)
+    return ss.lib().ss_backward(p(a["H"]), p(a["W"]), p(a["cand"]), p(a["slot"]), p(a["lse"]),
+                                a["T"], a["V"], a["C"], a["D"], a["scale"], a["acc"], p(a["dH"]),
+                                p(a["dW"]), p(a["ws"]), a["wsb"], None)
+
+
+def _cand(**kw):
+    a = dict(targets=FAKE, T=256, V=50304, C=4096, seed=0, cand=FAKE, slot=FAKE, U=None, ws=FAKE,
+             wsb=1 << 20)
+    a.update(kw)
+    return ss.lib().ss_build_candidates(p(a["targets"]), a["T"], a["V"], a["C"], a["seed"],
+                                        p(a["cand"]), p(a["slot"]), a["U"], p(a["ws"]), a["wsb"],
+                                        None)
+
+
+@pytest.mark.parametrize("fn", [_fwd, _bwd, _cand])
+def test_size_errors(fn):
+    assert fn(C=0) == INVALID
+    assert fn(C=50305) == INVALID
+    assert fn(T=-1) == INVALID
+    assert fn(V=ss.MAX_V + 1, C=10) == UNSUPPORTED
+    assert fn(T=1 << 31) == UNSUPPORTED
+
+
+@pytest.mark.parametrize("fn", [_fwd, _bwd])
+def test_width_errors(fn):
+    assert fn(D=100) == UNSUPPORTED
+    assert fn(D=0) == INVALID
+    assert fn(D=ss.MAX_D + 64) == UNSUPPORTED
+
+
+def test_null_and_alignment_errors():
+    for k in ("H", "W", "cand", "slot", "loss", "lse", "ws"):
+        assert _fwd(**{k: 0}) == INVALID, k
+    for k in ("H", "W", "ws"):
+        assert _fwd(**{k: FAKE + 8}) == INVALID, k      # 16-byte alignment
+    for k in ("cand", "slot", "loss", "lse"):
+        assert _fwd(**{k: FAKE + 2}) == INVALID, k      # 4-byte alignment
+    for k in ("H", "W", "cand", "slot", "lse", "dH", "dW", "ws"):
+        assert _bwd(**{k: 0}) == INVALID, k
+    assert _bwd(dH=FAKE + 8) == INVALID and _bwd(dW=FAKE + 4) == INVALID
+    assert _bwd(acc=2) == INVALID
+    for k in ("targets", "cand", "slot", "ws"):
+        assert _cand(**{k: 0}) == INVALID, k
+    assert _cand(targets=FAKE + 1) == INVALID
+
+
+def test_workspace_too_small():
+    L = ss.lib()
+    need = L.ss_workspace_size(256, 50304, 4096, 768)
+    assert _fwd(wsb=need - 1) == WORKSPACE
+    assert _bwd(wsb=need - 1) == WORKSPACE
+    assert _cand(wsb=16) == WORKSPACE
+    assert L.ss_read_status(p(FAKE), 16, None, None, None) == WORKSPACE
+    assert L.ss_read_status(None, 1 << 20, None, None, None) == INVALID
+
+
+def test_trace_bookkeeping_without_launches():
+    L = ss.lib()
+    assert L.ss_trace_begin(None, -1) == INVALID
+    assert L.ss_trace_begin(None, 4) == INVALID
+    assert L.ss_trace_begin(None, 0) == OK
+    assert L.ss_trace_end() == 0
+    assert L.ss_trace_kernel_name(0) is None
+
+
+def test_empty_batch_forward_is_a_no_op():
+    # T = 0: nothing to compute, returns before any device work
+    assert _fwd(T=0, H=0, slot=0, loss=0, lse=0) == OK

@@ -1,0 +1,226 @@
+"""GPU path vs the CPU oracle, through the C ABI.
+
+* small and ragged sizes (several tiles plus a ragged tail in T, C and D, the
+  degenerate cases C = 1, U = C, C = V, T = 1): every output element compared;
+* the five full-size workloads, in the launch configuration the benchmark
+  times: candidates bit-exact, sampled tokens and candidate rows against the
+  oracle computed one by one, and properties that hold at any size;
+* device-side error paths and the write-back contract of dW.
+"""
+import numpy as np
+import pytest
+import torch
+
+import synth
+from gpu_util import GRAD_RTOL, assert_loss_close, rel_fro, run_gpu, to_dev_bf16
+
+pytestmark = pytest.mark.gpu
+
+import sampled_softmax_output_gb300 as ss  # noqa: E402  (fails loudly if libss.so is missing)
+
+
+def _case(T, V, D, C, seed, s=1.1, w_std=0.02):
+    x = synth.make_inputs(T, V, D, s, seed, w_std=w_std)
+    U = len(np.unique(x["targets"]))
+    return x, max(C, U)
+
+
+def _full_oracle(orc, x, C, seed, scale=1.0, dW0=None, accumulate=False):
+    return orc.loss_and_grads(x["H"], x["W"], x["targets"], C, seed, scale, dW_init=dW0,
+                              accumulate=accumulate)
+
+
+SMALL = [
+    # T, V, D, C, seed, scale
+    (1, 64, 64, 1, 1, 1.0),          # a single candidate: loss = 0
+    (7, 300, 64, 37, 2, 1.0),
+    (128, 1000, 768, 256, 3, 1.0),   # exactly one tile each way
+    (300, 3000, 768, 517, 4, 1.0),   # ragged T and C tails
+    (257, 2000, 192, 1000, 5, 0.5),  # D not a multiple of the 256-wide gradient tile
+    (500, 1000, 128, 1000, 6, 1.0 / 500),  # C = V: full vocabulary
+    (200, 5000, 1024, 130, 7, 1.0),  # U close to C
+    (64, 4096, 768, 4096, 8, 1.0),   # C = V, one partial token tile
+]
+
+
+@pytest.mark.parametrize("T,V,D,C,seed,scale", SMALL)
+def test_small_parity(orc, T, V, D, C, seed, scale):
+    x, C = _case(T, V, D, C, seed)
+    ref = _full_oracle(orc, x, C, seed, scale)
+    got = run_gpu(ss, x, C, seed, scale)
+    assert got["status"] == 0
+    assert got["U"] == ref["U"]
+    np.testing.assert_array_equal(got["cand"], ref["cand"])
+    np.testing.assert_array_equal(got["slot"], ref["slot"])
+    assert_loss_close(got["loss"], ref["loss"])
+    assert_loss_close(got["lse"], ref["lse"])
+    assert rel_fro(got["dH"], ref["dH"]) < GRAD_RTOL
+    assert rel_fro(got["dW"], ref["dW"]) < GRAD_RTOL
+    outside = np.setdiff1d(np.arange(V), ref["cand"])
+    assert np.all(got["dW"][outside] == 0)
+
+
+def test_accumulate_and_untouched_rows(orc):
+    T, V, D, C, seed = 300, 2500, 256, 700, 11
+    x, C = _case(T, V, D, C, seed)
+    dW0 = np.random.default_rng(3).standard_normal((V, D)).astype(np.float32)
+    for acc in (False, True):
+        ref = _full_oracle(orc, x, C, seed, 0.25, dW0=dW0, accumulate=acc)
+        got = run_gpu(ss, x, C, seed, 0.25, dW0=dW0, accumulate=acc)
+        assert got["status"] == 0
+        outside = np.setdiff1d(np.arange(V), ref["cand"])
+        np.testing.assert_array_equal(got["dW"][outside], dW0[outside])
+        c = ref["cand"]
+        assert rel_fro(got["dW"][c] - (dW0[c] if acc else 0), ref["dW"][c] - (dW0[c] if acc else 0)) < GRAD_RTOL
+
+
+def test_repeated_calls_are_deterministic(orc):
+    T, V, D, C, seed = 400, 3000, 768, 1200, 12
+    x, C = _case(T, V, D, C, seed)
+    ws = ss.workspace(T, V, C, D)
+    a = run_gpu(ss, x, C, seed, ws=ws)
+    b = run_gpu(ss, x, C, seed, ws=ws)
+    for k in ("cand", "slot", "loss", "lse", "dH", "dW"):
+        np.testing.assert_array_equal(a[k], b[k], err_msg=k)
+
+
+def test_uniform_logits_ln_C(orc):
+    # H = 0: every logit is 0, loss = ln C for every token
+    T, V, D, C = 300, 5000, 768, 2500
+    x, C = _case(T, V, D, C, 13)
+    x["H"] = np.zeros_like(x["H"])
+    got = run_gpu(ss, x, C, 13)
+    np.testing.assert_allclose(got["loss"], np.log(C), rtol=1e-6)
+
+
+# ------------------------------------------------------------- full sizes
+
+@pytest.mark.parametrize("wid", [1, 2, 3, 4, 5])
+def test_full_size_workload(orc, wid):
+    w = synth.WORKLOADS[wid]
+    x = synth.workload_inputs(w)
+    T, V, D, C = w.T, w.V, w.D, w.C
+    # candidates first: bit-exact on the whole batch
+    cand_ref, slot_ref, U_ref = orc.build_candidates(x["targets"], V, C, w.seed)
+    H = to_dev_bf16(x["H"])
+    W = to_dev_bf16(x["W"])
+    targets = torch.from_numpy(x["targets"]).cuda()
+    ws = ss.workspace(T, V, C, D)
+    cand, slot, U = ss.build_candidates(targets, V, C, w.seed, ws, return_U=True)
+    assert U == U_ref
+    np.testing.assert_array_equal(cand.cpu().numpy(), cand_ref)
+    np.testing.assert_array_equal(slot.cpu().numpy(), slot_ref)
+    loss, lse = ss.forward(H, W, cand, slot, ws)
+    canary = 7.0
+    dW = torch.full((V, D), canary, dtype=torch.float32, device="cuda")
+    scale = 1.0 / T
+    dH, dW = ss.backward(H, W, cand, slot, lse, ws, scale=scale, dW=dW)
+    torch.cuda.synchronize()
+    assert ss.read_status(ws)[0] == 0
+    loss, lse = loss.cpu().numpy(), lse.cpu().numpy()
+    dH = dH.float().cpu().numpy()
+    dW = dW.cpu().numpy()
+    # sampled tokens, including both ends and the last partial tile
+    rng = np.random.default_rng(100 + wid)
+    rows = np.unique(np.concatenate([[0, T - 1, (T // 128) * 128 - 1], rng.integers(0, T, 45)]))
+    rows = rows[(rows >= 0) & (rows < T)]
+    l_ref, s_ref = orc.forward(x["H"], x["W"], cand_ref, slot_ref, rows=rows)
+    assert_loss_close(loss[rows], l_ref)
+    assert_loss_close(lse[rows], s_ref)
+    dH_ref = orc.backward_dH(x["H"], x["W"], cand_ref, slot_ref, s_ref, scale, rows=rows)
+    assert rel_fro(dH[rows], dH_ref) < GRAD_RTOL
+    # rows of dW outside the candidate set keep the canary bit for bit
+    outside = np.setdiff1d(np.arange(V), cand_ref)
+    assert outside.size == V - C
+    assert np.all(dW[outside] == canary)
+    dWc = dW[cand_ref].astype(np.float64)
+    # rows of P - Y sum to zero, so the candidate-row gradients sum to zero
+    assert np.linalg.norm(dWc.sum(0)) <= 0.02 * np.linalg.norm(dWc)
+    # <dW_c, W_c> = sum_tj G_tj S_tj = <dH, H>
+    W64 = synth.bf16_bits_to_f32(x["W"]).astype(np.float64)
+    H64 = synth.bf16_bits_to_f32(x["H"]).astype(np.float64)
+    lhs = float((dWc * W64[cand_ref]).sum())
+    rhs = float((dH.astype(np.float64) * H64).sum())
+    assert abs(lhs - rhs) <= 0.02 * abs(rhs)
+    # exact candidate rows where the oracle's full-batch lse is affordable
+    if T * C <= 16384 * 10240:
+        _, lse_all = orc.forward(x["H"], x["W"], cand_ref, slot_ref)
+        cols = np.unique(np.array([0, U_ref - 1, min(U_ref, C - 1), C - 1, C // 2, 1]))
+        ref_rows = orc.backward_dWc(x["H"], x["W"], cand_ref, slot_ref, lse_all, scale, cols=cols)
+        assert rel_fro(dW[cand_ref[cols]], ref_rows) < GRAD_RTOL
+        assert_loss_close(lse, lse_all)
+
+
+# ------------------------------------------------------------ error paths
+
+def _dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def test_target_out_of_range_is_reported_and_blocks_later_calls():
+    T, V, D, C = 100, 1000, 64, 200
+    x = synth.make_inputs(T, V, D, 1.1, 1)
+    x["targets"][17] = V  # out of range
+    ws = ss.workspace(T, V, C, D)
+    with pytest.raises(ss.SSError) as e:
+        ss.build_candidates(_dev(x["targets"]), V, C, 1, ws, return_U=True)
+    assert e.value.name == "SS_ERR_TARGET_RANGE"
+    # the sticky status makes the forward a no-op: outputs keep their sentinel
+    cand = torch.arange(C, dtype=torch.int32, device="cuda")
+    slot = torch.zeros(T, dtype=torch.int32, device="cuda")
+    loss = torch.full((T,), -5.0, device="cuda")
+    lse = torch.full((T,), -5.0, device="cuda")
+    ss.forward(to_dev_bf16(x["H"]), to_dev_bf16(x["W"]), cand, slot, ws, loss=loss, lse=lse)
+    assert ss.read_status(ws)[0] == 4
+    assert torch.all(loss == -5.0) and torch.all(lse == -5.0)
+    # a fresh candidate build clears it
+    x["targets"][17] = 3
+    ss.build_candidates(_dev(x["targets"]), V, C, 1, ws, return_U=True)
+    assert ss.read_status(ws)[0] == 0
+
+
+def test_capacity_error():
+    T, V, D = 50, 1000, 64
+    targets = np.arange(T, dtype=np.int32)
+    ws = ss.workspace(T, V, 40, D)
+    with pytest.raises(ss.SSError) as e:
+        ss.build_candidates(_dev(targets), V, 40, 0, ws, return_U=True)
+    assert e.value.name == "SS_ERR_CAPACITY"
+    assert ss.read_status(ws) == (3, T)
+
+
+def test_bad_cand_and_slot_are_reported():
+    T, V, D, C = 64, 500, 64, 100
+    x = synth.make_inputs(T, V, D, 1.1, 2)
+    ws = ss.workspace(T, V, C, D)
+    H, W = to_dev_bf16(x["H"]), to_dev_bf16(x["W"])
+    cand, slot, U = ss.build_candidates(_dev(x["targets"]), V, C, 2, ws, return_U=True)
+    bad = cand.clone()
+    bad[5] = V + 3
+    ss.forward(H, W, bad, slot, ws)
+    assert ss.read_status(ws)[0] == 8
+    ss.build_candidates(_dev(x["targets"]), V, C, 2, ws)
+    bslot = slot.clone()
+    bslot[3] = C
+    ss.forward(H, W, cand, bslot, ws)
+    assert ss.read_status(ws)[0] == 8
+
+
+def test_empty_batch():
+    V, D, C = 500, 64, 100
+    ws = ss.workspace(0, V, C, D)
+    targets = torch.empty(0, dtype=torch.int32, device="cuda")
+    cand, slot, U = ss.build_candidates(targets, V, C, 5, ws, return_U=True)
+    assert U == 0
+    c = cand.cpu().numpy()
+    assert np.all(np.diff(c) > 0) and c.min() >= 0 and c.max() < V
+    H = torch.empty(0, D, dtype=torch.bfloat16, device="cuda")
+    W = torch.randn(V, D, device="cuda").to(torch.bfloat16)
+    loss, lse = ss.forward(H, W, cand, slot, ws)
+    assert loss.numel() == 0
+    dW = torch.full((V, D), 3.0, device="cuda")
+    ss.backward(H, W, cand, slot, lse, ws, dW=dW)
+    torch.cuda.synchronize()
+    d = dW.cpu().numpy()
+    assert np.all(d[c] == 0)
+    assert np.all(d[np.setdiff1d(np.arange(V), c)] == 3.0)
