@@ -61,6 +61,8 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="target CPU seconds of the oracle sample")
+    ap.add_argument("--ref-step-seconds", type=float, default=None,
+                    help="reference arm: target seconds per step (default: fits the run in ~2.5 min)")
     return ap.parse_args()
 
 
@@ -79,9 +81,21 @@ def load_peaks():
                 "source": "fallback"}
 
 
-def csrc_sha() -> str:
+# the source files that define each traced kernel
+KERNEL_SOURCES = {
+    "gemm_forward_lse": ["ss_ptx.cuh", "ss_gemm.cuh", "ss_gemm_logits.cu"],
+    "gemm_softmax_grad": ["ss_ptx.cuh", "ss_gemm.cuh", "ss_gemm_logits.cu"],
+    "gemm_grad_h": ["ss_ptx.cuh", "ss_gemm.cuh", "ss_gemm_grads.cu"],
+    "gemm_grad_w_scatter": ["ss_ptx.cuh", "ss_gemm.cuh", "ss_gemm_grads.cu"],
+    "build_candidates": ["ss_ptx.cuh", "ss_candidates.cu"],
+}
+
+
+def kernel_sha(kernel: str) -> str:
+    """Hash of the sources of `kernel` (all of csrc/ for kernels not listed)."""
+    names = KERNEL_SOURCES.get(kernel) or sorted(os.listdir(CSRC))
     h = hashlib.sha256()
-    for name in sorted(os.listdir(CSRC)):
+    for name in names:
         with open(os.path.join(CSRC, name), "rb") as f:
             h.update(name.encode() + b"\0" + f.read())
     return h.hexdigest()[:16]
@@ -95,7 +109,7 @@ def load_traffic(kernel: str, workload: str):
             lines = [ln.strip() for ln in f if ln.strip() and not ln.startswith("#")]
     except OSError:
         return None
-    sha = csrc_sha()
+    sha = kernel_sha(kernel)
     for ln in lines:
         parts = dict(kv.split("=", 1) for kv in ln.split())
         if parts.get("kernel") == kernel and parts.get("workload") == workload:
@@ -394,7 +408,8 @@ def run_reference(args, world, rank):
     x = synth.workload_inputs(w)
     K = args.steps if args.steps is not None else 3
     W_ = max(args.warmup, 0)
-    per_step_s = min(5.0, 150.0 / max(K + W_, 1))
+    per_step_s = (args.ref_step_seconds if args.ref_step_seconds is not None
+                  else min(5.0, 150.0 / max(K + W_, 1)))
     scale = 1.0 / w.T
     t_small = oracle_sample(x, w, 8, scale)
     T_s = int(max(1, min(w.T, 8 * per_step_s / max(t_small, 1e-3))))

@@ -155,6 +155,11 @@ ss_status ss_read_status(const void* workspace, size_t workspace_bytes, ss_strea
 /* Static English text for a status code. */
 const char* ss_status_string(ss_status status);
 
+/* Text of the last failing CUDA call made by libss on the calling host thread
+ * (which call, the CUDA error string and code), or "" if none failed yet.
+ * Valid until the next libss call on this thread. */
+const char* ss_last_error(void);
+
 /*
  * Diagnostics: per-kernel timing with CUDA events, for benchmarks.
  * Between ss_trace_begin and ss_trace_end, on the calling host thread, every
@@ -162,9 +167,11 @@ const char* ss_status_string(ss_status status);
  * cudaEventRecord(events[2k + 1]) on the launch stream, for k = 0, 1, ...
  * while k < capacity; later launches are counted but not recorded.
  *   events   : host array of 2 * capacity cudaEvent_t created by the caller.
- * ss_trace_end returns the number of launches since ss_trace_begin;
- * ss_trace_kernel_name(k) is the static name of launch k (k < capacity and
- * k < that count), or NULL. Tracing adds only the event records.
+ * ss_trace_end returns the number of launches since ss_trace_begin, or -1 if
+ * an event record failed (e.g. an invalid event handle; the launches
+ * themselves are unaffected); ss_trace_kernel_name(k) is the static name of
+ * launch k (k < capacity and k < that count), or NULL. Tracing adds only the
+ * event records.
  */
 ss_status ss_trace_begin(void** events, int capacity);
 int ss_trace_end(void);

@@ -43,6 +43,8 @@ class SSError(RuntimeError):
         self.code = int(code)
         self.name = STATUS.get(self.code, str(code))
         msg = _lib.ss_status_string(self.code).decode() if _lib is not None else self.name
+        if self.code == 6 and _lib is not None:
+            msg += "; " + (_lib.ss_last_error() or b"").decode()
         super().__init__(f"{where}: {self.name} ({msg})")
 
 
@@ -66,6 +68,8 @@ def _load():
     L.ss_read_status.argtypes = [p, sz, p, p, p]
     L.ss_status_string.restype = ctypes.c_char_p
     L.ss_status_string.argtypes = [ctypes.c_int]
+    L.ss_last_error.restype = ctypes.c_char_p
+    L.ss_last_error.argtypes = []
     L.ss_trace_begin.restype = ctypes.c_int
     L.ss_trace_begin.argtypes = [p, ctypes.c_int]
     L.ss_trace_end.restype = ctypes.c_int
@@ -237,6 +241,10 @@ class KernelTrace:
     def __init__(self, capacity: int = 256):
         self.capacity = capacity
         self.events = [torch.cuda.Event(enable_timing=True) for _ in range(2 * capacity)]
+        # torch creates the CUDA event at its first record: create them all now
+        for e in self.events:
+            e.record()
+        torch.cuda.synchronize()
         self._handles = (ctypes.c_void_p * (2 * capacity))(
             *[ctypes.c_void_p(e.cuda_event) for e in self.events])
         self.count = 0
@@ -248,6 +256,8 @@ class KernelTrace:
 
     def __exit__(self, *exc):
         self.count = int(_lib.ss_trace_end())
+        if self.count < 0:
+            raise RuntimeError("ss_trace: a CUDA event record failed")
         self.names = [(_lib.ss_trace_kernel_name(k) or b"?").decode()
                       for k in range(min(self.count, self.capacity))]
         return False

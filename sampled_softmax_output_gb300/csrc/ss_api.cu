@@ -7,9 +7,11 @@
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
+#include <stdio.h>
 
 #include <atomic>
 #include <mutex>
+#include <vector>
 
 #include "ss.h"
 #include "ss_internal.h"
@@ -175,18 +177,27 @@ int rows_grid(int64_t rows, int num_sms) {
   return static_cast<int>(want < cap ? (want > 0 ? want : 1) : cap);
 }
 
-ss_status cuda_status(cudaError_t e) { return e == cudaSuccess ? SS_OK : SS_ERR_CUDA; }
+// Detail of the last failing CUDA call on this host thread (ss_last_error).
+thread_local char g_err[256] = "";
+
+ss_status fail(const char* what, cudaError_t e) {
+  snprintf(g_err, sizeof g_err, "%s: %s (%d)", what, cudaGetErrorString(e), static_cast<int>(e));
+  return SS_ERR_CUDA;
+}
+
+ss_status cuda_status(cudaError_t e, const char* what) {
+  return e == cudaSuccess ? SS_OK : fail(what, e);
+}
 
 // ------------------------------------------------------------ launch trace
 
-constexpr int kTraceNames = 4096;
-
 struct Trace {
   bool on = false;
+  bool failed = false;
   cudaEvent_t* events = nullptr;
   int capacity = 0;
   int count = 0;
-  const char* names[kTraceNames];
+  std::vector<const char*> names;  // one per recorded launch (host memory)
 };
 thread_local Trace g_trace;
 
@@ -194,15 +205,22 @@ void trace_pre(cudaStream_t s, const char* name) {
   Trace& t = g_trace;
   if (!t.on) return;
   if (t.count < t.capacity) {
-    cudaEventRecord(t.events[2 * t.count], s);
-    if (t.count < kTraceNames) t.names[t.count] = name;
+    // A failed record must not leave a pending error for the launch checks.
+    if (cudaEventRecord(t.events[2 * t.count], s) != cudaSuccess) {
+      (void)cudaGetLastError();
+      t.failed = true;
+    }
+    t.names.push_back(name);
   }
 }
 
 void trace_post(cudaStream_t s) {
   Trace& t = g_trace;
   if (!t.on) return;
-  if (t.count < t.capacity) cudaEventRecord(t.events[2 * t.count + 1], s);
+  if (t.count < t.capacity && cudaEventRecord(t.events[2 * t.count + 1], s) != cudaSuccess) {
+    (void)cudaGetLastError();
+    t.failed = true;
+  }
   ++t.count;
 }
 
@@ -229,17 +247,18 @@ ss_status ss_build_candidates(const int32_t* targets, int64_t T, int64_t V, int6
   if (workspace_bytes < kHdrBytes) return SS_ERR_WORKSPACE;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   int* hdr = static_cast<int*>(workspace);
-  if (cudaMemsetAsync(hdr, 0, 2 * sizeof(int), s) != cudaSuccess) return SS_ERR_CUDA;
+  cudaError_t e = cudaMemsetAsync(hdr, 0, 2 * sizeof(int), s);
+  if (e != cudaSuccess) return fail("cudaMemsetAsync(status)", e);
   trace_pre(s, "build_candidates");
-  const cudaError_t e = launch_build_candidates(targets, static_cast<int>(T), static_cast<int>(V),
+  e = launch_build_candidates(targets, static_cast<int>(T), static_cast<int>(V),
                                                 static_cast<int>(C), seed, cand, slot, hdr, s);
   trace_post(s);
-  if (e != cudaSuccess) return SS_ERR_CUDA;
+  if (e != cudaSuccess) return fail("launch k_build_candidates", e);
   if (U_host) {
     int32_t h[2] = {0, 0};
-    if (cudaMemcpyAsync(h, hdr, sizeof h, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
-        cudaStreamSynchronize(s) != cudaSuccess)
-      return SS_ERR_CUDA;
+    e = cudaMemcpyAsync(h, hdr, sizeof h, cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return fail("read status after candidate build", e);
     *U_host = h[1];
     return static_cast<ss_status>(h[0]);
   }
@@ -261,7 +280,7 @@ ss_status ss_forward(const uint16_t* H, const uint16_t* W, const int32_t* cand,
   if (workspace_bytes < L.total) return SS_ERR_WORKSPACE;
   if (T == 0) return SS_OK;
   const int nsm = num_sms_current();
-  if (nsm <= 0) return SS_ERR_CUDA;
+  if (nsm <= 0) return fail("cudaGetDevice/cudaDeviceGetAttribute", cudaGetLastError());
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   char* ws = static_cast<char*>(workspace);
   int* status = reinterpret_cast<int*>(ws + L.hdr);
@@ -274,23 +293,23 @@ ss_status ss_forward(const uint16_t* H, const uint16_t* W, const int32_t* cand,
                                                    static_cast<int>(V), static_cast<int>(D), Wc,
                                                    status);
   trace_post(s);
-  if (cudaGetLastError() != cudaSuccess) return SS_ERR_CUDA;
+  if (cudaError_t e0 = cudaGetLastError(); e0 != cudaSuccess) return fail("launch k_gather_rows", e0);
 
   CUtensorMap tH, tWc;
   if (!make_map(&tH, H, D, T, D * 2, 64, 128) || !make_map(&tWc, Wc, D, C, D * 2, 64, kBnLogits))
-    return SS_ERR_CUDA;
+    return fail("cuTensorMapEncodeTiled", cudaErrorInvalidValue);
   trace_pre(s, "gemm_forward_lse");
   const cudaError_t e = launch_forward_logits(tH, tWc, static_cast<int>(T), static_cast<int>(C),
                                               static_cast<int>(D), slot, part, tgt, status, nsm,
                                               s);
   trace_post(s);
-  if (e != cudaSuccess) return SS_ERR_CUDA;
+  if (e != cudaSuccess) return fail("launch gemm_forward_lse", e);
   const int blocks = static_cast<int>((T + 255) / 256);
   trace_pre(s, "lse_merge");
   k_lse_merge<<<blocks, 256, 0, s>>>(part, tgt, slot, static_cast<int>(T), static_cast<int>(C),
                                      static_cast<int>(L.n_ct), loss, lse, status);
   trace_post(s);
-  return cuda_status(cudaGetLastError());
+  return cuda_status(cudaGetLastError(), "launch k_lse_merge");
 }
 
 ss_status ss_backward(const uint16_t* H, const uint16_t* W, const int32_t* cand,
@@ -308,7 +327,7 @@ ss_status ss_backward(const uint16_t* H, const uint16_t* W, const int32_t* cand,
   const Layout L = make_layout(T, C, D);
   if (workspace_bytes < L.total) return SS_ERR_WORKSPACE;
   const int nsm = num_sms_current();
-  if (nsm <= 0) return SS_ERR_CUDA;
+  if (nsm <= 0) return fail("cudaGetDevice/cudaDeviceGetAttribute", cudaGetLastError());
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   char* ws = static_cast<char*>(workspace);
   int* status = reinterpret_cast<int*>(ws + L.hdr);
@@ -320,7 +339,7 @@ ss_status ss_backward(const uint16_t* H, const uint16_t* W, const int32_t* cand,
       trace_pre(s, "zero_rows");
       k_zero_rows<<<rows_grid(C, nsm), 256, 0, s>>>(cand, iC, iV, iD, dW, status);
       trace_post(s);
-      return cuda_status(cudaGetLastError());
+      return cuda_status(cudaGetLastError(), "launch k_zero_rows");
     }
     return SS_OK;
   }
@@ -330,28 +349,28 @@ ss_status ss_backward(const uint16_t* H, const uint16_t* W, const int32_t* cand,
   trace_pre(s, "gather_rows");
   k_gather_rows<<<rows_grid(C, nsm), 256, 0, s>>>(W, cand, iC, iV, iD, Wc, status);
   trace_post(s);
-  if (cudaGetLastError() != cudaSuccess) return SS_ERR_CUDA;
+  if (cudaError_t e0 = cudaGetLastError(); e0 != cudaSuccess) return fail("launch k_gather_rows", e0);
 
   CUtensorMap tH, tWc, tGk, tWcMn, tGmn, tHmn;
   const uint64_t gRow = static_cast<uint64_t>(L.ldG) * 2;
   if (!make_map(&tH, H, D, T, D * 2, 64, 128) || !make_map(&tWc, Wc, D, C, D * 2, 64, kBnLogits) ||
       !make_map(&tGk, G, C, T, gRow, 64, 128) || !make_map(&tWcMn, Wc, D, C, D * 2, 64, 64) ||
       !make_map(&tGmn, G, C, T, gRow, 64, 64) || !make_map(&tHmn, H, D, T, D * 2, 64, 64))
-    return SS_ERR_CUDA;
+    return fail("cuTensorMapEncodeTiled", cudaErrorInvalidValue);
 
   trace_pre(s, "gemm_softmax_grad");
   cudaError_t e = launch_softmax_grad(tH, tWc, iT, iC, iD, static_cast<int>(L.ldG), slot, lse,
                                       scale, G, status, nsm, s);
   trace_post(s);
-  if (e != cudaSuccess) return SS_ERR_CUDA;
+  if (e != cudaSuccess) return fail("launch gemm_softmax_grad", e);
   trace_pre(s, "gemm_grad_h");
   e = launch_grad_h(tGk, tWcMn, iT, iC, iD, dH, status, nsm, s);
   trace_post(s);
-  if (e != cudaSuccess) return SS_ERR_CUDA;
+  if (e != cudaSuccess) return fail("launch gemm_grad_h", e);
   trace_pre(s, "gemm_grad_w_scatter");
   e = launch_grad_w(tGmn, tHmn, iT, iC, iD, iV, accumulate, cand, dW, status, nsm, s);
   trace_post(s);
-  if (e != cudaSuccess) return SS_ERR_CUDA;
+  if (e != cudaSuccess) return fail("launch gemm_grad_w_scatter", e);
   return SS_OK;
 }
 
@@ -361,9 +380,9 @@ ss_status ss_read_status(const void* workspace, size_t workspace_bytes, ss_strea
   if (workspace_bytes < kHdrBytes) return SS_ERR_WORKSPACE;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   int32_t h[2] = {0, 0};
-  if (cudaMemcpyAsync(h, workspace, sizeof h, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
-      cudaStreamSynchronize(s) != cudaSuccess)
-    return SS_ERR_CUDA;
+  cudaError_t e = cudaMemcpyAsync(h, workspace, sizeof h, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return fail("ss_read_status", e);
   if (device_status_host) *device_status_host = h[0];
   if (U_status_host) *U_status_host = h[1];
   return static_cast<ss_status>(h[0]);
@@ -376,20 +395,24 @@ ss_status ss_trace_begin(void** events, int capacity) {
   t.events = reinterpret_cast<cudaEvent_t*>(events);
   t.capacity = capacity;
   t.count = 0;
+  t.failed = false;
+  t.names.clear();
   return SS_OK;
 }
 
 int ss_trace_end(void) {
   Trace& t = g_trace;
   t.on = false;
-  return t.count;
+  return t.failed ? -1 : t.count;
 }
 
 const char* ss_trace_kernel_name(int k) {
   const Trace& t = g_trace;
-  if (k < 0 || k >= t.count || k >= t.capacity || k >= kTraceNames) return nullptr;
+  if (k < 0 || k >= t.count || k >= static_cast<int>(t.names.size())) return nullptr;
   return t.names[k];
 }
+
+const char* ss_last_error(void) { return g_err; }
 
 const char* ss_status_string(ss_status status) {
   switch (status) {

@@ -224,3 +224,17 @@ def test_empty_batch():
     d = dW.cpu().numpy()
     assert np.all(d[c] == 0)
     assert np.all(d[np.setdiff1d(np.arange(V), c)] == 3.0)
+
+
+def test_kernel_trace_records_every_launch():
+    T, V, D, C = 300, 3000, 768, 517
+    x, C = _case(T, V, D, C, 4)
+    H, W = to_dev_bf16(x["H"]), to_dev_bf16(x["W"])
+    ws = ss.workspace(T, V, C, D)
+    with ss.KernelTrace(capacity=16) as tr:
+        ss.step(H, W, _dev(x["targets"]), C, 4, ws)
+    torch.cuda.synchronize()
+    names = [n for n, _ in tr.timings()]
+    assert names == ["build_candidates", "gather_rows", "gemm_forward_lse", "lse_merge",
+                     "gather_rows", "gemm_softmax_grad", "gemm_grad_h", "gemm_grad_w_scatter"]
+    assert all(ms > 0 for _, ms in tr.timings())
