@@ -144,6 +144,38 @@ ss_status ss_backward(const uint16_t* H, const uint16_t* W, const int32_t* cand,
                       void* workspace, size_t workspace_bytes, ss_stream stream);
 
 /*
+ * Allocation-free forward pass. Not part of the method on the pages (the
+ * paper has no counterpart): an operational variant of ss_forward for callers
+ * that cannot allocate device memory at all -- for example code running as a
+ * plugin inside a host program that has planned and owns every byte of device
+ * memory and hands the plugin only its input and output buffers, or code on a
+ * path where a cudaMalloc (which can synchronise the whole device) is not
+ * acceptable. Such a caller has no workspace to pass.
+ *
+ * Same arguments and results as ss_forward, minus the workspace: the scratch
+ * (gathered candidate rows, softmax partials, status word) lives in a
+ * fixed-size array inside the library's own device data, of
+ * SS_NOALLOC_SCRATCH_BYTES. Every GPU that loads the library holds that array
+ * until the process exits. Sizes whose scratch, 1 KB + C*D*2 +
+ * ceil(C/256)*T*8 + T*4 bytes (each term rounded up to 1 KB), exceeds it are
+ * rejected with SS_ERR_UNSUPPORTED (ss_last_error says by how much).
+ *   status_host : NULL, or a host int32 that receives the device status
+ *                 word of this call after the stream is synchronised; the
+ *                 call then also returns it (e.g. SS_ERR_INDEX).
+ * The first call on a device looks up the array's device address (once per
+ * device, with that device current); make that first call before any stream
+ * capture. The call allocates nothing: no cudaMalloc, no cudaFree, no
+ * allocating library routine. All calls share the one array, which keeps the
+ * previous call's contents; each call clears its status word first and
+ * overwrites everything else it reads. Calls whose work overlaps on the GPU
+ * (other streams, other host threads) race on the array: serialise them.
+ */
+#define SS_NOALLOC_SCRATCH_BYTES (32u << 20)
+ss_status ss_forward_noalloc(const uint16_t* H, const uint16_t* W, const int32_t* cand,
+                             const int32_t* slot, int64_t T, int64_t V, int64_t C, int64_t D,
+                             float* loss, float* lse, int32_t* status_host, ss_stream stream);
+
+/*
  * Synchronise `stream` and read the workspace status word (one of ss_status)
  * into *device_status_host and the last U written by ss_build_candidates into
  * *U_status_host (either may be NULL). Returns SS_ERR_CUDA if the
@@ -155,9 +187,10 @@ ss_status ss_read_status(const void* workspace, size_t workspace_bytes, ss_strea
 /* Static English text for a status code. */
 const char* ss_status_string(ss_status status);
 
-/* Text of the last failing CUDA call made by libss on the calling host thread
- * (which call, the CUDA error string and code), or "" if none failed yet.
- * Valid until the next libss call on this thread. */
+/* Text of the last failure recorded by libss on the calling host thread (the
+ * failing CUDA call with its error string and code, or a size limit that was
+ * exceeded), or "" if none yet. Valid until the next libss call on this
+ * thread. */
 const char* ss_last_error(void);
 
 /*

@@ -36,6 +36,7 @@ STATUS = {
 }
 MAX_V = 524288
 MAX_D = 16384
+NOALLOC_SCRATCH_BYTES = 32 << 20
 
 
 class SSError(RuntimeError):
@@ -68,6 +69,8 @@ def _load():
     L.ss_read_status.argtypes = [p, sz, p, p, p]
     L.ss_status_string.restype = ctypes.c_char_p
     L.ss_status_string.argtypes = [ctypes.c_int]
+    L.ss_forward_noalloc.restype = ctypes.c_int
+    L.ss_forward_noalloc.argtypes = [p, p, p, p, i64, i64, i64, i64, p, p, p, p]
     L.ss_last_error.restype = ctypes.c_char_p
     L.ss_last_error.argtypes = []
     L.ss_trace_begin.restype = ctypes.c_int
@@ -188,6 +191,32 @@ def forward(H: torch.Tensor, W: torch.Tensor, cand: torch.Tensor, slot: torch.Te
     code = _lib.ss_forward(_ptr(H), _ptr(W), _ptr(cand), _ptr(slot), T, V, C, D, _ptr(loss),
                            _ptr(lse), _ptr(ws), ws.numel(), _stream(dev))
     _check(code, "ss_forward")
+    return loss, lse
+
+
+def forward_noalloc(H: torch.Tensor, W: torch.Tensor, cand: torch.Tensor, slot: torch.Tensor,
+                    loss: torch.Tensor, lse: torch.Tensor, check_status: bool = False):
+    """ss_forward_noalloc: the forward pass with no workspace, for callers that
+    cannot allocate device memory (the library's fixed scratch array is used
+    instead; see include/ss.h). The caller passes the output tensors; this
+    wrapper allocates nothing either. check_status=True synchronises and
+    raises on a device-side error of this call."""
+    _need(H, "H", torch.bfloat16)
+    dev = H.device
+    T, D = H.shape
+    _need(W, "W", torch.bfloat16, dev)
+    V = W.shape[0]
+    C = cand.numel()
+    _need(W, "W", torch.bfloat16, dev, (V, D))
+    _need(cand, "cand", torch.int32, dev, (C,))
+    _need(slot, "slot", torch.int32, dev, (T,))
+    _need(loss, "loss", torch.float32, dev, (T,))
+    _need(lse, "lse", torch.float32, dev, (T,))
+    st = ctypes.c_int32(0)
+    code = _lib.ss_forward_noalloc(_ptr(H), _ptr(W), _ptr(cand), _ptr(slot), T, V, C, D,
+                                   _ptr(loss), _ptr(lse), ctypes.byref(st) if check_status else None,
+                                   _stream(dev))
+    _check(code, "ss_forward_noalloc")
     return loss, lse
 
 

@@ -224,6 +224,34 @@ void trace_post(cudaStream_t s) {
   ++t.count;
 }
 
+// ------------------------------------------------- allocation-free forward
+// Scratch of ss_forward_noalloc, in the library's own device data: callers
+// of that entry point pass no workspace. Host code must not use this name as
+// an address -- on the host it is only a stand-in; the device address comes
+// from cudaGetSymbolAddress below.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[SS_NOALLOC_SCRATCH_BYTES];
+
+std::mutex g_noalloc_mu;
+void* g_noalloc_addr[kMaxDevices];
+
+// Device address of g_noalloc_scratch on the current device, looked up once
+// per device (with that device current) and cached.
+cudaError_t noalloc_scratch_address(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (g_noalloc_addr[dev] == nullptr) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return e;
+    g_noalloc_addr[dev] = p;
+  }
+  *out = g_noalloc_addr[dev];
+  return cudaSuccess;
+}
+
 }  // namespace
 }  // namespace ss
 
@@ -371,6 +399,79 @@ ss_status ss_backward(const uint16_t* H, const uint16_t* W, const int32_t* cand,
   e = launch_grad_w(tGmn, tHmn, iT, iC, iD, iV, accumulate, cand, dW, status, nsm, s);
   trace_post(s);
   if (e != cudaSuccess) return fail("launch gemm_grad_w_scatter", e);
+  return SS_OK;
+}
+
+ss_status ss_forward_noalloc(const uint16_t* H, const uint16_t* W, const int32_t* cand,
+                             const int32_t* slot, int64_t T, int64_t V, int64_t C, int64_t D,
+                             float* loss, float* lse, int32_t* status_host, ss_stream stream) {
+  const ss_status st = check_sizes(T, V, C, D);
+  if (st != SS_OK) return st;
+  if (!W || !cand || (T > 0 && (!H || !slot || !loss || !lse))) return SS_ERR_INVALID;
+  if (!aligned(H, 16) || !aligned(W, 16) || !aligned(cand, 4) || !aligned(slot, 4) ||
+      !aligned(loss, 4) || !aligned(lse, 4))
+    return SS_ERR_INVALID;
+  // Everything up to the G region of the ordinary workspace: header, W_c,
+  // forward partials, target logits.
+  const Layout L = make_layout(T, C, D);
+  const size_t need = L.g;
+  if (need > SS_NOALLOC_SCRATCH_BYTES) {
+    snprintf(g_err, sizeof g_err,
+             "ss_forward_noalloc: T=%lld C=%lld D=%lld needs %zu bytes of scratch, the fixed "
+             "array holds %u",
+             static_cast<long long>(T), static_cast<long long>(C), static_cast<long long>(D),
+             need, static_cast<unsigned>(SS_NOALLOC_SCRATCH_BYTES));
+    return SS_ERR_UNSUPPORTED;
+  }
+  if (T == 0) {
+    if (status_host) *status_host = SS_OK;
+    return SS_OK;
+  }
+  const int nsm = num_sms_current();
+  if (nsm <= 0) return fail("cudaGetDevice/cudaDeviceGetAttribute", cudaGetLastError());
+  void* base = nullptr;
+  cudaError_t e = noalloc_scratch_address(&base);
+  if (e != cudaSuccess) return fail("cudaGetSymbolAddress(scratch)", e);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  char* ws = static_cast<char*>(base);
+  int* status = reinterpret_cast<int*>(ws + L.hdr);
+  uint16_t* Wc = reinterpret_cast<uint16_t*>(ws + L.wc);
+  float2* part = reinterpret_cast<float2*>(ws + L.part);
+  float* tgt = reinterpret_cast<float*>(ws + L.tgt);
+
+  // The array keeps the previous call's contents: the status word must start
+  // at zero; W_c, the partials and the target logits are overwritten before
+  // they are read.
+  e = cudaMemsetAsync(status, 0, 2 * sizeof(int), s);
+  if (e != cudaSuccess) return fail("cudaMemsetAsync(scratch status)", e);
+  trace_pre(s, "gather_rows");
+  k_gather_rows<<<rows_grid(C, nsm), 256, 0, s>>>(W, cand, static_cast<int>(C),
+                                                   static_cast<int>(V), static_cast<int>(D), Wc,
+                                                   status);
+  trace_post(s);
+  if (cudaError_t e0 = cudaGetLastError(); e0 != cudaSuccess) return fail("launch k_gather_rows", e0);
+  CUtensorMap tH, tWc;
+  if (!make_map(&tH, H, D, T, D * 2, 64, 128) || !make_map(&tWc, Wc, D, C, D * 2, 64, kBnLogits))
+    return fail("cuTensorMapEncodeTiled", cudaErrorInvalidValue);
+  trace_pre(s, "gemm_forward_lse");
+  e = launch_forward_logits(tH, tWc, static_cast<int>(T), static_cast<int>(C),
+                            static_cast<int>(D), slot, part, tgt, status, nsm, s);
+  trace_post(s);
+  if (e != cudaSuccess) return fail("launch gemm_forward_lse", e);
+  trace_pre(s, "lse_merge");
+  k_lse_merge<<<static_cast<int>((T + 255) / 256), 256, 0, s>>>(
+      part, tgt, slot, static_cast<int>(T), static_cast<int>(C), static_cast<int>(L.n_ct), loss,
+      lse, status);
+  trace_post(s);
+  if (cudaError_t e0 = cudaGetLastError(); e0 != cudaSuccess) return fail("launch k_lse_merge", e0);
+  if (status_host) {
+    int32_t h[2] = {0, 0};
+    e = cudaMemcpyAsync(h, status, sizeof h, cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return fail("read scratch status", e);
+    *status_host = h[0];
+    return static_cast<ss_status>(h[0]);
+  }
   return SS_OK;
 }
 

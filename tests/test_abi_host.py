@@ -18,7 +18,7 @@ def test_exports_every_declared_symbol():
     assert set(names) == {"ss_workspace_size", "ss_build_candidates", "ss_forward",
                           "ss_backward", "ss_read_status", "ss_status_string",
                           "ss_trace_begin", "ss_trace_end", "ss_trace_kernel_name",
-                          "ss_last_error"}
+                          "ss_last_error", "ss_forward_noalloc"}
     for n in names:
         assert hasattr(ss.lib(), n), n
 
