@@ -45,7 +45,8 @@ import synth  # noqa: E402
 METRIC = "sampled-softmax CE fwd+bwd tokens/s; % of GB300 bf16 tensor peak"
 UNIT = "tokens/s"
 L2_FLUSH_BYTES = 256 << 20
-GEMM_KERNELS = ("gemm_forward_lse", "gemm_softmax_grad", "gemm_grad_h", "gemm_grad_w_scatter")
+# algorithmic flops per launch of each GEMM kernel, in units of T*C*D
+GEMM_FLOPS_TCD = {"gemm_forward_lse": 2, "gemm_softmax_grad": 2, "gemm_grads_streamk": 4}
 CSRC = os.path.join(ROOT, "sampled_softmax_output_gb300", "csrc")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
 
@@ -85,8 +86,7 @@ def load_peaks():
 KERNEL_SOURCES = {
     "gemm_forward_lse": ["ss_ptx.cuh", "ss_gemm.cuh", "ss_gemm_logits.cu"],
     "gemm_softmax_grad": ["ss_ptx.cuh", "ss_gemm.cuh", "ss_gemm_logits.cu"],
-    "gemm_grad_h": ["ss_ptx.cuh", "ss_gemm.cuh", "ss_gemm_grads.cu"],
-    "gemm_grad_w_scatter": ["ss_ptx.cuh", "ss_gemm.cuh", "ss_gemm_grads.cu"],
+    "gemm_grads_streamk": ["ss_ptx.cuh", "ss_gemm.cuh", "ss_gemm_grads.cu"],
     "build_candidates": ["ss_ptx.cuh", "ss_candidates.cu"],
 }
 
@@ -335,8 +335,8 @@ def run_native(args, world, rank, local):
         k["share"] = k["total_ms"] / traced_total if traced_total > 0 else None
     dom = max(kern, key=lambda n: kern[n]["total_ms"])
     peaks = load_peaks()
-    flops = 2.0 * T * C * D
-    if dom in GEMM_KERNELS:
+    if dom in GEMM_FLOPS_TCD:
+        flops = float(GEMM_FLOPS_TCD[dom]) * T * C * D
         achieved = flops / (kern[dom]["avg_ms"] * 1e-3) / 1e12
         peak = peaks["bf16_tflops"]
         roof = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak,

@@ -23,7 +23,7 @@ namespace {
 // ------------------------------------------------------------ workspace
 
 struct Layout {
-  size_t hdr, wc, part, tgt, g, total;
+  size_t hdr, wc, part, tgt, g, gpart, gflags, total;
   int64_t ldG, n_ct;
 };
 
@@ -46,6 +46,10 @@ Layout make_layout(int64_t T, int64_t C, int64_t D) {
   off = align_up(off + static_cast<size_t>(T) * sizeof(float), 1024);
   L.g = off;
   off = align_up(off + static_cast<size_t>(T) * L.ldG * 2, 1024);
+  L.gpart = off;
+  off = align_up(off + grad_partial_bytes(), 1024);
+  L.gflags = off;
+  off = align_up(off + grad_flag_bytes(), 1024);
   L.total = off;
   return L;
 }
@@ -275,10 +279,9 @@ ss_status ss_build_candidates(const int32_t* targets, int64_t T, int64_t V, int6
   if (workspace_bytes < kHdrBytes) return SS_ERR_WORKSPACE;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   int* hdr = static_cast<int*>(workspace);
-  cudaError_t e = cudaMemsetAsync(hdr, 0, 2 * sizeof(int), s);
-  if (e != cudaSuccess) return fail("cudaMemsetAsync(status)", e);
+  // the kernel clears the status word before anything else
   trace_pre(s, "build_candidates");
-  e = launch_build_candidates(targets, static_cast<int>(T), static_cast<int>(V),
+  cudaError_t e = launch_build_candidates(targets, static_cast<int>(T), static_cast<int>(V),
                                                 static_cast<int>(C), seed, cand, slot, hdr, s);
   trace_post(s);
   if (e != cudaSuccess) return fail("launch k_build_candidates", e);
@@ -387,18 +390,15 @@ ss_status ss_backward(const uint16_t* H, const uint16_t* W, const int32_t* cand,
     return fail("cuTensorMapEncodeTiled", cudaErrorInvalidValue);
 
   trace_pre(s, "gemm_softmax_grad");
-  cudaError_t e = launch_softmax_grad(tH, tWc, iT, iC, iD, static_cast<int>(L.ldG), slot, lse,
-                                      scale, G, status, nsm, s);
+  cudaError_t e = launch_softmax_grad(tH, tWc, tGk, iT, iC, iD, slot, lse, scale, status, nsm, s);
   trace_post(s);
   if (e != cudaSuccess) return fail("launch gemm_softmax_grad", e);
-  trace_pre(s, "gemm_grad_h");
-  e = launch_grad_h(tGk, tWcMn, iT, iC, iD, dH, status, nsm, s);
+  trace_pre(s, "gemm_grads_streamk");
+  e = launch_grads(tGk, tWcMn, tGmn, tHmn, iT, iC, iD, iV, accumulate, cand, dH, dW,
+                   reinterpret_cast<float*>(ws + L.gpart), reinterpret_cast<int*>(ws + L.gflags),
+                   status, nsm, s);
   trace_post(s);
-  if (e != cudaSuccess) return fail("launch gemm_grad_h", e);
-  trace_pre(s, "gemm_grad_w_scatter");
-  e = launch_grad_w(tGmn, tHmn, iT, iC, iD, iV, accumulate, cand, dW, status, nsm, s);
-  trace_post(s);
-  if (e != cudaSuccess) return fail("launch gemm_grad_w_scatter", e);
+  if (e != cudaSuccess) return fail("launch gemm_grads_streamk", e);
   return SS_OK;
 }
 

@@ -13,14 +13,24 @@
 //                  without replacement when the hash behaves as random;
 //   slot[t]      = rank of targets[t] among the distinct targets.
 //
-// One CTA of 1024 threads does all of it with the vocabulary bitmap in shared
-// memory (V bits; 6.3 KB at V = 50,304):
-//   1. mark targets in the bitmap (range-checked);
-//   2. popcount + block scan -> U and the per-word target prefix;
-//   3. radix-select (4 passes of 8 bits) of the (C-U)-th smallest hash among
-//      non-targets, ties broken by id;
-//   4. block scans over the id range -> compaction into cand;
-//   5. slot[t] = word prefix + popcount of the lower bits of its word.
+// One thread-block cluster of 8 CTAs x 1024 threads. CTA r owns a contiguous
+// slice of the vocabulary bitmap in its shared memory; peers reach it through
+// distributed shared memory (DSMEM):
+//   1. mark targets in a CTA-local bitmap of the whole vocabulary (range-
+//      checked shared-memory atomics), then OR the eight local bitmaps into
+//      each owner's slice;
+//   2. popcounts + block scans + cluster prefix -> U, per-word target prefix;
+//   3. radix-select the (C-U)-th smallest key among non-targets with 12-bit
+//      digits over the 32-bit hash: per-CTA histograms, reduce-scattered over
+//      the cluster (CTA r sums one eighth of the bins); as soon as the
+//      selected bin holds at most kTieCap ids they are
+//      ranked exactly by (hash, id); at the last digit, equal hashes are
+//      taken in id order. Selected ids go into a second bitmap;
+//   4. compaction: popcount scans over the two bitmaps -> cand;
+//   5. slot[t] = word prefix + popcount of the lower bits of its word, from
+//      local copies of the whole bitmap and prefix array.
+// The whole vocabulary is hashed twice in the common case.
+#include <cooperative_groups.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -28,11 +38,23 @@
 #include "ss_internal.h"
 #include "ss_ptx.cuh"
 
+namespace cg = cooperative_groups;
+
 namespace ss {
 
 namespace {
 
+constexpr int kClusterCtas = 8;
 constexpr int kCandThreads = 1024;
+constexpr int kWarps = kCandThreads / 32;
+constexpr int kBins = 4096;   // 12-bit digits (the last digit has 8 bits)
+#ifndef SS_TIE_CAP
+#define SS_TIE_CAP 1024
+#endif
+constexpr int kTieCap = SS_TIE_CAP;  // ranked exactly when the selected bin is this small
+// tie-list entries allocated: at least 2 and even, so that the arrays after it
+// stay 16-byte aligned for vector access
+constexpr int kTieSlots = ((kTieCap > 2 ? kTieCap : 2) + 1) & ~1;
 
 __device__ __forceinline__ uint32_t negative_hash(uint64_t seed, uint32_t v) {
   uint64_t z = seed + (static_cast<uint64_t>(v) + 1ull) * 0x9E3779B97F4A7C15ull;
@@ -42,9 +64,8 @@ __device__ __forceinline__ uint32_t negative_hash(uint64_t seed, uint32_t v) {
   return static_cast<uint32_t>(z >> 32);
 }
 
-// Exclusive scan of one value per thread over the 1024-thread block.
-__device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t x, uint32_t* warp_sums,
-                                                         uint32_t* total) {
+// Exclusive scan of one value per thread over the block; *total = block sum.
+__device__ __forceinline__ uint32_t block_scan(uint32_t x, uint32_t* ws, uint32_t* total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   uint32_t incl = x;
 #pragma unroll
@@ -52,167 +73,391 @@ __device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t x, uint32_t* w
     const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
     if (lane >= o) incl += y;
   }
-  if (lane == 31) warp_sums[warp] = incl;
+  if (lane == 31) ws[warp] = incl;
   __syncthreads();
   if (warp == 0) {
-    uint32_t w = warp_sums[lane];
+    const uint32_t w = ws[lane];
     uint32_t wi = w;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const uint32_t y = __shfl_up_sync(0xffffffffu, wi, o);
       if (lane >= o) wi += y;
     }
-    warp_sums[lane] = wi - w;  // exclusive prefix of warp totals
-    if (lane == 31) warp_sums[32] = wi;
+    ws[lane] = wi - w;
+    if (lane == 31) ws[32] = wi;
   }
   __syncthreads();
-  const uint32_t r = warp_sums[warp] + incl - x;
-  *total = warp_sums[32];
-  __syncthreads();  // warp_sums may be reused by the caller's next scan
+  const uint32_t r = ws[warp] + incl - x;
+  *total = ws[32];
+  __syncthreads();
   return r;
 }
 
-__global__ void __launch_bounds__(kCandThreads, 1)
+struct Shared {
+  uint32_t scan[33];
+  int err;
+  uint32_t U_r, S_r, E_r;     // this CTA's targets, selected negatives, final-digit ties
+  uint32_t ntie;              // entries in this CTA's tie list
+  uint32_t slice_sum;         // sum of this CTA's slice of the cluster histogram
+  uint32_t b, rem, cnt;       // selected bin, remaining rank inside it, its size
+  uint32_t U, Uoff, Soff, Eoff, any_err, s_slice, s_rem;  // broadcast values
+};
+
+// All peer scalars are read by one thread and broadcast through shared memory:
+// distributed shared memory is limited by its request rate, so no phase lets
+// every thread of a CTA fetch the same remote word.
+__global__ void __cluster_dims__(kClusterCtas, 1, 1) __launch_bounds__(kCandThreads, 1)
     k_build_candidates(const int32_t* __restrict__ targets, int T, int V, int C, uint64_t seed,
-                       int32_t* __restrict__ cand, int32_t* __restrict__ slot, int* hdr) {
-  extern __shared__ uint32_t sm[];
-  __shared__ uint32_t warp_sums[33];
-  __shared__ uint32_t hist[256];
-  __shared__ int s_err;
-  __shared__ uint32_t s_digit, s_rem;
+                       int32_t* __restrict__ cand, int32_t* __restrict__ slot, int* hdr, int wpc) {
+  cg::cluster_group cluster = cg::this_cluster();
+  const int r = static_cast<int>(cluster.block_rank());
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
-  const int tid = threadIdx.x;
+  extern __shared__ __align__(16) uint32_t dyn[];
+  __shared__ Shared sh;
   const int nW = (V + 31) >> 5;
-  uint32_t* bm = sm;         // [nW] target bitmap
-  uint32_t* wpre = sm + nW;  // [nW] number of targets in words before w
+  const int nWp = (nW + 3) & ~3;   // padded to whole uint4
+  uint32_t* bm = dyn;              // [wpc] targets (this CTA's slice); wpc % 4 == 0
+  uint32_t* sel = bm + wpc;        // [wpc] selected negatives
+  uint32_t* eqb = sel + wpc;       // [wpc] final-digit ties
+  uint32_t* wpre = eqb + wpc;      // [wpc] targets in all words before this one
+  uint32_t* hist = wpre + wpc;     // [kBins] this CTA's histogram
+  uint32_t* hsl = hist + kBins;    // [kBins / 8] cluster totals of this CTA's slice of bins
+  uint64_t* tie = reinterpret_cast<uint64_t*>(hsl + kBins / kClusterCtas);  // [kTieCap]
+  uint32_t* local = reinterpret_cast<uint32_t*>(tie + kTieSlots);  // [nWp]
+  uint32_t* fwpre = local + nWp;   // [nWp] word prefixes of the whole vocabulary (for slots)
 
-  for (int w = tid; w < nW; w += kCandThreads) bm[w] = 0u;
-  if (tid == 0) s_err = 0;
-  __syncthreads();
-
-  // 1. mark
-  for (int t = tid; t < T; t += kCandThreads) {
-    const int v = __ldg(targets + t);
-    if (static_cast<unsigned>(v) >= static_cast<unsigned>(V)) {
-      s_err = 1;
-    } else {
-      const uint32_t bit = 1u << (v & 31);
-      if (!(bm[v >> 5] & bit)) atomicOr(&bm[v >> 5], bit);
-    }
+  const int w0 = r * wpc;
+  const int nw = max(0, min(wpc, nW - w0));  // words owned by this CTA
+  if (r == 0 && tid == 0) hdr[0] = 0;        // a new batch: clear the status word
+  for (int i = tid; i < wpc; i += kCandThreads) sel[i] = eqb[i] = 0u;
+  for (int i = tid; i < nWp; i += kCandThreads) local[i] = 0u;
+  if (tid == 0) {
+    sh.err = 0;
+    sh.ntie = 0;
   }
   __syncthreads();
-  if (s_err) {
-    if (tid == 0) {
+
+  // 1. mark this CTA's share of the targets in a CTA-local bitmap of the whole
+  //    vocabulary (shared-memory atomics, skipped when the bit is already set)
+  for (int t = r * kCandThreads + tid; t < T; t += kClusterCtas * kCandThreads) {
+    const int v = __ldg(targets + t);
+    if (static_cast<unsigned>(v) >= static_cast<unsigned>(V)) {
+      sh.err = 1;
+      continue;
+    }
+    const uint32_t bit = 1u << (v & 31);
+    if (!(local[v >> 5] & bit)) atomicOr(&local[v >> 5], bit);
+  }
+  cluster.sync();  // S1: local bitmaps complete
+  // this CTA's slice of the union bitmap = OR of the eight local bitmaps
+  for (int i = 4 * tid; i < wpc; i += 4 * kCandThreads) {
+    uint4 o = make_uint4(0u, 0u, 0u, 0u);
+    if (w0 + i < nWp) {
+#pragma unroll
+      for (int q = 0; q < kClusterCtas; ++q) {
+        const uint4 x = *reinterpret_cast<const uint4*>(cluster.map_shared_rank(local, q) + w0 + i);
+        o.x |= x.x;
+        o.y |= x.y;
+        o.z |= x.z;
+        o.w |= x.w;
+      }
+    }
+    *reinterpret_cast<uint4*>(bm + i) = o;
+  }
+  if (tid == 0) {
+    int err = 0;
+    for (int q = 0; q < kClusterCtas; ++q) err |= cluster.map_shared_rank(&sh, q)->err;
+    sh.any_err = static_cast<uint32_t>(err);
+  }
+  __syncthreads();
+  if (sh.any_err) {
+    if (r == 0 && tid == 0) {
       set_status(hdr, SS_ERR_TARGET_RANGE);
       hdr[1] = -1;
     }
+    cluster.sync();  // no CTA exits while a peer may still read its shared memory
     return;
   }
 
-  // 2. U and word prefixes; each thread owns a contiguous range of words
-  const int wpt = (nW + kCandThreads - 1) / kCandThreads;
-  const int w0 = min(tid * wpt, nW), w1 = min(w0 + wpt, nW);
-  const int v0 = w0 * 32, v1 = min(w1 * 32, V);
-  uint32_t cnt = 0;
-  for (int w = w0; w < w1; ++w) cnt += __popc(bm[w]);
-  uint32_t U;
-  const uint32_t tbase = block_exclusive_scan(cnt, warp_sums, &U);
+  // 2. per-CTA target count (contiguous word chunk per thread) and the
+  //    first-digit histogram of the non-targets' hashes; one cluster barrier
+  const int wpt = (wpc + kCandThreads - 1) / kCandThreads;
+  const int c0 = min(tid * wpt, nw), c1 = min(c0 + wpt, nw);
+  uint32_t tcnt = 0;
+  for (int i = c0; i < c1; ++i) tcnt += __popc(bm[i]);
+  uint32_t U_r;
+  const uint32_t t_excl = block_scan(tcnt, sh.scan, &U_r);
+  if (tid == 0) sh.U_r = U_r;
+  for (int i = tid; i < kBins; i += kCandThreads) hist[i] = 0u;
+  __syncthreads();
+  for (int i = warp; i < nw; i += kWarps) {
+    const int v = (w0 + i) * 32 + lane;
+    if (v < V && !((bm[i] >> lane) & 1u))
+      atomicAdd(&hist[negative_hash(seed, static_cast<uint32_t>(v)) >> 20], 1u);
+  }
+  cluster.sync();  // S2: target counts and histograms complete
+  if (tid == 0) {
+    uint32_t U = 0, Uoff = 0;
+    for (int q = 0; q < kClusterCtas; ++q) {
+      const uint32_t u = cluster.map_shared_rank(&sh, q)->U_r;
+      U += u;
+      if (q < r) Uoff += u;
+    }
+    sh.U = U;
+    sh.Uoff = Uoff;
+  }
+  __syncthreads();
+  const uint32_t U = sh.U, Uoff = sh.Uoff;
   {
-    uint32_t run = tbase;
-    for (int w = w0; w < w1; ++w) {
-      wpre[w] = run;
-      run += __popc(bm[w]);
+    uint32_t run = Uoff + t_excl;
+    for (int i = c0; i < c1; ++i) {
+      wpre[i] = run;
+      run += __popc(bm[i]);
     }
   }
   if (static_cast<int>(U) > C) {
-    if (tid == 0) {
+    if (r == 0 && tid == 0) {
       set_status(hdr, SS_ERR_CAPACITY);
       hdr[1] = static_cast<int>(U);
     }
+    cluster.sync();
     return;
   }
   const uint32_t k = static_cast<uint32_t>(C) - U;
+  const uint32_t n_non = static_cast<uint32_t>(V) - U;
 
-  // 3. radix-select the k-th smallest hash among non-targets
-  uint32_t prefix = 0, pmask = 0, rem = k;
-  if (k > 0) {
-#pragma unroll 1
-    for (int pass = 0; pass < 4; ++pass) {
-      const int shift = 24 - 8 * pass;
-      if (tid < 256) hist[tid] = 0u;
-      __syncthreads();
-      for (int v = v0; v < v1; ++v) {
-        if (bm[v >> 5] & (1u << (v & 31))) continue;
-        const uint32_t h = negative_hash(seed, static_cast<uint32_t>(v));
-        if ((h & pmask) == prefix) atomicAdd(&hist[(h >> shift) & 255u], 1u);
+  // 3. select the k non-targets with the smallest keys
+  if (k == n_non) {
+    for (int i = tid; i < nw; i += kCandThreads) {
+      const int vbase = (w0 + i) * 32;
+      const uint32_t valid = (V - vbase >= 32) ? 0xffffffffu : ((1u << (V - vbase)) - 1u);
+      sel[i] = ~bm[i] & valid;
+    }
+  } else if (k > 0) {
+    uint32_t prefix = 0, mask = 0, rem = k;
+    int level = 0;
+    for (;; ++level) {
+      const int shift = level == 0 ? 20 : (level == 1 ? 8 : 0);
+      const int nb = level == 2 ? 256 : kBins;
+      const bool last = level == 2;
+      if (level > 0) {  // level 0's histogram was built before the U exchange
+        for (int i = tid; i < nb; i += kCandThreads) hist[i] = 0u;
+        __syncthreads();
+        for (int i = warp; i < nw; i += kWarps) {
+          const int v = (w0 + i) * 32 + lane;
+          if (v < V && !((bm[i] >> lane) & 1u)) {
+            const uint32_t h = negative_hash(seed, static_cast<uint32_t>(v));
+            if ((h & mask) == prefix) atomicAdd(&hist[(h >> shift) & (nb - 1)], 1u);
+          }
+        }
+        cluster.sync();
       }
-      __syncthreads();
+      // reduce-scatter: CTA r sums bins [r*nb/8, (r+1)*nb/8) over the cluster
+      const int sl = nb / kClusterCtas;  // 512 or 32 bins, a multiple of 4
+      uint32_t part = 0;
+      if (4 * tid < sl) {
+        uint4 s4 = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+        for (int q = 0; q < kClusterCtas; ++q) {
+          const uint4 x =
+              *reinterpret_cast<const uint4*>(cluster.map_shared_rank(hist, q) + r * sl + 4 * tid);
+          s4.x += x.x;
+          s4.y += x.y;
+          s4.z += x.z;
+          s4.w += x.w;
+        }
+        *reinterpret_cast<uint4*>(hsl + 4 * tid) = s4;
+        part = s4.x + s4.y + s4.z + s4.w;
+      }
+      uint32_t ssum;
+      (void)block_scan(part, sh.scan, &ssum);
+      if (tid == 0) sh.slice_sum = ssum;
+      cluster.sync();  // slice totals complete (and peers are done with our histogram)
+      // every CTA: which slice holds rank rem, then which bin inside it
       if (tid == 0) {
-        uint32_t cum = 0, digit = 255;
-        for (int d = 0; d < 256; ++d) {
-          if (cum + hist[d] >= rem) {
-            digit = static_cast<uint32_t>(d);
+        uint32_t cum = 0, s = kClusterCtas - 1;
+        for (int q = 0; q < kClusterCtas; ++q) {
+          const uint32_t x = cluster.map_shared_rank(&sh, q)->slice_sum;
+          if (rem <= cum + x) {
+            s = static_cast<uint32_t>(q);
             break;
           }
-          cum += hist[d];
+          cum += x;
         }
-        s_digit = digit;
-        s_rem = rem - cum;
+        sh.s_slice = s;
+        sh.s_rem = rem - cum;
       }
       __syncthreads();
-      prefix |= s_digit << shift;
-      pmask |= 255u << shift;
-      rem = s_rem;
+      const uint32_t s = sh.s_slice, srem = sh.s_rem;
+      uint32_t b4[4] = {0u, 0u, 0u, 0u};
+      uint32_t psum = 0;
+      if (4 * tid < sl) {
+        const uint4 x = *reinterpret_cast<const uint4*>(cluster.map_shared_rank(hsl, s) + 4 * tid);
+        b4[0] = x.x;
+        b4[1] = x.y;
+        b4[2] = x.z;
+        b4[3] = x.w;
+        psum = x.x + x.y + x.z + x.w;
+      }
+      uint32_t tot;
+      const uint32_t before = block_scan(psum, sh.scan, &tot);
+      if (4 * tid < sl && before < srem && srem <= before + psum) {
+        uint32_t cum = before;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          if (srem <= cum + b4[j]) {
+            sh.b = s * sl + static_cast<uint32_t>(4 * tid + j);
+            sh.rem = srem - cum;
+            sh.cnt = b4[j];
+            break;
+          }
+          cum += b4[j];
+        }
+      }
+      __syncthreads();
+      const uint32_t b = sh.b, cnt = sh.cnt;
+      const bool collect = last || cnt <= static_cast<uint32_t>(kTieCap);
+      // another level rebuilds the histograms: peers must be done reading hsl
+      if (!collect) cluster.sync();
+      for (int i = warp; i < nw; i += kWarps) {
+        const int v = (w0 + i) * 32 + lane;
+        bool below = false, in_bin = false;
+        uint32_t h = 0;
+        if (v < V && !((bm[i] >> lane) & 1u)) {
+          h = negative_hash(seed, static_cast<uint32_t>(v));
+          if ((h & mask) == prefix) {
+            const uint32_t d = (h >> shift) & static_cast<uint32_t>(nb - 1);
+            below = d < b;
+            in_bin = d == b;
+          }
+        }
+        const uint32_t bw = __ballot_sync(0xffffffffu, below);
+        if (lane == 0 && bw) sel[i] |= bw;
+        if (collect) {
+          if (last) {
+            const uint32_t ew = __ballot_sync(0xffffffffu, in_bin);
+            if (lane == 0) eqb[i] = ew;
+          } else if (in_bin) {
+            const uint32_t at = atomicAdd(&sh.ntie, 1u);
+            tie[at] = (static_cast<uint64_t>(h) << 32) | static_cast<uint32_t>(v);
+          }
+        }
+      }
+      prefix |= b << shift;
+      mask |= static_cast<uint32_t>(nb - 1) << shift;
+      rem = sh.rem;
+      if (collect) break;
     }
-  }
-  // Selected negatives: hash < prefix, plus the first `rem` ids (ascending)
-  // whose hash == prefix.
-
-  // 4. compaction
-  uint32_t nlt = 0, neq = 0;
-  if (k > 0) {
-    for (int v = v0; v < v1; ++v) {
-      if (bm[v >> 5] & (1u << (v & 31))) continue;
-      const uint32_t h = negative_hash(seed, static_cast<uint32_t>(v));
-      nlt += (h < prefix);
-      neq += (h == prefix);
-    }
-  }
-  uint32_t eq_total, sel_total;
-  const uint32_t eq_base = block_exclusive_scan(neq, warp_sums, &eq_total);
-  const uint32_t take_eq = rem > eq_base ? min(rem - eq_base, neq) : 0u;
-  const uint32_t sel_base = block_exclusive_scan(nlt + take_eq, warp_sums, &sel_total);
-  {
-    uint32_t ti = tbase, ni = U + sel_base, ei = eq_base;
-    for (int v = v0; v < v1; ++v) {
-      if (bm[v >> 5] & (1u << (v & 31))) {
-        cand[ti++] = v;
-      } else if (k > 0) {
-        const uint32_t h = negative_hash(seed, static_cast<uint32_t>(v));
-        if (h < prefix) {
-          cand[ni++] = v;
-        } else if (h == prefix) {
-          if (ei < rem) cand[ni++] = v;
-          ++ei;
+    if (level < 2) {
+      // the selected bin is small: rank its ids exactly by (hash, id)
+      cluster.sync();
+      const uint32_t mine = sh.ntie;
+      for (uint32_t i = tid; i < mine; i += kCandThreads) {
+        const uint64_t key = tie[i];
+        uint32_t rank = 0;
+        for (int q = 0; q < kClusterCtas; ++q) {
+          const Shared* ps = cluster.map_shared_rank(&sh, q);
+          const uint64_t* pt = cluster.map_shared_rank(tie, q);
+          const uint32_t n = ps->ntie;
+          for (uint32_t j = 0; j < n; ++j) rank += pt[j] < key;
+        }
+        if (rank < rem) {
+          const int v = static_cast<int>(key & 0xffffffffu);
+          atomicOr(&sel[(v >> 5) - w0], 1u << (v & 31));
+        }
+      }
+    } else {
+      // all 32 hash bits equal: take the first `rem` of them in id order
+      uint32_t ecnt = 0;
+      for (int i = c0; i < c1; ++i) ecnt += __popc(eqb[i]);
+      uint32_t E_r;
+      const uint32_t e_excl = block_scan(ecnt, sh.scan, &E_r);
+      if (tid == 0) sh.E_r = E_r;
+      cluster.sync();
+      if (tid == 0) {
+        uint32_t Eoff = 0;
+        for (int q = 0; q < r; ++q) Eoff += cluster.map_shared_rank(&sh, q)->E_r;
+        sh.Eoff = Eoff;
+      }
+      __syncthreads();
+      uint32_t e = sh.Eoff + e_excl;
+      for (int i = c0; i < c1; ++i) {
+        uint32_t bits = eqb[i];
+        while (bits) {
+          const int j = __ffs(bits) - 1;
+          bits &= bits - 1;
+          if (e < rem) sel[i] |= 1u << j;
+          ++e;
         }
       }
     }
   }
-  __syncthreads();  // wpre complete
+  __syncthreads();
 
-  // 5. slots
-  for (int t = tid; t < T; t += kCandThreads) {
+  // 4. compaction: targets into [0, U), selected negatives into [U, C)
+  uint32_t scnt = 0;
+  for (int i = c0; i < c1; ++i) scnt += __popc(sel[i]);
+  uint32_t S_r;
+  const uint32_t s_excl = block_scan(scnt, sh.scan, &S_r);
+  if (tid == 0) sh.S_r = S_r;
+  cluster.sync();  // S_r and every slice's word prefixes complete
+  if (tid == 0) {
+    uint32_t Soff = 0;
+    for (int q = 0; q < r; ++q) Soff += cluster.map_shared_rank(&sh, q)->S_r;
+    sh.Soff = Soff;
+  }
+  // replicate the whole vocabulary's bitmap and word prefixes for the slots
+  // (`local` is free: peers finished reading it before the second barrier)
+  for (int i = 4 * tid; i < nWp; i += 4 * kCandThreads) {
+    const int q = i / wpc;
+    const int li = i - q * wpc;
+    *reinterpret_cast<uint4*>(local + i) =
+        *reinterpret_cast<const uint4*>(cluster.map_shared_rank(bm, q) + li);
+    *reinterpret_cast<uint4*>(fwpre + i) =
+        *reinterpret_cast<const uint4*>(cluster.map_shared_rank(wpre, q) + li);
+  }
+  __syncthreads();
+  {
+    uint32_t ti = Uoff + t_excl, si = U + sh.Soff + s_excl;
+    for (int i = c0; i < c1; ++i) {
+      const int vbase = (w0 + i) * 32;
+      uint32_t tb = bm[i], sb = sel[i];
+      while (tb) {
+        cand[ti++] = vbase + __ffs(tb) - 1;
+        tb &= tb - 1;
+      }
+      while (sb) {
+        cand[si++] = vbase + __ffs(sb) - 1;
+        sb &= sb - 1;
+      }
+    }
+  }
+
+  // 5. slots from the local copies
+  for (int t = r * kCandThreads + tid; t < T; t += kClusterCtas * kCandThreads) {
     const int v = __ldg(targets + t);
     const int w = v >> 5;
-    slot[t] = static_cast<int32_t>(wpre[w] + __popc(bm[w] & ((1u << (v & 31)) - 1u)));
+    slot[t] = static_cast<int32_t>(fwpre[w] + __popc(local[w] & ((1u << (v & 31)) - 1u)));
   }
-  if (tid == 0) hdr[1] = static_cast<int>(U);
+  if (r == 0 && tid == 0) hdr[1] = static_cast<int>(U);
+  cluster.sync();  // keep every CTA's shared memory alive until all peers are done
+}
+
+// words of the bitmap per CTA, a multiple of 4 (whole uint4 vectors)
+int words_per_cta(int64_t V) {
+  const int64_t nW = (V + 31) / 32;
+  const int64_t w = (nW + kClusterCtas - 1) / kClusterCtas;
+  return static_cast<int>((w + 3) / 4 * 4);
 }
 
 }  // namespace
 
 size_t build_candidates_smem_bytes(int64_t V) {
-  return static_cast<size_t>((V + 31) / 32) * 2 * sizeof(uint32_t);
+  const size_t nWp = static_cast<size_t>(((V + 31) / 32 + 3) / 4 * 4);
+  return static_cast<size_t>(words_per_cta(V)) * 4 * sizeof(uint32_t) +
+         (kBins + kBins / kClusterCtas) * sizeof(uint32_t) +
+         kTieSlots * sizeof(uint64_t) + 2 * nWp * sizeof(uint32_t);
 }
 
 cudaError_t launch_build_candidates(const int32_t* targets, int T, int V, int C, uint64_t seed,
@@ -223,7 +468,8 @@ cudaError_t launch_build_candidates(const int32_t* targets, int T, int V, int C,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  k_build_candidates<<<1, kCandThreads, smem, stream>>>(targets, T, V, C, seed, cand, slot, hdr);
+  k_build_candidates<<<kClusterCtas, kCandThreads, smem, stream>>>(targets, T, V, C, seed, cand,
+                                                                    slot, hdr, words_per_cta(V));
   return cudaGetLastError();
 }
 

@@ -33,14 +33,24 @@ constexpr int UMMA_K = 16;       // K of one tcgen05.mma kind::f16
 constexpr int GEMM_THREADS = 192;
 constexpr float kLog2e = 1.4426950408889634f;
 
-template <int BN, int STAGES>
+template <int BN, int STAGES, int EPI_BYTES>
 struct GemmSmem {
   static constexpr int A_BYTES = BM * BK * 2;
   static constexpr int B_BYTES = BN * BK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int TILES_BYTES = STAGES * STAGE_BYTES;
+  static constexpr int EPI_OFFSET = TILES_BYTES;              // epilogue staging (1024-aligned)
+  static constexpr int CTRL_OFFSET = TILES_BYTES + EPI_BYTES;
   static constexpr int CTRL_BYTES = 256;
-  static constexpr int TOTAL = TILES_BYTES + CTRL_BYTES + 1024;  // + 1024-byte alignment slack
+  static constexpr int TOTAL = CTRL_OFFSET + CTRL_BYTES + 1024;  // + 1024-byte alignment slack
+  static_assert(TOTAL <= 232448, "shared memory per CTA");
+};
+
+// Per-thread state the epilogue keeps across tiles.
+struct EpiState {
+  uint32_t stage;   // shared address of the epilogue staging region
+  int ep_tid;       // 0..127 among the epilogue threads
+  uint32_t rounds;  // staging buffers used so far
 };
 
 struct GemmCtrl {
@@ -51,6 +61,7 @@ struct GemmCtrl {
   uint64_t drain;
   uint32_t tmem_base;
   int abort_flag;
+  int vote[2][4];  // per-tile vote of the epilogue warps (alternating halves)
 };
 
 // Units are (m_tile, n_tile) pairs numbered m-major: u = m_tile * n_tiles + n_tile.
@@ -66,6 +77,7 @@ struct GemmShape {
 //   part[n_tile][t] = (max_j S[t,j], sum_j exp(S[t,j] - max)) over the tile's
 //   valid columns; tgt[t] = S[t, slot[t]] from the tile that holds slot[t].
 struct EpiFwd {
+  static constexpr int kStageBytes = 0;
   struct Params {
     int T, C;
     const int32_t* slot;
@@ -73,8 +85,10 @@ struct EpiFwd {
     float* tgt;
     int* status;
   };
+  __device__ static void finish(const Params&, EpiState&) {}
   template <int BN>
-  __device__ static void apply(const Params& p, int mt, int nt, int row, uint32_t taddr) {
+  __device__ static void apply(const Params& p, int mt, int nt, int row, uint32_t taddr,
+                               EpiState&) {
     const int t = mt * BM + row;
     const bool valid = t < p.T;
     const int sl = valid ? __ldg(p.slot + t) : -1;
@@ -122,63 +136,106 @@ struct EpiFwd {
 };
 
 // Backward, step 1: G[t, j] = scale * (exp(S[t,j] - lse[t]) - [j == slot[t]]), bf16.
+// Folded form: scale * exp(x - lse) = sign(scale) * 2^(x*log2e - (lse*log2e - log2|scale|)).
+// Each 64-column quarter of the tile is written into a 16 KB shared-memory
+// buffer in the 128-byte-swizzled layout of the G tensor map (two buffers,
+// alternating) and stored with one TMA bulk tensor store, so the global
+// writes leave as full lines instead of 32 rows per warp instruction. The
+// one-hot term touches one element per row: it is recomputed in fp32 and
+// patched into the staged tile.
 struct EpiG {
-  struct Params {
-    int T, C, ldG;
+  static constexpr int kStageBytes = 2 * 16384;
+  struct alignas(64) Params {
+    CUtensorMap tmG;  // G [T, C] bf16 (row pitch ldG), box 64 x 128, 128-byte swizzle
+    int T, C;
     const int32_t* slot;
     const float* lse;
-    float scale;
-    uint16_t* G;
+    float scale;       // d(objective)/d(loss)
+    float log2_scale;  // log2|scale| (-inf for 0)
     int* status;
   };
+  __device__ static void finish(const Params&, EpiState& es) {
+    if (es.ep_tid == 0) bulk_wait<0>();
+  }
   template <int BN>
-  __device__ static void apply(const Params& p, int mt, int nt, int row, uint32_t taddr) {
+  __device__ static void apply(const Params& p, int mt, int nt, int row, uint32_t taddr,
+                               EpiState& es) {
     const int t = mt * BM + row;
     const bool valid = t < p.T;
     const int sl = valid ? __ldg(p.slot + t) : -1;
     if (valid && nt == 0 && static_cast<unsigned>(sl) >= static_cast<unsigned>(p.C))
       set_status(p.status, SS_ERR_INDEX);
-    const float l2 = valid ? __ldg(p.lse + t) * kLog2e : 0.f;
-    const float sc = p.scale;
+    const float asc = fabsf(p.scale);
+    const uint32_t sgn = p.scale < 0.f ? 0x80008000u : 0u;
+    const float off2 = valid ? fmaf(__ldg(p.lse + t), kLog2e, -p.log2_scale) : 0.f;
     const int j0 = nt * BN;
     const int ncols = min(BN, p.C - j0);
-    uint16_t* grow = p.G + static_cast<size_t>(valid ? t : 0) * p.ldG + j0;
+    const uint32_t r7 = static_cast<uint32_t>(row & 7);
 #pragma unroll 1
-    for (int c = 0; c < BN / 32; ++c) {
-      const int jc = c * 32;
-      if (jc >= ncols) break;
-      uint32_t r[32];
-      tmem_ld32(taddr + jc, r);
-      tmem_ld_wait();
-      const int off = sl - j0 - jc;
-      uint32_t pk[16];
+    for (int q = 0; q < BN / 64; ++q) {
+      const int qc = q * 64;
+      if (qc >= ncols) break;  // uniform: depends on the tile only
+      const uint32_t buf = es.stage + (es.rounds & 1u) * 16384u;
+      // the store that used this buffer two rounds ago must have read it
+      if (es.rounds >= 2 && es.ep_tid == 0) bulk_wait_read<1>();
+      named_bar_sync(1, 128);
+      const uint32_t rowbase = buf + static_cast<uint32_t>(row) * 128u;
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        float g0 = ex2_approx(fmaf(__uint_as_float(r[2 * i]), kLog2e, -l2));
-        float g1 = ex2_approx(fmaf(__uint_as_float(r[2 * i + 1]), kLog2e, -l2));
-        if (off == 2 * i) g0 -= 1.f;
-        if (off == 2 * i + 1) g1 -= 1.f;
-        pk[i] = pack_bf16x2(sc * g0, sc * g1);
-      }
-      if (valid) {
-        uint4* dst = reinterpret_cast<uint4*>(grow + jc);
+      for (int h = 0; h < 2; ++h) {
+        const int jc = qc + 32 * h;
+        if (jc >= ncols) break;
+        uint32_t r[32];
+        tmem_ld32(taddr + jc, r);
+        tmem_ld_wait();
+        uint32_t pk[16];
 #pragma unroll
-        for (int v = 0; v < 4; ++v)
-          if (jc + 8 * v < ncols)
-            dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+        for (int i = 0; i < 16; ++i) {
+          const float g0 = ex2_approx(fmaf(__uint_as_float(r[2 * i]), kLog2e, -off2));
+          const float g1 = ex2_approx(fmaf(__uint_as_float(r[2 * i + 1]), kLog2e, -off2));
+          pk[i] = pack_bf16x2(g0, g1) ^ sgn;
+        }
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+          const uint32_t ci = static_cast<uint32_t>(h * 4 + v);
+          st_shared_v4(rowbase + ((ci ^ r7) << 4), pk[4 * v], pk[4 * v + 1], pk[4 * v + 2],
+                       pk[4 * v + 3]);
+        }
+        const int off = sl - j0 - jc;
+        const bool has = static_cast<unsigned>(off) < 32u;
+        if (__any_sync(0xffffffffu, has)) {
+          float xt = 0.f;
+#pragma unroll
+          for (int i = 0; i < 32; ++i) xt = (i == off) ? __uint_as_float(r[i]) : xt;
+          if (has) {
+            const float gt = ex2_approx(fmaf(xt, kLog2e, -off2)) - asc;
+            const uint16_t bits = bf16_bits(gt) ^ static_cast<uint16_t>(sgn & 0xffffu);
+            const uint32_t cc = static_cast<uint32_t>(32 * h + off);
+            st_shared_b16(rowbase + (((cc >> 3) ^ r7) << 4) + (cc & 7u) * 2u, bits);
+          }
+        }
       }
+      fence_proxy_async_smem();
+      named_bar_sync(1, 128);
+      if (es.ep_tid == 0) {
+        tma_store_2d(&p.tmG, buf, j0 + qc, mt * BM);
+        bulk_commit();
+      }
+      ++es.rounds;
     }
   }
 };
 
 // Backward, step 2: dH tile -> bf16.
 struct EpiDh {
+  static constexpr int kStageBytes = 0;
   struct Params {
     int T, D;
     uint16_t* dH;
   };
+  __device__ static void finish(const Params&, EpiState&) {}
   template <int BN>
-  __device__ static void apply(const Params& p, int mt, int nt, int row, uint32_t taddr) {
+  __device__ static void apply(const Params& p, int mt, int nt, int row, uint32_t taddr,
+                               EpiState&) {
     const int t = mt * BM + row;
     const bool valid = t < p.T;
     const int n0 = nt * BN;
@@ -209,14 +266,17 @@ struct EpiDh {
 // Backward, step 3: dW_c tile scattered into the owning rows dW[cand[j]]
 // (= or +=). Candidate ids are distinct, so no two threads write one row.
 struct EpiDw {
+  static constexpr int kStageBytes = 0;
   struct Params {
     int C, D, V, accumulate;
     const int32_t* cand;
     float* dW;
     int* status;
   };
+  __device__ static void finish(const Params&, EpiState&) {}
   template <int BN>
-  __device__ static void apply(const Params& p, int mt, int nt, int row, uint32_t taddr) {
+  __device__ static void apply(const Params& p, int mt, int nt, int row, uint32_t taddr,
+                               EpiState&) {
     const int j = mt * BM + row;
     bool valid = j < p.C;
     const int v = valid ? __ldg(p.cand + j) : 0;
@@ -259,16 +319,16 @@ struct EpiDw {
 template <int BN, int STAGES, bool A_MN, bool B_MN, class Epi>
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
     k_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-           GemmShape shp, typename Epi::Params ep, int* status) {
+           GemmShape shp, const __grid_constant__ typename Epi::Params ep, int* status) {
   static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "BN");
   static_assert(STAGES >= 2 && STAGES <= 8, "STAGES");
-  using L = GemmSmem<BN, STAGES>;
+  using L = GemmSmem<BN, STAGES, Epi::kStageBytes>;
   extern __shared__ uint8_t smem_raw[];
   __shared__ int s_go;
 
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
-  GemmCtrl* ctrl = reinterpret_cast<GemmCtrl*>(smem + L::TILES_BYTES);
+  GemmCtrl* ctrl = reinterpret_cast<GemmCtrl*>(smem + L::CTRL_OFFSET);
   const uint32_t tiles = smem_u32(smem);
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
@@ -398,14 +458,24 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     const int q = warp & 3;
     const int row = q * 32 + lane;
     const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+    EpiState es{tiles + L::EPI_OFFSET, static_cast<int>(threadIdx.x) - 64, 0u};
     int b = 0;
     uint32_t aph = 0;
     for (int u = blockIdx.x; u < num_units; u += gridDim.x) {
       const bool ok = mbar_wait(&ctrl->tfull[b], aph, abort_flag, status);
-      if (!__all_sync(0xffffffffu, ok)) break;
+      bool go = __all_sync(0xffffffffu, ok);
+      if constexpr (Epi::kStageBytes > 0) {
+        // This epilogue synchronises its four warps with named barriers, so
+        // they must leave the loop together: vote every tile.
+        if (lane == 0) ctrl->vote[(u / gridDim.x) & 1][q] = go ? 1 : 0;
+        named_bar_sync(2, 128);
+        const int* v = ctrl->vote[(u / gridDim.x) & 1];
+        go = (v[0] & v[1] & v[2] & v[3]) != 0;
+      }
+      if (!go) break;
       tc_fence_after();
       const int mt = u / shp.n_tiles, nt = u % shp.n_tiles;
-      Epi::template apply<BN>(ep, mt, nt, row, lane_addr + static_cast<uint32_t>(b * BN));
+      Epi::template apply<BN>(ep, mt, nt, row, lane_addr + static_cast<uint32_t>(b * BN), es);
       tc_fence_before();
       mbar_arrive(&ctrl->tempty[b]);
       if (++b == 2) {
@@ -413,6 +483,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         aph ^= 1u;
       }
     }
+    Epi::finish(ep, es);  // outstanding stores from shared memory complete before exit
   }
   __syncthreads();
   if (warp == 1) {
@@ -427,7 +498,7 @@ cudaError_t launch_gemm(const CUtensorMap& tA, const CUtensorMap& tB, GemmShape 
                         const typename Epi::Params& ep, int* status, int num_sms,
                         cudaStream_t stream) {
   auto kern = k_gemm<BN, STAGES, A_MN, B_MN, Epi>;
-  constexpr int smem = GemmSmem<BN, STAGES>::TOTAL;
+  constexpr int smem = GemmSmem<BN, STAGES, Epi::kStageBytes>::TOTAL;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const int units = shp.m_tiles * shp.n_tiles;

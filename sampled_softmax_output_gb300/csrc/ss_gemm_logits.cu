@@ -17,12 +17,20 @@ cudaError_t launch_forward_logits(const CUtensorMap& tH, const CUtensorMap& tWc,
                                                                      num_sms, stream);
 }
 
-cudaError_t launch_softmax_grad(const CUtensorMap& tH, const CUtensorMap& tWc, int T, int C,
-                                int D, int ldG, const int32_t* slot, const float* lse,
-                                float scale, uint16_t* G, int* status, int num_sms,
-                                cudaStream_t stream) {
+cudaError_t launch_softmax_grad(const CUtensorMap& tH, const CUtensorMap& tWc,
+                                const CUtensorMap& tG_store, int T, int C, int D,
+                                const int32_t* slot, const float* lse, float scale,
+                                int* status, int num_sms, cudaStream_t stream) {
   GemmShape shp{(T + BM - 1) / BM, (C + kBnLogits - 1) / kBnLogits, D / BK};
-  EpiG::Params ep{T, C, ldG, slot, lse, scale, G, status};
+  EpiG::Params ep;
+  ep.tmG = tG_store;
+  ep.T = T;
+  ep.C = C;
+  ep.slot = slot;
+  ep.lse = lse;
+  ep.scale = scale;
+  ep.log2_scale = scale == 0.f ? -INFINITY : log2f(fabsf(scale));
+  ep.status = status;
   return launch_gemm<kBnLogits, kStagesLogits, false, false, EpiG>(tH, tWc, shp, ep, status,
                                                                    num_sms, stream);
 }

@@ -23,18 +23,22 @@ cudaError_t launch_build_candidates(const int32_t* targets, int T, int V, int C,
 cudaError_t launch_forward_logits(const CUtensorMap& tH, const CUtensorMap& tWc, int T, int C,
                                   int D, const int32_t* slot, float2* part, float* tgt,
                                   int* status, int num_sms, cudaStream_t stream);
-cudaError_t launch_softmax_grad(const CUtensorMap& tH, const CUtensorMap& tWc, int T, int C,
-                                int D, int ldG, const int32_t* slot, const float* lse,
-                                float scale, uint16_t* G, int* status, int num_sms,
-                                cudaStream_t stream);
+// G is written through tG_store: G [T, C] bf16, box 64 x 128, 128-byte swizzle.
+cudaError_t launch_softmax_grad(const CUtensorMap& tH, const CUtensorMap& tWc,
+                                const CUtensorMap& tG_store, int T, int C, int D,
+                                const int32_t* slot, const float* lse, float scale,
+                                int* status, int num_sms, cudaStream_t stream);
 
-// ---- gradient GEMMs (ss_gemm_grads.cu)
-// dH = G . W_c : A = G [T, C] (K-major), B = W_c [C, D] (MN-major)
-cudaError_t launch_grad_h(const CUtensorMap& tG_kmaj, const CUtensorMap& tWc_mn, int T, int C,
-                          int D, uint16_t* dH, int* status, int num_sms, cudaStream_t stream);
-// dW[cand] (=|+=) G^T . H : A = G (MN-major), B = H [T, D] (MN-major)
-cudaError_t launch_grad_w(const CUtensorMap& tG_mn, const CUtensorMap& tH_mn, int T, int C, int D,
-                          int V, int accumulate, const int32_t* cand, float* dW, int* status,
-                          int num_sms, cudaStream_t stream);
+// ---- gradient GEMMs (ss_gemm_grads.cu), one stream-K kernel:
+// dH = G . W_c          : A = G [T, C] (K-major),  B = W_c [C, D] (MN-major)
+// dW[cand] (=|+=) G^T.H : A = G (MN-major),        B = H [T, D] (MN-major)
+constexpr int kMaxGradCtas = 256;  // workspace is sized for this many CTAs
+size_t grad_partial_bytes();       // fp32 partial tiles, one per CTA
+size_t grad_flag_bytes();          // hand-off flags, four per CTA
+cudaError_t launch_grads(const CUtensorMap& tG_kmaj, const CUtensorMap& tWc_mn,
+                         const CUtensorMap& tG_mn, const CUtensorMap& tH_mn, int T, int C, int D,
+                         int V, int accumulate, const int32_t* cand, uint16_t* dH, float* dW,
+                         float* partial, int* flags, int* status, int num_sms,
+                         cudaStream_t stream);
 
 }  // namespace ss
