@@ -23,7 +23,7 @@ namespace {
 // ------------------------------------------------------------ workspace
 
 struct Layout {
-  size_t hdr, wc, part, tgt, g, gpart, gflags, total;
+  size_t hdr, wc, part, tgt, g, total;
   int64_t ldG, n_ct;
 };
 
@@ -46,10 +46,6 @@ Layout make_layout(int64_t T, int64_t C, int64_t D) {
   off = align_up(off + static_cast<size_t>(T) * sizeof(float), 1024);
   L.g = off;
   off = align_up(off + static_cast<size_t>(T) * L.ldG * 2, 1024);
-  L.gpart = off;
-  off = align_up(off + grad_partial_bytes(), 1024);
-  L.gflags = off;
-  off = align_up(off + grad_flag_bytes(), 1024);
   L.total = off;
   return L;
 }
@@ -393,12 +389,14 @@ ss_status ss_backward(const uint16_t* H, const uint16_t* W, const int32_t* cand,
   cudaError_t e = launch_softmax_grad(tH, tWc, tGk, iT, iC, iD, slot, lse, scale, status, nsm, s);
   trace_post(s);
   if (e != cudaSuccess) return fail("launch gemm_softmax_grad", e);
-  trace_pre(s, "gemm_grads_streamk");
-  e = launch_grads(tGk, tWcMn, tGmn, tHmn, iT, iC, iD, iV, accumulate, cand, dH, dW,
-                   reinterpret_cast<float*>(ws + L.gpart), reinterpret_cast<int*>(ws + L.gflags),
-                   status, nsm, s);
+  trace_pre(s, "gemm_grad_h");
+  e = launch_grad_h(tGk, tWcMn, iT, iC, iD, dH, status, nsm, s);
   trace_post(s);
-  if (e != cudaSuccess) return fail("launch gemm_grads_streamk", e);
+  if (e != cudaSuccess) return fail("launch gemm_grad_h", e);
+  trace_pre(s, "gemm_grad_w_scatter");
+  e = launch_grad_w(tGmn, tHmn, iT, iC, iD, iV, accumulate, cand, dW, status, nsm, s);
+  trace_post(s);
+  if (e != cudaSuccess) return fail("launch gemm_grad_w_scatter", e);
   return SS_OK;
 }
 

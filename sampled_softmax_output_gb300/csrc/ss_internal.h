@@ -29,16 +29,13 @@ cudaError_t launch_softmax_grad(const CUtensorMap& tH, const CUtensorMap& tWc,
                                 const int32_t* slot, const float* lse, float scale,
                                 int* status, int num_sms, cudaStream_t stream);
 
-// ---- gradient GEMMs (ss_gemm_grads.cu), one stream-K kernel:
-// dH = G . W_c          : A = G [T, C] (K-major),  B = W_c [C, D] (MN-major)
-// dW[cand] (=|+=) G^T.H : A = G (MN-major),        B = H [T, D] (MN-major)
-constexpr int kMaxGradCtas = 256;  // workspace is sized for this many CTAs
-size_t grad_partial_bytes();       // fp32 partial tiles, one per CTA
-size_t grad_flag_bytes();          // hand-off flags, four per CTA
-cudaError_t launch_grads(const CUtensorMap& tG_kmaj, const CUtensorMap& tWc_mn,
-                         const CUtensorMap& tG_mn, const CUtensorMap& tH_mn, int T, int C, int D,
-                         int V, int accumulate, const int32_t* cand, uint16_t* dH, float* dW,
-                         float* partial, int* flags, int* status, int num_sms,
-                         cudaStream_t stream);
+// ---- gradient GEMMs (ss_gemm_grads.cu)
+// dH = G . W_c : A = G [T, C] (K-major), B = W_c [C, D] (MN-major)
+cudaError_t launch_grad_h(const CUtensorMap& tG_kmaj, const CUtensorMap& tWc_mn, int T, int C,
+                          int D, uint16_t* dH, int* status, int num_sms, cudaStream_t stream);
+// dW[cand] (=|+=) G^T . H : A = G (MN-major), B = H [T, D] (MN-major)
+cudaError_t launch_grad_w(const CUtensorMap& tG_mn, const CUtensorMap& tH_mn, int T, int C, int D,
+                          int V, int accumulate, const int32_t* cand, float* dW, int* status,
+                          int num_sms, cudaStream_t stream);
 
 }  // namespace ss
