@@ -46,8 +46,7 @@ METRIC = "sampled-softmax CE fwd+bwd tokens/s; % of GB300 bf16 tensor peak"
 UNIT = "tokens/s"
 L2_FLUSH_BYTES = 256 << 20
 # algorithmic flops per launch of each GEMM kernel, in units of T*C*D
-GEMM_FLOPS_TCD = {"gemm_forward_lse": 2, "gemm_softmax_grad": 2, "gemm_grad_h": 2,
-                  "gemm_grad_w_scatter": 2}
+GEMM_FLOPS_TCD = {"gemm_forward_lse": 2, "gemm_softmax_grad": 2, "gemm_grads": 4}
 CSRC = os.path.join(ROOT, "sampled_softmax_output_gb300", "csrc")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
 
@@ -87,8 +86,7 @@ def load_peaks():
 KERNEL_SOURCES = {
     "gemm_forward_lse": ["ss_ptx.cuh", "ss_gemm.cuh", "ss_gemm_logits.cu"],
     "gemm_softmax_grad": ["ss_ptx.cuh", "ss_gemm.cuh", "ss_gemm_logits.cu"],
-    "gemm_grad_h": ["ss_ptx.cuh", "ss_gemm.cuh", "ss_gemm_grads.cu"],
-    "gemm_grad_w_scatter": ["ss_ptx.cuh", "ss_gemm.cuh", "ss_gemm_grads.cu"],
+    "gemm_grads": ["ss_ptx.cuh", "ss_gemm.cuh", "ss_gemm_grads.cu"],
     "build_candidates": ["ss_ptx.cuh", "ss_candidates.cu"],
 }
 

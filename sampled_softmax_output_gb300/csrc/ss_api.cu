@@ -142,12 +142,25 @@ __global__ void __launch_bounds__(256) k_lse_merge(const float2* __restrict__ pa
     set_status(status, SS_ERR_INDEX);
     return;
   }
-  float M = -INFINITY;
-  for (int c = 0; c < n_ct; ++c) M = fmaxf(M, part[static_cast<size_t>(c) * T + t].x);
-  float S = 0.f;
-  for (int c = 0; c < n_ct; ++c) {
+  // one pass: online merge of the per-tile (max, sum) pairs, loads batched
+  float M = -INFINITY, S = 0.f;
+  int c = 0;
+  for (; c + 8 <= n_ct; c += 8) {
+    float2 q[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) q[i] = part[static_cast<size_t>(c + i) * T + t];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float nm = fmaxf(M, q[i].x);
+      S = S * expf(M - nm) + q[i].y * expf(q[i].x - nm);
+      M = nm;
+    }
+  }
+  for (; c < n_ct; ++c) {
     const float2 q = part[static_cast<size_t>(c) * T + t];
-    S += q.y * expf(q.x - M);
+    const float nm = fmaxf(M, q.x);
+    S = S * expf(M - nm) + q.y * expf(q.x - nm);
+    M = nm;
   }
   const float l = M + logf(S);
   lse[t] = l;
@@ -389,14 +402,11 @@ ss_status ss_backward(const uint16_t* H, const uint16_t* W, const int32_t* cand,
   cudaError_t e = launch_softmax_grad(tH, tWc, tGk, iT, iC, iD, slot, lse, scale, status, nsm, s);
   trace_post(s);
   if (e != cudaSuccess) return fail("launch gemm_softmax_grad", e);
-  trace_pre(s, "gemm_grad_h");
-  e = launch_grad_h(tGk, tWcMn, iT, iC, iD, dH, status, nsm, s);
+  trace_pre(s, "gemm_grads");
+  e = launch_grads(tGk, tWcMn, tGmn, tHmn, iT, iC, iD, iV, accumulate, cand, dH, dW, status, nsm,
+                   s);
   trace_post(s);
-  if (e != cudaSuccess) return fail("launch gemm_grad_h", e);
-  trace_pre(s, "gemm_grad_w_scatter");
-  e = launch_grad_w(tGmn, tHmn, iT, iC, iD, iV, accumulate, cand, dW, status, nsm, s);
-  trace_post(s);
-  if (e != cudaSuccess) return fail("launch gemm_grad_w_scatter", e);
+  if (e != cudaSuccess) return fail("launch gemm_grads", e);
   return SS_OK;
 }
 

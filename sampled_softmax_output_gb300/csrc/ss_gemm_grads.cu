@@ -3,6 +3,14 @@
 //   dWc = G^T . H          (M = C, N = D, K = T), scattered into dW[cand].
 // G is read in place in both: K-major for dH, MN-major (transposed through the
 // MMA's operand descriptor) for dW, so no transposed copy is ever made.
+#include <algorithm>
+#include <map>
+#include <memory>
+#include <mutex>
+#include <queue>
+#include <tuple>
+#include <vector>
+
 #include "ss_gemm.cuh"
 #include "ss_internal.h"
 
@@ -25,6 +33,283 @@ cudaError_t launch_grad_w(const CUtensorMap& tG_mn, const CUtensorMap& tH_mn, in
   EpiDw::Params ep{C, D, V, accumulate, cand, dW, status};
   return launch_gemm<kBnGrad, kStagesGrad, true, true, EpiDw>(tG_mn, tH_mn, shp, ep, status,
                                                               num_sms, stream);
+}
+
+// ------------------------------------------------- both GEMMs in one launch
+//
+// One persistent kernel runs the dW tiles and the dH tiles together. Which CTA
+// runs which tiles, in which order, is decided on the host by a greedy
+// longest-first list schedule (every tile goes to the CTA that becomes free
+// first, ties to the lowest CTA index) and passed in the kernel parameters.
+// Tiles handed out at the same moment start together, so the CTAs keep
+// marching through K side by side (the shared B operand stays in L2, and the
+// three tiles of a row block read their common A rows at the same time),
+// while the CTAs that finish their share of the long tiles early pick up the
+// short ones: this removes most of the idle tail two separate launches leave
+// on the SMs.
+
+namespace {
+
+constexpr int kSchedMaxCtas = 256;
+constexpr double kMergedGradsMaxBBytes = 96.0 * (1 << 20);
+constexpr int kSchedMaxUnits = 14080;
+
+struct GradSched {
+  uint16_t offs[kSchedMaxCtas + 1];  // CTA c runs units[offs[c] .. offs[c+1])
+  uint16_t units[kSchedMaxUnits];    // [0, n_dw): dW tiles, then dH tiles
+};
+
+struct GradBoth {
+  int n_dw, n_nt, kb_dw, kb_dh;
+  EpiDh::Params dh;
+  EpiDw::Params dw;
+  int* status;
+};
+
+using LG = GemmSmem<kBnGrad, kStagesGrad, 0>;
+
+__global__ void __launch_bounds__(GEMM_THREADS, 1)
+    k_grads(const __grid_constant__ CUtensorMap tmGk, const __grid_constant__ CUtensorMap tmWcMn,
+            const __grid_constant__ CUtensorMap tmGmn, const __grid_constant__ CUtensorMap tmHmn,
+            const __grid_constant__ GradBoth p, const __grid_constant__ GradSched sch) {
+  constexpr int BN = kBnGrad;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ int s_go;
+  const uint32_t raw = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+  GemmCtrl* ctrl = reinterpret_cast<GemmCtrl*>(smem + LG::CTRL_OFFSET);
+  const uint32_t tiles = smem_u32(smem);
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  int* status = p.status;
+  const int u_begin = sch.offs[blockIdx.x], u_end = sch.offs[blockIdx.x + 1];
+
+  if (threadIdx.x == 0) s_go = (read_status(status) == 0);
+  __syncthreads();
+  if (!s_go) return;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStagesGrad; ++s) {
+      mbar_init(&ctrl->full[s], 1);
+      mbar_init(&ctrl->empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&ctrl->tfull[b], 1);
+      mbar_init(&ctrl->tempty[b], 4 * 32);
+    }
+    mbar_init(&ctrl->drain, 1);
+    ctrl->abort_flag = 0;
+    fence_mbar_init();
+    tma_prefetch_map(&tmGk);
+    tma_prefetch_map(&tmWcMn);
+    tma_prefetch_map(&tmGmn);
+    tma_prefetch_map(&tmHmn);
+  }
+  if (warp == 1) {
+    tmem_alloc(&ctrl->tmem_base, 2 * BN);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = ctrl->tmem_base;
+  volatile int* abort_flag = &ctrl->abort_flag;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int s = 0;
+      uint32_t ph = 0, issued = 0, issued_ph = 0;
+      bool ok = true;
+      for (int i = u_begin; ok && i < u_end; ++i) {
+        const int u = sch.units[i];
+        const bool is_dw = u < p.n_dw;
+        const int v = is_dw ? u : u - p.n_dw;
+        const int mt = v / p.n_nt, nt = v % p.n_nt;
+        const int kbs = is_dw ? p.kb_dw : p.kb_dh;
+        for (int kb = 0; kb < kbs; ++kb) {
+          if (!mbar_wait(&ctrl->empty[s], ph ^ 1u, abort_flag, status)) {
+            ok = false;
+            break;
+          }
+          uint64_t* fb = &ctrl->full[s];
+          mbar_arrive_expect_tx(fb, LG::STAGE_BYTES);
+          const uint32_t a_dst = tiles + s * LG::STAGE_BYTES;
+          const uint32_t b_dst = a_dst + LG::A_BYTES;
+          if (is_dw) {  // A = G columns (MN-major), B = H (MN-major); K = tokens
+            tma_load_2d(a_dst, &tmGmn, fb, mt * BM, kb * BK);
+            tma_load_2d(a_dst + 8192, &tmGmn, fb, mt * BM + 64, kb * BK);
+#pragma unroll
+            for (int j = 0; j < BN / 64; ++j)
+              tma_load_2d(b_dst + j * 8192, &tmHmn, fb, nt * BN + 64 * j, kb * BK);
+          } else {      // A = G rows (K-major), B = W_c (MN-major); K = candidates
+            tma_load_2d(a_dst, &tmGk, fb, kb * BK, mt * BM);
+#pragma unroll
+            for (int j = 0; j < BN / 64; ++j)
+              tma_load_2d(b_dst + j * 8192, &tmWcMn, fb, nt * BN + 64 * j, kb * BK);
+          }
+          issued |= 1u << s;
+          issued_ph = (issued_ph & ~(1u << s)) | (ph << s);
+          if (++s == kStagesGrad) {
+            s = 0;
+            ph ^= 1u;
+          }
+        }
+      }
+      for (int j = 0; j < kStagesGrad; ++j)
+        if ((issued >> j) & 1u) mbar_drain(&ctrl->full[j], (issued_ph >> j) & 1u, status);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ---------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc_dw = idesc_bf16_f32(BM, BN, true, true);
+      constexpr uint32_t idesc_dh = idesc_bf16_f32(BM, BN, false, true);
+      int s = 0, b = 0;
+      uint32_t ph = 0, aph = 0;
+      bool ok = true;
+      for (int i = u_begin; ok && i < u_end; ++i) {
+        const bool is_dw = sch.units[i] < p.n_dw;
+        const int kbs = is_dw ? p.kb_dw : p.kb_dh;
+        if (!mbar_wait(&ctrl->tempty[b], aph ^ 1u, abort_flag, status)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(b * BN);
+        for (int kb = 0; kb < kbs; ++kb) {
+          if (!mbar_wait(&ctrl->full[s], ph, abort_flag, status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_addr = tiles + s * LG::STAGE_BYTES;
+          const uint32_t b_addr = a_addr + LG::A_BYTES;
+#pragma unroll
+          for (int k = 0; k < BK / UMMA_K; ++k) {
+            const uint64_t ad = is_dw ? sdesc_sw128(a_addr + k * 2048, 8192, 1024)
+                                      : sdesc_sw128(a_addr + k * 32, 16, 1024);
+            const uint64_t bd = sdesc_sw128(b_addr + k * 2048, 8192, 1024);
+            mma_bf16(d_tmem, ad, bd, is_dw ? idesc_dw : idesc_dh, (kb | k) != 0 ? 1u : 0u);
+          }
+          mma_commit(&ctrl->empty[s]);
+          if (++s == kStagesGrad) {
+            s = 0;
+            ph ^= 1u;
+          }
+        }
+        if (!ok) break;
+        mma_commit(&ctrl->tfull[b]);
+        if (++b == 2) {
+          b = 0;
+          aph ^= 1u;
+        }
+      }
+      mma_commit(&ctrl->drain);
+      mbar_drain(&ctrl->drain, 0, status);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;
+    const int row = q * 32 + lane;
+    const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+    EpiState es{0u, 0, 0u};
+    int b = 0;
+    uint32_t aph = 0;
+    for (int i = u_begin; i < u_end; ++i) {
+      const bool ok = mbar_wait(&ctrl->tfull[b], aph, abort_flag, status);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      tc_fence_after();
+      const int u = sch.units[i];
+      const bool is_dw = u < p.n_dw;
+      const int v = is_dw ? u : u - p.n_dw;
+      const uint32_t taddr = lane_addr + static_cast<uint32_t>(b * BN);
+      if (is_dw) EpiDw::template apply<BN>(p.dw, v / p.n_nt, v % p.n_nt, row, taddr, es);
+      else EpiDh::template apply<BN>(p.dh, v / p.n_nt, v % p.n_nt, row, taddr, es);
+      tc_fence_before();
+      mbar_arrive(&ctrl->tempty[b]);
+      if (++b == 2) {
+        b = 0;
+        aph ^= 1u;
+      }
+    }
+  }
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, 2 * BN);
+  }
+}
+
+// Greedy longest-first list schedule of the tiles over `ctas` CTAs; cached by
+// problem shape. Returns nullptr if it does not fit the kernel parameters.
+std::shared_ptr<const GradSched> grad_schedule(int n_dw, int kb_dw, int n_dh, int kb_dh, int ctas) {
+  static std::mutex mu;
+  static std::map<std::tuple<int, int, int, int, int>, std::shared_ptr<const GradSched>> cache;
+  const auto key = std::make_tuple(n_dw, kb_dw, n_dh, kb_dh, ctas);
+  std::lock_guard<std::mutex> lock(mu);
+  auto it = cache.find(key);
+  if (it != cache.end()) return it->second;
+  const long long n = static_cast<long long>(n_dw) + n_dh;
+  if (n > kSchedMaxUnits || ctas > kSchedMaxCtas || ctas < 1) return nullptr;
+  std::vector<std::vector<uint16_t>> lists(ctas);
+  using Slot = std::pair<long long, int>;  // (time the CTA becomes free, CTA)
+  std::priority_queue<Slot, std::vector<Slot>, std::greater<Slot>> free_at;
+  for (int c = 0; c < ctas; ++c) free_at.push({0, c});
+  auto place = [&](int u, int len) {
+    const Slot sl = free_at.top();
+    free_at.pop();
+    lists[sl.second].push_back(static_cast<uint16_t>(u));
+    free_at.push({sl.first + len, sl.second});
+  };
+  const bool dw_first = kb_dw >= kb_dh;
+  for (int pass = 0; pass < 2; ++pass) {
+    if ((pass == 0) == dw_first)
+      for (int u = 0; u < n_dw; ++u) place(u, kb_dw);
+    else
+      for (int u = 0; u < n_dh; ++u) place(n_dw + u, kb_dh);
+  }
+  auto sch = std::make_shared<GradSched>();
+  int at = 0;
+  for (int c = 0; c < ctas; ++c) {
+    sch->offs[c] = static_cast<uint16_t>(at);
+    for (uint16_t u : lists[c]) sch->units[at++] = u;
+  }
+  sch->offs[ctas] = static_cast<uint16_t>(at);
+  if (cache.size() > 64) cache.clear();
+  cache[key] = sch;
+  return sch;
+}
+
+}  // namespace
+
+cudaError_t launch_grads(const CUtensorMap& tG_kmaj, const CUtensorMap& tWc_mn,
+                         const CUtensorMap& tG_mn, const CUtensorMap& tH_mn, int T, int C, int D,
+                         int V, int accumulate, const int32_t* cand, uint16_t* dH, float* dW,
+                         int* status, int num_sms, cudaStream_t stream) {
+  GradBoth p;
+  p.n_nt = (D + kBnGrad - 1) / kBnGrad;
+  p.n_dw = (C + BM - 1) / BM * p.n_nt;
+  const int n_dh = (T + BM - 1) / BM * p.n_nt;
+  p.kb_dw = (T + BK - 1) / BK;
+  p.kb_dh = (C + BK - 1) / BK;
+  p.dh = EpiDh::Params{T, D, dH};
+  p.dw = EpiDw::Params{C, D, V, accumulate, cand, dW, status};
+  p.status = status;
+  const int ctas = std::min(num_sms, kSchedMaxCtas);
+  // Running dW and dH tiles side by side pays when their B operands (H and
+  // W_c) fit in L2 together; beyond that they evict each other and two
+  // phase-separated launches are faster (measured on GB300: merged is 5-17%
+  // faster at (T + C) * D * 2 = 41-72 MB, 10% slower at 138-177 MB).
+  const double b_bytes = (static_cast<double>(T) + C) * D * 2.0;
+  auto sch = b_bytes <= kMergedGradsMaxBBytes
+                 ? grad_schedule(p.n_dw, p.kb_dw, n_dh, p.kb_dh, ctas)
+                 : std::shared_ptr<const GradSched>();
+  if (!sch) {  // two phase-separated round-robin launches
+    cudaError_t e = launch_grad_h(tG_kmaj, tWc_mn, T, C, D, dH, status, num_sms, stream);
+    if (e != cudaSuccess) return e;
+    return launch_grad_w(tG_mn, tH_mn, T, C, D, V, accumulate, cand, dW, status, num_sms, stream);
+  }
+  cudaError_t e = cudaFuncSetAttribute(k_grads, cudaFuncAttributeMaxDynamicSharedMemorySize, LG::TOTAL);
+  if (e != cudaSuccess) return e;
+  k_grads<<<ctas, GEMM_THREADS, LG::TOTAL, stream>>>(tG_kmaj, tWc_mn, tG_mn, tH_mn, p, *sch);
+  return cudaGetLastError();
 }
 
 }  // namespace ss

@@ -37,5 +37,11 @@ cudaError_t launch_grad_h(const CUtensorMap& tG_kmaj, const CUtensorMap& tWc_mn,
 cudaError_t launch_grad_w(const CUtensorMap& tG_mn, const CUtensorMap& tH_mn, int T, int C, int D,
                           int V, int accumulate, const int32_t* cand, float* dW, int* status,
                           int num_sms, cudaStream_t stream);
+// Both gradient GEMMs in one launch with a host-computed balanced schedule
+// (falls back to the two launches above for very large problems).
+cudaError_t launch_grads(const CUtensorMap& tG_kmaj, const CUtensorMap& tWc_mn,
+                         const CUtensorMap& tG_mn, const CUtensorMap& tH_mn, int T, int C, int D,
+                         int V, int accumulate, const int32_t* cand, uint16_t* dH, float* dW,
+                         int* status, int num_sms, cudaStream_t stream);
 
 }  // namespace ss

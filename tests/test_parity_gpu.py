@@ -236,5 +236,5 @@ def test_kernel_trace_records_every_launch():
     torch.cuda.synchronize()
     names = [n for n, _ in tr.timings()]
     assert names == ["build_candidates", "gather_rows", "gemm_forward_lse", "lse_merge",
-                     "gather_rows", "gemm_softmax_grad", "gemm_grad_h", "gemm_grad_w_scatter"]
+                     "gather_rows", "gemm_softmax_grad", "gemm_grads"]
     assert all(ms > 0 for _, ms in tr.timings())
