@@ -86,7 +86,7 @@ def load_peaks():
 KERNEL_SOURCES = {
     "gemm_forward_lse": ["ss_ptx.cuh", "ss_gemm.cuh", "ss_gemm_logits.cu"],
     "gemm_softmax_grad": ["ss_ptx.cuh", "ss_gemm.cuh", "ss_gemm_logits.cu"],
-    "gemm_grads": ["ss_ptx.cuh", "ss_gemm.cuh", "ss_gemm_grads.cu"],
+    "gemm_grads": ["ss_ptx.cuh", "ss_gemm.cuh", "ss_gemm2.cuh", "ss_gemm_grads.cu"],
     "build_candidates": ["ss_ptx.cuh", "ss_candidates.cu"],
 }
 

@@ -41,7 +41,7 @@ Layout make_layout(int64_t T, int64_t C, int64_t D) {
   L.wc = off;
   off = align_up(off + static_cast<size_t>(C) * D * 2, 1024);
   L.part = off;
-  off = align_up(off + static_cast<size_t>(L.n_ct) * T * sizeof(float2), 1024);
+  off = align_up(off + static_cast<size_t>(L.n_ct) * kFwdGroups * T * sizeof(float2), 1024);
   L.tgt = off;
   off = align_up(off + static_cast<size_t>(T) * sizeof(float), 1024);
   L.g = off;
@@ -145,12 +145,14 @@ __global__ void __launch_bounds__(256) k_lse_merge(const float2* __restrict__ pa
   // one pass: online merge of the per-tile (max, sum) pairs, loads batched
   float M = -INFINITY, S = 0.f;
   int c = 0;
+  // (-inf, 0) marks a column group with no valid column: skipped
   for (; c + 8 <= n_ct; c += 8) {
     float2 q[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) q[i] = part[static_cast<size_t>(c + i) * T + t];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
+      if (q[i].x == -INFINITY) continue;
       const float nm = fmaxf(M, q[i].x);
       S = S * expf(M - nm) + q[i].y * expf(q[i].x - nm);
       M = nm;
@@ -158,6 +160,7 @@ __global__ void __launch_bounds__(256) k_lse_merge(const float2* __restrict__ pa
   }
   for (; c < n_ct; ++c) {
     const float2 q = part[static_cast<size_t>(c) * T + t];
+    if (q.x == -INFINITY) continue;
     const float nm = fmaxf(M, q.x);
     S = S * expf(M - nm) + q.y * expf(q.x - nm);
     M = nm;
@@ -347,7 +350,7 @@ ss_status ss_forward(const uint16_t* H, const uint16_t* W, const int32_t* cand,
   const int blocks = static_cast<int>((T + 255) / 256);
   trace_pre(s, "lse_merge");
   k_lse_merge<<<blocks, 256, 0, s>>>(part, tgt, slot, static_cast<int>(T), static_cast<int>(C),
-                                     static_cast<int>(L.n_ct), loss, lse, status);
+                                     static_cast<int>(L.n_ct * kFwdGroups), loss, lse, status);
   trace_post(s);
   return cuda_status(cudaGetLastError(), "launch k_lse_merge");
 }
@@ -468,8 +471,8 @@ ss_status ss_forward_noalloc(const uint16_t* H, const uint16_t* W, const int32_t
   if (e != cudaSuccess) return fail("launch gemm_forward_lse", e);
   trace_pre(s, "lse_merge");
   k_lse_merge<<<static_cast<int>((T + 255) / 256), 256, 0, s>>>(
-      part, tgt, slot, static_cast<int>(T), static_cast<int>(C), static_cast<int>(L.n_ct), loss,
-      lse, status);
+      part, tgt, slot, static_cast<int>(T), static_cast<int>(C),
+      static_cast<int>(L.n_ct * kFwdGroups), loss, lse, status);
   trace_post(s);
   if (cudaError_t e0 = cudaGetLastError(); e0 != cudaSuccess) return fail("launch k_lse_merge", e0);
   if (status_host) {

@@ -61,7 +61,7 @@ struct GemmCtrl {
   uint64_t drain;
   uint32_t tmem_base;
   int abort_flag;
-  int vote[2][4];  // per-tile vote of the epilogue warps (alternating halves)
+  int vote[2][8];  // per-tile vote of the epilogue warps (alternating halves)
 };
 
 // Units are (m_tile, n_tile) pairs numbered m-major: u = m_tile * n_tiles + n_tile.
@@ -73,9 +73,32 @@ struct GemmShape {
 
 // ----------------------------------------------------------------- epilogues
 
+// Runs fn(r, i) over the 32-column chunks [c_begin, c_begin + n) of this
+// thread's TMEM row, with the load of chunk i + 1 in flight while chunk i is
+// processed.
+template <int N, class F>
+__device__ __forceinline__ void for_tmem_chunks(uint32_t taddr, int c_begin, F&& fn) {
+  uint32_t ra[32], rb[32];
+  tmem_ld32(taddr + c_begin * 32, ra);
+#pragma unroll
+  for (int i = 0; i < N; i += 2) {
+    tmem_ld_wait(ra);
+    if (i + 1 < N) tmem_ld32(taddr + (c_begin + i + 1) * 32, rb);
+    fn(ra, i);
+    if (i + 1 < N) {
+      tmem_ld_wait(rb);
+      if (i + 2 < N) tmem_ld32(taddr + (c_begin + i + 2) * 32, ra);
+      fn(rb, i + 1);
+    }
+  }
+}
+
 // Forward: per-row softmax partials of one 128 x BN logit tile.
-//   part[n_tile][t] = (max_j S[t,j], sum_j exp(S[t,j] - max)) over the tile's
-//   valid columns; tgt[t] = S[t, slot[t]] from the tile that holds slot[t].
+//   With NCG column groups per tile (NCG epilogue warps per row block), group
+//   cg covers columns [cg * BN / NCG, (cg + 1) * BN / NCG) of the tile and
+//   writes part[nt * NCG + cg][t] = (max_j S[t,j], sum_j exp(S[t,j] - max))
+//   over its valid columns, or (-inf, 0) if it has none; tgt[t] = S[t, slot[t]]
+//   comes from the group that holds slot[t].
 struct EpiFwd {
   static constexpr int kStageBytes = 0;
   struct Params {
@@ -86,50 +109,49 @@ struct EpiFwd {
     int* status;
   };
   __device__ static void finish(const Params&, EpiState&) {}
-  template <int BN>
+  template <int BN, int NCG>
   __device__ static void apply(const Params& p, int mt, int nt, int row, uint32_t taddr,
-                               EpiState&) {
+                               EpiState&, int cg) {
+    constexpr int CPG = BN / 32 / NCG;  // chunks per group
     const int t = mt * BM + row;
     const bool valid = t < p.T;
     const int sl = valid ? __ldg(p.slot + t) : -1;
-    const int j0 = nt * BN;
-    const int ncols = min(BN, p.C - j0);
+    const int j0 = nt * BN + cg * CPG * 32;  // first column of this group
+    const int ncols = min(CPG * 32, p.C - j0);
     float m = -INFINITY, s = 0.f, tg = 0.f;
     bool has_t = false;
-#pragma unroll 1
-    for (int c = 0; c < BN / 32; ++c) {
-      const int jc = c * 32;
-      if (jc >= ncols) break;  // uniform: depends on the tile only
-      uint32_t r[32];
-      tmem_ld32(taddr + jc, r);
-      tmem_ld_wait();
-      const int nv = min(32, ncols - jc);
-      float cm = -INFINITY;
+    if (ncols > 0) {  // uniform: depends on the tile only
+      for_tmem_chunks<CPG>(taddr, cg * CPG, [&](const uint32_t(&r)[32], int i) {
+        const int jc = i * 32;
+        const int nv = min(32, ncols - jc);
+        if (nv <= 0) return;
+        float cm = -INFINITY;
 #pragma unroll
-      for (int i = 0; i < 32; ++i)
-        if (i < nv) cm = fmaxf(cm, __uint_as_float(r[i]));
-      const float nm = fmaxf(m, cm);
-      const float nm2 = nm * kLog2e;
-      float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+        for (int k = 0; k < 32; ++k)
+          if (k < nv) cm = fmaxf(cm, __uint_as_float(r[k]));
+        const float nm = fmaxf(m, cm);
+        const float nm2 = nm * kLog2e;
+        float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
 #pragma unroll
-      for (int i = 0; i < 32; i += 4) {
-        if (i + 0 < nv) a0 += ex2_approx(fmaf(__uint_as_float(r[i + 0]), kLog2e, -nm2));
-        if (i + 1 < nv) a1 += ex2_approx(fmaf(__uint_as_float(r[i + 1]), kLog2e, -nm2));
-        if (i + 2 < nv) a2 += ex2_approx(fmaf(__uint_as_float(r[i + 2]), kLog2e, -nm2));
-        if (i + 3 < nv) a3 += ex2_approx(fmaf(__uint_as_float(r[i + 3]), kLog2e, -nm2));
-      }
-      s = s * ex2_approx((m - nm) * kLog2e) + ((a0 + a1) + (a2 + a3));
-      m = nm;
-      const int off = sl - j0 - jc;
-      if (static_cast<unsigned>(off) < static_cast<unsigned>(nv)) {
+        for (int k = 0; k < 32; k += 4) {
+          if (k + 0 < nv) a0 += ex2_approx(fmaf(__uint_as_float(r[k + 0]), kLog2e, -nm2));
+          if (k + 1 < nv) a1 += ex2_approx(fmaf(__uint_as_float(r[k + 1]), kLog2e, -nm2));
+          if (k + 2 < nv) a2 += ex2_approx(fmaf(__uint_as_float(r[k + 2]), kLog2e, -nm2));
+          if (k + 3 < nv) a3 += ex2_approx(fmaf(__uint_as_float(r[k + 3]), kLog2e, -nm2));
+        }
+        s = s * ex2_approx((m - nm) * kLog2e) + ((a0 + a1) + (a2 + a3));
+        m = nm;
+        const int off = sl - j0 - jc;
+        if (static_cast<unsigned>(off) < static_cast<unsigned>(nv)) {
 #pragma unroll
-        for (int i = 0; i < 32; ++i)
-          if (i == off) tg = __uint_as_float(r[i]);
-        has_t = true;
-      }
+          for (int k = 0; k < 32; ++k)
+            if (k == off) tg = __uint_as_float(r[k]);
+          has_t = true;
+        }
+      });
     }
     if (valid) {
-      p.part[static_cast<size_t>(nt) * p.T + t] = make_float2(m, s);
+      p.part[static_cast<size_t>(nt * NCG + cg) * p.T + t] = make_float2(m, s);
       if (has_t) p.tgt[t] = tg;
     }
   }
@@ -145,7 +167,7 @@ struct EpiFwd {
 // patched into the staged tile.
 struct EpiG {
   static constexpr int kStageBytes = 2 * 16384;
-  struct alignas(64) Params {
+  struct Params {
     CUtensorMap tmG;  // G [T, C] bf16 (row pitch ldG), box 64 x 128, 128-byte swizzle
     int T, C;
     const int32_t* slot;
@@ -157,9 +179,10 @@ struct EpiG {
   __device__ static void finish(const Params&, EpiState& es) {
     if (es.ep_tid == 0) bulk_wait<0>();
   }
-  template <int BN>
+  template <int BN, int NCG>
   __device__ static void apply(const Params& p, int mt, int nt, int row, uint32_t taddr,
-                               EpiState& es) {
+                               EpiState& es, int) {
+    static_assert(NCG == 1, "the staged G epilogue runs with four epilogue warps");
     const int t = mt * BM + row;
     const bool valid = t < p.T;
     const int sl = valid ? __ldg(p.slot + t) : -1;
@@ -225,7 +248,7 @@ struct EpiG {
   }
 };
 
-// Backward, step 2: dH tile -> bf16.
+// Backward, step 2: dH tile -> bf16 (column group cg of NCG).
 struct EpiDh {
   static constexpr int kStageBytes = 0;
   struct Params {
@@ -233,38 +256,35 @@ struct EpiDh {
     uint16_t* dH;
   };
   __device__ static void finish(const Params&, EpiState&) {}
-  template <int BN>
+  template <int BN, int NCG>
   __device__ static void apply(const Params& p, int mt, int nt, int row, uint32_t taddr,
-                               EpiState&) {
+                               EpiState&, int cg) {
+    constexpr int CPG = BN / 32 / NCG;
     const int t = mt * BM + row;
     const bool valid = t < p.T;
-    const int n0 = nt * BN;
-    const int ncols = min(BN, p.D - n0);
+    const int n0 = nt * BN + cg * CPG * 32;
+    const int ncols = min(CPG * 32, p.D - n0);
+    if (ncols <= 0) return;
     uint16_t* drow = p.dH + static_cast<size_t>(valid ? t : 0) * p.D + n0;
-#pragma unroll 1
-    for (int c = 0; c < BN / 32; ++c) {
-      const int jc = c * 32;
-      if (jc >= ncols) break;
-      uint32_t r[32];
-      tmem_ld32(taddr + jc, r);
-      tmem_ld_wait();
-      if (valid) {
-        uint4* dst = reinterpret_cast<uint4*>(drow + jc);
+    for_tmem_chunks<CPG>(taddr, cg * CPG, [&](const uint32_t(&r)[32], int i) {
+      const int jc = i * 32;
+      if (jc >= ncols || !valid) return;
+      uint4* dst = reinterpret_cast<uint4*>(drow + jc);
 #pragma unroll
-        for (int v = 0; v < 4; ++v) {
-          uint32_t q0 = pack_bf16x2(__uint_as_float(r[8 * v + 0]), __uint_as_float(r[8 * v + 1]));
-          uint32_t q1 = pack_bf16x2(__uint_as_float(r[8 * v + 2]), __uint_as_float(r[8 * v + 3]));
-          uint32_t q2 = pack_bf16x2(__uint_as_float(r[8 * v + 4]), __uint_as_float(r[8 * v + 5]));
-          uint32_t q3 = pack_bf16x2(__uint_as_float(r[8 * v + 6]), __uint_as_float(r[8 * v + 7]));
-          dst[v] = make_uint4(q0, q1, q2, q3);
-        }
+      for (int v = 0; v < 4; ++v) {
+        const uint32_t q0 = pack_bf16x2(__uint_as_float(r[8 * v + 0]), __uint_as_float(r[8 * v + 1]));
+        const uint32_t q1 = pack_bf16x2(__uint_as_float(r[8 * v + 2]), __uint_as_float(r[8 * v + 3]));
+        const uint32_t q2 = pack_bf16x2(__uint_as_float(r[8 * v + 4]), __uint_as_float(r[8 * v + 5]));
+        const uint32_t q3 = pack_bf16x2(__uint_as_float(r[8 * v + 6]), __uint_as_float(r[8 * v + 7]));
+        dst[v] = make_uint4(q0, q1, q2, q3);
       }
-    }
+    });
   }
 };
 
 // Backward, step 3: dW_c tile scattered into the owning rows dW[cand[j]]
-// (= or +=). Candidate ids are distinct, so no two threads write one row.
+// (= or +=), column group cg of NCG. Candidate ids are distinct, so no two
+// threads write one row.
 struct EpiDw {
   static constexpr int kStageBytes = 0;
   struct Params {
@@ -274,43 +294,39 @@ struct EpiDw {
     int* status;
   };
   __device__ static void finish(const Params&, EpiState&) {}
-  template <int BN>
+  template <int BN, int NCG>
   __device__ static void apply(const Params& p, int mt, int nt, int row, uint32_t taddr,
-                               EpiState&) {
+                               EpiState&, int cg) {
+    constexpr int CPG = BN / 32 / NCG;
     const int j = mt * BM + row;
     bool valid = j < p.C;
     const int v = valid ? __ldg(p.cand + j) : 0;
     if (valid && static_cast<unsigned>(v) >= static_cast<unsigned>(p.V)) {
-      set_status(p.status, SS_ERR_INDEX);
+      if (cg == 0) set_status(p.status, SS_ERR_INDEX);
       valid = false;
     }
-    const int n0 = nt * BN;
-    const int ncols = min(BN, p.D - n0);
+    const int n0 = nt * BN + cg * CPG * 32;
+    const int ncols = min(CPG * 32, p.D - n0);
+    if (ncols <= 0) return;
     float* drow = p.dW + static_cast<size_t>(valid ? v : 0) * p.D + n0;
-#pragma unroll 1
-    for (int c = 0; c < BN / 32; ++c) {
-      const int jc = c * 32;
-      if (jc >= ncols) break;
-      uint32_t r[32];
-      tmem_ld32(taddr + jc, r);
-      tmem_ld_wait();
-      if (valid) {
-        float4* dst = reinterpret_cast<float4*>(drow + jc);
+    for_tmem_chunks<CPG>(taddr, cg * CPG, [&](const uint32_t(&r)[32], int i) {
+      const int jc = i * 32;
+      if (jc >= ncols || !valid) return;
+      float4* dst = reinterpret_cast<float4*>(drow + jc);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          float4 o = make_float4(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]),
-                                 __uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3]));
-          if (p.accumulate) {
-            const float4 old = dst[i];
-            o.x += old.x;
-            o.y += old.y;
-            o.z += old.z;
-            o.w += old.w;
-          }
-          dst[i] = o;
+      for (int k = 0; k < 8; ++k) {
+        float4 o = make_float4(__uint_as_float(r[4 * k]), __uint_as_float(r[4 * k + 1]),
+                               __uint_as_float(r[4 * k + 2]), __uint_as_float(r[4 * k + 3]));
+        if (p.accumulate) {
+          const float4 old = dst[k];
+          o.x += old.x;
+          o.y += old.y;
+          o.z += old.z;
+          o.w += old.w;
         }
+        dst[k] = o;
       }
-    }
+    });
   }
 };
 
@@ -475,7 +491,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       if (!go) break;
       tc_fence_after();
       const int mt = u / shp.n_tiles, nt = u % shp.n_tiles;
-      Epi::template apply<BN>(ep, mt, nt, row, lane_addr + static_cast<uint32_t>(b * BN), es);
+      Epi::template apply<BN, 1>(ep, mt, nt, row, lane_addr + static_cast<uint32_t>(b * BN), es, 0);
       tc_fence_before();
       mbar_arrive(&ctrl->tempty[b]);
       if (++b == 2) {

@@ -12,6 +12,7 @@
 #include <vector>
 
 #include "ss_gemm.cuh"
+#include "ss_gemm2.cuh"
 #include "ss_internal.h"
 
 namespace ss {
@@ -20,19 +21,19 @@ constexpr int kStagesGrad = 4;
 
 cudaError_t launch_grad_h(const CUtensorMap& tG_kmaj, const CUtensorMap& tWc_mn, int T, int C,
                           int D, uint16_t* dH, int* status, int num_sms, cudaStream_t stream) {
-  GemmShape shp{(T + BM - 1) / BM, (D + kBnGrad - 1) / kBnGrad, (C + BK - 1) / BK};
+  GemmShape shp{(T + 2 * BM - 1) / (2 * BM), (D + kBnGrad - 1) / kBnGrad, (C + BK - 1) / BK};
   EpiDh::Params ep{T, D, dH};
-  return launch_gemm<kBnGrad, kStagesGrad, false, true, EpiDh>(tG_kmaj, tWc_mn, shp, ep, status,
-                                                               num_sms, stream);
+  return launch_gemm2<kBnGrad, 6, false, true, EpiDh, 8>(tG_kmaj, tWc_mn, shp, ep, status, num_sms,
+                                                         stream);
 }
 
 cudaError_t launch_grad_w(const CUtensorMap& tG_mn, const CUtensorMap& tH_mn, int T, int C, int D,
                           int V, int accumulate, const int32_t* cand, float* dW, int* status,
                           int num_sms, cudaStream_t stream) {
-  GemmShape shp{(C + BM - 1) / BM, (D + kBnGrad - 1) / kBnGrad, (T + BK - 1) / BK};
+  GemmShape shp{(C + 2 * BM - 1) / (2 * BM), (D + kBnGrad - 1) / kBnGrad, (T + BK - 1) / BK};
   EpiDw::Params ep{C, D, V, accumulate, cand, dW, status};
-  return launch_gemm<kBnGrad, kStagesGrad, true, true, EpiDw>(tG_mn, tH_mn, shp, ep, status,
-                                                              num_sms, stream);
+  return launch_gemm2<kBnGrad, 6, true, true, EpiDw, 8>(tG_mn, tH_mn, shp, ep, status, num_sms,
+                                                        stream);
 }
 
 // ------------------------------------------------- both GEMMs in one launch
@@ -60,40 +61,51 @@ struct GradSched {
 };
 
 struct GradBoth {
-  int n_dw, n_nt, kb_dw, kb_dh;
+  int n_dw, n_nt, kb_dw, kb_dh;  // n_dw counts 256-row dW tiles (x column tiles)
   EpiDh::Params dh;
   EpiDw::Params dw;
   int* status;
 };
 
-using LG = GemmSmem<kBnGrad, kStagesGrad, 0>;
+constexpr int kStagesPairGrad = 6;
+constexpr int kGradEpiWarps = 8;
+using LG2 = Gemm2Smem<kBnGrad, kStagesPairGrad, 0>;
 
-__global__ void __launch_bounds__(GEMM_THREADS, 1)
+// Both gradient GEMMs on CTA pairs (see ss_gemm2.cuh for the pair protocol):
+// pair p runs the 256-row tiles sch.units[sch.offs[p] .. sch.offs[p + 1]).
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * kGradEpiWarps, 1)
     k_grads(const __grid_constant__ CUtensorMap tmGk, const __grid_constant__ CUtensorMap tmWcMn,
             const __grid_constant__ CUtensorMap tmGmn, const __grid_constant__ CUtensorMap tmHmn,
             const __grid_constant__ GradBoth p, const __grid_constant__ GradSched sch) {
   constexpr int BN = kBnGrad;
+  constexpr int STAGES = kStagesPairGrad;
+  constexpr int NCG = kGradEpiWarps / 4;
+  using L = LG2;
   extern __shared__ uint8_t smem_raw[];
   __shared__ int s_go;
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
-  GemmCtrl* ctrl = reinterpret_cast<GemmCtrl*>(smem + LG::CTRL_OFFSET);
+  GemmCtrl* ctrl = reinterpret_cast<GemmCtrl*>(smem + L::CTRL_OFFSET);
   const uint32_t tiles = smem_u32(smem);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const uint32_t rank = cluster_ctarank();
+  const int pair = blockIdx.x >> 1;
   int* status = p.status;
-  const int u_begin = sch.offs[blockIdx.x], u_end = sch.offs[blockIdx.x + 1];
+  const int u_begin = sch.offs[pair], u_end = sch.offs[pair + 1];
 
   if (threadIdx.x == 0) s_go = (read_status(status) == 0);
-  __syncthreads();
+  cluster_sync_all();
+  if (threadIdx.x == 0) s_go = s_go && ld_shared_cluster_u32(mapa_shared(smem_u32(&s_go), rank ^ 1u));
+  cluster_sync_all();
   if (!s_go) return;
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStagesGrad; ++s) {
+    for (int s = 0; s < STAGES; ++s) {
       mbar_init(&ctrl->full[s], 1);
       mbar_init(&ctrl->empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&ctrl->tfull[b], 1);
-      mbar_init(&ctrl->tempty[b], 4 * 32);
+      mbar_init(&ctrl->tempty[b], 2 * kGradEpiWarps);
     }
     mbar_init(&ctrl->drain, 1);
     ctrl->abort_flag = 0;
@@ -104,17 +116,17 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     tma_prefetch_map(&tmHmn);
   }
   if (warp == 1) {
-    tmem_alloc(&ctrl->tmem_base, 2 * BN);
-    tmem_relinquish();
+    tmem_alloc_pair(&ctrl->tmem_base, 2 * BN);
+    tmem_relinquish_pair();
   }
   tc_fence_before();
-  __syncthreads();
+  cluster_sync_all();
   tc_fence_after();
   const uint32_t tmem_base = ctrl->tmem_base;
   volatile int* abort_flag = &ctrl->abort_flag;
 
   if (warp == 0) {
-    // ------------------------------------------------------------ producer
+    // ------------------------------------------------ producer (both CTAs)
     if (lane == 0) {
       int s = 0;
       uint32_t ph = 0, issued = 0, issued_ph = 0;
@@ -124,45 +136,52 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         const bool is_dw = u < p.n_dw;
         const int v = is_dw ? u : u - p.n_dw;
         const int mt = v / p.n_nt, nt = v % p.n_nt;
+        const int m0 = mt * 2 * BM + static_cast<int>(rank) * BM;
+        const int n0 = nt * BN + static_cast<int>(rank) * (BN / 2);
         const int kbs = is_dw ? p.kb_dw : p.kb_dh;
         for (int kb = 0; kb < kbs; ++kb) {
           if (!mbar_wait(&ctrl->empty[s], ph ^ 1u, abort_flag, status)) {
             ok = false;
             break;
           }
-          uint64_t* fb = &ctrl->full[s];
-          mbar_arrive_expect_tx(fb, LG::STAGE_BYTES);
-          const uint32_t a_dst = tiles + s * LG::STAGE_BYTES;
-          const uint32_t b_dst = a_dst + LG::A_BYTES;
+          const uint32_t fb_local = smem_u32(&ctrl->full[s]);
+          if (rank == 0) mbar_arrive_expect_tx(&ctrl->full[s], 2 * L::STAGE_BYTES);
+          const uint32_t fb = rank == 0 ? fb_local : mapa_shared(fb_local, 0);
+          const uint32_t a_dst = tiles + s * L::STAGE_BYTES;
+          const uint32_t b_dst = a_dst + L::A_BYTES;
           if (is_dw) {  // A = G columns (MN-major), B = H (MN-major); K = tokens
-            tma_load_2d(a_dst, &tmGmn, fb, mt * BM, kb * BK);
-            tma_load_2d(a_dst + 8192, &tmGmn, fb, mt * BM + 64, kb * BK);
-#pragma unroll
-            for (int j = 0; j < BN / 64; ++j)
-              tma_load_2d(b_dst + j * 8192, &tmHmn, fb, nt * BN + 64 * j, kb * BK);
+            tma_load_2d_pair(a_dst, &tmGmn, fb, m0, kb * BK);
+            tma_load_2d_pair(a_dst + 8192, &tmGmn, fb, m0 + 64, kb * BK);
+            tma_load_2d_pair(b_dst, &tmHmn, fb, n0, kb * BK);
+            tma_load_2d_pair(b_dst + 8192, &tmHmn, fb, n0 + 64, kb * BK);
           } else {      // A = G rows (K-major), B = W_c (MN-major); K = candidates
-            tma_load_2d(a_dst, &tmGk, fb, kb * BK, mt * BM);
-#pragma unroll
-            for (int j = 0; j < BN / 64; ++j)
-              tma_load_2d(b_dst + j * 8192, &tmWcMn, fb, nt * BN + 64 * j, kb * BK);
+            tma_load_2d_pair(a_dst, &tmGk, fb, kb * BK, m0);
+            tma_load_2d_pair(b_dst, &tmWcMn, fb, n0, kb * BK);
+            tma_load_2d_pair(b_dst + 8192, &tmWcMn, fb, n0 + 64, kb * BK);
           }
           issued |= 1u << s;
           issued_ph = (issued_ph & ~(1u << s)) | (ph << s);
-          if (++s == kStagesGrad) {
+          if (++s == STAGES) {
             s = 0;
             ph ^= 1u;
           }
         }
       }
-      for (int j = 0; j < kStagesGrad; ++j)
-        if ((issued >> j) & 1u) mbar_drain(&ctrl->full[j], (issued_ph >> j) & 1u, status);
+      if (rank == 0) {
+        for (int j = 0; j < STAGES; ++j)
+          if ((issued >> j) & 1u) mbar_drain(&ctrl->full[j], (issued_ph >> j) & 1u, status);
+      } else if (!ok) {
+        const uint64_t t0 = globaltimer_ns();
+        while (globaltimer_ns() - t0 < 200000ull) {
+        }
+      }
     }
     __syncwarp();
   } else if (warp == 1) {
-    // ---------------------------------------------------------- MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idesc_dw = idesc_bf16_f32(BM, BN, true, true);
-      constexpr uint32_t idesc_dh = idesc_bf16_f32(BM, BN, false, true);
+    // ------------------------------------------------ MMA issuer (leader)
+    if (lane == 0 && rank == 0) {
+      constexpr uint32_t idesc_dw = idesc_bf16_f32(2 * BM, BN, true, true);
+      constexpr uint32_t idesc_dh = idesc_bf16_f32(2 * BM, BN, false, true);
       int s = 0, b = 0;
       uint32_t ph = 0, aph = 0;
       bool ok = true;
@@ -178,35 +197,36 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             break;
           }
           tc_fence_after();
-          const uint32_t a_addr = tiles + s * LG::STAGE_BYTES;
-          const uint32_t b_addr = a_addr + LG::A_BYTES;
+          const uint32_t a_addr = tiles + s * L::STAGE_BYTES;
+          const uint32_t b_addr = a_addr + L::A_BYTES;
 #pragma unroll
           for (int k = 0; k < BK / UMMA_K; ++k) {
             const uint64_t ad = is_dw ? sdesc_sw128(a_addr + k * 2048, 8192, 1024)
                                       : sdesc_sw128(a_addr + k * 32, 16, 1024);
             const uint64_t bd = sdesc_sw128(b_addr + k * 2048, 8192, 1024);
-            mma_bf16(d_tmem, ad, bd, is_dw ? idesc_dw : idesc_dh, (kb | k) != 0 ? 1u : 0u);
+            mma_bf16_pair(d_tmem, ad, bd, is_dw ? idesc_dw : idesc_dh, (kb | k) != 0 ? 1u : 0u);
           }
-          mma_commit(&ctrl->empty[s]);
-          if (++s == kStagesGrad) {
+          mma_commit_pair(&ctrl->empty[s], 0x3);
+          if (++s == STAGES) {
             s = 0;
             ph ^= 1u;
           }
         }
         if (!ok) break;
-        mma_commit(&ctrl->tfull[b]);
+        mma_commit_pair(&ctrl->tfull[b], 0x3);
         if (++b == 2) {
           b = 0;
           aph ^= 1u;
         }
       }
-      mma_commit(&ctrl->drain);
+      mma_commit_pair(&ctrl->drain, 0x1);
       mbar_drain(&ctrl->drain, 0, status);
     }
     __syncwarp();
   } else {
-    // ------------------------------------------------------------ epilogue
+    // ------------------------------------------------ epilogue (both CTAs)
     const int q = warp & 3;
+    const int cg = (warp - 2) / 4;
     const int row = q * 32 + lane;
     const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
     EpiState es{0u, 0, 0u};
@@ -219,11 +239,17 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       const int u = sch.units[i];
       const bool is_dw = u < p.n_dw;
       const int v = is_dw ? u : u - p.n_dw;
+      const int mt = (v / p.n_nt) * 2 + static_cast<int>(rank), nt = v % p.n_nt;
       const uint32_t taddr = lane_addr + static_cast<uint32_t>(b * BN);
-      if (is_dw) EpiDw::template apply<BN>(p.dw, v / p.n_nt, v % p.n_nt, row, taddr, es);
-      else EpiDh::template apply<BN>(p.dh, v / p.n_nt, v % p.n_nt, row, taddr, es);
+      if (is_dw) EpiDw::template apply<BN, NCG>(p.dw, mt, nt, row, taddr, es, cg);
+      else EpiDh::template apply<BN, NCG>(p.dh, mt, nt, row, taddr, es, cg);
       tc_fence_before();
-      mbar_arrive(&ctrl->tempty[b]);
+      __syncwarp();
+      if (lane == 0) {
+        const uint32_t te = smem_u32(&ctrl->tempty[b]);
+        if (rank == 0) mbar_arrive(&ctrl->tempty[b]);
+        else mbar_arrive_cluster(mapa_shared(te, 0));
+      }
       if (++b == 2) {
         b = 0;
         aph ^= 1u;
@@ -231,9 +257,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     }
   }
   __syncthreads();
+  cluster_sync_all();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, 2 * BN);
+    tmem_dealloc_pair(tmem_base, 2 * BN);
   }
 }
 
@@ -285,30 +312,32 @@ cudaError_t launch_grads(const CUtensorMap& tG_kmaj, const CUtensorMap& tWc_mn,
                          int* status, int num_sms, cudaStream_t stream) {
   GradBoth p;
   p.n_nt = (D + kBnGrad - 1) / kBnGrad;
-  p.n_dw = (C + BM - 1) / BM * p.n_nt;
-  const int n_dh = (T + BM - 1) / BM * p.n_nt;
+  p.n_dw = (C + 2 * BM - 1) / (2 * BM) * p.n_nt;
+  const int n_dh = (T + 2 * BM - 1) / (2 * BM) * p.n_nt;
   p.kb_dw = (T + BK - 1) / BK;
   p.kb_dh = (C + BK - 1) / BK;
   p.dh = EpiDh::Params{T, D, dH};
   p.dw = EpiDw::Params{C, D, V, accumulate, cand, dW, status};
   p.status = status;
-  const int ctas = std::min(num_sms, kSchedMaxCtas);
+  const int pairs = std::min(num_sms / 2, kSchedMaxCtas);
   // Running dW and dH tiles side by side pays when their B operands (H and
   // W_c) fit in L2 together; beyond that they evict each other and two
   // phase-separated launches are faster (measured on GB300: merged is 5-17%
   // faster at (T + C) * D * 2 = 41-72 MB, 10% slower at 138-177 MB).
   const double b_bytes = (static_cast<double>(T) + C) * D * 2.0;
   auto sch = b_bytes <= kMergedGradsMaxBBytes
-                 ? grad_schedule(p.n_dw, p.kb_dw, n_dh, p.kb_dh, ctas)
+                 ? grad_schedule(p.n_dw, p.kb_dw, n_dh, p.kb_dh, pairs)
                  : std::shared_ptr<const GradSched>();
   if (!sch) {  // two phase-separated round-robin launches
     cudaError_t e = launch_grad_h(tG_kmaj, tWc_mn, T, C, D, dH, status, num_sms, stream);
     if (e != cudaSuccess) return e;
     return launch_grad_w(tG_mn, tH_mn, T, C, D, V, accumulate, cand, dW, status, num_sms, stream);
   }
-  cudaError_t e = cudaFuncSetAttribute(k_grads, cudaFuncAttributeMaxDynamicSharedMemorySize, LG::TOTAL);
+  cudaError_t e =
+      cudaFuncSetAttribute(k_grads, cudaFuncAttributeMaxDynamicSharedMemorySize, LG2::TOTAL);
   if (e != cudaSuccess) return e;
-  k_grads<<<ctas, GEMM_THREADS, LG::TOTAL, stream>>>(tG_kmaj, tWc_mn, tG_mn, tH_mn, p, *sch);
+  k_grads<<<2 * pairs, 64 + 32 * kGradEpiWarps, LG2::TOTAL, stream>>>(tG_kmaj, tWc_mn, tG_mn, tH_mn,
+                                                                     p, *sch);
   return cudaGetLastError();
 }
 

@@ -8,6 +8,9 @@ namespace ss {
 
 constexpr int kStagesLogits = 4;
 
+// One CTA per 128 x 256 logit tile. (A CTA-pair variant with a 6-deep ring
+// and eight epilogue warps measured no faster here: this GEMM has K = D and
+// its operands stay in L2.)
 cudaError_t launch_forward_logits(const CUtensorMap& tH, const CUtensorMap& tWc, int T, int C,
                                   int D, const int32_t* slot, float2* part, float* tgt,
                                   int* status, int num_sms, cudaStream_t stream) {

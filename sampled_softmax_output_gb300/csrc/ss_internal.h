@@ -11,6 +11,7 @@ namespace ss {
 // Tile widths of the GEMMs (output columns per tile).
 constexpr int kBnLogits = 256;  // logit tiles: forward and softmax-gradient
 constexpr int kBnGrad = 256;    // dH and dW tiles along D
+constexpr int kFwdGroups = 1;    // softmax partials per row per logit tile
 
 struct GemmShape;
 
