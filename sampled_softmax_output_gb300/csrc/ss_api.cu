@@ -112,6 +112,7 @@ __global__ void __launch_bounds__(256) k_gather_rows(const uint16_t* __restrict_
                                                      const int32_t* __restrict__ cand, int C,
                                                      int V, int D, uint16_t* __restrict__ Wc,
                                                      int* status) {
+  pdl_enter();
   if (read_status(status) != 0) return;
   const int lane = threadIdx.x & 31;
   const int n16 = D / 8;
@@ -130,40 +131,45 @@ __global__ void __launch_bounds__(256) k_gather_rows(const uint16_t* __restrict_
 }
 
 // lse[t] = log sum over tiles of s_c * exp(m_c); loss[t] = lse[t] - tgt[t].
+// Eight threads per token: thread k folds tiles k, k + 8, ... online, then the
+// eight (max, sum) pairs are combined with shuffles. (-inf, 0) marks a tile
+// part without valid columns.
+constexpr int kMergeLanes = 8;
+
+__device__ __forceinline__ void lse_fold(float& M, float& S, float m, float s) {
+  if (m == -INFINITY) return;
+  const float nm = fmaxf(M, m);
+  S = S * expf(M - nm) + s * expf(m - nm);
+  M = nm;
+}
+
 __global__ void __launch_bounds__(256) k_lse_merge(const float2* __restrict__ part,
                                                    const float* __restrict__ tgt,
                                                    const int32_t* __restrict__ slot, int T, int C,
                                                    int n_ct, float* __restrict__ loss,
                                                    float* __restrict__ lse, int* status) {
+  pdl_enter();
   if (read_status(status) != 0) return;
-  const int t = blockIdx.x * blockDim.x + threadIdx.x;
-  if (t >= T) return;
+  const int gid = blockIdx.x * blockDim.x + threadIdx.x;
+  const int t = gid / kMergeLanes;
+  const int k = gid % kMergeLanes;
+  const bool valid = t < T;  // whole groups of 8 lanes share a token
+  float M = -INFINITY, S = 0.f;
+  if (valid)
+    for (int c = k; c < n_ct; c += kMergeLanes) {
+      const float2 q = part[static_cast<size_t>(c) * T + t];
+      lse_fold(M, S, q.x, q.y);
+    }
+#pragma unroll
+  for (int o = 1; o < kMergeLanes; o <<= 1) {
+    const float m2 = __shfl_xor_sync(0xffffffffu, M, o);
+    const float s2 = __shfl_xor_sync(0xffffffffu, S, o);
+    lse_fold(M, S, m2, s2);
+  }
+  if (!valid || k != 0) return;
   if (static_cast<unsigned>(__ldg(slot + t)) >= static_cast<unsigned>(C)) {
     set_status(status, SS_ERR_INDEX);
     return;
-  }
-  // one pass: online merge of the per-tile (max, sum) pairs, loads batched
-  float M = -INFINITY, S = 0.f;
-  int c = 0;
-  // (-inf, 0) marks a column group with no valid column: skipped
-  for (; c + 8 <= n_ct; c += 8) {
-    float2 q[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) q[i] = part[static_cast<size_t>(c + i) * T + t];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      if (q[i].x == -INFINITY) continue;
-      const float nm = fmaxf(M, q[i].x);
-      S = S * expf(M - nm) + q[i].y * expf(q[i].x - nm);
-      M = nm;
-    }
-  }
-  for (; c < n_ct; ++c) {
-    const float2 q = part[static_cast<size_t>(c) * T + t];
-    if (q.x == -INFINITY) continue;
-    const float nm = fmaxf(M, q.x);
-    S = S * expf(M - nm) + q.y * expf(q.x - nm);
-    M = nm;
   }
   const float l = M + logf(S);
   lse[t] = l;
@@ -173,6 +179,7 @@ __global__ void __launch_bounds__(256) k_lse_merge(const float2* __restrict__ pa
 // dW[cand[j], :] = 0 (the gradient of an empty batch).
 __global__ void __launch_bounds__(256) k_zero_rows(const int32_t* __restrict__ cand, int C, int V,
                                                    int D, float* __restrict__ dW, int* status) {
+  pdl_enter();
   if (read_status(status) != 0) return;
   const int lane = threadIdx.x & 31;
   const int warps = gridDim.x * (blockDim.x / 32);
@@ -332,11 +339,11 @@ ss_status ss_forward(const uint16_t* H, const uint16_t* W, const int32_t* cand,
   float* tgt = reinterpret_cast<float*>(ws + L.tgt);
 
   trace_pre(s, "gather_rows");
-  k_gather_rows<<<rows_grid(C, nsm), 256, 0, s>>>(W, cand, static_cast<int>(C),
-                                                   static_cast<int>(V), static_cast<int>(D), Wc,
-                                                   status);
+  cudaError_t eg = launch_pdl(k_gather_rows, dim3(rows_grid(C, nsm)), dim3(256), 0, s, W, cand,
+                              static_cast<int>(C), static_cast<int>(V), static_cast<int>(D), Wc,
+                              status);
   trace_post(s);
-  if (cudaError_t e0 = cudaGetLastError(); e0 != cudaSuccess) return fail("launch k_gather_rows", e0);
+  if (eg != cudaSuccess) return fail("launch k_gather_rows", eg);
 
   CUtensorMap tH, tWc;
   if (!make_map(&tH, H, D, T, D * 2, 64, 128) || !make_map(&tWc, Wc, D, C, D * 2, 64, kBnLogits))
@@ -347,12 +354,13 @@ ss_status ss_forward(const uint16_t* H, const uint16_t* W, const int32_t* cand,
                                               s);
   trace_post(s);
   if (e != cudaSuccess) return fail("launch gemm_forward_lse", e);
-  const int blocks = static_cast<int>((T + 255) / 256);
+  const int blocks = static_cast<int>((T * kMergeLanes + 255) / 256);
   trace_pre(s, "lse_merge");
-  k_lse_merge<<<blocks, 256, 0, s>>>(part, tgt, slot, static_cast<int>(T), static_cast<int>(C),
-                                     static_cast<int>(L.n_ct * kFwdGroups), loss, lse, status);
+  const cudaError_t em =
+      launch_pdl(k_lse_merge, dim3(blocks), dim3(256), 0, s, part, tgt, slot, static_cast<int>(T),
+                 static_cast<int>(C), static_cast<int>(L.n_ct * kFwdGroups), loss, lse, status);
   trace_post(s);
-  return cuda_status(cudaGetLastError(), "launch k_lse_merge");
+  return cuda_status(em, "launch k_lse_merge");
 }
 
 ss_status ss_backward(const uint16_t* H, const uint16_t* W, const int32_t* cand,
@@ -380,9 +388,10 @@ ss_status ss_backward(const uint16_t* H, const uint16_t* W, const int32_t* cand,
   if (T == 0) {
     if (!accumulate) {
       trace_pre(s, "zero_rows");
-      k_zero_rows<<<rows_grid(C, nsm), 256, 0, s>>>(cand, iC, iV, iD, dW, status);
+      const cudaError_t ez = launch_pdl(k_zero_rows, dim3(rows_grid(C, nsm)), dim3(256), 0, s,
+                                        cand, iC, iV, iD, dW, status);
       trace_post(s);
-      return cuda_status(cudaGetLastError(), "launch k_zero_rows");
+      return cuda_status(ez, "launch k_zero_rows");
     }
     return SS_OK;
   }
@@ -390,9 +399,10 @@ ss_status ss_backward(const uint16_t* H, const uint16_t* W, const int32_t* cand,
   uint16_t* G = reinterpret_cast<uint16_t*>(ws + L.g);
 
   trace_pre(s, "gather_rows");
-  k_gather_rows<<<rows_grid(C, nsm), 256, 0, s>>>(W, cand, iC, iV, iD, Wc, status);
+  cudaError_t eg = launch_pdl(k_gather_rows, dim3(rows_grid(C, nsm)), dim3(256), 0, s, W, cand, iC,
+                              iV, iD, Wc, status);
   trace_post(s);
-  if (cudaError_t e0 = cudaGetLastError(); e0 != cudaSuccess) return fail("launch k_gather_rows", e0);
+  if (eg != cudaSuccess) return fail("launch k_gather_rows", eg);
 
   CUtensorMap tH, tWc, tGk, tWcMn, tGmn, tHmn;
   const uint64_t gRow = static_cast<uint64_t>(L.ldG) * 2;
@@ -456,11 +466,11 @@ ss_status ss_forward_noalloc(const uint16_t* H, const uint16_t* W, const int32_t
   e = cudaMemsetAsync(status, 0, 2 * sizeof(int), s);
   if (e != cudaSuccess) return fail("cudaMemsetAsync(scratch status)", e);
   trace_pre(s, "gather_rows");
-  k_gather_rows<<<rows_grid(C, nsm), 256, 0, s>>>(W, cand, static_cast<int>(C),
-                                                   static_cast<int>(V), static_cast<int>(D), Wc,
-                                                   status);
+  cudaError_t eg = launch_pdl(k_gather_rows, dim3(rows_grid(C, nsm)), dim3(256), 0, s, W, cand,
+                              static_cast<int>(C), static_cast<int>(V), static_cast<int>(D), Wc,
+                              status);
   trace_post(s);
-  if (cudaError_t e0 = cudaGetLastError(); e0 != cudaSuccess) return fail("launch k_gather_rows", e0);
+  if (eg != cudaSuccess) return fail("launch k_gather_rows", eg);
   CUtensorMap tH, tWc;
   if (!make_map(&tH, H, D, T, D * 2, 64, 128) || !make_map(&tWc, Wc, D, C, D * 2, 64, kBnLogits))
     return fail("cuTensorMapEncodeTiled", cudaErrorInvalidValue);
@@ -470,11 +480,11 @@ ss_status ss_forward_noalloc(const uint16_t* H, const uint16_t* W, const int32_t
   trace_post(s);
   if (e != cudaSuccess) return fail("launch gemm_forward_lse", e);
   trace_pre(s, "lse_merge");
-  k_lse_merge<<<static_cast<int>((T + 255) / 256), 256, 0, s>>>(
-      part, tgt, slot, static_cast<int>(T), static_cast<int>(C),
-      static_cast<int>(L.n_ct * kFwdGroups), loss, lse, status);
+  e = launch_pdl(k_lse_merge, dim3(static_cast<int>((T * kMergeLanes + 255) / 256)), dim3(256), 0, s,
+                 part, tgt, slot, static_cast<int>(T), static_cast<int>(C),
+                 static_cast<int>(L.n_ct * kFwdGroups), loss, lse, status);
   trace_post(s);
-  if (cudaError_t e0 = cudaGetLastError(); e0 != cudaSuccess) return fail("launch k_lse_merge", e0);
+  if (e != cudaSuccess) return fail("launch k_lse_merge", e);
   if (status_host) {
     int32_t h[2] = {0, 0};
     e = cudaMemcpyAsync(h, status, sizeof h, cudaMemcpyDeviceToHost, s);

@@ -54,7 +54,7 @@ constexpr int kBins = 4096;   // 12-bit digits (the last digit has 8 bits)
 constexpr int kTieCap = SS_TIE_CAP;  // ranked exactly when the selected bin is this small
 // tie-list entries allocated: at least 2 and even, so that the arrays after it
 // stay 16-byte aligned for vector access
-constexpr int kTieSlots = ((kTieCap > 2 ? kTieCap : 2) + 1) & ~1;
+constexpr int kTieSlots = 2 * (((kTieCap > 2 ? kTieCap : 2) + 1) & ~1);  // own list + all lists
 
 __device__ __forceinline__ uint32_t negative_hash(uint64_t seed, uint32_t v) {
   uint64_t z = seed + (static_cast<uint64_t>(v) + 1ull) * 0x9E3779B97F4A7C15ull;
@@ -93,6 +93,22 @@ __device__ __forceinline__ uint32_t block_scan(uint32_t x, uint32_t* ws, uint32_
   return r;
 }
 
+// Warp 0: lane q < 8 fetches value q of the cluster (one DSMEM load each, in
+// parallel); returns (sum over q < r, total) on every lane of warp 0.
+template <class F>
+__device__ __forceinline__ void cluster_prefix(F&& fetch, int r, uint32_t* before, uint32_t* total) {
+  const int lane = threadIdx.x & 31;
+  const uint32_t x = lane < kClusterCtas ? fetch(lane) : 0u;
+  uint32_t incl = x;
+#pragma unroll
+  for (int o = 1; o < 8; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  *total = __shfl_sync(0xffffffffu, incl, kClusterCtas - 1);
+  *before = r > 0 ? __shfl_sync(0xffffffffu, incl, r - 1) : 0u;
+}
+
 struct Shared {
   uint32_t scan[33];
   int err;
@@ -109,6 +125,7 @@ struct Shared {
 __global__ void __cluster_dims__(kClusterCtas, 1, 1) __launch_bounds__(kCandThreads, 1)
     k_build_candidates(const int32_t* __restrict__ targets, int T, int V, int C, uint64_t seed,
                        int32_t* __restrict__ cand, int32_t* __restrict__ slot, int* hdr, int wpc) {
+  pdl_enter();
   cg::cluster_group cluster = cg::this_cluster();
   const int r = static_cast<int>(cluster.block_rank());
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -165,10 +182,11 @@ __global__ void __cluster_dims__(kClusterCtas, 1, 1) __launch_bounds__(kCandThre
     }
     *reinterpret_cast<uint4*>(bm + i) = o;
   }
-  if (tid == 0) {
-    int err = 0;
-    for (int q = 0; q < kClusterCtas; ++q) err |= cluster.map_shared_rank(&sh, q)->err;
-    sh.any_err = static_cast<uint32_t>(err);
+  if (warp == 0) {
+    uint32_t before, total;
+    cluster_prefix([&](int q) { return static_cast<uint32_t>(cluster.map_shared_rank(&sh, q)->err); },
+                   r, &before, &total);
+    if (lane == 0) sh.any_err = total;
   }
   __syncthreads();
   if (sh.any_err) {
@@ -197,15 +215,13 @@ __global__ void __cluster_dims__(kClusterCtas, 1, 1) __launch_bounds__(kCandThre
       atomicAdd(&hist[negative_hash(seed, static_cast<uint32_t>(v)) >> 20], 1u);
   }
   cluster.sync();  // S2: target counts and histograms complete
-  if (tid == 0) {
-    uint32_t U = 0, Uoff = 0;
-    for (int q = 0; q < kClusterCtas; ++q) {
-      const uint32_t u = cluster.map_shared_rank(&sh, q)->U_r;
-      U += u;
-      if (q < r) Uoff += u;
+  if (warp == 0) {
+    uint32_t before, total;
+    cluster_prefix([&](int q) { return cluster.map_shared_rank(&sh, q)->U_r; }, r, &before, &total);
+    if (lane == 0) {
+      sh.U = total;
+      sh.Uoff = before;
     }
-    sh.U = U;
-    sh.Uoff = Uoff;
   }
   __syncthreads();
   const uint32_t U = sh.U, Uoff = sh.Uoff;
@@ -275,18 +291,22 @@ __global__ void __cluster_dims__(kClusterCtas, 1, 1) __launch_bounds__(kCandThre
       if (tid == 0) sh.slice_sum = ssum;
       cluster.sync();  // slice totals complete (and peers are done with our histogram)
       // every CTA: which slice holds rank rem, then which bin inside it
-      if (tid == 0) {
-        uint32_t cum = 0, s = kClusterCtas - 1;
-        for (int q = 0; q < kClusterCtas; ++q) {
-          const uint32_t x = cluster.map_shared_rank(&sh, q)->slice_sum;
-          if (rem <= cum + x) {
-            s = static_cast<uint32_t>(q);
-            break;
-          }
-          cum += x;
+      if (warp == 0) {
+        // lane q < 8 holds slice q's total; find the slice where rank rem falls
+        const uint32_t x = lane < kClusterCtas ? cluster.map_shared_rank(&sh, lane)->slice_sum : 0u;
+        uint32_t incl = x;
+#pragma unroll
+        for (int o = 1; o < 8; o <<= 1) {
+          const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += y;
         }
-        sh.s_slice = s;
-        sh.s_rem = rem - cum;
+        const unsigned hit = __ballot_sync(0xffffffffu, lane < kClusterCtas && rem <= incl);
+        const int s = hit ? __ffs(hit) - 1 : kClusterCtas - 1;
+        const uint32_t cum = __shfl_sync(0xffffffffu, incl - x, s);
+        if (lane == 0) {
+          sh.s_slice = static_cast<uint32_t>(s);
+          sh.s_rem = rem - cum;
+        }
       }
       __syncthreads();
       const uint32_t s = sh.s_slice, srem = sh.s_rem;
@@ -350,18 +370,36 @@ __global__ void __cluster_dims__(kClusterCtas, 1, 1) __launch_bounds__(kCandThre
       if (collect) break;
     }
     if (level < 2) {
-      // the selected bin is small: rank its ids exactly by (hash, id)
+      // The selected bin is small: copy every CTA's list of its ids into
+      // local shared memory (after this CTA's own list), then rank this
+      // CTA's ids exactly by (hash, id).
       cluster.sync();
+      uint64_t* all = tie + sh.ntie;  // room: the bin holds at most kTieCap ids in total
+      __shared__ uint32_t s_off[kClusterCtas + 1];
+      if (warp == 0) {
+        const uint32_t n = lane < kClusterCtas ? cluster.map_shared_rank(&sh, lane)->ntie : 0u;
+        uint32_t incl = n;
+#pragma unroll
+        for (int o = 1; o < 8; o <<= 1) {
+          const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += y;
+        }
+        if (lane < kClusterCtas) s_off[lane] = incl - n;
+        if (lane == kClusterCtas - 1) s_off[kClusterCtas] = incl;
+      }
+      __syncthreads();
+      const uint32_t ntot = s_off[kClusterCtas];
+      for (uint32_t i = tid; i < ntot; i += kCandThreads) {
+        int q = 0;
+        while (q + 1 < kClusterCtas && s_off[q + 1] <= i) ++q;
+        all[i] = cluster.map_shared_rank(tie, q)[i - s_off[q]];
+      }
+      __syncthreads();
       const uint32_t mine = sh.ntie;
       for (uint32_t i = tid; i < mine; i += kCandThreads) {
         const uint64_t key = tie[i];
         uint32_t rank = 0;
-        for (int q = 0; q < kClusterCtas; ++q) {
-          const Shared* ps = cluster.map_shared_rank(&sh, q);
-          const uint64_t* pt = cluster.map_shared_rank(tie, q);
-          const uint32_t n = ps->ntie;
-          for (uint32_t j = 0; j < n; ++j) rank += pt[j] < key;
-        }
+        for (uint32_t j = 0; j < ntot; ++j) rank += all[j] < key;
         if (rank < rem) {
           const int v = static_cast<int>(key & 0xffffffffu);
           atomicOr(&sel[(v >> 5) - w0], 1u << (v & 31));
@@ -375,10 +413,11 @@ __global__ void __cluster_dims__(kClusterCtas, 1, 1) __launch_bounds__(kCandThre
       const uint32_t e_excl = block_scan(ecnt, sh.scan, &E_r);
       if (tid == 0) sh.E_r = E_r;
       cluster.sync();
-      if (tid == 0) {
-        uint32_t Eoff = 0;
-        for (int q = 0; q < r; ++q) Eoff += cluster.map_shared_rank(&sh, q)->E_r;
-        sh.Eoff = Eoff;
+      if (warp == 0) {
+        uint32_t before, total;
+        cluster_prefix([&](int q) { return cluster.map_shared_rank(&sh, q)->E_r; }, r, &before,
+                       &total);
+        if (lane == 0) sh.Eoff = before;
       }
       __syncthreads();
       uint32_t e = sh.Eoff + e_excl;
@@ -402,10 +441,10 @@ __global__ void __cluster_dims__(kClusterCtas, 1, 1) __launch_bounds__(kCandThre
   const uint32_t s_excl = block_scan(scnt, sh.scan, &S_r);
   if (tid == 0) sh.S_r = S_r;
   cluster.sync();  // S_r and every slice's word prefixes complete
-  if (tid == 0) {
-    uint32_t Soff = 0;
-    for (int q = 0; q < r; ++q) Soff += cluster.map_shared_rank(&sh, q)->S_r;
-    sh.Soff = Soff;
+  if (warp == 0) {
+    uint32_t before, total;
+    cluster_prefix([&](int q) { return cluster.map_shared_rank(&sh, q)->S_r; }, r, &before, &total);
+    if (lane == 0) sh.Soff = before;
   }
   // replicate the whole vocabulary's bitmap and word prefixes for the slots
   // (`local` is free: peers finished reading it before the second barrier)
@@ -468,9 +507,8 @@ cudaError_t launch_build_candidates(const int32_t* targets, int T, int V, int C,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  k_build_candidates<<<kClusterCtas, kCandThreads, smem, stream>>>(targets, T, V, C, seed, cand,
-                                                                    slot, hdr, words_per_cta(V));
-  return cudaGetLastError();
+  return launch_pdl(k_build_candidates, dim3(kClusterCtas), dim3(kCandThreads), smem, stream, targets,
+                    T, V, C, seed, cand, slot, hdr, words_per_cta(V));
 }
 
 }  // namespace ss

@@ -23,6 +23,7 @@
 
 #include <math.h>
 
+#include "ss_internal.h"
 #include "ss_ptx.cuh"
 
 namespace ss {
@@ -336,6 +337,7 @@ template <int BN, int STAGES, bool A_MN, bool B_MN, class Epi>
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
     k_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
            GemmShape shp, const __grid_constant__ typename Epi::Params ep, int* status) {
+  pdl_enter();
   static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "BN");
   static_assert(STAGES >= 2 && STAGES <= 8, "STAGES");
   using L = GemmSmem<BN, STAGES, Epi::kStageBytes>;
@@ -520,8 +522,7 @@ cudaError_t launch_gemm(const CUtensorMap& tA, const CUtensorMap& tB, GemmShape 
   const int units = shp.m_tiles * shp.n_tiles;
   if (units <= 0) return cudaSuccess;
   const int grid = units < num_sms ? units : num_sms;
-  kern<<<grid, GEMM_THREADS, smem, stream>>>(tA, tB, shp, ep, status);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3(grid), dim3(GEMM_THREADS), smem, stream, tA, tB, shp, ep, status);
 }
 
 }  // namespace ss

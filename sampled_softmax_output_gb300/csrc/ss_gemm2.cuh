@@ -44,6 +44,7 @@ template <int BN, int STAGES, bool A_MN, bool B_MN, class Epi, int EPI_WARPS>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * EPI_WARPS, 1)
     k_gemm2(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
             GemmShape shp, const __grid_constant__ typename Epi::Params ep, int* status) {
+  pdl_enter();
   static_assert(BN % 128 == 0 && BN >= 128 && BN <= 256, "BN");
   static_assert(STAGES >= 2 && STAGES <= 8, "STAGES");
   static_assert(EPI_WARPS == 4 || EPI_WARPS == 8, "EPI_WARPS");
@@ -255,8 +256,8 @@ cudaError_t launch_gemm2(const CUtensorMap& tA, const CUtensorMap& tB, GemmShape
   const int units = shp.m_tiles * shp.n_tiles;
   if (units <= 0) return cudaSuccess;
   const int pairs = units < num_sms / 2 ? units : num_sms / 2;
-  kern<<<2 * pairs, 64 + 32 * EPI_WARPS, smem, stream>>>(tA, tB, shp, ep, status);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3(2 * pairs), dim3(64 + 32 * EPI_WARPS), smem, stream, tA, tB, shp, ep,
+                    status);
 }
 
 }  // namespace ss

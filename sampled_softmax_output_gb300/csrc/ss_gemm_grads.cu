@@ -77,6 +77,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * kGradEpiWa
     k_grads(const __grid_constant__ CUtensorMap tmGk, const __grid_constant__ CUtensorMap tmWcMn,
             const __grid_constant__ CUtensorMap tmGmn, const __grid_constant__ CUtensorMap tmHmn,
             const __grid_constant__ GradBoth p, const __grid_constant__ GradSched sch) {
+  pdl_enter();
   constexpr int BN = kBnGrad;
   constexpr int STAGES = kStagesPairGrad;
   constexpr int NCG = kGradEpiWarps / 4;
@@ -336,9 +337,8 @@ cudaError_t launch_grads(const CUtensorMap& tG_kmaj, const CUtensorMap& tWc_mn,
   cudaError_t e =
       cudaFuncSetAttribute(k_grads, cudaFuncAttributeMaxDynamicSharedMemorySize, LG2::TOTAL);
   if (e != cudaSuccess) return e;
-  k_grads<<<2 * pairs, 64 + 32 * kGradEpiWarps, LG2::TOTAL, stream>>>(tG_kmaj, tWc_mn, tG_mn, tH_mn,
-                                                                     p, *sch);
-  return cudaGetLastError();
+  return launch_pdl(k_grads, dim3(2 * pairs), dim3(64 + 32 * kGradEpiWarps), LG2::TOTAL, stream,
+                    tG_kmaj, tWc_mn, tG_mn, tH_mn, p, *sch);
 }
 
 }  // namespace ss

@@ -6,7 +6,27 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <utility>
+
 namespace ss {
+
+// Launch with programmatic stream serialization: the kernel may be scheduled
+// while its predecessor in the stream drains, and waits for it in pdl_enter().
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
 
 // Tile widths of the GEMMs (output columns per tile).
 constexpr int kBnLogits = 256;  // logit tiles: forward and softmax-gradient

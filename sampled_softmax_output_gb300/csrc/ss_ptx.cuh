@@ -36,6 +36,16 @@ __device__ __forceinline__ int read_status(const int* status) {
   return *reinterpret_cast<const volatile int*>(status);
 }
 
+// --------------------------------------------- programmatic dependent launch
+// Every kernel of the library starts with pdl_enter(): wait until the grids it
+// depends on have completed and their writes are visible, then allow the next
+// kernel of the stream to be scheduled. Launched without the programmatic
+// attribute, both instructions do nothing.
+__device__ __forceinline__ void pdl_enter() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ------------------------------------------------------------------ mbarrier
 
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
