@@ -275,6 +275,10 @@ def run_native(args, world, rank, local):
     scale = 1.0 / T
 
     def step(h=H, tg=targets):
+        ss.step(h, W, tg, C, w.seed, ws, scale=scale, dW=dW, cand=cand, slot=slot, loss=loss,
+                lse=lse, dH=dH)
+
+    def step_three_calls(h=H, tg=targets):
         ss.build_candidates(tg, V, C, w.seed, ws, cand=cand, slot=slot)
         ss.forward(h, W, cand, slot, ws, loss=loss, lse=lse)
         ss.backward(h, W, cand, slot, lse, ws, scale=scale, dH=dH, dW=dW)
@@ -338,6 +342,20 @@ def run_native(args, world, rank, local):
             t_ends[k].record()
     torch.cuda.synchronize()
     traced_ms_per_step = sum(s.elapsed_time(e) for s, e in zip(t_starts, t_ends)) / Kt
+
+    # the same steps as three ABI calls (ss_build_candidates, ss_forward,
+    # ss_backward), untraced, for comparison
+    K3 = min(K, 300)
+    s3 = [torch.cuda.Event(enable_timing=True) for _ in range(K3)]
+    e3 = [torch.cuda.Event(enable_timing=True) for _ in range(K3)]
+    torch.cuda.synchronize()
+    for k in range(K3):
+        flush.zero_()
+        s3[k].record()
+        step_three_calls()
+        e3[k].record()
+    torch.cuda.synchronize()
+    three_calls_ms = sum(a.elapsed_time(b) for a, b in zip(s3, e3)) / K3
 
     # per-kernel times from the trace
     per = {}
@@ -403,7 +421,8 @@ def run_native(args, world, rank, local):
         "config": {"workload": w.name, "T": T, "V": V, "C": C, "D": D, "zipf_s": w.zipf_s,
                    "seed": w.seed, "parallelism": f"replicas x{world}" if world > 1 else "single",
                    "l2": "flushed between steps (256 MB write, outside the timed events)",
-                   "step": "ss_build_candidates + ss_forward + ss_backward",
+                   "step": "ss_step (= ss_build_candidates + ss_forward + ss_backward in one call)",
+                   "ms_per_step_three_calls": three_calls_ms,
                    "step_tflops_algorithmic_6TCD": step_tflops,
                    "pct_bf16_peak_algorithmic": 100.0 * step_tflops / peaks["bf16_tflops"]},
         "roofline": roof,

@@ -144,6 +144,19 @@ ss_status ss_backward(const uint16_t* H, const uint16_t* W, const int32_t* cand,
                       void* workspace, size_t workspace_bytes, ss_stream stream);
 
 /*
+ * One training step of the loss in a single call: ss_build_candidates (with
+ * U_host = NULL), ss_forward and ss_backward on the same batch, with the same
+ * arguments and results as those three calls. The candidate rows W[cand] are
+ * gathered once and serve both passes (the separate ss_backward gathers them
+ * again, since it cannot know whether W or cand changed after ss_forward).
+ * Pages: as for ss_forward and ss_backward.
+ */
+ss_status ss_step(const int32_t* targets, const uint16_t* H, const uint16_t* W, int64_t T,
+                  int64_t V, int64_t C, int64_t D, uint64_t seed, float scale, int accumulate,
+                  int32_t* cand, int32_t* slot, float* loss, float* lse, uint16_t* dH, float* dW,
+                  void* workspace, size_t workspace_bytes, ss_stream stream);
+
+/*
  * Allocation-free forward pass. Not part of the method on the pages (the
  * paper has no counterpart): an operational variant of ss_forward for callers
  * that cannot allocate device memory at all -- for example code running as a

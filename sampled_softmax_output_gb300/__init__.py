@@ -69,6 +69,9 @@ def _load():
     L.ss_read_status.argtypes = [p, sz, p, p, p]
     L.ss_status_string.restype = ctypes.c_char_p
     L.ss_status_string.argtypes = [ctypes.c_int]
+    L.ss_step.restype = ctypes.c_int
+    L.ss_step.argtypes = [p, p, p, i64, i64, i64, i64, ctypes.c_uint64, ctypes.c_float, ctypes.c_int,
+                          p, p, p, p, p, p, p, sz, p]
     L.ss_forward_noalloc.restype = ctypes.c_int
     L.ss_forward_noalloc.argtypes = [p, p, p, p, i64, i64, i64, i64, p, p, p, p]
     L.ss_last_error.restype = ctypes.c_char_p
@@ -297,8 +300,37 @@ class KernelTrace:
                 for k in range(min(self.count, self.capacity))]
 
 
-def step(H, W, targets, C: int, seed: int, ws, scale: float = 1.0, dW=None, accumulate=False):
-    """One full pass of the path: candidates, forward, backward."""
+def step(H, W, targets, C: int, seed: int, ws, scale: float = 1.0, dW=None, accumulate=False,
+         cand=None, slot=None, loss=None, lse=None, dH=None):
+    """One full pass of the path in one call (ss_step): candidates, forward,
+    backward, with one gather of the candidate rows shared by both passes."""
+    _need(H, "H", torch.bfloat16)
+    dev = H.device
+    T, D = H.shape
+    V = W.shape[0]
+    _need(W, "W", torch.bfloat16, dev, (V, D))
+    _need(targets, "targets", torch.int32, dev, (T,))
+    _need(ws, "workspace", torch.uint8, dev)
+    cand = torch.empty(C, dtype=torch.int32, device=dev) if cand is None else cand
+    slot = torch.empty(T, dtype=torch.int32, device=dev) if slot is None else slot
+    loss = torch.empty(T, dtype=torch.float32, device=dev) if loss is None else loss
+    lse = torch.empty(T, dtype=torch.float32, device=dev) if lse is None else lse
+    dH = torch.empty(T, D, dtype=torch.bfloat16, device=dev) if dH is None else dH
+    dW = torch.zeros(V, D, dtype=torch.float32, device=dev) if dW is None else dW
+    for t, name, dt, shape in ((cand, "cand", torch.int32, (C,)), (slot, "slot", torch.int32, (T,)),
+                               (loss, "loss", torch.float32, (T,)), (lse, "lse", torch.float32, (T,)),
+                               (dH, "dH", torch.bfloat16, (T, D)), (dW, "dW", torch.float32, (V, D))):
+        _need(t, name, dt, dev, shape)
+    code = _lib.ss_step(_ptr(targets), _ptr(H), _ptr(W), T, V, C, D, seed & (2**64 - 1),
+                        float(scale), 1 if accumulate else 0, _ptr(cand), _ptr(slot), _ptr(loss),
+                        _ptr(lse), _ptr(dH), _ptr(dW), _ptr(ws), ws.numel(), _stream(dev))
+    _check(code, "ss_step")
+    return {"cand": cand, "slot": slot, "loss": loss, "lse": lse, "dH": dH, "dW": dW}
+
+
+def step_separate(H, W, targets, C: int, seed: int, ws, scale: float = 1.0, dW=None,
+                  accumulate=False):
+    """The same pass as three calls: ss_build_candidates, ss_forward, ss_backward."""
     V = W.shape[0]
     cand, slot = build_candidates(targets, V, C, seed, ws)
     loss, lse = forward(H, W, cand, slot, ws)

@@ -275,6 +275,81 @@ cudaError_t noalloc_scratch_address(void** out) {
   return cudaSuccess;
 }
 
+// ------------------------------------------------------- launch sequences
+
+ss_status enqueue_gather(const uint16_t* W, const int32_t* cand, int64_t C, int64_t V, int64_t D,
+                         uint16_t* Wc, int* status, int nsm, cudaStream_t s) {
+  trace_pre(s, "gather_rows");
+  const cudaError_t e = launch_pdl(k_gather_rows, dim3(rows_grid(C, nsm)), dim3(256), 0, s, W, cand,
+                                   static_cast<int>(C), static_cast<int>(V), static_cast<int>(D),
+                                   Wc, status);
+  trace_post(s);
+  return e == cudaSuccess ? SS_OK : fail("launch k_gather_rows", e);
+}
+
+// forward GEMM (LSE partials, target logit) and the LSE merge, from W_c
+ss_status enqueue_forward(const uint16_t* H, const int32_t* slot, int64_t T, int64_t C, int64_t D,
+                          float* loss, float* lse, const Layout& L, char* ws, int nsm,
+                          cudaStream_t s) {
+  int* status = reinterpret_cast<int*>(ws + L.hdr);
+  uint16_t* Wc = reinterpret_cast<uint16_t*>(ws + L.wc);
+  float2* part = reinterpret_cast<float2*>(ws + L.part);
+  float* tgt = reinterpret_cast<float*>(ws + L.tgt);
+  CUtensorMap tH, tWc;
+  if (!make_map(&tH, H, D, T, D * 2, 64, 128) || !make_map(&tWc, Wc, D, C, D * 2, 64, kBnLogits))
+    return fail("cuTensorMapEncodeTiled", cudaErrorInvalidValue);
+  trace_pre(s, "gemm_forward_lse");
+  const cudaError_t e = launch_forward_logits(tH, tWc, static_cast<int>(T), static_cast<int>(C),
+                                              static_cast<int>(D), slot, part, tgt, status, nsm,
+                                              s);
+  trace_post(s);
+  if (e != cudaSuccess) return fail("launch gemm_forward_lse", e);
+  const int blocks = static_cast<int>((T * kMergeLanes + 255) / 256);
+  trace_pre(s, "lse_merge");
+  const cudaError_t em =
+      launch_pdl(k_lse_merge, dim3(blocks), dim3(256), 0, s, part, tgt, slot, static_cast<int>(T),
+                 static_cast<int>(C), static_cast<int>(L.n_ct * kFwdGroups), loss, lse, status);
+  trace_post(s);
+  return cuda_status(em, "launch k_lse_merge");
+}
+
+// softmax-gradient GEMM and the two gradient GEMMs, from W_c
+ss_status enqueue_backward(const uint16_t* H, const int32_t* cand, const int32_t* slot,
+                           const float* lse, int64_t T, int64_t V, int64_t C, int64_t D,
+                           float scale, int accumulate, uint16_t* dH, float* dW, const Layout& L,
+                           char* ws, int nsm, cudaStream_t s) {
+  int* status = reinterpret_cast<int*>(ws + L.hdr);
+  uint16_t* Wc = reinterpret_cast<uint16_t*>(ws + L.wc);
+  uint16_t* G = reinterpret_cast<uint16_t*>(ws + L.g);
+  const int iT = static_cast<int>(T), iV = static_cast<int>(V), iC = static_cast<int>(C),
+            iD = static_cast<int>(D);
+  CUtensorMap tH, tWc, tGk, tWcMn, tGmn, tHmn;
+  const uint64_t gRow = static_cast<uint64_t>(L.ldG) * 2;
+  if (!make_map(&tH, H, D, T, D * 2, 64, 128) || !make_map(&tWc, Wc, D, C, D * 2, 64, kBnLogits) ||
+      !make_map(&tGk, G, C, T, gRow, 64, 128) || !make_map(&tWcMn, Wc, D, C, D * 2, 64, 64) ||
+      !make_map(&tGmn, G, C, T, gRow, 64, 64) || !make_map(&tHmn, H, D, T, D * 2, 64, 64))
+    return fail("cuTensorMapEncodeTiled", cudaErrorInvalidValue);
+  trace_pre(s, "gemm_softmax_grad");
+  cudaError_t e = launch_softmax_grad(tH, tWc, tGk, iT, iC, iD, slot, lse, scale, status, nsm, s);
+  trace_post(s);
+  if (e != cudaSuccess) return fail("launch gemm_softmax_grad", e);
+  trace_pre(s, "gemm_grads");
+  e = launch_grads(tGk, tWcMn, tGmn, tHmn, iT, iC, iD, iV, accumulate, cand, dH, dW, status, nsm,
+                   s);
+  trace_post(s);
+  return e == cudaSuccess ? SS_OK : fail("launch gemm_grads", e);
+}
+
+ss_status enqueue_zero_rows(const int32_t* cand, int64_t C, int64_t V, int64_t D, float* dW,
+                            int* status, int nsm, cudaStream_t s) {
+  trace_pre(s, "zero_rows");
+  const cudaError_t e = launch_pdl(k_zero_rows, dim3(rows_grid(C, nsm)), dim3(256), 0, s, cand,
+                                   static_cast<int>(C), static_cast<int>(V), static_cast<int>(D),
+                                   dW, status);
+  trace_post(s);
+  return cuda_status(e, "launch k_zero_rows");
+}
+
 }  // namespace
 }  // namespace ss
 
@@ -333,34 +408,10 @@ ss_status ss_forward(const uint16_t* H, const uint16_t* W, const int32_t* cand,
   if (nsm <= 0) return fail("cudaGetDevice/cudaDeviceGetAttribute", cudaGetLastError());
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   char* ws = static_cast<char*>(workspace);
-  int* status = reinterpret_cast<int*>(ws + L.hdr);
-  uint16_t* Wc = reinterpret_cast<uint16_t*>(ws + L.wc);
-  float2* part = reinterpret_cast<float2*>(ws + L.part);
-  float* tgt = reinterpret_cast<float*>(ws + L.tgt);
-
-  trace_pre(s, "gather_rows");
-  cudaError_t eg = launch_pdl(k_gather_rows, dim3(rows_grid(C, nsm)), dim3(256), 0, s, W, cand,
-                              static_cast<int>(C), static_cast<int>(V), static_cast<int>(D), Wc,
-                              status);
-  trace_post(s);
-  if (eg != cudaSuccess) return fail("launch k_gather_rows", eg);
-
-  CUtensorMap tH, tWc;
-  if (!make_map(&tH, H, D, T, D * 2, 64, 128) || !make_map(&tWc, Wc, D, C, D * 2, 64, kBnLogits))
-    return fail("cuTensorMapEncodeTiled", cudaErrorInvalidValue);
-  trace_pre(s, "gemm_forward_lse");
-  const cudaError_t e = launch_forward_logits(tH, tWc, static_cast<int>(T), static_cast<int>(C),
-                                              static_cast<int>(D), slot, part, tgt, status, nsm,
-                                              s);
-  trace_post(s);
-  if (e != cudaSuccess) return fail("launch gemm_forward_lse", e);
-  const int blocks = static_cast<int>((T * kMergeLanes + 255) / 256);
-  trace_pre(s, "lse_merge");
-  const cudaError_t em =
-      launch_pdl(k_lse_merge, dim3(blocks), dim3(256), 0, s, part, tgt, slot, static_cast<int>(T),
-                 static_cast<int>(C), static_cast<int>(L.n_ct * kFwdGroups), loss, lse, status);
-  trace_post(s);
-  return cuda_status(em, "launch k_lse_merge");
+  const ss_status sg = enqueue_gather(W, cand, C, V, D, reinterpret_cast<uint16_t*>(ws + L.wc),
+                                      reinterpret_cast<int*>(ws + L.hdr), nsm, s);
+  if (sg != SS_OK) return sg;
+  return enqueue_forward(H, slot, T, C, D, loss, lse, L, ws, nsm, s);
 }
 
 ss_status ss_backward(const uint16_t* H, const uint16_t* W, const int32_t* cand,
@@ -382,45 +433,44 @@ ss_status ss_backward(const uint16_t* H, const uint16_t* W, const int32_t* cand,
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   char* ws = static_cast<char*>(workspace);
   int* status = reinterpret_cast<int*>(ws + L.hdr);
-  const int iT = static_cast<int>(T), iV = static_cast<int>(V), iC = static_cast<int>(C),
-            iD = static_cast<int>(D);
+  if (T == 0) return accumulate ? SS_OK : enqueue_zero_rows(cand, C, V, D, dW, status, nsm, s);
+  const ss_status sg =
+      enqueue_gather(W, cand, C, V, D, reinterpret_cast<uint16_t*>(ws + L.wc), status, nsm, s);
+  if (sg != SS_OK) return sg;
+  return enqueue_backward(H, cand, slot, lse, T, V, C, D, scale, accumulate, dH, dW, L, ws, nsm, s);
+}
 
-  if (T == 0) {
-    if (!accumulate) {
-      trace_pre(s, "zero_rows");
-      const cudaError_t ez = launch_pdl(k_zero_rows, dim3(rows_grid(C, nsm)), dim3(256), 0, s,
-                                        cand, iC, iV, iD, dW, status);
-      trace_post(s);
-      return cuda_status(ez, "launch k_zero_rows");
-    }
-    return SS_OK;
-  }
-  uint16_t* Wc = reinterpret_cast<uint16_t*>(ws + L.wc);
-  uint16_t* G = reinterpret_cast<uint16_t*>(ws + L.g);
-
-  trace_pre(s, "gather_rows");
-  cudaError_t eg = launch_pdl(k_gather_rows, dim3(rows_grid(C, nsm)), dim3(256), 0, s, W, cand, iC,
-                              iV, iD, Wc, status);
-  trace_post(s);
-  if (eg != cudaSuccess) return fail("launch k_gather_rows", eg);
-
-  CUtensorMap tH, tWc, tGk, tWcMn, tGmn, tHmn;
-  const uint64_t gRow = static_cast<uint64_t>(L.ldG) * 2;
-  if (!make_map(&tH, H, D, T, D * 2, 64, 128) || !make_map(&tWc, Wc, D, C, D * 2, 64, kBnLogits) ||
-      !make_map(&tGk, G, C, T, gRow, 64, 128) || !make_map(&tWcMn, Wc, D, C, D * 2, 64, 64) ||
-      !make_map(&tGmn, G, C, T, gRow, 64, 64) || !make_map(&tHmn, H, D, T, D * 2, 64, 64))
-    return fail("cuTensorMapEncodeTiled", cudaErrorInvalidValue);
-
-  trace_pre(s, "gemm_softmax_grad");
-  cudaError_t e = launch_softmax_grad(tH, tWc, tGk, iT, iC, iD, slot, lse, scale, status, nsm, s);
-  trace_post(s);
-  if (e != cudaSuccess) return fail("launch gemm_softmax_grad", e);
-  trace_pre(s, "gemm_grads");
-  e = launch_grads(tGk, tWcMn, tGmn, tHmn, iT, iC, iD, iV, accumulate, cand, dH, dW, status, nsm,
-                   s);
-  trace_post(s);
-  if (e != cudaSuccess) return fail("launch gemm_grads", e);
-  return SS_OK;
+ss_status ss_step(const int32_t* targets, const uint16_t* H, const uint16_t* W, int64_t T,
+                  int64_t V, int64_t C, int64_t D, uint64_t seed, float scale, int accumulate,
+                  int32_t* cand, int32_t* slot, float* loss, float* lse, uint16_t* dH, float* dW,
+                  void* workspace, size_t workspace_bytes, ss_stream stream) {
+  const ss_status st = check_sizes(T, V, C, D);
+  if (st != SS_OK) return st;
+  if (!W || !cand || !dW || !workspace ||
+      (T > 0 && (!targets || !H || !slot || !loss || !lse || !dH)))
+    return SS_ERR_INVALID;
+  if (!aligned(targets, 4) || !aligned(H, 16) || !aligned(W, 16) || !aligned(dH, 16) ||
+      !aligned(dW, 16) || !aligned(workspace, 16) || !aligned(cand, 4) || !aligned(slot, 4) ||
+      !aligned(loss, 4) || !aligned(lse, 4))
+    return SS_ERR_INVALID;
+  if (accumulate != 0 && accumulate != 1) return SS_ERR_INVALID;
+  const Layout L = make_layout(T, C, D);
+  if (workspace_bytes < L.total) return SS_ERR_WORKSPACE;
+  const ss_status sb = ss_build_candidates(targets, T, V, C, seed, cand, slot, nullptr, workspace,
+                                           workspace_bytes, stream);
+  if (sb != SS_OK) return sb;
+  const int nsm = num_sms_current();
+  if (nsm <= 0) return fail("cudaGetDevice/cudaDeviceGetAttribute", cudaGetLastError());
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  char* ws = static_cast<char*>(workspace);
+  int* status = reinterpret_cast<int*>(ws + L.hdr);
+  if (T == 0) return accumulate ? SS_OK : enqueue_zero_rows(cand, C, V, D, dW, status, nsm, s);
+  // one gather of W[cand] serves the forward and the backward
+  ss_status r = enqueue_gather(W, cand, C, V, D, reinterpret_cast<uint16_t*>(ws + L.wc), status, nsm, s);
+  if (r != SS_OK) return r;
+  r = enqueue_forward(H, slot, T, C, D, loss, lse, L, ws, nsm, s);
+  if (r != SS_OK) return r;
+  return enqueue_backward(H, cand, slot, lse, T, V, C, D, scale, accumulate, dH, dW, L, ws, nsm, s);
 }
 
 ss_status ss_forward_noalloc(const uint16_t* H, const uint16_t* W, const int32_t* cand,

@@ -50,7 +50,7 @@ struct GemmSmem {
 // Per-thread state the epilogue keeps across tiles.
 struct EpiState {
   uint32_t stage;   // shared address of the epilogue staging region
-  int ep_tid;       // 0..127 among the epilogue threads
+  int ep_tid;       // index among the epilogue threads
   uint32_t rounds;  // staging buffers used so far
 };
 
@@ -167,6 +167,7 @@ struct EpiFwd {
 // one-hot term touches one element per row: it is recomputed in fp32 and
 // patched into the staged tile.
 struct EpiG {
+  // two 16 KB staging buffers: both for one column group, one each for two
   static constexpr int kStageBytes = 2 * 16384;
   struct Params {
     CUtensorMap tmG;  // G [T, C] bf16 (row pitch ldG), box 64 x 128, 128-byte swizzle
@@ -178,12 +179,17 @@ struct EpiG {
     int* status;
   };
   __device__ static void finish(const Params&, EpiState& es) {
-    if (es.ep_tid == 0) bulk_wait<0>();
+    if ((es.ep_tid & 127) == 0) bulk_wait<0>();
   }
+  // Column group cg of NCG (four warps each) covers quarters
+  // [cg * 4 / NCG, (cg + 1) * 4 / NCG) of the tile with its own staging
+  // buffer(s), named barrier (1 + 2 * cg) and storing thread.
   template <int BN, int NCG>
   __device__ static void apply(const Params& p, int mt, int nt, int row, uint32_t taddr,
-                               EpiState& es, int) {
-    static_assert(NCG == 1, "the staged G epilogue runs with four epilogue warps");
+                               EpiState& es, int cg) {
+    static_assert(NCG == 1 || NCG == 2, "column groups");
+    const int bar = 1 + 2 * cg;
+    const bool leader = (es.ep_tid & 127) == 0;
     const int t = mt * BM + row;
     const bool valid = t < p.T;
     const int sl = valid ? __ldg(p.slot + t) : -1;
@@ -196,13 +202,18 @@ struct EpiG {
     const int ncols = min(BN, p.C - j0);
     const uint32_t r7 = static_cast<uint32_t>(row & 7);
 #pragma unroll 1
-    for (int q = 0; q < BN / 64; ++q) {
+    for (int q = cg * (BN / 64) / NCG; q < (cg + 1) * (BN / 64) / NCG; ++q) {
       const int qc = q * 64;
       if (qc >= ncols) break;  // uniform: depends on the tile only
-      const uint32_t buf = es.stage + (es.rounds & 1u) * 16384u;
-      // the store that used this buffer two rounds ago must have read it
-      if (es.rounds >= 2 && es.ep_tid == 0) bulk_wait_read<1>();
-      named_bar_sync(1, 128);
+      constexpr uint32_t kBufs = 2 / NCG;  // buffers per column group
+      const uint32_t buf = es.stage + static_cast<uint32_t>(cg) * 16384u * kBufs +
+                           (es.rounds % kBufs) * 16384u;
+      // the store that last used this buffer must have read it
+      if (es.rounds >= kBufs && leader) {
+        if constexpr (kBufs == 2) bulk_wait_read<1>();
+        else bulk_wait_read<0>();
+      }
+      named_bar_sync(bar, 128);
       const uint32_t rowbase = buf + static_cast<uint32_t>(row) * 128u;
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
@@ -239,8 +250,8 @@ struct EpiG {
         }
       }
       fence_proxy_async_smem();
-      named_bar_sync(1, 128);
-      if (es.ep_tid == 0) {
+      named_bar_sync(bar, 128);
+      if (leader) {
         tma_store_2d(&p.tmG, buf, j0 + qc, mt * BM);
         bulk_commit();
       }
@@ -333,13 +344,15 @@ struct EpiDw {
 
 // -------------------------------------------------------------------- kernel
 
-template <int BN, int STAGES, bool A_MN, bool B_MN, class Epi>
-__global__ void __launch_bounds__(GEMM_THREADS, 1)
+template <int BN, int STAGES, bool A_MN, bool B_MN, class Epi, int EPI_WARPS = 4>
+__global__ void __launch_bounds__(64 + 32 * EPI_WARPS, 1)
     k_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
            GemmShape shp, const __grid_constant__ typename Epi::Params ep, int* status) {
   pdl_enter();
   static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "BN");
   static_assert(STAGES >= 2 && STAGES <= 8, "STAGES");
+  static_assert(EPI_WARPS == 4 || EPI_WARPS == 8, "EPI_WARPS");
+  constexpr int NCG = EPI_WARPS / 4;
   using L = GemmSmem<BN, STAGES, Epi::kStageBytes>;
   extern __shared__ uint8_t smem_raw[];
   __shared__ int s_go;
@@ -363,7 +376,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&ctrl->tfull[b], 1);
-      mbar_init(&ctrl->tempty[b], 4 * 32);
+      mbar_init(&ctrl->tempty[b], EPI_WARPS * 32);
     }
     mbar_init(&ctrl->drain, 1);
     ctrl->abort_flag = 0;
@@ -473,7 +486,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------ epilogue
-    const int q = warp & 3;
+    const int q = warp & 3;         // TMEM lane quarter this warp may access
+    const int cg = (warp - 2) / 4;  // column group
     const int row = q * 32 + lane;
     const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
     EpiState es{tiles + L::EPI_OFFSET, static_cast<int>(threadIdx.x) - 64, 0u};
@@ -483,17 +497,21 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       const bool ok = mbar_wait(&ctrl->tfull[b], aph, abort_flag, status);
       bool go = __all_sync(0xffffffffu, ok);
       if constexpr (Epi::kStageBytes > 0) {
-        // This epilogue synchronises its four warps with named barriers, so
-        // they must leave the loop together: vote every tile.
-        if (lane == 0) ctrl->vote[(u / gridDim.x) & 1][q] = go ? 1 : 0;
-        named_bar_sync(2, 128);
+        // This epilogue synchronises its warps with named barriers, so they
+        // must leave the loop together: vote every tile.
+        if (lane == 0) ctrl->vote[(u / gridDim.x) & 1][warp - 2] = go ? 1 : 0;
+        named_bar_sync(2, 32 * EPI_WARPS);
         const int* v = ctrl->vote[(u / gridDim.x) & 1];
-        go = (v[0] & v[1] & v[2] & v[3]) != 0;
+        int all = 1;
+#pragma unroll
+        for (int i = 0; i < EPI_WARPS; ++i) all &= v[i];
+        go = all != 0;
       }
       if (!go) break;
       tc_fence_after();
       const int mt = u / shp.n_tiles, nt = u % shp.n_tiles;
-      Epi::template apply<BN, 1>(ep, mt, nt, row, lane_addr + static_cast<uint32_t>(b * BN), es, 0);
+      Epi::template apply<BN, NCG>(ep, mt, nt, row, lane_addr + static_cast<uint32_t>(b * BN), es,
+                                   cg);
       tc_fence_before();
       mbar_arrive(&ctrl->tempty[b]);
       if (++b == 2) {
@@ -511,18 +529,19 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
 }
 
 // Host-side launcher: grid = min(units, SMs), one CTA per SM.
-template <int BN, int STAGES, bool A_MN, bool B_MN, class Epi>
+template <int BN, int STAGES, bool A_MN, bool B_MN, class Epi, int EPI_WARPS = 4>
 cudaError_t launch_gemm(const CUtensorMap& tA, const CUtensorMap& tB, GemmShape shp,
                         const typename Epi::Params& ep, int* status, int num_sms,
                         cudaStream_t stream) {
-  auto kern = k_gemm<BN, STAGES, A_MN, B_MN, Epi>;
+  auto kern = k_gemm<BN, STAGES, A_MN, B_MN, Epi, EPI_WARPS>;
   constexpr int smem = GemmSmem<BN, STAGES, Epi::kStageBytes>::TOTAL;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const int units = shp.m_tiles * shp.n_tiles;
   if (units <= 0) return cudaSuccess;
   const int grid = units < num_sms ? units : num_sms;
-  return launch_pdl(kern, dim3(grid), dim3(GEMM_THREADS), smem, stream, tA, tB, shp, ep, status);
+  return launch_pdl(kern, dim3(grid), dim3(64 + 32 * EPI_WARPS), smem, stream, tA, tB, shp, ep,
+                    status);
 }
 
 }  // namespace ss

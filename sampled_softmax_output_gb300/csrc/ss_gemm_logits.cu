@@ -34,8 +34,9 @@ cudaError_t launch_softmax_grad(const CUtensorMap& tH, const CUtensorMap& tWc,
   ep.scale = scale;
   ep.log2_scale = scale == 0.f ? -INFINITY : log2f(fabsf(scale));
   ep.status = status;
-  return launch_gemm<kBnLogits, kStagesLogits, false, false, EpiG>(tH, tWc, shp, ep, status,
-                                                                   num_sms, stream);
+  // eight epilogue warps in two column groups, one staging buffer each
+  return launch_gemm<kBnLogits, kStagesLogits, false, false, EpiG, 8>(tH, tWc, shp, ep, status,
+                                                                      num_sms, stream);
 }
 
 }  // namespace ss

@@ -18,7 +18,7 @@ def test_exports_every_declared_symbol():
     assert set(names) == {"ss_workspace_size", "ss_build_candidates", "ss_forward",
                           "ss_backward", "ss_read_status", "ss_status_string",
                           "ss_trace_begin", "ss_trace_end", "ss_trace_kernel_name",
-                          "ss_last_error", "ss_forward_noalloc"}
+                          "ss_last_error", "ss_forward_noalloc", "ss_step"}
     for n in names:
         assert hasattr(ss.lib(), n), n
 
@@ -105,6 +105,25 @@ def test_null_and_alignment_errors():
     for k in ("targets", "cand", "slot", "ws"):
         assert _cand(**{k: 0}) == INVALID, k
     assert _cand(targets=FAKE + 1) == INVALID
+
+
+def _step(**kw):
+    a = dict(targets=FAKE, H=FAKE, W=FAKE, T=256, V=50304, C=4096, D=768, seed=0, scale=1.0, acc=0,
+             cand=FAKE, slot=FAKE, loss=FAKE, lse=FAKE, dH=FAKE, dW=FAKE, ws=FAKE, wsb=1 << 40)
+    a.update(kw)
+    return ss.lib().ss_step(p(a["targets"]), p(a["H"]), p(a["W"]), a["T"], a["V"], a["C"], a["D"],
+                            a["seed"], a["scale"], a["acc"], p(a["cand"]), p(a["slot"]),
+                            p(a["loss"]), p(a["lse"]), p(a["dH"]), p(a["dW"]), p(a["ws"]),
+                            a["wsb"], None)
+
+
+def test_step_argument_errors():
+    assert _step(C=0) == INVALID and _step(D=100) == UNSUPPORTED
+    for k in ("targets", "H", "W", "cand", "slot", "loss", "lse", "dH", "dW", "ws"):
+        assert _step(**{k: 0}) == INVALID, k
+    assert _step(H=FAKE + 8) == INVALID and _step(acc=3) == INVALID
+    need = ss.lib().ss_workspace_size(256, 50304, 4096, 768)
+    assert _step(wsb=need - 1) == WORKSPACE
 
 
 def test_workspace_too_small():

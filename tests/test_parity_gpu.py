@@ -226,15 +226,37 @@ def test_empty_batch():
     assert np.all(d[np.setdiff1d(np.arange(V), c)] == 3.0)
 
 
+def test_fused_step_equals_separate_calls(orc):
+    # ss_step runs the same kernels on the same data: bit-identical results
+    T, V, D, C, seed = 700, 6000, 768, 1500, 21
+    x, C = _case(T, V, D, C, seed)
+    H, W, tg = to_dev_bf16(x["H"]), to_dev_bf16(x["W"]), _dev(x["targets"])
+    ws = ss.workspace(T, V, C, D)
+    a = ss.step(H, W, tg, C, seed, ws, scale=0.5)
+    a = {k: v.clone() for k, v in a.items()}
+    b = ss.step_separate(H, W, tg, C, seed, ws, scale=0.5)
+    torch.cuda.synchronize()
+    for k in ("cand", "slot", "loss", "lse", "dH", "dW"):
+        assert torch.equal(a[k], b[k]), k
+    ref = _full_oracle(orc, x, C, seed, 0.5)
+    assert_loss_close(a["loss"].cpu().numpy(), ref["loss"])
+    assert rel_fro(a["dW"].cpu().numpy(), ref["dW"]) < GRAD_RTOL
+
+
 def test_kernel_trace_records_every_launch():
     T, V, D, C = 300, 3000, 768, 517
     x, C = _case(T, V, D, C, 4)
     H, W = to_dev_bf16(x["H"]), to_dev_bf16(x["W"])
     ws = ss.workspace(T, V, C, D)
     with ss.KernelTrace(capacity=16) as tr:
-        ss.step(H, W, _dev(x["targets"]), C, 4, ws)
+        ss.step_separate(H, W, _dev(x["targets"]), C, 4, ws)
     torch.cuda.synchronize()
     names = [n for n, _ in tr.timings()]
     assert names == ["build_candidates", "gather_rows", "gemm_forward_lse", "lse_merge",
                      "gather_rows", "gemm_softmax_grad", "gemm_grads"]
+    with ss.KernelTrace(capacity=16) as tr:
+        ss.step(H, W, _dev(x["targets"]), C, 4, ws)
+    torch.cuda.synchronize()
+    assert [n for n, _ in tr.timings()] == ["build_candidates", "gather_rows", "gemm_forward_lse",
+                                           "lse_merge", "gemm_softmax_grad", "gemm_grads"]
     assert all(ms > 0 for _, ms in tr.timings())
