@@ -102,6 +102,7 @@ __device__ __forceinline__ void for_tmem_chunks(uint32_t taddr, int c_begin, F&&
 //   comes from the group that holds slot[t].
 struct EpiFwd {
   static constexpr int kStageBytes = 0;
+  static constexpr bool kKeepOperands = false;
   struct Params {
     int T, C;
     const int32_t* slot;
@@ -169,6 +170,8 @@ struct EpiFwd {
 struct EpiG {
   // two 16 KB staging buffers: both for one column group, one each for two
   static constexpr int kStageBytes = 2 * 16384;
+  // G streams through L2 once; the H and W_c tiles are re-read by every CTA
+  static constexpr bool kKeepOperands = true;
   struct Params {
     CUtensorMap tmG;  // G [T, C] bf16 (row pitch ldG), box 64 x 128, 128-byte swizzle
     int T, C;
@@ -252,7 +255,7 @@ struct EpiG {
       fence_proxy_async_smem();
       named_bar_sync(bar, 128);
       if (leader) {
-        tma_store_2d(&p.tmG, buf, j0 + qc, mt * BM);
+        tma_store_2d_hint(&p.tmG, buf, j0 + qc, mt * BM, l2_evict_first());
         bulk_commit();
       }
       ++es.rounds;
@@ -263,6 +266,7 @@ struct EpiG {
 // Backward, step 2: dH tile -> bf16 (column group cg of NCG).
 struct EpiDh {
   static constexpr int kStageBytes = 0;
+  static constexpr bool kKeepOperands = false;
   struct Params {
     int T, D;
     uint16_t* dH;
@@ -299,6 +303,7 @@ struct EpiDh {
 // threads write one row.
 struct EpiDw {
   static constexpr int kStageBytes = 0;
+  static constexpr bool kKeepOperands = false;
   struct Params {
     int C, D, V, accumulate;
     const int32_t* cand;
@@ -412,19 +417,26 @@ __global__ void __launch_bounds__(64 + 32 * EPI_WARPS, 1)
           mbar_arrive_expect_tx(fb, L::STAGE_BYTES);
           const uint32_t a_dst = tiles + s * L::STAGE_BYTES;
           const uint32_t b_dst = a_dst + L::A_BYTES;
-          if (A_MN) {
-#pragma unroll
-            for (int i = 0; i < BM / 64; ++i)
-              tma_load_2d(a_dst + i * 8192, &tmA, fb, mt * BM + 64 * i, kb * BK);
+          if constexpr (Epi::kKeepOperands) {
+            static_assert(!A_MN && !B_MN, "cache-hinted loads are K-major");
+            const uint64_t pol = l2_evict_last();
+            tma_load_2d_hint(a_dst, &tmA, fb, kb * BK, mt * BM, pol);
+            tma_load_2d_hint(b_dst, &tmB, fb, kb * BK, nt * BN, pol);
           } else {
-            tma_load_2d(a_dst, &tmA, fb, kb * BK, mt * BM);
-          }
-          if (B_MN) {
+            if (A_MN) {
 #pragma unroll
-            for (int i = 0; i < BN / 64; ++i)
-              tma_load_2d(b_dst + i * 8192, &tmB, fb, nt * BN + 64 * i, kb * BK);
-          } else {
-            tma_load_2d(b_dst, &tmB, fb, kb * BK, nt * BN);
+              for (int i = 0; i < BM / 64; ++i)
+                tma_load_2d(a_dst + i * 8192, &tmA, fb, mt * BM + 64 * i, kb * BK);
+            } else {
+              tma_load_2d(a_dst, &tmA, fb, kb * BK, mt * BM);
+            }
+            if (B_MN) {
+#pragma unroll
+              for (int i = 0; i < BN / 64; ++i)
+                tma_load_2d(b_dst + i * 8192, &tmB, fb, nt * BN + 64 * i, kb * BK);
+            } else {
+              tma_load_2d(b_dst, &tmB, fb, kb * BK, nt * BN);
+            }
           }
           issued |= 1u << s;
           issued_ph = (issued_ph & ~(1u << s)) | (ph << s);

@@ -124,12 +124,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * EPI_WARPS,
           } else {
             tma_load_2d_pair(a_dst, &tmA, fb, kb * BK, m0);
           }
+          // B is re-read by every row tile: keep it in L2
+          const uint64_t keep = l2_evict_last();
           if (B_MN) {
 #pragma unroll
             for (int i = 0; i < BN / 128; ++i)
-              tma_load_2d_pair(b_dst + i * 8192, &tmB, fb, n0 + 64 * i, kb * BK);
+              tma_load_2d_pair_hint(b_dst + i * 8192, &tmB, fb, n0 + 64 * i, kb * BK, keep);
           } else {
-            tma_load_2d_pair(b_dst, &tmB, fb, kb * BK, n0);
+            tma_load_2d_pair_hint(b_dst, &tmB, fb, kb * BK, n0, keep);
           }
           issued |= 1u << s;
           issued_ph = (issued_ph & ~(1u << s)) | (ph << s);

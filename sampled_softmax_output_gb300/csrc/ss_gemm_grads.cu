@@ -150,15 +150,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * kGradEpiWa
           const uint32_t fb = rank == 0 ? fb_local : mapa_shared(fb_local, 0);
           const uint32_t a_dst = tiles + s * L::STAGE_BYTES;
           const uint32_t b_dst = a_dst + L::A_BYTES;
+          // B (H or W_c) is re-read by every row tile: keep it in L2
+          const uint64_t keep = l2_evict_last();
           if (is_dw) {  // A = G columns (MN-major), B = H (MN-major); K = tokens
             tma_load_2d_pair(a_dst, &tmGmn, fb, m0, kb * BK);
             tma_load_2d_pair(a_dst + 8192, &tmGmn, fb, m0 + 64, kb * BK);
-            tma_load_2d_pair(b_dst, &tmHmn, fb, n0, kb * BK);
-            tma_load_2d_pair(b_dst + 8192, &tmHmn, fb, n0 + 64, kb * BK);
+            tma_load_2d_pair_hint(b_dst, &tmHmn, fb, n0, kb * BK, keep);
+            tma_load_2d_pair_hint(b_dst + 8192, &tmHmn, fb, n0 + 64, kb * BK, keep);
           } else {      // A = G rows (K-major), B = W_c (MN-major); K = candidates
             tma_load_2d_pair(a_dst, &tmGk, fb, kb * BK, m0);
-            tma_load_2d_pair(b_dst, &tmWcMn, fb, n0, kb * BK);
-            tma_load_2d_pair(b_dst + 8192, &tmWcMn, fb, n0 + 64, kb * BK);
+            tma_load_2d_pair_hint(b_dst, &tmWcMn, fb, n0, kb * BK, keep);
+            tma_load_2d_pair_hint(b_dst + 8192, &tmWcMn, fb, n0 + 64, kb * BK, keep);
           }
           issued |= 1u << s;
           issued_ph = (issued_ph & ~(1u << s)) | (ph << s);
