@@ -155,10 +155,17 @@ __global__ void __launch_bounds__(256) k_lse_merge(const float2* __restrict__ pa
   const int k = gid % kMergeLanes;
   const bool valid = t < T;  // whole groups of 8 lanes share a token
   float M = -INFINITY, S = 0.f;
+  constexpr int kBatch = 8;  // loads a thread has in flight
   if (valid)
-    for (int c = k; c < n_ct; c += kMergeLanes) {
-      const float2 q = part[static_cast<size_t>(c) * T + t];
-      lse_fold(M, S, q.x, q.y);
+    for (int c0 = k; c0 < n_ct; c0 += kMergeLanes * kBatch) {
+      float2 q[kBatch];
+#pragma unroll
+      for (int i = 0; i < kBatch; ++i) {
+        const int c = c0 + i * kMergeLanes;
+        q[i] = c < n_ct ? __ldcg(part + static_cast<size_t>(c) * T + t) : make_float2(-INFINITY, 0.f);
+      }
+#pragma unroll
+      for (int i = 0; i < kBatch; ++i) lse_fold(M, S, q[i].x, q[i].y);
     }
 #pragma unroll
   for (int o = 1; o < kMergeLanes; o <<= 1) {
@@ -323,14 +330,16 @@ ss_status enqueue_backward(const uint16_t* H, const int32_t* cand, const int32_t
   uint16_t* G = reinterpret_cast<uint16_t*>(ws + L.g);
   const int iT = static_cast<int>(T), iV = static_cast<int>(V), iC = static_cast<int>(C),
             iD = static_cast<int>(D);
-  CUtensorMap tH, tWc, tGk, tWcMn, tGmn, tHmn;
+  CUtensorMap tH, tWc, tWc2, tGk, tWcMn, tGmn, tHmn;
   const uint64_t gRow = static_cast<uint64_t>(L.ldG) * 2;
   if (!make_map(&tH, H, D, T, D * 2, 64, 128) || !make_map(&tWc, Wc, D, C, D * 2, 64, kBnLogits) ||
+      !make_map(&tWc2, Wc, D, C, D * 2, 64, kBnLogits / 2) ||
       !make_map(&tGk, G, C, T, gRow, 64, 128) || !make_map(&tWcMn, Wc, D, C, D * 2, 64, 64) ||
       !make_map(&tGmn, G, C, T, gRow, 64, 64) || !make_map(&tHmn, H, D, T, D * 2, 64, 64))
     return fail("cuTensorMapEncodeTiled", cudaErrorInvalidValue);
   trace_pre(s, "gemm_softmax_grad");
-  cudaError_t e = launch_softmax_grad(tH, tWc, tGk, iT, iC, iD, slot, lse, scale, status, nsm, s);
+  cudaError_t e =
+      launch_softmax_grad(tH, tWc, tWc2, tGk, iT, iC, iD, slot, lse, scale, status, nsm, s);
   trace_post(s);
   if (e != cudaSuccess) return fail("launch gemm_softmax_grad", e);
   trace_pre(s, "gemm_grads");

@@ -17,7 +17,6 @@
 
 namespace ss {
 
-constexpr int kStagesGrad = 4;
 
 cudaError_t launch_grad_h(const CUtensorMap& tG_kmaj, const CUtensorMap& tWc_mn, int T, int C,
                           int D, uint16_t* dH, int* status, int num_sms, cudaStream_t stream) {
@@ -52,7 +51,6 @@ cudaError_t launch_grad_w(const CUtensorMap& tG_mn, const CUtensorMap& tH_mn, in
 namespace {
 
 constexpr int kSchedMaxCtas = 256;
-constexpr double kMergedGradsMaxBBytes = 96.0 * (1 << 20);
 constexpr int kSchedMaxUnits = 14080;
 
 struct GradSched {
@@ -327,8 +325,7 @@ cudaError_t launch_grads(const CUtensorMap& tG_kmaj, const CUtensorMap& tWc_mn,
   // W_c) fit in L2 together; beyond that they evict each other and two
   // phase-separated launches are faster (measured on GB300: merged is 5-17%
   // faster at (T + C) * D * 2 = 41-72 MB, 10% slower at 138-177 MB).
-  const double b_bytes = (static_cast<double>(T) + C) * D * 2.0;
-  auto sch = b_bytes <= kMergedGradsMaxBBytes
+  auto sch = !operands_exceed_l2(T, C, D)
                  ? grad_schedule(p.n_dw, p.kb_dw, n_dh, p.kb_dh, pairs)
                  : std::shared_ptr<const GradSched>();
   if (!sch) {  // two phase-separated round-robin launches

@@ -2,15 +2,16 @@
 // (K = D): the forward pass (log-sum-exp partials, target logit) and the
 // backward recompute (softmax gradient G in bf16). Neither writes S itself.
 #include "ss_gemm.cuh"
+#include "ss_gemm2.cuh"
 #include "ss_internal.h"
 
 namespace ss {
 
 constexpr int kStagesLogits = 4;
 
-// One CTA per 128 x 256 logit tile. (A CTA-pair variant with a 6-deep ring
-// and eight epilogue warps measured no faster here: this GEMM has K = D and
-// its operands stay in L2.)
+// One CTA per 128 x 256 logit tile. (CTA pairs on 256 x 256 tiles with a
+// 6-deep ring measured slower or even on GB300 at every size tried: this GEMM's
+// epilogue is light and K = D is short.)
 cudaError_t launch_forward_logits(const CUtensorMap& tH, const CUtensorMap& tWc, int T, int C,
                                   int D, const int32_t* slot, float2* part, float* tgt,
                                   int* status, int num_sms, cudaStream_t stream) {
@@ -21,10 +22,10 @@ cudaError_t launch_forward_logits(const CUtensorMap& tH, const CUtensorMap& tWc,
 }
 
 cudaError_t launch_softmax_grad(const CUtensorMap& tH, const CUtensorMap& tWc,
+                                const CUtensorMap& tWc_half,
                                 const CUtensorMap& tG_store, int T, int C, int D,
                                 const int32_t* slot, const float* lse, float scale,
                                 int* status, int num_sms, cudaStream_t stream) {
-  GemmShape shp{(T + BM - 1) / BM, (C + kBnLogits - 1) / kBnLogits, D / BK};
   EpiG::Params ep;
   ep.tmG = tG_store;
   ep.T = T;
@@ -34,7 +35,17 @@ cudaError_t launch_softmax_grad(const CUtensorMap& tH, const CUtensorMap& tWc,
   ep.scale = scale;
   ep.log2_scale = scale == 0.f ? -INFINITY : log2f(fabsf(scale));
   ep.status = status;
-  // eight epilogue warps in two column groups, one staging buffer each
+  // eight epilogue warps in two column groups, one staging buffer each; CTA
+  // pairs (each SM stages half of the W_c tile, a 6-deep ring beside the G
+  // staging) once the operands exceed L2 (measured on GB300: the pair is 5%
+  // slower at (T + C) * D * 2 = 41 MB, 2-3% faster at 138 and 177 MB)
+  const int n_tiles = (C + kBnLogits - 1) / kBnLogits;
+  if (operands_exceed_l2(T, C, D)) {
+    GemmShape shp{(T + 2 * BM - 1) / (2 * BM), n_tiles, D / BK};
+    return launch_gemm2<kBnLogits, 6, false, false, EpiG, 8>(tH, tWc_half, shp, ep, status,
+                                                             num_sms, stream);
+  }
+  GemmShape shp{(T + BM - 1) / BM, n_tiles, D / BK};
   return launch_gemm<kBnLogits, kStagesLogits, false, false, EpiG, 8>(tH, tWc, shp, ep, status,
                                                                       num_sms, stream);
 }

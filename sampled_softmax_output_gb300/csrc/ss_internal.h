@@ -35,17 +35,29 @@ constexpr int kFwdGroups = 1;    // softmax partials per row per logit tile
 
 struct GemmShape;
 
+// Above this size, H [T, D] and W_c [C, D] together (bf16) no longer stay in
+// L2 while a GEMM sweeps over them. The softmax-gradient GEMM then runs on
+// CTA pairs (each SM loads half of every W_c tile) and the two gradient GEMMs
+// in two phase-separated launches.
+constexpr double kL2OperandBytes = 96.0 * (1 << 20);
+inline bool operands_exceed_l2(int T, int C, int D) {
+  return (static_cast<double>(T) + C) * D * 2.0 > kL2OperandBytes;
+}
+
 // ---- candidate build (ss_candidates.cu)
 size_t build_candidates_smem_bytes(int64_t V);
 cudaError_t launch_build_candidates(const int32_t* targets, int T, int V, int C, uint64_t seed,
                                     int32_t* cand, int32_t* slot, int* hdr, cudaStream_t stream);
 
 // ---- logit GEMMs (ss_gemm_logits.cu): A = H [T, D] (K-major), B = W_c [C, D] (K-major)
+// tWc: box 64 x 256 (one 1-CTA tile); tWc_half: box 64 x 128 (a CTA's half of
+// a pair's tile).
 cudaError_t launch_forward_logits(const CUtensorMap& tH, const CUtensorMap& tWc, int T, int C,
                                   int D, const int32_t* slot, float2* part, float* tgt,
                                   int* status, int num_sms, cudaStream_t stream);
 // G is written through tG_store: G [T, C] bf16, box 64 x 128, 128-byte swizzle.
 cudaError_t launch_softmax_grad(const CUtensorMap& tH, const CUtensorMap& tWc,
+                                const CUtensorMap& tWc_half,
                                 const CUtensorMap& tG_store, int T, int C, int D,
                                 const int32_t* slot, const float* lse, float scale,
                                 int* status, int num_sms, cudaStream_t stream);

@@ -74,6 +74,23 @@ def test_accumulate_and_untouched_rows(orc):
         assert rel_fro(got["dW"][c] - (dW0[c] if acc else 0), ref["dW"][c] - (dW0[c] if acc else 0)) < GRAD_RTOL
 
 
+def test_workspace_reused_across_shapes(orc):
+    """One workspace serves problems of other shapes one after another (one
+    logit tile per row, many, a ragged token tail), each matching the oracle."""
+    cases = [(900, 4000, 256, 2000, 11), (129, 4000, 256, 200, 12), (900, 4000, 256, 2000, 13),
+             (300, 4000, 256, 517, 14)]
+    ws = ss.workspace(1000, 4000, 2100, 256)
+    for T, V, D, C, seed in cases:
+        x, C = _case(T, V, D, C, seed)
+        ref = _full_oracle(orc, x, C, seed)
+        got = run_gpu(ss, x, C, seed, ws=ws)
+        assert got["status"] == 0
+        assert_loss_close(got["loss"], ref["loss"])
+        assert_loss_close(got["lse"], ref["lse"])
+        assert rel_fro(got["dH"], ref["dH"]) < GRAD_RTOL
+        assert rel_fro(got["dW"], ref["dW"]) < GRAD_RTOL
+
+
 def test_repeated_calls_are_deterministic(orc):
     T, V, D, C, seed = 400, 3000, 768, 1200, 12
     x, C = _case(T, V, D, C, seed)
@@ -95,18 +112,17 @@ def test_uniform_logits_ln_C(orc):
 
 # ------------------------------------------------------------- full sizes
 
-@pytest.mark.parametrize("wid", [1, 2, 3, 4, 5])
-def test_full_size_workload(orc, wid):
-    w = synth.WORKLOADS[wid]
-    x = synth.workload_inputs(w)
-    T, V, D, C = w.T, w.V, w.D, w.C
-    # candidates first: bit-exact on the whole batch
-    cand_ref, slot_ref, U_ref = orc.build_candidates(x["targets"], V, C, w.seed)
+def _check_sampled(orc, x, T, V, D, C, seed, rng_seed, exact_cols):
+    """The whole path on one batch: candidates bit-exact, sampled token rows of
+    loss/lse/dH against the oracle, dW rows outside the candidate set
+    untouched, two identities of the gradients, and (exact_cols) some dW
+    candidate rows and the whole lse against the oracle."""
+    cand_ref, slot_ref, U_ref = orc.build_candidates(x["targets"], V, C, seed)
     H = to_dev_bf16(x["H"])
     W = to_dev_bf16(x["W"])
     targets = torch.from_numpy(x["targets"]).cuda()
     ws = ss.workspace(T, V, C, D)
-    cand, slot, U = ss.build_candidates(targets, V, C, w.seed, ws, return_U=True)
+    cand, slot, U = ss.build_candidates(targets, V, C, seed, ws, return_U=True)
     assert U == U_ref
     np.testing.assert_array_equal(cand.cpu().numpy(), cand_ref)
     np.testing.assert_array_equal(slot.cpu().numpy(), slot_ref)
@@ -121,8 +137,9 @@ def test_full_size_workload(orc, wid):
     dH = dH.float().cpu().numpy()
     dW = dW.cpu().numpy()
     # sampled tokens, including both ends and the last partial tile
-    rng = np.random.default_rng(100 + wid)
-    rows = np.unique(np.concatenate([[0, T - 1, (T // 128) * 128 - 1], rng.integers(0, T, 45)]))
+    rng = np.random.default_rng(rng_seed)
+    rows = np.unique(np.concatenate([[0, T - 1, (T // 128) * 128 - 1, (T // 256) * 256],
+                                     rng.integers(0, T, 45)]))
     rows = rows[(rows >= 0) & (rows < T)]
     l_ref, s_ref = orc.forward(x["H"], x["W"], cand_ref, slot_ref, rows=rows)
     assert_loss_close(loss[rows], l_ref)
@@ -142,13 +159,33 @@ def test_full_size_workload(orc, wid):
     lhs = float((dWc * W64[cand_ref]).sum())
     rhs = float((dH.astype(np.float64) * H64).sum())
     assert abs(lhs - rhs) <= 0.02 * abs(rhs)
-    # exact candidate rows where the oracle's full-batch lse is affordable
-    if T * C <= 16384 * 10240:
+    if exact_cols:
         _, lse_all = orc.forward(x["H"], x["W"], cand_ref, slot_ref)
-        cols = np.unique(np.array([0, U_ref - 1, min(U_ref, C - 1), C - 1, C // 2, 1]))
+        cols = np.unique(np.array([0, U_ref - 1, min(U_ref, C - 1), C - 1, C // 2, 1,
+                                   (C // 256) * 256]))
+        cols = cols[cols < C]
         ref_rows = orc.backward_dWc(x["H"], x["W"], cand_ref, slot_ref, lse_all, scale, cols=cols)
         assert rel_fro(dW[cand_ref[cols]], ref_rows) < GRAD_RTOL
         assert_loss_close(lse, lse_all)
+
+
+@pytest.mark.parametrize("wid", [1, 2, 3, 4, 5])
+def test_full_size_workload(orc, wid):
+    w = synth.WORKLOADS[wid]
+    x = synth.workload_inputs(w)
+    # exact candidate rows where the oracle's full-batch lse is affordable
+    _check_sampled(orc, x, w.T, w.V, w.D, w.C, w.seed, 100 + wid,
+                   exact_cols=w.T * w.C <= 16384 * 10240)
+
+
+def test_operands_beyond_l2_ragged(orc):
+    """H and W_c together above 96 MB (bf16): the softmax-gradient GEMM runs on CTA pairs
+    and the gradient GEMMs in two launches. Ragged T (not a multiple of the
+    256-row pair tile) and C."""
+    T, V, D, C, seed = 9001, 20000, 4096, 4001, 21
+    assert (T + C) * D * 2 > 96 * 2**20
+    x, C = _case(T, V, D, C, seed)
+    _check_sampled(orc, x, T, V, D, C, seed, 7, exact_cols=True)
 
 
 # ------------------------------------------------------------ error paths
