@@ -360,6 +360,37 @@ ss_status enqueue_zero_rows(const int32_t* cand, int64_t C, int64_t V, int64_t D
 }
 
 }  // namespace
+
+cudaError_t prepare_kernel(const void* kern, int dyn_smem_bytes) {
+  struct Done {
+    const void* kern;
+    int dev, smem;
+  };
+  static std::mutex mu;
+  static std::vector<Done> done;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(mu);
+  Done* d = nullptr;
+  for (auto& x : done)
+    if (x.kern == kern && x.dev == dev) d = &x;
+  if (d && d->smem >= dyn_smem_bytes) return cudaSuccess;
+  if (dyn_smem_bytes > 0) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn_smem_bytes);
+    if (e != cudaSuccess) return e;
+  }
+  if (d) {
+    d->smem = dyn_smem_bytes;
+    return cudaSuccess;
+  }
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                           cudaSharedmemCarveoutMaxShared);
+  if (e != cudaSuccess) return e;
+  done.push_back(Done{kern, dev, dyn_smem_bytes});
+  return cudaSuccess;
+}
+
 }  // namespace ss
 
 using namespace ss;

@@ -563,10 +563,6 @@ cudaError_t launch_build_candidates(const int32_t* targets, int T, int V, int C,
                                     int32_t* cand, int32_t* slot, int* hdr,
                                     cudaStream_t stream) {
   const size_t smem = build_candidates_smem_bytes(V);
-  cudaError_t e = cudaFuncSetAttribute(k_build_candidates,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
-  if (e != cudaSuccess) return e;
   return launch_pdl(k_build_candidates, dim3(kClusterCtas), dim3(kCandThreads), smem, stream, targets,
                     T, V, C, seed, cand, slot, hdr);
 }

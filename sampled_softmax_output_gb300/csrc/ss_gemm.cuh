@@ -547,8 +547,6 @@ cudaError_t launch_gemm(const CUtensorMap& tA, const CUtensorMap& tB, GemmShape 
                         cudaStream_t stream) {
   auto kern = k_gemm<BN, STAGES, A_MN, B_MN, Epi, EPI_WARPS>;
   constexpr int smem = GemmSmem<BN, STAGES, Epi::kStageBytes>::TOTAL;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (e != cudaSuccess) return e;
   const int units = shp.m_tiles * shp.n_tiles;
   if (units <= 0) return cudaSuccess;
   const int grid = units < num_sms ? units : num_sms;

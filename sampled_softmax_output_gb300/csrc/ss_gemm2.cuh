@@ -253,8 +253,6 @@ cudaError_t launch_gemm2(const CUtensorMap& tA, const CUtensorMap& tB, GemmShape
                          cudaStream_t stream) {
   auto kern = k_gemm2<BN, STAGES, A_MN, B_MN, Epi, EPI_WARPS>;
   constexpr int smem = Gemm2Smem<BN, STAGES, Epi::kStageBytes>::TOTAL;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (e != cudaSuccess) return e;
   const int units = shp.m_tiles * shp.n_tiles;
   if (units <= 0) return cudaSuccess;
   const int pairs = units < num_sms / 2 ? units : num_sms / 2;

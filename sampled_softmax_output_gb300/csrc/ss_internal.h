@@ -10,11 +10,23 @@
 
 namespace ss {
 
+// Sets a kernel's dynamic shared-memory limit and the largest shared-memory
+// carveout, once per kernel, device and process. Every kernel of the library
+// asks for the same L1/shared split, so consecutive launches need no SM
+// reconfiguration between them.
+cudaError_t prepare_kernel(const void* kern, int dyn_smem_bytes);
+template <typename... KArgs>
+cudaError_t prepare_kernel(void (*kern)(KArgs...), int dyn_smem_bytes) {
+  return prepare_kernel(reinterpret_cast<const void*>(kern), dyn_smem_bytes);
+}
+
 // Launch with programmatic stream serialization: the kernel may be scheduled
 // while its predecessor in the stream drains, and waits for it in pdl_enter().
 template <typename... KArgs, typename... Args>
 cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
                        cudaStream_t stream, Args&&... args) {
+  const cudaError_t e = prepare_kernel(kern, static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = block;
