@@ -84,10 +84,13 @@ def load_peaks():
 
 # the source files that define each traced kernel
 KERNEL_SOURCES = {
-    "gemm_forward_lse": ["ss_ptx.cuh", "ss_gemm.cuh", "ss_gemm_logits.cu"],
-    "gemm_softmax_grad": ["ss_ptx.cuh", "ss_gemm.cuh", "ss_gemm_logits.cu"],
-    "gemm_grads": ["ss_ptx.cuh", "ss_gemm.cuh", "ss_gemm2.cuh", "ss_gemm_grads.cu"],
-    "build_candidates": ["ss_ptx.cuh", "ss_candidates.cu"],
+    "gemm_forward_lse": ["ss_internal.h", "ss_ptx.cuh", "ss_gemm.cuh", "ss_gemm2.cuh",
+                         "ss_gemm_logits.cu"],
+    "gemm_softmax_grad": ["ss_internal.h", "ss_ptx.cuh", "ss_gemm.cuh", "ss_gemm2.cuh",
+                          "ss_gemm_logits.cu"],
+    "gemm_grads": ["ss_internal.h", "ss_ptx.cuh", "ss_gemm.cuh", "ss_gemm2.cuh",
+                   "ss_gemm_grads.cu"],
+    "build_candidates": ["ss_internal.h", "ss_ptx.cuh", "ss_candidates.cu"],
 }
 
 

@@ -159,6 +159,18 @@ def _check_sampled(orc, x, T, V, D, C, seed, rng_seed, exact_cols):
     lhs = float((dWc * W64[cand_ref]).sum())
     rhs = float((dH.astype(np.float64) * H64).sum())
     assert abs(lhs - rhs) <= 0.02 * abs(rhs)
+    # the fused entry point (one gather for both passes) gives the same bits
+    # as the three calls
+    fused = ss.step(H, W, targets, C, seed, ws, scale=scale,
+                    dW=torch.full((V, D), canary, dtype=torch.float32, device="cuda"))
+    torch.cuda.synchronize()
+    assert ss.read_status(ws)[0] == 0
+    np.testing.assert_array_equal(fused["cand"].cpu().numpy(), cand_ref)
+    np.testing.assert_array_equal(fused["loss"].cpu().numpy(), loss)
+    np.testing.assert_array_equal(fused["lse"].cpu().numpy(), lse)
+    np.testing.assert_array_equal(fused["dH"].float().cpu().numpy(), dH)
+    np.testing.assert_array_equal(fused["dW"].cpu().numpy(), dW)
+    del fused
     if exact_cols:
         _, lse_all = orc.forward(x["H"], x["W"], cand_ref, slot_ref)
         cols = np.unique(np.array([0, U_ref - 1, min(U_ref, C - 1), C - 1, C // 2, 1,
@@ -294,6 +306,7 @@ def test_kernel_trace_records_every_launch():
     with ss.KernelTrace(capacity=16) as tr:
         ss.step(H, W, _dev(x["targets"]), C, 4, ws)
     torch.cuda.synchronize()
+    # one gather shared by the forward and the backward
     assert [n for n, _ in tr.timings()] == ["build_candidates", "gather_rows", "gemm_forward_lse",
                                            "lse_merge", "gemm_softmax_grad", "gemm_grads"]
     assert all(ms > 0 for _, ms in tr.timings())
