@@ -59,12 +59,23 @@ def up_to_date() -> bool:
 def build(force: bool = False, verbose: bool = False) -> str:
     if not force and up_to_date():
         return LIB
-    os.makedirs(OUT_DIR, exist_ok=True)
+    return _build_into(OUT_DIR, LIB, [], verbose)
+
+
+def build_variant(out_dir: str, defines: list[str], verbose: bool = False) -> str:
+    """Build a copy of the library with extra preprocessor definitions (e.g.
+    ``SS_TIE_CAP=0``) into ``out_dir``; returns the path of its libss.so."""
+    return _build_into(out_dir, os.path.join(out_dir, "libss.so"), ["-D" + d for d in defines],
+                       verbose)
+
+
+def _build_into(out_dir: str, lib: str, extra: list[str], verbose: bool) -> str:
+    os.makedirs(out_dir, exist_ok=True)
     cc = nvcc()
-    flags = _flags(verbose)
+    flags = _flags(verbose) + extra
 
     def compile_one(src: str):
-        obj = os.path.join(OUT_DIR, src.replace(".cu", ".o"))
+        obj = os.path.join(out_dir, src.replace(".cu", ".o"))
         cmd = [cc] + flags + ["-c", os.path.join(CSRC, src), "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         return src, obj, r
@@ -79,13 +90,13 @@ def build(force: bool = False, verbose: bool = False) -> str:
             errors.append(f"{src}:\n{r.stdout}{r.stderr}")
     if errors:
         raise RuntimeError("nvcc failed:\n" + "\n".join(errors))
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib + f".tmp{os.getpid()}"
     cmd = [cc] + ARCH + ["-shared", "-o", tmp] + [o for _, o, _ in results] + ["-cudart", "static"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
