@@ -360,6 +360,25 @@ def run_native(args, world, rank, local):
     torch.cuda.synchronize()
     three_calls_ms = sum(a.elapsed_time(b) for a, b in zip(s3, e3)) / K3
 
+    # the same step replayed from a CUDA graph of ss_step (ss_step_graph_*)
+    graph = ss.StepGraph(H, W, targets, C, ws, scale=scale, cand=cand, slot=slot, loss=loss,
+                         lse=lse, dH=dH, dW=dW)
+    graph.launch(w.seed)
+    sg = [torch.cuda.Event(enable_timing=True) for _ in range(K3)]
+    eg = [torch.cuda.Event(enable_timing=True) for _ in range(K3)]
+    torch.cuda.synchronize()
+    for k in range(K3):
+        flush.zero_()
+        sg[k].record()
+        graph.launch(w.seed)
+        eg[k].record()
+    torch.cuda.synchronize()
+    graph_ms = sum(a.elapsed_time(b) for a, b in zip(sg, eg)) / K3
+    graph.close()
+    st, _ = ss.read_status(ws)
+    if st != 0:
+        raise RuntimeError(f"device status {st} after the graph region")
+
     # per-kernel times from the trace
     per = {}
     for name, ms in trace.timings():
@@ -426,6 +445,7 @@ def run_native(args, world, rank, local):
                    "l2": "flushed between steps (256 MB write, outside the timed events)",
                    "step": "ss_step (= ss_build_candidates + ss_forward + ss_backward in one call)",
                    "ms_per_step_three_calls": three_calls_ms,
+                   "ms_per_step_graph": graph_ms,
                    "step_tflops_algorithmic_6TCD": step_tflops,
                    "pct_bf16_peak_algorithmic": 100.0 * step_tflops / peaks["bf16_tflops"]},
         "roofline": roof,

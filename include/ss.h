@@ -157,6 +157,55 @@ ss_status ss_step(const int32_t* targets, const uint16_t* H, const uint16_t* W, 
                   void* workspace, size_t workspace_bytes, ss_stream stream);
 
 /*
+ * The pages' candidate schedule ("NanoGPT Training Record: Technical
+ * Optimizations & Speed", "Key Optimizations and Ablation Table Results":
+ * 10,240, then 14,336, then 24,576 candidates, then all rows for the final
+ * 87 steps). The pages do not say where the first three phases end; here
+ * the steps before the final SS_SCHEDULE_FULL_STEPS are split into three
+ * equal consecutive phases (step s of those n steps is in phase 3s / n,
+ * rounded down). Each count is capped at V.
+ *   step        : 0-based training step, 0 <= step < total_steps.
+ * Returns C for that step, or -1 for invalid arguments (V < 1 or V > SS_MAX_V,
+ * total_steps < 1, step outside [0, total_steps)).
+ */
+#define SS_SCHEDULE_FULL_STEPS 87
+int64_t ss_schedule_candidates(int64_t step, int64_t total_steps, int64_t V);
+
+/*
+ * Zero the rows rows[0 .. n) of dW [V, D] fp32 (device pointers; rows holds
+ * distinct ids in [0, V)), e.g. the rows an accumulation window wrote, before
+ * the next window accumulates into them ("KellerJordan/modded-nanogpt"
+ * README, technique list: lm_head gradients accumulated over 2 steps).
+ * Entries outside [0, V) set SS_ERR_INDEX in the workspace status word and
+ * are skipped. Stream-ordered; the workspace needs only its header
+ * (ss_workspace_size of any shape is enough).
+ */
+ss_status ss_clear_rows(const int32_t* rows, int64_t n, int64_t V, int64_t D, float* dW,
+                        void* workspace, size_t workspace_bytes, ss_stream stream);
+
+/*
+ * ss_step captured once into a CUDA graph and replayed ("NanoGPT Training
+ * Record: Technical Optimizations & Speed", "Key Optimizations and Ablation
+ * Table Results": training-step graph capture). ss_step_graph_create records
+ * ss_step with the given arguments (all of them fixed for the graph's life:
+ * the same buffers, shapes, scale and accumulate flag; the buffers' contents
+ * may change between launches) without running it. ss_step_graph_launch
+ * runs it on `stream` with `seed` for the candidate build; results are those
+ * of ss_step with the same arguments. The buffers must stay allocated until
+ * ss_step_graph_destroy. One graph must not run concurrently with itself or
+ * with another call on the same workspace. create returns the errors of
+ * ss_step's argument checks, or SS_ERR_CUDA.
+ */
+typedef struct ss_step_graph ss_step_graph;
+ss_status ss_step_graph_create(const int32_t* targets, const uint16_t* H, const uint16_t* W,
+                               int64_t T, int64_t V, int64_t C, int64_t D, float scale,
+                               int accumulate, int32_t* cand, int32_t* slot, float* loss,
+                               float* lse, uint16_t* dH, float* dW, void* workspace,
+                               size_t workspace_bytes, ss_step_graph** graph);
+ss_status ss_step_graph_launch(ss_step_graph* graph, uint64_t seed, ss_stream stream);
+void ss_step_graph_destroy(ss_step_graph* graph);
+
+/*
  * Allocation-free forward pass. Not part of the method on the pages (the
  * paper has no counterpart): an operational variant of ss_forward for callers
  * that cannot allocate device memory at all -- for example code running as a

@@ -82,6 +82,17 @@ def _load():
     L.ss_trace_end.argtypes = []
     L.ss_trace_kernel_name.restype = ctypes.c_char_p
     L.ss_trace_kernel_name.argtypes = [ctypes.c_int]
+    L.ss_schedule_candidates.restype = i64
+    L.ss_schedule_candidates.argtypes = [i64, i64, i64]
+    L.ss_clear_rows.restype = ctypes.c_int
+    L.ss_clear_rows.argtypes = [p, i64, i64, i64, p, p, sz, p]
+    L.ss_step_graph_create.restype = ctypes.c_int
+    L.ss_step_graph_create.argtypes = [p, p, p, i64, i64, i64, i64, ctypes.c_float, ctypes.c_int,
+                                       p, p, p, p, p, p, p, sz, ctypes.POINTER(p)]
+    L.ss_step_graph_launch.restype = ctypes.c_int
+    L.ss_step_graph_launch.argtypes = [p, ctypes.c_uint64, p]
+    L.ss_step_graph_destroy.restype = None
+    L.ss_step_graph_destroy.argtypes = [p]
     return L
 
 
@@ -336,3 +347,84 @@ def step_separate(H, W, targets, C: int, seed: int, ws, scale: float = 1.0, dW=N
     loss, lse = forward(H, W, cand, slot, ws)
     dH, dW = backward(H, W, cand, slot, lse, ws, scale=scale, accumulate=accumulate, dW=dW)
     return {"cand": cand, "slot": slot, "loss": loss, "lse": lse, "dH": dH, "dW": dW}
+
+
+SCHEDULE_FULL_STEPS = 87
+
+
+def schedule_candidates(step: int, total_steps: int, V: int) -> int:
+    """C of training step `step` under the pages' candidate schedule
+    (ss_schedule_candidates)."""
+    c = _lib.ss_schedule_candidates(step, total_steps, V)
+    if c < 0:
+        raise ValueError(f"ss_schedule_candidates({step}, {total_steps}, {V}): invalid arguments")
+    return int(c)
+
+
+def clear_rows(rows: torch.Tensor, dW: torch.Tensor, ws: torch.Tensor):
+    """dW[rows] = 0 (ss_clear_rows); rows: distinct int32 ids."""
+    _need(rows, "rows", torch.int32)
+    dev = rows.device
+    _need(dW, "dW", torch.float32, dev)
+    _need(ws, "workspace", torch.uint8, dev)
+    V, D = dW.shape
+    _check(_lib.ss_clear_rows(_ptr(rows), rows.numel(), V, D, _ptr(dW), _ptr(ws), ws.numel(),
+                              _stream(dev)), "ss_clear_rows")
+
+
+class StepGraph:
+    """ss_step captured into a CUDA graph (ss_step_graph_*): the buffers are
+    fixed at construction and kept alive here; launch(seed) replays the step
+    on the current stream."""
+
+    def __init__(self, H, W, targets, C: int, ws, scale: float = 1.0, accumulate=False,
+                 cand=None, slot=None, loss=None, lse=None, dH=None, dW=None):
+        _need(H, "H", torch.bfloat16)
+        dev = H.device
+        T, D = H.shape
+        V = W.shape[0]
+        _need(W, "W", torch.bfloat16, dev, (V, D))
+        _need(targets, "targets", torch.int32, dev, (T,))
+        _need(ws, "workspace", torch.uint8, dev)
+        self.cand = torch.empty(C, dtype=torch.int32, device=dev) if cand is None else cand
+        self.slot = torch.empty(T, dtype=torch.int32, device=dev) if slot is None else slot
+        self.loss = torch.empty(T, dtype=torch.float32, device=dev) if loss is None else loss
+        self.lse = torch.empty(T, dtype=torch.float32, device=dev) if lse is None else lse
+        self.dH = torch.empty(T, D, dtype=torch.bfloat16, device=dev) if dH is None else dH
+        self.dW = torch.zeros(V, D, dtype=torch.float32, device=dev) if dW is None else dW
+        for t, name, dt, shape in ((self.cand, "cand", torch.int32, (C,)),
+                                   (self.slot, "slot", torch.int32, (T,)),
+                                   (self.loss, "loss", torch.float32, (T,)),
+                                   (self.lse, "lse", torch.float32, (T,)),
+                                   (self.dH, "dH", torch.bfloat16, (T, D)),
+                                   (self.dW, "dW", torch.float32, (V, D))):
+            _need(t, name, dt, dev, shape)
+        self._keep = (H, W, targets, ws)
+        self.device = dev
+        h = ctypes.c_void_p()
+        code = _lib.ss_step_graph_create(_ptr(targets), _ptr(H), _ptr(W), T, V, C, D,
+                                         float(scale), 1 if accumulate else 0, _ptr(self.cand),
+                                         _ptr(self.slot), _ptr(self.loss), _ptr(self.lse),
+                                         _ptr(self.dH), _ptr(self.dW), _ptr(ws), ws.numel(),
+                                         ctypes.byref(h))
+        _check(code, "ss_step_graph_create")
+        self._h = h
+
+    def launch(self, seed: int):
+        if self._h is None:
+            raise RuntimeError("StepGraph is closed")
+        _check(_lib.ss_step_graph_launch(self._h, seed & (2**64 - 1), _stream(self.device)),
+               "ss_step_graph_launch")
+        return {"cand": self.cand, "slot": self.slot, "loss": self.loss, "lse": self.lse,
+                "dH": self.dH, "dW": self.dW}
+
+    def close(self):
+        if self._h is not None:
+            _lib.ss_step_graph_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

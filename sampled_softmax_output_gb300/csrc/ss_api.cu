@@ -359,6 +359,26 @@ ss_status enqueue_zero_rows(const int32_t* cand, int64_t C, int64_t V, int64_t D
   return cuda_status(e, "launch k_zero_rows");
 }
 
+// The argument checks of ss_step (and of ss_step_graph_create).
+ss_status step_args_status(const int32_t* targets, const uint16_t* H, const uint16_t* W,
+                           int64_t T, int64_t V, int64_t C, int64_t D, int accumulate,
+                           const int32_t* cand, const int32_t* slot, const float* loss,
+                           const float* lse, const uint16_t* dH, const float* dW,
+                           const void* workspace, size_t workspace_bytes) {
+  const ss_status st = check_sizes(T, V, C, D);
+  if (st != SS_OK) return st;
+  if (!W || !cand || !dW || !workspace ||
+      (T > 0 && (!targets || !H || !slot || !loss || !lse || !dH)))
+    return SS_ERR_INVALID;
+  if (!aligned(targets, 4) || !aligned(H, 16) || !aligned(W, 16) || !aligned(dH, 16) ||
+      !aligned(dW, 16) || !aligned(workspace, 16) || !aligned(cand, 4) || !aligned(slot, 4) ||
+      !aligned(loss, 4) || !aligned(lse, 4))
+    return SS_ERR_INVALID;
+  if (accumulate != 0 && accumulate != 1) return SS_ERR_INVALID;
+  if (workspace_bytes < make_layout(T, C, D).total) return SS_ERR_WORKSPACE;
+  return SS_OK;
+}
+
 }  // namespace
 
 cudaError_t prepare_kernel(const void* kern, int dyn_smem_bytes) {
@@ -394,6 +414,22 @@ cudaError_t prepare_kernel(const void* kern, int dyn_smem_bytes) {
 }  // namespace ss
 
 using namespace ss;
+
+// A captured ss_step: the graph, its executable, and the candidate kernel's
+// node with the argument values it is launched with (only `seed` changes).
+struct ss_step_graph {
+  cudaGraph_t graph = nullptr;
+  cudaGraphExec_t exec = nullptr;
+  cudaGraphNode_t cand_node = nullptr;
+  cudaKernelNodeParams base = {};
+  const int32_t* targets = nullptr;
+  int T = 0, V = 0, C = 0;
+  uint64_t seed = 0;
+  int32_t* cand = nullptr;
+  int32_t* slot = nullptr;
+  int* hdr = nullptr;
+  void* args[8] = {};
+};
 
 extern "C" {
 
@@ -484,18 +520,10 @@ ss_status ss_step(const int32_t* targets, const uint16_t* H, const uint16_t* W, 
                   int64_t V, int64_t C, int64_t D, uint64_t seed, float scale, int accumulate,
                   int32_t* cand, int32_t* slot, float* loss, float* lse, uint16_t* dH, float* dW,
                   void* workspace, size_t workspace_bytes, ss_stream stream) {
-  const ss_status st = check_sizes(T, V, C, D);
+  const ss_status st = step_args_status(targets, H, W, T, V, C, D, accumulate, cand, slot, loss,
+                                        lse, dH, dW, workspace, workspace_bytes);
   if (st != SS_OK) return st;
-  if (!W || !cand || !dW || !workspace ||
-      (T > 0 && (!targets || !H || !slot || !loss || !lse || !dH)))
-    return SS_ERR_INVALID;
-  if (!aligned(targets, 4) || !aligned(H, 16) || !aligned(W, 16) || !aligned(dH, 16) ||
-      !aligned(dW, 16) || !aligned(workspace, 16) || !aligned(cand, 4) || !aligned(slot, 4) ||
-      !aligned(loss, 4) || !aligned(lse, 4))
-    return SS_ERR_INVALID;
-  if (accumulate != 0 && accumulate != 1) return SS_ERR_INVALID;
   const Layout L = make_layout(T, C, D);
-  if (workspace_bytes < L.total) return SS_ERR_WORKSPACE;
   const ss_status sb = ss_build_candidates(targets, T, V, C, seed, cand, slot, nullptr, workspace,
                                            workspace_bytes, stream);
   if (sb != SS_OK) return sb;
@@ -511,6 +539,32 @@ ss_status ss_step(const int32_t* targets, const uint16_t* H, const uint16_t* W, 
   r = enqueue_forward(H, slot, T, C, D, loss, lse, L, ws, nsm, s);
   if (r != SS_OK) return r;
   return enqueue_backward(H, cand, slot, lse, T, V, C, D, scale, accumulate, dH, dW, L, ws, nsm, s);
+}
+
+int64_t ss_schedule_candidates(int64_t step, int64_t total_steps, int64_t V) {
+  if (V < 1 || V > SS_MAX_V || total_steps < 1 || step < 0 || step >= total_steps) return -1;
+  const int64_t sampled = total_steps > SS_SCHEDULE_FULL_STEPS
+                              ? total_steps - SS_SCHEDULE_FULL_STEPS
+                              : 0;
+  if (step >= sampled) return V;
+  static const int64_t kPhaseC[3] = {10240, 14336, 24576};
+  const int64_t c = kPhaseC[(3 * step) / sampled];
+  return c < V ? c : V;
+}
+
+ss_status ss_clear_rows(const int32_t* rows, int64_t n, int64_t V, int64_t D, float* dW,
+                        void* workspace, size_t workspace_bytes, ss_stream stream) {
+  if (n < 0 || V < 1 || n > V || D <= 0) return SS_ERR_INVALID;
+  if (V > SS_MAX_V || D < 64 || D % 64 != 0 || D > SS_MAX_D) return SS_ERR_UNSUPPORTED;
+  if (n == 0) return SS_OK;
+  if (!rows || !dW || !workspace || !aligned(rows, 4) || !aligned(dW, 16) ||
+      !aligned(workspace, 16))
+    return SS_ERR_INVALID;
+  if (workspace_bytes < kHdrBytes) return SS_ERR_WORKSPACE;
+  const int nsm = num_sms_current();
+  if (nsm <= 0) return fail("cudaGetDevice/cudaDeviceGetAttribute", cudaGetLastError());
+  return enqueue_zero_rows(rows, n, V, D, dW, static_cast<int*>(workspace), nsm,
+                           static_cast<cudaStream_t>(stream));
 }
 
 ss_status ss_forward_noalloc(const uint16_t* H, const uint16_t* W, const int32_t* cand,
@@ -622,6 +676,89 @@ const char* ss_trace_kernel_name(int k) {
   const Trace& t = g_trace;
   if (k < 0 || k >= t.count || k >= static_cast<int>(t.names.size())) return nullptr;
   return t.names[k];
+}
+
+ss_status ss_step_graph_create(const int32_t* targets, const uint16_t* H, const uint16_t* W,
+                               int64_t T, int64_t V, int64_t C, int64_t D, float scale,
+                               int accumulate, int32_t* cand, int32_t* slot, float* loss,
+                               float* lse, uint16_t* dH, float* dW, void* workspace,
+                               size_t workspace_bytes, ss_step_graph** graph) {
+  if (!graph) return SS_ERR_INVALID;
+  *graph = nullptr;
+  const ss_status st = step_args_status(targets, H, W, T, V, C, D, accumulate, cand, slot, loss,
+                                        lse, dH, dW, workspace, workspace_bytes);
+  if (st != SS_OK) return st;
+  // record ss_step on a private stream
+  cudaStream_t cs = nullptr;
+  cudaError_t e = cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking);
+  if (e != cudaSuccess) return fail("cudaStreamCreateWithFlags", e);
+  e = cudaStreamBeginCapture(cs, cudaStreamCaptureModeRelaxed);
+  if (e != cudaSuccess) {
+    cudaStreamDestroy(cs);
+    return fail("cudaStreamBeginCapture", e);
+  }
+  const ss_status r = ss_step(targets, H, W, T, V, C, D, 0, scale, accumulate, cand, slot, loss,
+                              lse, dH, dW, workspace, workspace_bytes, cs);
+  cudaGraph_t g = nullptr;
+  e = cudaStreamEndCapture(cs, &g);
+  cudaStreamDestroy(cs);
+  if (r != SS_OK || e != cudaSuccess) {
+    if (g) cudaGraphDestroy(g);
+    return r != SS_OK ? r : fail("cudaStreamEndCapture", e);
+  }
+  auto* sg = new ss_step_graph;
+  sg->graph = g;
+  size_t n = 0;
+  e = cudaGraphGetNodes(g, nullptr, &n);
+  std::vector<cudaGraphNode_t> nodes(n);
+  if (e == cudaSuccess && n > 0) e = cudaGraphGetNodes(g, nodes.data(), &n);
+  for (size_t i = 0; e == cudaSuccess && i < n && !sg->cand_node; ++i) {
+    cudaGraphNodeType type;
+    if (cudaGraphNodeGetType(nodes[i], &type) != cudaSuccess || type != cudaGraphNodeTypeKernel)
+      continue;
+    cudaKernelNodeParams p = {};
+    if (cudaGraphKernelNodeGetParams(nodes[i], &p) == cudaSuccess &&
+        p.func == build_candidates_kernel()) {
+      sg->cand_node = nodes[i];
+      sg->base = p;
+    }
+  }
+  if (e == cudaSuccess && !sg->cand_node) e = cudaErrorInvalidValue;
+  if (e == cudaSuccess) e = cudaGraphInstantiate(&sg->exec, g, 0);
+  if (e != cudaSuccess) {
+    ss_step_graph_destroy(sg);
+    return fail("capture of ss_step into a graph", e);
+  }
+  sg->targets = targets;
+  sg->T = static_cast<int>(T);
+  sg->V = static_cast<int>(V);
+  sg->C = static_cast<int>(C);
+  sg->cand = cand;
+  sg->slot = slot;
+  sg->hdr = static_cast<int*>(workspace);
+  void* a[8] = {&sg->targets, &sg->T, &sg->V, &sg->C, &sg->seed, &sg->cand, &sg->slot, &sg->hdr};
+  for (int i = 0; i < 8; ++i) sg->args[i] = a[i];
+  *graph = sg;
+  return SS_OK;
+}
+
+ss_status ss_step_graph_launch(ss_step_graph* graph, uint64_t seed, ss_stream stream) {
+  if (!graph || !graph->exec) return SS_ERR_INVALID;
+  graph->seed = seed;
+  cudaKernelNodeParams p = graph->base;
+  p.kernelParams = graph->args;
+  p.extra = nullptr;
+  cudaError_t e = cudaGraphExecKernelNodeSetParams(graph->exec, graph->cand_node, &p);
+  if (e != cudaSuccess) return fail("cudaGraphExecKernelNodeSetParams", e);
+  e = cudaGraphLaunch(graph->exec, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? SS_OK : fail("cudaGraphLaunch", e);
+}
+
+void ss_step_graph_destroy(ss_step_graph* graph) {
+  if (!graph) return;
+  if (graph->exec) cudaGraphExecDestroy(graph->exec);
+  if (graph->graph) cudaGraphDestroy(graph->graph);
+  delete graph;
 }
 
 const char* ss_last_error(void) { return g_err; }

@@ -559,6 +559,8 @@ size_t build_candidates_smem_bytes(int64_t V) {
   return bytes;
 }
 
+const void* build_candidates_kernel() { return reinterpret_cast<const void*>(k_build_candidates); }
+
 cudaError_t launch_build_candidates(const int32_t* targets, int T, int V, int C, uint64_t seed,
                                     int32_t* cand, int32_t* slot, int* hdr,
                                     cudaStream_t stream) {

@@ -58,6 +58,9 @@ inline bool operands_exceed_l2(int T, int C, int D) {
 
 // ---- candidate build (ss_candidates.cu)
 size_t build_candidates_smem_bytes(int64_t V);
+// The candidate kernel's entry (for locating its node in a captured graph);
+// its parameters are (targets, T, V, C, seed, cand, slot, hdr).
+const void* build_candidates_kernel();
 cudaError_t launch_build_candidates(const int32_t* targets, int T, int V, int C, uint64_t seed,
                                     int32_t* cand, int32_t* slot, int* hdr, cudaStream_t stream);
 

@@ -18,7 +18,9 @@ def test_exports_every_declared_symbol():
     assert set(names) == {"ss_workspace_size", "ss_build_candidates", "ss_forward",
                           "ss_backward", "ss_read_status", "ss_status_string",
                           "ss_trace_begin", "ss_trace_end", "ss_trace_kernel_name",
-                          "ss_last_error", "ss_forward_noalloc", "ss_step"}
+                          "ss_last_error", "ss_forward_noalloc", "ss_step",
+                          "ss_schedule_candidates", "ss_clear_rows", "ss_step_graph_create",
+                          "ss_step_graph_launch", "ss_step_graph_destroy"}
     for n in names:
         assert hasattr(ss.lib(), n), n
 
@@ -148,3 +150,58 @@ def test_trace_bookkeeping_without_launches():
 def test_empty_batch_forward_is_a_no_op():
     # T = 0: nothing to compute, returns before any device work
     assert _fwd(T=0, H=0, slot=0, loss=0, lse=0) == OK
+
+
+def test_schedule_candidates():
+    """The pages' schedule: 10,240 / 14,336 / 24,576 candidates in three equal
+    phases, then all V rows for the final 87 steps."""
+    V = 50304
+    for total in (87, 88, 100, 3000, 5960):
+        cs = [ss.schedule_candidates(s, total, V) for s in range(total)]
+        assert cs[-87:] == [V] * 87
+        head = cs[:total - 87]
+        assert head == sorted(head)                       # phases in order
+        counts = [head.count(c) for c in (10240, 14336, 24576)]
+        assert sum(counts) == len(head)
+        assert max(counts) - min(counts) <= 1             # equal phases (+-1 step)
+    assert ss.schedule_candidates(0, 3000, 8000) == 8000  # capped at V
+    L = ss.lib()
+    for args in ((-1, 10, V), (10, 10, V), (0, 0, V), (0, 10, 0), (0, 10, (1 << 19) + 1)):
+        assert L.ss_schedule_candidates(*args) == -1, args
+
+
+def test_clear_rows_argument_errors():
+    L = ss.lib()
+
+    def clear(rows=FAKE, n=16, V=50304, D=768, dW=FAKE, ws=FAKE, wsb=1 << 20):
+        return L.ss_clear_rows(p(rows), n, V, D, p(dW), p(ws), wsb, None)
+
+    assert clear(n=0) == OK                        # nothing to do, nothing enqueued
+    assert clear(n=-1) == INVALID and clear(n=50305) == INVALID and clear(V=0) == INVALID
+    assert clear(V=(1 << 19) + 1, n=1) == UNSUPPORTED and clear(D=100) == UNSUPPORTED
+    assert clear(rows=0) == INVALID and clear(dW=0) == INVALID and clear(ws=0) == INVALID
+    assert clear(rows=FAKE + 2) == INVALID and clear(dW=FAKE + 8) == INVALID
+    assert clear(wsb=16) == WORKSPACE
+
+
+def test_step_graph_argument_errors():
+    L = ss.lib()
+    h = ctypes.c_void_p()
+
+    def create(**kw):
+        a = dict(targets=FAKE, H=FAKE, W=FAKE, T=256, V=50304, C=4096, D=768, scale=1.0, acc=0,
+                 cand=FAKE, slot=FAKE, loss=FAKE, lse=FAKE, dH=FAKE, dW=FAKE, ws=FAKE,
+                 wsb=1 << 40)
+        a.update(kw)
+        return L.ss_step_graph_create(p(a["targets"]), p(a["H"]), p(a["W"]), a["T"], a["V"],
+                                      a["C"], a["D"], a["scale"], a["acc"], p(a["cand"]),
+                                      p(a["slot"]), p(a["loss"]), p(a["lse"]), p(a["dH"]),
+                                      p(a["dW"]), p(a["ws"]), a["wsb"], ctypes.byref(h))
+
+    assert create(C=0) == INVALID and create(D=100) == UNSUPPORTED and create(acc=2) == INVALID
+    assert create(H=0) == INVALID and create(dW=FAKE + 4) == INVALID
+    need = L.ss_workspace_size(256, 50304, 4096, 768)
+    assert create(wsb=need - 1) == WORKSPACE
+    assert h.value is None                          # nothing was created
+    assert L.ss_step_graph_launch(None, 0, None) == INVALID
+    L.ss_step_graph_destroy(None)                   # a no-op
