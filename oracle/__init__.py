@@ -68,6 +68,15 @@ def load(path: str):
         f = getattr(L, f"orc_backward_dW_{suf}")
         f.restype = None
         f.argtypes = [_p, _p, _p, _p, _p, _i64, _i64, _i64, real, _p, _i64, _p]
+        f = getattr(L, f"orc_forward_head_{suf}")
+        f.restype = None
+        f.argtypes = [_p, _p, _p, _p, _i64, _i64, _i64, real, real, _p, _i64, _p, _p]
+        f = getattr(L, f"orc_backward_dH_head_{suf}")
+        f.restype = None
+        f.argtypes = [_p, _p, _p, _p, _p, _i64, _i64, _i64, real, real, real, _p, _i64, _p]
+        f = getattr(L, f"orc_backward_dW_head_{suf}")
+        f.restype = None
+        f.argtypes = [_p, _p, _p, _p, _p, _i64, _i64, _i64, real, real, real, _p, _i64, _p]
     L.orc_num_threads.restype = ctypes.c_int
     L.orc_num_threads.argtypes = []
     return L
@@ -138,8 +147,9 @@ def _rows(rows):
     return r, r.shape[0]
 
 
-def forward(H, W, cand, slot, rows=None, dtype=np.float32):
-    """Per-token (loss, lse) for all tokens or for the listed token rows."""
+def forward(H, W, cand, slot, rows=None, dtype=np.float32, cap=0.0, tau=1.0):
+    """Per-token (loss, lse) for all tokens or for the listed token rows.
+    cap > 0: the capped head z = cap / (1 + exp(-s / tau)) (cap = 0: plain)."""
     suf, real = _real(dtype)
     H = _inputs(H, suf)
     W = _inputs(W, suf)
@@ -151,12 +161,13 @@ def forward(H, W, cand, slot, rows=None, dtype=np.float32):
     n = nr if r is not None else T
     loss = np.empty(n, real)
     lse = np.empty(n, real)
-    getattr(lib(), f"orc_forward_{suf}")(_ptr(H), _ptr(W), _ptr(cand), _ptr(slot), T, C, D,
-                                         _ptr(r), nr, _ptr(loss), _ptr(lse))
+    getattr(lib(), f"orc_forward_head_{suf}")(_ptr(H), _ptr(W), _ptr(cand), _ptr(slot), T, C, D,
+                                              cap, tau, _ptr(r), nr, _ptr(loss), _ptr(lse))
     return loss, lse
 
 
-def backward_dH(H, W, cand, slot, lse_rows, scale=1.0, rows=None, dtype=np.float32):
+def backward_dH(H, W, cand, slot, lse_rows, scale=1.0, rows=None, dtype=np.float32, cap=0.0,
+                tau=1.0):
     """dH rows [n, D]; lse_rows are the oracle's lse of exactly those rows."""
     suf, real = _real(dtype)
     H = _inputs(H, suf)
@@ -170,13 +181,14 @@ def backward_dH(H, W, cand, slot, lse_rows, scale=1.0, rows=None, dtype=np.float
     n = nr if r is not None else T
     assert lse_rows.shape[0] == n
     dH = np.empty((n, D), real)
-    getattr(lib(), f"orc_backward_dH_{suf}")(_ptr(H), _ptr(W), _ptr(cand), _ptr(slot),
-                                             _ptr(lse_rows), T, C, D, scale, _ptr(r), nr,
-                                             _ptr(dH))
+    getattr(lib(), f"orc_backward_dH_head_{suf}")(_ptr(H), _ptr(W), _ptr(cand), _ptr(slot),
+                                                  _ptr(lse_rows), T, C, D, cap, tau, scale,
+                                                  _ptr(r), nr, _ptr(dH))
     return dH
 
 
-def backward_dWc(H, W, cand, slot, lse, scale=1.0, cols=None, dtype=np.float32):
+def backward_dWc(H, W, cand, slot, lse, scale=1.0, cols=None, dtype=np.float32, cap=0.0,
+                 tau=1.0):
     """Candidate-row gradients dWc [n, D] (row i belongs to vocabulary row cand[cols[i]]).
     `lse` must be the oracle's lse of ALL T tokens."""
     suf, real = _real(dtype)
@@ -191,20 +203,21 @@ def backward_dWc(H, W, cand, slot, lse, scale=1.0, cols=None, dtype=np.float32):
     c, nc = _rows(cols)
     n = nc if c is not None else C
     dWc = np.empty((n, D), real)
-    getattr(lib(), f"orc_backward_dW_{suf}")(_ptr(H), _ptr(W), _ptr(cand), _ptr(slot),
-                                             _ptr(lse), T, C, D, scale, _ptr(c), nc, _ptr(dWc))
+    getattr(lib(), f"orc_backward_dW_head_{suf}")(_ptr(H), _ptr(W), _ptr(cand), _ptr(slot),
+                                                  _ptr(lse), T, C, D, cap, tau, scale, _ptr(c),
+                                                  nc, _ptr(dWc))
     return dWc
 
 
 def loss_and_grads(H, W, targets, C, seed, scale=1.0, dtype=np.float32, dW_init=None,
-                   accumulate=False):
+                   accumulate=False, cap=0.0, tau=1.0):
     """The whole definition on one batch: candidates, per-token loss and lse,
     dH [T, D], and dW [V, D] whose candidate rows are written (or added to)."""
     V = W.shape[0]
     cand, slot, U = build_candidates(targets, V, C, seed)
-    loss, lse = forward(H, W, cand, slot, dtype=dtype)
-    dH = backward_dH(H, W, cand, slot, lse, scale, dtype=dtype)
-    dWc = backward_dWc(H, W, cand, slot, lse, scale, dtype=dtype)
+    loss, lse = forward(H, W, cand, slot, dtype=dtype, cap=cap, tau=tau)
+    dH = backward_dH(H, W, cand, slot, lse, scale, dtype=dtype, cap=cap, tau=tau)
+    dWc = backward_dWc(H, W, cand, slot, lse, scale, dtype=dtype, cap=cap, tau=tau)
     _, real = _real(dtype)
     dW = np.zeros(W.shape, real) if dW_init is None else np.array(dW_init, dtype=real, copy=True)
     if accumulate:

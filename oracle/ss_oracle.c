@@ -31,6 +31,17 @@
  *               dH[t]   = sum_j G[t][j] * W[cand[j]]               (j ascending)
  *               dW[cand[j]] = sum_t G[t][j] * H[t]                 (t ascending)
  *
+ * Head variant ("KellerJordan/modded-nanogpt" README, technique list: the
+ * logits are rescaled asymmetrically and soft-capped; the pages give no
+ * formula). Reading: a logistic cap applied to every candidate logit before
+ * the softmax,
+ *               z[t][j] = A / (1 + exp(-s[t][j] / tau))        A > 0, tau > 0,
+ *   bounded to (0, A), not symmetric about 0 (up to a shift, which the
+ *   softmax ignores, it is the symmetric cap (A/2) tanh(s / (2 tau))). The
+ *   forward and backward above then run on z: lse and loss from z, and by the
+ *   chain rule G[t][j] = scale * (exp(z - lse) - [j == slot[t]]) * dz/ds with
+ *   dz/ds = z (A - z) / (A tau). A = 0 selects the plain head (z = s).
+ *
  * Negative-sampling key (the pages name no sampler; reading: uniform without
  * replacement over the non-targets, driven by a counter-based generator so
  * that a CPU and a GPU implementation can agree bit for bit):
@@ -181,9 +192,18 @@ int orc_build_candidates(const int32_t* targets, int64_t T, int64_t V, int64_t C
     }                                                                                        \
   }                                                                                          \
                                                                                              \
-  void orc_forward_##SUF(const IN_T* H, const IN_T* W, const int32_t* cand,                  \
-                         const int32_t* slot, int64_t T, int64_t C, int64_t D,               \
-                         const int64_t* rows, int64_t nrows, REAL* loss, REAL* lse) {        \
+  /* the head transform z(s) (cap A = 0: the plain head, z = s) and dz/ds */                 \
+  static REAL head_z_##SUF(REAL s, REAL cap, REAL tau) {                                     \
+    return cap > 0 ? cap / ((REAL)1 + EXP(-s / tau)) : s;                                    \
+  }                                                                                          \
+  static REAL head_dz_##SUF(REAL z, REAL cap, REAL tau) {                                    \
+    return cap > 0 ? z * (cap - z) / (cap * tau) : (REAL)1;                                  \
+  }                                                                                          \
+                                                                                             \
+  void orc_forward_head_##SUF(const IN_T* H, const IN_T* W, const int32_t* cand,             \
+                              const int32_t* slot, int64_t T, int64_t C, int64_t D,          \
+                              REAL cap, REAL tau, const int64_t* rows, int64_t nrows,        \
+                              REAL* loss, REAL* lse) {                                       \
     int64_t n = rows ? nrows : T;                                                            \
     _Pragma("omp parallel")                                                                  \
     {                                                                                        \
@@ -192,6 +212,7 @@ int orc_build_candidates(const int32_t* targets, int64_t T, int64_t V, int64_t C
       for (int64_t i = 0; i < n; ++i) {                                                      \
         int64_t t = rows ? rows[i] : i;                                                      \
         logits_##SUF(H, W, cand, C, D, t, s);                                                \
+        for (int64_t j = 0; j < C; ++j) s[j] = head_z_##SUF(s[j], cap, tau);                 \
         REAL m = s[0];                                                                       \
         for (int64_t j = 1; j < C; ++j)                                                      \
           if (s[j] > m) m = s[j];                                                            \
@@ -206,10 +227,10 @@ int orc_build_candidates(const int32_t* targets, int64_t T, int64_t V, int64_t C
   }                                                                                          \
                                                                                              \
   /* dH rows: needs lse of those tokens (lse_rows packed like rows) */                       \
-  void orc_backward_dH_##SUF(const IN_T* H, const IN_T* W, const int32_t* cand,              \
-                             const int32_t* slot, const REAL* lse_rows, int64_t T,           \
-                             int64_t C, int64_t D, REAL scale, const int64_t* rows,          \
-                             int64_t nrows, REAL* dH) {                                      \
+  void orc_backward_dH_head_##SUF(const IN_T* H, const IN_T* W, const int32_t* cand,         \
+                                  const int32_t* slot, const REAL* lse_rows, int64_t T,      \
+                                  int64_t C, int64_t D, REAL cap, REAL tau, REAL scale,      \
+                                  const int64_t* rows, int64_t nrows, REAL* dH) {            \
     int64_t n = rows ? nrows : T;                                                            \
     _Pragma("omp parallel")                                                                  \
     {                                                                                        \
@@ -222,7 +243,8 @@ int orc_build_candidates(const int32_t* targets, int64_t T, int64_t V, int64_t C
         for (int64_t d = 0; d < D; ++d) out[d] = 0;                                          \
         for (int64_t j = 0; j < C; ++j) {                                                    \
           REAL y = (j == slot[t]) ? (REAL)1 : (REAL)0;                                       \
-          REAL g = scale * (EXP(s[j] - lse_rows[i]) - y);                                    \
+          REAL z = head_z_##SUF(s[j], cap, tau);                                             \
+          REAL g = scale * (EXP(z - lse_rows[i]) - y) * head_dz_##SUF(z, cap, tau);          \
           const IN_T* w = W + (int64_t)cand[j] * D;                                          \
           for (int64_t d = 0; d < D; ++d) out[d] += g * (REAL)LOAD(w[d]);                    \
         }                                                                                    \
@@ -232,10 +254,10 @@ int orc_build_candidates(const int32_t* targets, int64_t T, int64_t V, int64_t C
   }                                                                                          \
                                                                                              \
   /* dW_c rows (candidate index j): needs lse of ALL T tokens */                             \
-  void orc_backward_dW_##SUF(const IN_T* H, const IN_T* W, const int32_t* cand,              \
-                             const int32_t* slot, const REAL* lse, int64_t T, int64_t C,     \
-                             int64_t D, REAL scale, const int64_t* cols, int64_t ncols,      \
-                             REAL* dWc) {                                                    \
+  void orc_backward_dW_head_##SUF(const IN_T* H, const IN_T* W, const int32_t* cand,         \
+                                  const int32_t* slot, const REAL* lse, int64_t T, int64_t C, \
+                                  int64_t D, REAL cap, REAL tau, REAL scale,                 \
+                                  const int64_t* cols, int64_t ncols, REAL* dWc) {           \
     int64_t n = cols ? ncols : C;                                                            \
     _Pragma("omp parallel for schedule(dynamic, 1)")                                         \
     for (int64_t i = 0; i < n; ++i) {                                                        \
@@ -248,10 +270,32 @@ int orc_build_candidates(const int32_t* targets, int64_t T, int64_t V, int64_t C
         REAL st = 0;                                                                         \
         for (int64_t d = 0; d < D; ++d) st += (REAL)LOAD(h[d]) * (REAL)LOAD(w[d]);           \
         REAL y = (j == slot[t]) ? (REAL)1 : (REAL)0;                                         \
-        REAL g = scale * (EXP(st - lse[t]) - y);                                             \
+        REAL z = head_z_##SUF(st, cap, tau);                                                 \
+        REAL g = scale * (EXP(z - lse[t]) - y) * head_dz_##SUF(z, cap, tau);                 \
         for (int64_t d = 0; d < D; ++d) out[d] += g * (REAL)LOAD(h[d]);                      \
       }                                                                                      \
     }                                                                                        \
+  }                                                                                          \
+                                                                                             \
+  /* the plain head */                                                                       \
+  void orc_forward_##SUF(const IN_T* H, const IN_T* W, const int32_t* cand,                  \
+                         const int32_t* slot, int64_t T, int64_t C, int64_t D,               \
+                         const int64_t* rows, int64_t nrows, REAL* loss, REAL* lse) {        \
+    orc_forward_head_##SUF(H, W, cand, slot, T, C, D, 0, 1, rows, nrows, loss, lse);         \
+  }                                                                                          \
+  void orc_backward_dH_##SUF(const IN_T* H, const IN_T* W, const int32_t* cand,              \
+                             const int32_t* slot, const REAL* lse_rows, int64_t T,           \
+                             int64_t C, int64_t D, REAL scale, const int64_t* rows,          \
+                             int64_t nrows, REAL* dH) {                                      \
+    orc_backward_dH_head_##SUF(H, W, cand, slot, lse_rows, T, C, D, 0, 1, scale, rows,       \
+                               nrows, dH);                                                   \
+  }                                                                                          \
+  void orc_backward_dW_##SUF(const IN_T* H, const IN_T* W, const int32_t* cand,              \
+                             const int32_t* slot, const REAL* lse, int64_t T, int64_t C,     \
+                             int64_t D, REAL scale, const int64_t* cols, int64_t ncols,      \
+                             REAL* dWc) {                                                    \
+    orc_backward_dW_head_##SUF(H, W, cand, slot, lse, T, C, D, 0, 1, scale, cols, ncols,     \
+                               dWc);                                                         \
   }
 
 ORC_DEFINE(float, f32, uint16_t, LOAD_BF16, expf, logf)

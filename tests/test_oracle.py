@@ -170,10 +170,14 @@ def _case(T, V, D, C, seed, w_std=0.3, s=1.1):
     return x, C
 
 
-def _torch_ref(H64, W64, cand, slot, scale=1.0):
+def _torch_ref(H64, W64, cand, slot, scale=1.0, cap=0.0, tau=1.0):
+    """torch autograd of the loss; cap > 0 applies cap * sigmoid(logits / tau)
+    (torch's own sigmoid) to the logits first."""
     Ht = torch.tensor(H64, requires_grad=True)
     Wt = torch.tensor(W64, requires_grad=True)
     logits = Ht @ Wt[torch.from_numpy(cand.astype(np.int64))].T
+    if cap > 0:
+        logits = cap * torch.sigmoid(logits / tau)
     y = torch.from_numpy(slot.astype(np.int64))
     loss = F.cross_entropy(logits, y, reduction="none")
     (scale * loss.sum()).backward()
@@ -358,8 +362,13 @@ def test_row_subsets_match_full(orc):
 # ------------------------------------------------------ planted mistakes
 
 MUTATIONS = [
-    ("drop one-hot term in dH", "REAL g = scale * (EXP(s[j] - lse_rows[i]) - y);",
-     "REAL g = scale * (EXP(s[j] - lse_rows[i]));"),
+    ("drop one-hot term in dH", "REAL g = scale * (EXP(z - lse_rows[i]) - y) *",
+     "REAL g = scale * (EXP(z - lse_rows[i])) *"),
+    ("capped head: dz/ds factor dropped in dW",
+     "REAL g = scale * (EXP(z - lse[t]) - y) * head_dz_##SUF(z, cap, tau);",
+     "REAL g = scale * (EXP(z - lse[t]) - y);"),
+    ("capped head: logistic of +s", "cap / ((REAL)1 + EXP(-s / tau))", "cap / ((REAL)1 + EXP(s / tau))"),
+    ("capped head: dz/ds without (A - z)", "z * (cap - z) / (cap * tau)", "z / tau"),
     ("sign of the log-sum", "REAL l = m + LOG(sum);", "REAL l = m - LOG(sum);"),
     ("transposed operand in dW", "for (int64_t d = 0; d < D; ++d) out[d] += g * (REAL)LOAD(h[d]);",
      "for (int64_t d = 0; d < D; ++d) out[d] += g * (REAL)LOAD(w[d]);"),
@@ -399,6 +408,18 @@ def _battery(orc):
         failed.append("dH")
     if not np.allclose(dWc, gW[cand], rtol=1e-8, atol=1e-12):
         failed.append("dW")
+    # the capped head against torch autograd of cap * sigmoid(logits / tau)
+    cap, tau = 6.0, 0.7
+    loss, _, gH, gW = _torch_ref(_f64(x["H"]), _f64(x["W"]), cand, slot, cap=cap, tau=tau)
+    l64, s64 = orc.forward(x["H"], x["W"], cand, slot, dtype=np.float64, cap=cap, tau=tau)
+    if not np.allclose(l64, loss, rtol=1e-10):
+        failed.append("capped forward")
+    dH = orc.backward_dH(x["H"], x["W"], cand, slot, s64, dtype=np.float64, cap=cap, tau=tau)
+    dWc = orc.backward_dWc(x["H"], x["W"], cand, slot, s64, dtype=np.float64, cap=cap, tau=tau)
+    if not np.allclose(dH, gH, rtol=1e-8, atol=1e-12):
+        failed.append("capped dH")
+    if not np.allclose(dWc, gW[cand], rtol=1e-8, atol=1e-12):
+        failed.append("capped dW")
     return failed
 
 
@@ -428,3 +449,100 @@ def test_pins_catch_planted_mistakes(orc, tmp_path):
                         "-o", str(so), str(mut), "-lm"], check=True)
         failed = _battery_in_subprocess(so)
         assert failed, f"planted mistake not caught: {name}"
+
+
+# ----------------------------------------------------- the capped head variant
+
+CAPS = [(30.0, 7.5), (6.0, 0.7), (15.0, 3.0)]
+
+
+@pytest.mark.parametrize("cap,tau", CAPS)
+def test_capped_head_against_torch_autograd(orc, cap, tau):
+    """z = cap * sigmoid(s / tau), the loss and both gradients, against torch
+    (its sigmoid, its cross-entropy, its autograd) in fp64; the fp32 oracle
+    within fp32 rounding of it."""
+    T, V, D, C = 30, 400, 24, 90
+    x, C = _case(T, V, D, C, 7, w_std=0.3)
+    cand, slot, _ = orc.build_candidates(x["targets"], V, C, 7)
+    loss, lse, gH, gW = _torch_ref(_f64(x["H"]), _f64(x["W"]), cand, slot, scale=0.5, cap=cap,
+                                   tau=tau)
+    l64, s64 = orc.forward(x["H"], x["W"], cand, slot, dtype=np.float64, cap=cap, tau=tau)
+    np.testing.assert_allclose(l64, loss, rtol=1e-12)
+    np.testing.assert_allclose(s64, lse, rtol=1e-12)
+    dH = orc.backward_dH(x["H"], x["W"], cand, slot, s64, 0.5, dtype=np.float64, cap=cap, tau=tau)
+    dWc = orc.backward_dWc(x["H"], x["W"], cand, slot, s64, 0.5, dtype=np.float64, cap=cap,
+                           tau=tau)
+    np.testing.assert_allclose(dH, gH, rtol=1e-9, atol=1e-13)
+    np.testing.assert_allclose(dWc, gW[cand], rtol=1e-9, atol=1e-13)
+    l32, _ = orc.forward(x["H"], x["W"], cand, slot, cap=cap, tau=tau)
+    np.testing.assert_allclose(l32, loss, rtol=2e-5, atol=1e-6)
+
+
+def test_capped_head_is_a_shifted_tanh_softcap(orc):
+    """cap * sigmoid(s / tau) = cap/2 + (cap/2) tanh(s / (2 tau)), and softmax
+    ignores the shift: the loss equals cross-entropy of the symmetric softcap
+    (cap/2) tanh(s / (2 tau)), written here with numpy's tanh."""
+    T, V, D, C = 25, 300, 16, 70
+    x, C = _case(T, V, D, C, 8, w_std=0.5)
+    cand, slot, _ = orc.build_candidates(x["targets"], V, C, 8)
+    cap, tau = 20.0, 2.5
+    S = _f64(x["H"]) @ _f64(x["W"])[cand].T
+    z = (cap / 2) * np.tanh(S / (2 * tau))
+    m = z.max(1, keepdims=True)
+    lse = (m + np.log(np.exp(z - m).sum(1, keepdims=True)))[:, 0]
+    expect = lse - z[np.arange(T), slot]
+    l64, _ = orc.forward(x["H"], x["W"], cand, slot, dtype=np.float64, cap=cap, tau=tau)
+    np.testing.assert_allclose(l64, expect, rtol=1e-12)
+
+
+def test_capped_head_uniform_logits_closed_form(orc):
+    """W = 0: every z = cap / 2, so loss = ln C, dH = 0, and
+    dW[cand[j]] = scale * cap / (4 tau) * sum_t (1/C - [slot[t] = j]) H[t]."""
+    T, V, D, C = 20, 100, 8, 37
+    x, C = _case(T, V, D, C, 9)
+    x["W"] = np.zeros_like(x["W"])
+    cand, slot, _ = orc.build_candidates(x["targets"], V, C, 9)
+    cap, tau, scale = 12.0, 1.5, 0.3
+    l64, s64 = orc.forward(x["H"], x["W"], cand, slot, dtype=np.float64, cap=cap, tau=tau)
+    np.testing.assert_allclose(l64, np.log(C), rtol=1e-14)
+    dH = orc.backward_dH(x["H"], x["W"], cand, slot, s64, scale, dtype=np.float64, cap=cap, tau=tau)
+    assert np.all(dH == 0)
+    dWc = orc.backward_dWc(x["H"], x["W"], cand, slot, s64, scale, dtype=np.float64, cap=cap,
+                           tau=tau)
+    H64 = _f64(x["H"])
+    Y = np.zeros((T, C))
+    Y[np.arange(T), slot] = 1
+    expect = scale * cap / (4 * tau) * ((1.0 / C - Y).T @ H64)
+    np.testing.assert_allclose(dWc, expect, rtol=1e-10, atol=1e-14)
+
+
+def test_capped_head_finite_differences(orc):
+    """Central differences in fp64 over every element of H and of the candidate
+    rows of W, with the capped head."""
+    T, V, D, C = 3, 12, 5, 6
+    rng = np.random.default_rng(10)
+    H = rng.normal(size=(T, D))
+    W = rng.normal(size=(V, D))
+    targets = rng.integers(0, V, T).astype(np.int32)
+    cand, slot, _ = orc.build_candidates(targets, V, C, 10)
+    cap, tau, scale = 5.0, 0.8, 1.0
+    _, lse = orc.forward(H, W, cand, slot, dtype=np.float64, cap=cap, tau=tau)
+    dH = orc.backward_dH(H, W, cand, slot, lse, scale, dtype=np.float64, cap=cap, tau=tau)
+    dWc = orc.backward_dWc(H, W, cand, slot, lse, scale, dtype=np.float64, cap=cap, tau=tau)
+
+    def total(Hx, Wx):
+        return orc.forward(Hx, Wx, cand, slot, dtype=np.float64, cap=cap, tau=tau)[0].sum()
+
+    eps = 1e-6
+    for (t, d) in np.ndindex(T, D):
+        Hp, Hm = H.copy(), H.copy()
+        Hp[t, d] += eps
+        Hm[t, d] -= eps
+        fd = (total(Hp, W) - total(Hm, W)) / (2 * eps)
+        assert abs(fd - dH[t, d]) <= 1e-6 * max(1.0, abs(fd))
+    for (j, d) in np.ndindex(C, D):
+        Wp, Wm = W.copy(), W.copy()
+        Wp[cand[j], d] += eps
+        Wm[cand[j], d] -= eps
+        fd = (total(H, Wp) - total(H, Wm)) / (2 * eps)
+        assert abs(fd - dWc[j, d]) <= 1e-6 * max(1.0, abs(fd))
