@@ -62,6 +62,9 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="target CPU seconds of the oracle sample")
+    ap.add_argument("--cap", type=float, default=0.0,
+                    help="capped head: logits z = cap / (1 + exp(-s / tau)) (0: plain head)")
+    ap.add_argument("--tau", type=float, default=7.5)
     ap.add_argument("--ref-step-seconds", type=float, default=None,
                     help="reference arm: target seconds per step (default: fits the run in ~2.5 min)")
     return ap.parse_args()
@@ -224,28 +227,28 @@ def barrier(world: int):
 
 # ------------------------------------------------------------- CPU oracle
 
-def oracle_sample(x: dict, w, T_s: int, scale: float):
+def oracle_sample(x: dict, w, T_s: int, scale: float, cap: float = 0.0, tau: float = 1.0):
     """One oracle pass over a bounded sample: the full-batch candidate build,
     then forward + backward for the first T_s tokens against that candidate
-    set. Returns seconds."""
+    set (with the same head as the native arm). Returns seconds."""
     import oracle
     t0 = time.perf_counter()
     cand, slot, U = oracle.build_candidates(x["targets"], w.V, w.C, w.seed)
     Hs = x["H"][:T_s]
     ss_ = slot[:T_s]
-    loss, lse = oracle.forward(Hs, x["W"], cand, ss_)
-    oracle.backward_dH(Hs, x["W"], cand, ss_, lse, scale)
-    oracle.backward_dWc(Hs, x["W"], cand, ss_, lse, scale)
+    loss, lse = oracle.forward(Hs, x["W"], cand, ss_, cap=cap, tau=tau)
+    oracle.backward_dH(Hs, x["W"], cand, ss_, lse, scale, cap=cap, tau=tau)
+    oracle.backward_dWc(Hs, x["W"], cand, ss_, lse, scale, cap=cap, tau=tau)
     return time.perf_counter() - t0
 
 
-def cpu_baseline(x: dict, w, target_s: float) -> dict:
+def cpu_baseline(x: dict, w, target_s: float, cap: float = 0.0, tau: float = 1.0) -> dict:
     import oracle
     oracle.build()
     scale = 1.0 / w.T
-    t_small = oracle_sample(x, w, 16, scale)
+    t_small = oracle_sample(x, w, 16, scale, cap, tau)
     T_s = int(max(16, min(w.T, 16 * target_s / max(t_small, 1e-3))))
-    dt = oracle_sample(x, w, T_s, scale)
+    dt = oracle_sample(x, w, T_s, scale, cap, tau)
     return {"value": T_s / dt, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
             "sample": (f"{w.name}: full-batch candidate build (T={w.T}) + forward/backward of the "
                        f"first {T_s} tokens against all C={w.C} candidates; {dt:.1f} s"),
@@ -277,14 +280,16 @@ def run_native(args, world, rank, local):
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     scale = 1.0 / T
 
+    cap, tau = args.cap, args.tau
+
     def step(h=H, tg=targets):
         ss.step(h, W, tg, C, w.seed, ws, scale=scale, dW=dW, cand=cand, slot=slot, loss=loss,
-                lse=lse, dH=dH)
+                lse=lse, dH=dH, cap=cap, tau=tau)
 
     def step_three_calls(h=H, tg=targets):
         ss.build_candidates(tg, V, C, w.seed, ws, cand=cand, slot=slot)
-        ss.forward(h, W, cand, slot, ws, loss=loss, lse=lse)
-        ss.backward(h, W, cand, slot, lse, ws, scale=scale, dH=dH, dW=dW)
+        ss.forward(h, W, cand, slot, ws, loss=loss, lse=lse, cap=cap, tau=tau)
+        ss.backward(h, W, cand, slot, lse, ws, scale=scale, dH=dH, dW=dW, cap=cap, tau=tau)
 
     for _ in range(max(args.warmup, 1)):
         flush.zero_()
@@ -362,7 +367,7 @@ def run_native(args, world, rank, local):
 
     # the same step replayed from a CUDA graph of ss_step (ss_step_graph_*)
     graph = ss.StepGraph(H, W, targets, C, ws, scale=scale, cand=cand, slot=slot, loss=loss,
-                         lse=lse, dH=dH, dW=dW)
+                         lse=lse, dH=dH, dW=dW, cap=cap, tau=tau)
     graph.launch(w.seed)
     sg = [torch.cuda.Event(enable_timing=True) for _ in range(K3)]
     eg = [torch.cuda.Event(enable_timing=True) for _ in range(K3)]
@@ -444,6 +449,8 @@ def run_native(args, world, rank, local):
                    "seed": w.seed, "parallelism": f"replicas x{world}" if world > 1 else "single",
                    "l2": "flushed between steps (256 MB write, outside the timed events)",
                    "step": "ss_step (= ss_build_candidates + ss_forward + ss_backward in one call)",
+                   "head": ({"cap": cap, "tau": tau, "logits": "cap / (1 + exp(-s / tau))"}
+                            if cap else "plain"),
                    "ms_per_step_three_calls": three_calls_ms,
                    "ms_per_step_graph": graph_ms,
                    "step_tflops_algorithmic_6TCD": step_tflops,
@@ -473,13 +480,13 @@ def run_reference(args, world, rank):
     per_step_s = (args.ref_step_seconds if args.ref_step_seconds is not None
                   else min(5.0, 150.0 / max(K + W_, 1)))
     scale = 1.0 / w.T
-    t_small = oracle_sample(x, w, 8, scale)
+    t_small = oracle_sample(x, w, 8, scale, args.cap, args.tau)
     T_s = int(max(1, min(w.T, 8 * per_step_s / max(t_small, 1e-3))))
     for _ in range(W_):
-        oracle_sample(x, w, T_s, scale)
+        oracle_sample(x, w, T_s, scale, args.cap, args.tau)
     dt = 0.0
     for _ in range(K):
-        dt += oracle_sample(x, w, T_s, scale)
+        dt += oracle_sample(x, w, T_s, scale, args.cap, args.tau)
     value = T_s * K / dt
     cores = oracle.num_threads()
     sample = (f"{w.name}: per step, full-batch candidate build (T={w.T}) + forward/backward of "
@@ -506,7 +513,7 @@ def main():
     line, x, w = run_native(args, world, rank, local)
     if rank == 0:
         if world == 1 and not args.no_cpu_baseline:
-            line["cpu_baseline"] = cpu_baseline(x, w, args.cpu_seconds)
+            line["cpu_baseline"] = cpu_baseline(x, w, args.cpu_seconds, args.cap, args.tau)
         else:
             line["cpu_baseline"] = None
         print(json.dumps(line), flush=True)

@@ -144,6 +144,34 @@ ss_status ss_backward(const uint16_t* H, const uint16_t* W, const int32_t* cand,
                       void* workspace, size_t workspace_bytes, ss_stream stream);
 
 /*
+ * Head options ("KellerJordan/modded-nanogpt" README, technique list: the
+ * head's logits are rescaled asymmetrically and soft-capped; the pages give
+ * no formula). With cap > 0 every candidate logit s passes through
+ *   z = cap / (1 + exp(-s / tau))          (bounded to (0, cap))
+ * before the softmax: lse and loss are of z, and the backward multiplies
+ * G by dz/ds = z (cap - z) / (cap tau). Up to a shift, which the softmax
+ * ignores, z is the symmetric soft cap (cap/2) tanh(s / (2 tau)).
+ *   cap : 0 (or a NULL ss_head pointer) -> the plain head; else finite > 0.
+ *   tau : finite > 0 when cap > 0.
+ * Other values -> SS_ERR_INVALID. The *_head entry points below take it; the
+ * same head must be passed to the forward and the backward of one batch.
+ */
+typedef struct ss_head {
+  float cap;
+  float tau;
+} ss_head;
+
+ss_status ss_forward_head(const uint16_t* H, const uint16_t* W, const int32_t* cand,
+                          const int32_t* slot, int64_t T, int64_t V, int64_t C, int64_t D,
+                          const ss_head* head, float* loss, float* lse, void* workspace,
+                          size_t workspace_bytes, ss_stream stream);
+ss_status ss_backward_head(const uint16_t* H, const uint16_t* W, const int32_t* cand,
+                           const int32_t* slot, const float* lse, int64_t T, int64_t V,
+                           int64_t C, int64_t D, const ss_head* head, float scale,
+                           int accumulate, uint16_t* dH, float* dW, void* workspace,
+                           size_t workspace_bytes, ss_stream stream);
+
+/*
  * One training step of the loss in a single call: ss_build_candidates (with
  * U_host = NULL), ss_forward and ss_backward on the same batch, with the same
  * arguments and results as those three calls. The candidate rows W[cand] are
@@ -155,6 +183,12 @@ ss_status ss_step(const int32_t* targets, const uint16_t* H, const uint16_t* W, 
                   int64_t V, int64_t C, int64_t D, uint64_t seed, float scale, int accumulate,
                   int32_t* cand, int32_t* slot, float* loss, float* lse, uint16_t* dH, float* dW,
                   void* workspace, size_t workspace_bytes, ss_stream stream);
+/* ss_step with head options (see ss_head). */
+ss_status ss_step_head(const int32_t* targets, const uint16_t* H, const uint16_t* W, int64_t T,
+                       int64_t V, int64_t C, int64_t D, uint64_t seed, const ss_head* head,
+                       float scale, int accumulate, int32_t* cand, int32_t* slot, float* loss,
+                       float* lse, uint16_t* dH, float* dW, void* workspace,
+                       size_t workspace_bytes, ss_stream stream);
 
 /*
  * The pages' candidate schedule ("NanoGPT Training Record: Technical
@@ -187,7 +221,7 @@ ss_status ss_clear_rows(const int32_t* rows, int64_t n, int64_t V, int64_t D, fl
  * ss_step captured once into a CUDA graph and replayed ("NanoGPT Training
  * Record: Technical Optimizations & Speed", "Key Optimizations and Ablation
  * Table Results": training-step graph capture). ss_step_graph_create records
- * ss_step with the given arguments (all of them fixed for the graph's life:
+ * ss_step_head (head may be NULL: the plain head) with the given arguments (all of them fixed for the graph's life:
  * the same buffers, shapes, scale and accumulate flag; the buffers' contents
  * may change between launches) without running it. ss_step_graph_launch
  * runs it on `stream` with `seed` for the candidate build; results are those
@@ -198,9 +232,9 @@ ss_status ss_clear_rows(const int32_t* rows, int64_t n, int64_t V, int64_t D, fl
  */
 typedef struct ss_step_graph ss_step_graph;
 ss_status ss_step_graph_create(const int32_t* targets, const uint16_t* H, const uint16_t* W,
-                               int64_t T, int64_t V, int64_t C, int64_t D, float scale,
-                               int accumulate, int32_t* cand, int32_t* slot, float* loss,
-                               float* lse, uint16_t* dH, float* dW, void* workspace,
+                               int64_t T, int64_t V, int64_t C, int64_t D, const ss_head* head,
+                               float scale, int accumulate, int32_t* cand, int32_t* slot,
+                               float* loss, float* lse, uint16_t* dH, float* dW, void* workspace,
                                size_t workspace_bytes, ss_step_graph** graph);
 ss_status ss_step_graph_launch(ss_step_graph* graph, uint64_t seed, ss_stream stream);
 void ss_step_graph_destroy(ss_step_graph* graph);
@@ -219,7 +253,7 @@ void ss_step_graph_destroy(ss_step_graph* graph);
  * fixed-size array inside the library's own device data, of
  * SS_NOALLOC_SCRATCH_BYTES. Every GPU that loads the library holds that array
  * until the process exits. Sizes whose scratch, 1 KB + C*D*2 +
- * ceil(C/256)*T*8 + T*4 bytes (each term rounded up to 1 KB), exceeds it are
+ * ceil(C/256)*T*16 + T*4 bytes (each term rounded up to 1 KB), exceeds it are
  * rejected with SS_ERR_UNSUPPORTED (ss_last_error says by how much).
  *   status_host : NULL, or a host int32 that receives the device status
  *                 word of this call after the stream is synchronised; the

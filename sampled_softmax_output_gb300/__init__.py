@@ -39,6 +39,15 @@ MAX_D = 16384
 NOALLOC_SCRATCH_BYTES = 32 << 20
 
 
+class Head(ctypes.Structure):
+    """ss_head: cap > 0 -> logits z = cap / (1 + exp(-s / tau)); cap = 0 -> plain."""
+    _fields_ = [("cap", ctypes.c_float), ("tau", ctypes.c_float)]
+
+
+def _head(cap: float, tau: float):
+    return None if cap == 0 else ctypes.byref(Head(float(cap), float(tau)))
+
+
 class SSError(RuntimeError):
     def __init__(self, code: int, where: str):
         self.code = int(code)
@@ -82,13 +91,22 @@ def _load():
     L.ss_trace_end.argtypes = []
     L.ss_trace_kernel_name.restype = ctypes.c_char_p
     L.ss_trace_kernel_name.argtypes = [ctypes.c_int]
+    hp = ctypes.POINTER(Head)
+    L.ss_forward_head.restype = ctypes.c_int
+    L.ss_forward_head.argtypes = [p, p, p, p, i64, i64, i64, i64, hp, p, p, p, sz, p]
+    L.ss_backward_head.restype = ctypes.c_int
+    L.ss_backward_head.argtypes = [p, p, p, p, p, i64, i64, i64, i64, hp, ctypes.c_float,
+                                   ctypes.c_int, p, p, p, sz, p]
+    L.ss_step_head.restype = ctypes.c_int
+    L.ss_step_head.argtypes = [p, p, p, i64, i64, i64, i64, ctypes.c_uint64, hp, ctypes.c_float,
+                               ctypes.c_int, p, p, p, p, p, p, p, sz, p]
     L.ss_schedule_candidates.restype = i64
     L.ss_schedule_candidates.argtypes = [i64, i64, i64]
     L.ss_clear_rows.restype = ctypes.c_int
     L.ss_clear_rows.argtypes = [p, i64, i64, i64, p, p, sz, p]
     L.ss_step_graph_create.restype = ctypes.c_int
-    L.ss_step_graph_create.argtypes = [p, p, p, i64, i64, i64, i64, ctypes.c_float, ctypes.c_int,
-                                       p, p, p, p, p, p, p, sz, ctypes.POINTER(p)]
+    L.ss_step_graph_create.argtypes = [p, p, p, i64, i64, i64, i64, hp, ctypes.c_float,
+                                       ctypes.c_int, p, p, p, p, p, p, p, sz, ctypes.POINTER(p)]
     L.ss_step_graph_launch.restype = ctypes.c_int
     L.ss_step_graph_launch.argtypes = [p, ctypes.c_uint64, p]
     L.ss_step_graph_destroy.restype = None
@@ -184,8 +202,10 @@ def build_candidates(targets: torch.Tensor, V: int, C: int, seed: int, ws: torch
 
 
 def forward(H: torch.Tensor, W: torch.Tensor, cand: torch.Tensor, slot: torch.Tensor,
-            ws: torch.Tensor, loss: torch.Tensor | None = None, lse: torch.Tensor | None = None):
-    """Per-token loss [T] and log-sum-exp [T] (fp32) over the candidate rows."""
+            ws: torch.Tensor, loss: torch.Tensor | None = None, lse: torch.Tensor | None = None,
+            cap: float = 0.0, tau: float = 1.0):
+    """Per-token loss [T] and log-sum-exp [T] (fp32) over the candidate rows
+    (cap > 0: of the capped logits, ss_forward_head)."""
     _need(H, "H", torch.bfloat16)
     dev = H.device
     T, D = H.shape
@@ -202,8 +222,13 @@ def forward(H: torch.Tensor, W: torch.Tensor, cand: torch.Tensor, slot: torch.Te
         lse = torch.empty(T, dtype=torch.float32, device=dev)
     _need(loss, "loss", torch.float32, dev, (T,))
     _need(lse, "lse", torch.float32, dev, (T,))
-    code = _lib.ss_forward(_ptr(H), _ptr(W), _ptr(cand), _ptr(slot), T, V, C, D, _ptr(loss),
-                           _ptr(lse), _ptr(ws), ws.numel(), _stream(dev))
+    if cap == 0:
+        code = _lib.ss_forward(_ptr(H), _ptr(W), _ptr(cand), _ptr(slot), T, V, C, D, _ptr(loss),
+                               _ptr(lse), _ptr(ws), ws.numel(), _stream(dev))
+    else:
+        code = _lib.ss_forward_head(_ptr(H), _ptr(W), _ptr(cand), _ptr(slot), T, V, C, D,
+                                    _head(cap, tau), _ptr(loss), _ptr(lse), _ptr(ws), ws.numel(),
+                                    _stream(dev))
     _check(code, "ss_forward")
     return loss, lse
 
@@ -236,7 +261,8 @@ def forward_noalloc(H: torch.Tensor, W: torch.Tensor, cand: torch.Tensor, slot: 
 
 def backward(H: torch.Tensor, W: torch.Tensor, cand: torch.Tensor, slot: torch.Tensor,
              lse: torch.Tensor, ws: torch.Tensor, scale: float = 1.0, accumulate: bool = False,
-             dH: torch.Tensor | None = None, dW: torch.Tensor | None = None):
+             dH: torch.Tensor | None = None, dW: torch.Tensor | None = None, cap: float = 0.0,
+             tau: float = 1.0):
     """dH [T, D] bf16 and dW [V, D] fp32 (only candidate rows written / added to).
     A new dW is zero-filled, so that it is the dense gradient."""
     _need(H, "H", torch.bfloat16)
@@ -256,9 +282,14 @@ def backward(H: torch.Tensor, W: torch.Tensor, cand: torch.Tensor, slot: torch.T
         dW = torch.zeros(V, D, dtype=torch.float32, device=dev)
     _need(dH, "dH", torch.bfloat16, dev, (T, D))
     _need(dW, "dW", torch.float32, dev, (V, D))
-    code = _lib.ss_backward(_ptr(H), _ptr(W), _ptr(cand), _ptr(slot), _ptr(lse), T, V, C, D,
-                            float(scale), 1 if accumulate else 0, _ptr(dH), _ptr(dW), _ptr(ws),
-                            ws.numel(), _stream(dev))
+    if cap == 0:
+        code = _lib.ss_backward(_ptr(H), _ptr(W), _ptr(cand), _ptr(slot), _ptr(lse), T, V, C, D,
+                                float(scale), 1 if accumulate else 0, _ptr(dH), _ptr(dW),
+                                _ptr(ws), ws.numel(), _stream(dev))
+    else:
+        code = _lib.ss_backward_head(_ptr(H), _ptr(W), _ptr(cand), _ptr(slot), _ptr(lse), T, V,
+                                     C, D, _head(cap, tau), float(scale), 1 if accumulate else 0,
+                                     _ptr(dH), _ptr(dW), _ptr(ws), ws.numel(), _stream(dev))
     _check(code, "ss_backward")
     return dH, dW
 
@@ -312,7 +343,7 @@ class KernelTrace:
 
 
 def step(H, W, targets, C: int, seed: int, ws, scale: float = 1.0, dW=None, accumulate=False,
-         cand=None, slot=None, loss=None, lse=None, dH=None):
+         cand=None, slot=None, loss=None, lse=None, dH=None, cap: float = 0.0, tau: float = 1.0):
     """One full pass of the path in one call (ss_step): candidates, forward,
     backward, with one gather of the candidate rows shared by both passes."""
     _need(H, "H", torch.bfloat16)
@@ -332,20 +363,28 @@ def step(H, W, targets, C: int, seed: int, ws, scale: float = 1.0, dW=None, accu
                                (loss, "loss", torch.float32, (T,)), (lse, "lse", torch.float32, (T,)),
                                (dH, "dH", torch.bfloat16, (T, D)), (dW, "dW", torch.float32, (V, D))):
         _need(t, name, dt, dev, shape)
-    code = _lib.ss_step(_ptr(targets), _ptr(H), _ptr(W), T, V, C, D, seed & (2**64 - 1),
-                        float(scale), 1 if accumulate else 0, _ptr(cand), _ptr(slot), _ptr(loss),
-                        _ptr(lse), _ptr(dH), _ptr(dW), _ptr(ws), ws.numel(), _stream(dev))
+    if cap == 0:
+        code = _lib.ss_step(_ptr(targets), _ptr(H), _ptr(W), T, V, C, D, seed & (2**64 - 1),
+                            float(scale), 1 if accumulate else 0, _ptr(cand), _ptr(slot),
+                            _ptr(loss), _ptr(lse), _ptr(dH), _ptr(dW), _ptr(ws), ws.numel(),
+                            _stream(dev))
+    else:
+        code = _lib.ss_step_head(_ptr(targets), _ptr(H), _ptr(W), T, V, C, D, seed & (2**64 - 1),
+                                 _head(cap, tau), float(scale), 1 if accumulate else 0,
+                                 _ptr(cand), _ptr(slot), _ptr(loss), _ptr(lse), _ptr(dH),
+                                 _ptr(dW), _ptr(ws), ws.numel(), _stream(dev))
     _check(code, "ss_step")
     return {"cand": cand, "slot": slot, "loss": loss, "lse": lse, "dH": dH, "dW": dW}
 
 
 def step_separate(H, W, targets, C: int, seed: int, ws, scale: float = 1.0, dW=None,
-                  accumulate=False):
+                  accumulate=False, cap: float = 0.0, tau: float = 1.0):
     """The same pass as three calls: ss_build_candidates, ss_forward, ss_backward."""
     V = W.shape[0]
     cand, slot = build_candidates(targets, V, C, seed, ws)
-    loss, lse = forward(H, W, cand, slot, ws)
-    dH, dW = backward(H, W, cand, slot, lse, ws, scale=scale, accumulate=accumulate, dW=dW)
+    loss, lse = forward(H, W, cand, slot, ws, cap=cap, tau=tau)
+    dH, dW = backward(H, W, cand, slot, lse, ws, scale=scale, accumulate=accumulate, dW=dW,
+                      cap=cap, tau=tau)
     return {"cand": cand, "slot": slot, "loss": loss, "lse": lse, "dH": dH, "dW": dW}
 
 
@@ -378,7 +417,8 @@ class StepGraph:
     on the current stream."""
 
     def __init__(self, H, W, targets, C: int, ws, scale: float = 1.0, accumulate=False,
-                 cand=None, slot=None, loss=None, lse=None, dH=None, dW=None):
+                 cand=None, slot=None, loss=None, lse=None, dH=None, dW=None, cap: float = 0.0,
+                 tau: float = 1.0):
         _need(H, "H", torch.bfloat16)
         dev = H.device
         T, D = H.shape
@@ -403,7 +443,8 @@ class StepGraph:
         self.device = dev
         h = ctypes.c_void_p()
         code = _lib.ss_step_graph_create(_ptr(targets), _ptr(H), _ptr(W), T, V, C, D,
-                                         float(scale), 1 if accumulate else 0, _ptr(self.cand),
+                                         _head(cap, tau), float(scale), 1 if accumulate else 0,
+                                         _ptr(self.cand),
                                          _ptr(self.slot), _ptr(self.loss), _ptr(self.lse),
                                          _ptr(self.dH), _ptr(self.dW), _ptr(ws), ws.numel(),
                                          ctypes.byref(h))

@@ -10,6 +10,7 @@
 #include <stdio.h>
 
 #include <atomic>
+#include <cmath>
 #include <mutex>
 #include <vector>
 
@@ -41,7 +42,7 @@ Layout make_layout(int64_t T, int64_t C, int64_t D) {
   L.wc = off;
   off = align_up(off + static_cast<size_t>(C) * D * 2, 1024);
   L.part = off;
-  off = align_up(off + static_cast<size_t>(L.n_ct) * kFwdGroups * T * sizeof(float2), 1024);
+  off = align_up(off + static_cast<size_t>(L.n_ct) * kFwdGroupsMax * T * sizeof(float2), 1024);
   L.tgt = off;
   off = align_up(off + static_cast<size_t>(T) * sizeof(float), 1024);
   L.g = off;
@@ -296,8 +297,8 @@ ss_status enqueue_gather(const uint16_t* W, const int32_t* cand, int64_t C, int6
 
 // forward GEMM (LSE partials, target logit) and the LSE merge, from W_c
 ss_status enqueue_forward(const uint16_t* H, const int32_t* slot, int64_t T, int64_t C, int64_t D,
-                          float* loss, float* lse, const Layout& L, char* ws, int nsm,
-                          cudaStream_t s) {
+                          float cap, float tau, float* loss, float* lse, const Layout& L,
+                          char* ws, int nsm, cudaStream_t s) {
   int* status = reinterpret_cast<int*>(ws + L.hdr);
   uint16_t* Wc = reinterpret_cast<uint16_t*>(ws + L.wc);
   float2* part = reinterpret_cast<float2*>(ws + L.part);
@@ -307,15 +308,16 @@ ss_status enqueue_forward(const uint16_t* H, const int32_t* slot, int64_t T, int
     return fail("cuTensorMapEncodeTiled", cudaErrorInvalidValue);
   trace_pre(s, "gemm_forward_lse");
   const cudaError_t e = launch_forward_logits(tH, tWc, static_cast<int>(T), static_cast<int>(C),
-                                              static_cast<int>(D), slot, part, tgt, status, nsm,
-                                              s);
+                                              static_cast<int>(D), slot, part, tgt, cap, tau,
+                                              status, nsm, s);
   trace_post(s);
   if (e != cudaSuccess) return fail("launch gemm_forward_lse", e);
   const int blocks = static_cast<int>((T * kMergeLanes + 255) / 256);
   trace_pre(s, "lse_merge");
   const cudaError_t em =
       launch_pdl(k_lse_merge, dim3(blocks), dim3(256), 0, s, part, tgt, slot, static_cast<int>(T),
-                 static_cast<int>(C), static_cast<int>(L.n_ct * kFwdGroups), loss, lse, status);
+                 static_cast<int>(C), static_cast<int>(L.n_ct * fwd_groups(cap)), loss, lse,
+                 status);
   trace_post(s);
   return cuda_status(em, "launch k_lse_merge");
 }
@@ -323,8 +325,8 @@ ss_status enqueue_forward(const uint16_t* H, const int32_t* slot, int64_t T, int
 // softmax-gradient GEMM and the two gradient GEMMs, from W_c
 ss_status enqueue_backward(const uint16_t* H, const int32_t* cand, const int32_t* slot,
                            const float* lse, int64_t T, int64_t V, int64_t C, int64_t D,
-                           float scale, int accumulate, uint16_t* dH, float* dW, const Layout& L,
-                           char* ws, int nsm, cudaStream_t s) {
+                           float cap, float tau, float scale, int accumulate, uint16_t* dH,
+                           float* dW, const Layout& L, char* ws, int nsm, cudaStream_t s) {
   int* status = reinterpret_cast<int*>(ws + L.hdr);
   uint16_t* Wc = reinterpret_cast<uint16_t*>(ws + L.wc);
   uint16_t* G = reinterpret_cast<uint16_t*>(ws + L.g);
@@ -339,7 +341,8 @@ ss_status enqueue_backward(const uint16_t* H, const int32_t* cand, const int32_t
     return fail("cuTensorMapEncodeTiled", cudaErrorInvalidValue);
   trace_pre(s, "gemm_softmax_grad");
   cudaError_t e =
-      launch_softmax_grad(tH, tWc, tWc2, tGk, iT, iC, iD, slot, lse, scale, status, nsm, s);
+      launch_softmax_grad(tH, tWc, tWc2, tGk, iT, iC, iD, slot, lse, scale, cap, tau, status,
+                          nsm, s);
   trace_post(s);
   if (e != cudaSuccess) return fail("launch gemm_softmax_grad", e);
   trace_pre(s, "gemm_grads");
@@ -466,10 +469,10 @@ ss_status ss_build_candidates(const int32_t* targets, int64_t T, int64_t V, int6
   return SS_OK;
 }
 
-ss_status ss_forward(const uint16_t* H, const uint16_t* W, const int32_t* cand,
-                     const int32_t* slot, int64_t T, int64_t V, int64_t C, int64_t D,
-                     float* loss, float* lse, void* workspace, size_t workspace_bytes,
-                     ss_stream stream) {
+static ss_status forward_impl(const uint16_t* H, const uint16_t* W, const int32_t* cand,
+                              const int32_t* slot, int64_t T, int64_t V, int64_t C, int64_t D,
+                              float cap, float tau, float* loss, float* lse, void* workspace,
+                              size_t workspace_bytes, ss_stream stream) {
   const ss_status st = check_sizes(T, V, C, D);
   if (st != SS_OK) return st;
   if (!W || !cand || !workspace || (T > 0 && (!H || !slot || !loss || !lse)))
@@ -487,13 +490,14 @@ ss_status ss_forward(const uint16_t* H, const uint16_t* W, const int32_t* cand,
   const ss_status sg = enqueue_gather(W, cand, C, V, D, reinterpret_cast<uint16_t*>(ws + L.wc),
                                       reinterpret_cast<int*>(ws + L.hdr), nsm, s);
   if (sg != SS_OK) return sg;
-  return enqueue_forward(H, slot, T, C, D, loss, lse, L, ws, nsm, s);
+  return enqueue_forward(H, slot, T, C, D, cap, tau, loss, lse, L, ws, nsm, s);
 }
 
-ss_status ss_backward(const uint16_t* H, const uint16_t* W, const int32_t* cand,
-                      const int32_t* slot, const float* lse, int64_t T, int64_t V, int64_t C,
-                      int64_t D, float scale, int accumulate, uint16_t* dH, float* dW,
-                      void* workspace, size_t workspace_bytes, ss_stream stream) {
+static ss_status backward_impl(const uint16_t* H, const uint16_t* W, const int32_t* cand,
+                               const int32_t* slot, const float* lse, int64_t T, int64_t V,
+                               int64_t C, int64_t D, float cap, float tau, float scale,
+                               int accumulate, uint16_t* dH, float* dW, void* workspace,
+                               size_t workspace_bytes, ss_stream stream) {
   const ss_status st = check_sizes(T, V, C, D);
   if (st != SS_OK) return st;
   if (!W || !cand || !dW || !workspace || (T > 0 && (!H || !slot || !lse || !dH)))
@@ -513,13 +517,15 @@ ss_status ss_backward(const uint16_t* H, const uint16_t* W, const int32_t* cand,
   const ss_status sg =
       enqueue_gather(W, cand, C, V, D, reinterpret_cast<uint16_t*>(ws + L.wc), status, nsm, s);
   if (sg != SS_OK) return sg;
-  return enqueue_backward(H, cand, slot, lse, T, V, C, D, scale, accumulate, dH, dW, L, ws, nsm, s);
+  return enqueue_backward(H, cand, slot, lse, T, V, C, D, cap, tau, scale, accumulate, dH, dW, L,
+                          ws, nsm, s);
 }
 
-ss_status ss_step(const int32_t* targets, const uint16_t* H, const uint16_t* W, int64_t T,
-                  int64_t V, int64_t C, int64_t D, uint64_t seed, float scale, int accumulate,
-                  int32_t* cand, int32_t* slot, float* loss, float* lse, uint16_t* dH, float* dW,
-                  void* workspace, size_t workspace_bytes, ss_stream stream) {
+static ss_status step_impl(const int32_t* targets, const uint16_t* H, const uint16_t* W,
+                           int64_t T, int64_t V, int64_t C, int64_t D, uint64_t seed, float cap,
+                           float tau, float scale, int accumulate, int32_t* cand, int32_t* slot,
+                           float* loss, float* lse, uint16_t* dH, float* dW, void* workspace,
+                           size_t workspace_bytes, ss_stream stream) {
   const ss_status st = step_args_status(targets, H, W, T, V, C, D, accumulate, cand, slot, loss,
                                         lse, dH, dW, workspace, workspace_bytes);
   if (st != SS_OK) return st;
@@ -536,9 +542,82 @@ ss_status ss_step(const int32_t* targets, const uint16_t* H, const uint16_t* W, 
   // one gather of W[cand] serves the forward and the backward
   ss_status r = enqueue_gather(W, cand, C, V, D, reinterpret_cast<uint16_t*>(ws + L.wc), status, nsm, s);
   if (r != SS_OK) return r;
-  r = enqueue_forward(H, slot, T, C, D, loss, lse, L, ws, nsm, s);
+  r = enqueue_forward(H, slot, T, C, D, cap, tau, loss, lse, L, ws, nsm, s);
   if (r != SS_OK) return r;
-  return enqueue_backward(H, cand, slot, lse, T, V, C, D, scale, accumulate, dH, dW, L, ws, nsm, s);
+  return enqueue_backward(H, cand, slot, lse, T, V, C, D, cap, tau, scale, accumulate, dH, dW, L,
+                          ws, nsm, s);
+}
+
+// the head options: NULL or cap == 0 is the plain head
+static ss_status head_args(const ss_head* head, float* cap, float* tau) {
+  *cap = 0.f;
+  *tau = 1.f;
+  if (!head || head->cap == 0.f) return SS_OK;
+  if (!(head->cap > 0.f) || !std::isfinite(head->cap) || !(head->tau > 0.f) ||
+      !std::isfinite(head->tau))
+    return SS_ERR_INVALID;
+  *cap = head->cap;
+  *tau = head->tau;
+  return SS_OK;
+}
+
+ss_status ss_forward(const uint16_t* H, const uint16_t* W, const int32_t* cand,
+                     const int32_t* slot, int64_t T, int64_t V, int64_t C, int64_t D,
+                     float* loss, float* lse, void* workspace, size_t workspace_bytes,
+                     ss_stream stream) {
+  return forward_impl(H, W, cand, slot, T, V, C, D, 0.f, 1.f, loss, lse, workspace,
+                      workspace_bytes, stream);
+}
+
+ss_status ss_forward_head(const uint16_t* H, const uint16_t* W, const int32_t* cand,
+                          const int32_t* slot, int64_t T, int64_t V, int64_t C, int64_t D,
+                          const ss_head* head, float* loss, float* lse, void* workspace,
+                          size_t workspace_bytes, ss_stream stream) {
+  float cap, tau;
+  const ss_status h = head_args(head, &cap, &tau);
+  if (h != SS_OK) return h;
+  return forward_impl(H, W, cand, slot, T, V, C, D, cap, tau, loss, lse, workspace,
+                      workspace_bytes, stream);
+}
+
+ss_status ss_backward(const uint16_t* H, const uint16_t* W, const int32_t* cand,
+                      const int32_t* slot, const float* lse, int64_t T, int64_t V, int64_t C,
+                      int64_t D, float scale, int accumulate, uint16_t* dH, float* dW,
+                      void* workspace, size_t workspace_bytes, ss_stream stream) {
+  return backward_impl(H, W, cand, slot, lse, T, V, C, D, 0.f, 1.f, scale, accumulate, dH, dW,
+                       workspace, workspace_bytes, stream);
+}
+
+ss_status ss_backward_head(const uint16_t* H, const uint16_t* W, const int32_t* cand,
+                           const int32_t* slot, const float* lse, int64_t T, int64_t V,
+                           int64_t C, int64_t D, const ss_head* head, float scale,
+                           int accumulate, uint16_t* dH, float* dW, void* workspace,
+                           size_t workspace_bytes, ss_stream stream) {
+  float cap, tau;
+  const ss_status h = head_args(head, &cap, &tau);
+  if (h != SS_OK) return h;
+  return backward_impl(H, W, cand, slot, lse, T, V, C, D, cap, tau, scale, accumulate, dH, dW,
+                       workspace, workspace_bytes, stream);
+}
+
+ss_status ss_step(const int32_t* targets, const uint16_t* H, const uint16_t* W, int64_t T,
+                  int64_t V, int64_t C, int64_t D, uint64_t seed, float scale, int accumulate,
+                  int32_t* cand, int32_t* slot, float* loss, float* lse, uint16_t* dH, float* dW,
+                  void* workspace, size_t workspace_bytes, ss_stream stream) {
+  return step_impl(targets, H, W, T, V, C, D, seed, 0.f, 1.f, scale, accumulate, cand, slot, loss,
+                   lse, dH, dW, workspace, workspace_bytes, stream);
+}
+
+ss_status ss_step_head(const int32_t* targets, const uint16_t* H, const uint16_t* W, int64_t T,
+                       int64_t V, int64_t C, int64_t D, uint64_t seed, const ss_head* head,
+                       float scale, int accumulate, int32_t* cand, int32_t* slot, float* loss,
+                       float* lse, uint16_t* dH, float* dW, void* workspace,
+                       size_t workspace_bytes, ss_stream stream) {
+  float cap, tau;
+  const ss_status h = head_args(head, &cap, &tau);
+  if (h != SS_OK) return h;
+  return step_impl(targets, H, W, T, V, C, D, seed, cap, tau, scale, accumulate, cand, slot, loss,
+                   lse, dH, dW, workspace, workspace_bytes, stream);
 }
 
 int64_t ss_schedule_candidates(int64_t step, int64_t total_steps, int64_t V) {
@@ -620,13 +699,13 @@ ss_status ss_forward_noalloc(const uint16_t* H, const uint16_t* W, const int32_t
     return fail("cuTensorMapEncodeTiled", cudaErrorInvalidValue);
   trace_pre(s, "gemm_forward_lse");
   e = launch_forward_logits(tH, tWc, static_cast<int>(T), static_cast<int>(C),
-                            static_cast<int>(D), slot, part, tgt, status, nsm, s);
+                            static_cast<int>(D), slot, part, tgt, 0.f, 1.f, status, nsm, s);
   trace_post(s);
   if (e != cudaSuccess) return fail("launch gemm_forward_lse", e);
   trace_pre(s, "lse_merge");
   e = launch_pdl(k_lse_merge, dim3(static_cast<int>((T * kMergeLanes + 255) / 256)), dim3(256), 0, s,
                  part, tgt, slot, static_cast<int>(T), static_cast<int>(C),
-                 static_cast<int>(L.n_ct * kFwdGroups), loss, lse, status);
+                 static_cast<int>(L.n_ct * fwd_groups(0.f)), loss, lse, status);
   trace_post(s);
   if (e != cudaSuccess) return fail("launch k_lse_merge", e);
   if (status_host) {
@@ -679,14 +758,17 @@ const char* ss_trace_kernel_name(int k) {
 }
 
 ss_status ss_step_graph_create(const int32_t* targets, const uint16_t* H, const uint16_t* W,
-                               int64_t T, int64_t V, int64_t C, int64_t D, float scale,
-                               int accumulate, int32_t* cand, int32_t* slot, float* loss,
-                               float* lse, uint16_t* dH, float* dW, void* workspace,
+                               int64_t T, int64_t V, int64_t C, int64_t D, const ss_head* head,
+                               float scale, int accumulate, int32_t* cand, int32_t* slot,
+                               float* loss, float* lse, uint16_t* dH, float* dW, void* workspace,
                                size_t workspace_bytes, ss_step_graph** graph) {
   if (!graph) return SS_ERR_INVALID;
   *graph = nullptr;
-  const ss_status st = step_args_status(targets, H, W, T, V, C, D, accumulate, cand, slot, loss,
-                                        lse, dH, dW, workspace, workspace_bytes);
+  float cap, tau;
+  ss_status st = head_args(head, &cap, &tau);
+  if (st != SS_OK) return st;
+  st = step_args_status(targets, H, W, T, V, C, D, accumulate, cand, slot, loss, lse, dH, dW,
+                        workspace, workspace_bytes);
   if (st != SS_OK) return st;
   // record ss_step on a private stream
   cudaStream_t cs = nullptr;
@@ -697,8 +779,8 @@ ss_status ss_step_graph_create(const int32_t* targets, const uint16_t* H, const 
     cudaStreamDestroy(cs);
     return fail("cudaStreamBeginCapture", e);
   }
-  const ss_status r = ss_step(targets, H, W, T, V, C, D, 0, scale, accumulate, cand, slot, loss,
-                              lse, dH, dW, workspace, workspace_bytes, cs);
+  const ss_status r = step_impl(targets, H, W, T, V, C, D, 0, cap, tau, scale, accumulate, cand,
+                                slot, loss, lse, dH, dW, workspace, workspace_bytes, cs);
   cudaGraph_t g = nullptr;
   e = cudaStreamEndCapture(cs, &g);
   cudaStreamDestroy(cs);

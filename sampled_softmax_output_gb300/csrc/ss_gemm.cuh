@@ -94,13 +94,26 @@ __device__ __forceinline__ void for_tmem_chunks(uint32_t taddr, int c_begin, F&&
   }
 }
 
+// The capped head: z = cap / (1 + exp(-s / tau)) = cap * 1 / (1 + 2^(-s k1)),
+// k1 = log2(e) / tau, and dz/ds = z (cap - z) icap_tau, icap_tau = 1 / (cap tau).
+struct HeadCap {
+  float cap, k1, icap_tau;
+};
+__device__ __forceinline__ float head_z(float s, const HeadCap& h) {
+  return h.cap * rcp_approx(1.f + ex2_approx(-s * h.k1));
+}
+__device__ __forceinline__ float head_dz(float z, const HeadCap& h) {
+  return z * (h.cap - z) * h.icap_tau;
+}
+
 // Forward: per-row softmax partials of one 128 x BN logit tile.
 //   With NCG column groups per tile (NCG epilogue warps per row block), group
 //   cg covers columns [cg * BN / NCG, (cg + 1) * BN / NCG) of the tile and
 //   writes part[nt * NCG + cg][t] = (max_j S[t,j], sum_j exp(S[t,j] - max))
 //   over its valid columns, or (-inf, 0) if it has none; tgt[t] = S[t, slot[t]]
 //   comes from the group that holds slot[t].
-struct EpiFwd {
+template <bool CAP>
+struct EpiFwdT {
   static constexpr int kStageBytes = 0;
   static constexpr bool kKeepOperands = false;
   struct Params {
@@ -109,6 +122,7 @@ struct EpiFwd {
     float2* part;
     float* tgt;
     int* status;
+    HeadCap head;  // used when CAP: the partials and the target logit are of z
   };
   __device__ static void finish(const Params&, EpiState&) {}
   template <int BN, int NCG>
@@ -127,19 +141,23 @@ struct EpiFwd {
         const int jc = i * 32;
         const int nv = min(32, ncols - jc);
         if (nv <= 0) return;
+        float v[32];
+#pragma unroll
+        for (int k = 0; k < 32; ++k)
+          v[k] = CAP ? head_z(__uint_as_float(r[k]), p.head) : __uint_as_float(r[k]);
         float cm = -INFINITY;
 #pragma unroll
         for (int k = 0; k < 32; ++k)
-          if (k < nv) cm = fmaxf(cm, __uint_as_float(r[k]));
+          if (k < nv) cm = fmaxf(cm, v[k]);
         const float nm = fmaxf(m, cm);
         const float nm2 = nm * kLog2e;
         float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
 #pragma unroll
         for (int k = 0; k < 32; k += 4) {
-          if (k + 0 < nv) a0 += ex2_approx(fmaf(__uint_as_float(r[k + 0]), kLog2e, -nm2));
-          if (k + 1 < nv) a1 += ex2_approx(fmaf(__uint_as_float(r[k + 1]), kLog2e, -nm2));
-          if (k + 2 < nv) a2 += ex2_approx(fmaf(__uint_as_float(r[k + 2]), kLog2e, -nm2));
-          if (k + 3 < nv) a3 += ex2_approx(fmaf(__uint_as_float(r[k + 3]), kLog2e, -nm2));
+          if (k + 0 < nv) a0 += ex2_approx(fmaf(v[k + 0], kLog2e, -nm2));
+          if (k + 1 < nv) a1 += ex2_approx(fmaf(v[k + 1], kLog2e, -nm2));
+          if (k + 2 < nv) a2 += ex2_approx(fmaf(v[k + 2], kLog2e, -nm2));
+          if (k + 3 < nv) a3 += ex2_approx(fmaf(v[k + 3], kLog2e, -nm2));
         }
         s = s * ex2_approx((m - nm) * kLog2e) + ((a0 + a1) + (a2 + a3));
         m = nm;
@@ -147,7 +165,7 @@ struct EpiFwd {
         if (static_cast<unsigned>(off) < static_cast<unsigned>(nv)) {
 #pragma unroll
           for (int k = 0; k < 32; ++k)
-            if (k == off) tg = __uint_as_float(r[k]);
+            if (k == off) tg = v[k];
           has_t = true;
         }
       });
@@ -158,6 +176,7 @@ struct EpiFwd {
     }
   }
 };
+using EpiFwd = EpiFwdT<false>;
 
 // Backward, step 1: G[t, j] = scale * (exp(S[t,j] - lse[t]) - [j == slot[t]]), bf16.
 // Folded form: scale * exp(x - lse) = sign(scale) * 2^(x*log2e - (lse*log2e - log2|scale|)).
@@ -167,7 +186,8 @@ struct EpiFwd {
 // writes leave as full lines instead of 32 rows per warp instruction. The
 // one-hot term touches one element per row: it is recomputed in fp32 and
 // patched into the staged tile.
-struct EpiG {
+template <bool CAP>
+struct EpiGT {
   // two 16 KB staging buffers: both for one column group, one each for two
   static constexpr int kStageBytes = 2 * 16384;
   // G streams through L2 once; the H and W_c tiles are re-read by every CTA
@@ -180,6 +200,7 @@ struct EpiG {
     float scale;       // d(objective)/d(loss)
     float log2_scale;  // log2|scale| (-inf for 0)
     int* status;
+    HeadCap head;      // used when CAP: G = scale * (P(z) - Y) * dz/ds
   };
   __device__ static void finish(const Params&, EpiState& es) {
     if ((es.ep_tid & 127) == 0) bulk_wait<0>();
@@ -228,8 +249,16 @@ struct EpiG {
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          const float g0 = ex2_approx(fmaf(__uint_as_float(r[2 * i]), kLog2e, -off2));
-          const float g1 = ex2_approx(fmaf(__uint_as_float(r[2 * i + 1]), kLog2e, -off2));
+          float g0, g1;
+          if constexpr (CAP) {
+            const float z0 = head_z(__uint_as_float(r[2 * i]), p.head);
+            const float z1 = head_z(__uint_as_float(r[2 * i + 1]), p.head);
+            g0 = ex2_approx(fmaf(z0, kLog2e, -off2)) * head_dz(z0, p.head);
+            g1 = ex2_approx(fmaf(z1, kLog2e, -off2)) * head_dz(z1, p.head);
+          } else {
+            g0 = ex2_approx(fmaf(__uint_as_float(r[2 * i]), kLog2e, -off2));
+            g1 = ex2_approx(fmaf(__uint_as_float(r[2 * i + 1]), kLog2e, -off2));
+          }
           pk[i] = pack_bf16x2(g0, g1) ^ sgn;
         }
 #pragma unroll
@@ -245,7 +274,13 @@ struct EpiG {
 #pragma unroll
           for (int i = 0; i < 32; ++i) xt = (i == off) ? __uint_as_float(r[i]) : xt;
           if (has) {
-            const float gt = ex2_approx(fmaf(xt, kLog2e, -off2)) - asc;
+            float gt;
+            if constexpr (CAP) {
+              const float zt = head_z(xt, p.head);
+              gt = (ex2_approx(fmaf(zt, kLog2e, -off2)) - asc) * head_dz(zt, p.head);
+            } else {
+              gt = ex2_approx(fmaf(xt, kLog2e, -off2)) - asc;
+            }
             const uint16_t bits = bf16_bits(gt) ^ static_cast<uint16_t>(sgn & 0xffffu);
             const uint32_t cc = static_cast<uint32_t>(32 * h + off);
             st_shared_b16(rowbase + (((cc >> 3) ^ r7) << 4) + (cc & 7u) * 2u, bits);
@@ -262,6 +297,7 @@ struct EpiG {
     }
   }
 };
+using EpiG = EpiGT<false>;
 
 // Backward, step 2: dH tile -> bf16 (column group cg of NCG).
 struct EpiDh {

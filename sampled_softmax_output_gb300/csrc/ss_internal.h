@@ -43,7 +43,11 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
 // Tile widths of the GEMMs (output columns per tile).
 constexpr int kBnLogits = 256;  // logit tiles: forward and softmax-gradient
 constexpr int kBnGrad = 256;    // dH and dW tiles along D
-constexpr int kFwdGroups = 1;    // softmax partials per row per logit tile
+// Softmax partials per row per logit tile: 1 for the plain head (four
+// epilogue warps), 2 for the capped head (eight warps in two column groups:
+// its epilogue does three MUFU operations per logit); the workspace holds 2.
+constexpr int kFwdGroupsMax = 2;
+inline int fwd_groups(float cap) { return cap > 0.f ? 2 : 1; }
 
 struct GemmShape;
 
@@ -67,15 +71,17 @@ cudaError_t launch_build_candidates(const int32_t* targets, int T, int V, int C,
 // ---- logit GEMMs (ss_gemm_logits.cu): A = H [T, D] (K-major), B = W_c [C, D] (K-major)
 // tWc: box 64 x 256 (one 1-CTA tile); tWc_half: box 64 x 128 (a CTA's half of
 // a pair's tile).
+// cap > 0: the capped head z = cap / (1 + exp(-s / tau)) replaces the logits.
 cudaError_t launch_forward_logits(const CUtensorMap& tH, const CUtensorMap& tWc, int T, int C,
                                   int D, const int32_t* slot, float2* part, float* tgt,
-                                  int* status, int num_sms, cudaStream_t stream);
+                                  float cap, float tau, int* status, int num_sms,
+                                  cudaStream_t stream);
 // G is written through tG_store: G [T, C] bf16, box 64 x 128, 128-byte swizzle.
 cudaError_t launch_softmax_grad(const CUtensorMap& tH, const CUtensorMap& tWc,
                                 const CUtensorMap& tWc_half,
                                 const CUtensorMap& tG_store, int T, int C, int D,
-                                const int32_t* slot, const float* lse, float scale,
-                                int* status, int num_sms, cudaStream_t stream);
+                                const int32_t* slot, const float* lse, float scale, float cap,
+                                float tau, int* status, int num_sms, cudaStream_t stream);
 
 // ---- gradient GEMMs (ss_gemm_grads.cu)
 // dH = G . W_c : A = G [T, C] (K-major), B = W_c [C, D] (MN-major)

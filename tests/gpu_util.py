@@ -24,7 +24,8 @@ def to_dev_bf16(bits: np.ndarray) -> torch.Tensor:
 
 
 def run_gpu(ss, x: dict, C: int, seed: int, scale: float = 1.0, dW0: np.ndarray | None = None,
-            accumulate: bool = False, ws: torch.Tensor | None = None) -> dict:
+            accumulate: bool = False, ws: torch.Tensor | None = None, cap: float = 0.0,
+            tau: float = 1.0) -> dict:
     H = to_dev_bf16(x["H"])
     W = to_dev_bf16(x["W"])
     T, D = H.shape
@@ -33,10 +34,11 @@ def run_gpu(ss, x: dict, C: int, seed: int, scale: float = 1.0, dW0: np.ndarray 
     if ws is None:
         ws = ss.workspace(T, V, C, D)
     cand, slot, U = ss.build_candidates(targets, V, C, seed, ws, return_U=True)
-    loss, lse = ss.forward(H, W, cand, slot, ws)
+    loss, lse = ss.forward(H, W, cand, slot, ws, cap=cap, tau=tau)
     dW = (torch.from_numpy(np.ascontiguousarray(dW0, np.float32)).cuda() if dW0 is not None
           else torch.zeros(V, D, dtype=torch.float32, device="cuda"))
-    dH, dW = ss.backward(H, W, cand, slot, lse, ws, scale=scale, accumulate=accumulate, dW=dW)
+    dH, dW = ss.backward(H, W, cand, slot, lse, ws, scale=scale, accumulate=accumulate, dW=dW,
+                         cap=cap, tau=tau)
     torch.cuda.synchronize()
     status, _ = ss.read_status(ws)
     return {"cand": cand.cpu().numpy(), "slot": slot.cpu().numpy(), "U": U,

@@ -20,7 +20,8 @@ def test_exports_every_declared_symbol():
                           "ss_trace_begin", "ss_trace_end", "ss_trace_kernel_name",
                           "ss_last_error", "ss_forward_noalloc", "ss_step",
                           "ss_schedule_candidates", "ss_clear_rows", "ss_step_graph_create",
-                          "ss_step_graph_launch", "ss_step_graph_destroy"}
+                          "ss_step_graph_launch", "ss_step_graph_destroy", "ss_forward_head",
+                          "ss_backward_head", "ss_step_head"}
     for n in names:
         assert hasattr(ss.lib(), n), n
 
@@ -194,7 +195,8 @@ def test_step_graph_argument_errors():
                  wsb=1 << 40)
         a.update(kw)
         return L.ss_step_graph_create(p(a["targets"]), p(a["H"]), p(a["W"]), a["T"], a["V"],
-                                      a["C"], a["D"], a["scale"], a["acc"], p(a["cand"]),
+                                      a["C"], a["D"], a.get("head"), a["scale"], a["acc"],
+                                      p(a["cand"]),
                                       p(a["slot"]), p(a["loss"]), p(a["lse"]), p(a["dH"]),
                                       p(a["dW"]), p(a["ws"]), a["wsb"], ctypes.byref(h))
 
@@ -205,3 +207,30 @@ def test_step_graph_argument_errors():
     assert h.value is None                          # nothing was created
     assert L.ss_step_graph_launch(None, 0, None) == INVALID
     L.ss_step_graph_destroy(None)                   # a no-op
+
+
+def test_head_argument_errors():
+    """Head options: cap 0 (or NULL) is the plain head; a negative or
+    non-finite cap, or a capped head without a positive finite tau, is invalid."""
+    L = ss.lib()
+    a = dict(H=FAKE, W=FAKE, cand=FAKE, slot=FAKE, T=256, V=50304, C=4096, D=768)
+
+    def fwd(head, wsb=1 << 40):
+        return L.ss_forward_head(p(a["H"]), p(a["W"]), p(a["cand"]), p(a["slot"]), 0, a["V"],
+                                 a["C"], a["D"], head, p(FAKE), p(FAKE), p(FAKE), wsb, None)
+
+    def step(head):
+        return L.ss_step_head(p(FAKE), p(FAKE), p(FAKE), 0, 50304, 4096, 768, 0, head, 1.0, 0,
+                              p(FAKE), p(FAKE), p(FAKE), p(FAKE), p(FAKE), p(FAKE), p(FAKE),
+                              16, None)
+
+    assert fwd(None) == OK and fwd(ctypes.byref(ss.Head(0.0, 0.0))) == OK  # T = 0: no-op
+    for cap, tau in ((-1.0, 1.0), (30.0, 0.0), (30.0, -2.0), (float("inf"), 1.0),
+                     (float("nan"), 1.0), (30.0, float("nan"))):
+        h = ctypes.byref(ss.Head(cap, tau))
+        assert fwd(h) == INVALID, (cap, tau)
+        assert step(h) == INVALID, (cap, tau)
+        bwd = L.ss_backward_head(p(FAKE), p(FAKE), p(FAKE), p(FAKE), p(FAKE), 0, 50304, 4096, 768,
+                                 h, 1.0, 0, p(FAKE), p(FAKE), p(FAKE), 1 << 40, None)
+        assert bwd == INVALID, (cap, tau)
+    assert fwd(ctypes.byref(ss.Head(30.0, 7.5)), wsb=16) == WORKSPACE

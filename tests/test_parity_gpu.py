@@ -25,9 +25,9 @@ def _case(T, V, D, C, seed, s=1.1, w_std=0.02):
     return x, max(C, U)
 
 
-def _full_oracle(orc, x, C, seed, scale=1.0, dW0=None, accumulate=False):
+def _full_oracle(orc, x, C, seed, scale=1.0, dW0=None, accumulate=False, cap=0.0, tau=1.0):
     return orc.loss_and_grads(x["H"], x["W"], x["targets"], C, seed, scale, dW_init=dW0,
-                              accumulate=accumulate)
+                              accumulate=accumulate, cap=cap, tau=tau)
 
 
 SMALL = [
@@ -112,7 +112,7 @@ def test_uniform_logits_ln_C(orc):
 
 # ------------------------------------------------------------- full sizes
 
-def _check_sampled(orc, x, T, V, D, C, seed, rng_seed, exact_cols):
+def _check_sampled(orc, x, T, V, D, C, seed, rng_seed, exact_cols, cap=0.0, tau=1.0):
     """The whole path on one batch: candidates bit-exact, sampled token rows of
     loss/lse/dH against the oracle, dW rows outside the candidate set
     untouched, two identities of the gradients, and (exact_cols) some dW
@@ -126,11 +126,11 @@ def _check_sampled(orc, x, T, V, D, C, seed, rng_seed, exact_cols):
     assert U == U_ref
     np.testing.assert_array_equal(cand.cpu().numpy(), cand_ref)
     np.testing.assert_array_equal(slot.cpu().numpy(), slot_ref)
-    loss, lse = ss.forward(H, W, cand, slot, ws)
+    loss, lse = ss.forward(H, W, cand, slot, ws, cap=cap, tau=tau)
     canary = 7.0
     dW = torch.full((V, D), canary, dtype=torch.float32, device="cuda")
     scale = 1.0 / T
-    dH, dW = ss.backward(H, W, cand, slot, lse, ws, scale=scale, dW=dW)
+    dH, dW = ss.backward(H, W, cand, slot, lse, ws, scale=scale, dW=dW, cap=cap, tau=tau)
     torch.cuda.synchronize()
     assert ss.read_status(ws)[0] == 0
     loss, lse = loss.cpu().numpy(), lse.cpu().numpy()
@@ -141,10 +141,11 @@ def _check_sampled(orc, x, T, V, D, C, seed, rng_seed, exact_cols):
     rows = np.unique(np.concatenate([[0, T - 1, (T // 128) * 128 - 1, (T // 256) * 256],
                                      rng.integers(0, T, 45)]))
     rows = rows[(rows >= 0) & (rows < T)]
-    l_ref, s_ref = orc.forward(x["H"], x["W"], cand_ref, slot_ref, rows=rows)
+    l_ref, s_ref = orc.forward(x["H"], x["W"], cand_ref, slot_ref, rows=rows, cap=cap, tau=tau)
     assert_loss_close(loss[rows], l_ref)
     assert_loss_close(lse[rows], s_ref)
-    dH_ref = orc.backward_dH(x["H"], x["W"], cand_ref, slot_ref, s_ref, scale, rows=rows)
+    dH_ref = orc.backward_dH(x["H"], x["W"], cand_ref, slot_ref, s_ref, scale, rows=rows, cap=cap,
+                             tau=tau)
     assert rel_fro(dH[rows], dH_ref) < GRAD_RTOL
     # rows of dW outside the candidate set keep the canary bit for bit
     outside = np.setdiff1d(np.arange(V), cand_ref)
@@ -152,7 +153,9 @@ def _check_sampled(orc, x, T, V, D, C, seed, rng_seed, exact_cols):
     assert np.all(dW[outside] == canary)
     dWc = dW[cand_ref].astype(np.float64)
     # rows of P - Y sum to zero, so the candidate-row gradients sum to zero
-    assert np.linalg.norm(dWc.sum(0)) <= 0.02 * np.linalg.norm(dWc)
+    # (not with a capped head: G carries the per-logit factor dz/ds)
+    if cap == 0:
+        assert np.linalg.norm(dWc.sum(0)) <= 0.02 * np.linalg.norm(dWc)
     # <dW_c, W_c> = sum_tj G_tj S_tj = <dH, H>
     W64 = synth.bf16_bits_to_f32(x["W"]).astype(np.float64)
     H64 = synth.bf16_bits_to_f32(x["H"]).astype(np.float64)
@@ -161,7 +164,7 @@ def _check_sampled(orc, x, T, V, D, C, seed, rng_seed, exact_cols):
     assert abs(lhs - rhs) <= 0.02 * abs(rhs)
     # the fused entry point (one gather for both passes) gives the same bits
     # as the three calls
-    fused = ss.step(H, W, targets, C, seed, ws, scale=scale,
+    fused = ss.step(H, W, targets, C, seed, ws, scale=scale, cap=cap, tau=tau,
                     dW=torch.full((V, D), canary, dtype=torch.float32, device="cuda"))
     torch.cuda.synchronize()
     assert ss.read_status(ws)[0] == 0
@@ -172,11 +175,12 @@ def _check_sampled(orc, x, T, V, D, C, seed, rng_seed, exact_cols):
     np.testing.assert_array_equal(fused["dW"].cpu().numpy(), dW)
     del fused
     if exact_cols:
-        _, lse_all = orc.forward(x["H"], x["W"], cand_ref, slot_ref)
+        _, lse_all = orc.forward(x["H"], x["W"], cand_ref, slot_ref, cap=cap, tau=tau)
         cols = np.unique(np.array([0, U_ref - 1, min(U_ref, C - 1), C - 1, C // 2, 1,
                                    (C // 256) * 256]))
         cols = cols[cols < C]
-        ref_rows = orc.backward_dWc(x["H"], x["W"], cand_ref, slot_ref, lse_all, scale, cols=cols)
+        ref_rows = orc.backward_dWc(x["H"], x["W"], cand_ref, slot_ref, lse_all, scale, cols=cols,
+                                    cap=cap, tau=tau)
         assert rel_fro(dW[cand_ref[cols]], ref_rows) < GRAD_RTOL
         assert_loss_close(lse, lse_all)
 
@@ -310,3 +314,60 @@ def test_kernel_trace_records_every_launch():
     assert [n for n, _ in tr.timings()] == ["build_candidates", "gather_rows", "gemm_forward_lse",
                                            "lse_merge", "gemm_softmax_grad", "gemm_grads"]
     assert all(ms > 0 for _, ms in tr.timings())
+
+
+# ------------------------------------------------------------ capped head
+
+CAPPED = [
+    # T, V, D, C, seed, scale, cap, tau
+    (1, 64, 64, 1, 1, 1.0, 30.0, 7.5),
+    (300, 3000, 768, 517, 4, 1.0, 30.0, 7.5),     # ragged T and C tails
+    (257, 2000, 192, 1000, 5, 0.5, 6.0, 0.7),     # strongly saturated cap
+    (500, 1000, 128, 1000, 6, 1.0 / 500, 15.0, 3.0),  # C = V
+]
+
+
+@pytest.mark.parametrize("T,V,D,C,seed,scale,cap,tau", CAPPED)
+def test_capped_head_parity(orc, T, V, D, C, seed, scale, cap, tau):
+    """z = cap / (1 + exp(-s / tau)) before the softmax: every element against
+    the oracle of the same head."""
+    x, C = _case(T, V, D, C, seed)
+    x["W"] = synth.make_inputs(1, V, D, 1.1, seed + 50, w_std=0.2)["W"]  # wide logits
+    ref = _full_oracle(orc, x, C, seed, scale, cap=cap, tau=tau)
+    got = run_gpu(ss, x, C, seed, scale, cap=cap, tau=tau)
+    assert got["status"] == 0
+    np.testing.assert_array_equal(got["cand"], ref["cand"])
+    assert_loss_close(got["loss"], ref["loss"])
+    assert_loss_close(got["lse"], ref["lse"])
+    assert rel_fro(got["dH"], ref["dH"]) < GRAD_RTOL
+    assert rel_fro(got["dW"], ref["dW"]) < GRAD_RTOL
+    # and it differs from the plain head (the cap is really applied)
+    plain = _full_oracle(orc, x, C, seed, scale)
+    if C > 1:
+        assert not np.allclose(plain["loss"], ref["loss"], rtol=1e-2)
+
+
+@pytest.mark.parametrize("wid", [2, 4])
+def test_full_size_capped_head(orc, wid):
+    """Workloads T16384_C10240 (single-CTA tiles) and T65536_C24576 (CTA-pair
+    softmax-gradient tiles) with the capped head, as in the plain full-size check."""
+    w = synth.WORKLOADS[wid]
+    x = synth.workload_inputs(w)
+    _check_sampled(orc, x, w.T, w.V, w.D, w.C, w.seed, 200 + wid, exact_cols=wid == 2, cap=30.0,
+                   tau=7.5)
+
+
+def test_capped_graph_replay_equals_step():
+    T, V, D, C, seed = 700, 6000, 768, 1500, 33
+    x, C = _case(T, V, D, C, seed)
+    H, W, tg = to_dev_bf16(x["H"]), to_dev_bf16(x["W"]), _dev(x["targets"])
+    ws, ws2 = ss.workspace(T, V, C, D), ss.workspace(T, V, C, D)
+    g = ss.StepGraph(H, W, tg, C, ws, scale=0.5, cap=15.0, tau=2.0)
+    got = g.launch(seed)
+    ref = ss.step(H, W, tg, C, seed, ws2, scale=0.5, cap=15.0, tau=2.0)
+    plain = ss.step(H, W, tg, C, seed, ss.workspace(T, V, C, D), scale=0.5)
+    torch.cuda.synchronize()
+    for k in ("cand", "slot", "loss", "lse", "dH", "dW"):
+        assert torch.equal(got[k], ref[k]), k
+    assert not torch.equal(got["loss"], plain["loss"])
+    g.close()
