@@ -77,6 +77,18 @@ def load(path: str):
         f = getattr(L, f"orc_backward_dW_head_{suf}")
         f.restype = None
         f.argtypes = [_p, _p, _p, _p, _p, _i64, _i64, _i64, real, real, real, _p, _i64, _p]
+    for suf, real in (("f32", ctypes.c_float), ("f64", ctypes.c_double)):
+        f = getattr(L, f"orc_forward_mtp_{suf}")
+        f.restype = None
+        f.argtypes = [_p, _p, _p, _p, _i64, _p, _i64, _i64, _i64, real, real, _p, _i64, _p, _p]
+        f = getattr(L, f"orc_backward_dH_mtp_{suf}")
+        f.restype = None
+        f.argtypes = [_p, _p, _p, _p, _i64, _p, _p, _i64, _i64, _i64, real, real, real, _p, _i64,
+                      _p]
+        f = getattr(L, f"orc_backward_dW_mtp_{suf}")
+        f.restype = None
+        f.argtypes = [_p, _p, _p, _p, _i64, _p, _p, _i64, _i64, _i64, real, real, real, _p, _i64,
+                      _p]
     L.orc_num_threads.restype = ctypes.c_int
     L.orc_num_threads.argtypes = []
     return L
@@ -224,5 +236,97 @@ def loss_and_grads(H, W, targets, C, seed, scale=1.0, dtype=np.float32, dW_init=
         dW[cand] += dWc
     else:
         dW[cand] = dWc
+    return {"cand": cand, "slot": slot, "U": U, "loss": loss, "lse": lse, "dH": dH, "dW": dW,
+            "dWc": dWc}
+
+
+# -------------------------------------------------- several targets per token
+
+def _mtp_args(slot, weights, real):
+    slot = np.ascontiguousarray(slot, np.int32)
+    assert slot.ndim == 2, "slot is [K, T]"
+    w = np.ascontiguousarray(weights, real)
+    assert w.shape == (slot.shape[0],)
+    return slot, w
+
+
+def forward_mtp(H, W, cand, slot, weights, rows=None, dtype=np.float32, cap=0.0, tau=1.0):
+    """K targets per token (slot [K, T], weights [K]): per-token
+    loss = sum_k w[k] (lse - z[slot[k]]) and lse, for all tokens or the listed rows."""
+    suf, real = _real(dtype)
+    H = _inputs(H, suf)
+    W = _inputs(W, suf)
+    cand = np.ascontiguousarray(cand, np.int32)
+    slot, w = _mtp_args(slot, weights, real)
+    K, T = slot.shape
+    D = H.shape[1]
+    C = cand.shape[0]
+    r, nr = _rows(rows)
+    n = nr if r is not None else T
+    loss = np.empty(n, real)
+    lse = np.empty(n, real)
+    getattr(lib(), f"orc_forward_mtp_{suf}")(_ptr(H), _ptr(W), _ptr(cand), _ptr(slot), K, _ptr(w),
+                                             T, C, D, cap, tau, _ptr(r), nr, _ptr(loss),
+                                             _ptr(lse))
+    return loss, lse
+
+
+def backward_dH_mtp(H, W, cand, slot, weights, lse_rows, scale=1.0, rows=None, dtype=np.float32,
+                    cap=0.0, tau=1.0):
+    suf, real = _real(dtype)
+    H = _inputs(H, suf)
+    W = _inputs(W, suf)
+    cand = np.ascontiguousarray(cand, np.int32)
+    slot, w = _mtp_args(slot, weights, real)
+    K, T = slot.shape
+    D = H.shape[1]
+    C = cand.shape[0]
+    lse_rows = np.ascontiguousarray(lse_rows, real)
+    r, nr = _rows(rows)
+    n = nr if r is not None else T
+    assert lse_rows.shape[0] == n
+    dH = np.empty((n, D), real)
+    getattr(lib(), f"orc_backward_dH_mtp_{suf}")(_ptr(H), _ptr(W), _ptr(cand), _ptr(slot), K,
+                                                 _ptr(w), _ptr(lse_rows), T, C, D, cap, tau,
+                                                 scale, _ptr(r), nr, _ptr(dH))
+    return dH
+
+
+def backward_dWc_mtp(H, W, cand, slot, weights, lse, scale=1.0, cols=None, dtype=np.float32,
+                     cap=0.0, tau=1.0):
+    suf, real = _real(dtype)
+    H = _inputs(H, suf)
+    W = _inputs(W, suf)
+    cand = np.ascontiguousarray(cand, np.int32)
+    slot, w = _mtp_args(slot, weights, real)
+    K, T = slot.shape
+    D = H.shape[1]
+    C = cand.shape[0]
+    lse = np.ascontiguousarray(lse, real)
+    assert lse.shape[0] == T
+    c, nc = _rows(cols)
+    n = nc if c is not None else C
+    dWc = np.empty((n, D), real)
+    getattr(lib(), f"orc_backward_dW_mtp_{suf}")(_ptr(H), _ptr(W), _ptr(cand), _ptr(slot), K,
+                                                 _ptr(w), _ptr(lse), T, C, D, cap, tau, scale,
+                                                 _ptr(c), nc, _ptr(dWc))
+    return dWc
+
+
+def loss_and_grads_mtp(H, W, targets, weights, C, seed, scale=1.0, dtype=np.float32, cap=0.0,
+                       tau=1.0):
+    """targets [K, T]: the candidate set is built over all K*T targets (k-major);
+    returns the same keys as loss_and_grads with slot [K, T]."""
+    targets = np.ascontiguousarray(targets, np.int32)
+    K, T = targets.shape
+    V = W.shape[0]
+    cand, slot_flat, U = build_candidates(targets.reshape(-1), V, C, seed)
+    slot = slot_flat.reshape(K, T)
+    loss, lse = forward_mtp(H, W, cand, slot, weights, dtype=dtype, cap=cap, tau=tau)
+    dH = backward_dH_mtp(H, W, cand, slot, weights, lse, scale, dtype=dtype, cap=cap, tau=tau)
+    dWc = backward_dWc_mtp(H, W, cand, slot, weights, lse, scale, dtype=dtype, cap=cap, tau=tau)
+    _, real = _real(dtype)
+    dW = np.zeros(W.shape, real)
+    dW[cand] = dWc
     return {"cand": cand, "slot": slot, "U": U, "loss": loss, "lse": lse, "dH": dH, "dW": dW,
             "dWc": dWc}

@@ -42,6 +42,15 @@
  *   chain rule G[t][j] = scale * (exp(z - lse) - [j == slot[t]]) * dz/ds with
  *   dz/ds = z (A - z) / (A tau). A = 0 selects the plain head (z = s).
  *
+ * Several targets per token ("KellerJordan/modded-nanogpt" README,
+ * technique list: multi-token prediction, a prefix-token prediction
+ * auxiliary loss; no formula on the pages). Reading: token t has K targets
+ * y[k][t] with weights w[k] >= 0, all scored against the same logits (one
+ * GEMM), and the candidate set is built over all K*T targets:
+ *               loss[t] = sum_k w[k] * (lse[t] - z[t][slot[k][t]])
+ *               G[t][j] = scale * (W exp(z[t][j] - lse[t]) - sum_k w[k] [j == slot[k][t]]) dz/ds
+ *   with W = sum_k w[k]. K = 1, w = 1 is the single-target loss above.
+ *
  * Negative-sampling key (the pages name no sampler; reading: uniform without
  * replacement over the non-targets, driven by a counter-based generator so
  * that a CPU and a GPU implementation can agree bit for bit):
@@ -200,10 +209,11 @@ int orc_build_candidates(const int32_t* targets, int64_t T, int64_t V, int64_t C
     return cap > 0 ? z * (cap - z) / (cap * tau) : (REAL)1;                                  \
   }                                                                                          \
                                                                                              \
-  void orc_forward_head_##SUF(const IN_T* H, const IN_T* W, const int32_t* cand,             \
-                              const int32_t* slot, int64_t T, int64_t C, int64_t D,          \
-                              REAL cap, REAL tau, const int64_t* rows, int64_t nrows,        \
-                              REAL* loss, REAL* lse) {                                       \
+  /* K targets per token: slot[k * T + t], weights w[k] */                                  \
+  void orc_forward_mtp_##SUF(const IN_T* H, const IN_T* W, const int32_t* cand,              \
+                             const int32_t* slot, int64_t K, const REAL* w, int64_t T,       \
+                             int64_t C, int64_t D, REAL cap, REAL tau, const int64_t* rows,  \
+                             int64_t nrows, REAL* loss, REAL* lse) {                         \
     int64_t n = rows ? nrows : T;                                                            \
     _Pragma("omp parallel")                                                                  \
     {                                                                                        \
@@ -220,18 +230,32 @@ int orc_build_candidates(const int32_t* targets, int64_t T, int64_t V, int64_t C
         for (int64_t j = 0; j < C; ++j) sum += EXP(s[j] - m);                                \
         REAL l = m + LOG(sum);                                                               \
         lse[i] = l;                                                                          \
-        loss[i] = l - s[slot[t]];                                                            \
+        REAL acc = 0;                                                                        \
+        for (int64_t k = 0; k < K; ++k) acc += w[k] * (l - s[slot[k * T + t]]);              \
+        loss[i] = acc;                                                                       \
       }                                                                                      \
       free(s);                                                                               \
     }                                                                                        \
   }                                                                                          \
                                                                                              \
+  /* the weighted target indicator sum_k w[k] [j == slot[k][t]] */                           \
+  static REAL target_weight_##SUF(const int32_t* slot, int64_t K, const REAL* w, int64_t T,  \
+                                  int64_t t, int64_t j) {                                    \
+    REAL y = 0;                                                                              \
+    for (int64_t k = 0; k < K; ++k)                                                          \
+      if (slot[k * T + t] == j) y += w[k];                                                   \
+    return y;                                                                                \
+  }                                                                                          \
+                                                                                             \
   /* dH rows: needs lse of those tokens (lse_rows packed like rows) */                       \
-  void orc_backward_dH_head_##SUF(const IN_T* H, const IN_T* W, const int32_t* cand,         \
-                                  const int32_t* slot, const REAL* lse_rows, int64_t T,      \
-                                  int64_t C, int64_t D, REAL cap, REAL tau, REAL scale,      \
-                                  const int64_t* rows, int64_t nrows, REAL* dH) {            \
+  void orc_backward_dH_mtp_##SUF(const IN_T* H, const IN_T* W, const int32_t* cand,          \
+                                 const int32_t* slot, int64_t K, const REAL* w,              \
+                                 const REAL* lse_rows, int64_t T, int64_t C, int64_t D,      \
+                                 REAL cap, REAL tau, REAL scale, const int64_t* rows,        \
+                                 int64_t nrows, REAL* dH) {                                  \
     int64_t n = rows ? nrows : T;                                                            \
+    REAL wsum = 0;                                                                           \
+    for (int64_t k = 0; k < K; ++k) wsum += w[k];                                            \
     _Pragma("omp parallel")                                                                  \
     {                                                                                        \
       REAL* s = (REAL*)malloc(sizeof(REAL) * (size_t)C);                                     \
@@ -242,11 +266,11 @@ int orc_build_candidates(const int32_t* targets, int64_t T, int64_t V, int64_t C
         REAL* out = dH + i * D;                                                              \
         for (int64_t d = 0; d < D; ++d) out[d] = 0;                                          \
         for (int64_t j = 0; j < C; ++j) {                                                    \
-          REAL y = (j == slot[t]) ? (REAL)1 : (REAL)0;                                       \
+          REAL y = target_weight_##SUF(slot, K, w, T, t, j);                                 \
           REAL z = head_z_##SUF(s[j], cap, tau);                                             \
-          REAL g = scale * (EXP(z - lse_rows[i]) - y) * head_dz_##SUF(z, cap, tau);          \
-          const IN_T* w = W + (int64_t)cand[j] * D;                                          \
-          for (int64_t d = 0; d < D; ++d) out[d] += g * (REAL)LOAD(w[d]);                    \
+          REAL g = scale * (wsum * EXP(z - lse_rows[i]) - y) * head_dz_##SUF(z, cap, tau);   \
+          const IN_T* wr = W + (int64_t)cand[j] * D;                                         \
+          for (int64_t d = 0; d < D; ++d) out[d] += g * (REAL)LOAD(wr[d]);                   \
         }                                                                                    \
       }                                                                                      \
       free(s);                                                                               \
@@ -254,27 +278,56 @@ int orc_build_candidates(const int32_t* targets, int64_t T, int64_t V, int64_t C
   }                                                                                          \
                                                                                              \
   /* dW_c rows (candidate index j): needs lse of ALL T tokens */                             \
-  void orc_backward_dW_head_##SUF(const IN_T* H, const IN_T* W, const int32_t* cand,         \
-                                  const int32_t* slot, const REAL* lse, int64_t T, int64_t C, \
-                                  int64_t D, REAL cap, REAL tau, REAL scale,                 \
-                                  const int64_t* cols, int64_t ncols, REAL* dWc) {           \
+  void orc_backward_dW_mtp_##SUF(const IN_T* H, const IN_T* W, const int32_t* cand,          \
+                                 const int32_t* slot, int64_t K, const REAL* w,              \
+                                 const REAL* lse, int64_t T, int64_t C, int64_t D, REAL cap, \
+                                 REAL tau, REAL scale, const int64_t* cols, int64_t ncols,   \
+                                 REAL* dWc) {                                                \
     int64_t n = cols ? ncols : C;                                                            \
+    REAL wsum = 0;                                                                           \
+    for (int64_t k = 0; k < K; ++k) wsum += w[k];                                            \
     _Pragma("omp parallel for schedule(dynamic, 1)")                                         \
     for (int64_t i = 0; i < n; ++i) {                                                        \
       int64_t j = cols ? cols[i] : i;                                                        \
-      const IN_T* w = W + (int64_t)cand[j] * D;                                              \
+      const IN_T* wr = W + (int64_t)cand[j] * D;                                             \
       REAL* out = dWc + i * D;                                                               \
       for (int64_t d = 0; d < D; ++d) out[d] = 0;                                            \
       for (int64_t t = 0; t < T; ++t) {                                                      \
         const IN_T* h = H + t * D;                                                           \
         REAL st = 0;                                                                         \
-        for (int64_t d = 0; d < D; ++d) st += (REAL)LOAD(h[d]) * (REAL)LOAD(w[d]);           \
-        REAL y = (j == slot[t]) ? (REAL)1 : (REAL)0;                                         \
+        for (int64_t d = 0; d < D; ++d) st += (REAL)LOAD(h[d]) * (REAL)LOAD(wr[d]);          \
+        REAL y = target_weight_##SUF(slot, K, w, T, t, j);                                   \
         REAL z = head_z_##SUF(st, cap, tau);                                                 \
-        REAL g = scale * (EXP(z - lse[t]) - y) * head_dz_##SUF(z, cap, tau);                 \
+        REAL g = scale * (wsum * EXP(z - lse[t]) - y) * head_dz_##SUF(z, cap, tau);          \
         for (int64_t d = 0; d < D; ++d) out[d] += g * (REAL)LOAD(h[d]);                      \
       }                                                                                      \
     }                                                                                        \
+  }                                                                                          \
+                                                                                             \
+  /* one target per token */                                                                 \
+  void orc_forward_head_##SUF(const IN_T* H, const IN_T* W, const int32_t* cand,             \
+                              const int32_t* slot, int64_t T, int64_t C, int64_t D,          \
+                              REAL cap, REAL tau, const int64_t* rows, int64_t nrows,        \
+                              REAL* loss, REAL* lse) {                                       \
+    const REAL one = 1;                                                                      \
+    orc_forward_mtp_##SUF(H, W, cand, slot, 1, &one, T, C, D, cap, tau, rows, nrows, loss,   \
+                          lse);                                                              \
+  }                                                                                          \
+  void orc_backward_dH_head_##SUF(const IN_T* H, const IN_T* W, const int32_t* cand,         \
+                                  const int32_t* slot, const REAL* lse_rows, int64_t T,      \
+                                  int64_t C, int64_t D, REAL cap, REAL tau, REAL scale,      \
+                                  const int64_t* rows, int64_t nrows, REAL* dH) {            \
+    const REAL one = 1;                                                                      \
+    orc_backward_dH_mtp_##SUF(H, W, cand, slot, 1, &one, lse_rows, T, C, D, cap, tau, scale, \
+                              rows, nrows, dH);                                              \
+  }                                                                                          \
+  void orc_backward_dW_head_##SUF(const IN_T* H, const IN_T* W, const int32_t* cand,         \
+                                  const int32_t* slot, const REAL* lse, int64_t T, int64_t C, \
+                                  int64_t D, REAL cap, REAL tau, REAL scale,                 \
+                                  const int64_t* cols, int64_t ncols, REAL* dWc) {           \
+    const REAL one = 1;                                                                      \
+    orc_backward_dW_mtp_##SUF(H, W, cand, slot, 1, &one, lse, T, C, D, cap, tau, scale, cols, \
+                              ncols, dWc);                                                   \
   }                                                                                          \
                                                                                              \
   /* the plain head */                                                                       \

@@ -362,17 +362,23 @@ def test_row_subsets_match_full(orc):
 # ------------------------------------------------------ planted mistakes
 
 MUTATIONS = [
-    ("drop one-hot term in dH", "REAL g = scale * (EXP(z - lse_rows[i]) - y) *",
-     "REAL g = scale * (EXP(z - lse_rows[i])) *"),
+    ("drop one-hot term in dH", "REAL g = scale * (wsum * EXP(z - lse_rows[i]) - y) *",
+     "REAL g = scale * (wsum * EXP(z - lse_rows[i])) *"),
     ("capped head: dz/ds factor dropped in dW",
-     "REAL g = scale * (EXP(z - lse[t]) - y) * head_dz_##SUF(z, cap, tau);",
-     "REAL g = scale * (EXP(z - lse[t]) - y);"),
+     "REAL g = scale * (wsum * EXP(z - lse[t]) - y) * head_dz_##SUF(z, cap, tau);",
+     "REAL g = scale * (wsum * EXP(z - lse[t]) - y);"),
+    ("several targets: weights ignored in the loss", "acc += w[k] * (l - s[slot[k * T + t]]);",
+     "acc += (l - s[slot[k * T + t]]);"),
+    ("several targets: weight sum missing in dH", "REAL g = scale * (wsum * EXP(z - lse_rows[i]) - y)",
+     "REAL g = scale * (EXP(z - lse_rows[i]) - y)"),
+    ("several targets: only the first target in G", "if (slot[k * T + t] == j) y += w[k];",
+     "if (k == 0 && slot[k * T + t] == j) y += w[k];"),
     ("capped head: logistic of +s", "cap / ((REAL)1 + EXP(-s / tau))", "cap / ((REAL)1 + EXP(s / tau))"),
     ("capped head: dz/ds without (A - z)", "z * (cap - z) / (cap * tau)", "z / tau"),
     ("sign of the log-sum", "REAL l = m + LOG(sum);", "REAL l = m - LOG(sum);"),
     ("transposed operand in dW", "for (int64_t d = 0; d < D; ++d) out[d] += g * (REAL)LOAD(h[d]);",
      "for (int64_t d = 0; d < D; ++d) out[d] += g * (REAL)LOAD(w[d]);"),
-    ("wrong target index", "loss[i] = l - s[slot[t]];", "loss[i] = l - s[0];"),
+    ("wrong target index", "s[slot[k * T + t]]", "s[0]"),
     ("dropped term of the dot product", "for (int64_t d = 0; d < D; ++d) acc +=",
      "for (int64_t d = 1; d < D; ++d) acc +="),
     ("negatives left in key order", "qsort(neg, (size_t)k, sizeof(int32_t), cmp_i32);", ""),
@@ -420,6 +426,12 @@ def _battery(orc):
         failed.append("capped dH")
     if not np.allclose(dWc, gW[cand], rtol=1e-8, atol=1e-12):
         failed.append("capped dW")
+    # two weighted targets per token against torch autograd
+    try:
+        bad = _mtp_mismatch(orc, 12, 80, 8, 30, 32, [1.0, 0.5], 0.0, 1.0)
+    except Exception:
+        bad = ["mtp crashed"]
+    failed += bad
     return failed
 
 
@@ -546,3 +558,99 @@ def test_capped_head_finite_differences(orc):
         Wm[cand[j], d] -= eps
         fd = (total(H, Wp) - total(H, Wm)) / (2 * eps)
         assert abs(fd - dWc[j, d]) <= 1e-6 * max(1.0, abs(fd))
+
+
+# ------------------------------------------------ several targets per token
+
+def _torch_ref_mtp(H64, W64, cand, slot, weights, scale=1.0, cap=0.0, tau=1.0):
+    """torch autograd of sum_k w[k] * CE(logits, slot[k]) (slot [K, T])."""
+    Ht = torch.tensor(H64, requires_grad=True)
+    Wt = torch.tensor(W64, requires_grad=True)
+    logits = Ht @ Wt[torch.from_numpy(cand.astype(np.int64))].T
+    if cap > 0:
+        logits = cap * torch.sigmoid(logits / tau)
+    loss = 0
+    for k, wk in enumerate(weights):
+        loss = loss + wk * F.cross_entropy(logits, torch.from_numpy(slot[k].astype(np.int64)),
+                                           reduction="none")
+    (scale * loss.sum()).backward()
+    return (loss.detach().numpy(), torch.logsumexp(logits, 1).detach().numpy(),
+            Ht.grad.numpy(), Wt.grad.numpy())
+
+
+def _mtp_case(T, V, D, C, seed, K, w_std=0.3):
+    rng = np.random.default_rng(seed)
+    x = synth.make_inputs(T, V, D, 1.1, seed, w_std=w_std)
+    tg = np.stack([x["targets"]] + [synth.zipf_targets(rng, T, V, 1.1) for _ in range(K - 1)])
+    C = max(C, len(np.unique(tg)))
+    return x, tg.astype(np.int32), C
+
+
+def _mtp_mismatch(orc, T, V, D, C, seed, weights, cap, tau):
+    """Names of the quantities where the fp64 oracle disagrees with torch."""
+    x, tg, C = _mtp_case(T, V, D, C, seed, len(weights))
+    cand, slot_flat, _ = orc.build_candidates(tg.reshape(-1), V, C, seed)
+    slot = slot_flat.reshape(tg.shape)
+    loss, lse, gH, gW = _torch_ref_mtp(_f64(x["H"]), _f64(x["W"]), cand, slot, weights, 0.7, cap,
+                                       tau)
+    l64, s64 = orc.forward_mtp(x["H"], x["W"], cand, slot, weights, dtype=np.float64, cap=cap,
+                               tau=tau)
+    dH = orc.backward_dH_mtp(x["H"], x["W"], cand, slot, weights, s64, 0.7, dtype=np.float64,
+                             cap=cap, tau=tau)
+    dWc = orc.backward_dWc_mtp(x["H"], x["W"], cand, slot, weights, s64, 0.7, dtype=np.float64,
+                               cap=cap, tau=tau)
+    bad = []
+    if not np.allclose(l64, loss, rtol=1e-11):
+        bad.append("mtp forward")
+    if not np.allclose(s64, lse, rtol=1e-12):
+        bad.append("mtp lse")
+    if not np.allclose(dH, gH, rtol=1e-9, atol=1e-13):
+        bad.append("mtp dH")
+    if not np.allclose(dWc, gW[cand], rtol=1e-9, atol=1e-13):
+        bad.append("mtp dW")
+    return bad
+
+
+@pytest.mark.parametrize("weights,cap,tau", [([1.0, 0.5], 0.0, 1.0), ([1.0, 0.3, 0.2], 0.0, 1.0),
+                                             ([0.6, 0.4], 20.0, 4.0), ([2.0], 0.0, 1.0)])
+def test_several_targets_against_torch_autograd(orc, weights, cap, tau):
+    """sum_k w[k] * CE over the same logits, both gradients, against torch in
+    fp64, with and without the capped head."""
+    assert _mtp_mismatch(orc, 40, 500, 24, 120, 11, weights, cap, tau) == []
+
+
+def test_single_weight_one_target_is_the_plain_loss(orc):
+    """K = 1, w = 1 gives the single-target results bit for bit."""
+    x, tg, C = _mtp_case(50, 700, 32, 200, 12, 1)
+    cand, slot, _ = orc.build_candidates(tg[0], 700, C, 12)
+    for dt in (np.float32, np.float64):
+        l1, s1 = orc.forward(x["H"], x["W"], cand, slot, dtype=dt)
+        lk, sk = orc.forward_mtp(x["H"], x["W"], cand, slot[None], [1.0], dtype=dt)
+        np.testing.assert_array_equal(l1, lk)
+        np.testing.assert_array_equal(s1, sk)
+        d1 = orc.backward_dWc(x["H"], x["W"], cand, slot, s1, 0.5, dtype=dt)
+        dk = orc.backward_dWc_mtp(x["H"], x["W"], cand, slot[None], [1.0], sk, 0.5, dtype=dt)
+        np.testing.assert_array_equal(d1, dk)
+
+
+def test_repeated_target_counts_its_weights(orc):
+    """Two target rows equal to each other with weights a and b give the loss of
+    one target row with weight a + b (a weighted one-hot term adds up)."""
+    x, tg, C = _mtp_case(30, 400, 16, 100, 13, 1)
+    cand, slot, _ = orc.build_candidates(tg[0], 400, C, 13)
+    two = np.stack([slot, slot])
+    l2, s2 = orc.forward_mtp(x["H"], x["W"], cand, two, [0.25, 0.5], dtype=np.float64)
+    l1, _ = orc.forward_mtp(x["H"], x["W"], cand, slot[None], [0.75], dtype=np.float64)
+    np.testing.assert_allclose(l2, l1, rtol=1e-14)
+    d2 = orc.backward_dH_mtp(x["H"], x["W"], cand, two, [0.25, 0.5], s2, dtype=np.float64)
+    d1 = orc.backward_dH_mtp(x["H"], x["W"], cand, slot[None], [0.75], s2, dtype=np.float64)
+    np.testing.assert_allclose(d2, d1, rtol=1e-12, atol=1e-15)
+
+
+def test_several_targets_loss_and_grads_builds_over_all_targets(orc):
+    x, tg, C = _mtp_case(60, 900, 16, 150, 14, 3)
+    ref = orc.loss_and_grads_mtp(x["H"], x["W"], tg, [1.0, 0.5, 0.25], C, 14)
+    allt = np.unique(tg)
+    assert ref["U"] == allt.size
+    np.testing.assert_array_equal(ref["cand"][:allt.size], allt)
+    np.testing.assert_array_equal(ref["cand"][ref["slot"]], tg)
