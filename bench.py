@@ -65,6 +65,9 @@ def parse_args():
     ap.add_argument("--cap", type=float, default=0.0,
                     help="capped head: logits z = cap / (1 + exp(-s / tau)) (0: plain head)")
     ap.add_argument("--tau", type=float, default=7.5)
+    ap.add_argument("--targets", type=int, default=1,
+                    help="targets per token (multi-token prediction over one set of logits): "
+                         "offsets 1..K of one Zipf stream, weights 1, 1/2, 1/4, ...")
     ap.add_argument("--ref-step-seconds", type=float, default=None,
                     help="reference arm: target seconds per step (default: fits the run in ~2.5 min)")
     return ap.parse_args()
@@ -281,8 +284,19 @@ def run_native(args, world, rank, local):
     scale = 1.0 / T
 
     cap, tau = args.cap, args.tau
+    n_tg = args.targets
+    mtp_weights = [0.5 ** k for k in range(n_tg)]
+    if n_tg > 1:
+        extra = synth.zipf_targets(np.random.default_rng(w.seed + 77), n_tg - 1, V, w.zipf_s)
+        stream = np.concatenate([x["targets"], extra])
+        targets_k = torch.from_numpy(
+            np.stack([stream[k:k + T] for k in range(n_tg)]).astype(np.int32)).to(dev)
 
     def step(h=H, tg=targets):
+        if n_tg > 1:
+            ss.step_mtp(h, W, targets_k, mtp_weights, C, w.seed, ws, scale=scale, dW=dW, cap=cap,
+                        tau=tau)
+            return
         ss.step(h, W, tg, C, w.seed, ws, scale=scale, dW=dW, cand=cand, slot=slot, loss=loss,
                 lse=lse, dH=dH, cap=cap, tau=tau)
 
@@ -353,7 +367,7 @@ def run_native(args, world, rank, local):
 
     # the same steps as three ABI calls (ss_build_candidates, ss_forward,
     # ss_backward), untraced, for comparison
-    K3 = min(K, 300)
+    K3 = min(K, 300) if n_tg == 1 else 0
     s3 = [torch.cuda.Event(enable_timing=True) for _ in range(K3)]
     e3 = [torch.cuda.Event(enable_timing=True) for _ in range(K3)]
     torch.cuda.synchronize()
@@ -363,26 +377,28 @@ def run_native(args, world, rank, local):
         step_three_calls()
         e3[k].record()
     torch.cuda.synchronize()
-    three_calls_ms = sum(a.elapsed_time(b) for a, b in zip(s3, e3)) / K3
+    three_calls_ms = sum(a.elapsed_time(b) for a, b in zip(s3, e3)) / K3 if K3 else None
 
     # the same step replayed from a CUDA graph of ss_step (ss_step_graph_*)
-    graph = ss.StepGraph(H, W, targets, C, ws, scale=scale, cand=cand, slot=slot, loss=loss,
-                         lse=lse, dH=dH, dW=dW, cap=cap, tau=tau)
-    graph.launch(w.seed)
-    sg = [torch.cuda.Event(enable_timing=True) for _ in range(K3)]
-    eg = [torch.cuda.Event(enable_timing=True) for _ in range(K3)]
-    torch.cuda.synchronize()
-    for k in range(K3):
-        flush.zero_()
-        sg[k].record()
+    graph_ms = None
+    if n_tg == 1:
+        graph = ss.StepGraph(H, W, targets, C, ws, scale=scale, cand=cand, slot=slot, loss=loss,
+                             lse=lse, dH=dH, dW=dW, cap=cap, tau=tau)
         graph.launch(w.seed)
-        eg[k].record()
-    torch.cuda.synchronize()
-    graph_ms = sum(a.elapsed_time(b) for a, b in zip(sg, eg)) / K3
-    graph.close()
-    st, _ = ss.read_status(ws)
-    if st != 0:
-        raise RuntimeError(f"device status {st} after the graph region")
+        sg = [torch.cuda.Event(enable_timing=True) for _ in range(K3)]
+        eg = [torch.cuda.Event(enable_timing=True) for _ in range(K3)]
+        torch.cuda.synchronize()
+        for k in range(K3):
+            flush.zero_()
+            sg[k].record()
+            graph.launch(w.seed)
+            eg[k].record()
+        torch.cuda.synchronize()
+        graph_ms = sum(a.elapsed_time(b) for a, b in zip(sg, eg)) / K3
+        graph.close()
+        st, _ = ss.read_status(ws)
+        if st != 0:
+            raise RuntimeError(f"device status {st} after the graph region")
 
     # per-kernel times from the trace
     per = {}
@@ -451,6 +467,8 @@ def run_native(args, world, rank, local):
                    "step": "ss_step (= ss_build_candidates + ss_forward + ss_backward in one call)",
                    "head": ({"cap": cap, "tau": tau, "logits": "cap / (1 + exp(-s / tau))"}
                             if cap else "plain"),
+                   "targets_per_token": n_tg,
+                   **({"target_weights": mtp_weights} if n_tg > 1 else {}),
                    "ms_per_step_three_calls": three_calls_ms,
                    "ms_per_step_graph": graph_ms,
                    "step_tflops_algorithmic_6TCD": step_tflops,

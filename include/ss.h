@@ -191,6 +191,35 @@ ss_status ss_step_head(const int32_t* targets, const uint16_t* H, const uint16_t
                        size_t workspace_bytes, ss_stream stream);
 
 /*
+ * Several targets per token scored against the same logits
+ * ("KellerJordan/modded-nanogpt" README, technique list: multi-token
+ * prediction; a prefix-token prediction auxiliary loss; the pages give no
+ * formula). Token t has K targets targets[k * T + t] (k-major, [K, T]) with
+ * host weights w[k] >= 0 (finite, sum W > 0), 1 <= K <= SS_MAX_TARGETS:
+ *   loss[t] = sum_k w[k] (lse[t] - z[t, slot[k * T + t]])
+ *   G       = scale (W P - sum_k w[k] onehot(slot[k])) (* dz/ds when capped)
+ * The candidate set is built over all K * T targets, so slot is [K, T] too.
+ * Same conventions and results otherwise as ss_forward / ss_backward /
+ * ss_step with the same head; K = 1, w = {1} gives their results exactly.
+ * Bad K or weights -> SS_ERR_INVALID.
+ */
+#define SS_MAX_TARGETS 8
+ss_status ss_forward_mtp(const uint16_t* H, const uint16_t* W, const int32_t* cand,
+                         const int32_t* slot, int64_t K, const float* weights, int64_t T,
+                         int64_t V, int64_t C, int64_t D, const ss_head* head, float* loss,
+                         float* lse, void* workspace, size_t workspace_bytes, ss_stream stream);
+ss_status ss_backward_mtp(const uint16_t* H, const uint16_t* W, const int32_t* cand,
+                          const int32_t* slot, int64_t K, const float* weights, const float* lse,
+                          int64_t T, int64_t V, int64_t C, int64_t D, const ss_head* head,
+                          float scale, int accumulate, uint16_t* dH, float* dW, void* workspace,
+                          size_t workspace_bytes, ss_stream stream);
+ss_status ss_step_mtp(const int32_t* targets, int64_t K, const float* weights, const uint16_t* H,
+                      const uint16_t* W, int64_t T, int64_t V, int64_t C, int64_t D, uint64_t seed,
+                      const ss_head* head, float scale, int accumulate, int32_t* cand,
+                      int32_t* slot, float* loss, float* lse, uint16_t* dH, float* dW,
+                      void* workspace, size_t workspace_bytes, ss_stream stream);
+
+/*
  * The pages' candidate schedule ("NanoGPT Training Record: Technical
  * Optimizations & Speed", "Key Optimizations and Ablation Table Results":
  * 10,240, then 14,336, then 24,576 candidates, then all rows for the final

@@ -100,6 +100,15 @@ def _load():
     L.ss_step_head.restype = ctypes.c_int
     L.ss_step_head.argtypes = [p, p, p, i64, i64, i64, i64, ctypes.c_uint64, hp, ctypes.c_float,
                                ctypes.c_int, p, p, p, p, p, p, p, sz, p]
+    fp = ctypes.POINTER(ctypes.c_float)
+    L.ss_forward_mtp.restype = ctypes.c_int
+    L.ss_forward_mtp.argtypes = [p, p, p, p, i64, fp, i64, i64, i64, i64, hp, p, p, p, sz, p]
+    L.ss_backward_mtp.restype = ctypes.c_int
+    L.ss_backward_mtp.argtypes = [p, p, p, p, i64, fp, p, i64, i64, i64, i64, hp, ctypes.c_float,
+                                  ctypes.c_int, p, p, p, sz, p]
+    L.ss_step_mtp.restype = ctypes.c_int
+    L.ss_step_mtp.argtypes = [p, i64, fp, p, p, i64, i64, i64, i64, ctypes.c_uint64, hp,
+                              ctypes.c_float, ctypes.c_int, p, p, p, p, p, p, p, sz, p]
     L.ss_schedule_candidates.restype = i64
     L.ss_schedule_candidates.argtypes = [i64, i64, i64]
     L.ss_clear_rows.restype = ctypes.c_int
@@ -469,3 +478,83 @@ class StepGraph:
             self.close()
         except Exception:
             pass
+
+
+MAX_TARGETS = 8
+
+
+def _weights(weights):
+    w = (ctypes.c_float * len(weights))(*[float(v) for v in weights])
+    return w, len(weights)
+
+
+def step_mtp(H, W, targets, weights, C: int, seed: int, ws, scale: float = 1.0, dW=None,
+             accumulate=False, cap: float = 0.0, tau: float = 1.0):
+    """ss_step_mtp: targets [K, T] int32 (K weighted targets per token), one
+    candidate set over all of them; returns slot [K, T]."""
+    _need(H, "H", torch.bfloat16)
+    dev = H.device
+    T, D = H.shape
+    V = W.shape[0]
+    K = len(weights)
+    _need(W, "W", torch.bfloat16, dev, (V, D))
+    _need(targets, "targets", torch.int32, dev, (K, T))
+    _need(ws, "workspace", torch.uint8, dev)
+    cand = torch.empty(C, dtype=torch.int32, device=dev)
+    slot = torch.empty(K, T, dtype=torch.int32, device=dev)
+    loss = torch.empty(T, dtype=torch.float32, device=dev)
+    lse = torch.empty(T, dtype=torch.float32, device=dev)
+    dH = torch.empty(T, D, dtype=torch.bfloat16, device=dev)
+    dW = torch.zeros(V, D, dtype=torch.float32, device=dev) if dW is None else dW
+    _need(dW, "dW", torch.float32, dev, (V, D))
+    w, K = _weights(weights)
+    code = _lib.ss_step_mtp(_ptr(targets), K, w, _ptr(H), _ptr(W), T, V, C, D, seed & (2**64 - 1),
+                            _head(cap, tau), float(scale), 1 if accumulate else 0, _ptr(cand),
+                            _ptr(slot), _ptr(loss), _ptr(lse), _ptr(dH), _ptr(dW), _ptr(ws),
+                            ws.numel(), _stream(dev))
+    _check(code, "ss_step_mtp")
+    return {"cand": cand, "slot": slot, "loss": loss, "lse": lse, "dH": dH, "dW": dW}
+
+
+def forward_mtp(H, W, cand, slot, weights, ws, cap: float = 0.0, tau: float = 1.0):
+    """ss_forward_mtp: slot [K, T]; per-token weighted loss [T] and lse [T]."""
+    _need(H, "H", torch.bfloat16)
+    dev = H.device
+    T, D = H.shape
+    V = W.shape[0]
+    C = cand.numel()
+    K = len(weights)
+    _need(W, "W", torch.bfloat16, dev, (V, D))
+    _need(cand, "cand", torch.int32, dev, (C,))
+    _need(slot, "slot", torch.int32, dev, (K, T))
+    _need(ws, "workspace", torch.uint8, dev)
+    loss = torch.empty(T, dtype=torch.float32, device=dev)
+    lse = torch.empty(T, dtype=torch.float32, device=dev)
+    w, K = _weights(weights)
+    code = _lib.ss_forward_mtp(_ptr(H), _ptr(W), _ptr(cand), _ptr(slot), K, w, T, V, C, D,
+                               _head(cap, tau), _ptr(loss), _ptr(lse), _ptr(ws), ws.numel(),
+                               _stream(dev))
+    _check(code, "ss_forward_mtp")
+    return loss, lse
+
+
+def backward_mtp(H, W, cand, slot, weights, lse, ws, scale: float = 1.0, accumulate=False,
+                 dW=None, cap: float = 0.0, tau: float = 1.0):
+    """ss_backward_mtp: dH [T, D] bf16 and dW [V, D] fp32 (candidate rows)."""
+    _need(H, "H", torch.bfloat16)
+    dev = H.device
+    T, D = H.shape
+    V = W.shape[0]
+    C = cand.numel()
+    K = len(weights)
+    _need(slot, "slot", torch.int32, dev, (K, T))
+    _need(lse, "lse", torch.float32, dev, (T,))
+    dH = torch.empty(T, D, dtype=torch.bfloat16, device=dev)
+    dW = torch.zeros(V, D, dtype=torch.float32, device=dev) if dW is None else dW
+    _need(dW, "dW", torch.float32, dev, (V, D))
+    w, K = _weights(weights)
+    code = _lib.ss_backward_mtp(_ptr(H), _ptr(W), _ptr(cand), _ptr(slot), K, w, _ptr(lse), T, V,
+                                C, D, _head(cap, tau), float(scale), 1 if accumulate else 0,
+                                _ptr(dH), _ptr(dW), _ptr(ws), ws.numel(), _stream(dev))
+    _check(code, "ss_backward_mtp")
+    return dH, dW

@@ -21,7 +21,8 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT_DIR, "libss.so")
-SOURCES = ["ss_api.cu", "ss_candidates.cu", "ss_gemm_logits.cu", "ss_gemm_grads.cu"]
+SOURCES = ["ss_api.cu", "ss_candidates.cu", "ss_gemm_logits.cu", "ss_gemm_logits_mtp.cu",
+           "ss_gemm_grads.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

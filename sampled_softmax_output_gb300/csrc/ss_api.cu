@@ -43,8 +43,8 @@ Layout make_layout(int64_t T, int64_t C, int64_t D) {
   off = align_up(off + static_cast<size_t>(C) * D * 2, 1024);
   L.part = off;
   off = align_up(off + static_cast<size_t>(L.n_ct) * kFwdGroupsMax * T * sizeof(float2), 1024);
-  L.tgt = off;
-  off = align_up(off + static_cast<size_t>(T) * sizeof(float), 1024);
+  L.tgt = off;  // target logits, up to kMaxTargets per token
+  off = align_up(off + static_cast<size_t>(T) * kMaxTargets * sizeof(float), 1024);
   L.g = off;
   off = align_up(off + static_cast<size_t>(T) * L.ldG * 2, 1024);
   L.total = off;
@@ -147,7 +147,8 @@ __device__ __forceinline__ void lse_fold(float& M, float& S, float m, float s) {
 __global__ void __launch_bounds__(256) k_lse_merge(const float2* __restrict__ part,
                                                    const float* __restrict__ tgt,
                                                    const int32_t* __restrict__ slot, int T, int C,
-                                                   int n_ct, float* __restrict__ loss,
+                                                   int n_ct, Targets tg,
+                                                   float* __restrict__ loss,
                                                    float* __restrict__ lse, int* status) {
   pdl_enter();
   if (read_status(status) != 0) return;
@@ -175,13 +176,18 @@ __global__ void __launch_bounds__(256) k_lse_merge(const float2* __restrict__ pa
     lse_fold(M, S, m2, s2);
   }
   if (!valid || k != 0) return;
-  if (static_cast<unsigned>(__ldg(slot + t)) >= static_cast<unsigned>(C)) {
-    set_status(status, SS_ERR_INDEX);
-    return;
-  }
+  for (int j = 0; j < tg.K; ++j)
+    if (static_cast<unsigned>(__ldg(slot + static_cast<size_t>(j) * T + t)) >=
+        static_cast<unsigned>(C)) {
+      set_status(status, SS_ERR_INDEX);
+      return;
+    }
   const float l = M + logf(S);
   lse[t] = l;
-  loss[t] = l - tgt[t];
+  // sum over the targets of w[j] (lse - target logit); one target: lse - tgt
+  float acc = 0.f;
+  for (int j = 0; j < tg.K; ++j) acc += tg.w[j] * (l - tgt[static_cast<size_t>(j) * T + t]);
+  loss[t] = acc;
 }
 
 // dW[cand[j], :] = 0 (the gradient of an empty batch).
@@ -297,8 +303,8 @@ ss_status enqueue_gather(const uint16_t* W, const int32_t* cand, int64_t C, int6
 
 // forward GEMM (LSE partials, target logit) and the LSE merge, from W_c
 ss_status enqueue_forward(const uint16_t* H, const int32_t* slot, int64_t T, int64_t C, int64_t D,
-                          float cap, float tau, float* loss, float* lse, const Layout& L,
-                          char* ws, int nsm, cudaStream_t s) {
+                          float cap, float tau, const Targets& tg, float* loss, float* lse,
+                          const Layout& L, char* ws, int nsm, cudaStream_t s) {
   int* status = reinterpret_cast<int*>(ws + L.hdr);
   uint16_t* Wc = reinterpret_cast<uint16_t*>(ws + L.wc);
   float2* part = reinterpret_cast<float2*>(ws + L.part);
@@ -309,14 +315,14 @@ ss_status enqueue_forward(const uint16_t* H, const int32_t* slot, int64_t T, int
   trace_pre(s, "gemm_forward_lse");
   const cudaError_t e = launch_forward_logits(tH, tWc, static_cast<int>(T), static_cast<int>(C),
                                               static_cast<int>(D), slot, part, tgt, cap, tau,
-                                              status, nsm, s);
+                                              tg, status, nsm, s);
   trace_post(s);
   if (e != cudaSuccess) return fail("launch gemm_forward_lse", e);
   const int blocks = static_cast<int>((T * kMergeLanes + 255) / 256);
   trace_pre(s, "lse_merge");
   const cudaError_t em =
       launch_pdl(k_lse_merge, dim3(blocks), dim3(256), 0, s, part, tgt, slot, static_cast<int>(T),
-                 static_cast<int>(C), static_cast<int>(L.n_ct * fwd_groups(cap)), loss, lse,
+                 static_cast<int>(C), static_cast<int>(L.n_ct * fwd_groups(cap)), tg, loss, lse,
                  status);
   trace_post(s);
   return cuda_status(em, "launch k_lse_merge");
@@ -325,8 +331,9 @@ ss_status enqueue_forward(const uint16_t* H, const int32_t* slot, int64_t T, int
 // softmax-gradient GEMM and the two gradient GEMMs, from W_c
 ss_status enqueue_backward(const uint16_t* H, const int32_t* cand, const int32_t* slot,
                            const float* lse, int64_t T, int64_t V, int64_t C, int64_t D,
-                           float cap, float tau, float scale, int accumulate, uint16_t* dH,
-                           float* dW, const Layout& L, char* ws, int nsm, cudaStream_t s) {
+                           float cap, float tau, const Targets& tg, float scale,
+                           int accumulate, uint16_t* dH, float* dW, const Layout& L, char* ws,
+                           int nsm, cudaStream_t s) {
   int* status = reinterpret_cast<int*>(ws + L.hdr);
   uint16_t* Wc = reinterpret_cast<uint16_t*>(ws + L.wc);
   uint16_t* G = reinterpret_cast<uint16_t*>(ws + L.g);
@@ -341,8 +348,8 @@ ss_status enqueue_backward(const uint16_t* H, const int32_t* cand, const int32_t
     return fail("cuTensorMapEncodeTiled", cudaErrorInvalidValue);
   trace_pre(s, "gemm_softmax_grad");
   cudaError_t e =
-      launch_softmax_grad(tH, tWc, tWc2, tGk, iT, iC, iD, slot, lse, scale, cap, tau, status,
-                          nsm, s);
+      launch_softmax_grad(tH, tWc, tWc2, tGk, iT, iC, iD, slot, lse, scale, cap, tau, tg,
+                          status, nsm, s);
   trace_post(s);
   if (e != cudaSuccess) return fail("launch gemm_softmax_grad", e);
   trace_pre(s, "gemm_grads");
@@ -361,6 +368,8 @@ ss_status enqueue_zero_rows(const int32_t* cand, int64_t C, int64_t V, int64_t D
   trace_post(s);
   return cuda_status(e, "launch k_zero_rows");
 }
+
+constexpr Targets kOneTarget = {1, {1.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f}};
 
 // The argument checks of ss_step (and of ss_step_graph_create).
 ss_status step_args_status(const int32_t* targets, const uint16_t* H, const uint16_t* W,
@@ -471,8 +480,8 @@ ss_status ss_build_candidates(const int32_t* targets, int64_t T, int64_t V, int6
 
 static ss_status forward_impl(const uint16_t* H, const uint16_t* W, const int32_t* cand,
                               const int32_t* slot, int64_t T, int64_t V, int64_t C, int64_t D,
-                              float cap, float tau, float* loss, float* lse, void* workspace,
-                              size_t workspace_bytes, ss_stream stream) {
+                              float cap, float tau, const Targets& tg, float* loss, float* lse,
+                              void* workspace, size_t workspace_bytes, ss_stream stream) {
   const ss_status st = check_sizes(T, V, C, D);
   if (st != SS_OK) return st;
   if (!W || !cand || !workspace || (T > 0 && (!H || !slot || !loss || !lse)))
@@ -490,14 +499,14 @@ static ss_status forward_impl(const uint16_t* H, const uint16_t* W, const int32_
   const ss_status sg = enqueue_gather(W, cand, C, V, D, reinterpret_cast<uint16_t*>(ws + L.wc),
                                       reinterpret_cast<int*>(ws + L.hdr), nsm, s);
   if (sg != SS_OK) return sg;
-  return enqueue_forward(H, slot, T, C, D, cap, tau, loss, lse, L, ws, nsm, s);
+  return enqueue_forward(H, slot, T, C, D, cap, tau, tg, loss, lse, L, ws, nsm, s);
 }
 
 static ss_status backward_impl(const uint16_t* H, const uint16_t* W, const int32_t* cand,
                                const int32_t* slot, const float* lse, int64_t T, int64_t V,
-                               int64_t C, int64_t D, float cap, float tau, float scale,
-                               int accumulate, uint16_t* dH, float* dW, void* workspace,
-                               size_t workspace_bytes, ss_stream stream) {
+                               int64_t C, int64_t D, float cap, float tau, const Targets& tg,
+                               float scale, int accumulate, uint16_t* dH, float* dW,
+                               void* workspace, size_t workspace_bytes, ss_stream stream) {
   const ss_status st = check_sizes(T, V, C, D);
   if (st != SS_OK) return st;
   if (!W || !cand || !dW || !workspace || (T > 0 && (!H || !slot || !lse || !dH)))
@@ -517,21 +526,23 @@ static ss_status backward_impl(const uint16_t* H, const uint16_t* W, const int32
   const ss_status sg =
       enqueue_gather(W, cand, C, V, D, reinterpret_cast<uint16_t*>(ws + L.wc), status, nsm, s);
   if (sg != SS_OK) return sg;
-  return enqueue_backward(H, cand, slot, lse, T, V, C, D, cap, tau, scale, accumulate, dH, dW, L,
-                          ws, nsm, s);
+  return enqueue_backward(H, cand, slot, lse, T, V, C, D, cap, tau, tg, scale, accumulate, dH, dW,
+                          L, ws, nsm, s);
 }
 
 static ss_status step_impl(const int32_t* targets, const uint16_t* H, const uint16_t* W,
                            int64_t T, int64_t V, int64_t C, int64_t D, uint64_t seed, float cap,
-                           float tau, float scale, int accumulate, int32_t* cand, int32_t* slot,
-                           float* loss, float* lse, uint16_t* dH, float* dW, void* workspace,
-                           size_t workspace_bytes, ss_stream stream) {
+                           float tau, const Targets& tg, float scale, int accumulate,
+                           int32_t* cand, int32_t* slot, float* loss, float* lse, uint16_t* dH,
+                           float* dW, void* workspace, size_t workspace_bytes, ss_stream stream) {
   const ss_status st = step_args_status(targets, H, W, T, V, C, D, accumulate, cand, slot, loss,
                                         lse, dH, dW, workspace, workspace_bytes);
   if (st != SS_OK) return st;
+  if (T * tg.K >= (int64_t(1) << 31)) return SS_ERR_UNSUPPORTED;
   const Layout L = make_layout(T, C, D);
-  const ss_status sb = ss_build_candidates(targets, T, V, C, seed, cand, slot, nullptr, workspace,
-                                           workspace_bytes, stream);
+  // the candidate set covers every target of every token (targets [K, T])
+  const ss_status sb = ss_build_candidates(targets, T * tg.K, V, C, seed, cand, slot, nullptr,
+                                           workspace, workspace_bytes, stream);
   if (sb != SS_OK) return sb;
   const int nsm = num_sms_current();
   if (nsm <= 0) return fail("cudaGetDevice/cudaDeviceGetAttribute", cudaGetLastError());
@@ -542,10 +553,24 @@ static ss_status step_impl(const int32_t* targets, const uint16_t* H, const uint
   // one gather of W[cand] serves the forward and the backward
   ss_status r = enqueue_gather(W, cand, C, V, D, reinterpret_cast<uint16_t*>(ws + L.wc), status, nsm, s);
   if (r != SS_OK) return r;
-  r = enqueue_forward(H, slot, T, C, D, cap, tau, loss, lse, L, ws, nsm, s);
+  r = enqueue_forward(H, slot, T, C, D, cap, tau, tg, loss, lse, L, ws, nsm, s);
   if (r != SS_OK) return r;
-  return enqueue_backward(H, cand, slot, lse, T, V, C, D, cap, tau, scale, accumulate, dH, dW, L,
-                          ws, nsm, s);
+  return enqueue_backward(H, cand, slot, lse, T, V, C, D, cap, tau, tg, scale, accumulate, dH, dW,
+                          L, ws, nsm, s);
+}
+
+// K targets per token with host weights w[0..K): 1 <= K <= kMaxTargets, each
+// w[k] finite and >= 0, their sum > 0
+static ss_status targets_args(int64_t K, const float* w, Targets* tg) {
+  if (K < 1 || K > kMaxTargets || !w) return SS_ERR_INVALID;
+  float sum = 0.f;
+  *tg = Targets{static_cast<int>(K), {}};
+  for (int64_t k = 0; k < K; ++k) {
+    if (!(w[k] >= 0.f) || !std::isfinite(w[k])) return SS_ERR_INVALID;
+    tg->w[k] = w[k];
+    sum += w[k];
+  }
+  return sum > 0.f && std::isfinite(sum) ? SS_OK : SS_ERR_INVALID;
 }
 
 // the head options: NULL or cap == 0 is the plain head
@@ -565,7 +590,7 @@ ss_status ss_forward(const uint16_t* H, const uint16_t* W, const int32_t* cand,
                      const int32_t* slot, int64_t T, int64_t V, int64_t C, int64_t D,
                      float* loss, float* lse, void* workspace, size_t workspace_bytes,
                      ss_stream stream) {
-  return forward_impl(H, W, cand, slot, T, V, C, D, 0.f, 1.f, loss, lse, workspace,
+  return forward_impl(H, W, cand, slot, T, V, C, D, 0.f, 1.f, kOneTarget, loss, lse, workspace,
                       workspace_bytes, stream);
 }
 
@@ -576,7 +601,7 @@ ss_status ss_forward_head(const uint16_t* H, const uint16_t* W, const int32_t* c
   float cap, tau;
   const ss_status h = head_args(head, &cap, &tau);
   if (h != SS_OK) return h;
-  return forward_impl(H, W, cand, slot, T, V, C, D, cap, tau, loss, lse, workspace,
+  return forward_impl(H, W, cand, slot, T, V, C, D, cap, tau, kOneTarget, loss, lse, workspace,
                       workspace_bytes, stream);
 }
 
@@ -584,8 +609,8 @@ ss_status ss_backward(const uint16_t* H, const uint16_t* W, const int32_t* cand,
                       const int32_t* slot, const float* lse, int64_t T, int64_t V, int64_t C,
                       int64_t D, float scale, int accumulate, uint16_t* dH, float* dW,
                       void* workspace, size_t workspace_bytes, ss_stream stream) {
-  return backward_impl(H, W, cand, slot, lse, T, V, C, D, 0.f, 1.f, scale, accumulate, dH, dW,
-                       workspace, workspace_bytes, stream);
+  return backward_impl(H, W, cand, slot, lse, T, V, C, D, 0.f, 1.f, kOneTarget, scale, accumulate,
+                       dH, dW, workspace, workspace_bytes, stream);
 }
 
 ss_status ss_backward_head(const uint16_t* H, const uint16_t* W, const int32_t* cand,
@@ -596,16 +621,16 @@ ss_status ss_backward_head(const uint16_t* H, const uint16_t* W, const int32_t* 
   float cap, tau;
   const ss_status h = head_args(head, &cap, &tau);
   if (h != SS_OK) return h;
-  return backward_impl(H, W, cand, slot, lse, T, V, C, D, cap, tau, scale, accumulate, dH, dW,
-                       workspace, workspace_bytes, stream);
+  return backward_impl(H, W, cand, slot, lse, T, V, C, D, cap, tau, kOneTarget, scale, accumulate,
+                       dH, dW, workspace, workspace_bytes, stream);
 }
 
 ss_status ss_step(const int32_t* targets, const uint16_t* H, const uint16_t* W, int64_t T,
                   int64_t V, int64_t C, int64_t D, uint64_t seed, float scale, int accumulate,
                   int32_t* cand, int32_t* slot, float* loss, float* lse, uint16_t* dH, float* dW,
                   void* workspace, size_t workspace_bytes, ss_stream stream) {
-  return step_impl(targets, H, W, T, V, C, D, seed, 0.f, 1.f, scale, accumulate, cand, slot, loss,
-                   lse, dH, dW, workspace, workspace_bytes, stream);
+  return step_impl(targets, H, W, T, V, C, D, seed, 0.f, 1.f, kOneTarget, scale, accumulate, cand,
+                   slot, loss, lse, dH, dW, workspace, workspace_bytes, stream);
 }
 
 ss_status ss_step_head(const int32_t* targets, const uint16_t* H, const uint16_t* W, int64_t T,
@@ -616,8 +641,49 @@ ss_status ss_step_head(const int32_t* targets, const uint16_t* H, const uint16_t
   float cap, tau;
   const ss_status h = head_args(head, &cap, &tau);
   if (h != SS_OK) return h;
-  return step_impl(targets, H, W, T, V, C, D, seed, cap, tau, scale, accumulate, cand, slot, loss,
-                   lse, dH, dW, workspace, workspace_bytes, stream);
+  return step_impl(targets, H, W, T, V, C, D, seed, cap, tau, kOneTarget, scale, accumulate, cand,
+                   slot, loss, lse, dH, dW, workspace, workspace_bytes, stream);
+}
+
+ss_status ss_forward_mtp(const uint16_t* H, const uint16_t* W, const int32_t* cand,
+                         const int32_t* slot, int64_t K, const float* weights, int64_t T,
+                         int64_t V, int64_t C, int64_t D, const ss_head* head, float* loss,
+                         float* lse, void* workspace, size_t workspace_bytes, ss_stream stream) {
+  float cap, tau;
+  Targets tg;
+  ss_status a = head_args(head, &cap, &tau);
+  if (a == SS_OK) a = targets_args(K, weights, &tg);
+  if (a != SS_OK) return a;
+  return forward_impl(H, W, cand, slot, T, V, C, D, cap, tau, tg, loss, lse, workspace,
+                      workspace_bytes, stream);
+}
+
+ss_status ss_backward_mtp(const uint16_t* H, const uint16_t* W, const int32_t* cand,
+                          const int32_t* slot, int64_t K, const float* weights, const float* lse,
+                          int64_t T, int64_t V, int64_t C, int64_t D, const ss_head* head,
+                          float scale, int accumulate, uint16_t* dH, float* dW, void* workspace,
+                          size_t workspace_bytes, ss_stream stream) {
+  float cap, tau;
+  Targets tg;
+  ss_status a = head_args(head, &cap, &tau);
+  if (a == SS_OK) a = targets_args(K, weights, &tg);
+  if (a != SS_OK) return a;
+  return backward_impl(H, W, cand, slot, lse, T, V, C, D, cap, tau, tg, scale, accumulate, dH, dW,
+                       workspace, workspace_bytes, stream);
+}
+
+ss_status ss_step_mtp(const int32_t* targets, int64_t K, const float* weights, const uint16_t* H,
+                      const uint16_t* W, int64_t T, int64_t V, int64_t C, int64_t D, uint64_t seed,
+                      const ss_head* head, float scale, int accumulate, int32_t* cand,
+                      int32_t* slot, float* loss, float* lse, uint16_t* dH, float* dW,
+                      void* workspace, size_t workspace_bytes, ss_stream stream) {
+  float cap, tau;
+  Targets tg;
+  ss_status a = head_args(head, &cap, &tau);
+  if (a == SS_OK) a = targets_args(K, weights, &tg);
+  if (a != SS_OK) return a;
+  return step_impl(targets, H, W, T, V, C, D, seed, cap, tau, tg, scale, accumulate, cand, slot,
+                   loss, lse, dH, dW, workspace, workspace_bytes, stream);
 }
 
 int64_t ss_schedule_candidates(int64_t step, int64_t total_steps, int64_t V) {
@@ -699,13 +765,14 @@ ss_status ss_forward_noalloc(const uint16_t* H, const uint16_t* W, const int32_t
     return fail("cuTensorMapEncodeTiled", cudaErrorInvalidValue);
   trace_pre(s, "gemm_forward_lse");
   e = launch_forward_logits(tH, tWc, static_cast<int>(T), static_cast<int>(C),
-                            static_cast<int>(D), slot, part, tgt, 0.f, 1.f, status, nsm, s);
+                            static_cast<int>(D), slot, part, tgt, 0.f, 1.f, kOneTarget, status,
+                            nsm, s);
   trace_post(s);
   if (e != cudaSuccess) return fail("launch gemm_forward_lse", e);
   trace_pre(s, "lse_merge");
   e = launch_pdl(k_lse_merge, dim3(static_cast<int>((T * kMergeLanes + 255) / 256)), dim3(256), 0, s,
                  part, tgt, slot, static_cast<int>(T), static_cast<int>(C),
-                 static_cast<int>(L.n_ct * fwd_groups(0.f)), loss, lse, status);
+                 static_cast<int>(L.n_ct * fwd_groups(0.f)), kOneTarget, loss, lse, status);
   trace_post(s);
   if (e != cudaSuccess) return fail("launch k_lse_merge", e);
   if (status_host) {
@@ -779,8 +846,9 @@ ss_status ss_step_graph_create(const int32_t* targets, const uint16_t* H, const 
     cudaStreamDestroy(cs);
     return fail("cudaStreamBeginCapture", e);
   }
-  const ss_status r = step_impl(targets, H, W, T, V, C, D, 0, cap, tau, scale, accumulate, cand,
-                                slot, loss, lse, dH, dW, workspace, workspace_bytes, cs);
+  const ss_status r = step_impl(targets, H, W, T, V, C, D, 0, cap, tau, kOneTarget, scale,
+                                accumulate, cand, slot, loss, lse, dH, dW, workspace,
+                                workspace_bytes, cs);
   cudaGraph_t g = nullptr;
   e = cudaStreamEndCapture(cs, &g);
   cudaStreamDestroy(cs);

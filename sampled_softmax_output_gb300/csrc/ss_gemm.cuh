@@ -112,7 +112,7 @@ __device__ __forceinline__ float head_dz(float z, const HeadCap& h) {
 //   writes part[nt * NCG + cg][t] = (max_j S[t,j], sum_j exp(S[t,j] - max))
 //   over its valid columns, or (-inf, 0) if it has none; tgt[t] = S[t, slot[t]]
 //   comes from the group that holds slot[t].
-template <bool CAP>
+template <bool CAP, int KMAX = 1>
 struct EpiFwdT {
   static constexpr int kStageBytes = 0;
   static constexpr bool kKeepOperands = false;
@@ -120,9 +120,10 @@ struct EpiFwdT {
     int T, C;
     const int32_t* slot;
     float2* part;
-    float* tgt;
+    float* tgt;    // [K * T]: the logit (z when CAP) of each target
     int* status;
     HeadCap head;  // used when CAP: the partials and the target logit are of z
+    Targets tg;    // used when KMAX > 1
   };
   __device__ static void finish(const Params&, EpiState&) {}
   template <int BN, int NCG>
@@ -131,11 +132,15 @@ struct EpiFwdT {
     constexpr int CPG = BN / 32 / NCG;  // chunks per group
     const int t = mt * BM + row;
     const bool valid = t < p.T;
-    const int sl = valid ? __ldg(p.slot + t) : -1;
+    const int K = KMAX > 1 ? p.tg.K : 1;
+    int sl[KMAX];
+#pragma unroll
+    for (int k = 0; k < KMAX; ++k)
+      sl[k] = (valid && k < K) ? __ldg(p.slot + static_cast<size_t>(k) * p.T + t) : -1;
     const int j0 = nt * BN + cg * CPG * 32;  // first column of this group
     const int ncols = min(CPG * 32, p.C - j0);
-    float m = -INFINITY, s = 0.f, tg = 0.f;
-    bool has_t = false;
+    float m = -INFINITY, s = 0.f, tg[KMAX];
+    uint32_t has_t = 0u;  // bit k: target k lies in this group's columns
     if (ncols > 0) {  // uniform: depends on the tile only
       for_tmem_chunks<CPG>(taddr, cg * CPG, [&](const uint32_t(&r)[32], int i) {
         const int jc = i * 32;
@@ -161,18 +166,31 @@ struct EpiFwdT {
         }
         s = s * ex2_approx((m - nm) * kLog2e) + ((a0 + a1) + (a2 + a3));
         m = nm;
-        const int off = sl - j0 - jc;
-        if (static_cast<unsigned>(off) < static_cast<unsigned>(nv)) {
 #pragma unroll
-          for (int k = 0; k < 32; ++k)
-            if (k == off) tg = v[k];
-          has_t = true;
+        for (int k = 0; k < KMAX; ++k) {
+          if (k >= K) break;  // uniform
+          const int off = sl[k] - j0 - jc;
+          const bool hit = static_cast<unsigned>(off) < static_cast<unsigned>(nv);
+          // a target falls in a given 32-column chunk for a few rows of a warp
+          // at most: skip the selection unless one does
+          if (KMAX == 1 || __any_sync(0xffffffffu, hit)) {
+            if (hit) {
+              float x = 0.f;
+#pragma unroll
+              for (int e = 0; e < 32; ++e)
+                if (e == off) x = v[e];
+              tg[k] = x;
+              has_t |= 1u << k;
+            }
+          }
         }
       });
     }
     if (valid) {
       p.part[static_cast<size_t>(nt * NCG + cg) * p.T + t] = make_float2(m, s);
-      if (has_t) p.tgt[t] = tg;
+#pragma unroll
+      for (int k = 0; k < KMAX; ++k)
+        if ((has_t >> k) & 1u) p.tgt[static_cast<size_t>(k) * p.T + t] = tg[k];
     }
   }
 };
@@ -186,7 +204,7 @@ using EpiFwd = EpiFwdT<false>;
 // writes leave as full lines instead of 32 rows per warp instruction. The
 // one-hot term touches one element per row: it is recomputed in fp32 and
 // patched into the staged tile.
-template <bool CAP>
+template <bool CAP, int KMAX = 1>
 struct EpiGT {
   // two 16 KB staging buffers: both for one column group, one each for two
   static constexpr int kStageBytes = 2 * 16384;
@@ -201,6 +219,8 @@ struct EpiGT {
     float log2_scale;  // log2|scale| (-inf for 0)
     int* status;
     HeadCap head;      // used when CAP: G = scale * (P(z) - Y) * dz/ds
+    Targets tg;        // used when KMAX > 1: G = scale (W P - sum_k w[k] Y_k), W = sum_k w[k];
+                       // log2_scale is then log2(|scale| W)
   };
   __device__ static void finish(const Params&, EpiState& es) {
     if ((es.ep_tid & 127) == 0) bulk_wait<0>();
@@ -216,9 +236,14 @@ struct EpiGT {
     const bool leader = (es.ep_tid & 127) == 0;
     const int t = mt * BM + row;
     const bool valid = t < p.T;
-    const int sl = valid ? __ldg(p.slot + t) : -1;
-    if (valid && nt == 0 && static_cast<unsigned>(sl) >= static_cast<unsigned>(p.C))
-      set_status(p.status, SS_ERR_INDEX);
+    const int K = KMAX > 1 ? p.tg.K : 1;
+    int sl[KMAX];
+#pragma unroll
+    for (int k = 0; k < KMAX; ++k) {
+      sl[k] = (valid && k < K) ? __ldg(p.slot + static_cast<size_t>(k) * p.T + t) : -1;
+      if (valid && k < K && nt == 0 && static_cast<unsigned>(sl[k]) >= static_cast<unsigned>(p.C))
+        set_status(p.status, SS_ERR_INDEX);
+    }
     const float asc = fabsf(p.scale);
     const uint32_t sgn = p.scale < 0.f ? 0x80008000u : 0u;
     const float off2 = valid ? fmaf(__ldg(p.lse + t), kLog2e, -p.log2_scale) : 0.f;
@@ -267,23 +292,34 @@ struct EpiGT {
           st_shared_v4(rowbase + ((ci ^ r7) << 4), pk[4 * v], pk[4 * v + 1], pk[4 * v + 2],
                        pk[4 * v + 3]);
         }
-        const int off = sl - j0 - jc;
-        const bool has = static_cast<unsigned>(off) < 32u;
-        if (__any_sync(0xffffffffu, has)) {
-          float xt = 0.f;
 #pragma unroll
-          for (int i = 0; i < 32; ++i) xt = (i == off) ? __uint_as_float(r[i]) : xt;
-          if (has) {
-            float gt;
-            if constexpr (CAP) {
-              const float zt = head_z(xt, p.head);
-              gt = (ex2_approx(fmaf(zt, kLog2e, -off2)) - asc) * head_dz(zt, p.head);
-            } else {
-              gt = ex2_approx(fmaf(xt, kLog2e, -off2)) - asc;
+        for (int k = 0; k < KMAX; ++k) {
+          if (k >= K) break;  // uniform
+          const int off = sl[k] - j0 - jc;
+          const bool has = static_cast<unsigned>(off) < 32u;
+          if (__any_sync(0xffffffffu, has)) {
+            float xt = 0.f;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) xt = (i == off) ? __uint_as_float(r[i]) : xt;
+            if (has) {
+              // the one-hot weight of this column: every target k2 that falls on it
+              float wt = 1.f;
+              if constexpr (KMAX > 1) {
+                wt = 0.f;
+#pragma unroll
+                for (int k2 = 0; k2 < KMAX; ++k2) wt += (sl[k2] == sl[k]) ? p.tg.w[k2] : 0.f;
+              }
+              float gt;
+              if constexpr (CAP) {
+                const float zt = head_z(xt, p.head);
+                gt = (ex2_approx(fmaf(zt, kLog2e, -off2)) - asc * wt) * head_dz(zt, p.head);
+              } else {
+                gt = ex2_approx(fmaf(xt, kLog2e, -off2)) - asc * wt;
+              }
+              const uint16_t bits = bf16_bits(gt) ^ static_cast<uint16_t>(sgn & 0xffffu);
+              const uint32_t cc = static_cast<uint32_t>(32 * h + off);
+              st_shared_b16(rowbase + (((cc >> 3) ^ r7) << 4) + (cc & 7u) * 2u, bits);
             }
-            const uint16_t bits = bf16_bits(gt) ^ static_cast<uint16_t>(sgn & 0xffffu);
-            const uint32_t cc = static_cast<uint32_t>(32 * h + off);
-            st_shared_b16(rowbase + (((cc >> 3) ^ r7) << 4) + (cc & 7u) * 2u, bits);
           }
         }
       }

@@ -1,0 +1,70 @@
+// ss_gemm_logits.cuh -- launch templates of the two logit GEMMs (forward
+// partials, softmax gradient) for a head (plain or capped) and a number of
+// targets per token; instantiated by ss_gemm_logits.cu (one target) and
+// ss_gemm_logits_mtp.cu (several).
+#pragma once
+
+#include <math.h>
+
+#include "ss_gemm.cuh"
+#include "ss_gemm2.cuh"
+#include "ss_internal.h"
+
+namespace ss {
+
+constexpr int kStagesLogits = 4;
+
+template <bool CAP, int KMAX>
+cudaError_t forward_logits(const CUtensorMap& tH, const CUtensorMap& tWc, int T, int C, int D,
+                           const int32_t* slot, float2* part, float* tgt, const HeadCap& head,
+                           const Targets& tg, int* status, int num_sms, cudaStream_t stream) {
+  GemmShape shp{(T + BM - 1) / BM, (C + kBnLogits - 1) / kBnLogits, D / BK};
+  typename EpiFwdT<CAP, KMAX>::Params ep{T, C, slot, part, tgt, status, head, tg};
+  // the capped head's epilogue (three MUFU operations per logit) runs eight
+  // warps in two column groups, two partials per row per tile
+  return launch_gemm<kBnLogits, kStagesLogits, false, false, EpiFwdT<CAP, KMAX>, CAP ? 8 : 4>(
+      tH, tWc, shp, ep, status, num_sms, stream);
+}
+
+template <bool CAP, int KMAX>
+cudaError_t softmax_grad(const CUtensorMap& tH, const CUtensorMap& tWc,
+                         const CUtensorMap& tWc_half, const CUtensorMap& tG_store, int T, int C,
+                         int D, const int32_t* slot, const float* lse, float scale,
+                         const HeadCap& head, const Targets& tg, int* status, int num_sms,
+                         cudaStream_t stream) {
+  typename EpiGT<CAP, KMAX>::Params ep;
+  ep.tmG = tG_store;
+  ep.T = T;
+  ep.C = C;
+  ep.slot = slot;
+  ep.lse = lse;
+  ep.scale = scale;
+  float wsum = 0.f;
+  for (int k = 0; k < tg.K; ++k) wsum += tg.w[k];
+  const float sw = fabsf(scale) * wsum;  // the bulk term is scale * W * P
+  ep.log2_scale = sw == 0.f ? -INFINITY : log2f(sw);
+  ep.status = status;
+  ep.head = head;
+  ep.tg = tg;
+  // eight epilogue warps in two column groups, one staging buffer each; CTA
+  // pairs (each SM stages half of the W_c tile, a 6-deep ring beside the G
+  // staging) once the operands exceed L2 (measured on GB300: the pair is 5%
+  // slower at (T + C) * D * 2 = 41 MB, 2-3% faster at 138 and 177 MB)
+  const int n_tiles = (C + kBnLogits - 1) / kBnLogits;
+  if (operands_exceed_l2(T, C, D)) {
+    GemmShape shp{(T + 2 * BM - 1) / (2 * BM), n_tiles, D / BK};
+    return launch_gemm2<kBnLogits, 6, false, false, EpiGT<CAP, KMAX>, 8>(tH, tWc_half, shp, ep,
+                                                                   status, num_sms, stream);
+  }
+  GemmShape shp{(T + BM - 1) / BM, n_tiles, D / BK};
+  return launch_gemm<kBnLogits, kStagesLogits, false, false, EpiGT<CAP, KMAX>, 8>(tH, tWc, shp, ep,
+                                                                            status, num_sms,
+                                                                            stream);
+}
+
+inline HeadCap head_cap(float cap, float tau) {
+  const float log2e = 1.4426950408889634f;
+  return cap > 0.f ? HeadCap{cap, log2e / tau, 1.f / (cap * tau)} : HeadCap{0.f, 0.f, 0.f};
+}
+
+}  // namespace ss

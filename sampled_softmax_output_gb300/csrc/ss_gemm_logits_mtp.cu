@@ -1,0 +1,33 @@
+// ss_gemm_logits_mtp.cu -- the logit GEMMs for several targets per token
+// (multi-token prediction over one set of logits): up to kMaxTargets target
+// logits per row in the forward, the weighted one-hot terms in the softmax
+// gradient. A translation unit of its own so that the instantiations compile
+// in parallel with the single-target ones.
+#include "ss_gemm_logits.cuh"
+
+namespace ss {
+
+cudaError_t launch_forward_logits_mtp(const CUtensorMap& tH, const CUtensorMap& tWc, int T, int C,
+                                      int D, const int32_t* slot, float2* part, float* tgt,
+                                      float cap, float tau, const Targets& tg, int* status,
+                                      int num_sms, cudaStream_t stream) {
+  const HeadCap h = head_cap(cap, tau);
+  return cap > 0.f ? forward_logits<true, kMaxTargets>(tH, tWc, T, C, D, slot, part, tgt, h, tg,
+                                                       status, num_sms, stream)
+                   : forward_logits<false, kMaxTargets>(tH, tWc, T, C, D, slot, part, tgt, h, tg,
+                                                        status, num_sms, stream);
+}
+
+cudaError_t launch_softmax_grad_mtp(const CUtensorMap& tH, const CUtensorMap& tWc,
+                                    const CUtensorMap& tWc_half, const CUtensorMap& tG_store,
+                                    int T, int C, int D, const int32_t* slot, const float* lse,
+                                    float scale, float cap, float tau, const Targets& tg,
+                                    int* status, int num_sms, cudaStream_t stream) {
+  const HeadCap h = head_cap(cap, tau);
+  return cap > 0.f ? softmax_grad<true, kMaxTargets>(tH, tWc, tWc_half, tG_store, T, C, D, slot,
+                                                     lse, scale, h, tg, status, num_sms, stream)
+                   : softmax_grad<false, kMaxTargets>(tH, tWc, tWc_half, tG_store, T, C, D, slot,
+                                                      lse, scale, h, tg, status, num_sms, stream);
+}
+
+}  // namespace ss

@@ -51,6 +51,14 @@ inline int fwd_groups(float cap) { return cap > 0.f ? 2 : 1; }
 
 struct GemmShape;
 
+// Targets per token: K (at most kMaxTargets) target slots per row,
+// slot[k * T + t], with weights w[k] (K = 1, w = 1: the single-target loss).
+constexpr int kMaxTargets = 8;
+struct Targets {
+  int K;
+  float w[kMaxTargets];
+};
+
 // Above this size, H [T, D] and W_c [C, D] together (bf16) no longer stay in
 // L2 while a GEMM sweeps over them. The softmax-gradient GEMM then runs on
 // CTA pairs (each SM loads half of every W_c tile) and the two gradient GEMMs
@@ -72,16 +80,28 @@ cudaError_t launch_build_candidates(const int32_t* targets, int T, int V, int C,
 // tWc: box 64 x 256 (one 1-CTA tile); tWc_half: box 64 x 128 (a CTA's half of
 // a pair's tile).
 // cap > 0: the capped head z = cap / (1 + exp(-s / tau)) replaces the logits.
+// tg: the targets per token (K = 1, w = 1 for the single-target loss).
 cudaError_t launch_forward_logits(const CUtensorMap& tH, const CUtensorMap& tWc, int T, int C,
                                   int D, const int32_t* slot, float2* part, float* tgt,
-                                  float cap, float tau, int* status, int num_sms,
-                                  cudaStream_t stream);
+                                  float cap, float tau, const Targets& tg, int* status,
+                                  int num_sms, cudaStream_t stream);
 // G is written through tG_store: G [T, C] bf16, box 64 x 128, 128-byte swizzle.
 cudaError_t launch_softmax_grad(const CUtensorMap& tH, const CUtensorMap& tWc,
                                 const CUtensorMap& tWc_half,
                                 const CUtensorMap& tG_store, int T, int C, int D,
                                 const int32_t* slot, const float* lse, float scale, float cap,
-                                float tau, int* status, int num_sms, cudaStream_t stream);
+                                float tau, const Targets& tg, int* status, int num_sms,
+                                cudaStream_t stream);
+// the same GEMMs for K > 1 targets per token (ss_gemm_logits_mtp.cu)
+cudaError_t launch_forward_logits_mtp(const CUtensorMap& tH, const CUtensorMap& tWc, int T, int C,
+                                      int D, const int32_t* slot, float2* part, float* tgt,
+                                      float cap, float tau, const Targets& tg, int* status,
+                                      int num_sms, cudaStream_t stream);
+cudaError_t launch_softmax_grad_mtp(const CUtensorMap& tH, const CUtensorMap& tWc,
+                                    const CUtensorMap& tWc_half, const CUtensorMap& tG_store,
+                                    int T, int C, int D, const int32_t* slot, const float* lse,
+                                    float scale, float cap, float tau, const Targets& tg,
+                                    int* status, int num_sms, cudaStream_t stream);
 
 // ---- gradient GEMMs (ss_gemm_grads.cu)
 // dH = G . W_c : A = G [T, C] (K-major), B = W_c [C, D] (MN-major)

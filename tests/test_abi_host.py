@@ -21,7 +21,8 @@ def test_exports_every_declared_symbol():
                           "ss_last_error", "ss_forward_noalloc", "ss_step",
                           "ss_schedule_candidates", "ss_clear_rows", "ss_step_graph_create",
                           "ss_step_graph_launch", "ss_step_graph_destroy", "ss_forward_head",
-                          "ss_backward_head", "ss_step_head"}
+                          "ss_backward_head", "ss_step_head", "ss_forward_mtp", "ss_backward_mtp",
+                          "ss_step_mtp"}
     for n in names:
         assert hasattr(ss.lib(), n), n
 
@@ -234,3 +235,28 @@ def test_head_argument_errors():
                                  h, 1.0, 0, p(FAKE), p(FAKE), p(FAKE), 1 << 40, None)
         assert bwd == INVALID, (cap, tau)
     assert fwd(ctypes.byref(ss.Head(30.0, 7.5)), wsb=16) == WORKSPACE
+
+
+def test_several_targets_argument_errors():
+    """K in [1, SS_MAX_TARGETS]; weights finite, >= 0, with a positive sum."""
+    L = ss.lib()
+
+    def step(weights, K=None, T=0, wsb=1 << 40):
+        w = (ctypes.c_float * max(1, len(weights)))(*weights) if weights else None
+        K = len(weights) if K is None else K
+        return L.ss_step_mtp(p(FAKE), K, w, p(FAKE), p(FAKE), T, 50304, 4096, 768, 0, None, 1.0, 0,
+                             p(FAKE), p(FAKE), p(FAKE), p(FAKE), p(FAKE), p(FAKE), p(FAKE), wsb,
+                             None)
+
+    for bad in ([], [0.0], [0.0, 0.0], [-1.0, 2.0], [float("nan")], [float("inf"), 1.0],
+                [1.0] * 9):
+        assert step(bad) == INVALID, bad
+    assert step([1.0], K=0) == INVALID
+    need = L.ss_workspace_size(256, 50304, 4096, 768)
+    assert step([1.0, 0.5], T=256, wsb=need - 1) == WORKSPACE
+    w = (ctypes.c_float * 2)(1.0, -0.5)
+    assert L.ss_forward_mtp(p(FAKE), p(FAKE), p(FAKE), p(FAKE), 2, w, 0, 50304, 4096, 768, None,
+                            p(FAKE), p(FAKE), p(FAKE), 1 << 40, None) == INVALID
+    assert L.ss_backward_mtp(p(FAKE), p(FAKE), p(FAKE), p(FAKE), 2, w, p(FAKE), 0, 50304, 4096,
+                             768, None, 1.0, 0, p(FAKE), p(FAKE), p(FAKE), 1 << 40,
+                             None) == INVALID
