@@ -136,6 +136,7 @@ __global__ void __launch_bounds__(256) k_gather_rows(const uint16_t* __restrict_
 // eight (max, sum) pairs are combined with shuffles. (-inf, 0) marks a tile
 // part without valid columns.
 constexpr int kMergeLanes = 8;
+static_assert(kMaxTargets <= kMergeLanes, "one lane of a token's group per target");
 
 __device__ __forceinline__ void lse_fold(float& M, float& S, float m, float s) {
   if (m == -INFINITY) return;
@@ -156,6 +157,14 @@ __global__ void __launch_bounds__(256) k_lse_merge(const float2* __restrict__ pa
   const int t = gid / kMergeLanes;
   const int k = gid % kMergeLanes;
   const bool valid = t < T;  // whole groups of 8 lanes share a token
+  // lane j < K of the group fetches target j's slot and logit along with the
+  // partials (one memory round trip for all of them)
+  int my_slot = 0;
+  float my_tgt = 0.f;
+  if (valid && k < tg.K) {
+    my_slot = __ldg(slot + static_cast<size_t>(k) * T + t);
+    my_tgt = __ldcg(tgt + static_cast<size_t>(k) * T + t);
+  }
   float M = -INFINITY, S = 0.f;
   constexpr int kBatch = 8;  // loads a thread has in flight
   if (valid)
@@ -175,18 +184,24 @@ __global__ void __launch_bounds__(256) k_lse_merge(const float2* __restrict__ pa
     const float s2 = __shfl_xor_sync(0xffffffffu, S, o);
     lse_fold(M, S, m2, s2);
   }
-  if (!valid || k != 0) return;
-  for (int j = 0; j < tg.K; ++j)
-    if (static_cast<unsigned>(__ldg(slot + static_cast<size_t>(j) * T + t)) >=
-        static_cast<unsigned>(C)) {
-      set_status(status, SS_ERR_INDEX);
-      return;
-    }
   const float l = M + logf(S);
-  lse[t] = l;
-  // sum over the targets of w[j] (lse - target logit); one target: lse - tgt
+  // sum over the targets of w[j] (lse - target logit), lanes 0..K-1 of the
+  // group (one target: lse - tgt); a slot out of range is an error
+  bool bad = valid && k < tg.K && static_cast<unsigned>(my_slot) >= static_cast<unsigned>(C);
   float acc = 0.f;
-  for (int j = 0; j < tg.K; ++j) acc += tg.w[j] * (l - tgt[static_cast<size_t>(j) * T + t]);
+  const int base = (threadIdx.x & 31) & ~(kMergeLanes - 1);
+  for (int j = 0; j < tg.K; ++j) {  // K <= kMergeLanes
+    const float tj = __shfl_sync(0xffffffffu, my_tgt, base + j);
+    acc += tg.w[j] * (l - tj);
+  }
+#pragma unroll
+  for (int o = 1; o < kMergeLanes; o <<= 1) bad |= __shfl_xor_sync(0xffffffffu, bad, o) != 0;
+  if (!valid || k != 0) return;
+  if (bad) {
+    set_status(status, SS_ERR_INDEX);
+    return;
+  }
+  lse[t] = l;
   loss[t] = acc;
 }
 
