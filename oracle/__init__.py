@@ -89,6 +89,12 @@ def load(path: str):
         f.restype = None
         f.argtypes = [_p, _p, _p, _p, _i64, _p, _p, _i64, _i64, _i64, real, real, real, _p, _i64,
                       _p]
+    L.orc_round_e4m3.restype = ctypes.c_float
+    L.orc_round_e4m3.argtypes = [ctypes.c_float]
+    L.orc_e4m3_scale_exponent.restype = ctypes.c_int
+    L.orc_e4m3_scale_exponent.argtypes = [ctypes.c_float]
+    L.orc_quantize_e4m3_bf16.restype = None
+    L.orc_quantize_e4m3_bf16.argtypes = [_p, _i64, ctypes.c_int, _p]
     L.orc_num_threads.restype = ctypes.c_int
     L.orc_num_threads.argtypes = []
     return L
@@ -330,3 +336,54 @@ def loss_and_grads_mtp(H, W, targets, weights, C, seed, scale=1.0, dtype=np.floa
     dW[cand] = dWc
     return {"cand": cand, "slot": slot, "U": U, "loss": loss, "lse": lse, "dH": dH, "dW": dW,
             "dWc": dWc}
+
+
+# ------------------------------------------------------------------ FP8 head
+
+def round_e4m3(x: float) -> float:
+    return float(lib().orc_round_e4m3(x))
+
+
+def e4m3_scale_exponent(amax: float) -> int:
+    return int(lib().orc_e4m3_scale_exponent(amax))
+
+
+def quantize_e4m3(bits: np.ndarray, e: int | None = None):
+    """bf16 bit patterns -> (rounded bf16 bit patterns, e): every value scaled
+    by 2^e (e from the tensor's amax unless given), rounded to e4m3, scaled back."""
+    b = np.ascontiguousarray(bits, np.uint16)
+    if e is None:
+        from synth import bf16_bits_to_f32
+        amax = float(np.abs(bf16_bits_to_f32(b)).max()) if b.size else 0.0
+        e = e4m3_scale_exponent(amax)
+    out = np.empty_like(b)
+    lib().orc_quantize_e4m3_bf16(_ptr(b), b.size, e, _ptr(out))
+    return out, e
+
+
+def fp8_inputs(H, W, cand):
+    """The FP8 head's operands: H rounded with its own exponent, the candidate
+    rows of W rounded with theirs (the other rows of W are never read)."""
+    Hq, eH = quantize_e4m3(H)
+    Wc_q, eW = quantize_e4m3(np.asarray(W)[cand])
+    Wq = np.array(W, copy=True)
+    Wq[cand] = Wc_q
+    return Hq, Wq, eH, eW
+
+
+def loss_and_grads_fp8(H, W, targets, C, seed, scale=1.0, dW_init=None, accumulate=False):
+    """The whole definition with the FP8 head: the single-target loss and its
+    gradients on the rounded operands (rows of dW outside cand untouched)."""
+    V = W.shape[0]
+    cand, slot, U = build_candidates(targets, V, C, seed)
+    Hq, Wq, eH, eW = fp8_inputs(H, W, cand)
+    loss, lse = forward(Hq, Wq, cand, slot)
+    dH = backward_dH(Hq, Wq, cand, slot, lse, scale)
+    dWc = backward_dWc(Hq, Wq, cand, slot, lse, scale)
+    dW = np.zeros(W.shape, np.float32) if dW_init is None else np.array(dW_init, np.float32)
+    if accumulate:
+        dW[cand] += dWc
+    else:
+        dW[cand] = dWc
+    return {"cand": cand, "slot": slot, "U": U, "loss": loss, "lse": lse, "dH": dH, "dW": dW,
+            "dWc": dWc, "eH": eH, "eW": eW}

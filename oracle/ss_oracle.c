@@ -60,6 +60,17 @@
  *   "Fast splittable pseudorandom number generators", OOPSLA 2014; the
  *   splitmix64.c reference by S. Vigna) is mix(seed + (i + 1) * 0x9E3779B97F4A7C15).
  *
+ * FP8 head ("KellerJordan/modded-nanogpt" README, technique list: FP8 for
+ * the head; no format details on the pages). Reading: the head's operands are
+ * rounded to the e4m3 grid (1 sign, 4 exponent bits with bias 7, 3 mantissa
+ * bits, subnormals down to 2^-9, largest value 448; round to nearest, ties to
+ * even) after scaling by one power of two per tensor, 2^e with e the largest
+ * integer such that amax * 2^e <= 448 (amax = max |x| over the tensor: all of
+ * H, all candidate rows of W), then scaled back. Everything downstream (the
+ * logits, the softmax, the gradients, which use the same rounded operands)
+ * is the definition above applied to the rounded H and W[cand]; G itself
+ * stays in the working precision.
+ *
  * Precision: the definition is fp32. Its inputs are bf16 bit patterns widened
  * exactly to float. An fp64 instantiation of the same loops, on double inputs,
  * exists for the finite-difference and library cross-checks. Build with
@@ -353,6 +364,41 @@ int orc_build_candidates(const int32_t* targets, int64_t T, int64_t V, int64_t C
 
 ORC_DEFINE(float, f32, uint16_t, LOAD_BF16, expf, logf)
 ORC_DEFINE(double, f64, double, LOAD_REAL, exp, log)
+
+/* ------------------------------------------------------------- e4m3 rounding */
+
+/* x rounded to the e4m3 grid, ties to even; |x| >= 448 saturates to 448. */
+float orc_round_e4m3(float x) {
+  if (x != x) return x;
+  const float a = fabsf(x);
+  if (a == 0.0f) return x;
+  if (a >= 448.0f) return copysignf(448.0f, x);
+  int e2;
+  frexpf(a, &e2);          /* a = m * 2^e2, m in [0.5, 1): a in [2^(e2-1), 2^e2) */
+  int E = e2 - 1;          /* binade exponent */
+  if (E < -6) E = -6;      /* below 2^-6: subnormals, spacing 2^-9 */
+  const float q = ldexpf(1.0f, E - 3);  /* grid spacing in this binade */
+  return copysignf(rintf(a / q) * q, x); /* a / q is exact; rintf rounds half to even */
+}
+
+/* the largest integer e with amax * 2^e <= 448 (0 for amax = 0) */
+int orc_e4m3_scale_exponent(float amax) {
+  if (!(amax > 0.0f)) return 0;
+  int k;
+  const float m = frexpf(amax, &k); /* amax = m 2^k, m in [0.5, 1); 448 = 0.875 * 2^9 */
+  return m <= 0.875f ? 9 - k : 8 - k;
+}
+
+/* out[i] = round_e4m3(x[i] * 2^e) * 2^-e for the bf16 values x (n of them), as
+ * bf16 bit patterns (the rounded values are exact in bf16) */
+void orc_quantize_e4m3_bf16(const uint16_t* x, int64_t n, int e, uint16_t* out) {
+  for (int64_t i = 0; i < n; ++i) {
+    const float v = ldexpf(orc_round_e4m3(ldexpf(bf16_to_float(x[i]), e)), -e);
+    uint32_t u;
+    memcpy(&u, &v, 4);
+    out[i] = (uint16_t)(u >> 16); /* exact: at most 4 significant bits */
+  }
+}
 
 int orc_num_threads(void) {
 #ifdef _OPENMP

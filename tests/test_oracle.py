@@ -654,3 +654,68 @@ def test_several_targets_loss_and_grads_builds_over_all_targets(orc):
     assert ref["U"] == allt.size
     np.testing.assert_array_equal(ref["cand"][:allt.size], allt)
     np.testing.assert_array_equal(ref["cand"][ref["slot"]], tg)
+
+
+# ------------------------------------------------------------------ FP8 head
+
+def test_e4m3_rounding_against_torch(orc):
+    """round_e4m3 against torch's float8_e4m3fn conversion (round to nearest,
+    ties to even) on values spread over every binade and on the grid's midpoints."""
+    rng = np.random.default_rng(20)
+    mags = np.exp2(rng.uniform(-12, np.log2(448.0), 20000)).astype(np.float32)
+    x = (mags * rng.choice([-1, 1], mags.size)).astype(np.float32)
+    grid = torch.arange(256, dtype=torch.int32).to(torch.uint8).view(torch.float8_e4m3fn).float()
+    grid = np.unique(grid[torch.isfinite(grid)].numpy().astype(np.float32))
+    mids = ((grid[1:] + grid[:-1]) / 2).astype(np.float32)
+    x = np.concatenate([x, grid, mids, -mids]).astype(np.float32)
+    x = x[np.abs(x) < 448.0]
+    ref = torch.from_numpy(x).to(torch.float8_e4m3fn).float().numpy()
+    got = np.array([orc.round_e4m3(float(v)) for v in x], np.float32)
+    np.testing.assert_array_equal(got, ref)
+
+
+def test_e4m3_grid_is_fixed_and_ties_go_to_even(orc):
+    grid = torch.arange(256, dtype=torch.int32).to(torch.uint8).view(torch.float8_e4m3fn).float()
+    grid = np.unique(grid[torch.isfinite(grid)].numpy().astype(np.float32))
+    assert grid.size == 253 and grid.max() == 448.0 and grid[grid > 0].min() == 2.0 ** -9
+    for v in grid:
+        assert orc.round_e4m3(float(v)) == v
+    codes = torch.from_numpy(grid).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    for a, b, ca, cb in zip(grid[:-1], grid[1:], codes[:-1], codes[1:]):
+        if a < 0 or b <= 0:
+            continue  # the positive half suffices (the rounding is sign-symmetric)
+        even = a if int(ca) % 2 == 0 else b
+        assert orc.round_e4m3(float((a + b) / 2)) == even, (a, b)
+    assert orc.round_e4m3(1000.0) == 448.0 and orc.round_e4m3(-449.0) == -448.0
+
+
+def test_e4m3_scale_exponent_is_the_largest_that_fits(orc):
+    rng = np.random.default_rng(21)
+    for amax in np.concatenate([np.exp2(rng.uniform(-20, 20, 2000)), [448.0, 224.0, 1.0, 0.875]]):
+        amax = float(np.float32(amax))
+        e = orc.e4m3_scale_exponent(amax)
+        assert amax * 2.0 ** e <= 448.0 < amax * 2.0 ** (e + 1), amax
+    assert orc.e4m3_scale_exponent(0.0) == 0
+
+
+def test_fp8_head_is_the_plain_loss_on_grid_inputs(orc):
+    """Inputs already on the scaled e4m3 grid are left as they are, so the FP8
+    head gives the plain head's results on them bit for bit; on ordinary bf16
+    inputs it rounds every operand to 4 significant bits."""
+    T, V, D, C = 40, 500, 32, 120
+    x, C = _case(T, V, D, C, 22)
+    Hq, _ = orc.quantize_e4m3(x["H"])
+    cand, _, _ = orc.build_candidates(x["targets"], V, C, 22)
+    Wq_rows, _ = orc.quantize_e4m3(x["W"][cand])
+    W2 = x["W"].copy()
+    W2[cand] = Wq_rows
+    a = orc.loss_and_grads_fp8(Hq, W2, x["targets"], C, 22, 0.5)
+    b = orc.loss_and_grads(Hq, W2, x["targets"], C, 22, 0.5)
+    for k in ("loss", "lse", "dH", "dW"):
+        np.testing.assert_array_equal(a[k], b[k])
+    vals = synth.bf16_bits_to_f32(Hq) * 2.0 ** a["eH"]
+    assert np.all([orc.round_e4m3(float(v)) == v for v in vals.ravel()[:500]])
+    c = orc.loss_and_grads_fp8(x["H"], x["W"], x["targets"], C, 22, 0.5)
+    d = orc.loss_and_grads(x["H"], x["W"], x["targets"], C, 22, 0.5)
+    assert not np.array_equal(c["loss"], d["loss"])
+    np.testing.assert_allclose(c["loss"], d["loss"], rtol=0.05)
