@@ -65,6 +65,8 @@ def parse_args():
     ap.add_argument("--cap", type=float, default=0.0,
                     help="capped head: logits z = cap / (1 + exp(-s / tau)) (0: plain head)")
     ap.add_argument("--tau", type=float, default=7.5)
+    ap.add_argument("--fp8", action="store_true",
+                    help="the FP8 head: e4m3 operands for the two logit GEMMs")
     ap.add_argument("--targets", type=int, default=1,
                     help="targets per token (multi-token prediction over one set of logits): "
                          "offsets 1..K of one Zipf stream, weights 1, 1/2, 1/4, ...")
@@ -230,28 +232,34 @@ def barrier(world: int):
 
 # ------------------------------------------------------------- CPU oracle
 
-def oracle_sample(x: dict, w, T_s: int, scale: float, cap: float = 0.0, tau: float = 1.0):
-    """One oracle pass over a bounded sample: the full-batch candidate build,
-    then forward + backward for the first T_s tokens against that candidate
-    set (with the same head as the native arm). Returns seconds."""
+def oracle_sample(x: dict, w, T_s: int, scale: float, cap: float = 0.0, tau: float = 1.0,
+                  fp8: bool = False):
+    """One oracle pass over a bounded sample: the full-batch candidate build
+    (and, for the FP8 head, the rounding of H and W[cand]), then forward +
+    backward for the first T_s tokens against that candidate set (with the
+    same head as the native arm). Returns seconds."""
     import oracle
     t0 = time.perf_counter()
     cand, slot, U = oracle.build_candidates(x["targets"], w.V, w.C, w.seed)
-    Hs = x["H"][:T_s]
+    H, W = x["H"], x["W"]
+    if fp8:
+        H, W, _, _ = oracle.fp8_inputs(H, W, cand)
+    Hs = H[:T_s]
     ss_ = slot[:T_s]
-    loss, lse = oracle.forward(Hs, x["W"], cand, ss_, cap=cap, tau=tau)
-    oracle.backward_dH(Hs, x["W"], cand, ss_, lse, scale, cap=cap, tau=tau)
-    oracle.backward_dWc(Hs, x["W"], cand, ss_, lse, scale, cap=cap, tau=tau)
+    loss, lse = oracle.forward(Hs, W, cand, ss_, cap=cap, tau=tau)
+    oracle.backward_dH(Hs, W, cand, ss_, lse, scale, cap=cap, tau=tau)
+    oracle.backward_dWc(Hs, W, cand, ss_, lse, scale, cap=cap, tau=tau)
     return time.perf_counter() - t0
 
 
-def cpu_baseline(x: dict, w, target_s: float, cap: float = 0.0, tau: float = 1.0) -> dict:
+def cpu_baseline(x: dict, w, target_s: float, cap: float = 0.0, tau: float = 1.0,
+                 fp8: bool = False) -> dict:
     import oracle
     oracle.build()
     scale = 1.0 / w.T
-    t_small = oracle_sample(x, w, 16, scale, cap, tau)
+    t_small = oracle_sample(x, w, 16, scale, cap, tau, fp8)
     T_s = int(max(16, min(w.T, 16 * target_s / max(t_small, 1e-3))))
-    dt = oracle_sample(x, w, T_s, scale, cap, tau)
+    dt = oracle_sample(x, w, T_s, scale, cap, tau, fp8)
     return {"value": T_s / dt, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
             "sample": (f"{w.name}: full-batch candidate build (T={w.T}) + forward/backward of the "
                        f"first {T_s} tokens against all C={w.C} candidates; {dt:.1f} s"),
@@ -283,7 +291,7 @@ def run_native(args, world, rank, local):
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     scale = 1.0 / T
 
-    cap, tau = args.cap, args.tau
+    cap, tau, fp8 = args.cap, args.tau, args.fp8
     n_tg = args.targets
     mtp_weights = [0.5 ** k for k in range(n_tg)]
     if n_tg > 1:
@@ -298,12 +306,13 @@ def run_native(args, world, rank, local):
                         tau=tau)
             return
         ss.step(h, W, tg, C, w.seed, ws, scale=scale, dW=dW, cand=cand, slot=slot, loss=loss,
-                lse=lse, dH=dH, cap=cap, tau=tau)
+                lse=lse, dH=dH, cap=cap, tau=tau, fp8=fp8)
 
     def step_three_calls(h=H, tg=targets):
         ss.build_candidates(tg, V, C, w.seed, ws, cand=cand, slot=slot)
-        ss.forward(h, W, cand, slot, ws, loss=loss, lse=lse, cap=cap, tau=tau)
-        ss.backward(h, W, cand, slot, lse, ws, scale=scale, dH=dH, dW=dW, cap=cap, tau=tau)
+        ss.forward(h, W, cand, slot, ws, loss=loss, lse=lse, cap=cap, tau=tau, fp8=fp8)
+        ss.backward(h, W, cand, slot, lse, ws, scale=scale, dH=dH, dW=dW, cap=cap, tau=tau,
+                    fp8=fp8)
 
     for _ in range(max(args.warmup, 1)):
         flush.zero_()
@@ -383,7 +392,7 @@ def run_native(args, world, rank, local):
     graph_ms = None
     if n_tg == 1:
         graph = ss.StepGraph(H, W, targets, C, ws, scale=scale, cand=cand, slot=slot, loss=loss,
-                             lse=lse, dH=dH, dW=dW, cap=cap, tau=tau)
+                             lse=lse, dH=dH, dW=dW, cap=cap, tau=tau, fp8=fp8)
         graph.launch(w.seed)
         sg = [torch.cuda.Event(enable_timing=True) for _ in range(K3)]
         eg = [torch.cuda.Event(enable_timing=True) for _ in range(K3)]
@@ -468,6 +477,7 @@ def run_native(args, world, rank, local):
                    "head": ({"cap": cap, "tau": tau, "logits": "cap / (1 + exp(-s / tau))"}
                             if cap else "plain"),
                    "targets_per_token": n_tg,
+                   "operands": "e4m3 (FP8 head) for the logit GEMMs" if fp8 else "bf16",
                    **({"target_weights": mtp_weights} if n_tg > 1 else {}),
                    "ms_per_step_three_calls": three_calls_ms,
                    "ms_per_step_graph": graph_ms,
@@ -498,13 +508,13 @@ def run_reference(args, world, rank):
     per_step_s = (args.ref_step_seconds if args.ref_step_seconds is not None
                   else min(5.0, 150.0 / max(K + W_, 1)))
     scale = 1.0 / w.T
-    t_small = oracle_sample(x, w, 8, scale, args.cap, args.tau)
+    t_small = oracle_sample(x, w, 8, scale, args.cap, args.tau, args.fp8)
     T_s = int(max(1, min(w.T, 8 * per_step_s / max(t_small, 1e-3))))
     for _ in range(W_):
-        oracle_sample(x, w, T_s, scale, args.cap, args.tau)
+        oracle_sample(x, w, T_s, scale, args.cap, args.tau, args.fp8)
     dt = 0.0
     for _ in range(K):
-        dt += oracle_sample(x, w, T_s, scale, args.cap, args.tau)
+        dt += oracle_sample(x, w, T_s, scale, args.cap, args.tau, args.fp8)
     value = T_s * K / dt
     cores = oracle.num_threads()
     sample = (f"{w.name}: per step, full-batch candidate build (T={w.T}) + forward/backward of "
@@ -531,7 +541,8 @@ def main():
     line, x, w = run_native(args, world, rank, local)
     if rank == 0:
         if world == 1 and not args.no_cpu_baseline:
-            line["cpu_baseline"] = cpu_baseline(x, w, args.cpu_seconds, args.cap, args.tau)
+            line["cpu_baseline"] = cpu_baseline(x, w, args.cpu_seconds, args.cap, args.tau,
+                                                args.fp8)
         else:
             line["cpu_baseline"] = None
         print(json.dumps(line), flush=True)

@@ -43,7 +43,9 @@
  *     C, a cand or slot entry out of range, a device wait that timed out) are
  *     recorded in a status word inside the workspace: the first error wins,
  *     later kernels of any call that shares the workspace see it and do no
- *     work, and ss_read_status returns it. ss_build_candidates clears it.
+ *     work, and ss_read_status returns it. ss_build_candidates clears it. A
+ *     new workspace must start with its first 1024 bytes (the header) zero,
+ *     unless its first call is ss_build_candidates or ss_step.
  *   - Limits: 1 <= C <= V <= SS_MAX_V; 0 <= T < 2^31; D % 64 == 0 and
  *     64 <= D <= SS_MAX_D. Out of range -> SS_ERR_UNSUPPORTED (or
  *     SS_ERR_INVALID for values that can never be valid).
@@ -155,10 +157,21 @@ ss_status ss_backward(const uint16_t* H, const uint16_t* W, const int32_t* cand,
  *   tau : finite > 0 when cap > 0.
  * Other values -> SS_ERR_INVALID. The *_head entry points below take it; the
  * same head must be passed to the forward and the backward of one batch.
+ *
+ * fp8 = 1: the FP8 head ("KellerJordan/modded-nanogpt" README, technique
+ * list: FP8 for the head). H and the candidate rows W_c are each scaled by
+ * 2^e (e the largest integer with max|x| * 2^e <= 448), rounded to e4m3 (to
+ * nearest, ties to even) and used in that form by both logit GEMMs
+ * (tcgen05 kind::f8f6f4, twice the bf16 rate); the gradient GEMMs use the
+ * same rounded operands in bf16, G stays bf16. Results are those of the
+ * plain head on the rounded operands. Requires cap = 0 (else
+ * SS_ERR_UNSUPPORTED) and D % 128 == 0 (else SS_ERR_UNSUPPORTED); the
+ * several-targets entry points take no FP8 head (SS_ERR_UNSUPPORTED).
  */
 typedef struct ss_head {
   float cap;
   float tau;
+  int fp8;  /* 1: the FP8 head (see below); 0: bf16 operands */
 } ss_head;
 
 ss_status ss_forward_head(const uint16_t* H, const uint16_t* W, const int32_t* cand,
@@ -203,6 +216,17 @@ ss_status ss_step_head(const int32_t* targets, const uint16_t* H, const uint16_t
  * ss_step with the same head; K = 1, w = {1} gives their results exactly.
  * Bad K or weights -> SS_ERR_INVALID.
  */
+/*
+ * The FP8 head's rounding of one tensor (see ss_head): x [n] bf16 (device,
+ * n % 8 == 0) is scaled by 2^e, e the largest integer with max|x| 2^e <= 448,
+ * rounded to e4m3 (to nearest, ties to even) into q [n] (device, 8-byte
+ * aligned, e4m3 codes), and scaled back into xq [n] bf16 (exact; xq may alias
+ * x). Uses 8 bytes of the workspace header of its own (any ss_workspace_size;
+ * the workspace's status word is neither read nor written). Stream-ordered.
+ */
+ss_status ss_quantize_e4m3(const uint16_t* x, int64_t n, uint8_t* q, uint16_t* xq,
+                           void* workspace, size_t workspace_bytes, ss_stream stream);
+
 #define SS_MAX_TARGETS 8
 ss_status ss_forward_mtp(const uint16_t* H, const uint16_t* W, const int32_t* cand,
                          const int32_t* slot, int64_t K, const float* weights, int64_t T,

@@ -40,12 +40,15 @@ NOALLOC_SCRATCH_BYTES = 32 << 20
 
 
 class Head(ctypes.Structure):
-    """ss_head: cap > 0 -> logits z = cap / (1 + exp(-s / tau)); cap = 0 -> plain."""
-    _fields_ = [("cap", ctypes.c_float), ("tau", ctypes.c_float)]
+    """ss_head: cap > 0 -> logits z = cap / (1 + exp(-s / tau)); cap = 0 -> plain;
+    fp8 = 1 -> the FP8 head."""
+    _fields_ = [("cap", ctypes.c_float), ("tau", ctypes.c_float), ("fp8", ctypes.c_int)]
 
 
-def _head(cap: float, tau: float):
-    return None if cap == 0 else ctypes.byref(Head(float(cap), float(tau)))
+def _head(cap: float, tau: float, fp8: bool = False):
+    if cap == 0 and not fp8:
+        return None
+    return ctypes.byref(Head(float(cap), float(tau), 1 if fp8 else 0))
 
 
 class SSError(RuntimeError):
@@ -109,6 +112,8 @@ def _load():
     L.ss_step_mtp.restype = ctypes.c_int
     L.ss_step_mtp.argtypes = [p, i64, fp, p, p, i64, i64, i64, i64, ctypes.c_uint64, hp,
                               ctypes.c_float, ctypes.c_int, p, p, p, p, p, p, p, sz, p]
+    L.ss_quantize_e4m3.restype = ctypes.c_int
+    L.ss_quantize_e4m3.argtypes = [p, i64, p, p, p, sz, p]
     L.ss_schedule_candidates.restype = i64
     L.ss_schedule_candidates.argtypes = [i64, i64, i64]
     L.ss_clear_rows.restype = ctypes.c_int
@@ -181,10 +186,16 @@ def workspace_size(T: int, V: int, C: int, D: int) -> int:
     return int(n)
 
 
+WORKSPACE_HEADER_BYTES = 1024
+
+
 def workspace(T: int, V: int, C: int, D: int, device=None) -> torch.Tensor:
-    """A device byte buffer large enough for one batch of size (T, V, C, D)."""
-    return torch.empty(workspace_size(T, V, C, D), dtype=torch.uint8,
-                       device=device if device is not None else "cuda")
+    """A device byte buffer large enough for one batch of size (T, V, C, D),
+    its header (status word) zeroed as include/ss.h requires of a new one."""
+    ws = torch.empty(workspace_size(T, V, C, D), dtype=torch.uint8,
+                     device=device if device is not None else "cuda")
+    ws[:WORKSPACE_HEADER_BYTES].zero_()
+    return ws
 
 
 def build_candidates(targets: torch.Tensor, V: int, C: int, seed: int, ws: torch.Tensor,
@@ -212,7 +223,7 @@ def build_candidates(targets: torch.Tensor, V: int, C: int, seed: int, ws: torch
 
 def forward(H: torch.Tensor, W: torch.Tensor, cand: torch.Tensor, slot: torch.Tensor,
             ws: torch.Tensor, loss: torch.Tensor | None = None, lse: torch.Tensor | None = None,
-            cap: float = 0.0, tau: float = 1.0):
+            cap: float = 0.0, tau: float = 1.0, fp8: bool = False):
     """Per-token loss [T] and log-sum-exp [T] (fp32) over the candidate rows
     (cap > 0: of the capped logits, ss_forward_head)."""
     _need(H, "H", torch.bfloat16)
@@ -231,12 +242,12 @@ def forward(H: torch.Tensor, W: torch.Tensor, cand: torch.Tensor, slot: torch.Te
         lse = torch.empty(T, dtype=torch.float32, device=dev)
     _need(loss, "loss", torch.float32, dev, (T,))
     _need(lse, "lse", torch.float32, dev, (T,))
-    if cap == 0:
+    if cap == 0 and not fp8:
         code = _lib.ss_forward(_ptr(H), _ptr(W), _ptr(cand), _ptr(slot), T, V, C, D, _ptr(loss),
                                _ptr(lse), _ptr(ws), ws.numel(), _stream(dev))
     else:
         code = _lib.ss_forward_head(_ptr(H), _ptr(W), _ptr(cand), _ptr(slot), T, V, C, D,
-                                    _head(cap, tau), _ptr(loss), _ptr(lse), _ptr(ws), ws.numel(),
+                                    _head(cap, tau, fp8), _ptr(loss), _ptr(lse), _ptr(ws), ws.numel(),
                                     _stream(dev))
     _check(code, "ss_forward")
     return loss, lse
@@ -271,7 +282,7 @@ def forward_noalloc(H: torch.Tensor, W: torch.Tensor, cand: torch.Tensor, slot: 
 def backward(H: torch.Tensor, W: torch.Tensor, cand: torch.Tensor, slot: torch.Tensor,
              lse: torch.Tensor, ws: torch.Tensor, scale: float = 1.0, accumulate: bool = False,
              dH: torch.Tensor | None = None, dW: torch.Tensor | None = None, cap: float = 0.0,
-             tau: float = 1.0):
+             tau: float = 1.0, fp8: bool = False):
     """dH [T, D] bf16 and dW [V, D] fp32 (only candidate rows written / added to).
     A new dW is zero-filled, so that it is the dense gradient."""
     _need(H, "H", torch.bfloat16)
@@ -291,13 +302,14 @@ def backward(H: torch.Tensor, W: torch.Tensor, cand: torch.Tensor, slot: torch.T
         dW = torch.zeros(V, D, dtype=torch.float32, device=dev)
     _need(dH, "dH", torch.bfloat16, dev, (T, D))
     _need(dW, "dW", torch.float32, dev, (V, D))
-    if cap == 0:
+    if cap == 0 and not fp8:
         code = _lib.ss_backward(_ptr(H), _ptr(W), _ptr(cand), _ptr(slot), _ptr(lse), T, V, C, D,
                                 float(scale), 1 if accumulate else 0, _ptr(dH), _ptr(dW),
                                 _ptr(ws), ws.numel(), _stream(dev))
     else:
         code = _lib.ss_backward_head(_ptr(H), _ptr(W), _ptr(cand), _ptr(slot), _ptr(lse), T, V,
-                                     C, D, _head(cap, tau), float(scale), 1 if accumulate else 0,
+                                     C, D, _head(cap, tau, fp8), float(scale),
+                                     1 if accumulate else 0,
                                      _ptr(dH), _ptr(dW), _ptr(ws), ws.numel(), _stream(dev))
     _check(code, "ss_backward")
     return dH, dW
@@ -352,7 +364,8 @@ class KernelTrace:
 
 
 def step(H, W, targets, C: int, seed: int, ws, scale: float = 1.0, dW=None, accumulate=False,
-         cand=None, slot=None, loss=None, lse=None, dH=None, cap: float = 0.0, tau: float = 1.0):
+         cand=None, slot=None, loss=None, lse=None, dH=None, cap: float = 0.0, tau: float = 1.0,
+         fp8: bool = False):
     """One full pass of the path in one call (ss_step): candidates, forward,
     backward, with one gather of the candidate rows shared by both passes."""
     _need(H, "H", torch.bfloat16)
@@ -372,14 +385,14 @@ def step(H, W, targets, C: int, seed: int, ws, scale: float = 1.0, dW=None, accu
                                (loss, "loss", torch.float32, (T,)), (lse, "lse", torch.float32, (T,)),
                                (dH, "dH", torch.bfloat16, (T, D)), (dW, "dW", torch.float32, (V, D))):
         _need(t, name, dt, dev, shape)
-    if cap == 0:
+    if cap == 0 and not fp8:
         code = _lib.ss_step(_ptr(targets), _ptr(H), _ptr(W), T, V, C, D, seed & (2**64 - 1),
                             float(scale), 1 if accumulate else 0, _ptr(cand), _ptr(slot),
                             _ptr(loss), _ptr(lse), _ptr(dH), _ptr(dW), _ptr(ws), ws.numel(),
                             _stream(dev))
     else:
         code = _lib.ss_step_head(_ptr(targets), _ptr(H), _ptr(W), T, V, C, D, seed & (2**64 - 1),
-                                 _head(cap, tau), float(scale), 1 if accumulate else 0,
+                                 _head(cap, tau, fp8), float(scale), 1 if accumulate else 0,
                                  _ptr(cand), _ptr(slot), _ptr(loss), _ptr(lse), _ptr(dH),
                                  _ptr(dW), _ptr(ws), ws.numel(), _stream(dev))
     _check(code, "ss_step")
@@ -387,13 +400,13 @@ def step(H, W, targets, C: int, seed: int, ws, scale: float = 1.0, dW=None, accu
 
 
 def step_separate(H, W, targets, C: int, seed: int, ws, scale: float = 1.0, dW=None,
-                  accumulate=False, cap: float = 0.0, tau: float = 1.0):
+                  accumulate=False, cap: float = 0.0, tau: float = 1.0, fp8: bool = False):
     """The same pass as three calls: ss_build_candidates, ss_forward, ss_backward."""
     V = W.shape[0]
     cand, slot = build_candidates(targets, V, C, seed, ws)
-    loss, lse = forward(H, W, cand, slot, ws, cap=cap, tau=tau)
+    loss, lse = forward(H, W, cand, slot, ws, cap=cap, tau=tau, fp8=fp8)
     dH, dW = backward(H, W, cand, slot, lse, ws, scale=scale, accumulate=accumulate, dW=dW,
-                      cap=cap, tau=tau)
+                      cap=cap, tau=tau, fp8=fp8)
     return {"cand": cand, "slot": slot, "loss": loss, "lse": lse, "dH": dH, "dW": dW}
 
 
@@ -427,7 +440,7 @@ class StepGraph:
 
     def __init__(self, H, W, targets, C: int, ws, scale: float = 1.0, accumulate=False,
                  cand=None, slot=None, loss=None, lse=None, dH=None, dW=None, cap: float = 0.0,
-                 tau: float = 1.0):
+                 tau: float = 1.0, fp8: bool = False):
         _need(H, "H", torch.bfloat16)
         dev = H.device
         T, D = H.shape
@@ -452,8 +465,8 @@ class StepGraph:
         self.device = dev
         h = ctypes.c_void_p()
         code = _lib.ss_step_graph_create(_ptr(targets), _ptr(H), _ptr(W), T, V, C, D,
-                                         _head(cap, tau), float(scale), 1 if accumulate else 0,
-                                         _ptr(self.cand),
+                                         _head(cap, tau, fp8), float(scale),
+                                         1 if accumulate else 0, _ptr(self.cand),
                                          _ptr(self.slot), _ptr(self.loss), _ptr(self.lse),
                                          _ptr(self.dH), _ptr(self.dW), _ptr(ws), ws.numel(),
                                          ctypes.byref(h))
@@ -558,3 +571,15 @@ def backward_mtp(H, W, cand, slot, weights, lse, ws, scale: float = 1.0, accumul
                                 _ptr(dH), _ptr(dW), _ptr(ws), ws.numel(), _stream(dev))
     _check(code, "ss_backward_mtp")
     return dH, dW
+
+
+def quantize_e4m3(x: torch.Tensor, ws: torch.Tensor):
+    """ss_quantize_e4m3: the FP8 head's rounding of one bf16 tensor; returns
+    (e4m3 codes as uint8, the rounded values as bf16)."""
+    _need(x, "x", torch.bfloat16)
+    dev = x.device
+    q = torch.empty(x.shape, dtype=torch.uint8, device=dev)
+    xq = torch.empty_like(x)
+    _check(_lib.ss_quantize_e4m3(_ptr(x), x.numel(), _ptr(q), _ptr(xq), _ptr(ws), ws.numel(),
+                                 _stream(dev)), "ss_quantize_e4m3")
+    return q, xq

@@ -5,6 +5,7 @@
 // the zeroing of candidate rows for an empty batch.
 #include <cuda.h>
 #include <cudaTypedefs.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 #include <stdio.h>
@@ -24,11 +25,13 @@ namespace {
 // ------------------------------------------------------------ workspace
 
 struct Layout {
-  size_t hdr, wc, part, tgt, g, total;
+  size_t hdr, wc, part, tgt, g, h8, hq, w8, total;
   int64_t ldG, n_ct;
 };
 
-constexpr size_t kHdrBytes = 1024;  // int32 status, int32 U, padding
+constexpr size_t kHdrBytes = 1024;  // int32 status, int32 U, padding, FP8 amax words
+constexpr size_t kHdrAmax = 64;     // byte offset of float amax[2] (max |H|, max |W_c|)
+constexpr size_t kHdrQuant = 80;    // ss_quantize_e4m3's own float amax + int32 status
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -47,6 +50,13 @@ Layout make_layout(int64_t T, int64_t C, int64_t D) {
   off = align_up(off + static_cast<size_t>(T) * kMaxTargets * sizeof(float), 1024);
   L.g = off;
   off = align_up(off + static_cast<size_t>(T) * L.ldG * 2, 1024);
+  // the FP8 head's operands: H and W_c in e4m3, H rounded to the e4m3 grid in bf16
+  L.h8 = off;
+  off = align_up(off + static_cast<size_t>(T) * D, 1024);
+  L.hq = off;
+  off = align_up(off + static_cast<size_t>(T) * D * 2, 1024);
+  L.w8 = off;
+  off = align_up(off + static_cast<size_t>(C) * D, 1024);
   L.total = off;
   return L;
 }
@@ -94,14 +104,15 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 // Row-major bf16 matrix [outer, inner] with `row_bytes` between rows, read in
 // boxes of box_outer rows x box_inner elements with the 128-byte swizzle.
 bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
-              uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer) {
+              uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
+              CUtensorMapDataType dtype = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {inner, outer};
   cuuint64_t strides[1] = {row_bytes};
   cuuint32_t box[2] = {box_inner, box_outer};
   cuuint32_t es[2] = {1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+  return fn(m, dtype, 2, const_cast<void*>(base), dims, strides, box,
             es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -112,12 +123,13 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
 __global__ void __launch_bounds__(256) k_gather_rows(const uint16_t* __restrict__ W,
                                                      const int32_t* __restrict__ cand, int C,
                                                      int V, int D, uint16_t* __restrict__ Wc,
-                                                     int* status) {
+                                                     float* amax, int* status) {
   pdl_enter();
   if (read_status(status) != 0) return;
   const int lane = threadIdx.x & 31;
   const int n16 = D / 8;
   const int warps = gridDim.x * (blockDim.x / 32);
+  uint32_t mx = 0u;  // amax != nullptr: max |x| over the copied rows, as bf16 magnitude bits
   for (int j = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32; j < C; j += warps) {
     const int v = __ldg(cand + j);
     uint4* dst = reinterpret_cast<uint4*>(Wc + static_cast<size_t>(j) * D);
@@ -127,7 +139,72 @@ __global__ void __launch_bounds__(256) k_gather_rows(const uint16_t* __restrict_
       continue;
     }
     const uint4* src = reinterpret_cast<const uint4*>(W + static_cast<size_t>(v) * D);
-    for (int i = lane; i < n16; i += 32) dst[i] = __ldg(src + i);
+    for (int i = lane; i < n16; i += 32) {
+      const uint4 x = __ldg(src + i);
+      dst[i] = x;
+      if (amax) mx = max(mx, bf16x8_absmax_bits(x));
+    }
+  }
+  if (amax) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    if (lane == 0 && mx) atomicMax(reinterpret_cast<unsigned*>(amax), mx << 16);
+  }
+}
+
+// amax[0] = max over x of |x| (n bf16 values, n % 8 == 0), as an atomic max of
+// the non-negative float's bits
+__global__ void __launch_bounds__(256) k_amax_bf16(const uint16_t* __restrict__ x, int64_t n8,
+                                                   float* amax, int* status) {
+  pdl_enter();
+  if (read_status(status) != 0) return;
+  uint32_t mx = 0u;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n8; i += stride)
+    mx = max(mx, bf16x8_absmax_bits(__ldg(reinterpret_cast<const uint4*>(x) + i)));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  if ((threadIdx.x & 31) == 0 && mx) atomicMax(reinterpret_cast<unsigned*>(amax), mx << 16);
+}
+
+// The FP8 head's operands, two tensors in one launch (job 0: H, job 1: W_c):
+// q = e4m3(x * 2^e) and xq = bf16(e4m3 value * 2^-e) (exact), e from the
+// tensor's amax; xq may alias x.
+struct QuantJob {
+  const uint16_t* x;
+  uint8_t* q;
+  uint16_t* xq;
+  const float* amax;
+  int64_t n8;  // groups of 8 values
+};
+__global__ void __launch_bounds__(256) k_quantize_e4m3(QuantJob a, QuantJob b, int* status) {
+  pdl_enter();
+  if (read_status(status) != 0) return;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int job = 0; job < 2; ++job) {
+    const QuantJob& J = job == 0 ? a : b;
+    const int e = e4m3_exponent(__ldcg(J.amax));
+    const float up = exp2i(e), down = exp2i(-e);
+    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < J.n8;
+         i += stride) {
+      const uint4 v = __ldg(reinterpret_cast<const uint4*>(J.x) + i);
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+      uint32_t qw[2], out[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float lo = __uint_as_float(w[k] << 16) * up;
+        const float hi = __uint_as_float(w[k] & 0xffff0000u) * up;
+        const uint16_t c = e4m3x2(lo, hi);
+        const uint32_t h2 = e4m3x2_to_f16x2(c);
+        const float dlo = __half2float(__ushort_as_half(static_cast<uint16_t>(h2 & 0xffffu))) * down;
+        const float dhi = __half2float(__ushort_as_half(static_cast<uint16_t>(h2 >> 16))) * down;
+        out[k] = (__float_as_uint(dlo) >> 16) | (__float_as_uint(dhi) & 0xffff0000u);
+        if (k & 1) qw[k >> 1] |= static_cast<uint32_t>(c) << 16;
+        else qw[k >> 1] = c;
+      }
+      reinterpret_cast<uint2*>(J.q)[i] = make_uint2(qw[0], qw[1]);
+      reinterpret_cast<uint4*>(J.xq)[i] = make_uint4(out[0], out[1], out[2], out[3]);
+    }
   }
 }
 
@@ -307,38 +384,73 @@ cudaError_t noalloc_scratch_address(void** out) {
 // ------------------------------------------------------- launch sequences
 
 ss_status enqueue_gather(const uint16_t* W, const int32_t* cand, int64_t C, int64_t V, int64_t D,
-                         uint16_t* Wc, int* status, int nsm, cudaStream_t s) {
+                         uint16_t* Wc, int* status, int nsm, cudaStream_t s,
+                         float* amax = nullptr) {
   trace_pre(s, "gather_rows");
   const cudaError_t e = launch_pdl(k_gather_rows, dim3(rows_grid(C, nsm)), dim3(256), 0, s, W, cand,
                                    static_cast<int>(C), static_cast<int>(V), static_cast<int>(D),
-                                   Wc, status);
+                                   Wc, amax, status);
   trace_post(s);
   return e == cudaSuccess ? SS_OK : fail("launch k_gather_rows", e);
 }
 
+// W_c = W[cand] and, for the FP8 head, the e4m3 operands: amax of W_c (in
+// the gather) and of H, then H -> (h8, hq) and W_c -> (w8, W_c rounded in place)
+ss_status enqueue_gather_operands(const uint16_t* W, const int32_t* cand, const uint16_t* H,
+                                  int64_t T, int64_t C, int64_t V, int64_t D, bool fp8,
+                                  const Layout& L, char* ws, int nsm, cudaStream_t s) {
+  int* status = reinterpret_cast<int*>(ws + L.hdr);
+  uint16_t* Wc = reinterpret_cast<uint16_t*>(ws + L.wc);
+  if (!fp8) return enqueue_gather(W, cand, C, V, D, Wc, status, nsm, s);
+  float* amax = reinterpret_cast<float*>(ws + L.hdr + kHdrAmax);
+  cudaError_t e = cudaMemsetAsync(amax, 0, 2 * sizeof(float), s);
+  if (e != cudaSuccess) return fail("cudaMemsetAsync(amax)", e);
+  ss_status r = enqueue_gather(W, cand, C, V, D, Wc, status, nsm, s, amax + 1);
+  if (r != SS_OK) return r;
+  trace_pre(s, "amax_H");
+  e = launch_pdl(k_amax_bf16, dim3(nsm * 2), dim3(256), 0, s, H, T * D / 8, amax, status);
+  trace_post(s);
+  if (e != cudaSuccess) return fail("launch k_amax_bf16", e);
+  const QuantJob jh{H, reinterpret_cast<uint8_t*>(ws + L.h8), reinterpret_cast<uint16_t*>(ws + L.hq),
+                    amax, T * D / 8};
+  const QuantJob jw{Wc, reinterpret_cast<uint8_t*>(ws + L.w8), Wc, amax + 1, C * D / 8};
+  trace_pre(s, "quantize_e4m3");
+  e = launch_pdl(k_quantize_e4m3, dim3(nsm * 4), dim3(256), 0, s, jh, jw, status);
+  trace_post(s);
+  return e == cudaSuccess ? SS_OK : fail("launch k_quantize_e4m3", e);
+}
+
 // forward GEMM (LSE partials, target logit) and the LSE merge, from W_c
 ss_status enqueue_forward(const uint16_t* H, const int32_t* slot, int64_t T, int64_t C, int64_t D,
-                          float cap, float tau, const Targets& tg, float* loss, float* lse,
-                          const Layout& L, char* ws, int nsm, cudaStream_t s) {
+                          float cap, float tau, const Targets& tg, bool fp8, float* loss,
+                          float* lse, const Layout& L, char* ws, int nsm, cudaStream_t s) {
   int* status = reinterpret_cast<int*>(ws + L.hdr);
   uint16_t* Wc = reinterpret_cast<uint16_t*>(ws + L.wc);
   float2* part = reinterpret_cast<float2*>(ws + L.part);
   float* tgt = reinterpret_cast<float*>(ws + L.tgt);
   CUtensorMap tH, tWc;
-  if (!make_map(&tH, H, D, T, D * 2, 64, 128) || !make_map(&tWc, Wc, D, C, D * 2, 64, kBnLogits))
+  const float* amax = nullptr;
+  if (fp8) {  // e4m3 copies: 128 elements = 128 bytes per row of a k-block
+    amax = reinterpret_cast<const float*>(ws + L.hdr + kHdrAmax);
+    if (!make_map(&tH, ws + L.h8, D, T, D, 128, 128, CU_TENSOR_MAP_DATA_TYPE_UINT8) ||
+        !make_map(&tWc, ws + L.w8, D, C, D, 128, kBnLogits, CU_TENSOR_MAP_DATA_TYPE_UINT8))
+      return fail("cuTensorMapEncodeTiled", cudaErrorInvalidValue);
+  } else if (!make_map(&tH, H, D, T, D * 2, 64, 128) ||
+             !make_map(&tWc, Wc, D, C, D * 2, 64, kBnLogits)) {
     return fail("cuTensorMapEncodeTiled", cudaErrorInvalidValue);
+  }
   trace_pre(s, "gemm_forward_lse");
   const cudaError_t e = launch_forward_logits(tH, tWc, static_cast<int>(T), static_cast<int>(C),
                                               static_cast<int>(D), slot, part, tgt, cap, tau,
-                                              tg, status, nsm, s);
+                                              tg, amax, status, nsm, s);
   trace_post(s);
   if (e != cudaSuccess) return fail("launch gemm_forward_lse", e);
   const int blocks = static_cast<int>((T * kMergeLanes + 255) / 256);
   trace_pre(s, "lse_merge");
   const cudaError_t em =
       launch_pdl(k_lse_merge, dim3(blocks), dim3(256), 0, s, part, tgt, slot, static_cast<int>(T),
-                 static_cast<int>(C), static_cast<int>(L.n_ct * fwd_groups(cap)), tg, loss, lse,
-                 status);
+                 static_cast<int>(C), static_cast<int>(L.n_ct * fwd_groups(cap, fp8)), tg, loss,
+                 lse, status);
   trace_post(s);
   return cuda_status(em, "launch k_lse_merge");
 }
@@ -346,7 +458,7 @@ ss_status enqueue_forward(const uint16_t* H, const int32_t* slot, int64_t T, int
 // softmax-gradient GEMM and the two gradient GEMMs, from W_c
 ss_status enqueue_backward(const uint16_t* H, const int32_t* cand, const int32_t* slot,
                            const float* lse, int64_t T, int64_t V, int64_t C, int64_t D,
-                           float cap, float tau, const Targets& tg, float scale,
+                           float cap, float tau, const Targets& tg, bool fp8, float scale,
                            int accumulate, uint16_t* dH, float* dW, const Layout& L, char* ws,
                            int nsm, cudaStream_t s) {
   int* status = reinterpret_cast<int*>(ws + L.hdr);
@@ -356,14 +468,22 @@ ss_status enqueue_backward(const uint16_t* H, const int32_t* cand, const int32_t
             iD = static_cast<int>(D);
   CUtensorMap tH, tWc, tWc2, tGk, tWcMn, tGmn, tHmn;
   const uint64_t gRow = static_cast<uint64_t>(L.ldG) * 2;
-  if (!make_map(&tH, H, D, T, D * 2, 64, 128) || !make_map(&tWc, Wc, D, C, D * 2, 64, kBnLogits) ||
-      !make_map(&tWc2, Wc, D, C, D * 2, 64, kBnLogits / 2) ||
-      !make_map(&tGk, G, C, T, gRow, 64, 128) || !make_map(&tWcMn, Wc, D, C, D * 2, 64, 64) ||
-      !make_map(&tGmn, G, C, T, gRow, 64, 64) || !make_map(&tHmn, H, D, T, D * 2, 64, 64))
-    return fail("cuTensorMapEncodeTiled", cudaErrorInvalidValue);
+  // the FP8 head: the logit recompute reads the e4m3 copies, the gradient
+  // GEMMs the same rounded operands in bf16 (H rounded in hq, W_c in place)
+  const uint16_t* Hg = fp8 ? reinterpret_cast<const uint16_t*>(ws + L.hq) : H;
+  const float* amax = fp8 ? reinterpret_cast<const float*>(ws + L.hdr + kHdrAmax) : nullptr;
+  bool ok = fp8 ? make_map(&tH, ws + L.h8, D, T, D, 128, 128, CU_TENSOR_MAP_DATA_TYPE_UINT8) &&
+                      make_map(&tWc, ws + L.w8, D, C, D, 128, kBnLogits,
+                               CU_TENSOR_MAP_DATA_TYPE_UINT8)
+                : make_map(&tH, H, D, T, D * 2, 64, 128) &&
+                      make_map(&tWc, Wc, D, C, D * 2, 64, kBnLogits);
+  ok = ok && make_map(&tWc2, Wc, D, C, D * 2, 64, kBnLogits / 2) &&
+       make_map(&tGk, G, C, T, gRow, 64, 128) && make_map(&tWcMn, Wc, D, C, D * 2, 64, 64) &&
+       make_map(&tGmn, G, C, T, gRow, 64, 64) && make_map(&tHmn, Hg, D, T, D * 2, 64, 64);
+  if (!ok) return fail("cuTensorMapEncodeTiled", cudaErrorInvalidValue);
   trace_pre(s, "gemm_softmax_grad");
   cudaError_t e =
-      launch_softmax_grad(tH, tWc, tWc2, tGk, iT, iC, iD, slot, lse, scale, cap, tau, tg,
+      launch_softmax_grad(tH, tWc, tWc2, tGk, iT, iC, iD, slot, lse, scale, cap, tau, tg, amax,
                           status, nsm, s);
   trace_post(s);
   if (e != cudaSuccess) return fail("launch gemm_softmax_grad", e);
@@ -495,8 +615,9 @@ ss_status ss_build_candidates(const int32_t* targets, int64_t T, int64_t V, int6
 
 static ss_status forward_impl(const uint16_t* H, const uint16_t* W, const int32_t* cand,
                               const int32_t* slot, int64_t T, int64_t V, int64_t C, int64_t D,
-                              float cap, float tau, const Targets& tg, float* loss, float* lse,
-                              void* workspace, size_t workspace_bytes, ss_stream stream) {
+                              float cap, float tau, const Targets& tg, bool fp8, float* loss,
+                              float* lse, void* workspace, size_t workspace_bytes,
+                              ss_stream stream) {
   const ss_status st = check_sizes(T, V, C, D);
   if (st != SS_OK) return st;
   if (!W || !cand || !workspace || (T > 0 && (!H || !slot || !loss || !lse)))
@@ -511,16 +632,15 @@ static ss_status forward_impl(const uint16_t* H, const uint16_t* W, const int32_
   if (nsm <= 0) return fail("cudaGetDevice/cudaDeviceGetAttribute", cudaGetLastError());
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   char* ws = static_cast<char*>(workspace);
-  const ss_status sg = enqueue_gather(W, cand, C, V, D, reinterpret_cast<uint16_t*>(ws + L.wc),
-                                      reinterpret_cast<int*>(ws + L.hdr), nsm, s);
+  const ss_status sg = enqueue_gather_operands(W, cand, H, T, C, V, D, fp8, L, ws, nsm, s);
   if (sg != SS_OK) return sg;
-  return enqueue_forward(H, slot, T, C, D, cap, tau, tg, loss, lse, L, ws, nsm, s);
+  return enqueue_forward(H, slot, T, C, D, cap, tau, tg, fp8, loss, lse, L, ws, nsm, s);
 }
 
 static ss_status backward_impl(const uint16_t* H, const uint16_t* W, const int32_t* cand,
                                const int32_t* slot, const float* lse, int64_t T, int64_t V,
                                int64_t C, int64_t D, float cap, float tau, const Targets& tg,
-                               float scale, int accumulate, uint16_t* dH, float* dW,
+                               bool fp8, float scale, int accumulate, uint16_t* dH, float* dW,
                                void* workspace, size_t workspace_bytes, ss_stream stream) {
   const ss_status st = check_sizes(T, V, C, D);
   if (st != SS_OK) return st;
@@ -538,16 +658,15 @@ static ss_status backward_impl(const uint16_t* H, const uint16_t* W, const int32
   char* ws = static_cast<char*>(workspace);
   int* status = reinterpret_cast<int*>(ws + L.hdr);
   if (T == 0) return accumulate ? SS_OK : enqueue_zero_rows(cand, C, V, D, dW, status, nsm, s);
-  const ss_status sg =
-      enqueue_gather(W, cand, C, V, D, reinterpret_cast<uint16_t*>(ws + L.wc), status, nsm, s);
+  const ss_status sg = enqueue_gather_operands(W, cand, H, T, C, V, D, fp8, L, ws, nsm, s);
   if (sg != SS_OK) return sg;
-  return enqueue_backward(H, cand, slot, lse, T, V, C, D, cap, tau, tg, scale, accumulate, dH, dW,
-                          L, ws, nsm, s);
+  return enqueue_backward(H, cand, slot, lse, T, V, C, D, cap, tau, tg, fp8, scale, accumulate, dH,
+                          dW, L, ws, nsm, s);
 }
 
 static ss_status step_impl(const int32_t* targets, const uint16_t* H, const uint16_t* W,
                            int64_t T, int64_t V, int64_t C, int64_t D, uint64_t seed, float cap,
-                           float tau, const Targets& tg, float scale, int accumulate,
+                           float tau, const Targets& tg, bool fp8, float scale, int accumulate,
                            int32_t* cand, int32_t* slot, float* loss, float* lse, uint16_t* dH,
                            float* dW, void* workspace, size_t workspace_bytes, ss_stream stream) {
   const ss_status st = step_args_status(targets, H, W, T, V, C, D, accumulate, cand, slot, loss,
@@ -566,12 +685,12 @@ static ss_status step_impl(const int32_t* targets, const uint16_t* H, const uint
   int* status = reinterpret_cast<int*>(ws + L.hdr);
   if (T == 0) return accumulate ? SS_OK : enqueue_zero_rows(cand, C, V, D, dW, status, nsm, s);
   // one gather of W[cand] serves the forward and the backward
-  ss_status r = enqueue_gather(W, cand, C, V, D, reinterpret_cast<uint16_t*>(ws + L.wc), status, nsm, s);
+  ss_status r = enqueue_gather_operands(W, cand, H, T, C, V, D, fp8, L, ws, nsm, s);
   if (r != SS_OK) return r;
-  r = enqueue_forward(H, slot, T, C, D, cap, tau, tg, loss, lse, L, ws, nsm, s);
+  r = enqueue_forward(H, slot, T, C, D, cap, tau, tg, fp8, loss, lse, L, ws, nsm, s);
   if (r != SS_OK) return r;
-  return enqueue_backward(H, cand, slot, lse, T, V, C, D, cap, tau, tg, scale, accumulate, dH, dW,
-                          L, ws, nsm, s);
+  return enqueue_backward(H, cand, slot, lse, T, V, C, D, cap, tau, tg, fp8, scale, accumulate, dH,
+                          dW, L, ws, nsm, s);
 }
 
 // K targets per token with host weights w[0..K): 1 <= K <= kMaxTargets, each
@@ -588,10 +707,19 @@ static ss_status targets_args(int64_t K, const float* w, Targets* tg) {
   return sum > 0.f && std::isfinite(sum) ? SS_OK : SS_ERR_INVALID;
 }
 
-// the head options: NULL or cap == 0 is the plain head
-static ss_status head_args(const ss_head* head, float* cap, float* tau) {
+// the head options: NULL or cap == 0 is the plain head; fp8 (plain logits
+// only) sets *fp8
+static ss_status head_args(const ss_head* head, float* cap, float* tau, bool* fp8 = nullptr) {
   *cap = 0.f;
   *tau = 1.f;
+  if (fp8) *fp8 = false;
+  if (head && head->fp8 != 0) {
+    if (head->fp8 != 1) return SS_ERR_INVALID;
+    if (!fp8) return SS_ERR_UNSUPPORTED;  // this entry point has no FP8 path
+    if (head->cap != 0.f) return SS_ERR_UNSUPPORTED;
+    *fp8 = true;
+    return SS_OK;
+  }
   if (!head || head->cap == 0.f) return SS_OK;
   if (!(head->cap > 0.f) || !std::isfinite(head->cap) || !(head->tau > 0.f) ||
       !std::isfinite(head->tau))
@@ -605,8 +733,8 @@ ss_status ss_forward(const uint16_t* H, const uint16_t* W, const int32_t* cand,
                      const int32_t* slot, int64_t T, int64_t V, int64_t C, int64_t D,
                      float* loss, float* lse, void* workspace, size_t workspace_bytes,
                      ss_stream stream) {
-  return forward_impl(H, W, cand, slot, T, V, C, D, 0.f, 1.f, kOneTarget, loss, lse, workspace,
-                      workspace_bytes, stream);
+  return forward_impl(H, W, cand, slot, T, V, C, D, 0.f, 1.f, kOneTarget, false, loss, lse,
+                      workspace, workspace_bytes, stream);
 }
 
 ss_status ss_forward_head(const uint16_t* H, const uint16_t* W, const int32_t* cand,
@@ -614,18 +742,20 @@ ss_status ss_forward_head(const uint16_t* H, const uint16_t* W, const int32_t* c
                           const ss_head* head, float* loss, float* lse, void* workspace,
                           size_t workspace_bytes, ss_stream stream) {
   float cap, tau;
-  const ss_status h = head_args(head, &cap, &tau);
+  bool fp8;
+  const ss_status h = head_args(head, &cap, &tau, &fp8);
   if (h != SS_OK) return h;
-  return forward_impl(H, W, cand, slot, T, V, C, D, cap, tau, kOneTarget, loss, lse, workspace,
-                      workspace_bytes, stream);
+  if (fp8 && D % 128 != 0) return SS_ERR_UNSUPPORTED;
+  return forward_impl(H, W, cand, slot, T, V, C, D, cap, tau, kOneTarget, fp8, loss, lse,
+                      workspace, workspace_bytes, stream);
 }
 
 ss_status ss_backward(const uint16_t* H, const uint16_t* W, const int32_t* cand,
                       const int32_t* slot, const float* lse, int64_t T, int64_t V, int64_t C,
                       int64_t D, float scale, int accumulate, uint16_t* dH, float* dW,
                       void* workspace, size_t workspace_bytes, ss_stream stream) {
-  return backward_impl(H, W, cand, slot, lse, T, V, C, D, 0.f, 1.f, kOneTarget, scale, accumulate,
-                       dH, dW, workspace, workspace_bytes, stream);
+  return backward_impl(H, W, cand, slot, lse, T, V, C, D, 0.f, 1.f, kOneTarget, false, scale,
+                       accumulate, dH, dW, workspace, workspace_bytes, stream);
 }
 
 ss_status ss_backward_head(const uint16_t* H, const uint16_t* W, const int32_t* cand,
@@ -634,18 +764,20 @@ ss_status ss_backward_head(const uint16_t* H, const uint16_t* W, const int32_t* 
                            int accumulate, uint16_t* dH, float* dW, void* workspace,
                            size_t workspace_bytes, ss_stream stream) {
   float cap, tau;
-  const ss_status h = head_args(head, &cap, &tau);
+  bool fp8;
+  const ss_status h = head_args(head, &cap, &tau, &fp8);
   if (h != SS_OK) return h;
-  return backward_impl(H, W, cand, slot, lse, T, V, C, D, cap, tau, kOneTarget, scale, accumulate,
-                       dH, dW, workspace, workspace_bytes, stream);
+  if (fp8 && D % 128 != 0) return SS_ERR_UNSUPPORTED;
+  return backward_impl(H, W, cand, slot, lse, T, V, C, D, cap, tau, kOneTarget, fp8, scale,
+                       accumulate, dH, dW, workspace, workspace_bytes, stream);
 }
 
 ss_status ss_step(const int32_t* targets, const uint16_t* H, const uint16_t* W, int64_t T,
                   int64_t V, int64_t C, int64_t D, uint64_t seed, float scale, int accumulate,
                   int32_t* cand, int32_t* slot, float* loss, float* lse, uint16_t* dH, float* dW,
                   void* workspace, size_t workspace_bytes, ss_stream stream) {
-  return step_impl(targets, H, W, T, V, C, D, seed, 0.f, 1.f, kOneTarget, scale, accumulate, cand,
-                   slot, loss, lse, dH, dW, workspace, workspace_bytes, stream);
+  return step_impl(targets, H, W, T, V, C, D, seed, 0.f, 1.f, kOneTarget, false, scale, accumulate,
+                   cand, slot, loss, lse, dH, dW, workspace, workspace_bytes, stream);
 }
 
 ss_status ss_step_head(const int32_t* targets, const uint16_t* H, const uint16_t* W, int64_t T,
@@ -654,10 +786,12 @@ ss_status ss_step_head(const int32_t* targets, const uint16_t* H, const uint16_t
                        float* lse, uint16_t* dH, float* dW, void* workspace,
                        size_t workspace_bytes, ss_stream stream) {
   float cap, tau;
-  const ss_status h = head_args(head, &cap, &tau);
+  bool fp8;
+  const ss_status h = head_args(head, &cap, &tau, &fp8);
   if (h != SS_OK) return h;
-  return step_impl(targets, H, W, T, V, C, D, seed, cap, tau, kOneTarget, scale, accumulate, cand,
-                   slot, loss, lse, dH, dW, workspace, workspace_bytes, stream);
+  if (fp8 && D % 128 != 0) return SS_ERR_UNSUPPORTED;
+  return step_impl(targets, H, W, T, V, C, D, seed, cap, tau, kOneTarget, fp8, scale, accumulate,
+                   cand, slot, loss, lse, dH, dW, workspace, workspace_bytes, stream);
 }
 
 ss_status ss_forward_mtp(const uint16_t* H, const uint16_t* W, const int32_t* cand,
@@ -669,7 +803,7 @@ ss_status ss_forward_mtp(const uint16_t* H, const uint16_t* W, const int32_t* ca
   ss_status a = head_args(head, &cap, &tau);
   if (a == SS_OK) a = targets_args(K, weights, &tg);
   if (a != SS_OK) return a;
-  return forward_impl(H, W, cand, slot, T, V, C, D, cap, tau, tg, loss, lse, workspace,
+  return forward_impl(H, W, cand, slot, T, V, C, D, cap, tau, tg, false, loss, lse, workspace,
                       workspace_bytes, stream);
 }
 
@@ -683,8 +817,8 @@ ss_status ss_backward_mtp(const uint16_t* H, const uint16_t* W, const int32_t* c
   ss_status a = head_args(head, &cap, &tau);
   if (a == SS_OK) a = targets_args(K, weights, &tg);
   if (a != SS_OK) return a;
-  return backward_impl(H, W, cand, slot, lse, T, V, C, D, cap, tau, tg, scale, accumulate, dH, dW,
-                       workspace, workspace_bytes, stream);
+  return backward_impl(H, W, cand, slot, lse, T, V, C, D, cap, tau, tg, false, scale, accumulate,
+                       dH, dW, workspace, workspace_bytes, stream);
 }
 
 ss_status ss_step_mtp(const int32_t* targets, int64_t K, const float* weights, const uint16_t* H,
@@ -697,8 +831,8 @@ ss_status ss_step_mtp(const int32_t* targets, int64_t K, const float* weights, c
   ss_status a = head_args(head, &cap, &tau);
   if (a == SS_OK) a = targets_args(K, weights, &tg);
   if (a != SS_OK) return a;
-  return step_impl(targets, H, W, T, V, C, D, seed, cap, tau, tg, scale, accumulate, cand, slot,
-                   loss, lse, dH, dW, workspace, workspace_bytes, stream);
+  return step_impl(targets, H, W, T, V, C, D, seed, cap, tau, tg, false, scale, accumulate, cand,
+                   slot, loss, lse, dH, dW, workspace, workspace_bytes, stream);
 }
 
 int64_t ss_schedule_candidates(int64_t step, int64_t total_steps, int64_t V) {
@@ -710,6 +844,32 @@ int64_t ss_schedule_candidates(int64_t step, int64_t total_steps, int64_t V) {
   static const int64_t kPhaseC[3] = {10240, 14336, 24576};
   const int64_t c = kPhaseC[(3 * step) / sampled];
   return c < V ? c : V;
+}
+
+ss_status ss_quantize_e4m3(const uint16_t* x, int64_t n, uint8_t* q, uint16_t* xq,
+                           void* workspace, size_t workspace_bytes, ss_stream stream) {
+  if (n < 0 || n % 8 != 0) return SS_ERR_INVALID;
+  if (n == 0) return SS_OK;
+  if (!x || !q || !xq || !workspace || !aligned(x, 16) || !aligned(q, 8) || !aligned(xq, 16) ||
+      !aligned(workspace, 16))
+    return SS_ERR_INVALID;
+  if (workspace_bytes < kHdrBytes) return SS_ERR_WORKSPACE;
+  const int nsm = num_sms_current();
+  if (nsm <= 0) return fail("cudaGetDevice/cudaDeviceGetAttribute", cudaGetLastError());
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  char* ws = static_cast<char*>(workspace);
+  // A status word of its own, cleared with amax: the call neither depends on
+  // nor disturbs the status of the steps that share the workspace.
+  float* amax = reinterpret_cast<float*>(ws + kHdrQuant);
+  int* status = reinterpret_cast<int*>(ws + kHdrQuant + 4);
+  cudaError_t e = cudaMemsetAsync(amax, 0, 8, s);
+  if (e == cudaSuccess)
+    e = launch_pdl(k_amax_bf16, dim3(nsm * 2), dim3(256), 0, s, x, n / 8, amax, status);
+  const QuantJob j{x, q, xq, amax, n / 8};
+  const QuantJob none{x, q, xq, amax, 0};
+  if (e == cudaSuccess)
+    e = launch_pdl(k_quantize_e4m3, dim3(nsm * 4), dim3(256), 0, s, j, none, status);
+  return e == cudaSuccess ? SS_OK : fail("ss_quantize_e4m3", e);
 }
 
 ss_status ss_clear_rows(const int32_t* rows, int64_t n, int64_t V, int64_t D, float* dW,
@@ -772,7 +932,7 @@ ss_status ss_forward_noalloc(const uint16_t* H, const uint16_t* W, const int32_t
   trace_pre(s, "gather_rows");
   cudaError_t eg = launch_pdl(k_gather_rows, dim3(rows_grid(C, nsm)), dim3(256), 0, s, W, cand,
                               static_cast<int>(C), static_cast<int>(V), static_cast<int>(D), Wc,
-                              status);
+                              static_cast<float*>(nullptr), status);
   trace_post(s);
   if (eg != cudaSuccess) return fail("launch k_gather_rows", eg);
   CUtensorMap tH, tWc;
@@ -780,8 +940,8 @@ ss_status ss_forward_noalloc(const uint16_t* H, const uint16_t* W, const int32_t
     return fail("cuTensorMapEncodeTiled", cudaErrorInvalidValue);
   trace_pre(s, "gemm_forward_lse");
   e = launch_forward_logits(tH, tWc, static_cast<int>(T), static_cast<int>(C),
-                            static_cast<int>(D), slot, part, tgt, 0.f, 1.f, kOneTarget, status,
-                            nsm, s);
+                            static_cast<int>(D), slot, part, tgt, 0.f, 1.f, kOneTarget, nullptr,
+                            status, nsm, s);
   trace_post(s);
   if (e != cudaSuccess) return fail("launch gemm_forward_lse", e);
   trace_pre(s, "lse_merge");
@@ -847,8 +1007,10 @@ ss_status ss_step_graph_create(const int32_t* targets, const uint16_t* H, const 
   if (!graph) return SS_ERR_INVALID;
   *graph = nullptr;
   float cap, tau;
-  ss_status st = head_args(head, &cap, &tau);
+  bool fp8;
+  ss_status st = head_args(head, &cap, &tau, &fp8);
   if (st != SS_OK) return st;
+  if (fp8 && D % 128 != 0) return SS_ERR_UNSUPPORTED;
   st = step_args_status(targets, H, W, T, V, C, D, accumulate, cand, slot, loss, lse, dH, dW,
                         workspace, workspace_bytes);
   if (st != SS_OK) return st;
@@ -861,7 +1023,7 @@ ss_status ss_step_graph_create(const int32_t* targets, const uint16_t* H, const 
     cudaStreamDestroy(cs);
     return fail("cudaStreamBeginCapture", e);
   }
-  const ss_status r = step_impl(targets, H, W, T, V, C, D, 0, cap, tau, kOneTarget, scale,
+  const ss_status r = step_impl(targets, H, W, T, V, C, D, 0, cap, tau, kOneTarget, fp8, scale,
                                 accumulate, cand, slot, loss, lse, dH, dW, workspace,
                                 workspace_bytes, cs);
   cudaGraph_t g = nullptr;

@@ -21,6 +21,8 @@
 // and K edges need no special casing in the main loop.
 #pragma once
 
+#include <string.h>
+
 #include <math.h>
 
 #include "ss_internal.h"
@@ -106,13 +108,19 @@ __device__ __forceinline__ float head_dz(float z, const HeadCap& h) {
   return z * (h.cap - z) * h.icap_tau;
 }
 
+// amax[0] = max |H|, amax[1] = max |W_c|: the scale that turns the e4m3
+// accumulator back into logits
+__device__ __forceinline__ float e4m3_logit_scale(const float* amax) {
+  return exp2i(-(e4m3_exponent(__ldcg(amax)) + e4m3_exponent(__ldcg(amax + 1))));
+}
+
 // Forward: per-row softmax partials of one 128 x BN logit tile.
 //   With NCG column groups per tile (NCG epilogue warps per row block), group
 //   cg covers columns [cg * BN / NCG, (cg + 1) * BN / NCG) of the tile and
 //   writes part[nt * NCG + cg][t] = (max_j S[t,j], sum_j exp(S[t,j] - max))
 //   over its valid columns, or (-inf, 0) if it has none; tgt[t] = S[t, slot[t]]
 //   comes from the group that holds slot[t].
-template <bool CAP, int KMAX = 1>
+template <bool CAP, int KMAX = 1, bool F8 = false>
 struct EpiFwdT {
   static constexpr int kStageBytes = 0;
   static constexpr bool kKeepOperands = false;
@@ -124,6 +132,7 @@ struct EpiFwdT {
     int* status;
     HeadCap head;  // used when CAP: the partials and the target logit are of z
     Targets tg;    // used when KMAX > 1
+    const float* amax;  // used when F8: logits = accumulator * e4m3_logit_scale(amax)
   };
   __device__ static void finish(const Params&, EpiState&) {}
   template <int BN, int NCG>
@@ -141,6 +150,8 @@ struct EpiFwdT {
     const int ncols = min(CPG * 32, p.C - j0);
     float m = -INFINITY, s = 0.f, tg[KMAX];
     uint32_t has_t = 0u;  // bit k: target k lies in this group's columns
+    float sig = 1.f;
+    if constexpr (F8) sig = e4m3_logit_scale(p.amax);
     if (ncols > 0) {  // uniform: depends on the tile only
       for_tmem_chunks<CPG>(taddr, cg * CPG, [&](const uint32_t(&r)[32], int i) {
         const int jc = i * 32;
@@ -148,8 +159,10 @@ struct EpiFwdT {
         if (nv <= 0) return;
         float v[32];
 #pragma unroll
-        for (int k = 0; k < 32; ++k)
-          v[k] = CAP ? head_z(__uint_as_float(r[k]), p.head) : __uint_as_float(r[k]);
+        for (int k = 0; k < 32; ++k) {
+          const float acc = F8 ? __uint_as_float(r[k]) * sig : __uint_as_float(r[k]);
+          v[k] = CAP ? head_z(acc, p.head) : acc;
+        }
         float cm = -INFINITY;
 #pragma unroll
         for (int k = 0; k < 32; ++k)
@@ -204,7 +217,7 @@ using EpiFwd = EpiFwdT<false>;
 // writes leave as full lines instead of 32 rows per warp instruction. The
 // one-hot term touches one element per row: it is recomputed in fp32 and
 // patched into the staged tile.
-template <bool CAP, int KMAX = 1>
+template <bool CAP, int KMAX = 1, bool F8 = false>
 struct EpiGT {
   // two 16 KB staging buffers: both for one column group, one each for two
   static constexpr int kStageBytes = 2 * 16384;
@@ -221,6 +234,7 @@ struct EpiGT {
     HeadCap head;      // used when CAP: G = scale * (P(z) - Y) * dz/ds
     Targets tg;        // used when KMAX > 1: G = scale (W P - sum_k w[k] Y_k), W = sum_k w[k];
                        // log2_scale is then log2(|scale| W)
+    const float* amax;  // used when F8: logits = accumulator * e4m3_logit_scale(amax)
   };
   __device__ static void finish(const Params&, EpiState& es) {
     if ((es.ep_tid & 127) == 0) bulk_wait<0>();
@@ -245,6 +259,8 @@ struct EpiGT {
         set_status(p.status, SS_ERR_INDEX);
     }
     const float asc = fabsf(p.scale);
+    float sig = 1.f;
+    if constexpr (F8) sig = e4m3_logit_scale(p.amax);
     const uint32_t sgn = p.scale < 0.f ? 0x80008000u : 0u;
     const float off2 = valid ? fmaf(__ldg(p.lse + t), kLog2e, -p.log2_scale) : 0.f;
     const int j0 = nt * BN;
@@ -275,14 +291,17 @@ struct EpiGT {
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           float g0, g1;
+          const float x0 = F8 ? __uint_as_float(r[2 * i]) * sig : __uint_as_float(r[2 * i]);
+          const float x1 =
+              F8 ? __uint_as_float(r[2 * i + 1]) * sig : __uint_as_float(r[2 * i + 1]);
           if constexpr (CAP) {
-            const float z0 = head_z(__uint_as_float(r[2 * i]), p.head);
-            const float z1 = head_z(__uint_as_float(r[2 * i + 1]), p.head);
+            const float z0 = head_z(x0, p.head);
+            const float z1 = head_z(x1, p.head);
             g0 = ex2_approx(fmaf(z0, kLog2e, -off2)) * head_dz(z0, p.head);
             g1 = ex2_approx(fmaf(z1, kLog2e, -off2)) * head_dz(z1, p.head);
           } else {
-            g0 = ex2_approx(fmaf(__uint_as_float(r[2 * i]), kLog2e, -off2));
-            g1 = ex2_approx(fmaf(__uint_as_float(r[2 * i + 1]), kLog2e, -off2));
+            g0 = ex2_approx(fmaf(x0, kLog2e, -off2));
+            g1 = ex2_approx(fmaf(x1, kLog2e, -off2));
           }
           pk[i] = pack_bf16x2(g0, g1) ^ sgn;
         }
@@ -301,6 +320,7 @@ struct EpiGT {
             float xt = 0.f;
 #pragma unroll
             for (int i = 0; i < 32; ++i) xt = (i == off) ? __uint_as_float(r[i]) : xt;
+            if constexpr (F8) xt *= sig;
             if (has) {
               // the one-hot weight of this column: every target k2 that falls on it
               float wt = 1.f;
@@ -421,7 +441,9 @@ struct EpiDw {
 
 // -------------------------------------------------------------------- kernel
 
-template <int BN, int STAGES, bool A_MN, bool B_MN, class Epi, int EPI_WARPS = 4>
+// F8: e4m3 operands (kind::f8f6f4, K-major only): the same 128-byte
+// swizzled rows then hold 128 elements, so a k-block covers 128 of K.
+template <int BN, int STAGES, bool A_MN, bool B_MN, class Epi, int EPI_WARPS = 4, bool F8 = false>
 __global__ void __launch_bounds__(64 + 32 * EPI_WARPS, 1)
     k_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
            GemmShape shp, const __grid_constant__ typename Epi::Params ep, int* status) {
@@ -429,6 +451,8 @@ __global__ void __launch_bounds__(64 + 32 * EPI_WARPS, 1)
   static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "BN");
   static_assert(STAGES >= 2 && STAGES <= 8, "STAGES");
   static_assert(EPI_WARPS == 4 || EPI_WARPS == 8, "EPI_WARPS");
+  static_assert(!F8 || (!A_MN && !B_MN), "e4m3 operands are K-major");
+  constexpr int KB = F8 ? 2 * BK : BK;  // elements of K per k-block
   constexpr int NCG = EPI_WARPS / 4;
   using L = GemmSmem<BN, STAGES, Epi::kStageBytes>;
   extern __shared__ uint8_t smem_raw[];
@@ -492,22 +516,22 @@ __global__ void __launch_bounds__(64 + 32 * EPI_WARPS, 1)
           if constexpr (Epi::kKeepOperands) {
             static_assert(!A_MN && !B_MN, "cache-hinted loads are K-major");
             const uint64_t pol = l2_evict_last();
-            tma_load_2d_hint(a_dst, &tmA, fb, kb * BK, mt * BM, pol);
-            tma_load_2d_hint(b_dst, &tmB, fb, kb * BK, nt * BN, pol);
+            tma_load_2d_hint(a_dst, &tmA, fb, kb * KB, mt * BM, pol);
+            tma_load_2d_hint(b_dst, &tmB, fb, kb * KB, nt * BN, pol);
           } else {
             if (A_MN) {
 #pragma unroll
               for (int i = 0; i < BM / 64; ++i)
                 tma_load_2d(a_dst + i * 8192, &tmA, fb, mt * BM + 64 * i, kb * BK);
             } else {
-              tma_load_2d(a_dst, &tmA, fb, kb * BK, mt * BM);
+              tma_load_2d(a_dst, &tmA, fb, kb * KB, mt * BM);
             }
             if (B_MN) {
 #pragma unroll
               for (int i = 0; i < BN / 64; ++i)
                 tma_load_2d(b_dst + i * 8192, &tmB, fb, nt * BN + 64 * i, kb * BK);
             } else {
-              tma_load_2d(b_dst, &tmB, fb, kb * BK, nt * BN);
+              tma_load_2d(b_dst, &tmB, fb, kb * KB, nt * BN);
             }
           }
           issued |= 1u << s;
@@ -526,7 +550,7 @@ __global__ void __launch_bounds__(64 + 32 * EPI_WARPS, 1)
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
     if (lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16_f32(BM, BN, A_MN, B_MN);
+      constexpr uint32_t idesc = F8 ? idesc_e4m3_f32(BM, BN) : idesc_bf16_f32(BM, BN, A_MN, B_MN);
       int s = 0, b = 0;
       uint32_t ph = 0, aph = 0;
       bool ok = true;
@@ -548,7 +572,8 @@ __global__ void __launch_bounds__(64 + 32 * EPI_WARPS, 1)
                                      : sdesc_sw128(a_addr + k * 32, 16, 1024);
             const uint64_t bd = B_MN ? sdesc_sw128(b_addr + k * 2048, 8192, 1024)
                                      : sdesc_sw128(b_addr + k * 32, 16, 1024);
-            mma_bf16(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+            if constexpr (F8) mma_e4m3(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+            else mma_bf16(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
           }
           mma_commit(&ctrl->empty[s]);
           if (++s == STAGES) {
@@ -613,11 +638,11 @@ __global__ void __launch_bounds__(64 + 32 * EPI_WARPS, 1)
 }
 
 // Host-side launcher: grid = min(units, SMs), one CTA per SM.
-template <int BN, int STAGES, bool A_MN, bool B_MN, class Epi, int EPI_WARPS = 4>
+template <int BN, int STAGES, bool A_MN, bool B_MN, class Epi, int EPI_WARPS = 4, bool F8 = false>
 cudaError_t launch_gemm(const CUtensorMap& tA, const CUtensorMap& tB, GemmShape shp,
                         const typename Epi::Params& ep, int* status, int num_sms,
                         cudaStream_t stream) {
-  auto kern = k_gemm<BN, STAGES, A_MN, B_MN, Epi, EPI_WARPS>;
+  auto kern = k_gemm<BN, STAGES, A_MN, B_MN, Epi, EPI_WARPS, F8>;
   constexpr int smem = GemmSmem<BN, STAGES, Epi::kStageBytes>::TOTAL;
   const int units = shp.m_tiles * shp.n_tiles;
   if (units <= 0) return cudaSuccess;

@@ -11,32 +11,38 @@ namespace ss {
 // epilogue is light and K = D is short.)
 cudaError_t launch_forward_logits(const CUtensorMap& tH, const CUtensorMap& tWc, int T, int C,
                                   int D, const int32_t* slot, float2* part, float* tgt,
-                                  float cap, float tau, const Targets& tg, int* status,
-                                  int num_sms, cudaStream_t stream) {
+                                  float cap, float tau, const Targets& tg, const float* amax,
+                                  int* status, int num_sms, cudaStream_t stream) {
+  if (amax)  // the FP8 head (plain logits, one target per token)
+    return forward_logits<false, 1, true>(tH, tWc, T, C, D, slot, part, tgt, head_cap(0.f, 1.f),
+                                          tg, amax, status, num_sms, stream);
   if (tg.K > 1)
     return launch_forward_logits_mtp(tH, tWc, T, C, D, slot, part, tgt, cap, tau, tg, status,
                                      num_sms, stream);
   const HeadCap h = head_cap(cap, tau);
-  return cap > 0.f ? forward_logits<true, 1>(tH, tWc, T, C, D, slot, part, tgt, h, tg, status,
-                                             num_sms, stream)
-                   : forward_logits<false, 1>(tH, tWc, T, C, D, slot, part, tgt, h, tg, status,
-                                              num_sms, stream);
+  return cap > 0.f ? forward_logits<true, 1>(tH, tWc, T, C, D, slot, part, tgt, h, tg, nullptr,
+                                             status, num_sms, stream)
+                   : forward_logits<false, 1>(tH, tWc, T, C, D, slot, part, tgt, h, tg, nullptr,
+                                              status, num_sms, stream);
 }
 
 cudaError_t launch_softmax_grad(const CUtensorMap& tH, const CUtensorMap& tWc,
                                 const CUtensorMap& tWc_half,
                                 const CUtensorMap& tG_store, int T, int C, int D,
                                 const int32_t* slot, const float* lse, float scale, float cap,
-                                float tau, const Targets& tg, int* status, int num_sms,
-                                cudaStream_t stream) {
+                                float tau, const Targets& tg, const float* amax, int* status,
+                                int num_sms, cudaStream_t stream) {
+  if (amax)
+    return softmax_grad<false, 1, true>(tH, tWc, tWc_half, tG_store, T, C, D, slot, lse, scale,
+                                        head_cap(0.f, 1.f), tg, amax, status, num_sms, stream);
   if (tg.K > 1)
     return launch_softmax_grad_mtp(tH, tWc, tWc_half, tG_store, T, C, D, slot, lse, scale, cap,
                                    tau, tg, status, num_sms, stream);
   const HeadCap h = head_cap(cap, tau);
   return cap > 0.f ? softmax_grad<true, 1>(tH, tWc, tWc_half, tG_store, T, C, D, slot, lse,
-                                           scale, h, tg, status, num_sms, stream)
+                                           scale, h, tg, nullptr, status, num_sms, stream)
                    : softmax_grad<false, 1>(tH, tWc, tWc_half, tG_store, T, C, D, slot, lse,
-                                            scale, h, tg, status, num_sms, stream);
+                                            scale, h, tg, nullptr, status, num_sms, stream);
 }
 
 }  // namespace ss

@@ -14,25 +14,29 @@ namespace ss {
 
 constexpr int kStagesLogits = 4;
 
-template <bool CAP, int KMAX>
+// F8: e4m3 operands (tH, tWc are maps of the e4m3 copies), logits rescaled
+// from amax in the epilogue.
+template <bool CAP, int KMAX, bool F8 = false>
 cudaError_t forward_logits(const CUtensorMap& tH, const CUtensorMap& tWc, int T, int C, int D,
                            const int32_t* slot, float2* part, float* tgt, const HeadCap& head,
-                           const Targets& tg, int* status, int num_sms, cudaStream_t stream) {
-  GemmShape shp{(T + BM - 1) / BM, (C + kBnLogits - 1) / kBnLogits, D / BK};
-  typename EpiFwdT<CAP, KMAX>::Params ep{T, C, slot, part, tgt, status, head, tg};
-  // the capped head's epilogue (three MUFU operations per logit) runs eight
-  // warps in two column groups, two partials per row per tile
-  return launch_gemm<kBnLogits, kStagesLogits, false, false, EpiFwdT<CAP, KMAX>, CAP ? 8 : 4>(
-      tH, tWc, shp, ep, status, num_sms, stream);
+                           const Targets& tg, const float* amax, int* status, int num_sms,
+                           cudaStream_t stream) {
+  GemmShape shp{(T + BM - 1) / BM, (C + kBnLogits - 1) / kBnLogits, D / (F8 ? 2 * BK : BK)};
+  typename EpiFwdT<CAP, KMAX, F8>::Params ep{T, C, slot, part, tgt, status, head, tg, amax};
+  // the capped head's epilogue (three MUFU operations per logit), and the FP8
+  // head's (its mainloop is twice as fast), run eight warps in two column
+  // groups, two partials per row per tile
+  return launch_gemm<kBnLogits, kStagesLogits, false, false, EpiFwdT<CAP, KMAX, F8>,
+                     (CAP || F8) ? 8 : 4, F8>(tH, tWc, shp, ep, status, num_sms, stream);
 }
 
-template <bool CAP, int KMAX>
+template <bool CAP, int KMAX, bool F8 = false>
 cudaError_t softmax_grad(const CUtensorMap& tH, const CUtensorMap& tWc,
                          const CUtensorMap& tWc_half, const CUtensorMap& tG_store, int T, int C,
                          int D, const int32_t* slot, const float* lse, float scale,
-                         const HeadCap& head, const Targets& tg, int* status, int num_sms,
-                         cudaStream_t stream) {
-  typename EpiGT<CAP, KMAX>::Params ep;
+                         const HeadCap& head, const Targets& tg, const float* amax, int* status,
+                         int num_sms, cudaStream_t stream) {
+  typename EpiGT<CAP, KMAX, F8>::Params ep;
   ep.tmG = tG_store;
   ep.T = T;
   ep.C = C;
@@ -46,20 +50,23 @@ cudaError_t softmax_grad(const CUtensorMap& tH, const CUtensorMap& tWc,
   ep.status = status;
   ep.head = head;
   ep.tg = tg;
+  ep.amax = amax;
   // eight epilogue warps in two column groups, one staging buffer each; CTA
   // pairs (each SM stages half of the W_c tile, a 6-deep ring beside the G
   // staging) once the operands exceed L2 (measured on GB300: the pair is 5%
   // slower at (T + C) * D * 2 = 41 MB, 2-3% faster at 138 and 177 MB)
   const int n_tiles = (C + kBnLogits - 1) / kBnLogits;
-  if (operands_exceed_l2(T, C, D)) {
-    GemmShape shp{(T + 2 * BM - 1) / (2 * BM), n_tiles, D / BK};
-    return launch_gemm2<kBnLogits, 6, false, false, EpiGT<CAP, KMAX>, 8>(tH, tWc_half, shp, ep,
-                                                                   status, num_sms, stream);
+  if constexpr (!F8) {  // the e4m3 operands are half the bytes: single CTAs throughout
+    if (operands_exceed_l2(T, C, D)) {
+      GemmShape shp{(T + 2 * BM - 1) / (2 * BM), n_tiles, D / BK};
+      return launch_gemm2<kBnLogits, 6, false, false, EpiGT<CAP, KMAX>, 8>(tH, tWc_half, shp, ep,
+                                                                           status, num_sms,
+                                                                           stream);
+    }
   }
-  GemmShape shp{(T + BM - 1) / BM, n_tiles, D / BK};
-  return launch_gemm<kBnLogits, kStagesLogits, false, false, EpiGT<CAP, KMAX>, 8>(tH, tWc, shp, ep,
-                                                                            status, num_sms,
-                                                                            stream);
+  GemmShape shp{(T + BM - 1) / BM, n_tiles, D / (F8 ? 2 * BK : BK)};
+  return launch_gemm<kBnLogits, kStagesLogits, false, false, EpiGT<CAP, KMAX, F8>, 8, F8>(
+      tH, tWc, shp, ep, status, num_sms, stream);
 }
 
 inline HeadCap head_cap(float cap, float tau) {

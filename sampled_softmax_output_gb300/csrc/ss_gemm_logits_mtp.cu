@@ -13,9 +13,9 @@ cudaError_t launch_forward_logits_mtp(const CUtensorMap& tH, const CUtensorMap& 
                                       int num_sms, cudaStream_t stream) {
   const HeadCap h = head_cap(cap, tau);
   return cap > 0.f ? forward_logits<true, kMaxTargets>(tH, tWc, T, C, D, slot, part, tgt, h, tg,
-                                                       status, num_sms, stream)
+                                                       nullptr, status, num_sms, stream)
                    : forward_logits<false, kMaxTargets>(tH, tWc, T, C, D, slot, part, tgt, h, tg,
-                                                        status, num_sms, stream);
+                                                        nullptr, status, num_sms, stream);
 }
 
 cudaError_t launch_softmax_grad_mtp(const CUtensorMap& tH, const CUtensorMap& tWc,
@@ -25,9 +25,11 @@ cudaError_t launch_softmax_grad_mtp(const CUtensorMap& tH, const CUtensorMap& tW
                                     int* status, int num_sms, cudaStream_t stream) {
   const HeadCap h = head_cap(cap, tau);
   return cap > 0.f ? softmax_grad<true, kMaxTargets>(tH, tWc, tWc_half, tG_store, T, C, D, slot,
-                                                     lse, scale, h, tg, status, num_sms, stream)
+                                                     lse, scale, h, tg, nullptr, status, num_sms,
+                                                     stream)
                    : softmax_grad<false, kMaxTargets>(tH, tWc, tWc_half, tG_store, T, C, D, slot,
-                                                      lse, scale, h, tg, status, num_sms, stream);
+                                                      lse, scale, h, tg, nullptr, status,
+                                                      num_sms, stream);
 }
 
 }  // namespace ss

@@ -47,7 +47,7 @@ constexpr int kBnGrad = 256;    // dH and dW tiles along D
 // epilogue warps), 2 for the capped head (eight warps in two column groups:
 // its epilogue does three MUFU operations per logit); the workspace holds 2.
 constexpr int kFwdGroupsMax = 2;
-inline int fwd_groups(float cap) { return cap > 0.f ? 2 : 1; }
+inline int fwd_groups(float cap, bool fp8 = false) { return cap > 0.f || fp8 ? 2 : 1; }
 
 struct GemmShape;
 
@@ -83,15 +83,18 @@ cudaError_t launch_build_candidates(const int32_t* targets, int T, int V, int C,
 // tg: the targets per token (K = 1, w = 1 for the single-target loss).
 cudaError_t launch_forward_logits(const CUtensorMap& tH, const CUtensorMap& tWc, int T, int C,
                                   int D, const int32_t* slot, float2* part, float* tgt,
-                                  float cap, float tau, const Targets& tg, int* status,
-                                  int num_sms, cudaStream_t stream);
+                                  float cap, float tau, const Targets& tg, const float* amax,
+                                  int* status, int num_sms, cudaStream_t stream);
+// amax != nullptr: the FP8 head, tH / tWc map the e4m3 copies (box 128 x 128
+// and 128 x 256 bytes), amax[2] their tensors' max |x|; plain logits, one
+// target per token.
 // G is written through tG_store: G [T, C] bf16, box 64 x 128, 128-byte swizzle.
 cudaError_t launch_softmax_grad(const CUtensorMap& tH, const CUtensorMap& tWc,
                                 const CUtensorMap& tWc_half,
                                 const CUtensorMap& tG_store, int T, int C, int D,
                                 const int32_t* slot, const float* lse, float scale, float cap,
-                                float tau, const Targets& tg, int* status, int num_sms,
-                                cudaStream_t stream);
+                                float tau, const Targets& tg, const float* amax, int* status,
+                                int num_sms, cudaStream_t stream);
 // the same GEMMs for K > 1 targets per token (ss_gemm_logits_mtp.cu)
 cudaError_t launch_forward_logits_mtp(const CUtensorMap& tH, const CUtensorMap& tWc, int T, int C,
                                       int D, const int32_t* slot, float2* part, float* tgt,

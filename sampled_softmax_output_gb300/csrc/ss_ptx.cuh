@@ -250,6 +250,17 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64
       : "memory");
 }
 
+// D (+)= A . B for 8-bit e4m3 operands (K = 32 per instruction), fp32 in TMEM
+__device__ __forceinline__ void mma_e4m3(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                         uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // Arrive once on `bar` when every tcgen05 operation this thread issued so far
 // has completed.
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
@@ -317,6 +328,47 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn, b
   return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn ? 1u : 0u) << 15) |
          ((b_mn ? 1u : 0u) << 16) | (static_cast<uint32_t>(N >> 3) << 17) |
          (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// Instruction descriptor of kind::f8f6f4 with e4m3 A and B (format 0 in
+// bits 7-9 and 10-12), fp32 D, K-major operands.
+__host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N) {
+  return (1u << 4) | (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// The FP8 head: operands scaled by 2^e per tensor, e the largest integer with
+// amax * 2^e <= 448 (the e4m3 range), so logits = accumulator * 2^-(eH + eW).
+__device__ __forceinline__ int e4m3_exponent(float amax) {
+  if (!(amax > 0.f)) return 0;
+  int k;
+  const float m = frexpf(amax, &k);  // amax = m 2^k, m in [0.5, 1); 448 = 0.875 * 2^9
+  return m <= 0.875f ? 9 - k : 8 - k;
+}
+__device__ __forceinline__ float exp2i(int e) {  // 2^e, |e| <= 126
+  return __int_as_float((127 + e) << 23);
+}
+
+// max of the magnitude bits (sign cleared) of 8 bf16 values
+__device__ __forceinline__ uint32_t bf16x8_absmax_bits(uint4 v) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  uint32_t m = 0u;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) m = max(m, max(w[k] & 0x7fffu, (w[k] >> 16) & 0x7fffu));
+  return m;
+}
+
+// Two floats to two e4m3 codes (round to nearest, ties to even, saturating
+// at +-448): lo -> bits 0-7, hi -> bits 8-15.
+__device__ __forceinline__ uint16_t e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+// Two e4m3 codes back to two halves (exact): bits 0-7 -> low half.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t v) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(v));
+  return r;
 }
 
 // ------------------------------------------------------- CTA pairs (2-SM MMA)

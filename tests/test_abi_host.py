@@ -22,7 +22,7 @@ def test_exports_every_declared_symbol():
                           "ss_schedule_candidates", "ss_clear_rows", "ss_step_graph_create",
                           "ss_step_graph_launch", "ss_step_graph_destroy", "ss_forward_head",
                           "ss_backward_head", "ss_step_head", "ss_forward_mtp", "ss_backward_mtp",
-                          "ss_step_mtp"}
+                          "ss_step_mtp", "ss_quantize_e4m3"}
     for n in names:
         assert hasattr(ss.lib(), n), n
 
@@ -260,3 +260,28 @@ def test_several_targets_argument_errors():
     assert L.ss_backward_mtp(p(FAKE), p(FAKE), p(FAKE), p(FAKE), 2, w, p(FAKE), 0, 50304, 4096,
                              768, None, 1.0, 0, p(FAKE), p(FAKE), p(FAKE), 1 << 40,
                              None) == INVALID
+
+
+def test_fp8_head_argument_errors():
+    """The FP8 head needs plain logits (cap 0) and D % 128 == 0; the
+    several-targets entry points have no FP8 path; fp8 must be 0 or 1."""
+    L = ss.lib()
+
+    def step(head, D=768, T=256):  # a workspace too small: accepted arguments say so
+        return L.ss_step_head(p(FAKE), p(FAKE), p(FAKE), T, 50304, 4096, D, 0, head, 1.0, 0,
+                              p(FAKE), p(FAKE), p(FAKE), p(FAKE), p(FAKE), p(FAKE), p(FAKE),
+                              16, None)
+
+    assert step(ctypes.byref(ss.Head(0.0, 1.0, 1))) == WORKSPACE       # the FP8 head is accepted
+    assert step(ctypes.byref(ss.Head(30.0, 7.5, 1))) == UNSUPPORTED    # cap with FP8
+    assert step(ctypes.byref(ss.Head(0.0, 1.0, 1)), D=192) == UNSUPPORTED
+    assert step(ctypes.byref(ss.Head(0.0, 1.0, 2))) == INVALID
+    w = (ctypes.c_float * 1)(1.0)
+    assert L.ss_step_mtp(p(FAKE), 1, w, p(FAKE), p(FAKE), 0, 50304, 4096, 768, 0,
+                         ctypes.byref(ss.Head(0.0, 1.0, 1)), 1.0, 0, p(FAKE), p(FAKE), p(FAKE),
+                         p(FAKE), p(FAKE), p(FAKE), p(FAKE), 1 << 40, None) == UNSUPPORTED
+    q = L.ss_quantize_e4m3
+    assert q(p(FAKE), 0, p(FAKE), p(FAKE), p(FAKE), 1024, None) == OK
+    assert q(p(FAKE), 12, p(FAKE), p(FAKE), p(FAKE), 1024, None) == INVALID    # n % 8
+    assert q(p(FAKE + 8), 16, p(FAKE), p(FAKE), p(FAKE), 1024, None) == INVALID
+    assert q(p(FAKE), 16, p(FAKE), p(FAKE), p(FAKE), 16, None) == WORKSPACE
