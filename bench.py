@@ -65,8 +65,9 @@ def parse_args():
     ap.add_argument("--cap", type=float, default=0.0,
                     help="capped head: logits z = cap / (1 + exp(-s / tau)) (0: plain head)")
     ap.add_argument("--tau", type=float, default=7.5)
-    ap.add_argument("--fp8", action="store_true",
-                    help="the FP8 head: e4m3 operands for the two logit GEMMs")
+    ap.add_argument("--fp8", nargs="?", const="logits", default=None, choices=["logits", "all"],
+                    help="the FP8 head: e4m3 operands for the two logit GEMMs ('logits', the "
+                         "default), or also e5m2 G for the two gradient GEMMs ('all')")
     ap.add_argument("--targets", type=int, default=1,
                     help="targets per token (multi-token prediction over one set of logits): "
                          "offsets 1..K of one Zipf stream, weights 1, 1/2, 1/4, ...")
@@ -93,9 +94,9 @@ def load_peaks():
 # the source files that define each traced kernel
 KERNEL_SOURCES = {
     "gemm_forward_lse": ["ss_internal.h", "ss_ptx.cuh", "ss_gemm.cuh", "ss_gemm2.cuh",
-                         "ss_gemm_logits.cu"],
+                         "ss_gemm_logits.cuh", "ss_gemm_logits.cu"],
     "gemm_softmax_grad": ["ss_internal.h", "ss_ptx.cuh", "ss_gemm.cuh", "ss_gemm2.cuh",
-                          "ss_gemm_logits.cu"],
+                          "ss_gemm_logits.cuh", "ss_gemm_logits.cu"],
     "gemm_grads": ["ss_internal.h", "ss_ptx.cuh", "ss_gemm.cuh", "ss_gemm2.cuh",
                    "ss_gemm_grads.cu"],
     "build_candidates": ["ss_internal.h", "ss_ptx.cuh", "ss_candidates.cu"],
@@ -112,9 +113,10 @@ def kernel_sha(kernel: str) -> str:
     return h.hexdigest()[:16]
 
 
-def load_traffic(kernel: str, workload: str):
+def load_traffic(kernel: str, workload: str, operands: str = "bf16"):
     """DRAM bytes per launch of `kernel` from the committed ncu summary, or None
-    if there is none or the kernel sources changed since it was captured."""
+    if there is none or the kernel sources changed since it was captured.
+    `operands`: bf16 (lines without the key), fp8_1 or fp8_2 (the FP8 head)."""
     try:
         with open(TRAFFIC_FILE) as f:
             lines = [ln.strip() for ln in f if ln.strip() and not ln.startswith("#")]
@@ -123,7 +125,8 @@ def load_traffic(kernel: str, workload: str):
     sha = kernel_sha(kernel)
     for ln in lines:
         parts = dict(kv.split("=", 1) for kv in ln.split())
-        if parts.get("kernel") == kernel and parts.get("workload") == workload:
+        if (parts.get("kernel") == kernel and parts.get("workload") == workload
+                and parts.get("operands", "bf16") == operands):
             if parts.get("src_sha") != sha:
                 return None
             return float(parts["dram_bytes_per_launch"])
@@ -232,8 +235,17 @@ def barrier(world: int):
 
 # ------------------------------------------------------------- CPU oracle
 
+def fp8_mode(arg) -> int:
+    return {None: 0, "logits": 1, "all": 2}[arg]
+
+
+OPERANDS = {0: "bf16",
+            1: "e4m3 (FP8 head) for the logit GEMMs, bf16 for the gradient GEMMs",
+            2: "e4m3 (FP8 head) for the logit GEMMs, e5m2 G x e4m3 for the gradient GEMMs"}
+
+
 def oracle_sample(x: dict, w, T_s: int, scale: float, cap: float = 0.0, tau: float = 1.0,
-                  fp8: bool = False):
+                  fp8: int = 0):
     """One oracle pass over a bounded sample: the full-batch candidate build
     (and, for the FP8 head, the rounding of H and W[cand]), then forward +
     backward for the first T_s tokens against that candidate set (with the
@@ -247,13 +259,17 @@ def oracle_sample(x: dict, w, T_s: int, scale: float, cap: float = 0.0, tau: flo
     Hs = H[:T_s]
     ss_ = slot[:T_s]
     loss, lse = oracle.forward(Hs, W, cand, ss_, cap=cap, tau=tau)
-    oracle.backward_dH(Hs, W, cand, ss_, lse, scale, cap=cap, tau=tau)
-    oracle.backward_dWc(Hs, W, cand, ss_, lse, scale, cap=cap, tau=tau)
+    if fp8 == 2:  # FP8 gradients: e5m2 G
+        oracle.backward_dH_g8(Hs, W, cand, ss_, lse, scale)
+        oracle.backward_dWc_g8(Hs, W, cand, ss_, lse, scale)
+    else:
+        oracle.backward_dH(Hs, W, cand, ss_, lse, scale, cap=cap, tau=tau)
+        oracle.backward_dWc(Hs, W, cand, ss_, lse, scale, cap=cap, tau=tau)
     return time.perf_counter() - t0
 
 
 def cpu_baseline(x: dict, w, target_s: float, cap: float = 0.0, tau: float = 1.0,
-                 fp8: bool = False) -> dict:
+                 fp8: int = 0) -> dict:
     import oracle
     oracle.build()
     scale = 1.0 / w.T
@@ -291,7 +307,7 @@ def run_native(args, world, rank, local):
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     scale = 1.0 / T
 
-    cap, tau, fp8 = args.cap, args.tau, args.fp8
+    cap, tau, fp8 = args.cap, args.tau, fp8_mode(args.fp8)
     n_tg = args.targets
     mtp_weights = [0.5 ** k for k in range(n_tg)]
     if n_tg > 1:
@@ -425,13 +441,19 @@ def run_native(args, world, rank, local):
     if dom in GEMM_FLOPS_TCD:
         flops = float(GEMM_FLOPS_TCD[dom]) * T * C * D
         achieved = flops / (kern[dom]["avg_ms"] * 1e-3) / 1e12
-        peak = peaks["bf16_tflops"]
+        # a kernel on 8-bit operands takes the measured bf16 peak times the
+        # nominal fp8 / bf16 ratio (4.5 / 2.25 PFLOP/s dense)
+        f8 = (fp8 >= 1 and dom in ("gemm_forward_lse", "gemm_softmax_grad")) or \
+             (fp8 == 2 and dom == "gemm_grads")
+        ratio = 2.0 if f8 else 1.0
+        peak = peaks["bf16_tflops"] * ratio
+        src = (f"{peaks['source']} bf16 burst (MEASURED_PEAKS.json)"
+               if peaks["source"] == "measured" else "fallback")
         roof = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak,
                 "unit": "TFLOP/s", "frac": achieved / peak,
-                "traffic": load_traffic(dom, w.name),
-                "peak_source": f"{peaks['source']} bf16 burst (MEASURED_PEAKS.json)"
-                if peaks["source"] == "measured" else "fallback",
-                "frac_of_sustained": achieved / peaks["bf16_tflops_sustained"],
+                "traffic": load_traffic(dom, w.name, f"fp8_{fp8}" if fp8 else "bf16"),
+                "peak_source": src + (" x 2, the nominal e4m3 / bf16 ratio" if f8 else ""),
+                "frac_of_sustained": achieved / (peaks["bf16_tflops_sustained"] * ratio),
                 "algorithmic_flops_per_launch": flops}
     else:
         roof = {"bound": "hbm", "kernel": dom, "achieved": None, "peak": peaks["hbm_gbs"],
@@ -477,7 +499,7 @@ def run_native(args, world, rank, local):
                    "head": ({"cap": cap, "tau": tau, "logits": "cap / (1 + exp(-s / tau))"}
                             if cap else "plain"),
                    "targets_per_token": n_tg,
-                   "operands": "e4m3 (FP8 head) for the logit GEMMs" if fp8 else "bf16",
+                   "operands": OPERANDS[fp8],
                    **({"target_weights": mtp_weights} if n_tg > 1 else {}),
                    "ms_per_step_three_calls": three_calls_ms,
                    "ms_per_step_graph": graph_ms,
@@ -508,13 +530,13 @@ def run_reference(args, world, rank):
     per_step_s = (args.ref_step_seconds if args.ref_step_seconds is not None
                   else min(5.0, 150.0 / max(K + W_, 1)))
     scale = 1.0 / w.T
-    t_small = oracle_sample(x, w, 8, scale, args.cap, args.tau, args.fp8)
+    t_small = oracle_sample(x, w, 8, scale, args.cap, args.tau, fp8_mode(args.fp8))
     T_s = int(max(1, min(w.T, 8 * per_step_s / max(t_small, 1e-3))))
     for _ in range(W_):
-        oracle_sample(x, w, T_s, scale, args.cap, args.tau, args.fp8)
+        oracle_sample(x, w, T_s, scale, args.cap, args.tau, fp8_mode(args.fp8))
     dt = 0.0
     for _ in range(K):
-        dt += oracle_sample(x, w, T_s, scale, args.cap, args.tau, args.fp8)
+        dt += oracle_sample(x, w, T_s, scale, args.cap, args.tau, fp8_mode(args.fp8))
     value = T_s * K / dt
     cores = oracle.num_threads()
     sample = (f"{w.name}: per step, full-batch candidate build (T={w.T}) + forward/backward of "
@@ -542,7 +564,7 @@ def main():
     if rank == 0:
         if world == 1 and not args.no_cpu_baseline:
             line["cpu_baseline"] = cpu_baseline(x, w, args.cpu_seconds, args.cap, args.tau,
-                                                args.fp8)
+                                                fp8_mode(args.fp8))
         else:
             line["cpu_baseline"] = None
         print(json.dumps(line), flush=True)

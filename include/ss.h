@@ -164,14 +164,25 @@ ss_status ss_backward(const uint16_t* H, const uint16_t* W, const int32_t* cand,
  * nearest, ties to even) and used in that form by both logit GEMMs
  * (tcgen05 kind::f8f6f4, twice the bf16 rate); the gradient GEMMs use the
  * same rounded operands in bf16, G stays bf16. Results are those of the
- * plain head on the rounded operands. Requires cap = 0 (else
- * SS_ERR_UNSUPPORTED) and D % 128 == 0 (else SS_ERR_UNSUPPORTED); the
- * several-targets entry points take no FP8 head (SS_ERR_UNSUPPORTED).
+ * plain head on the rounded operands.
+ * fp8 = 2: the same, and FP8 through the backward pass too ("NanoGPT
+ * Training Record: Technical Optimizations & Speed": FP8 quantisation
+ * reaches through the backward pass; the pages give no format). Reading,
+ * after the usual FP8 training split (E4M3 for values, E5M2 for gradients;
+ * Micikevicius et al., "FP8 Formats for Deep Learning", 2022): the gradient
+ * matrix, before the factor `scale`, is scaled by 2^15 (its bound
+ * |P - Y| <= 1 then stays within e5m2's largest finite value 57344) and
+ * rounded to e5m2 (to nearest, ties to even), G8 = e5m2(2^15 (P - Y));
+ * the two gradient GEMMs run on G8 and the e4m3 operands
+ * (dH = scale 2^-15 G8 . W_c,q and dW_c = scale 2^-15 G8^T . H_q).
+ * Both modes require cap = 0 (else SS_ERR_UNSUPPORTED) and D % 128 == 0
+ * (else SS_ERR_UNSUPPORTED); the several-targets entry points take no FP8
+ * head (SS_ERR_UNSUPPORTED); other fp8 values -> SS_ERR_INVALID.
  */
 typedef struct ss_head {
   float cap;
   float tau;
-  int fp8;  /* 1: the FP8 head (see below); 0: bf16 operands */
+  int fp8;  /* 0: bf16 operands; 1: FP8 logit GEMMs; 2: FP8 logit and gradient GEMMs */
 } ss_head;
 
 ss_status ss_forward_head(const uint16_t* H, const uint16_t* W, const int32_t* cand,

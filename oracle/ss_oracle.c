@@ -71,6 +71,20 @@
  * is the definition above applied to the rounded H and W[cand]; G itself
  * stays in the working precision.
  *
+ * FP8 through the backward pass ("NanoGPT Training Record: Technical
+ * Optimizations & Speed": FP8 quantisation reaches through the backward pass;
+ * no format on the pages). Reading, after the common FP8 training split of
+ * e4m3 for values and e5m2 for gradients (Micikevicius et al., "FP8 Formats
+ * for Deep Learning", 2022): on top of the FP8 head above, the gradient
+ * matrix before the factor `scale` is scaled by 2^15 (so that its bound
+ * |P - Y| <= 1 stays inside e5m2's largest finite value 57344) and rounded
+ * to the e5m2 grid (1 sign, 5 exponent bits with bias 15, 2 mantissa bits,
+ * subnormals down to 2^-16; round to nearest, ties to even):
+ *               G8[t][j] = round_e5m2(2^15 (exp(s[t][j] - lse[t]) - [j == slot[t]]))
+ *               dH[t]    = scale 2^-15 sum_j G8[t][j] * W[cand[j]]
+ *               dW[cand[j]] = scale 2^-15 sum_t G8[t][j] * H[t]
+ *   with H and W the e4m3-rounded operands.
+ *
  * Precision: the definition is fp32. Its inputs are bf16 bit patterns widened
  * exactly to float. An fp64 instantiation of the same loops, on double inputs,
  * exists for the finite-difference and library cross-checks. Build with
@@ -397,6 +411,75 @@ void orc_quantize_e4m3_bf16(const uint16_t* x, int64_t n, int e, uint16_t* out) 
     uint32_t u;
     memcpy(&u, &v, 4);
     out[i] = (uint16_t)(u >> 16); /* exact: at most 4 significant bits */
+  }
+}
+
+/* ------------------------------------------------------------- e5m2 rounding */
+
+/* x rounded to the e5m2 grid, ties to even; |x| >= 57344 saturates to 57344. */
+float orc_round_e5m2(float x) {
+  if (x != x) return x;
+  const float a = fabsf(x);
+  if (a == 0.0f) return x;
+  if (a >= 57344.0f) return copysignf(57344.0f, x);
+  int e2;
+  frexpf(a, &e2);          /* a in [2^(e2-1), 2^e2) */
+  int E = e2 - 1;
+  if (E < -14) E = -14;    /* below 2^-14: subnormals, spacing 2^-16 */
+  const float q = ldexpf(1.0f, E - 2);  /* grid spacing in this binade */
+  return copysignf(rintf(a / q) * q, x);
+}
+
+/* G8 of one logit: round_e5m2(2^15 (exp(s - lse) - y)) */
+static float g8_of(float s, float lse, float y) {
+  return orc_round_e5m2(ldexpf(expf(s - lse) - y, 15));
+}
+
+/* FP8 gradients, one target per token, plain head: dH rows (lse_rows of
+ * exactly those rows), inputs already rounded to e4m3 (bf16 bit patterns). */
+void orc_backward_dH_g8(const uint16_t* H, const uint16_t* W, const int32_t* cand,
+                        const int32_t* slot, const float* lse_rows, int64_t T, int64_t C,
+                        int64_t D, float scale, const int64_t* rows, int64_t nrows, float* dH) {
+  int64_t n = rows ? nrows : T;
+  const float f = ldexpf(scale, -15);
+#pragma omp parallel
+  {
+    float* s = (float*)malloc(sizeof(float) * (size_t)C);
+#pragma omp for schedule(dynamic, 1)
+    for (int64_t i = 0; i < n; ++i) {
+      int64_t t = rows ? rows[i] : i;
+      logits_f32(H, W, cand, C, D, t, s);
+      float* out = dH + i * D;
+      for (int64_t d = 0; d < D; ++d) out[d] = 0;
+      for (int64_t j = 0; j < C; ++j) {
+        const float g = f * g8_of(s[j], lse_rows[i], slot[t] == j ? 1.0f : 0.0f);
+        const uint16_t* wr = W + (int64_t)cand[j] * D;
+        for (int64_t d = 0; d < D; ++d) out[d] += g * bf16_to_float(wr[d]);
+      }
+    }
+    free(s);
+  }
+}
+
+/* ... and dW_c rows (candidate index j; lse of ALL T tokens) */
+void orc_backward_dW_g8(const uint16_t* H, const uint16_t* W, const int32_t* cand,
+                        const int32_t* slot, const float* lse, int64_t T, int64_t C, int64_t D,
+                        float scale, const int64_t* cols, int64_t ncols, float* dWc) {
+  int64_t n = cols ? ncols : C;
+  const float f = ldexpf(scale, -15);
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int64_t i = 0; i < n; ++i) {
+    int64_t j = cols ? cols[i] : i;
+    const uint16_t* wr = W + (int64_t)cand[j] * D;
+    float* out = dWc + i * D;
+    for (int64_t d = 0; d < D; ++d) out[d] = 0;
+    for (int64_t t = 0; t < T; ++t) {
+      const uint16_t* h = H + t * D;
+      float st = 0;
+      for (int64_t d = 0; d < D; ++d) st += bf16_to_float(h[d]) * bf16_to_float(wr[d]);
+      const float g = f * g8_of(st, lse[t], slot[t] == j ? 1.0f : 0.0f);
+      for (int64_t d = 0; d < D; ++d) out[d] += g * bf16_to_float(h[d]);
+    }
   }
 }
 

@@ -41,14 +41,17 @@ NOALLOC_SCRATCH_BYTES = 32 << 20
 
 class Head(ctypes.Structure):
     """ss_head: cap > 0 -> logits z = cap / (1 + exp(-s / tau)); cap = 0 -> plain;
-    fp8 = 1 -> the FP8 head."""
+    fp8 = 1 -> the FP8 head (e4m3 logit GEMMs); fp8 = 2 -> FP8 through the
+    backward too (e5m2 G in the gradient GEMMs)."""
     _fields_ = [("cap", ctypes.c_float), ("tau", ctypes.c_float), ("fp8", ctypes.c_int)]
 
 
-def _head(cap: float, tau: float, fp8: bool = False):
+def _head(cap: float, tau: float, fp8: int = 0):
+    """``fp8``: 0 / False (bf16), 1 / True (FP8 logit GEMMs), 2 (FP8 logit and
+    gradient GEMMs)."""
     if cap == 0 and not fp8:
         return None
-    return ctypes.byref(Head(float(cap), float(tau), 1 if fp8 else 0))
+    return ctypes.byref(Head(float(cap), float(tau), int(fp8)))
 
 
 class SSError(RuntimeError):
@@ -223,7 +226,7 @@ def build_candidates(targets: torch.Tensor, V: int, C: int, seed: int, ws: torch
 
 def forward(H: torch.Tensor, W: torch.Tensor, cand: torch.Tensor, slot: torch.Tensor,
             ws: torch.Tensor, loss: torch.Tensor | None = None, lse: torch.Tensor | None = None,
-            cap: float = 0.0, tau: float = 1.0, fp8: bool = False):
+            cap: float = 0.0, tau: float = 1.0, fp8: int = 0):
     """Per-token loss [T] and log-sum-exp [T] (fp32) over the candidate rows
     (cap > 0: of the capped logits, ss_forward_head)."""
     _need(H, "H", torch.bfloat16)
@@ -282,7 +285,7 @@ def forward_noalloc(H: torch.Tensor, W: torch.Tensor, cand: torch.Tensor, slot: 
 def backward(H: torch.Tensor, W: torch.Tensor, cand: torch.Tensor, slot: torch.Tensor,
              lse: torch.Tensor, ws: torch.Tensor, scale: float = 1.0, accumulate: bool = False,
              dH: torch.Tensor | None = None, dW: torch.Tensor | None = None, cap: float = 0.0,
-             tau: float = 1.0, fp8: bool = False):
+             tau: float = 1.0, fp8: int = 0):
     """dH [T, D] bf16 and dW [V, D] fp32 (only candidate rows written / added to).
     A new dW is zero-filled, so that it is the dense gradient."""
     _need(H, "H", torch.bfloat16)
@@ -365,7 +368,7 @@ class KernelTrace:
 
 def step(H, W, targets, C: int, seed: int, ws, scale: float = 1.0, dW=None, accumulate=False,
          cand=None, slot=None, loss=None, lse=None, dH=None, cap: float = 0.0, tau: float = 1.0,
-         fp8: bool = False):
+         fp8: int = 0):
     """One full pass of the path in one call (ss_step): candidates, forward,
     backward, with one gather of the candidate rows shared by both passes."""
     _need(H, "H", torch.bfloat16)
@@ -400,7 +403,7 @@ def step(H, W, targets, C: int, seed: int, ws, scale: float = 1.0, dW=None, accu
 
 
 def step_separate(H, W, targets, C: int, seed: int, ws, scale: float = 1.0, dW=None,
-                  accumulate=False, cap: float = 0.0, tau: float = 1.0, fp8: bool = False):
+                  accumulate=False, cap: float = 0.0, tau: float = 1.0, fp8: int = 0):
     """The same pass as three calls: ss_build_candidates, ss_forward, ss_backward."""
     V = W.shape[0]
     cand, slot = build_candidates(targets, V, C, seed, ws)
@@ -440,7 +443,7 @@ class StepGraph:
 
     def __init__(self, H, W, targets, C: int, ws, scale: float = 1.0, accumulate=False,
                  cand=None, slot=None, loss=None, lse=None, dH=None, dW=None, cap: float = 0.0,
-                 tau: float = 1.0, fp8: bool = False):
+                 tau: float = 1.0, fp8: int = 0):
         _need(H, "H", torch.bfloat16)
         dev = H.device
         T, D = H.shape

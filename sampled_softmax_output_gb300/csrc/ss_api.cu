@@ -10,6 +10,7 @@
 #include <stdint.h>
 #include <stdio.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <mutex>
@@ -25,8 +26,9 @@ namespace {
 // ------------------------------------------------------------ workspace
 
 struct Layout {
-  size_t hdr, wc, part, tgt, g, h8, hq, w8, total;
+  size_t hdr, wc, part, tgt, g, g8t, h8, hq, h8t, w8, w8t, total;
   int64_t ldG, n_ct;
+  int64_t ldT8, ldC8;  // row pitch (bytes) of the transposed e4m3 / e5m2 copies
 };
 
 constexpr size_t kHdrBytes = 1024;  // int32 status, int32 U, padding, FP8 amax words
@@ -48,15 +50,26 @@ Layout make_layout(int64_t T, int64_t C, int64_t D) {
   off = align_up(off + static_cast<size_t>(L.n_ct) * kFwdGroupsMax * T * sizeof(float2), 1024);
   L.tgt = off;  // target logits, up to kMaxTargets per token
   off = align_up(off + static_cast<size_t>(T) * kMaxTargets * sizeof(float), 1024);
+  L.ldT8 = (T + 15) / 16 * 16;
+  L.ldC8 = (C + 15) / 16 * 16;
+  // G in bf16, or (FP8 gradients) G8 [T, ldG] and G8^T [C, ldT8] in e5m2
   L.g = off;
-  off = align_up(off + static_cast<size_t>(T) * L.ldG * 2, 1024);
-  // the FP8 head's operands: H and W_c in e4m3, H rounded to the e4m3 grid in bf16
+  L.g8t = align_up(off + static_cast<size_t>(T) * L.ldG, 1024);
+  off = align_up(std::max(off + static_cast<size_t>(T) * L.ldG * 2,
+                          L.g8t + static_cast<size_t>(C) * L.ldT8),
+                 1024);
+  // the FP8 head's operands: H and W_c in e4m3; H rounded to the e4m3 grid in
+  // bf16 (FP8 logits only) or, in the same place, H^T in e4m3 (FP8 gradients);
+  // W_c^T in e4m3 (FP8 gradients)
   L.h8 = off;
   off = align_up(off + static_cast<size_t>(T) * D, 1024);
-  L.hq = off;
-  off = align_up(off + static_cast<size_t>(T) * D * 2, 1024);
+  L.hq = L.h8t = off;
+  off = align_up(off + std::max(static_cast<size_t>(T) * D * 2, static_cast<size_t>(D) * L.ldT8),
+                 1024);
   L.w8 = off;
   off = align_up(off + static_cast<size_t>(C) * D, 1024);
+  L.w8t = off;
+  off = align_up(off + static_cast<size_t>(D) * L.ldC8, 1024);
   L.total = off;
   return L;
 }
@@ -102,10 +115,12 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 // Row-major bf16 matrix [outer, inner] with `row_bytes` between rows, read in
-// boxes of box_outer rows x box_inner elements with the 128-byte swizzle.
+// boxes of box_outer rows x box_inner elements with the 128-byte swizzle (or
+// another element type and swizzle).
 bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
               uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
-              CUtensorMapDataType dtype = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
+              CUtensorMapDataType dtype = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+              CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {inner, outer};
@@ -113,7 +128,7 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
   cuuint32_t box[2] = {box_inner, box_outer};
   cuuint32_t es[2] = {1, 1};
   return fn(m, dtype, 2, const_cast<void*>(base), dims, strides, box,
-            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            es, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -204,6 +219,66 @@ __global__ void __launch_bounds__(256) k_quantize_e4m3(QuantJob a, QuantJob b, i
       }
       reinterpret_cast<uint2*>(J.q)[i] = make_uint2(qw[0], qw[1]);
       reinterpret_cast<uint4*>(J.xq)[i] = make_uint4(out[0], out[1], out[2], out[3]);
+    }
+  }
+}
+
+// FP8 gradients: x [R, D] bf16 (D % 64 == 0) to e4m3 codes twice, q [R, D]
+// row-major (the logit GEMMs) and qt [D, ldR] transposed (the gradient GEMMs,
+// which need K = R contiguous), e from the tensor's amax. One 64 x 64 tile per
+// iteration, transposed through shared memory; two tensors in one launch.
+struct QuantTJob {
+  const uint16_t* x;
+  uint8_t* q;
+  uint8_t* qt;
+  const float* amax;
+  int R, D, ldR, tiles;  // tiles = ceil(R / 64) * (D / 64)
+};
+constexpr int kQtPitch = 72;  // bytes per row of the shared tile (64 + 8 against conflicts)
+__global__ void __launch_bounds__(256) k_quantize_e4m3_t(QuantTJob a, QuantTJob b, int* status) {
+  pdl_enter();
+  if (read_status(status) != 0) return;
+  __shared__ __align__(16) uint8_t tile[64 * kQtPitch];
+  for (int w = blockIdx.x; w < a.tiles + b.tiles; w += gridDim.x) {
+    const bool first = w < a.tiles;
+    const QuantTJob& J = first ? a : b;
+    const int ti = first ? w : w - a.tiles;
+    const int nct = J.D / 64;
+    const int r0 = (ti / nct) * 64, c0 = (ti % nct) * 64;
+    const float up = exp2i(e4m3_exponent(__ldcg(J.amax)));
+    __syncthreads();  // the previous tile's transposed reads are done
+    for (int v = threadIdx.x; v < 512; v += blockDim.x) {
+      const int r = v >> 3, c8 = (v & 7) * 8;  // row r, columns c8 .. c8 + 7 of the tile
+      uint32_t qw[2] = {0u, 0u};
+      if (r0 + r < J.R) {
+        const size_t at = static_cast<size_t>(r0 + r) * J.D + c0 + c8;
+        const uint4 x = __ldg(reinterpret_cast<const uint4*>(J.x + at));
+        const uint32_t xw[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const uint16_t c = e4m3x2(__uint_as_float(xw[k] << 16) * up,
+                                    __uint_as_float(xw[k] & 0xffff0000u) * up);
+          qw[k >> 1] |= static_cast<uint32_t>(c) << (16 * (k & 1));
+        }
+        *reinterpret_cast<uint2*>(J.q + at) = make_uint2(qw[0], qw[1]);
+      }
+      *reinterpret_cast<uint2*>(tile + r * kQtPitch + c8) = make_uint2(qw[0], qw[1]);
+    }
+    __syncthreads();
+    for (int v = threadIdx.x; v < 512; v += blockDim.x) {
+      const int c = v >> 3, rg = (v & 7) * 8;  // column c, rows rg .. rg + 7 of the tile
+      const int nr = min(8, J.R - r0 - rg);
+      if (nr <= 0) continue;
+      uint32_t o[2] = {0u, 0u};
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+        o[k >> 2] |= static_cast<uint32_t>(tile[(rg + k) * kQtPitch + c]) << (8 * (k & 3));
+      uint8_t* dst = J.qt + static_cast<size_t>(c0 + c) * J.ldR + r0 + rg;
+      if (nr == 8) {
+        *reinterpret_cast<uint2*>(dst) = make_uint2(o[0], o[1]);
+      } else {
+        for (int k = 0; k < nr; ++k) dst[k] = static_cast<uint8_t>(o[k >> 2] >> (8 * (k & 3)));
+      }
     }
   }
 }
@@ -397,7 +472,7 @@ ss_status enqueue_gather(const uint16_t* W, const int32_t* cand, int64_t C, int6
 // W_c = W[cand] and, for the FP8 head, the e4m3 operands: amax of W_c (in
 // the gather) and of H, then H -> (h8, hq) and W_c -> (w8, W_c rounded in place)
 ss_status enqueue_gather_operands(const uint16_t* W, const int32_t* cand, const uint16_t* H,
-                                  int64_t T, int64_t C, int64_t V, int64_t D, bool fp8,
+                                  int64_t T, int64_t C, int64_t V, int64_t D, int fp8,
                                   const Layout& L, char* ws, int nsm, cudaStream_t s) {
   int* status = reinterpret_cast<int*>(ws + L.hdr);
   uint16_t* Wc = reinterpret_cast<uint16_t*>(ws + L.wc);
@@ -411,6 +486,21 @@ ss_status enqueue_gather_operands(const uint16_t* W, const int32_t* cand, const 
   e = launch_pdl(k_amax_bf16, dim3(nsm * 2), dim3(256), 0, s, H, T * D / 8, amax, status);
   trace_post(s);
   if (e != cudaSuccess) return fail("launch k_amax_bf16", e);
+  if (fp8 == 2) {  // FP8 gradients: row-major and transposed codes, no bf16 copies
+    if ((T + 63) / 64 * (D / 64) > INT32_MAX / 2) return SS_ERR_UNSUPPORTED;
+    const QuantTJob th{H, reinterpret_cast<uint8_t*>(ws + L.h8),
+                       reinterpret_cast<uint8_t*>(ws + L.h8t), amax, static_cast<int>(T),
+                       static_cast<int>(D), static_cast<int>(L.ldT8),
+                       static_cast<int>((T + 63) / 64 * (D / 64))};
+    const QuantTJob tw{Wc, reinterpret_cast<uint8_t*>(ws + L.w8),
+                       reinterpret_cast<uint8_t*>(ws + L.w8t), amax + 1, static_cast<int>(C),
+                       static_cast<int>(D), static_cast<int>(L.ldC8),
+                       static_cast<int>((C + 63) / 64 * (D / 64))};
+    trace_pre(s, "quantize_e4m3");
+    e = launch_pdl(k_quantize_e4m3_t, dim3(nsm * 4), dim3(256), 0, s, th, tw, status);
+    trace_post(s);
+    return e == cudaSuccess ? SS_OK : fail("launch k_quantize_e4m3_t", e);
+  }
   const QuantJob jh{H, reinterpret_cast<uint8_t*>(ws + L.h8), reinterpret_cast<uint16_t*>(ws + L.hq),
                     amax, T * D / 8};
   const QuantJob jw{Wc, reinterpret_cast<uint8_t*>(ws + L.w8), Wc, amax + 1, C * D / 8};
@@ -422,7 +512,7 @@ ss_status enqueue_gather_operands(const uint16_t* W, const int32_t* cand, const 
 
 // forward GEMM (LSE partials, target logit) and the LSE merge, from W_c
 ss_status enqueue_forward(const uint16_t* H, const int32_t* slot, int64_t T, int64_t C, int64_t D,
-                          float cap, float tau, const Targets& tg, bool fp8, float* loss,
+                          float cap, float tau, const Targets& tg, int fp8, float* loss,
                           float* lse, const Layout& L, char* ws, int nsm, cudaStream_t s) {
   int* status = reinterpret_cast<int*>(ws + L.hdr);
   uint16_t* Wc = reinterpret_cast<uint16_t*>(ws + L.wc);
@@ -449,18 +539,57 @@ ss_status enqueue_forward(const uint16_t* H, const int32_t* slot, int64_t T, int
   trace_pre(s, "lse_merge");
   const cudaError_t em =
       launch_pdl(k_lse_merge, dim3(blocks), dim3(256), 0, s, part, tgt, slot, static_cast<int>(T),
-                 static_cast<int>(C), static_cast<int>(L.n_ct * fwd_groups(cap, fp8)), tg, loss,
+                 static_cast<int>(C), static_cast<int>(L.n_ct * fwd_groups(cap, fp8 != 0)), tg, loss,
                  lse, status);
   trace_post(s);
   return cuda_status(em, "launch k_lse_merge");
 }
 
+// FP8 gradients: G8 and G8^T (e5m2) from the e4m3 logits, then both gradient
+// GEMMs on e5m2 x e4m3, every operand K-major
+ss_status enqueue_backward_fp8(const int32_t* cand, const int32_t* slot, const float* lse,
+                               int64_t T, int64_t V, int64_t C, int64_t D, float scale,
+                               int accumulate, uint16_t* dH, float* dW, const Layout& L, char* ws,
+                               int nsm, cudaStream_t s) {
+  int* status = reinterpret_cast<int*>(ws + L.hdr);
+  const float* amax = reinterpret_cast<const float*>(ws + L.hdr + kHdrAmax);
+  const auto u8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
+  const uint64_t ldG = static_cast<uint64_t>(L.ldG), ldT = static_cast<uint64_t>(L.ldT8),
+                 ldC = static_cast<uint64_t>(L.ldC8);
+  CUtensorMap tH8, tW8, tG8s, tG8ts, tG8, tW8t, tG8t, tH8t;
+  const bool ok =
+      make_map(&tH8, ws + L.h8, D, T, D, 128, 128, u8) &&
+      make_map(&tW8, ws + L.w8, D, C, D, 128, kBnLogits, u8) &&
+      make_map(&tG8s, ws + L.g, C, T, ldG, 64, 128, u8, CU_TENSOR_MAP_SWIZZLE_64B) &&
+      make_map(&tG8ts, ws + L.g8t, T, C, ldT, 128, 64, u8) &&
+      make_map(&tG8, ws + L.g, C, T, ldG, 128, 128, u8) &&
+      make_map(&tW8t, ws + L.w8t, C, D, ldC, 128, 128, u8) &&
+      make_map(&tG8t, ws + L.g8t, T, C, ldT, 128, 128, u8) &&
+      make_map(&tH8t, ws + L.h8t, T, D, ldT, 128, 128, u8);
+  if (!ok) return fail("cuTensorMapEncodeTiled", cudaErrorInvalidValue);
+  const int iT = static_cast<int>(T), iV = static_cast<int>(V), iC = static_cast<int>(C),
+            iD = static_cast<int>(D);
+  trace_pre(s, "gemm_softmax_grad");
+  cudaError_t e = launch_softmax_grad_fp8(tH8, tW8, tG8s, tG8ts, iT, iC, iD, slot, lse, amax,
+                                          status, nsm, s);
+  trace_post(s);
+  if (e != cudaSuccess) return fail("launch gemm_softmax_grad", e);
+  trace_pre(s, "gemm_grads");
+  e = launch_grads_fp8(tG8, tW8t, tG8t, tH8t, iT, iC, iD, iV, accumulate, cand, scale, amax, dH,
+                       dW, status, nsm, s);
+  trace_post(s);
+  return e == cudaSuccess ? SS_OK : fail("launch gemm_grads", e);
+}
+
 // softmax-gradient GEMM and the two gradient GEMMs, from W_c
 ss_status enqueue_backward(const uint16_t* H, const int32_t* cand, const int32_t* slot,
                            const float* lse, int64_t T, int64_t V, int64_t C, int64_t D,
-                           float cap, float tau, const Targets& tg, bool fp8, float scale,
+                           float cap, float tau, const Targets& tg, int fp8, float scale,
                            int accumulate, uint16_t* dH, float* dW, const Layout& L, char* ws,
                            int nsm, cudaStream_t s) {
+  if (fp8 == 2)
+    return enqueue_backward_fp8(cand, slot, lse, T, V, C, D, scale, accumulate, dH, dW, L, ws, nsm,
+                                s);
   int* status = reinterpret_cast<int*>(ws + L.hdr);
   uint16_t* Wc = reinterpret_cast<uint16_t*>(ws + L.wc);
   uint16_t* G = reinterpret_cast<uint16_t*>(ws + L.g);
@@ -615,7 +744,7 @@ ss_status ss_build_candidates(const int32_t* targets, int64_t T, int64_t V, int6
 
 static ss_status forward_impl(const uint16_t* H, const uint16_t* W, const int32_t* cand,
                               const int32_t* slot, int64_t T, int64_t V, int64_t C, int64_t D,
-                              float cap, float tau, const Targets& tg, bool fp8, float* loss,
+                              float cap, float tau, const Targets& tg, int fp8, float* loss,
                               float* lse, void* workspace, size_t workspace_bytes,
                               ss_stream stream) {
   const ss_status st = check_sizes(T, V, C, D);
@@ -640,7 +769,7 @@ static ss_status forward_impl(const uint16_t* H, const uint16_t* W, const int32_
 static ss_status backward_impl(const uint16_t* H, const uint16_t* W, const int32_t* cand,
                                const int32_t* slot, const float* lse, int64_t T, int64_t V,
                                int64_t C, int64_t D, float cap, float tau, const Targets& tg,
-                               bool fp8, float scale, int accumulate, uint16_t* dH, float* dW,
+                               int fp8, float scale, int accumulate, uint16_t* dH, float* dW,
                                void* workspace, size_t workspace_bytes, ss_stream stream) {
   const ss_status st = check_sizes(T, V, C, D);
   if (st != SS_OK) return st;
@@ -666,7 +795,7 @@ static ss_status backward_impl(const uint16_t* H, const uint16_t* W, const int32
 
 static ss_status step_impl(const int32_t* targets, const uint16_t* H, const uint16_t* W,
                            int64_t T, int64_t V, int64_t C, int64_t D, uint64_t seed, float cap,
-                           float tau, const Targets& tg, bool fp8, float scale, int accumulate,
+                           float tau, const Targets& tg, int fp8, float scale, int accumulate,
                            int32_t* cand, int32_t* slot, float* loss, float* lse, uint16_t* dH,
                            float* dW, void* workspace, size_t workspace_bytes, ss_stream stream) {
   const ss_status st = step_args_status(targets, H, W, T, V, C, D, accumulate, cand, slot, loss,
@@ -707,17 +836,17 @@ static ss_status targets_args(int64_t K, const float* w, Targets* tg) {
   return sum > 0.f && std::isfinite(sum) ? SS_OK : SS_ERR_INVALID;
 }
 
-// the head options: NULL or cap == 0 is the plain head; fp8 (plain logits
-// only) sets *fp8
-static ss_status head_args(const ss_head* head, float* cap, float* tau, bool* fp8 = nullptr) {
+// the head options: NULL or cap == 0 is the plain head; fp8 = 1 or 2 (plain
+// logits only) sets *fp8
+static ss_status head_args(const ss_head* head, float* cap, float* tau, int* fp8 = nullptr) {
   *cap = 0.f;
   *tau = 1.f;
-  if (fp8) *fp8 = false;
+  if (fp8) *fp8 = 0;
   if (head && head->fp8 != 0) {
-    if (head->fp8 != 1) return SS_ERR_INVALID;
+    if (head->fp8 != 1 && head->fp8 != 2) return SS_ERR_INVALID;
     if (!fp8) return SS_ERR_UNSUPPORTED;  // this entry point has no FP8 path
     if (head->cap != 0.f) return SS_ERR_UNSUPPORTED;
-    *fp8 = true;
+    *fp8 = head->fp8;
     return SS_OK;
   }
   if (!head || head->cap == 0.f) return SS_OK;
@@ -742,7 +871,7 @@ ss_status ss_forward_head(const uint16_t* H, const uint16_t* W, const int32_t* c
                           const ss_head* head, float* loss, float* lse, void* workspace,
                           size_t workspace_bytes, ss_stream stream) {
   float cap, tau;
-  bool fp8;
+  int fp8;
   const ss_status h = head_args(head, &cap, &tau, &fp8);
   if (h != SS_OK) return h;
   if (fp8 && D % 128 != 0) return SS_ERR_UNSUPPORTED;
@@ -764,7 +893,7 @@ ss_status ss_backward_head(const uint16_t* H, const uint16_t* W, const int32_t* 
                            int accumulate, uint16_t* dH, float* dW, void* workspace,
                            size_t workspace_bytes, ss_stream stream) {
   float cap, tau;
-  bool fp8;
+  int fp8;
   const ss_status h = head_args(head, &cap, &tau, &fp8);
   if (h != SS_OK) return h;
   if (fp8 && D % 128 != 0) return SS_ERR_UNSUPPORTED;
@@ -786,7 +915,7 @@ ss_status ss_step_head(const int32_t* targets, const uint16_t* H, const uint16_t
                        float* lse, uint16_t* dH, float* dW, void* workspace,
                        size_t workspace_bytes, ss_stream stream) {
   float cap, tau;
-  bool fp8;
+  int fp8;
   const ss_status h = head_args(head, &cap, &tau, &fp8);
   if (h != SS_OK) return h;
   if (fp8 && D % 128 != 0) return SS_ERR_UNSUPPORTED;
@@ -1007,7 +1136,7 @@ ss_status ss_step_graph_create(const int32_t* targets, const uint16_t* H, const 
   if (!graph) return SS_ERR_INVALID;
   *graph = nullptr;
   float cap, tau;
-  bool fp8;
+  int fp8;
   ss_status st = head_args(head, &cap, &tau, &fp8);
   if (st != SS_OK) return st;
   if (fp8 && D % 128 != 0) return SS_ERR_UNSUPPORTED;

@@ -355,13 +355,137 @@ struct EpiGT {
 };
 using EpiG = EpiGT<false>;
 
-// Backward, step 2: dH tile -> bf16 (column group cg of NCG).
-struct EpiDh {
+// FP8 gradients: G is scaled by 2^kG8Exp, the largest power of two that keeps
+// its bound |P - Y| <= 1 within e5m2's largest finite value (57344), and
+// rounded to e5m2; the scale and the operand's e4m3 exponent come back out of
+// the gradient GEMMs' fp32 accumulators.
+constexpr int kG8Exp = 15;
+__device__ __forceinline__ float fp8_grad_alpha(float scale, const float* amax_b) {
+  return scale * exp2i(-(kG8Exp + e4m3_exponent(__ldcg(amax_b))));
+}
+
+// Backward, step 1 with FP8 gradients (e4m3 logit operands):
+//   G8[t, j] = e5m2(2^15 (exp(S[t,j] - lse[t]) - [j == slot[t]])),
+// written twice through TMA bulk tensor stores: row-major G8 [T, C] (the
+// K-major A operand of dH = G W_c) and transposed G8t [C, T] (the K-major A
+// operand of dW_c = G^T H). Each 64-column quarter is staged as a 128 x 64-byte
+// tile in the 64-byte-swizzled layout of G8's map and a 64 x 128-byte tile in
+// the 128-byte-swizzled layout of G8t's map (16 KB per column group).
+struct EpiG8 {
+  static constexpr int kStageBytes = 2 * 16384;
+  static constexpr bool kKeepOperands = true;
+  struct Params {
+    CUtensorMap tmG;   // G8 [T, C] (row pitch ldG bytes), box 64 x 128, 64-byte swizzle
+    CUtensorMap tmGt;  // G8t [C, T] (row pitch ldT bytes), box 128 x 64, 128-byte swizzle
+    int T, C;
+    const int32_t* slot;
+    const float* lse;
+    int* status;
+    const float* amax;  // logits = accumulator * e4m3_logit_scale(amax)
+  };
+  __device__ static void finish(const Params&, EpiState& es) {
+    if ((es.ep_tid & 127) == 0) bulk_wait<0>();
+  }
+  template <int BN, int NCG>
+  __device__ static void apply(const Params& p, int mt, int nt, int row, uint32_t taddr,
+                               EpiState& es, int cg) {
+    static_assert(NCG == 1 || NCG == 2, "column groups");
+    const int bar = 1 + 2 * cg;
+    const bool leader = (es.ep_tid & 127) == 0;
+    const int t = mt * BM + row;
+    const bool valid = t < p.T;
+    const int sl = valid ? __ldg(p.slot + t) : -1;
+    if (valid && nt == 0 && static_cast<unsigned>(sl) >= static_cast<unsigned>(p.C))
+      set_status(p.status, SS_ERR_INDEX);
+    const float sig = e4m3_logit_scale(p.amax);
+    // 2^15 exp(s - lse) = 2^(s log2e - (lse log2e - 15))
+    const float off2 = valid ? fmaf(__ldg(p.lse + t), kLog2e, -static_cast<float>(kG8Exp)) : 0.f;
+    const float one_hot = static_cast<float>(1 << kG8Exp);
+    const int j0 = nt * BN;
+    const int ncols = min(BN, p.C - j0);
+    // this thread's byte in row jj of the transposed tile: 16-byte chunk
+    // (row / 16) ^ (jj % 8) of the 128-byte row, byte row % 16
+    uint32_t toff[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+      toff[k] = ((static_cast<uint32_t>(row >> 4) ^ static_cast<uint32_t>(k)) << 4) |
+                static_cast<uint32_t>(row & 15);
+    const uint32_t r64 = static_cast<uint32_t>((row >> 1) & 3);  // 64-byte swizzle of this row
+#pragma unroll 1
+    for (int q = cg * (BN / 64) / NCG; q < (cg + 1) * (BN / 64) / NCG; ++q) {
+      const int qc = q * 64;
+      if (qc >= ncols) break;  // uniform: depends on the tile only
+      constexpr uint32_t kBufs = 2 / NCG;
+      const uint32_t buf = es.stage + static_cast<uint32_t>(cg) * 16384u * kBufs +
+                           (es.rounds % kBufs) * 16384u;
+      const uint32_t rbuf = buf, tbuf = buf + 8192u;
+      if (es.rounds >= kBufs && leader) {
+        if constexpr (kBufs == 2) bulk_wait_read<1>();
+        else bulk_wait_read<0>();
+      }
+      named_bar_sync(bar, 128);
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int jc = qc + 32 * h;
+        if (jc >= ncols) break;
+        uint32_t r[32];
+        tmem_ld32(taddr + jc, r);
+        tmem_ld_wait();
+        const int off = sl - j0 - jc;
+        float g[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          g[i] = ex2_approx(fmaf(__uint_as_float(r[i]) * sig, kLog2e, -off2));
+        if (__any_sync(0xffffffffu, static_cast<unsigned>(off) < 32u)) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            if (i == off) g[i] -= one_hot;
+        }
+        uint16_t pr[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) pr[i] = e5m2x2(g[2 * i], g[2 * i + 1]);
+        // row-major tile: 32 bytes = 16-byte chunks 2h, 2h + 1 of this row
+#pragma unroll
+        for (int v = 0; v < 2; ++v) {
+          const uint32_t c = static_cast<uint32_t>(2 * h + v);
+          const uint16_t* w = pr + 8 * v;
+          st_shared_v4(rbuf + static_cast<uint32_t>(row) * 64u + ((c ^ r64) << 4),
+                       w[0] | (static_cast<uint32_t>(w[1]) << 16),
+                       w[2] | (static_cast<uint32_t>(w[3]) << 16),
+                       w[4] | (static_cast<uint32_t>(w[5]) << 16),
+                       w[6] | (static_cast<uint32_t>(w[7]) << 16));
+        }
+        // transposed tile: column jj = 32h + i is row jj of it
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const uint16_t b = (i & 1) ? static_cast<uint16_t>(pr[i >> 1] >> 8) : pr[i >> 1];
+          st_shared_u8(tbuf + static_cast<uint32_t>(32 * h + i) * 128u + toff[i & 7], b);
+        }
+      }
+      fence_proxy_async_smem();
+      named_bar_sync(bar, 128);
+      if (leader) {
+        const uint64_t pol = l2_evict_first();
+        tma_store_2d_hint(&p.tmG, rbuf, j0 + qc, mt * BM, pol);
+        tma_store_2d_hint(&p.tmGt, tbuf, mt * BM, j0 + qc, pol);
+        bulk_commit();
+      }
+      ++es.rounds;
+    }
+  }
+};
+
+// Backward, step 2: dH tile -> bf16 (column group cg of NCG). F8G: the
+// accumulator is of e5m2 G and e4m3 W_c, times fp8_grad_alpha.
+template <bool F8G = false>
+struct EpiDhT {
   static constexpr int kStageBytes = 0;
   static constexpr bool kKeepOperands = false;
   struct Params {
     int T, D;
     uint16_t* dH;
+    float scale;         // used when F8G
+    const float* amax;   // used when F8G: max |W_c|
   };
   __device__ static void finish(const Params&, EpiState&) {}
   template <int BN, int NCG>
@@ -374,26 +498,31 @@ struct EpiDh {
     const int ncols = min(CPG * 32, p.D - n0);
     if (ncols <= 0) return;
     uint16_t* drow = p.dH + static_cast<size_t>(valid ? t : 0) * p.D + n0;
+    float al = 1.f;
+    if constexpr (F8G) al = fp8_grad_alpha(p.scale, p.amax);
     for_tmem_chunks<CPG>(taddr, cg * CPG, [&](const uint32_t(&r)[32], int i) {
       const int jc = i * 32;
       if (jc >= ncols || !valid) return;
       uint4* dst = reinterpret_cast<uint4*>(drow + jc);
+      auto x = [&](int k) { return F8G ? __uint_as_float(r[k]) * al : __uint_as_float(r[k]); };
 #pragma unroll
       for (int v = 0; v < 4; ++v) {
-        const uint32_t q0 = pack_bf16x2(__uint_as_float(r[8 * v + 0]), __uint_as_float(r[8 * v + 1]));
-        const uint32_t q1 = pack_bf16x2(__uint_as_float(r[8 * v + 2]), __uint_as_float(r[8 * v + 3]));
-        const uint32_t q2 = pack_bf16x2(__uint_as_float(r[8 * v + 4]), __uint_as_float(r[8 * v + 5]));
-        const uint32_t q3 = pack_bf16x2(__uint_as_float(r[8 * v + 6]), __uint_as_float(r[8 * v + 7]));
+        const uint32_t q0 = pack_bf16x2(x(8 * v + 0), x(8 * v + 1));
+        const uint32_t q1 = pack_bf16x2(x(8 * v + 2), x(8 * v + 3));
+        const uint32_t q2 = pack_bf16x2(x(8 * v + 4), x(8 * v + 5));
+        const uint32_t q3 = pack_bf16x2(x(8 * v + 6), x(8 * v + 7));
         dst[v] = make_uint4(q0, q1, q2, q3);
       }
     });
   }
 };
+using EpiDh = EpiDhT<false>;
 
 // Backward, step 3: dW_c tile scattered into the owning rows dW[cand[j]]
 // (= or +=), column group cg of NCG. Candidate ids are distinct, so no two
-// threads write one row.
-struct EpiDw {
+// threads write one row. F8G: as for EpiDhT, with H's e4m3 exponent.
+template <bool F8G = false>
+struct EpiDwT {
   static constexpr int kStageBytes = 0;
   static constexpr bool kKeepOperands = false;
   struct Params {
@@ -401,6 +530,8 @@ struct EpiDw {
     const int32_t* cand;
     float* dW;
     int* status;
+    float scale;         // used when F8G
+    const float* amax;   // used when F8G: max |H|
   };
   __device__ static void finish(const Params&, EpiState&) {}
   template <int BN, int NCG>
@@ -418,14 +549,16 @@ struct EpiDw {
     const int ncols = min(CPG * 32, p.D - n0);
     if (ncols <= 0) return;
     float* drow = p.dW + static_cast<size_t>(valid ? v : 0) * p.D + n0;
+    float al = 1.f;
+    if constexpr (F8G) al = fp8_grad_alpha(p.scale, p.amax);
     for_tmem_chunks<CPG>(taddr, cg * CPG, [&](const uint32_t(&r)[32], int i) {
       const int jc = i * 32;
       if (jc >= ncols || !valid) return;
       float4* dst = reinterpret_cast<float4*>(drow + jc);
+      auto x = [&](int k) { return F8G ? __uint_as_float(r[k]) * al : __uint_as_float(r[k]); };
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
-        float4 o = make_float4(__uint_as_float(r[4 * k]), __uint_as_float(r[4 * k + 1]),
-                               __uint_as_float(r[4 * k + 2]), __uint_as_float(r[4 * k + 3]));
+        float4 o = make_float4(x(4 * k), x(4 * k + 1), x(4 * k + 2), x(4 * k + 3));
         if (p.accumulate) {
           const float4 old = dst[k];
           o.x += old.x;
@@ -438,6 +571,7 @@ struct EpiDw {
     });
   }
 };
+using EpiDw = EpiDwT<false>;
 
 // -------------------------------------------------------------------- kernel
 

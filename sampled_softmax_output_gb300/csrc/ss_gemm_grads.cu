@@ -1,8 +1,10 @@
 // ss_gemm_grads.cu -- the two gradient GEMMs of the backward pass:
 //   dH  = G . W_c          (M = T, N = D, K = C)
 //   dWc = G^T . H          (M = C, N = D, K = T), scattered into dW[cand].
-// G is read in place in both: K-major for dH, MN-major (transposed through the
-// MMA's operand descriptor) for dW, so no transposed copy is ever made.
+// bf16: G is read in place in both, K-major for dH and MN-major (transposed
+// through the MMA's operand descriptor) for dW, so no transposed copy is made.
+// FP8 gradients: e5m2 G and e4m3 H, W_c, all K-major (G8 and G8^T as the
+// softmax-gradient GEMM wrote them, H^T and W_c^T from the quantizer).
 #include <algorithm>
 #include <map>
 #include <memory>
@@ -57,10 +59,13 @@ struct GradSched {
   uint16_t units[kSchedMaxUnits];    // [0, n_dw): dW tiles, then dH tiles
 };
 
+template <bool F8G>
 struct GradBoth {
   int n_dw, n_nt, kb_dw, kb_dh;  // n_dw counts 256-row dW tiles (x column tiles)
-  EpiDh::Params dh;
-  EpiDw::Params dw;
+  int n_units;  // used when F8G: with rr, pair p runs units p, p + pairs, ... < n_units
+  int rr;
+  typename EpiDhT<F8G>::Params dh;
+  typename EpiDwT<F8G>::Params dw;
   int* status;
 };
 
@@ -70,14 +75,19 @@ using LG2 = Gemm2Smem<kBnGrad, kStagesPairGrad, 0>;
 
 // Both gradient GEMMs on CTA pairs (see ss_gemm2.cuh for the pair protocol):
 // pair p runs the 256-row tiles sch.units[sch.offs[p] .. sch.offs[p + 1]).
+// Operand maps: dH tiles read A from tmAh and B from tmBh, dW tiles A from
+// tmAw and B from tmBw. bf16: G (K-major), W_c (MN-major), G (MN-major), H
+// (MN-major). F8G: G8, W8^T, G8^T, H8^T, all K-major, 128 of K per k-block.
+template <bool F8G>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * kGradEpiWarps, 1)
-    k_grads(const __grid_constant__ CUtensorMap tmGk, const __grid_constant__ CUtensorMap tmWcMn,
-            const __grid_constant__ CUtensorMap tmGmn, const __grid_constant__ CUtensorMap tmHmn,
-            const __grid_constant__ GradBoth p, const __grid_constant__ GradSched sch) {
+    k_grads(const __grid_constant__ CUtensorMap tmAh, const __grid_constant__ CUtensorMap tmBh,
+            const __grid_constant__ CUtensorMap tmAw, const __grid_constant__ CUtensorMap tmBw,
+            const __grid_constant__ GradBoth<F8G> p, const __grid_constant__ GradSched sch) {
   pdl_enter();
   constexpr int BN = kBnGrad;
   constexpr int STAGES = kStagesPairGrad;
   constexpr int NCG = kGradEpiWarps / 4;
+  constexpr int KB = F8G ? 2 * BK : BK;  // elements of K per k-block
   using L = LG2;
   extern __shared__ uint8_t smem_raw[];
   __shared__ int s_go;
@@ -89,7 +99,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * kGradEpiWa
   const uint32_t rank = cluster_ctarank();
   const int pair = blockIdx.x >> 1;
   int* status = p.status;
-  const int u_begin = sch.offs[pair], u_end = sch.offs[pair + 1];
+  // this pair's units: i = u_begin, u_begin + u_step, ... < u_end; unit(i)
+  const bool rr = F8G && p.rr != 0;
+  const int u_begin = rr ? pair : sch.offs[pair];
+  const int u_end = rr ? p.n_units : sch.offs[pair + 1];
+  const int u_step = rr ? static_cast<int>(gridDim.x >> 1) : 1;
+  auto unit = [&](int i) { return rr ? i : static_cast<int>(sch.units[i]); };
 
   if (threadIdx.x == 0) s_go = (read_status(status) == 0);
   cluster_sync_all();
@@ -108,10 +123,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * kGradEpiWa
     mbar_init(&ctrl->drain, 1);
     ctrl->abort_flag = 0;
     fence_mbar_init();
-    tma_prefetch_map(&tmGk);
-    tma_prefetch_map(&tmWcMn);
-    tma_prefetch_map(&tmGmn);
-    tma_prefetch_map(&tmHmn);
+    tma_prefetch_map(&tmAh);
+    tma_prefetch_map(&tmBh);
+    tma_prefetch_map(&tmAw);
+    tma_prefetch_map(&tmBw);
   }
   if (warp == 1) {
     tmem_alloc_pair(&ctrl->tmem_base, 2 * BN);
@@ -129,8 +144,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * kGradEpiWa
       int s = 0;
       uint32_t ph = 0, issued = 0, issued_ph = 0;
       bool ok = true;
-      for (int i = u_begin; ok && i < u_end; ++i) {
-        const int u = sch.units[i];
+      for (int i = u_begin; ok && i < u_end; i += u_step) {
+        const int u = unit(i);
         const bool is_dw = u < p.n_dw;
         const int v = is_dw ? u : u - p.n_dw;
         const int mt = v / p.n_nt, nt = v % p.n_nt;
@@ -149,15 +164,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * kGradEpiWa
           const uint32_t b_dst = a_dst + L::A_BYTES;
           // B (H or W_c) is re-read by every row tile: keep it in L2
           const uint64_t keep = l2_evict_last();
-          if (is_dw) {  // A = G columns (MN-major), B = H (MN-major); K = tokens
-            tma_load_2d_pair(a_dst, &tmGmn, fb, m0, kb * BK);
-            tma_load_2d_pair(a_dst + 8192, &tmGmn, fb, m0 + 64, kb * BK);
-            tma_load_2d_pair_hint(b_dst, &tmHmn, fb, n0, kb * BK, keep);
-            tma_load_2d_pair_hint(b_dst + 8192, &tmHmn, fb, n0 + 64, kb * BK, keep);
+          if constexpr (F8G) {  // one 128 x 128-byte box of A and of B, K-major
+            const CUtensorMap* ma = is_dw ? &tmAw : &tmAh;
+            const CUtensorMap* mb = is_dw ? &tmBw : &tmBh;
+            tma_load_2d_pair(a_dst, ma, fb, kb * KB, m0);
+            tma_load_2d_pair_hint(b_dst, mb, fb, kb * KB, n0, keep);
+          } else if (is_dw) {  // A = G columns (MN-major), B = H (MN-major); K = tokens
+            tma_load_2d_pair(a_dst, &tmAw, fb, m0, kb * BK);
+            tma_load_2d_pair(a_dst + 8192, &tmAw, fb, m0 + 64, kb * BK);
+            tma_load_2d_pair_hint(b_dst, &tmBw, fb, n0, kb * BK, keep);
+            tma_load_2d_pair_hint(b_dst + 8192, &tmBw, fb, n0 + 64, kb * BK, keep);
           } else {      // A = G rows (K-major), B = W_c (MN-major); K = candidates
-            tma_load_2d_pair(a_dst, &tmGk, fb, kb * BK, m0);
-            tma_load_2d_pair_hint(b_dst, &tmWcMn, fb, n0, kb * BK, keep);
-            tma_load_2d_pair_hint(b_dst + 8192, &tmWcMn, fb, n0 + 64, kb * BK, keep);
+            tma_load_2d_pair(a_dst, &tmAh, fb, kb * BK, m0);
+            tma_load_2d_pair_hint(b_dst, &tmBh, fb, n0, kb * BK, keep);
+            tma_load_2d_pair_hint(b_dst + 8192, &tmBh, fb, n0 + 64, kb * BK, keep);
           }
           issued |= 1u << s;
           issued_ph = (issued_ph & ~(1u << s)) | (ph << s);
@@ -182,11 +202,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * kGradEpiWa
     if (lane == 0 && rank == 0) {
       constexpr uint32_t idesc_dw = idesc_bf16_f32(2 * BM, BN, true, true);
       constexpr uint32_t idesc_dh = idesc_bf16_f32(2 * BM, BN, false, true);
+      constexpr uint32_t idesc_f8 = idesc_f8_f32(2 * BM, BN, kFmtE5M2, kFmtE4M3);
       int s = 0, b = 0;
       uint32_t ph = 0, aph = 0;
       bool ok = true;
-      for (int i = u_begin; ok && i < u_end; ++i) {
-        const bool is_dw = sch.units[i] < p.n_dw;
+      for (int i = u_begin; ok && i < u_end; i += u_step) {
+        const bool is_dw = unit(i) < p.n_dw;
         const int kbs = is_dw ? p.kb_dw : p.kb_dh;
         if (!mbar_wait(&ctrl->tempty[b], aph ^ 1u, abort_flag, status)) break;
         tc_fence_after();
@@ -201,10 +222,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * kGradEpiWa
           const uint32_t b_addr = a_addr + L::A_BYTES;
 #pragma unroll
           for (int k = 0; k < BK / UMMA_K; ++k) {
-            const uint64_t ad = is_dw ? sdesc_sw128(a_addr + k * 2048, 8192, 1024)
-                                      : sdesc_sw128(a_addr + k * 32, 16, 1024);
-            const uint64_t bd = sdesc_sw128(b_addr + k * 2048, 8192, 1024);
-            mma_bf16_pair(d_tmem, ad, bd, is_dw ? idesc_dw : idesc_dh, (kb | k) != 0 ? 1u : 0u);
+            if constexpr (F8G) {  // K = 32 e5m2 / e4m3 per instruction: 32 bytes along K
+              const uint64_t ad = sdesc_sw128(a_addr + k * 32, 16, 1024);
+              const uint64_t bd = sdesc_sw128(b_addr + k * 32, 16, 1024);
+              mma_f8_pair(d_tmem, ad, bd, idesc_f8, (kb | k) != 0 ? 1u : 0u);
+            } else {
+              const uint64_t ad = is_dw ? sdesc_sw128(a_addr + k * 2048, 8192, 1024)
+                                        : sdesc_sw128(a_addr + k * 32, 16, 1024);
+              const uint64_t bd = sdesc_sw128(b_addr + k * 2048, 8192, 1024);
+              mma_bf16_pair(d_tmem, ad, bd, is_dw ? idesc_dw : idesc_dh,
+                            (kb | k) != 0 ? 1u : 0u);
+            }
           }
           mma_commit_pair(&ctrl->empty[s], 0x3);
           if (++s == STAGES) {
@@ -232,17 +260,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * kGradEpiWa
     EpiState es{0u, 0, 0u};
     int b = 0;
     uint32_t aph = 0;
-    for (int i = u_begin; i < u_end; ++i) {
+    for (int i = u_begin; i < u_end; i += u_step) {
       const bool ok = mbar_wait(&ctrl->tfull[b], aph, abort_flag, status);
       if (!__all_sync(0xffffffffu, ok)) break;
       tc_fence_after();
-      const int u = sch.units[i];
+      const int u = unit(i);
       const bool is_dw = u < p.n_dw;
       const int v = is_dw ? u : u - p.n_dw;
       const int mt = (v / p.n_nt) * 2 + static_cast<int>(rank), nt = v % p.n_nt;
       const uint32_t taddr = lane_addr + static_cast<uint32_t>(b * BN);
-      if (is_dw) EpiDw::template apply<BN, NCG>(p.dw, mt, nt, row, taddr, es, cg);
-      else EpiDh::template apply<BN, NCG>(p.dh, mt, nt, row, taddr, es, cg);
+      if (is_dw) EpiDwT<F8G>::template apply<BN, NCG>(p.dw, mt, nt, row, taddr, es, cg);
+      else EpiDhT<F8G>::template apply<BN, NCG>(p.dh, mt, nt, row, taddr, es, cg);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
@@ -408,12 +436,14 @@ cudaError_t launch_grads(const CUtensorMap& tG_kmaj, const CUtensorMap& tWc_mn,
                          const CUtensorMap& tG_mn, const CUtensorMap& tH_mn, int T, int C, int D,
                          int V, int accumulate, const int32_t* cand, uint16_t* dH, float* dW,
                          int* status, int num_sms, cudaStream_t stream) {
-  GradBoth p;
+  GradBoth<false> p;
   p.n_nt = (D + kBnGrad - 1) / kBnGrad;
   p.n_dw = (C + 2 * BM - 1) / (2 * BM) * p.n_nt;
   const int n_dh = (T + 2 * BM - 1) / (2 * BM) * p.n_nt;
   p.kb_dw = (T + BK - 1) / BK;
   p.kb_dh = (C + BK - 1) / BK;
+  p.n_units = 0;
+  p.rr = 0;
   p.dh = EpiDh::Params{T, D, dH};
   p.dw = EpiDw::Params{C, D, V, accumulate, cand, dW, status};
   p.status = status;
@@ -430,8 +460,34 @@ cudaError_t launch_grads(const CUtensorMap& tG_kmaj, const CUtensorMap& tWc_mn,
     if (e != cudaSuccess) return e;
     return launch_grad_w(tG_mn, tH_mn, T, C, D, V, accumulate, cand, dW, status, num_sms, stream);
   }
-  return launch_pdl(k_grads, dim3(2 * pairs), dim3(64 + 32 * kGradEpiWarps), LG2::TOTAL, stream,
-                    tG_kmaj, tWc_mn, tG_mn, tH_mn, p, *sch);
+  return launch_pdl(k_grads<false>, dim3(2 * pairs), dim3(64 + 32 * kGradEpiWarps), LG2::TOTAL,
+                    stream, tG_kmaj, tWc_mn, tG_mn, tH_mn, p, *sch);
+}
+
+cudaError_t launch_grads_fp8(const CUtensorMap& tG8, const CUtensorMap& tW8t,
+                             const CUtensorMap& tG8t, const CUtensorMap& tH8t, int T, int C, int D,
+                             int V, int accumulate, const int32_t* cand, float scale,
+                             const float* amax, uint16_t* dH, float* dW, int* status, int num_sms,
+                             cudaStream_t stream) {
+  constexpr int KB = 2 * BK;
+  GradBoth<true> p;
+  p.n_nt = (D + kBnGrad - 1) / kBnGrad;
+  p.n_dw = (C + 2 * BM - 1) / (2 * BM) * p.n_nt;
+  const int n_dh = (T + 2 * BM - 1) / (2 * BM) * p.n_nt;
+  p.kb_dw = (T + KB - 1) / KB;
+  p.kb_dh = (C + KB - 1) / KB;
+  p.n_units = p.n_dw + n_dh;
+  p.dh = EpiDhT<true>::Params{T, D, dH, scale, amax + 1};
+  p.dw = EpiDwT<true>::Params{C, D, V, accumulate, cand, dW, status, scale, amax};
+  p.status = status;
+  const int pairs = std::min(num_sms / 2, kSchedMaxCtas);
+  // the balanced schedule where it fits the kernel parameters, else every
+  // pair walks the units round-robin (dW tiles first)
+  auto sch = grad_schedule(p.n_dw, p.kb_dw, n_dh, p.kb_dh, pairs);
+  static const GradSched kNone = {};
+  p.rr = sch ? 0 : 1;
+  return launch_pdl(k_grads<true>, dim3(2 * pairs), dim3(64 + 32 * kGradEpiWarps), LG2::TOTAL,
+                    stream, tG8, tW8t, tG8t, tH8t, p, sch ? *sch : kNone);
 }
 
 }  // namespace ss

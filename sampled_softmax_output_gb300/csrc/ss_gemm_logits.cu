@@ -45,4 +45,25 @@ cudaError_t launch_softmax_grad(const CUtensorMap& tH, const CUtensorMap& tWc,
                                             scale, h, tg, nullptr, status, num_sms, stream);
 }
 
+// FP8 gradients: G8 and G8^T in e5m2 from the e4m3 logits (one target, plain head)
+cudaError_t launch_softmax_grad_fp8(const CUtensorMap& tH8, const CUtensorMap& tW8,
+                                    const CUtensorMap& tG8_store, const CUtensorMap& tG8t_store,
+                                    int T, int C, int D, const int32_t* slot, const float* lse,
+                                    const float* amax, int* status, int num_sms,
+                                    cudaStream_t stream) {
+  EpiG8::Params ep;
+  ep.tmG = tG8_store;
+  ep.tmGt = tG8t_store;
+  ep.T = T;
+  ep.C = C;
+  ep.slot = slot;
+  ep.lse = lse;
+  ep.status = status;
+  ep.amax = amax;
+  GemmShape shp{(T + BM - 1) / BM, (C + kBnLogits - 1) / kBnLogits, D / (2 * BK)};
+  return launch_gemm<kBnLogits, kStagesLogits, false, false, EpiG8, 8, true>(tH8, tW8, shp, ep,
+                                                                             status, num_sms,
+                                                                             stream);
+}
+
 }  // namespace ss

@@ -213,6 +213,11 @@ __device__ __forceinline__ void st_shared_b16(uint32_t addr, uint16_t v) {
   asm volatile("st.shared.b16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
 }
 
+// the low byte of v
+__device__ __forceinline__ void st_shared_u8(uint32_t addr, uint16_t v) {
+  asm volatile("st.shared.u8 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
+}
+
 // ------------------------------------------------------------------- tcgen05
 
 __device__ __forceinline__ void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {
@@ -336,6 +341,14 @@ __host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N) {
   return (1u << 4) | (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
 }
 
+// kind::f8f6f4 with A and B formats of their own (bits 7-9 and 10-12:
+// 0 = E4M3, 1 = E5M2), fp32 D, K-major operands.
+constexpr uint32_t kFmtE4M3 = 0u, kFmtE5M2 = 1u;
+__host__ __device__ constexpr uint32_t idesc_f8_f32(int M, int N, uint32_t a_fmt, uint32_t b_fmt) {
+  return (1u << 4) | (a_fmt << 7) | (b_fmt << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
+         (static_cast<uint32_t>(M >> 4) << 24);
+}
+
 // The FP8 head: operands scaled by 2^e per tensor, e the largest integer with
 // amax * 2^e <= 448 (the e4m3 range), so logits = accumulator * 2^-(eH + eW).
 __device__ __forceinline__ int e4m3_exponent(float amax) {
@@ -362,6 +375,13 @@ __device__ __forceinline__ uint32_t bf16x8_absmax_bits(uint4 v) {
 __device__ __forceinline__ uint16_t e4m3x2(float lo, float hi) {
   uint16_t r;
   asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+// Two floats to two e5m2 codes (round to nearest, ties to even, saturating
+// at +-57344): lo -> bits 0-7, hi -> bits 8-15.
+__device__ __forceinline__ uint16_t e5m2x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e5m2x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
   return r;
 }
 // Two e4m3 codes back to two halves (exact): bits 0-7 -> low half.
@@ -454,6 +474,17 @@ __device__ __forceinline__ void mma_bf16_pair(uint32_t d_tmem, uint64_t adesc, u
       "{\n\t.reg .pred p;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// The same on 8-bit operands (kind::f8f6f4, formats in idesc): K = 32.
+__device__ __forceinline__ void mma_f8_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                            uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
 }

@@ -264,7 +264,7 @@ def test_several_targets_argument_errors():
 
 def test_fp8_head_argument_errors():
     """The FP8 head needs plain logits (cap 0) and D % 128 == 0; the
-    several-targets entry points have no FP8 path; fp8 must be 0 or 1."""
+    several-targets entry points have no FP8 path; fp8 must be 0, 1 or 2."""
     L = ss.lib()
 
     def step(head, D=768, T=256):  # a workspace too small: accepted arguments say so
@@ -275,7 +275,11 @@ def test_fp8_head_argument_errors():
     assert step(ctypes.byref(ss.Head(0.0, 1.0, 1))) == WORKSPACE       # the FP8 head is accepted
     assert step(ctypes.byref(ss.Head(30.0, 7.5, 1))) == UNSUPPORTED    # cap with FP8
     assert step(ctypes.byref(ss.Head(0.0, 1.0, 1)), D=192) == UNSUPPORTED
-    assert step(ctypes.byref(ss.Head(0.0, 1.0, 2))) == INVALID
+    assert step(ctypes.byref(ss.Head(0.0, 1.0, 2))) == WORKSPACE       # FP8 gradients too
+    assert step(ctypes.byref(ss.Head(30.0, 7.5, 2))) == UNSUPPORTED
+    assert step(ctypes.byref(ss.Head(0.0, 1.0, 2)), D=192) == UNSUPPORTED
+    assert step(ctypes.byref(ss.Head(0.0, 1.0, 3))) == INVALID
+    assert step(ctypes.byref(ss.Head(0.0, 1.0, -1))) == INVALID
     w = (ctypes.c_float * 1)(1.0)
     assert L.ss_step_mtp(p(FAKE), 1, w, p(FAKE), p(FAKE), 0, 50304, 4096, 768, 0,
                          ctypes.byref(ss.Head(0.0, 1.0, 1)), 1.0, 0, p(FAKE), p(FAKE), p(FAKE),

@@ -3,8 +3,11 @@ README, technique list: FP8 for the head).
 
 H and the candidate rows W_c are each scaled by 2^e (e the largest integer
 with max|x| 2^e <= 448), rounded to e4m3 and used in that form by both logit
-GEMMs (tcgen05 kind::f8f6f4); the gradient GEMMs use the same rounded operands
-in bf16. The oracle is the plain definition on the rounded operands.
+GEMMs (tcgen05 kind::f8f6f4). fp8 = 1: the gradient GEMMs use the same rounded
+operands in bf16, and the oracle is the plain definition on the rounded
+operands. fp8 = 2 (FP8 through the backward pass, the record page): G is
+scaled by 2^15 and rounded to e5m2, and the gradient GEMMs run on e5m2 x e4m3;
+the oracle rounds G the same way.
 """
 import numpy as np
 import pytest
@@ -46,16 +49,17 @@ CASES = [
 ]
 
 
+@pytest.mark.parametrize("mode", [1, 2])
 @pytest.mark.parametrize("T,V,D,C,seed,scale", CASES)
-def test_fp8_head_parity(orc, T, V, D, C, seed, scale):
+def test_fp8_head_parity(orc, T, V, D, C, seed, scale, mode):
     x = synth.make_inputs(T, V, D, 1.1, seed)
     C = max(C, len(np.unique(x["targets"])))
-    ref = orc.loss_and_grads_fp8(x["H"], x["W"], x["targets"], C, seed, scale)
+    ref = orc.loss_and_grads_fp8(x["H"], x["W"], x["targets"], C, seed, scale, grads=mode == 2)
     H, W = to_dev_bf16(x["H"]), to_dev_bf16(x["W"])
     tg = torch.from_numpy(x["targets"]).cuda()
     ws = ss.workspace(T, V, C, D)
-    got = ss.step(H, W, tg, C, seed, ws, scale=scale, fp8=True)
-    sep = ss.step_separate(H, W, tg, C, seed, ss.workspace(T, V, C, D), scale=scale, fp8=True)
+    got = ss.step(H, W, tg, C, seed, ws, scale=scale, fp8=mode)
+    sep = ss.step_separate(H, W, tg, C, seed, ss.workspace(T, V, C, D), scale=scale, fp8=mode)
     torch.cuda.synchronize()
     assert ss.read_status(ws)[0] == 0
     for k in ("cand", "slot", "loss", "lse", "dH", "dW"):
@@ -70,7 +74,30 @@ def test_fp8_head_parity(orc, T, V, D, C, seed, scale):
         assert np.abs(plain["loss"] - ref["loss"]).max() > 1e-4
 
 
-def test_fp8_head_full_size(orc):
+def test_fp8_gradients_accumulate_and_scale_sign(orc):
+    """FP8 gradients with accumulate = 1 into a non-zero dW and a negative
+    scale: dW rows += the oracle's e5m2-gradient rows, other rows untouched."""
+    T, V, D, C, seed, scale = 300, 3000, 256, 700, 8, -0.25
+    x = synth.make_inputs(T, V, D, 1.1, seed)
+    C = max(C, len(np.unique(x["targets"])))
+    dW0 = np.random.default_rng(9).standard_normal((V, D)).astype(np.float32)
+    ref = orc.loss_and_grads_fp8(x["H"], x["W"], x["targets"], C, seed, scale, dW_init=dW0,
+                                 accumulate=True, grads=True)
+    H, W = to_dev_bf16(x["H"]), to_dev_bf16(x["W"])
+    tg = torch.from_numpy(x["targets"]).cuda()
+    dW = torch.from_numpy(dW0).cuda()
+    ws = ss.workspace(T, V, C, D)
+    got = ss.step(H, W, tg, C, seed, ws, scale=scale, fp8=2, accumulate=True, dW=dW)
+    torch.cuda.synchronize()
+    assert ss.read_status(ws)[0] == 0
+    other = np.setdiff1d(np.arange(V), ref["cand"])
+    np.testing.assert_array_equal(got["dW"].cpu().numpy()[other], dW0[other])
+    assert rel_fro(got["dW"].cpu().numpy()[ref["cand"]] - dW0[ref["cand"]], ref["dWc"]) < GRAD_RTOL
+    assert rel_fro(got["dH"].float().cpu().numpy(), ref["dH"]) < GRAD_RTOL
+
+
+@pytest.mark.parametrize("mode", [1, 2])
+def test_fp8_head_full_size(orc, mode):
     """T16384_C10240 with the FP8 head: cand bit-exact, sampled token rows of
     loss, lse and dH, and exact candidate rows of dW, against the oracle."""
     w = synth.WORKLOADS[2]
@@ -79,7 +106,7 @@ def test_fp8_head_full_size(orc):
     tg = torch.from_numpy(x["targets"]).cuda()
     ws = ss.workspace(w.T, w.V, w.C, w.D)
     scale = 1.0 / w.T
-    got = ss.step(H, W, tg, w.C, w.seed, ws, scale=scale, fp8=True)
+    got = ss.step(H, W, tg, w.C, w.seed, ws, scale=scale, fp8=mode)
     torch.cuda.synchronize()
     assert ss.read_status(ws)[0] == 0
     cand, slot, _ = orc.build_candidates(x["targets"], w.V, w.C, w.seed)
@@ -90,9 +117,11 @@ def test_fp8_head_full_size(orc):
     l_ref, s_ref = orc.forward(Hq, Wq, cand, slot, rows=rows)
     assert_loss_close(got["loss"].cpu().numpy()[rows], l_ref)
     assert_loss_close(got["lse"].cpu().numpy()[rows], s_ref)
-    dH_ref = orc.backward_dH(Hq, Wq, cand, slot, s_ref, scale, rows=rows)
+    dH_fn = orc.backward_dH_g8 if mode == 2 else orc.backward_dH
+    dH_ref = dH_fn(Hq, Wq, cand, slot, s_ref, scale, rows=rows)
     assert rel_fro(got["dH"].float().cpu().numpy()[rows], dH_ref) < GRAD_RTOL
     _, lse_all = orc.forward(Hq, Wq, cand, slot)
     cols = np.array([0, 1, w.C // 2, w.C - 1])
-    ref_rows = orc.backward_dWc(Hq, Wq, cand, slot, lse_all, scale, cols=cols)
+    dW_fn = orc.backward_dWc_g8 if mode == 2 else orc.backward_dWc
+    ref_rows = dW_fn(Hq, Wq, cand, slot, lse_all, scale, cols=cols)
     assert rel_fro(got["dW"].cpu().numpy()[cand[cols]], ref_rows) < GRAD_RTOL

@@ -384,6 +384,16 @@ MUTATIONS = [
     ("negatives left in key order", "qsort(neg, (size_t)k, sizeof(int32_t), cmp_i32);", ""),
     ("targets not deduplicated", "if (U == 0 || u[U - 1] != u[i]) u[U++] = u[i];", "u[U++] = u[i];"),
     ("wrong hash constant", "0xBF58476D1CE4E5B9ull", "0xBF58476D1CE4E5B8ull"),
+    ("FP8 head: e4m3 grid one bit too fine", "const float q = ldexpf(1.0f, E - 3);",
+     "const float q = ldexpf(1.0f, E - 4);"),
+    ("FP8 head: scale exponent one too large", "return m <= 0.875f ? 9 - k : 8 - k;",
+     "return m <= 0.875f ? 10 - k : 9 - k;"),
+    ("FP8 gradients: e5m2 grid one bit too fine", "const float q = ldexpf(1.0f, E - 2);",
+     "const float q = ldexpf(1.0f, E - 3);"),
+    ("FP8 gradients: G not rounded", "return orc_round_e5m2(ldexpf(expf(s - lse) - y, 15));",
+     "return ldexpf(expf(s - lse) - y, 15);"),
+    ("FP8 gradients: wrong power-of-two scale", "const float f = ldexpf(scale, -15);\n#pragma omp parallel\n",
+     "const float f = ldexpf(scale, -14);\n#pragma omp parallel\n"),
 ]
 
 
@@ -432,6 +442,14 @@ def _battery(orc):
     except Exception:
         bad = ["mtp crashed"]
     failed += bad
+    # the FP8 roundings against torch's float8 conversions, and the closed form
+    # of the FP8 gradients at H = 0
+    if _fp8_rounding_mismatch(orc, 2000):
+        failed.append("fp8 rounding")
+    if _e4m3_exponent_mismatch(orc):
+        failed.append("e4m3 scale exponent")
+    if _fp8_grad_closed_form_mismatch(orc):
+        failed.append("fp8 gradients")
     return failed
 
 
@@ -689,13 +707,114 @@ def test_e4m3_grid_is_fixed_and_ties_go_to_even(orc):
     assert orc.round_e4m3(1000.0) == 448.0 and orc.round_e4m3(-449.0) == -448.0
 
 
-def test_e4m3_scale_exponent_is_the_largest_that_fits(orc):
+def _e4m3_exponent_mismatch(orc):
     rng = np.random.default_rng(21)
     for amax in np.concatenate([np.exp2(rng.uniform(-20, 20, 2000)), [448.0, 224.0, 1.0, 0.875]]):
         amax = float(np.float32(amax))
         e = orc.e4m3_scale_exponent(amax)
-        assert amax * 2.0 ** e <= 448.0 < amax * 2.0 ** (e + 1), amax
-    assert orc.e4m3_scale_exponent(0.0) == 0
+        if not amax * 2.0 ** e <= 448.0 < amax * 2.0 ** (e + 1):
+            return True
+    return orc.e4m3_scale_exponent(0.0) != 0
+
+
+def test_e4m3_scale_exponent_is_the_largest_that_fits(orc):
+    assert not _e4m3_exponent_mismatch(orc)
+
+
+def _float8_grid(dtype):
+    grid = torch.arange(256, dtype=torch.int32).to(torch.uint8).view(dtype).float()
+    return np.unique(grid[torch.isfinite(grid)].numpy().astype(np.float32))
+
+
+def _fp8_rounding_mismatch(orc, n):
+    """Both roundings against torch's float8 conversions (round to nearest,
+    ties to even) over every binade, the grid points and their midpoints."""
+    rng = np.random.default_rng(23)
+    for dt, top, fn, lo in ((torch.float8_e4m3fn, 448.0, orc.round_e4m3, -12),
+                            (torch.float8_e5m2, 57344.0, orc.round_e5m2, -19)):
+        mags = np.exp2(rng.uniform(lo, np.log2(top), n)).astype(np.float32)
+        x = (mags * rng.choice([-1, 1], mags.size)).astype(np.float32)
+        grid = _float8_grid(dt)
+        mids = ((grid[1:] + grid[:-1]) / 2).astype(np.float32)
+        x = np.concatenate([x, grid, mids]).astype(np.float32)
+        x = x[np.abs(x) < top]
+        ref = torch.from_numpy(x).to(dt).float().numpy()
+        got = np.array([fn(float(v)) for v in x], np.float32)
+        if not np.array_equal(got, ref):
+            return True
+    return False
+
+
+def test_e5m2_rounding_against_torch(orc):
+    assert not _fp8_rounding_mismatch(orc, 20000)
+
+
+def test_e5m2_grid_is_fixed_and_ties_go_to_even(orc):
+    grid = _float8_grid(torch.float8_e5m2)
+    assert grid.size == 247 and grid.max() == 57344.0 and grid[grid > 0].min() == 2.0 ** -16
+    for v in grid:
+        assert orc.round_e5m2(float(v)) == v
+    codes = torch.from_numpy(grid).to(torch.float8_e5m2).view(torch.uint8).numpy()
+    for a, b, ca, cb in zip(grid[:-1], grid[1:], codes[:-1], codes[1:]):
+        if a < 0 or b <= 0:
+            continue
+        even = a if int(ca) % 2 == 0 else b
+        assert orc.round_e5m2(float((a + b) / 2)) == even, (a, b)
+    assert orc.round_e5m2(1e6) == 57344.0 and orc.round_e5m2(-60000.0) == -57344.0
+
+
+def _fp8_grad_closed_form_mismatch(orc):
+    """FP8 gradients at H = 0 with C = 32: every logit is 0, P = 1/32, so
+    2^15 P = 1024 is on the e5m2 grid while the target entry 2^15 (1/32 - 1)
+    = -31744 rounds to -32768 (spacing 4096 in that binade, not a tie):
+    dH[t] = scale (sum_j W_q[cand[j]] / 32 - (33/32) W_q[y_t]) and dW = 0,
+    where the exact-G gradient would have (32/32) W_q[y_t]."""
+    T, V, D, C, seed, scale = 4, 64, 16, 32, 33, 0.75
+    x = synth.make_inputs(T, V, D, 1.1, seed)
+    H0 = np.zeros_like(x["H"])
+    r = orc.loss_and_grads_fp8(H0, x["W"], x["targets"], C, seed, scale, grads=True)
+    Wq = synth.bf16_bits_to_f32(orc.fp8_inputs(H0, x["W"], r["cand"])[1]).astype(np.float64)
+    Wc = Wq[r["cand"]]
+    y = Wq[x["targets"]]
+    expect = scale * (Wc.sum(0)[None, :] / 32.0 - (33.0 / 32.0) * y)
+    plain = scale * (Wc.sum(0)[None, :] / 32.0 - y)
+    bad = not np.allclose(r["dH"], expect, rtol=1e-5, atol=1e-7)
+    bad |= np.allclose(r["dH"], plain, rtol=1e-5, atol=1e-7)
+    bad |= bool(np.any(r["dW"] != 0))
+    bad |= not np.allclose(r["loss"], np.log(32.0), rtol=1e-6)
+    return bad
+
+
+def test_fp8_gradients_closed_form_at_zero_H(orc):
+    assert not _fp8_grad_closed_form_mismatch(orc)
+
+
+def test_fp8_gradients_within_the_e5m2_rounding_bound(orc):
+    """On ordinary inputs the FP8-gradient dH and dW_c differ from the
+    exact-G gradients on the same rounded operands by no more than the e5m2
+    rounding bound: half a unit in the last place (2^-3 relative for normals,
+    2^-17 absolute below 2^-14) of every G8 entry, scaled back, times the
+    operand (plus fp32 slack); and they do differ."""
+    T, V, D, C, seed, scale = 24, 300, 32, 80, 34, 0.5
+    x, C = _case(T, V, D, C, seed)
+    a = orc.loss_and_grads_fp8(x["H"], x["W"], x["targets"], C, seed, scale, grads=True)
+    b = orc.loss_and_grads_fp8(x["H"], x["W"], x["targets"], C, seed, scale, grads=False)
+    cand, slot = a["cand"], a["slot"]
+    Hq, Wq, _, _ = orc.fp8_inputs(x["H"], x["W"], cand)
+    H64 = synth.bf16_bits_to_f32(Hq).astype(np.float64)
+    Wc64 = synth.bf16_bits_to_f32(Wq[cand]).astype(np.float64)
+    S = H64 @ Wc64.T
+    P = np.exp(S - a["lse"].astype(np.float64)[:, None])
+    G = P.copy()
+    G[np.arange(T), slot] -= 1.0
+    err = 2.0 ** -3 * np.abs(G) + 2.0 ** -32  # per entry, in units of G
+    slack = 1e-5
+    bH = abs(scale) * ((err + slack * np.abs(G)) @ np.abs(Wc64))
+    bW = abs(scale) * ((err + slack * np.abs(G)).T @ np.abs(H64))
+    assert np.all(np.abs(a["dH"] - b["dH"]) <= bH + 1e-9)
+    assert np.all(np.abs(a["dWc"] - b["dWc"]) <= bW + 1e-9)
+    assert not np.array_equal(a["dH"], b["dH"])
+    np.testing.assert_array_equal(a["loss"], b["loss"])
 
 
 def test_fp8_head_is_the_plain_loss_on_grid_inputs(orc):
