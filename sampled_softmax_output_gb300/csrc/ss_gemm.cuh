@@ -152,6 +152,11 @@ struct EpiFwdT {
     uint32_t has_t = 0u;  // bit k: target k lies in this group's columns
     float sig = 1.f;
     if constexpr (F8) sig = e4m3_logit_scale(p.amax);
+    // Plain head: v holds the raw accumulator and the logit is v * vs (the
+    // FP8 scale is a power of two, so it commutes exactly with the max and
+    // folds into the exponent's constant); capped head: v = z, vs = 1.
+    const float vs = CAP ? 1.f : sig;
+    const float k2 = vs * kLog2e;
     if (ncols > 0) {  // uniform: depends on the tile only
       for_tmem_chunks<CPG>(taddr, cg * CPG, [&](const uint32_t(&r)[32], int i) {
         const int jc = i * 32;
@@ -160,22 +165,37 @@ struct EpiFwdT {
         float v[32];
 #pragma unroll
         for (int k = 0; k < 32; ++k) {
-          const float acc = F8 ? __uint_as_float(r[k]) * sig : __uint_as_float(r[k]);
-          v[k] = CAP ? head_z(acc, p.head) : acc;
+          const float acc = __uint_as_float(r[k]);
+          v[k] = CAP ? head_z(F8 ? acc * sig : acc, p.head) : acc;
         }
         float cm = -INFINITY;
-#pragma unroll
-        for (int k = 0; k < 32; ++k)
-          if (k < nv) cm = fmaxf(cm, v[k]);
-        const float nm = fmaxf(m, cm);
-        const float nm2 = nm * kLog2e;
         float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+        float nm;
+        if (nv == 32) {  // a full chunk (all but a ragged tail): no per-column predicates
 #pragma unroll
-        for (int k = 0; k < 32; k += 4) {
-          if (k + 0 < nv) a0 += ex2_approx(fmaf(v[k + 0], kLog2e, -nm2));
-          if (k + 1 < nv) a1 += ex2_approx(fmaf(v[k + 1], kLog2e, -nm2));
-          if (k + 2 < nv) a2 += ex2_approx(fmaf(v[k + 2], kLog2e, -nm2));
-          if (k + 3 < nv) a3 += ex2_approx(fmaf(v[k + 3], kLog2e, -nm2));
+          for (int k = 0; k < 32; ++k) cm = fmaxf(cm, v[k]);
+          nm = fmaxf(m, cm * vs);
+          const float nm2 = nm * kLog2e;
+#pragma unroll
+          for (int k = 0; k < 32; k += 4) {
+            a0 += ex2_approx(fmaf(v[k + 0], k2, -nm2));
+            a1 += ex2_approx(fmaf(v[k + 1], k2, -nm2));
+            a2 += ex2_approx(fmaf(v[k + 2], k2, -nm2));
+            a3 += ex2_approx(fmaf(v[k + 3], k2, -nm2));
+          }
+        } else {
+#pragma unroll
+          for (int k = 0; k < 32; ++k)
+            if (k < nv) cm = fmaxf(cm, v[k]);
+          nm = fmaxf(m, cm * vs);
+          const float nm2 = nm * kLog2e;
+#pragma unroll
+          for (int k = 0; k < 32; k += 4) {
+            if (k + 0 < nv) a0 += ex2_approx(fmaf(v[k + 0], k2, -nm2));
+            if (k + 1 < nv) a1 += ex2_approx(fmaf(v[k + 1], k2, -nm2));
+            if (k + 2 < nv) a2 += ex2_approx(fmaf(v[k + 2], k2, -nm2));
+            if (k + 3 < nv) a3 += ex2_approx(fmaf(v[k + 3], k2, -nm2));
+          }
         }
         s = s * ex2_approx((m - nm) * kLog2e) + ((a0 + a1) + (a2 + a3));
         m = nm;
@@ -186,13 +206,13 @@ struct EpiFwdT {
           const bool hit = static_cast<unsigned>(off) < static_cast<unsigned>(nv);
           // a target falls in a given 32-column chunk for a few rows of a warp
           // at most: skip the selection unless one does
-          if (KMAX == 1 || __any_sync(0xffffffffu, hit)) {
+          if (__any_sync(0xffffffffu, hit)) {
             if (hit) {
               float x = 0.f;
 #pragma unroll
               for (int e = 0; e < 32; ++e)
                 if (e == off) x = v[e];
-              tg[k] = x;
+              tg[k] = x * vs;
               has_t |= 1u << k;
             }
           }
@@ -261,6 +281,7 @@ struct EpiGT {
     const float asc = fabsf(p.scale);
     float sig = 1.f;
     if constexpr (F8) sig = e4m3_logit_scale(p.amax);
+    const float k2 = sig * kLog2e;
     const uint32_t sgn = p.scale < 0.f ? 0x80008000u : 0u;
     const float off2 = valid ? fmaf(__ldg(p.lse + t), kLog2e, -p.log2_scale) : 0.f;
     const int j0 = nt * BN;
@@ -291,17 +312,17 @@ struct EpiGT {
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           float g0, g1;
-          const float x0 = F8 ? __uint_as_float(r[2 * i]) * sig : __uint_as_float(r[2 * i]);
-          const float x1 =
-              F8 ? __uint_as_float(r[2 * i + 1]) * sig : __uint_as_float(r[2 * i + 1]);
           if constexpr (CAP) {
+            const float x0 = F8 ? __uint_as_float(r[2 * i]) * sig : __uint_as_float(r[2 * i]);
+            const float x1 =
+                F8 ? __uint_as_float(r[2 * i + 1]) * sig : __uint_as_float(r[2 * i + 1]);
             const float z0 = head_z(x0, p.head);
             const float z1 = head_z(x1, p.head);
             g0 = ex2_approx(fmaf(z0, kLog2e, -off2)) * head_dz(z0, p.head);
             g1 = ex2_approx(fmaf(z1, kLog2e, -off2)) * head_dz(z1, p.head);
-          } else {
-            g0 = ex2_approx(fmaf(x0, kLog2e, -off2));
-            g1 = ex2_approx(fmaf(x1, kLog2e, -off2));
+          } else {  // sig (a power of two) folded into the constant: the same value
+            g0 = ex2_approx(fmaf(__uint_as_float(r[2 * i]), k2, -off2));
+            g1 = ex2_approx(fmaf(__uint_as_float(r[2 * i + 1]), k2, -off2));
           }
           pk[i] = pack_bf16x2(g0, g1) ^ sgn;
         }
@@ -397,7 +418,8 @@ struct EpiG8 {
     const int sl = valid ? __ldg(p.slot + t) : -1;
     if (valid && nt == 0 && static_cast<unsigned>(sl) >= static_cast<unsigned>(p.C))
       set_status(p.status, SS_ERR_INDEX);
-    const float sig = e4m3_logit_scale(p.amax);
+    // the e4m3 scale (a power of two) folded into the exponent's constant
+    const float k2 = e4m3_logit_scale(p.amax) * kLog2e;
     // 2^15 exp(s - lse) = 2^(s log2e - (lse log2e - 15))
     const float off2 = valid ? fmaf(__ldg(p.lse + t), kLog2e, -static_cast<float>(kG8Exp)) : 0.f;
     const float one_hot = static_cast<float>(1 << kG8Exp);
@@ -434,8 +456,7 @@ struct EpiG8 {
         const int off = sl - j0 - jc;
         float g[32];
 #pragma unroll
-        for (int i = 0; i < 32; ++i)
-          g[i] = ex2_approx(fmaf(__uint_as_float(r[i]) * sig, kLog2e, -off2));
+        for (int i = 0; i < 32; ++i) g[i] = ex2_approx(fmaf(__uint_as_float(r[i]), k2, -off2));
         if (__any_sync(0xffffffffu, static_cast<unsigned>(off) < 32u)) {
 #pragma unroll
           for (int i = 0; i < 32; ++i)
