@@ -134,11 +134,39 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
 
 // ------------------------------------------------------------ small kernels
 
-// W_c[j, :] = W[cand[j], :]; one warp per row, 16-byte vectors.
+// max |x| over this thread's grid-stride slice of x (n8 groups of 8 bf16),
+// four loads in flight, as bf16 magnitude bits
+__device__ __forceinline__ uint32_t absmax_slice(const uint16_t* __restrict__ x, int64_t n8) {
+  const uint4* v = reinterpret_cast<const uint4*>(x);
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
+  uint32_t mx = 0u;
+  for (; i + 3 * stride < n8; i += 4 * stride) {
+    const uint4 a = __ldg(v + i), b = __ldg(v + i + stride), c = __ldg(v + i + 2 * stride),
+                d = __ldg(v + i + 3 * stride);
+    mx = max(mx, max(max(bf16x8_absmax_bits(a), bf16x8_absmax_bits(b)),
+                     max(bf16x8_absmax_bits(c), bf16x8_absmax_bits(d))));
+  }
+  for (; i < n8; i += stride) mx = max(mx, bf16x8_absmax_bits(__ldg(v + i)));
+  return mx;
+}
+
+// *amax = max(*amax, the warp's largest magnitude): an atomic max of the
+// non-negative float's bits
+__device__ __forceinline__ void warp_atomic_max(float* amax, uint32_t mx) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  if ((threadIdx.x & 31) == 0 && mx) atomicMax(reinterpret_cast<unsigned*>(amax), mx << 16);
+}
+
+// W_c[j, :] = W[cand[j], :]; one warp per row, 16-byte vectors. For the FP8
+// head also max |W_c| into *amax and, over a second tensor x (n8 groups of 8),
+// max |x| into *x_amax.
 __global__ void __launch_bounds__(256) k_gather_rows(const uint16_t* __restrict__ W,
                                                      const int32_t* __restrict__ cand, int C,
                                                      int V, int D, uint16_t* __restrict__ Wc,
-                                                     float* amax, int* status) {
+                                                     float* amax, const uint16_t* __restrict__ x,
+                                                     int64_t x_n8, float* x_amax, int* status) {
   pdl_enter();
   if (read_status(status) != 0) return;
   const int lane = threadIdx.x & 31;
@@ -160,11 +188,8 @@ __global__ void __launch_bounds__(256) k_gather_rows(const uint16_t* __restrict_
       if (amax) mx = max(mx, bf16x8_absmax_bits(x));
     }
   }
-  if (amax) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    if (lane == 0 && mx) atomicMax(reinterpret_cast<unsigned*>(amax), mx << 16);
-  }
+  if (amax) warp_atomic_max(amax, mx);
+  if (x_amax) warp_atomic_max(x_amax, absmax_slice(x, x_n8));
 }
 
 // amax[0] = max over x of |x| (n bf16 values, n % 8 == 0), as an atomic max of
@@ -173,13 +198,7 @@ __global__ void __launch_bounds__(256) k_amax_bf16(const uint16_t* __restrict__ 
                                                    float* amax, int* status) {
   pdl_enter();
   if (read_status(status) != 0) return;
-  uint32_t mx = 0u;
-  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n8; i += stride)
-    mx = max(mx, bf16x8_absmax_bits(__ldg(reinterpret_cast<const uint4*>(x) + i)));
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-  if ((threadIdx.x & 31) == 0 && mx) atomicMax(reinterpret_cast<unsigned*>(amax), mx << 16);
+  warp_atomic_max(amax, absmax_slice(x, n8));
 }
 
 // The FP8 head's operands, two tensors in one launch (job 0: H, job 1: W_c):
@@ -460,17 +479,19 @@ cudaError_t noalloc_scratch_address(void** out) {
 
 ss_status enqueue_gather(const uint16_t* W, const int32_t* cand, int64_t C, int64_t V, int64_t D,
                          uint16_t* Wc, int* status, int nsm, cudaStream_t s,
-                         float* amax = nullptr) {
+                         float* amax = nullptr, const uint16_t* x = nullptr, int64_t x_n8 = 0,
+                         float* x_amax = nullptr) {
   trace_pre(s, "gather_rows");
   const cudaError_t e = launch_pdl(k_gather_rows, dim3(rows_grid(C, nsm)), dim3(256), 0, s, W, cand,
                                    static_cast<int>(C), static_cast<int>(V), static_cast<int>(D),
-                                   Wc, amax, status);
+                                   Wc, amax, x, x_n8, x_amax, status);
   trace_post(s);
   return e == cudaSuccess ? SS_OK : fail("launch k_gather_rows", e);
 }
 
-// W_c = W[cand] and, for the FP8 head, the e4m3 operands: amax of W_c (in
-// the gather) and of H, then H -> (h8, hq) and W_c -> (w8, W_c rounded in place)
+// W_c = W[cand] and, for the FP8 head, the e4m3 operands: amax of W_c and of
+// H (both in the gather's launch), then H -> (h8, hq) and W_c -> (w8, W_c
+// rounded in place), or (FP8 gradients) the row-major and transposed codes
 ss_status enqueue_gather_operands(const uint16_t* W, const int32_t* cand, const uint16_t* H,
                                   int64_t T, int64_t C, int64_t V, int64_t D, int fp8,
                                   const Layout& L, char* ws, int nsm, cudaStream_t s) {
@@ -480,12 +501,8 @@ ss_status enqueue_gather_operands(const uint16_t* W, const int32_t* cand, const 
   float* amax = reinterpret_cast<float*>(ws + L.hdr + kHdrAmax);
   cudaError_t e = cudaMemsetAsync(amax, 0, 2 * sizeof(float), s);
   if (e != cudaSuccess) return fail("cudaMemsetAsync(amax)", e);
-  ss_status r = enqueue_gather(W, cand, C, V, D, Wc, status, nsm, s, amax + 1);
+  ss_status r = enqueue_gather(W, cand, C, V, D, Wc, status, nsm, s, amax + 1, H, T * D / 8, amax);
   if (r != SS_OK) return r;
-  trace_pre(s, "amax_H");
-  e = launch_pdl(k_amax_bf16, dim3(nsm * 2), dim3(256), 0, s, H, T * D / 8, amax, status);
-  trace_post(s);
-  if (e != cudaSuccess) return fail("launch k_amax_bf16", e);
   if (fp8 == 2) {  // FP8 gradients: row-major and transposed codes, no bf16 copies
     if ((T + 63) / 64 * (D / 64) > INT32_MAX / 2) return SS_ERR_UNSUPPORTED;
     const QuantTJob th{H, reinterpret_cast<uint8_t*>(ws + L.h8),
@@ -1061,7 +1078,8 @@ ss_status ss_forward_noalloc(const uint16_t* H, const uint16_t* W, const int32_t
   trace_pre(s, "gather_rows");
   cudaError_t eg = launch_pdl(k_gather_rows, dim3(rows_grid(C, nsm)), dim3(256), 0, s, W, cand,
                               static_cast<int>(C), static_cast<int>(V), static_cast<int>(D), Wc,
-                              static_cast<float*>(nullptr), status);
+                              static_cast<float*>(nullptr), static_cast<const uint16_t*>(nullptr),
+                              int64_t(0), static_cast<float*>(nullptr), status);
   trace_post(s);
   if (eg != cudaSuccess) return fail("launch k_gather_rows", eg);
   CUtensorMap tH, tWc;
