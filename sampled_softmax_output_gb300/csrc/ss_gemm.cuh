@@ -239,8 +239,10 @@ using EpiFwd = EpiFwdT<false>;
 // patched into the staged tile.
 template <bool CAP, int KMAX = 1, bool F8 = false>
 struct EpiGT {
-  // two 16 KB staging buffers: both for one column group, one each for two
-  static constexpr int kStageBytes = 2 * 16384;
+  // 16 KB staging buffers, split between the column groups: two (bf16), or
+  // four with the e4m3 operands, whose tiles take half as long, so that a
+  // group never waits for its last store to have read the buffer
+  static constexpr int kStageBytes = (F8 ? 4 : 2) * 16384;
   // G streams through L2 once; the H and W_c tiles are re-read by every CTA
   static constexpr bool kKeepOperands = true;
   struct Params {
@@ -291,14 +293,11 @@ struct EpiGT {
     for (int q = cg * (BN / 64) / NCG; q < (cg + 1) * (BN / 64) / NCG; ++q) {
       const int qc = q * 64;
       if (qc >= ncols) break;  // uniform: depends on the tile only
-      constexpr uint32_t kBufs = 2 / NCG;  // buffers per column group
+      constexpr uint32_t kBufs = kStageBytes / 16384 / NCG;  // buffers per column group
       const uint32_t buf = es.stage + static_cast<uint32_t>(cg) * 16384u * kBufs +
                            (es.rounds % kBufs) * 16384u;
       // the store that last used this buffer must have read it
-      if (es.rounds >= kBufs && leader) {
-        if constexpr (kBufs == 2) bulk_wait_read<1>();
-        else bulk_wait_read<0>();
-      }
+      if (es.rounds >= kBufs && leader) bulk_wait_read<static_cast<int>(kBufs) - 1>();
       named_bar_sync(bar, 128);
       const uint32_t rowbase = buf + static_cast<uint32_t>(row) * 128u;
 #pragma unroll
@@ -393,7 +392,7 @@ __device__ __forceinline__ float fp8_grad_alpha(float scale, const float* amax_b
 // tile in the 64-byte-swizzled layout of G8's map and a 64 x 128-byte tile in
 // the 128-byte-swizzled layout of G8t's map (16 KB per column group).
 struct EpiG8 {
-  static constexpr int kStageBytes = 2 * 16384;
+  static constexpr int kStageBytes = 4 * 16384;  // two 16 KB buffers per column group
   static constexpr bool kKeepOperands = true;
   struct Params {
     CUtensorMap tmG;   // G8 [T, C] (row pitch ldG bytes), box 64 x 128, 64-byte swizzle
@@ -437,14 +436,11 @@ struct EpiG8 {
     for (int q = cg * (BN / 64) / NCG; q < (cg + 1) * (BN / 64) / NCG; ++q) {
       const int qc = q * 64;
       if (qc >= ncols) break;  // uniform: depends on the tile only
-      constexpr uint32_t kBufs = 2 / NCG;
+      constexpr uint32_t kBufs = kStageBytes / 16384 / NCG;
       const uint32_t buf = es.stage + static_cast<uint32_t>(cg) * 16384u * kBufs +
                            (es.rounds % kBufs) * 16384u;
       const uint32_t rbuf = buf, tbuf = buf + 8192u;
-      if (es.rounds >= kBufs && leader) {
-        if constexpr (kBufs == 2) bulk_wait_read<1>();
-        else bulk_wait_read<0>();
-      }
+      if (es.rounds >= kBufs && leader) bulk_wait_read<static_cast<int>(kBufs) - 1>();
       named_bar_sync(bar, 128);
 #pragma unroll
       for (int h = 0; h < 2; ++h) {

@@ -61,7 +61,7 @@ cudaError_t launch_softmax_grad_fp8(const CUtensorMap& tH8, const CUtensorMap& t
   ep.status = status;
   ep.amax = amax;
   GemmShape shp{(T + BM - 1) / BM, (C + kBnLogits - 1) / kBnLogits, D / (2 * BK)};
-  return launch_gemm<kBnLogits, kStagesLogits, false, false, EpiG8, 8, true>(tH8, tW8, shp, ep,
+  return launch_gemm<kBnLogits, kStagesGradF8, false, false, EpiG8, 8, true>(tH8, tW8, shp, ep,
                                                                              status, num_sms,
                                                                              stream);
 }

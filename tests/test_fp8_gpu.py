@@ -125,3 +125,25 @@ def test_fp8_head_full_size(orc, mode):
     dW_fn = orc.backward_dWc_g8 if mode == 2 else orc.backward_dWc
     ref_rows = dW_fn(Hq, Wq, cand, slot, lse_all, scale, cols=cols)
     assert rel_fro(got["dW"].cpu().numpy()[cand[cols]], ref_rows) < GRAD_RTOL
+
+
+@pytest.mark.parametrize("mode", [1, 2])
+def test_fp8_graph_replay_equals_direct_step(mode):
+    """A captured FP8 step replayed with new seeds gives the bits of ss_step."""
+    T, V, D, C = 700, 6000, 768, 1500
+    x = synth.make_inputs(T, V, D, 1.1, 41)
+    C = max(C, len(np.unique(x["targets"])))
+    H, W = to_dev_bf16(x["H"]), to_dev_bf16(x["W"])
+    tg = torch.from_numpy(x["targets"]).cuda()
+    ws = ss.workspace(T, V, C, D)
+    g = ss.StepGraph(H, W, tg, C, ws, scale=0.25, fp8=mode)
+    ws2 = ss.workspace(T, V, C, D)
+    for seed in (5, 9):
+        g.dW.zero_()
+        got = g.launch(seed)
+        ref = ss.step(H, W, tg, C, seed, ws2, scale=0.25, fp8=mode)
+        torch.cuda.synchronize()
+        assert ss.read_status(ws)[0] == 0
+        for k in ("cand", "slot", "loss", "lse", "dH", "dW"):
+            assert torch.equal(got[k], ref[k]), (seed, k)
+    g.close()
