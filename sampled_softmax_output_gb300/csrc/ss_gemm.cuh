@@ -54,6 +54,7 @@ struct EpiState {
   uint32_t stage;   // shared address of the epilogue staging region
   int ep_tid;       // index among the epilogue threads
   uint32_t rounds;  // staging buffers used so far
+  float f0;         // a per-launch constant an epilogue computes in begin() (FP8 scales)
 };
 
 struct GemmCtrl {
@@ -134,10 +135,14 @@ struct EpiFwdT {
     Targets tg;    // used when KMAX > 1
     const float* amax;  // used when F8: logits = accumulator * e4m3_logit_scale(amax)
   };
+  // F8: the logit scale, the same for every tile, loaded once per launch
+  __device__ static void begin(const Params& p, EpiState& es) {
+    if constexpr (F8) es.f0 = e4m3_logit_scale(p.amax);
+  }
   __device__ static void finish(const Params&, EpiState&) {}
   template <int BN, int NCG>
   __device__ static void apply(const Params& p, int mt, int nt, int row, uint32_t taddr,
-                               EpiState&, int cg) {
+                               EpiState& es, int cg) {
     constexpr int CPG = BN / 32 / NCG;  // chunks per group
     const int t = mt * BM + row;
     const bool valid = t < p.T;
@@ -151,7 +156,7 @@ struct EpiFwdT {
     float m = -INFINITY, s = 0.f, tg[KMAX];
     uint32_t has_t = 0u;  // bit k: target k lies in this group's columns
     float sig = 1.f;
-    if constexpr (F8) sig = e4m3_logit_scale(p.amax);
+    if constexpr (F8) sig = es.f0;
     // Plain head: v holds the raw accumulator and the logit is v * vs (the
     // FP8 scale is a power of two, so it commutes exactly with the max and
     // folds into the exponent's constant); capped head: v = z, vs = 1.
@@ -258,6 +263,9 @@ struct EpiGT {
                        // log2_scale is then log2(|scale| W)
     const float* amax;  // used when F8: logits = accumulator * e4m3_logit_scale(amax)
   };
+  __device__ static void begin(const Params& p, EpiState& es) {
+    if constexpr (F8) es.f0 = e4m3_logit_scale(p.amax);
+  }
   __device__ static void finish(const Params&, EpiState& es) {
     if ((es.ep_tid & 127) == 0) bulk_wait<0>();
   }
@@ -282,7 +290,7 @@ struct EpiGT {
     }
     const float asc = fabsf(p.scale);
     float sig = 1.f;
-    if constexpr (F8) sig = e4m3_logit_scale(p.amax);
+    if constexpr (F8) sig = es.f0;
     const float k2 = sig * kLog2e;
     const uint32_t sgn = p.scale < 0.f ? 0x80008000u : 0u;
     const float off2 = valid ? fmaf(__ldg(p.lse + t), kLog2e, -p.log2_scale) : 0.f;
@@ -403,6 +411,9 @@ struct EpiG8 {
     int* status;
     const float* amax;  // logits = accumulator * e4m3_logit_scale(amax)
   };
+  __device__ static void begin(const Params& p, EpiState& es) {
+    es.f0 = e4m3_logit_scale(p.amax) * kLog2e;
+  }
   __device__ static void finish(const Params&, EpiState& es) {
     if ((es.ep_tid & 127) == 0) bulk_wait<0>();
   }
@@ -418,7 +429,7 @@ struct EpiG8 {
     if (valid && nt == 0 && static_cast<unsigned>(sl) >= static_cast<unsigned>(p.C))
       set_status(p.status, SS_ERR_INDEX);
     // the e4m3 scale (a power of two) folded into the exponent's constant
-    const float k2 = e4m3_logit_scale(p.amax) * kLog2e;
+    const float k2 = es.f0;
     // 2^15 exp(s - lse) = 2^(s log2e - (lse log2e - 15))
     const float off2 = valid ? fmaf(__ldg(p.lse + t), kLog2e, -static_cast<float>(kG8Exp)) : 0.f;
     const float one_hot = static_cast<float>(1 << kG8Exp);
@@ -504,10 +515,13 @@ struct EpiDhT {
     float scale;         // used when F8G
     const float* amax;   // used when F8G: max |W_c|
   };
+  __device__ static void begin(const Params& p, EpiState& es) {
+    if constexpr (F8G) es.f0 = fp8_grad_alpha(p.scale, p.amax);
+  }
   __device__ static void finish(const Params&, EpiState&) {}
   template <int BN, int NCG>
   __device__ static void apply(const Params& p, int mt, int nt, int row, uint32_t taddr,
-                               EpiState&, int cg) {
+                               EpiState& es, int cg) {
     constexpr int CPG = BN / 32 / NCG;
     const int t = mt * BM + row;
     const bool valid = t < p.T;
@@ -516,7 +530,7 @@ struct EpiDhT {
     if (ncols <= 0) return;
     uint16_t* drow = p.dH + static_cast<size_t>(valid ? t : 0) * p.D + n0;
     float al = 1.f;
-    if constexpr (F8G) al = fp8_grad_alpha(p.scale, p.amax);
+    if constexpr (F8G) al = es.f0;
     for_tmem_chunks<CPG>(taddr, cg * CPG, [&](const uint32_t(&r)[32], int i) {
       const int jc = i * 32;
       if (jc >= ncols || !valid) return;
@@ -550,10 +564,13 @@ struct EpiDwT {
     float scale;         // used when F8G
     const float* amax;   // used when F8G: max |H|
   };
+  __device__ static void begin(const Params& p, EpiState& es) {
+    if constexpr (F8G) es.f0 = fp8_grad_alpha(p.scale, p.amax);
+  }
   __device__ static void finish(const Params&, EpiState&) {}
   template <int BN, int NCG>
   __device__ static void apply(const Params& p, int mt, int nt, int row, uint32_t taddr,
-                               EpiState&, int cg) {
+                               EpiState& es, int cg) {
     constexpr int CPG = BN / 32 / NCG;
     const int j = mt * BM + row;
     bool valid = j < p.C;
@@ -567,7 +584,7 @@ struct EpiDwT {
     if (ncols <= 0) return;
     float* drow = p.dW + static_cast<size_t>(valid ? v : 0) * p.D + n0;
     float al = 1.f;
-    if constexpr (F8G) al = fp8_grad_alpha(p.scale, p.amax);
+    if constexpr (F8G) al = es.f0;
     for_tmem_chunks<CPG>(taddr, cg * CPG, [&](const uint32_t(&r)[32], int i) {
       const int jc = i * 32;
       if (jc >= ncols || !valid) return;
@@ -750,7 +767,8 @@ __global__ void __launch_bounds__(64 + 32 * EPI_WARPS, 1)
     const int cg = (warp - 2) / 4;  // column group
     const int row = q * 32 + lane;
     const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
-    EpiState es{tiles + L::EPI_OFFSET, static_cast<int>(threadIdx.x) - 64, 0u};
+    EpiState es{tiles + L::EPI_OFFSET, static_cast<int>(threadIdx.x) - 64, 0u, 0.f};
+    Epi::begin(ep, es);
     int b = 0;
     uint32_t aph = 0;
     for (int u = blockIdx.x; u < num_units; u += gridDim.x) {

@@ -204,7 +204,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * EPI_WARPS,
     const int cg = (warp - 2) / 4;   // column group
     const int row = q * 32 + lane;
     const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
-    EpiState es{tiles + L::EPI_OFFSET, static_cast<int>(threadIdx.x) - 64, 0u};
+    EpiState es{tiles + L::EPI_OFFSET, static_cast<int>(threadIdx.x) - 64, 0u, 0.f};
+    Epi::begin(ep, es);
     int b = 0;
     uint32_t aph = 0;
     for (int u = pair; u < num_units; u += npairs) {

@@ -257,7 +257,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * kGradEpiWa
     const int cg = (warp - 2) / 4;
     const int row = q * 32 + lane;
     const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
-    EpiState es{0u, 0, 0u};
+    // one EpiState per kind of tile: each holds that epilogue's per-launch scale
+    EpiState es{0u, 0, 0u, 0.f}, es_h{0u, 0, 0u, 0.f};
+    EpiDwT<F8G>::begin(p.dw, es);
+    EpiDhT<F8G>::begin(p.dh, es_h);
     int b = 0;
     uint32_t aph = 0;
     for (int i = u_begin; i < u_end; i += u_step) {
@@ -270,7 +273,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * kGradEpiWa
       const int mt = (v / p.n_nt) * 2 + static_cast<int>(rank), nt = v % p.n_nt;
       const uint32_t taddr = lane_addr + static_cast<uint32_t>(b * BN);
       if (is_dw) EpiDwT<F8G>::template apply<BN, NCG>(p.dw, mt, nt, row, taddr, es, cg);
-      else EpiDhT<F8G>::template apply<BN, NCG>(p.dh, mt, nt, row, taddr, es, cg);
+      else EpiDhT<F8G>::template apply<BN, NCG>(p.dh, mt, nt, row, taddr, es_h, cg);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
