@@ -556,7 +556,7 @@ ss_status enqueue_forward(const uint16_t* H, const int32_t* slot, int64_t T, int
   trace_pre(s, "lse_merge");
   const cudaError_t em =
       launch_pdl(k_lse_merge, dim3(blocks), dim3(256), 0, s, part, tgt, slot, static_cast<int>(T),
-                 static_cast<int>(C), static_cast<int>(L.n_ct * fwd_groups(cap, fp8 != 0)), tg, loss,
+                 static_cast<int>(C), static_cast<int>(L.n_ct * fwd_groups(cap, fp8 != 0, tg.K)), tg, loss,
                  lse, status);
   trace_post(s);
   return cuda_status(em, "launch k_lse_merge");

@@ -28,11 +28,12 @@ cudaError_t forward_logits(const CUtensorMap& tH, const CUtensorMap& tWc, int T,
                            cudaStream_t stream) {
   GemmShape shp{(T + BM - 1) / BM, (C + kBnLogits - 1) / kBnLogits, D / (F8 ? 2 * BK : BK)};
   typename EpiFwdT<CAP, KMAX, F8>::Params ep{T, C, slot, part, tgt, status, head, tg, amax};
-  // the capped head's epilogue (three MUFU operations per logit), and the FP8
-  // head's (its mainloop is twice as fast), run eight warps in two column
-  // groups, two partials per row per tile
+  // the capped head's epilogue (three MUFU operations per logit), the FP8
+  // head's (its mainloop is twice as fast) and that of several targets run
+  // eight warps in two column groups, two partials per row per tile
   return launch_gemm<kBnLogits, kStagesLogits, false, false, EpiFwdT<CAP, KMAX, F8>,
-                     (CAP || F8) ? 8 : 4, F8>(tH, tWc, shp, ep, status, num_sms, stream);
+                     (CAP || F8 || KMAX > 1) ? 8 : 4, F8>(tH, tWc, shp, ep, status, num_sms,
+                                                          stream);
 }
 
 template <bool CAP, int KMAX, bool F8 = false>

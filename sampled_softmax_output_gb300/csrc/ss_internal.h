@@ -43,11 +43,15 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
 // Tile widths of the GEMMs (output columns per tile).
 constexpr int kBnLogits = 256;  // logit tiles: forward and softmax-gradient
 constexpr int kBnGrad = 256;    // dH and dW tiles along D
-// Softmax partials per row per logit tile: 1 for the plain head (four
-// epilogue warps), 2 for the capped head (eight warps in two column groups:
-// its epilogue does three MUFU operations per logit); the workspace holds 2.
+// Softmax partials per row per logit tile: 1 for the plain single-target
+// head (four epilogue warps); 2 (eight warps in two column groups) for the
+// heads whose epilogue does more per logit than the MMAs can hide: the capped
+// head (three MUFU operations per logit), the FP8 head (a mainloop twice as
+// fast) and several targets per token. The workspace holds 2.
 constexpr int kFwdGroupsMax = 2;
-inline int fwd_groups(float cap, bool fp8 = false) { return cap > 0.f || fp8 ? 2 : 1; }
+inline int fwd_groups(float cap, bool fp8 = false, int targets = 1) {
+  return cap > 0.f || fp8 || targets > 1 ? 2 : 1;
+}
 
 struct GemmShape;
 
