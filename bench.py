@@ -261,8 +261,8 @@ def oracle_sample(x: dict, w, T_s: int, scale: float, cap: float = 0.0, tau: flo
     ss_ = slot[:T_s]
     loss, lse = oracle.forward(Hs, W, cand, ss_, cap=cap, tau=tau)
     if fp8 == 2:  # FP8 gradients: e5m2 G
-        oracle.backward_dH_g8(Hs, W, cand, ss_, lse, scale)
-        oracle.backward_dWc_g8(Hs, W, cand, ss_, lse, scale)
+        oracle.backward_dH_g8(Hs, W, cand, ss_, lse, scale, cap=cap, tau=tau)
+        oracle.backward_dWc_g8(Hs, W, cand, ss_, lse, scale, cap=cap, tau=tau)
     else:
         oracle.backward_dH(Hs, W, cand, ss_, lse, scale, cap=cap, tau=tau)
         oracle.backward_dWc(Hs, W, cand, ss_, lse, scale, cap=cap, tau=tau)

@@ -175,7 +175,11 @@ ss_status ss_backward(const uint16_t* H, const uint16_t* W, const int32_t* cand,
  * rounded to e5m2 (to nearest, ties to even), G8 = e5m2(2^15 (P - Y));
  * the two gradient GEMMs run on G8 and the e4m3 operands
  * (dH = scale 2^-15 G8 . W_c,q and dW_c = scale 2^-15 G8^T . H_q).
- * Both modes require cap = 0 (else SS_ERR_UNSUPPORTED) and D % 128 == 0
+ * Both modes combine with the capped head (the pages' head is FP8 and
+ * soft-capped): the logits z are taken from the rounded operands, and with
+ * FP8 gradients G8 = e5m2(2^e (P - Y) dz/ds) with e the largest integer such
+ * that B 2^e <= 57344, B = cap / (4 tau) the bound of dz/ds (e = 15 for the
+ * plain head; also 15 for cap = 4 tau). Both modes require D % 128 == 0
  * (else SS_ERR_UNSUPPORTED); the several-targets entry points take no FP8
  * head (SS_ERR_UNSUPPORTED); other fp8 values -> SS_ERR_INVALID.
  */
@@ -304,8 +308,8 @@ ss_status ss_step_graph_launch(ss_step_graph* graph, uint64_t seed, ss_stream st
 void ss_step_graph_destroy(ss_step_graph* graph);
 
 /*
- * Allocation-free forward pass. Not part of the method on the pages (the
- * paper has no counterpart): an operational variant of ss_forward for callers
+ * Allocation-free forward pass. Not part of the method the pages describe
+ * (they have no counterpart): an operational variant of ss_forward for callers
  * that cannot allocate device memory at all -- for example code running as a
  * plugin inside a host program that has planned and owns every byte of device
  * memory and hands the plugin only its input and output buffers, or code on a

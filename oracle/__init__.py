@@ -100,7 +100,10 @@ def load(path: str):
     for name in ("orc_backward_dH_g8", "orc_backward_dW_g8"):
         f = getattr(L, name)
         f.restype = None
-        f.argtypes = [_p, _p, _p, _p, _p, _i64, _i64, _i64, ctypes.c_float, _p, _i64, _p]
+        f.argtypes = [_p, _p, _p, _p, _p, _i64, _i64, _i64, ctypes.c_float, ctypes.c_float,
+                      ctypes.c_float, _p, _i64, _p]
+    L.orc_g8_exponent.restype = ctypes.c_int
+    L.orc_g8_exponent.argtypes = [ctypes.c_float, ctypes.c_float]
     L.orc_num_threads.restype = ctypes.c_int
     L.orc_num_threads.argtypes = []
     return L
@@ -381,9 +384,13 @@ def round_e5m2(x: float) -> float:
     return float(lib().orc_round_e5m2(x))
 
 
-def backward_dH_g8(H, W, cand, slot, lse_rows, scale=1.0, rows=None):
-    """FP8 gradients (e5m2 G, one target, plain head): dH rows [n, D] on
-    operands already rounded to e4m3 (bf16 bit patterns)."""
+def g8_exponent(cap: float = 0.0, tau: float = 1.0) -> int:
+    return int(lib().orc_g8_exponent(cap, tau))
+
+
+def backward_dH_g8(H, W, cand, slot, lse_rows, scale=1.0, rows=None, cap=0.0, tau=1.0):
+    """FP8 gradients (e5m2 G, one target; cap > 0: the capped head): dH rows
+    [n, D] on operands already rounded to e4m3 (bf16 bit patterns)."""
     H = _inputs(H, "f32")
     W = _inputs(W, "f32")
     cand = np.ascontiguousarray(cand, np.int32)
@@ -395,11 +402,11 @@ def backward_dH_g8(H, W, cand, slot, lse_rows, scale=1.0, rows=None):
     assert lse_rows.shape[0] == n
     dH = np.empty((n, D), np.float32)
     lib().orc_backward_dH_g8(_ptr(H), _ptr(W), _ptr(cand), _ptr(slot), _ptr(lse_rows), T,
-                             cand.shape[0], D, scale, _ptr(r), nr, _ptr(dH))
+                             cand.shape[0], D, cap, tau, scale, _ptr(r), nr, _ptr(dH))
     return dH
 
 
-def backward_dWc_g8(H, W, cand, slot, lse, scale=1.0, cols=None):
+def backward_dWc_g8(H, W, cand, slot, lse, scale=1.0, cols=None, cap=0.0, tau=1.0):
     """FP8 gradients: candidate-row gradients dWc [n, D]; `lse` of ALL T tokens."""
     H = _inputs(H, "f32")
     W = _inputs(W, "f32")
@@ -412,26 +419,27 @@ def backward_dWc_g8(H, W, cand, slot, lse, scale=1.0, cols=None):
     c, nc = _rows(cols)
     n = nc if c is not None else C
     dWc = np.empty((n, D), np.float32)
-    lib().orc_backward_dW_g8(_ptr(H), _ptr(W), _ptr(cand), _ptr(slot), _ptr(lse), T, C, D, scale,
-                             _ptr(c), nc, _ptr(dWc))
+    lib().orc_backward_dW_g8(_ptr(H), _ptr(W), _ptr(cand), _ptr(slot), _ptr(lse), T, C, D, cap,
+                             tau, scale, _ptr(c), nc, _ptr(dWc))
     return dWc
 
 
 def loss_and_grads_fp8(H, W, targets, C, seed, scale=1.0, dW_init=None, accumulate=False,
-                       grads=False):
+                       grads=False, cap=0.0, tau=1.0):
     """The whole definition with the FP8 head: the single-target loss and its
     gradients on the rounded operands (rows of dW outside cand untouched);
-    grads=True: FP8 through the backward too (e5m2 G)."""
+    grads=True: FP8 through the backward too (e5m2 G); cap > 0: the capped
+    head on the rounded operands."""
     V = W.shape[0]
     cand, slot, U = build_candidates(targets, V, C, seed)
     Hq, Wq, eH, eW = fp8_inputs(H, W, cand)
-    loss, lse = forward(Hq, Wq, cand, slot)
+    loss, lse = forward(Hq, Wq, cand, slot, cap=cap, tau=tau)
     if grads:
-        dH = backward_dH_g8(Hq, Wq, cand, slot, lse, scale)
-        dWc = backward_dWc_g8(Hq, Wq, cand, slot, lse, scale)
+        dH = backward_dH_g8(Hq, Wq, cand, slot, lse, scale, cap=cap, tau=tau)
+        dWc = backward_dWc_g8(Hq, Wq, cand, slot, lse, scale, cap=cap, tau=tau)
     else:
-        dH = backward_dH(Hq, Wq, cand, slot, lse, scale)
-        dWc = backward_dWc(Hq, Wq, cand, slot, lse, scale)
+        dH = backward_dH(Hq, Wq, cand, slot, lse, scale, cap=cap, tau=tau)
+        dWc = backward_dWc(Hq, Wq, cand, slot, lse, scale, cap=cap, tau=tau)
     dW = np.zeros(W.shape, np.float32) if dW_init is None else np.array(dW_init, np.float32)
     if accumulate:
         dW[cand] += dWc

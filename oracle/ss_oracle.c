@@ -83,7 +83,12 @@
  *               G8[t][j] = round_e5m2(2^15 (exp(s[t][j] - lse[t]) - [j == slot[t]]))
  *               dH[t]    = scale 2^-15 sum_j G8[t][j] * W[cand[j]]
  *               dW[cand[j]] = scale 2^-15 sum_t G8[t][j] * H[t]
- *   with H and W the e4m3-rounded operands.
+ *   with H and W the e4m3-rounded operands. With the capped head the
+ *   gradient matrix carries the factor dz/ds, at most A / (4 tau) (at
+ *   z = A / 2), so its bound is B = A / (4 tau) instead of 1, and the power
+ *   of two is 2^eG with eG the largest integer such that B 2^eG <= 57344
+ *   (eG = 15 for the plain head):
+ *               G8 = round_e5m2(2^eG (exp(z - lse) - [j == slot]) dz/ds).
  *
  * Precision: the definition is fp32. Its inputs are bf16 bit patterns widened
  * exactly to float. An fp64 instantiation of the same loops, on double inputs,
@@ -430,18 +435,31 @@ float orc_round_e5m2(float x) {
   return copysignf(rintf(a / q) * q, x);
 }
 
-/* G8 of one logit: round_e5m2(2^15 (exp(s - lse) - y)) */
-static float g8_of(float s, float lse, float y) {
-  return orc_round_e5m2(ldexpf(expf(s - lse) - y, 15));
+/* the largest integer e with B 2^e <= 57344, B the bound of |(P - Y) dz/ds|:
+ * 1 for the plain head (A = 0, e = 15), A / (4 tau) for the capped head */
+int orc_g8_exponent(float cap, float tau) {
+  const double B = cap > 0 ? (double)cap / (4.0 * (double)tau) : 1.0;
+  int e = 15;
+  while (B * ldexp(1.0, e) > 57344.0) --e;
+  while (B * ldexp(1.0, e + 1) <= 57344.0) ++e;
+  return e;
+}
+
+/* G8 of one logit s (z = the head's logit): round_e5m2(2^e (exp(z - lse) - y) dz/ds) */
+static float g8_of(float s, float lse, float y, float cap, float tau, int e) {
+  const float z = head_z_f32(s, cap, tau);
+  return orc_round_e5m2(ldexpf((expf(z - lse) - y) * head_dz_f32(z, cap, tau), e));
 }
 
 /* FP8 gradients, one target per token, plain head: dH rows (lse_rows of
  * exactly those rows), inputs already rounded to e4m3 (bf16 bit patterns). */
 void orc_backward_dH_g8(const uint16_t* H, const uint16_t* W, const int32_t* cand,
                         const int32_t* slot, const float* lse_rows, int64_t T, int64_t C,
-                        int64_t D, float scale, const int64_t* rows, int64_t nrows, float* dH) {
+                        int64_t D, float cap, float tau, float scale, const int64_t* rows,
+                        int64_t nrows, float* dH) {
   int64_t n = rows ? nrows : T;
-  const float f = ldexpf(scale, -15);
+  const int e = orc_g8_exponent(cap, tau);
+  const float f = ldexpf(scale, -e);
 #pragma omp parallel
   {
     float* s = (float*)malloc(sizeof(float) * (size_t)C);
@@ -452,7 +470,7 @@ void orc_backward_dH_g8(const uint16_t* H, const uint16_t* W, const int32_t* can
       float* out = dH + i * D;
       for (int64_t d = 0; d < D; ++d) out[d] = 0;
       for (int64_t j = 0; j < C; ++j) {
-        const float g = f * g8_of(s[j], lse_rows[i], slot[t] == j ? 1.0f : 0.0f);
+        const float g = f * g8_of(s[j], lse_rows[i], slot[t] == j ? 1.0f : 0.0f, cap, tau, e);
         const uint16_t* wr = W + (int64_t)cand[j] * D;
         for (int64_t d = 0; d < D; ++d) out[d] += g * bf16_to_float(wr[d]);
       }
@@ -464,9 +482,11 @@ void orc_backward_dH_g8(const uint16_t* H, const uint16_t* W, const int32_t* can
 /* ... and dW_c rows (candidate index j; lse of ALL T tokens) */
 void orc_backward_dW_g8(const uint16_t* H, const uint16_t* W, const int32_t* cand,
                         const int32_t* slot, const float* lse, int64_t T, int64_t C, int64_t D,
-                        float scale, const int64_t* cols, int64_t ncols, float* dWc) {
+                        float cap, float tau, float scale, const int64_t* cols, int64_t ncols,
+                        float* dWc) {
   int64_t n = cols ? ncols : C;
-  const float f = ldexpf(scale, -15);
+  const int e = orc_g8_exponent(cap, tau);
+  const float f = ldexpf(scale, -e);
 #pragma omp parallel for schedule(dynamic, 1)
   for (int64_t i = 0; i < n; ++i) {
     int64_t j = cols ? cols[i] : i;
@@ -477,7 +497,7 @@ void orc_backward_dW_g8(const uint16_t* H, const uint16_t* W, const int32_t* can
       const uint16_t* h = H + t * D;
       float st = 0;
       for (int64_t d = 0; d < D; ++d) st += bf16_to_float(h[d]) * bf16_to_float(wr[d]);
-      const float g = f * g8_of(st, lse[t], slot[t] == j ? 1.0f : 0.0f);
+      const float g = f * g8_of(st, lse[t], slot[t] == j ? 1.0f : 0.0f, cap, tau, e);
       for (int64_t d = 0; d < D; ++d) out[d] += g * bf16_to_float(h[d]);
     }
   }

@@ -564,10 +564,21 @@ ss_status enqueue_forward(const uint16_t* H, const int32_t* slot, int64_t T, int
 
 // FP8 gradients: G8 and G8^T (e5m2) from the e4m3 logits, then both gradient
 // GEMMs on e5m2 x e4m3, every operand K-major
+// G8's power of two: the largest e with B 2^e <= 57344 (e5m2's largest finite
+// value), B the bound of |(P - Y) dz/ds|: 1 for the plain head, cap / (4 tau)
+// (the largest dz/ds) for the capped head
+int g8_exponent(float cap, float tau) {
+  const double B = cap > 0.f ? static_cast<double>(cap) / (4.0 * tau) : 1.0;
+  int k;
+  std::frexp(57344.0 / B, &k);  // 57344 / B in [2^(k-1), 2^k)
+  return std::max(-100, std::min(100, k - 1));
+}
+
 ss_status enqueue_backward_fp8(const int32_t* cand, const int32_t* slot, const float* lse,
-                               int64_t T, int64_t V, int64_t C, int64_t D, float scale,
-                               int accumulate, uint16_t* dH, float* dW, const Layout& L, char* ws,
-                               int nsm, cudaStream_t s) {
+                               int64_t T, int64_t V, int64_t C, int64_t D, float cap, float tau,
+                               float scale, int accumulate, uint16_t* dH, float* dW,
+                               const Layout& L, char* ws, int nsm, cudaStream_t s) {
+  const int g8e = g8_exponent(cap, tau);
   int* status = reinterpret_cast<int*>(ws + L.hdr);
   const float* amax = reinterpret_cast<const float*>(ws + L.hdr + kHdrAmax);
   const auto u8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
@@ -587,13 +598,13 @@ ss_status enqueue_backward_fp8(const int32_t* cand, const int32_t* slot, const f
   const int iT = static_cast<int>(T), iV = static_cast<int>(V), iC = static_cast<int>(C),
             iD = static_cast<int>(D);
   trace_pre(s, "gemm_softmax_grad");
-  cudaError_t e = launch_softmax_grad_fp8(tH8, tW8, tG8s, tG8ts, iT, iC, iD, slot, lse, amax,
-                                          status, nsm, s);
+  cudaError_t e = launch_softmax_grad_fp8(tH8, tW8, tG8s, tG8ts, iT, iC, iD, slot, lse, cap, tau,
+                                          g8e, amax, status, nsm, s);
   trace_post(s);
   if (e != cudaSuccess) return fail("launch gemm_softmax_grad", e);
   trace_pre(s, "gemm_grads");
-  e = launch_grads_fp8(tG8, tW8t, tG8t, tH8t, iT, iC, iD, iV, accumulate, cand, scale, amax, dH,
-                       dW, status, nsm, s);
+  e = launch_grads_fp8(tG8, tW8t, tG8t, tH8t, iT, iC, iD, iV, accumulate, cand, scale, g8e, amax,
+                       dH, dW, status, nsm, s);
   trace_post(s);
   return e == cudaSuccess ? SS_OK : fail("launch gemm_grads", e);
 }
@@ -605,8 +616,8 @@ ss_status enqueue_backward(const uint16_t* H, const int32_t* cand, const int32_t
                            int accumulate, uint16_t* dH, float* dW, const Layout& L, char* ws,
                            int nsm, cudaStream_t s) {
   if (fp8 == 2)
-    return enqueue_backward_fp8(cand, slot, lse, T, V, C, D, scale, accumulate, dH, dW, L, ws, nsm,
-                                s);
+    return enqueue_backward_fp8(cand, slot, lse, T, V, C, D, cap, tau, scale, accumulate, dH, dW,
+                                L, ws, nsm, s);
   int* status = reinterpret_cast<int*>(ws + L.hdr);
   uint16_t* Wc = reinterpret_cast<uint16_t*>(ws + L.wc);
   uint16_t* G = reinterpret_cast<uint16_t*>(ws + L.g);
@@ -862,9 +873,7 @@ static ss_status head_args(const ss_head* head, float* cap, float* tau, int* fp8
   if (head && head->fp8 != 0) {
     if (head->fp8 != 1 && head->fp8 != 2) return SS_ERR_INVALID;
     if (!fp8) return SS_ERR_UNSUPPORTED;  // this entry point has no FP8 path
-    if (head->cap != 0.f) return SS_ERR_UNSUPPORTED;
     *fp8 = head->fp8;
-    return SS_OK;
   }
   if (!head || head->cap == 0.f) return SS_OK;
   if (!(head->cap > 0.f) || !std::isfinite(head->cap) || !(head->tau > 0.f) ||

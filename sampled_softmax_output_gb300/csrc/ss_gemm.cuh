@@ -383,23 +383,25 @@ struct EpiGT {
 };
 using EpiG = EpiGT<false>;
 
-// FP8 gradients: G is scaled by 2^kG8Exp, the largest power of two that keeps
-// its bound |P - Y| <= 1 within e5m2's largest finite value (57344), and
-// rounded to e5m2; the scale and the operand's e4m3 exponent come back out of
-// the gradient GEMMs' fp32 accumulators.
-constexpr int kG8Exp = 15;
-__device__ __forceinline__ float fp8_grad_alpha(float scale, const float* amax_b) {
-  return scale * exp2i(-(kG8Exp + e4m3_exponent(__ldcg(amax_b))));
+// FP8 gradients: G (before `scale`) is scaled by 2^g8e, the largest power of
+// two that keeps its bound -- |P - Y| <= 1, times dz/ds <= cap / (4 tau) with
+// the capped head -- within e5m2's largest finite value (57344) (g8e = 15 for
+// the plain head), and rounded to e5m2; the scale and the operand's e4m3
+// exponent come back out of the gradient GEMMs' fp32 accumulators.
+__device__ __forceinline__ float fp8_grad_alpha(float scale, int g8e, const float* amax_b) {
+  return scale * exp2i(-(g8e + e4m3_exponent(__ldcg(amax_b))));
 }
 
 // Backward, step 1 with FP8 gradients (e4m3 logit operands):
-//   G8[t, j] = e5m2(2^15 (exp(S[t,j] - lse[t]) - [j == slot[t]])),
+//   G8[t, j] = e5m2(2^g8e (exp(z[t,j] - lse[t]) - [j == slot[t]]) dz/ds)
+// (z = S and dz/ds = 1 for the plain head),
 // written twice through TMA bulk tensor stores: row-major G8 [T, C] (the
 // K-major A operand of dH = G W_c) and transposed G8t [C, T] (the K-major A
 // operand of dW_c = G^T H). Each 64-column quarter is staged as a 128 x 64-byte
 // tile in the 64-byte-swizzled layout of G8's map and a 64 x 128-byte tile in
 // the 128-byte-swizzled layout of G8t's map (16 KB per column group).
-struct EpiG8 {
+template <bool CAP>
+struct EpiG8T {
   static constexpr int kStageBytes = 4 * 16384;  // two 16 KB buffers per column group
   static constexpr bool kKeepOperands = true;
   struct Params {
@@ -410,9 +412,13 @@ struct EpiG8 {
     const float* lse;
     int* status;
     const float* amax;  // logits = accumulator * e4m3_logit_scale(amax)
+    HeadCap head;       // used when CAP
+    int g8e;            // G8 = e5m2(2^g8e (P - Y) dz/ds)
   };
+  // the plain head folds the e4m3 scale into the exponent's constant; the
+  // capped head needs the logit itself
   __device__ static void begin(const Params& p, EpiState& es) {
-    es.f0 = e4m3_logit_scale(p.amax) * kLog2e;
+    es.f0 = e4m3_logit_scale(p.amax) * (CAP ? 1.f : kLog2e);
   }
   __device__ static void finish(const Params&, EpiState& es) {
     if ((es.ep_tid & 127) == 0) bulk_wait<0>();
@@ -428,11 +434,10 @@ struct EpiG8 {
     const int sl = valid ? __ldg(p.slot + t) : -1;
     if (valid && nt == 0 && static_cast<unsigned>(sl) >= static_cast<unsigned>(p.C))
       set_status(p.status, SS_ERR_INDEX);
-    // the e4m3 scale (a power of two) folded into the exponent's constant
-    const float k2 = es.f0;
-    // 2^15 exp(s - lse) = 2^(s log2e - (lse log2e - 15))
-    const float off2 = valid ? fmaf(__ldg(p.lse + t), kLog2e, -static_cast<float>(kG8Exp)) : 0.f;
-    const float one_hot = static_cast<float>(1 << kG8Exp);
+    const float k2 = es.f0;  // plain: scale * log2e; capped: the logit scale
+    // 2^g8e exp(z - lse) = 2^(z log2e - (lse log2e - g8e))
+    const float off2 = valid ? fmaf(__ldg(p.lse + t), kLog2e, -static_cast<float>(p.g8e)) : 0.f;
+    const float one_hot = exp2i(p.g8e);
     const int j0 = nt * BN;
     const int ncols = min(BN, p.C - j0);
     // this thread's byte in row jj of the transposed tile: 16-byte chunk
@@ -462,12 +467,21 @@ struct EpiG8 {
         tmem_ld_wait();
         const int off = sl - j0 - jc;
         float g[32];
+        if constexpr (CAP) {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) g[i] = ex2_approx(fmaf(__uint_as_float(r[i]), k2, -off2));
-        if (__any_sync(0xffffffffu, static_cast<unsigned>(off) < 32u)) {
+          for (int i = 0; i < 32; ++i) {
+            const float z = head_z(__uint_as_float(r[i]) * k2, p.head);
+            const float y = i == off ? one_hot : 0.f;
+            g[i] = (ex2_approx(fmaf(z, kLog2e, -off2)) - y) * head_dz(z, p.head);
+          }
+        } else {
 #pragma unroll
-          for (int i = 0; i < 32; ++i)
-            if (i == off) g[i] -= one_hot;
+          for (int i = 0; i < 32; ++i) g[i] = ex2_approx(fmaf(__uint_as_float(r[i]), k2, -off2));
+          if (__any_sync(0xffffffffu, static_cast<unsigned>(off) < 32u)) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              if (i == off) g[i] -= one_hot;
+          }
         }
         uint16_t pr[16];
 #pragma unroll
@@ -503,6 +517,8 @@ struct EpiG8 {
   }
 };
 
+using EpiG8 = EpiG8T<false>;
+
 // Backward, step 2: dH tile -> bf16 (column group cg of NCG). F8G: the
 // accumulator is of e5m2 G and e4m3 W_c, times fp8_grad_alpha.
 template <bool F8G = false>
@@ -514,9 +530,10 @@ struct EpiDhT {
     uint16_t* dH;
     float scale;         // used when F8G
     const float* amax;   // used when F8G: max |W_c|
+    int g8e;             // used when F8G: G8's power of two
   };
   __device__ static void begin(const Params& p, EpiState& es) {
-    if constexpr (F8G) es.f0 = fp8_grad_alpha(p.scale, p.amax);
+    if constexpr (F8G) es.f0 = fp8_grad_alpha(p.scale, p.g8e, p.amax);
   }
   __device__ static void finish(const Params&, EpiState&) {}
   template <int BN, int NCG>
@@ -563,9 +580,10 @@ struct EpiDwT {
     int* status;
     float scale;         // used when F8G
     const float* amax;   // used when F8G: max |H|
+    int g8e;             // used when F8G: G8's power of two
   };
   __device__ static void begin(const Params& p, EpiState& es) {
-    if constexpr (F8G) es.f0 = fp8_grad_alpha(p.scale, p.amax);
+    if constexpr (F8G) es.f0 = fp8_grad_alpha(p.scale, p.g8e, p.amax);
   }
   __device__ static void finish(const Params&, EpiState&) {}
   template <int BN, int NCG>

@@ -469,7 +469,7 @@ cudaError_t launch_grads(const CUtensorMap& tG_kmaj, const CUtensorMap& tWc_mn,
 
 cudaError_t launch_grads_fp8(const CUtensorMap& tG8, const CUtensorMap& tW8t,
                              const CUtensorMap& tG8t, const CUtensorMap& tH8t, int T, int C, int D,
-                             int V, int accumulate, const int32_t* cand, float scale,
+                             int V, int accumulate, const int32_t* cand, float scale, int g8e,
                              const float* amax, uint16_t* dH, float* dW, int* status, int num_sms,
                              cudaStream_t stream) {
   constexpr int KB = 2 * BK;
@@ -480,8 +480,8 @@ cudaError_t launch_grads_fp8(const CUtensorMap& tG8, const CUtensorMap& tW8t,
   p.kb_dw = (T + KB - 1) / KB;
   p.kb_dh = (C + KB - 1) / KB;
   p.n_units = p.n_dw + n_dh;
-  p.dh = EpiDhT<true>::Params{T, D, dH, scale, amax + 1};
-  p.dw = EpiDwT<true>::Params{C, D, V, accumulate, cand, dW, status, scale, amax};
+  p.dh = EpiDhT<true>::Params{T, D, dH, scale, amax + 1, g8e};
+  p.dw = EpiDwT<true>::Params{C, D, V, accumulate, cand, dW, status, scale, amax, g8e};
   p.status = status;
   const int pairs = std::min(num_sms / 2, kSchedMaxCtas);
   // the balanced schedule where it fits the kernel parameters, else every

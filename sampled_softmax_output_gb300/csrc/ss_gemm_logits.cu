@@ -13,9 +13,13 @@ cudaError_t launch_forward_logits(const CUtensorMap& tH, const CUtensorMap& tWc,
                                   int D, const int32_t* slot, float2* part, float* tgt,
                                   float cap, float tau, const Targets& tg, const float* amax,
                                   int* status, int num_sms, cudaStream_t stream) {
-  if (amax)  // the FP8 head (plain logits, one target per token)
-    return forward_logits<false, 1, true>(tH, tWc, T, C, D, slot, part, tgt, head_cap(0.f, 1.f),
-                                          tg, amax, status, num_sms, stream);
+  if (amax) {  // the FP8 head (one target per token)
+    const HeadCap h = head_cap(cap, tau);
+    return cap > 0.f ? forward_logits<true, 1, true>(tH, tWc, T, C, D, slot, part, tgt, h, tg,
+                                                     amax, status, num_sms, stream)
+                     : forward_logits<false, 1, true>(tH, tWc, T, C, D, slot, part, tgt, h, tg,
+                                                      amax, status, num_sms, stream);
+  }
   if (tg.K > 1)
     return launch_forward_logits_mtp(tH, tWc, T, C, D, slot, part, tgt, cap, tau, tg, status,
                                      num_sms, stream);
@@ -32,9 +36,15 @@ cudaError_t launch_softmax_grad(const CUtensorMap& tH, const CUtensorMap& tWc,
                                 const int32_t* slot, const float* lse, float scale, float cap,
                                 float tau, const Targets& tg, const float* amax, int* status,
                                 int num_sms, cudaStream_t stream) {
-  if (amax)
-    return softmax_grad<false, 1, true>(tH, tWc, tWc_half, tG_store, T, C, D, slot, lse, scale,
-                                        head_cap(0.f, 1.f), tg, amax, status, num_sms, stream);
+  if (amax) {
+    const HeadCap h = head_cap(cap, tau);
+    return cap > 0.f ? softmax_grad<true, 1, true>(tH, tWc, tWc_half, tG_store, T, C, D, slot,
+                                                   lse, scale, h, tg, amax, status, num_sms,
+                                                   stream)
+                     : softmax_grad<false, 1, true>(tH, tWc, tWc_half, tG_store, T, C, D, slot,
+                                                    lse, scale, h, tg, amax, status, num_sms,
+                                                    stream);
+  }
   if (tg.K > 1)
     return launch_softmax_grad_mtp(tH, tWc, tWc_half, tG_store, T, C, D, slot, lse, scale, cap,
                                    tau, tg, status, num_sms, stream);
@@ -45,13 +55,14 @@ cudaError_t launch_softmax_grad(const CUtensorMap& tH, const CUtensorMap& tWc,
                                             scale, h, tg, nullptr, status, num_sms, stream);
 }
 
-// FP8 gradients: G8 and G8^T in e5m2 from the e4m3 logits (one target, plain head)
-cudaError_t launch_softmax_grad_fp8(const CUtensorMap& tH8, const CUtensorMap& tW8,
-                                    const CUtensorMap& tG8_store, const CUtensorMap& tG8t_store,
-                                    int T, int C, int D, const int32_t* slot, const float* lse,
-                                    const float* amax, int* status, int num_sms,
-                                    cudaStream_t stream) {
-  EpiG8::Params ep;
+// FP8 gradients: G8 and G8^T in e5m2 from the e4m3 logits (one target)
+template <bool CAP>
+cudaError_t softmax_grad_fp8(const CUtensorMap& tH8, const CUtensorMap& tW8,
+                             const CUtensorMap& tG8_store, const CUtensorMap& tG8t_store, int T,
+                             int C, int D, const int32_t* slot, const float* lse, float cap,
+                             float tau, int g8e, const float* amax, int* status, int num_sms,
+                             cudaStream_t stream) {
+  typename EpiG8T<CAP>::Params ep;
   ep.tmG = tG8_store;
   ep.tmGt = tG8t_store;
   ep.T = T;
@@ -60,10 +71,22 @@ cudaError_t launch_softmax_grad_fp8(const CUtensorMap& tH8, const CUtensorMap& t
   ep.lse = lse;
   ep.status = status;
   ep.amax = amax;
+  ep.head = head_cap(cap, tau);
+  ep.g8e = g8e;
   GemmShape shp{(T + BM - 1) / BM, (C + kBnLogits - 1) / kBnLogits, D / (2 * BK)};
-  return launch_gemm<kBnLogits, kStagesGradF8, false, false, EpiG8, 8, true>(tH8, tW8, shp, ep,
-                                                                             status, num_sms,
-                                                                             stream);
+  return launch_gemm<kBnLogits, kStagesGradF8, false, false, EpiG8T<CAP>, 8, true>(
+      tH8, tW8, shp, ep, status, num_sms, stream);
+}
+
+cudaError_t launch_softmax_grad_fp8(const CUtensorMap& tH8, const CUtensorMap& tW8,
+                                    const CUtensorMap& tG8_store, const CUtensorMap& tG8t_store,
+                                    int T, int C, int D, const int32_t* slot, const float* lse,
+                                    float cap, float tau, int g8e, const float* amax, int* status,
+                                    int num_sms, cudaStream_t stream) {
+  return cap > 0.f ? softmax_grad_fp8<true>(tH8, tW8, tG8_store, tG8t_store, T, C, D, slot, lse,
+                                            cap, tau, g8e, amax, status, num_sms, stream)
+                   : softmax_grad_fp8<false>(tH8, tW8, tG8_store, tG8t_store, T, C, D, slot, lse,
+                                             cap, tau, g8e, amax, status, num_sms, stream);
 }
 
 }  // namespace ss

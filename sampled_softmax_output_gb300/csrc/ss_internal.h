@@ -99,14 +99,15 @@ cudaError_t launch_softmax_grad(const CUtensorMap& tH, const CUtensorMap& tWc,
                                 const int32_t* slot, const float* lse, float scale, float cap,
                                 float tau, const Targets& tg, const float* amax, int* status,
                                 int num_sms, cudaStream_t stream);
-// FP8 gradients (plain logits, one target): tH8 / tW8 as for amax above;
-// G8 [T, C] e5m2 through tG8_store (box 64 x 128 bytes, 64-byte swizzle) and
-// G8^T [C, T] through tG8t_store (box 128 x 64 bytes, 128-byte swizzle).
+// FP8 gradients (one target; cap > 0: the capped head): tH8 / tW8 as for
+// amax above; G8 = e5m2(2^g8e (P - Y) dz/ds) [T, C] through tG8_store (box
+// 64 x 128 bytes, 64-byte swizzle) and G8^T [C, T] through tG8t_store (box
+// 128 x 64 bytes, 128-byte swizzle).
 cudaError_t launch_softmax_grad_fp8(const CUtensorMap& tH8, const CUtensorMap& tW8,
                                     const CUtensorMap& tG8_store, const CUtensorMap& tG8t_store,
                                     int T, int C, int D, const int32_t* slot, const float* lse,
-                                    const float* amax, int* status, int num_sms,
-                                    cudaStream_t stream);
+                                    float cap, float tau, int g8e, const float* amax, int* status,
+                                    int num_sms, cudaStream_t stream);
 // the same GEMMs for K > 1 targets per token (ss_gemm_logits_mtp.cu)
 cudaError_t launch_forward_logits_mtp(const CUtensorMap& tH, const CUtensorMap& tWc, int T, int C,
                                       int D, const int32_t* slot, float2* part, float* tgt,
@@ -136,10 +137,11 @@ cudaError_t launch_grads(const CUtensorMap& tG_kmaj, const CUtensorMap& tWc_mn,
 // FP8 gradients: dH = G8 . W8 and dW[cand] (=|+=) G8^T . H8 on e5m2 x e4m3,
 // all operands K-major in boxes of 128 x 128 bytes: tG8 [T, C], tW8t [D, C],
 // tG8t [C, T], tH8t [D, T]; the accumulators times scale * 2^-(15 + e) with e
-// the other operand's e4m3 exponent (amax[0] = max |H|, amax[1] = max |W_c|).
+// the other operand's e4m3 exponent (amax[0] = max |H|, amax[1] = max |W_c|)
+// and g8e G8's power of two.
 cudaError_t launch_grads_fp8(const CUtensorMap& tG8, const CUtensorMap& tW8t,
                              const CUtensorMap& tG8t, const CUtensorMap& tH8t, int T, int C, int D,
-                             int V, int accumulate, const int32_t* cand, float scale,
+                             int V, int accumulate, const int32_t* cand, float scale, int g8e,
                              const float* amax, uint16_t* dH, float* dW, int* status, int num_sms,
                              cudaStream_t stream);
 

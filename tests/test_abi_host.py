@@ -263,7 +263,7 @@ def test_several_targets_argument_errors():
 
 
 def test_fp8_head_argument_errors():
-    """The FP8 head needs plain logits (cap 0) and D % 128 == 0; the
+    """The FP8 head (capped or not) needs D % 128 == 0; the
     several-targets entry points have no FP8 path; fp8 must be 0, 1 or 2."""
     L = ss.lib()
 
@@ -273,10 +273,11 @@ def test_fp8_head_argument_errors():
                               16, None)
 
     assert step(ctypes.byref(ss.Head(0.0, 1.0, 1))) == WORKSPACE       # the FP8 head is accepted
-    assert step(ctypes.byref(ss.Head(30.0, 7.5, 1))) == UNSUPPORTED    # cap with FP8
+    assert step(ctypes.byref(ss.Head(30.0, 7.5, 1))) == WORKSPACE      # capped FP8 head
     assert step(ctypes.byref(ss.Head(0.0, 1.0, 1)), D=192) == UNSUPPORTED
     assert step(ctypes.byref(ss.Head(0.0, 1.0, 2))) == WORKSPACE       # FP8 gradients too
-    assert step(ctypes.byref(ss.Head(30.0, 7.5, 2))) == UNSUPPORTED
+    assert step(ctypes.byref(ss.Head(30.0, 7.5, 2))) == WORKSPACE
+    assert step(ctypes.byref(ss.Head(-1.0, 7.5, 2))) == INVALID
     assert step(ctypes.byref(ss.Head(0.0, 1.0, 2)), D=192) == UNSUPPORTED
     assert step(ctypes.byref(ss.Head(0.0, 1.0, 3))) == INVALID
     assert step(ctypes.byref(ss.Head(0.0, 1.0, -1))) == INVALID

@@ -147,3 +147,62 @@ def test_fp8_graph_replay_equals_direct_step(mode):
         for k in ("cand", "slot", "loss", "lse", "dH", "dW"):
             assert torch.equal(got[k], ref[k]), (seed, k)
     g.close()
+
+
+@pytest.mark.parametrize("mode", [1, 2])
+@pytest.mark.parametrize("cap,tau", [(30.0, 7.5), (6.0, 0.7)])
+def test_capped_fp8_head_parity(orc, mode, cap, tau):
+    """The pages' head, FP8 and soft-capped: z = cap / (1 + exp(-s / tau)) of
+    the e4m3 logits, and (mode 2) G8 = e5m2(2^e (P - Y) dz/ds), e from the
+    bound cap / (4 tau), against the oracle of the same head."""
+    T, V, D, C, seed, scale = 300, 3000, 768, 517, 11, 0.5
+    x = synth.make_inputs(T, V, D, 1.1, seed)
+    C = max(C, len(np.unique(x["targets"])))
+    ref = orc.loss_and_grads_fp8(x["H"], x["W"], x["targets"], C, seed, scale, grads=mode == 2,
+                                 cap=cap, tau=tau)
+    H, W = to_dev_bf16(x["H"]), to_dev_bf16(x["W"])
+    tg = torch.from_numpy(x["targets"]).cuda()
+    ws = ss.workspace(T, V, C, D)
+    got = ss.step(H, W, tg, C, seed, ws, scale=scale, fp8=mode, cap=cap, tau=tau)
+    sep = ss.step_separate(H, W, tg, C, seed, ss.workspace(T, V, C, D), scale=scale, fp8=mode,
+                           cap=cap, tau=tau)
+    torch.cuda.synchronize()
+    assert ss.read_status(ws)[0] == 0
+    for k in ("cand", "slot", "loss", "lse", "dH", "dW"):
+        assert torch.equal(got[k], sep[k]), k
+    assert_loss_close(got["loss"].cpu().numpy(), ref["loss"])
+    assert_loss_close(got["lse"].cpu().numpy(), ref["lse"])
+    assert rel_fro(got["dH"].float().cpu().numpy(), ref["dH"]) < GRAD_RTOL
+    assert rel_fro(got["dW"].cpu().numpy(), ref["dW"]) < GRAD_RTOL
+    plain = orc.loss_and_grads_fp8(x["H"], x["W"], x["targets"], C, seed, scale, grads=mode == 2)
+    assert np.abs(plain["loss"] - ref["loss"]).max() > 1e-3  # and the cap is applied
+
+
+def test_capped_fp8_gradients_full_size(orc):
+    """T16384_C10240 with the capped FP8 head and FP8 gradients (cap 30, tau
+    7.5): cand bit-exact, sampled token rows of loss, lse and dH, and exact
+    candidate rows of dW, against the oracle."""
+    w = synth.WORKLOADS[2]
+    cap, tau = 30.0, 7.5
+    x = synth.workload_inputs(w)
+    H, W = to_dev_bf16(x["H"]), to_dev_bf16(x["W"])
+    tg = torch.from_numpy(x["targets"]).cuda()
+    ws = ss.workspace(w.T, w.V, w.C, w.D)
+    scale = 1.0 / w.T
+    got = ss.step(H, W, tg, w.C, w.seed, ws, scale=scale, fp8=2, cap=cap, tau=tau)
+    torch.cuda.synchronize()
+    assert ss.read_status(ws)[0] == 0
+    cand, slot, _ = orc.build_candidates(x["targets"], w.V, w.C, w.seed)
+    np.testing.assert_array_equal(got["cand"].cpu().numpy(), cand)
+    Hq, Wq, _, _ = orc.fp8_inputs(x["H"], x["W"], cand)
+    rng = np.random.default_rng(32)
+    rows = np.unique(np.concatenate([[0, w.T - 1], rng.integers(0, w.T, 40)]))
+    l_ref, s_ref = orc.forward(Hq, Wq, cand, slot, rows=rows, cap=cap, tau=tau)
+    assert_loss_close(got["loss"].cpu().numpy()[rows], l_ref)
+    assert_loss_close(got["lse"].cpu().numpy()[rows], s_ref)
+    dH_ref = orc.backward_dH_g8(Hq, Wq, cand, slot, s_ref, scale, rows=rows, cap=cap, tau=tau)
+    assert rel_fro(got["dH"].float().cpu().numpy()[rows], dH_ref) < GRAD_RTOL
+    _, lse_all = orc.forward(Hq, Wq, cand, slot, cap=cap, tau=tau)
+    cols = np.array([0, 1, w.C // 2, w.C - 1])
+    ref_rows = orc.backward_dWc_g8(Hq, Wq, cand, slot, lse_all, scale, cols=cols, cap=cap, tau=tau)
+    assert rel_fro(got["dW"].cpu().numpy()[cand[cols]], ref_rows) < GRAD_RTOL

@@ -390,10 +390,14 @@ MUTATIONS = [
      "return m <= 0.875f ? 10 - k : 9 - k;"),
     ("FP8 gradients: e5m2 grid one bit too fine", "const float q = ldexpf(1.0f, E - 2);",
      "const float q = ldexpf(1.0f, E - 3);"),
-    ("FP8 gradients: G not rounded", "return orc_round_e5m2(ldexpf(expf(s - lse) - y, 15));",
-     "return ldexpf(expf(s - lse) - y, 15);"),
-    ("FP8 gradients: wrong power-of-two scale", "const float f = ldexpf(scale, -15);\n#pragma omp parallel\n",
-     "const float f = ldexpf(scale, -14);\n#pragma omp parallel\n"),
+    ("FP8 gradients: G not rounded",
+     "return orc_round_e5m2(ldexpf((expf(z - lse) - y) * head_dz_f32(z, cap, tau), e));",
+     "return ldexpf((expf(z - lse) - y) * head_dz_f32(z, cap, tau), e);"),
+    ("FP8 gradients: wrong power-of-two scale", "const float f = ldexpf(scale, -e);\n#pragma omp parallel\n",
+     "const float f = ldexpf(scale, 1 - e);\n#pragma omp parallel\n"),
+    ("FP8 gradients: capped dz/ds dropped", "* head_dz_f32(z, cap, tau), e));", ", e));"),
+    ("FP8 gradients: exponent bound doubled", "while (B * ldexp(1.0, e + 1) <= 57344.0) ++e;",
+     "while (B * ldexp(1.0, e + 1) <= 114688.0) ++e;"),
 ]
 
 
@@ -450,6 +454,11 @@ def _battery(orc):
         failed.append("e4m3 scale exponent")
     if _fp8_grad_closed_form_mismatch(orc):
         failed.append("fp8 gradients")
+    if _g8_exponent_mismatch(orc):
+        failed.append("fp8 gradient exponent")
+    for k in (4.0, 8.0):
+        if _fp8_grad_closed_form_mismatch(orc, cap_over_tau=k):
+            failed.append(f"capped fp8 gradients {k}")
     return failed
 
 
@@ -763,33 +772,64 @@ def test_e5m2_grid_is_fixed_and_ties_go_to_even(orc):
     assert orc.round_e5m2(1e6) == 57344.0 and orc.round_e5m2(-60000.0) == -57344.0
 
 
-def _fp8_grad_closed_form_mismatch(orc):
+def _fp8_grad_closed_form_mismatch(orc, cap_over_tau=0.0):
     """FP8 gradients at H = 0 with C = 32: every logit is 0, P = 1/32, so
     2^15 P = 1024 is on the e5m2 grid while the target entry 2^15 (1/32 - 1)
     = -31744 rounds to -32768 (spacing 4096 in that binade, not a tie):
     dH[t] = scale (sum_j W_q[cand[j]] / 32 - (33/32) W_q[y_t]) and dW = 0,
-    where the exact-G gradient would have (32/32) W_q[y_t]."""
+    where the exact-G gradient would have (32/32) W_q[y_t].
+    With the capped head (cap = k tau), z = cap / 2 everywhere, so P is the
+    same and dz/ds = k / 4: the bound k / 4 moves the exponent to 15 - log2(k/4)
+    and the same e5m2 values come out, times k / 4."""
     T, V, D, C, seed, scale = 4, 64, 16, 32, 33, 0.75
+    tau = 1.5
+    cap = cap_over_tau * tau
     x = synth.make_inputs(T, V, D, 1.1, seed)
     H0 = np.zeros_like(x["H"])
-    r = orc.loss_and_grads_fp8(H0, x["W"], x["targets"], C, seed, scale, grads=True)
+    r = orc.loss_and_grads_fp8(H0, x["W"], x["targets"], C, seed, scale, grads=True, cap=cap,
+                               tau=tau)
     Wq = synth.bf16_bits_to_f32(orc.fp8_inputs(H0, x["W"], r["cand"])[1]).astype(np.float64)
     Wc = Wq[r["cand"]]
     y = Wq[x["targets"]]
-    expect = scale * (Wc.sum(0)[None, :] / 32.0 - (33.0 / 32.0) * y)
-    plain = scale * (Wc.sum(0)[None, :] / 32.0 - y)
+    f = cap_over_tau / 4.0 if cap_over_tau else 1.0
+    expect = f * scale * (Wc.sum(0)[None, :] / 32.0 - (33.0 / 32.0) * y)
+    plain = f * scale * (Wc.sum(0)[None, :] / 32.0 - y)
     bad = not np.allclose(r["dH"], expect, rtol=1e-5, atol=1e-7)
     bad |= np.allclose(r["dH"], plain, rtol=1e-5, atol=1e-7)
     bad |= bool(np.any(r["dW"] != 0))
-    bad |= not np.allclose(r["loss"], np.log(32.0), rtol=1e-6)
+    z0 = cap / 2.0 if cap_over_tau else 0.0
+    bad |= not np.allclose(r["lse"], z0 + np.log(32.0), rtol=1e-6)
     return bad
+
+
+def _g8_exponent_mismatch(orc):
+    if orc.g8_exponent(0.0, 1.0) != 15 or orc.g8_exponent(30.0, 7.5) != 15:
+        return True
+    for cap, tau in ((4.0, 0.5), (100.0, 1.0), (1.0, 10.0), (3.0, 7.0)):
+        B = cap / (4.0 * tau)
+        e = orc.g8_exponent(cap, tau)
+        if not B * 2.0 ** e <= 57344.0 < B * 2.0 ** (e + 1):
+            return True
+    return False
+
+
+def test_fp8_gradient_exponent_is_the_largest_that_fits(orc):
+    """2^15 for the plain head (|P - Y| <= 1); for the capped head the bound is
+    cap / (4 tau), the largest dz/ds (at z = cap / 2)."""
+    assert not _g8_exponent_mismatch(orc)
+
+
+@pytest.mark.parametrize("k", [4.0, 8.0])
+def test_capped_fp8_gradients_closed_form_at_zero_H(orc, k):
+    assert not _fp8_grad_closed_form_mismatch(orc, cap_over_tau=k)
 
 
 def test_fp8_gradients_closed_form_at_zero_H(orc):
     assert not _fp8_grad_closed_form_mismatch(orc)
 
 
-def test_fp8_gradients_within_the_e5m2_rounding_bound(orc):
+@pytest.mark.parametrize("cap,tau", [(0.0, 1.0), (30.0, 7.5), (6.0, 0.7)])
+def test_fp8_gradients_within_the_e5m2_rounding_bound(orc, cap, tau):
     """On ordinary inputs the FP8-gradient dH and dW_c differ from the
     exact-G gradients on the same rounded operands by no more than the e5m2
     rounding bound: half a unit in the last place (2^-3 relative for normals,
@@ -797,18 +837,24 @@ def test_fp8_gradients_within_the_e5m2_rounding_bound(orc):
     operand (plus fp32 slack); and they do differ."""
     T, V, D, C, seed, scale = 24, 300, 32, 80, 34, 0.5
     x, C = _case(T, V, D, C, seed)
-    a = orc.loss_and_grads_fp8(x["H"], x["W"], x["targets"], C, seed, scale, grads=True)
-    b = orc.loss_and_grads_fp8(x["H"], x["W"], x["targets"], C, seed, scale, grads=False)
+    a = orc.loss_and_grads_fp8(x["H"], x["W"], x["targets"], C, seed, scale, grads=True,
+                               cap=cap, tau=tau)
+    b = orc.loss_and_grads_fp8(x["H"], x["W"], x["targets"], C, seed, scale, grads=False,
+                               cap=cap, tau=tau)
     cand, slot = a["cand"], a["slot"]
     Hq, Wq, _, _ = orc.fp8_inputs(x["H"], x["W"], cand)
     H64 = synth.bf16_bits_to_f32(Hq).astype(np.float64)
     Wc64 = synth.bf16_bits_to_f32(Wq[cand]).astype(np.float64)
     S = H64 @ Wc64.T
-    P = np.exp(S - a["lse"].astype(np.float64)[:, None])
+    Z = cap / (1.0 + np.exp(-S / tau)) if cap else S
+    dz = Z * (cap - Z) / (cap * tau) if cap else np.ones_like(S)
+    P = np.exp(Z - a["lse"].astype(np.float64)[:, None])
     G = P.copy()
     G[np.arange(T), slot] -= 1.0
-    err = 2.0 ** -3 * np.abs(G) + 2.0 ** -32  # per entry, in units of G
-    slack = 1e-5
+    G *= dz
+    e = orc.g8_exponent(cap, tau)
+    err = 2.0 ** -3 * np.abs(G) + 2.0 ** -(17 + e)  # half an ulp, in units of G
+    slack = 1e-4
     bH = abs(scale) * ((err + slack * np.abs(G)) @ np.abs(Wc64))
     bW = abs(scale) * ((err + slack * np.abs(G)).T @ np.abs(H64))
     assert np.all(np.abs(a["dH"] - b["dH"]) <= bH + 1e-9)
