@@ -153,10 +153,17 @@ struct EpiFwdT {
       sl[k] = (valid && k < K) ? __ldg(p.slot + static_cast<size_t>(k) * p.T + t) : -1;
     const int j0 = nt * BN + cg * CPG * 32;  // first column of this group
     const int ncols = min(CPG * 32, p.C - j0);
-    float m = -INFINITY, s = 0.f, tg[KMAX];
+    float s = 0.f, tg[KMAX];
     uint32_t has_t = 0u;  // bit k: target k lies in this group's columns
     float sig = 1.f;
     if constexpr (F8) sig = es.f0;
+    // capped head: the e4m3 scale folds into the cap's exponent constant, and
+    // z < cap, so (for cap <= 64, where exp(z - cap) stays normal) cap itself
+    // is the softmax offset and no running max is needed
+    HeadCap hz = p.head;
+    if constexpr (CAP && F8) hz.k1 *= sig;
+    const bool fixed = CAP && p.head.cap <= 64.f;  // uniform
+    float m = fixed && ncols > 0 ? p.head.cap : -INFINITY;
     // Plain head: v holds the raw accumulator and the logit is v * vs (the
     // FP8 scale is a power of two, so it commutes exactly with the max and
     // folds into the exponent's constant); capped head: v = z, vs = 1.
@@ -171,12 +178,22 @@ struct EpiFwdT {
 #pragma unroll
         for (int k = 0; k < 32; ++k) {
           const float acc = __uint_as_float(r[k]);
-          v[k] = CAP ? head_z(F8 ? acc * sig : acc, p.head) : acc;
+          v[k] = CAP ? head_z(acc, hz) : acc;
         }
         float cm = -INFINITY;
         float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
         float nm;
-        if (nv == 32) {  // a full chunk (all but a ragged tail): no per-column predicates
+        if (CAP && fixed) {  // offset cap: no max, no rescale
+          nm = m;
+          const float nm2 = nm * kLog2e;
+#pragma unroll
+          for (int k = 0; k < 32; k += 4) {
+            if (nv == 32 || k + 0 < nv) a0 += ex2_approx(fmaf(v[k + 0], kLog2e, -nm2));
+            if (nv == 32 || k + 1 < nv) a1 += ex2_approx(fmaf(v[k + 1], kLog2e, -nm2));
+            if (nv == 32 || k + 2 < nv) a2 += ex2_approx(fmaf(v[k + 2], kLog2e, -nm2));
+            if (nv == 32 || k + 3 < nv) a3 += ex2_approx(fmaf(v[k + 3], kLog2e, -nm2));
+          }
+        } else if (nv == 32) {  // a full chunk (all but a ragged tail): no per-column predicates
 #pragma unroll
           for (int k = 0; k < 32; ++k) cm = fmaxf(cm, v[k]);
           nm = fmaxf(m, cm * vs);
@@ -202,8 +219,12 @@ struct EpiFwdT {
             if (k + 3 < nv) a3 += ex2_approx(fmaf(v[k + 3], k2, -nm2));
           }
         }
-        s = s * ex2_approx((m - nm) * kLog2e) + ((a0 + a1) + (a2 + a3));
-        m = nm;
+        if (CAP && fixed) {
+          s += (a0 + a1) + (a2 + a3);
+        } else {
+          s = s * ex2_approx((m - nm) * kLog2e) + ((a0 + a1) + (a2 + a3));
+          m = nm;
+        }
 #pragma unroll
         for (int k = 0; k < KMAX; ++k) {
           if (k >= K) break;  // uniform
@@ -292,6 +313,8 @@ struct EpiGT {
     float sig = 1.f;
     if constexpr (F8) sig = es.f0;
     const float k2 = sig * kLog2e;
+    HeadCap hz = p.head;  // capped: the e4m3 scale folded into the exponent constant
+    if constexpr (CAP && F8) hz.k1 *= sig;
     const uint32_t sgn = p.scale < 0.f ? 0x80008000u : 0u;
     const float off2 = valid ? fmaf(__ldg(p.lse + t), kLog2e, -p.log2_scale) : 0.f;
     const int j0 = nt * BN;
@@ -320,11 +343,8 @@ struct EpiGT {
         for (int i = 0; i < 16; ++i) {
           float g0, g1;
           if constexpr (CAP) {
-            const float x0 = F8 ? __uint_as_float(r[2 * i]) * sig : __uint_as_float(r[2 * i]);
-            const float x1 =
-                F8 ? __uint_as_float(r[2 * i + 1]) * sig : __uint_as_float(r[2 * i + 1]);
-            const float z0 = head_z(x0, p.head);
-            const float z1 = head_z(x1, p.head);
+            const float z0 = head_z(__uint_as_float(r[2 * i]), hz);
+            const float z1 = head_z(__uint_as_float(r[2 * i + 1]), hz);
             g0 = ex2_approx(fmaf(z0, kLog2e, -off2)) * head_dz(z0, p.head);
             g1 = ex2_approx(fmaf(z1, kLog2e, -off2)) * head_dz(z1, p.head);
           } else {  // sig (a power of two) folded into the constant: the same value
@@ -348,7 +368,7 @@ struct EpiGT {
             float xt = 0.f;
 #pragma unroll
             for (int i = 0; i < 32; ++i) xt = (i == off) ? __uint_as_float(r[i]) : xt;
-            if constexpr (F8) xt *= sig;
+            if constexpr (F8 && !CAP) xt *= sig;  // capped: hz carries the scale
             if (has) {
               // the one-hot weight of this column: every target k2 that falls on it
               float wt = 1.f;
@@ -359,7 +379,7 @@ struct EpiGT {
               }
               float gt;
               if constexpr (CAP) {
-                const float zt = head_z(xt, p.head);
+                const float zt = head_z(xt, hz);
                 gt = (ex2_approx(fmaf(zt, kLog2e, -off2)) - asc * wt) * head_dz(zt, p.head);
               } else {
                 gt = ex2_approx(fmaf(xt, kLog2e, -off2)) - asc * wt;
@@ -435,6 +455,8 @@ struct EpiG8T {
     if (valid && nt == 0 && static_cast<unsigned>(sl) >= static_cast<unsigned>(p.C))
       set_status(p.status, SS_ERR_INDEX);
     const float k2 = es.f0;  // plain: scale * log2e; capped: the logit scale
+    HeadCap hz = p.head;     // capped: the logit scale folded into the exponent constant
+    if constexpr (CAP) hz.k1 *= k2;
     // 2^g8e exp(z - lse) = 2^(z log2e - (lse log2e - g8e))
     const float off2 = valid ? fmaf(__ldg(p.lse + t), kLog2e, -static_cast<float>(p.g8e)) : 0.f;
     const float one_hot = exp2i(p.g8e);
@@ -470,7 +492,7 @@ struct EpiG8T {
         if constexpr (CAP) {
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
-            const float z = head_z(__uint_as_float(r[i]) * k2, p.head);
+            const float z = head_z(__uint_as_float(r[i]), hz);
             const float y = i == off ? one_hot : 0.f;
             g[i] = (ex2_approx(fmaf(z, kLog2e, -off2)) - y) * head_dz(z, p.head);
           }
