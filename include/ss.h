@@ -304,6 +304,15 @@ ss_status ss_step_graph_create(const int32_t* targets, const uint16_t* H, const 
                                float scale, int accumulate, int32_t* cand, int32_t* slot,
                                float* loss, float* lse, uint16_t* dH, float* dW, void* workspace,
                                size_t workspace_bytes, ss_step_graph** graph);
+/* The same for ss_step_mtp: K weighted targets per token (targets [K, T],
+ * slot [K, T]); its errors are those of ss_step_mtp's argument checks, or
+ * SS_ERR_CUDA. The graph is launched and destroyed as above. */
+ss_status ss_step_graph_create_mtp(const int32_t* targets, int64_t K, const float* weights,
+                                   const uint16_t* H, const uint16_t* W, int64_t T, int64_t V,
+                                   int64_t C, int64_t D, const ss_head* head, float scale,
+                                   int accumulate, int32_t* cand, int32_t* slot, float* loss,
+                                   float* lse, uint16_t* dH, float* dW, void* workspace,
+                                   size_t workspace_bytes, ss_step_graph** graph);
 ss_status ss_step_graph_launch(ss_step_graph* graph, uint64_t seed, ss_stream stream);
 void ss_step_graph_destroy(ss_step_graph* graph);
 
@@ -321,7 +330,7 @@ void ss_step_graph_destroy(ss_step_graph* graph);
  * fixed-size array inside the library's own device data, of
  * SS_NOALLOC_SCRATCH_BYTES. Every GPU that loads the library holds that array
  * until the process exits. Sizes whose scratch, 1 KB + C*D*2 +
- * ceil(C/256)*T*16 + T*4 bytes (each term rounded up to 1 KB), exceeds it are
+ * ceil(C/256)*T*16 + T*32 bytes (each term rounded up to 1 KB), exceeds it are
  * rejected with SS_ERR_UNSUPPORTED (ss_last_error says by how much).
  *   status_host : NULL, or a host int32 that receives the device status
  *                 word of this call after the stream is synchronised; the

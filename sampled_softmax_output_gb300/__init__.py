@@ -124,6 +124,10 @@ def _load():
     L.ss_step_graph_create.restype = ctypes.c_int
     L.ss_step_graph_create.argtypes = [p, p, p, i64, i64, i64, i64, hp, ctypes.c_float,
                                        ctypes.c_int, p, p, p, p, p, p, p, sz, ctypes.POINTER(p)]
+    L.ss_step_graph_create_mtp.restype = ctypes.c_int
+    L.ss_step_graph_create_mtp.argtypes = [p, i64, fp, p, p, i64, i64, i64, i64, hp,
+                                           ctypes.c_float, ctypes.c_int, p, p, p, p, p, p, p, sz,
+                                           ctypes.POINTER(p)]
     L.ss_step_graph_launch.restype = ctypes.c_int
     L.ss_step_graph_launch.argtypes = [p, ctypes.c_uint64, p]
     L.ss_step_graph_destroy.restype = None
@@ -439,26 +443,28 @@ def clear_rows(rows: torch.Tensor, dW: torch.Tensor, ws: torch.Tensor):
 class StepGraph:
     """ss_step captured into a CUDA graph (ss_step_graph_*): the buffers are
     fixed at construction and kept alive here; launch(seed) replays the step
-    on the current stream."""
+    on the current stream. With `weights` (K of them), the step of several
+    targets per token (ss_step_mtp): targets and slot are [K, T]."""
 
     def __init__(self, H, W, targets, C: int, ws, scale: float = 1.0, accumulate=False,
                  cand=None, slot=None, loss=None, lse=None, dH=None, dW=None, cap: float = 0.0,
-                 tau: float = 1.0, fp8: int = 0):
+                 tau: float = 1.0, fp8: int = 0, weights=None):
         _need(H, "H", torch.bfloat16)
         dev = H.device
         T, D = H.shape
         V = W.shape[0]
+        tshape = (T,) if weights is None else (len(weights), T)
         _need(W, "W", torch.bfloat16, dev, (V, D))
-        _need(targets, "targets", torch.int32, dev, (T,))
+        _need(targets, "targets", torch.int32, dev, tshape)
         _need(ws, "workspace", torch.uint8, dev)
         self.cand = torch.empty(C, dtype=torch.int32, device=dev) if cand is None else cand
-        self.slot = torch.empty(T, dtype=torch.int32, device=dev) if slot is None else slot
+        self.slot = torch.empty(tshape, dtype=torch.int32, device=dev) if slot is None else slot
         self.loss = torch.empty(T, dtype=torch.float32, device=dev) if loss is None else loss
         self.lse = torch.empty(T, dtype=torch.float32, device=dev) if lse is None else lse
         self.dH = torch.empty(T, D, dtype=torch.bfloat16, device=dev) if dH is None else dH
         self.dW = torch.zeros(V, D, dtype=torch.float32, device=dev) if dW is None else dW
         for t, name, dt, shape in ((self.cand, "cand", torch.int32, (C,)),
-                                   (self.slot, "slot", torch.int32, (T,)),
+                                   (self.slot, "slot", torch.int32, tshape),
                                    (self.loss, "loss", torch.float32, (T,)),
                                    (self.lse, "lse", torch.float32, (T,)),
                                    (self.dH, "dH", torch.bfloat16, (T, D)),
@@ -467,13 +473,20 @@ class StepGraph:
         self._keep = (H, W, targets, ws)
         self.device = dev
         h = ctypes.c_void_p()
-        code = _lib.ss_step_graph_create(_ptr(targets), _ptr(H), _ptr(W), T, V, C, D,
-                                         _head(cap, tau, fp8), float(scale),
-                                         1 if accumulate else 0, _ptr(self.cand),
-                                         _ptr(self.slot), _ptr(self.loss), _ptr(self.lse),
-                                         _ptr(self.dH), _ptr(self.dW), _ptr(ws), ws.numel(),
-                                         ctypes.byref(h))
-        _check(code, "ss_step_graph_create")
+        outs = (_ptr(self.cand), _ptr(self.slot), _ptr(self.loss), _ptr(self.lse), _ptr(self.dH),
+                _ptr(self.dW), _ptr(ws), ws.numel(), ctypes.byref(h))
+        if weights is None:
+            code = _lib.ss_step_graph_create(_ptr(targets), _ptr(H), _ptr(W), T, V, C, D,
+                                             _head(cap, tau, fp8), float(scale),
+                                             1 if accumulate else 0, *outs)
+            _check(code, "ss_step_graph_create")
+        else:
+            w, K = _weights(weights)
+            self._keep_w = w
+            code = _lib.ss_step_graph_create_mtp(_ptr(targets), K, w, _ptr(H), _ptr(W), T, V, C,
+                                                 D, _head(cap, tau, fp8), float(scale),
+                                                 1 if accumulate else 0, *outs)
+            _check(code, "ss_step_graph_create_mtp")
         self._h = h
 
     def launch(self, seed: int):

@@ -1155,22 +1155,21 @@ const char* ss_trace_kernel_name(int k) {
   return t.names[k];
 }
 
-ss_status ss_step_graph_create(const int32_t* targets, const uint16_t* H, const uint16_t* W,
-                               int64_t T, int64_t V, int64_t C, int64_t D, const ss_head* head,
-                               float scale, int accumulate, int32_t* cand, int32_t* slot,
-                               float* loss, float* lse, uint16_t* dH, float* dW, void* workspace,
-                               size_t workspace_bytes, ss_step_graph** graph) {
-  if (!graph) return SS_ERR_INVALID;
-  *graph = nullptr;
-  float cap, tau;
-  int fp8;
-  ss_status st = head_args(head, &cap, &tau, &fp8);
-  if (st != SS_OK) return st;
+}  // extern "C"
+
+// Capture step_impl on a private stream into a graph and find the candidate
+// kernel's node (the only one whose arguments change between replays: seed).
+static ss_status graph_create(const int32_t* targets, const Targets& tg, const uint16_t* H,
+                              const uint16_t* W, int64_t T, int64_t V, int64_t C, int64_t D,
+                              float cap, float tau, int fp8, float scale, int accumulate,
+                              int32_t* cand, int32_t* slot, float* loss, float* lse, uint16_t* dH,
+                              float* dW, void* workspace, size_t workspace_bytes,
+                              ss_step_graph** graph) {
   if (fp8 && D % 128 != 0) return SS_ERR_UNSUPPORTED;
-  st = step_args_status(targets, H, W, T, V, C, D, accumulate, cand, slot, loss, lse, dH, dW,
-                        workspace, workspace_bytes);
+  ss_status st = step_args_status(targets, H, W, T, V, C, D, accumulate, cand, slot, loss, lse,
+                                  dH, dW, workspace, workspace_bytes);
   if (st != SS_OK) return st;
-  // record ss_step on a private stream
+  if (T * tg.K >= (int64_t(1) << 31)) return SS_ERR_UNSUPPORTED;
   cudaStream_t cs = nullptr;
   cudaError_t e = cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking);
   if (e != cudaSuccess) return fail("cudaStreamCreateWithFlags", e);
@@ -1179,7 +1178,7 @@ ss_status ss_step_graph_create(const int32_t* targets, const uint16_t* H, const 
     cudaStreamDestroy(cs);
     return fail("cudaStreamBeginCapture", e);
   }
-  const ss_status r = step_impl(targets, H, W, T, V, C, D, 0, cap, tau, kOneTarget, fp8, scale,
+  const ss_status r = step_impl(targets, H, W, T, V, C, D, 0, cap, tau, tg, fp8, scale,
                                 accumulate, cand, slot, loss, lse, dH, dW, workspace,
                                 workspace_bytes, cs);
   cudaGraph_t g = nullptr;
@@ -1212,8 +1211,9 @@ ss_status ss_step_graph_create(const int32_t* targets, const uint16_t* H, const 
     ss_step_graph_destroy(sg);
     return fail("capture of ss_step into a graph", e);
   }
+  // the candidate kernel runs over all K * T targets (targets [K, T])
   sg->targets = targets;
-  sg->T = static_cast<int>(T);
+  sg->T = static_cast<int>(T * tg.K);
   sg->V = static_cast<int>(V);
   sg->C = static_cast<int>(C);
   sg->cand = cand;
@@ -1223,6 +1223,40 @@ ss_status ss_step_graph_create(const int32_t* targets, const uint16_t* H, const 
   for (int i = 0; i < 8; ++i) sg->args[i] = a[i];
   *graph = sg;
   return SS_OK;
+}
+
+extern "C" {
+
+ss_status ss_step_graph_create(const int32_t* targets, const uint16_t* H, const uint16_t* W,
+                               int64_t T, int64_t V, int64_t C, int64_t D, const ss_head* head,
+                               float scale, int accumulate, int32_t* cand, int32_t* slot,
+                               float* loss, float* lse, uint16_t* dH, float* dW, void* workspace,
+                               size_t workspace_bytes, ss_step_graph** graph) {
+  if (!graph) return SS_ERR_INVALID;
+  *graph = nullptr;
+  float cap, tau;
+  int fp8;
+  const ss_status st = head_args(head, &cap, &tau, &fp8);
+  if (st != SS_OK) return st;
+  return graph_create(targets, kOneTarget, H, W, T, V, C, D, cap, tau, fp8, scale, accumulate,
+                      cand, slot, loss, lse, dH, dW, workspace, workspace_bytes, graph);
+}
+
+ss_status ss_step_graph_create_mtp(const int32_t* targets, int64_t K, const float* weights,
+                                   const uint16_t* H, const uint16_t* W, int64_t T, int64_t V,
+                                   int64_t C, int64_t D, const ss_head* head, float scale,
+                                   int accumulate, int32_t* cand, int32_t* slot, float* loss,
+                                   float* lse, uint16_t* dH, float* dW, void* workspace,
+                                   size_t workspace_bytes, ss_step_graph** graph) {
+  if (!graph) return SS_ERR_INVALID;
+  *graph = nullptr;
+  float cap, tau;
+  Targets tg;
+  ss_status st = head_args(head, &cap, &tau);
+  if (st == SS_OK) st = targets_args(K, weights, &tg);
+  if (st != SS_OK) return st;
+  return graph_create(targets, tg, H, W, T, V, C, D, cap, tau, 0, scale, accumulate, cand, slot,
+                      loss, lse, dH, dW, workspace, workspace_bytes, graph);
 }
 
 ss_status ss_step_graph_launch(ss_step_graph* graph, uint64_t seed, ss_stream stream) {

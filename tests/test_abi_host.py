@@ -20,6 +20,7 @@ def test_exports_every_declared_symbol():
                           "ss_trace_begin", "ss_trace_end", "ss_trace_kernel_name",
                           "ss_last_error", "ss_forward_noalloc", "ss_step",
                           "ss_schedule_candidates", "ss_clear_rows", "ss_step_graph_create",
+                          "ss_step_graph_create_mtp",
                           "ss_step_graph_launch", "ss_step_graph_destroy", "ss_forward_head",
                           "ss_backward_head", "ss_step_head", "ss_forward_mtp", "ss_backward_mtp",
                           "ss_step_mtp", "ss_quantize_e4m3"}
@@ -208,6 +209,26 @@ def test_step_graph_argument_errors():
     assert h.value is None                          # nothing was created
     assert L.ss_step_graph_launch(None, 0, None) == INVALID
     L.ss_step_graph_destroy(None)                   # a no-op
+
+
+def test_several_targets_step_graph_argument_errors():
+    L = ss.lib()
+    h = ctypes.c_void_p()
+
+    def create(K=2, w=(1.0, 0.5), head=None, wsb=1 << 40, C=4096, out=True):
+        wa = (ctypes.c_float * max(len(w), 1))(*w)
+        return L.ss_step_graph_create_mtp(p(FAKE), K, wa, p(FAKE), p(FAKE), 256, 50304, C, 768,
+                                          head, 1.0, 0, p(FAKE), p(FAKE), p(FAKE), p(FAKE),
+                                          p(FAKE), p(FAKE), p(FAKE), wsb,
+                                          ctypes.byref(h) if out else None)
+
+    assert create(K=0, w=()) == INVALID and create(K=9, w=(1.0,) * 9) == INVALID
+    assert create(w=(1.0, -0.5)) == INVALID and create(w=(0.0, 0.0)) == INVALID
+    assert create(head=ctypes.byref(ss.Head(0.0, 1.0, 1))) == UNSUPPORTED  # no FP8 path
+    assert create(C=0) == INVALID and create(out=False) == INVALID
+    need = L.ss_workspace_size(256, 50304, 4096, 768)
+    assert create(wsb=need - 1) == WORKSPACE
+    assert h.value is None
 
 
 def test_head_argument_errors():

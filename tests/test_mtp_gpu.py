@@ -118,3 +118,27 @@ def test_several_targets_full_size(orc):
     lhs = float((dWc * W64[cand_ref]).sum())
     rhs = float((got["dH"].astype(np.float64) * H64).sum())
     assert abs(lhs - rhs) <= 0.02 * abs(rhs)
+
+
+@pytest.mark.parametrize("cap,tau", [(0.0, 1.0), (30.0, 7.5)])
+def test_several_targets_graph_replay_equals_step(cap, tau):
+    """ss_step_graph_create_mtp: replays with new seeds give the bits of
+    ss_step_mtp."""
+    T, V, D, C = 500, 4000, 768, 1200
+    x, tg = _mtp_inputs(T, V, D, 2, 12)
+    C = max(C, len(np.unique(tg)))
+    H, W = to_dev_bf16(x["H"]), to_dev_bf16(x["W"])
+    t = torch.from_numpy(tg).cuda()
+    weights = [1.0, 0.5]
+    ws = ss.workspace(T, V, C, D)
+    g = ss.StepGraph(H, W, t, C, ws, scale=0.5, weights=weights, cap=cap, tau=tau)
+    ws2 = ss.workspace(T, V, C, D)
+    for seed in (3, 8):
+        g.dW.zero_()
+        got = g.launch(seed)
+        ref = ss.step_mtp(H, W, t, weights, C, seed, ws2, scale=0.5, cap=cap, tau=tau)
+        torch.cuda.synchronize()
+        assert ss.read_status(ws)[0] == 0
+        for k in ("cand", "slot", "loss", "lse", "dH", "dW"):
+            assert torch.equal(got[k], ref[k]), (seed, k)
+    g.close()
