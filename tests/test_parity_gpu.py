@@ -371,3 +371,31 @@ def test_capped_graph_replay_equals_step():
         assert torch.equal(got[k], ref[k]), k
     assert not torch.equal(got["loss"], plain["loss"])
     g.close()
+
+
+def test_permuted_ids_parity(orc):
+    """The robustness variant of the synthetic inputs: the token ids of the
+    Zipf law permuted by a fixed seed, so that the frequent ids (and with them
+    the unique targets) are spread over the whole vocabulary instead of
+    filling its first rows. Every element against the oracle."""
+    T, V, D, C, seed = 500, 6000, 768, 1400, 12
+    x = synth.make_inputs(T, V, D, 1.1, seed, permute_seed=99)
+    C = max(C, len(np.unique(x["targets"])))
+    assert x["targets"].max() > V // 2  # the frequent ids are no longer the first rows
+    ref = _full_oracle(orc, x, C, seed, 1.0 / T)
+    got = run_gpu(ss, x, C, seed, 1.0 / T)
+    assert got["status"] == 0
+    assert got["U"] == ref["U"]
+    np.testing.assert_array_equal(got["cand"], ref["cand"])
+    np.testing.assert_array_equal(got["slot"], ref["slot"])
+    assert_loss_close(got["loss"], ref["loss"])
+    assert rel_fro(got["dH"], ref["dH"]) < GRAD_RTOL
+    assert rel_fro(got["dW"], ref["dW"]) < GRAD_RTOL
+
+
+def test_permuted_ids_full_size(orc):
+    """T16384_C10240 with permuted ids: cand and slot bit-exact, sampled rows
+    and the gradient identities (as for the benchmark workload)."""
+    w = synth.WORKLOADS[2]
+    x = synth.make_inputs(w.T, w.V, w.D, w.zipf_s, w.seed, permute_seed=7)
+    _check_sampled(orc, x, w.T, w.V, w.D, w.C, w.seed, 21, exact_cols=False)
