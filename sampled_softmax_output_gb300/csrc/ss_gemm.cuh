@@ -97,6 +97,22 @@ __device__ __forceinline__ void for_tmem_chunks(uint32_t taddr, int c_begin, F&&
   }
 }
 
+// x[off & 31]: a five-level select tree on the bits of off (31 selects,
+// where comparing every index with off takes 32 compares and 32 selects)
+template <class Tv>
+__device__ __forceinline__ Tv select32(const Tv (&x)[32], int off) {
+  Tv a[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) a[i] = (off & 1) ? x[2 * i + 1] : x[2 * i];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) a[i] = (off & 2) ? a[2 * i + 1] : a[2 * i];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) a[i] = (off & 4) ? a[2 * i + 1] : a[2 * i];
+#pragma unroll
+  for (int i = 0; i < 2; ++i) a[i] = (off & 8) ? a[2 * i + 1] : a[2 * i];
+  return (off & 16) ? a[1] : a[0];
+}
+
 // The capped head: z = cap / (1 + exp(-s / tau)) = cap * 1 / (1 + 2^(-s k1)),
 // k1 = log2(e) / tau, and dz/ds = z (cap - z) icap_tau, icap_tau = 1 / (cap tau).
 struct HeadCap {
@@ -234,11 +250,7 @@ struct EpiFwdT {
           // at most: skip the selection unless one does
           if (__any_sync(0xffffffffu, hit)) {
             if (hit) {
-              float x = 0.f;
-#pragma unroll
-              for (int e = 0; e < 32; ++e)
-                if (e == off) x = v[e];
-              tg[k] = x * vs;
+              tg[k] = select32(v, off) * vs;
               has_t |= 1u << k;
             }
           }
@@ -365,9 +377,7 @@ struct EpiGT {
           const int off = sl[k] - j0 - jc;
           const bool has = static_cast<unsigned>(off) < 32u;
           if (__any_sync(0xffffffffu, has)) {
-            float xt = 0.f;
-#pragma unroll
-            for (int i = 0; i < 32; ++i) xt = (i == off) ? __uint_as_float(r[i]) : xt;
+            float xt = __uint_as_float(select32(r, off));  // used where has
             if constexpr (F8 && !CAP) xt *= sig;  // capped: hz carries the scale
             if (has) {
               // the one-hot weight of this column: every target k2 that falls on it
