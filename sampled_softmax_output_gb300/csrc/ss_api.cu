@@ -219,6 +219,20 @@ __global__ void __launch_bounds__(256) k_amax_bf16(const uint16_t* __restrict__ 
   warp_atomic_max(amax, absmax_slice(x, n8));
 }
 
+// amax[0] = max |x| (as k_amax_bf16) beside the candidate build, launched
+// right after it. Its dependents may start once every CTA of the build has
+// itself started, by which time the build's own predecessors (the producer of
+// x among them) are complete; x is nothing the build writes, so this kernel
+// reads it without waiting. It waits for the build only before it exits, so
+// that the kernels after it, which wait for it, find the build's results. No
+// status check: the build clears the status word while this kernel may run.
+__global__ void __launch_bounds__(256) k_amax_beside(const uint16_t* __restrict__ x, int64_t n8,
+                                                     float* amax) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  warp_atomic_max(amax, absmax_slice(x, n8));
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // The FP8 head's operands, two tensors in one launch (job 0: H, job 1: W_c):
 // q = e4m3(x * 2^e) and xq = bf16(e4m3 value * 2^-e) (exact), e from the
 // tensor's amax; xq may alias x.
@@ -512,18 +526,25 @@ ss_status enqueue_gather(const uint16_t* W, const int32_t* cand, int64_t C, int6
 }
 
 // W_c = W[cand] and, for the FP8 head, the e4m3 operands: amax of W_c and of
-// H (both in the gather's launch), then H -> (h8, hq) and W_c -> (w8, W_c
+// H (both in the gather's launch, unless h_amax_done: amax zeroed and max |H|
+// taken beside the candidate build), then H -> (h8, hq) and W_c -> (w8, W_c
 // rounded in place), or (FP8 gradients) the row-major and transposed codes
 ss_status enqueue_gather_operands(const uint16_t* W, const int32_t* cand, const uint16_t* H,
                                   int64_t T, int64_t C, int64_t V, int64_t D, int fp8,
-                                  const Layout& L, char* ws, int nsm, cudaStream_t s) {
+                                  const Layout& L, char* ws, int nsm, cudaStream_t s,
+                                  bool h_amax_done = false) {
   int* status = reinterpret_cast<int*>(ws + L.hdr);
   uint16_t* Wc = reinterpret_cast<uint16_t*>(ws + L.wc);
   if (!fp8) return enqueue_gather(W, cand, C, V, D, Wc, status, nsm, s);
   float* amax = reinterpret_cast<float*>(ws + L.hdr + kHdrAmax);
-  cudaError_t e = cudaMemsetAsync(amax, 0, 2 * sizeof(float), s);
-  if (e != cudaSuccess) return fail("cudaMemsetAsync(amax)", e);
-  ss_status r = enqueue_gather(W, cand, C, V, D, Wc, status, nsm, s, amax + 1, H, T * D / 8, amax);
+  cudaError_t e = cudaSuccess;
+  if (!h_amax_done) {
+    e = cudaMemsetAsync(amax, 0, 2 * sizeof(float), s);
+    if (e != cudaSuccess) return fail("cudaMemsetAsync(amax)", e);
+  }
+  ss_status r = h_amax_done ? enqueue_gather(W, cand, C, V, D, Wc, status, nsm, s, amax + 1)
+                            : enqueue_gather(W, cand, C, V, D, Wc, status, nsm, s, amax + 1, H,
+                                             T * D / 8, amax);
   if (r != SS_OK) return r;
   if (fp8 == 2) {  // FP8 gradients: row-major and transposed codes, no bf16 copies
     if ((T + 63) / 64 * (D / 64) > INT32_MAX / 2) return SS_ERR_UNSUPPORTED;
@@ -853,18 +874,34 @@ static ss_status step_impl(const int32_t* targets, const uint16_t* H, const uint
   if (st != SS_OK) return st;
   if (T * tg.K >= (int64_t(1) << 31)) return SS_ERR_UNSUPPORTED;
   const Layout L = make_layout(T, C, D);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  char* ws = static_cast<char*>(workspace);
+  // the FP8 head: max |H| depends on no candidate, so it is taken beside the
+  // candidate build (one cluster of 8 SMs), its accumulators zeroed before
+  float* amax = reinterpret_cast<float*>(ws + L.hdr + kHdrAmax);
+  const bool h_amax_beside = fp8 != 0 && T > 0;
+  if (h_amax_beside) {
+    const cudaError_t e = cudaMemsetAsync(amax, 0, 2 * sizeof(float), s);
+    if (e != cudaSuccess) return fail("cudaMemsetAsync(amax)", e);
+  }
   // the candidate set covers every target of every token (targets [K, T])
   const ss_status sb = ss_build_candidates(targets, T * tg.K, V, C, seed, cand, slot, nullptr,
                                            workspace, workspace_bytes, stream);
   if (sb != SS_OK) return sb;
   const int nsm = num_sms_current();
   if (nsm <= 0) return fail("cudaGetDevice/cudaDeviceGetAttribute", cudaGetLastError());
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  char* ws = static_cast<char*>(workspace);
   int* status = reinterpret_cast<int*>(ws + L.hdr);
   if (T == 0) return accumulate ? SS_OK : enqueue_zero_rows(cand, C, V, D, dW, status, nsm, s);
+  if (h_amax_beside) {
+    trace_pre(s, "amax_h");
+    const cudaError_t e =
+        launch_pdl(k_amax_beside, dim3(2 * nsm), dim3(256), 0, s, H, T * D / 8, amax);
+    trace_post(s);
+    if (e != cudaSuccess) return fail("launch k_amax_beside", e);
+  }
   // one gather of W[cand] serves the forward and the backward
-  ss_status r = enqueue_gather_operands(W, cand, H, T, C, V, D, fp8, L, ws, nsm, s);
+  ss_status r =
+      enqueue_gather_operands(W, cand, H, T, C, V, D, fp8, L, ws, nsm, s, h_amax_beside);
   if (r != SS_OK) return r;
   r = enqueue_forward(H, slot, T, C, D, cap, tau, tg, fp8, loss, lse, L, ws, nsm, s);
   if (r != SS_OK) return r;
