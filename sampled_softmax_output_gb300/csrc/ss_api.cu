@@ -228,9 +228,9 @@ __global__ void __launch_bounds__(256) k_amax_bf16(const uint16_t* __restrict__ 
 // status check: the build clears the status word while this kernel may run.
 __global__ void __launch_bounds__(256) k_amax_beside(const uint16_t* __restrict__ x, int64_t n8,
                                                      float* amax) {
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  pdl_launch_dependents();
   warp_atomic_max(amax, absmax_slice(x, n8));
-  asm volatile("griddepcontrol.wait;" ::: "memory");
+  pdl_wait();
 }
 
 // The FP8 head's operands, two tensors in one launch (job 0: H, job 1: W_c):
@@ -356,56 +356,63 @@ __global__ void __launch_bounds__(256) k_lse_merge(const float2* __restrict__ pa
                                                    float* __restrict__ lse, int* status) {
   pdl_enter();
   if (read_status(status) != 0) return;
-  const int gid = blockIdx.x * blockDim.x + threadIdx.x;
-  const int t = gid / kMergeLanes;
-  const int k = gid % kMergeLanes;
-  const bool valid = t < T;  // whole groups of 8 lanes share a token
-  // lane j < K of the group fetches target j's slot and logit along with the
-  // partials (one memory round trip for all of them)
-  int my_slot = 0;
-  float my_tgt = 0.f;
-  if (valid && k < tg.K) {
-    my_slot = __ldg(slot + static_cast<size_t>(k) * T + t);
-    my_tgt = __ldcg(tgt + static_cast<size_t>(k) * T + t);
-  }
-  float M = -INFINITY, S = 0.f;
-  constexpr int kBatch = 8;  // loads a thread has in flight
-  if (valid)
-    for (int c0 = k; c0 < n_ct; c0 += kMergeLanes * kBatch) {
-      float2 q[kBatch];
+  // grid-stride over tokens, the same trip count for a whole block
+  const int64_t lanes = static_cast<int64_t>(T) * kMergeLanes;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t g0 = static_cast<int64_t>(blockIdx.x) * blockDim.x; g0 < lanes; g0 += stride) {
+    const int64_t gid = g0 + threadIdx.x;
+    const int t = static_cast<int>(gid / kMergeLanes);
+    const int k = static_cast<int>(gid % kMergeLanes);
+    const bool valid = gid < lanes;  // whole groups of 8 lanes share a token
+    // lane j < K of the group fetches target j's slot and logit along with the
+    // partials (one memory round trip for all of them)
+    int my_slot = 0;
+    float my_tgt = 0.f;
+    if (valid && k < tg.K) {
+      my_slot = __ldg(slot + static_cast<size_t>(k) * T + t);
+      my_tgt = __ldcg(tgt + static_cast<size_t>(k) * T + t);
+    }
+    float M = -INFINITY, S = 0.f;
+    constexpr int kBatch = 8;  // loads a thread has in flight
+    if (valid)
+      for (int c0 = k; c0 < n_ct; c0 += kMergeLanes * kBatch) {
+        float2 q[kBatch];
 #pragma unroll
-      for (int i = 0; i < kBatch; ++i) {
-        const int c = c0 + i * kMergeLanes;
-        q[i] = c < n_ct ? __ldcg(part + static_cast<size_t>(c) * T + t) : make_float2(-INFINITY, 0.f);
+        for (int i = 0; i < kBatch; ++i) {
+          const int c = c0 + i * kMergeLanes;
+          q[i] = c < n_ct ? __ldcg(part + static_cast<size_t>(c) * T + t)
+                          : make_float2(-INFINITY, 0.f);
+        }
+#pragma unroll
+        for (int i = 0; i < kBatch; ++i) lse_fold(M, S, q[i].x, q[i].y);
       }
 #pragma unroll
-      for (int i = 0; i < kBatch; ++i) lse_fold(M, S, q[i].x, q[i].y);
+    for (int o = 1; o < kMergeLanes; o <<= 1) {
+      const float m2 = __shfl_xor_sync(0xffffffffu, M, o);
+      const float s2 = __shfl_xor_sync(0xffffffffu, S, o);
+      lse_fold(M, S, m2, s2);
+    }
+    const float l = M + logf(S);
+    // sum over the targets of w[j] (lse - target logit), lanes 0..K-1 of the
+    // group (one target: lse - tgt); a slot out of range is an error
+    bool bad = valid && k < tg.K && static_cast<unsigned>(my_slot) >= static_cast<unsigned>(C);
+    float acc = 0.f;
+    const int base = (threadIdx.x & 31) & ~(kMergeLanes - 1);
+    for (int j = 0; j < tg.K; ++j) {  // K <= kMergeLanes
+      const float tj = __shfl_sync(0xffffffffu, my_tgt, base + j);
+      acc += tg.w[j] * (l - tj);
     }
 #pragma unroll
-  for (int o = 1; o < kMergeLanes; o <<= 1) {
-    const float m2 = __shfl_xor_sync(0xffffffffu, M, o);
-    const float s2 = __shfl_xor_sync(0xffffffffu, S, o);
-    lse_fold(M, S, m2, s2);
+    for (int o = 1; o < kMergeLanes; o <<= 1) bad |= __shfl_xor_sync(0xffffffffu, bad, o) != 0;
+    if (valid && k == 0) {
+      if (bad) {
+        set_status(status, SS_ERR_INDEX);
+      } else {
+        lse[t] = l;
+        loss[t] = acc;
+      }
+    }
   }
-  const float l = M + logf(S);
-  // sum over the targets of w[j] (lse - target logit), lanes 0..K-1 of the
-  // group (one target: lse - tgt); a slot out of range is an error
-  bool bad = valid && k < tg.K && static_cast<unsigned>(my_slot) >= static_cast<unsigned>(C);
-  float acc = 0.f;
-  const int base = (threadIdx.x & 31) & ~(kMergeLanes - 1);
-  for (int j = 0; j < tg.K; ++j) {  // K <= kMergeLanes
-    const float tj = __shfl_sync(0xffffffffu, my_tgt, base + j);
-    acc += tg.w[j] * (l - tj);
-  }
-#pragma unroll
-  for (int o = 1; o < kMergeLanes; o <<= 1) bad |= __shfl_xor_sync(0xffffffffu, bad, o) != 0;
-  if (!valid || k != 0) return;
-  if (bad) {
-    set_status(status, SS_ERR_INDEX);
-    return;
-  }
-  lse[t] = l;
-  loss[t] = acc;
 }
 
 // dW[cand[j], :] = 0 (the gradient of an empty batch).
@@ -570,10 +577,13 @@ ss_status enqueue_gather_operands(const uint16_t* W, const int32_t* cand, const 
   return e == cudaSuccess ? SS_OK : fail("launch k_quantize_e4m3", e);
 }
 
-// forward GEMM (LSE partials, target logit) and the LSE merge, from W_c
+// forward GEMM (LSE partials, target logit) and the LSE merge, from W_c.
+// narrow_merge: at most two merge blocks per SM, for a softmax-gradient GEMM
+// that follows with after_merge (enqueue_backward)
 ss_status enqueue_forward(const uint16_t* H, const int32_t* slot, int64_t T, int64_t C, int64_t D,
                           float cap, float tau, const Targets& tg, int fp8, float* loss,
-                          float* lse, const Layout& L, char* ws, int nsm, cudaStream_t s) {
+                          float* lse, const Layout& L, char* ws, int nsm, cudaStream_t s,
+                          bool narrow_merge = false) {
   int* status = reinterpret_cast<int*>(ws + L.hdr);
   uint16_t* Wc = reinterpret_cast<uint16_t*>(ws + L.wc);
   float2* part = reinterpret_cast<float2*>(ws + L.part);
@@ -595,7 +605,12 @@ ss_status enqueue_forward(const uint16_t* H, const int32_t* slot, int64_t T, int
                                               tg, amax, status, nsm, s);
   trace_post(s);
   if (e != cudaSuccess) return fail("launch gemm_forward_lse", e);
-  const int blocks = static_cast<int>((T * kMergeLanes + 255) / 256);
+  // narrow_merge: at most two blocks per SM (40 registers x 256 threads
+  // each), so that the softmax-gradient GEMM after it, whose mainloop starts
+  // while the merge runs, finds room for its CTA beside them
+  const int64_t want = (T * kMergeLanes + 255) / 256;
+  const int blocks =
+      static_cast<int>(narrow_merge ? std::min<int64_t>(want, 2 * int64_t(nsm)) : want);
   trace_pre(s, "lse_merge");
   const cudaError_t em =
       launch_pdl(k_lse_merge, dim3(blocks), dim3(256), 0, s, part, tgt, slot, static_cast<int>(T),
@@ -620,7 +635,8 @@ int g8_exponent(float cap, float tau) {
 ss_status enqueue_backward_fp8(const int32_t* cand, const int32_t* slot, const float* lse,
                                int64_t T, int64_t V, int64_t C, int64_t D, float cap, float tau,
                                float scale, int accumulate, uint16_t* dH, float* dW,
-                               const Layout& L, char* ws, int nsm, cudaStream_t s) {
+                               const Layout& L, char* ws, int nsm, cudaStream_t s,
+                               bool after_merge) {
   const int g8e = g8_exponent(cap, tau);
   int* status = reinterpret_cast<int*>(ws + L.hdr);
   const float* amax = reinterpret_cast<const float*>(ws + L.hdr + kHdrAmax);
@@ -642,7 +658,7 @@ ss_status enqueue_backward_fp8(const int32_t* cand, const int32_t* slot, const f
             iD = static_cast<int>(D);
   trace_pre(s, "gemm_softmax_grad");
   cudaError_t e = launch_softmax_grad_fp8(tH8, tW8, tG8s, tG8ts, iT, iC, iD, slot, lse, cap, tau,
-                                          g8e, amax, status, nsm, s);
+                                          g8e, amax, status, nsm, s, after_merge);
   trace_post(s);
   if (e != cudaSuccess) return fail("launch gemm_softmax_grad", e);
   trace_pre(s, "gemm_grads");
@@ -652,15 +668,18 @@ ss_status enqueue_backward_fp8(const int32_t* cand, const int32_t* slot, const f
   return e == cudaSuccess ? SS_OK : fail("launch gemm_grads", e);
 }
 
-// softmax-gradient GEMM and the two gradient GEMMs, from W_c
+// softmax-gradient GEMM and the two gradient GEMMs, from W_c. after_merge:
+// the LSE merge is the kernel just before in the stream (ss_step), and W_c,
+// H and slot are older, so the softmax-gradient GEMM's mainloop does not wait
+// for the merge; only its epilogue, which reads lse, does.
 ss_status enqueue_backward(const uint16_t* H, const int32_t* cand, const int32_t* slot,
                            const float* lse, int64_t T, int64_t V, int64_t C, int64_t D,
                            float cap, float tau, const Targets& tg, int fp8, float scale,
                            int accumulate, uint16_t* dH, float* dW, const Layout& L, char* ws,
-                           int nsm, cudaStream_t s) {
+                           int nsm, cudaStream_t s, bool after_merge = false) {
   if (fp8 == 2)
     return enqueue_backward_fp8(cand, slot, lse, T, V, C, D, cap, tau, scale, accumulate, dH, dW,
-                                L, ws, nsm, s);
+                                L, ws, nsm, s, after_merge);
   int* status = reinterpret_cast<int*>(ws + L.hdr);
   uint16_t* Wc = reinterpret_cast<uint16_t*>(ws + L.wc);
   uint16_t* G = reinterpret_cast<uint16_t*>(ws + L.g);
@@ -684,7 +703,7 @@ ss_status enqueue_backward(const uint16_t* H, const int32_t* cand, const int32_t
   trace_pre(s, "gemm_softmax_grad");
   cudaError_t e =
       launch_softmax_grad(tH, tWc, tWc2, tGk, iT, iC, iD, slot, lse, scale, cap, tau, tg, amax,
-                          status, nsm, s);
+                          status, nsm, s, after_merge);
   trace_post(s);
   if (e != cudaSuccess) return fail("launch gemm_softmax_grad", e);
   trace_pre(s, "gemm_grads");
@@ -903,10 +922,15 @@ static ss_status step_impl(const int32_t* targets, const uint16_t* H, const uint
   ss_status r =
       enqueue_gather_operands(W, cand, H, T, C, V, D, fp8, L, ws, nsm, s, h_amax_beside);
   if (r != SS_OK) return r;
-  r = enqueue_forward(H, slot, T, C, D, cap, tau, tg, fp8, loss, lse, L, ws, nsm, s);
+  // the softmax-gradient GEMM's mainloop beside the LSE merge: measured with
+  // the plain bf16 head (one partial per row and logit tile); the heads whose
+  // merge folds two per tile keep the wide merge and the full wait
+  const bool overlap_merge = fwd_groups(cap, fp8 != 0, tg.K) == 1;
+  r = enqueue_forward(H, slot, T, C, D, cap, tau, tg, fp8, loss, lse, L, ws, nsm, s,
+                      overlap_merge);
   if (r != SS_OK) return r;
   return enqueue_backward(H, cand, slot, lse, T, V, C, D, cap, tau, tg, fp8, scale, accumulate, dH,
-                          dW, L, ws, nsm, s);
+                          dW, L, ws, nsm, s, overlap_merge);
 }
 
 // K targets per token with host weights w[0..K): 1 <= K <= kMaxTargets, each

@@ -73,6 +73,11 @@ struct GemmShape {
   int m_tiles;
   int n_tiles;
   int k_blocks;
+  // 1: the operands are older than the kernel just before this one in the
+  // stream, and only the epilogue reads what that kernel writes. The producer
+  // and MMA warps then start at once; the epilogue waits before its first
+  // tile. (k_gemm only; the CTA-pair kernel always waits first.)
+  int late_wait;
 };
 
 // ----------------------------------------------------------------- epilogues
@@ -665,7 +670,8 @@ template <int BN, int STAGES, bool A_MN, bool B_MN, class Epi, int EPI_WARPS = 4
 __global__ void __launch_bounds__(64 + 32 * EPI_WARPS, 1)
     k_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
            GemmShape shp, const __grid_constant__ typename Epi::Params ep, int* status) {
-  pdl_enter();
+  if (shp.late_wait) pdl_launch_dependents();
+  else pdl_enter();
   static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "BN");
   static_assert(STAGES >= 2 && STAGES <= 8, "STAGES");
   static_assert(EPI_WARPS == 4 || EPI_WARPS == 8, "EPI_WARPS");
@@ -818,6 +824,7 @@ __global__ void __launch_bounds__(64 + 32 * EPI_WARPS, 1)
     const int row = q * 32 + lane;
     const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
     EpiState es{tiles + L::EPI_OFFSET, static_cast<int>(threadIdx.x) - 64, 0u, 0.f};
+    if (shp.late_wait) pdl_wait();
     Epi::begin(ep, es);
     int b = 0;
     uint32_t aph = 0;

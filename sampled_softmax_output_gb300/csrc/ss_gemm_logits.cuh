@@ -41,7 +41,7 @@ cudaError_t softmax_grad(const CUtensorMap& tH, const CUtensorMap& tWc,
                          const CUtensorMap& tWc_half, const CUtensorMap& tG_store, int T, int C,
                          int D, const int32_t* slot, const float* lse, float scale,
                          const HeadCap& head, const Targets& tg, const float* amax, int* status,
-                         int num_sms, cudaStream_t stream) {
+                         int num_sms, cudaStream_t stream, bool late_wait) {
   typename EpiGT<CAP, KMAX, F8>::Params ep;
   ep.tmG = tG_store;
   ep.T = T;
@@ -70,7 +70,7 @@ cudaError_t softmax_grad(const CUtensorMap& tH, const CUtensorMap& tWc,
                                                                            stream);
     }
   }
-  GemmShape shp{(T + BM - 1) / BM, n_tiles, D / (F8 ? 2 * BK : BK)};
+  GemmShape shp{(T + BM - 1) / BM, n_tiles, D / (F8 ? 2 * BK : BK), late_wait ? 1 : 0};
   return launch_gemm<kBnLogits, F8 ? kStagesGradF8 : kStagesLogits, false, false,
                      EpiGT<CAP, KMAX, F8>, 8, F8>(tH, tWc, shp, ep, status, num_sms, stream);
 }
