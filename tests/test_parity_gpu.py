@@ -296,6 +296,28 @@ def test_fused_step_equals_separate_calls(orc):
     assert rel_fro(a["dW"].cpu().numpy(), ref["dW"]) < GRAD_RTOL
 
 
+def test_step_merge_beside_softmax_grad(orc):
+    # ss_step with the plain head runs the LSE merge on two blocks per SM,
+    # several passes of its grid-stride loop at this T, while the
+    # softmax-gradient GEMM's mainloop starts beside it; the separate calls
+    # run the wide merge and wait in full
+    T, V, D, C, seed = 20000, 3000, 64, 2000, 22
+    x, C = _case(T, V, D, C, seed)
+    H, W, tg = to_dev_bf16(x["H"]), to_dev_bf16(x["W"]), _dev(x["targets"])
+    ws = ss.workspace(T, V, C, D)
+    a = ss.step(H, W, tg, C, seed, ws, scale=1.0 / T)
+    a = {k: v.clone() for k, v in a.items()}
+    b = ss.step_separate(H, W, tg, C, seed, ws, scale=1.0 / T)
+    torch.cuda.synchronize()
+    assert ss.read_status(ws)[0] == 0
+    for k in ("cand", "slot", "loss", "lse", "dH", "dW"):
+        assert torch.equal(a[k], b[k]), k
+    ref = _full_oracle(orc, x, C, seed, 1.0 / T)
+    assert_loss_close(a["loss"].cpu().numpy(), ref["loss"])
+    assert rel_fro(a["dH"].float().cpu().numpy(), ref["dH"]) < GRAD_RTOL
+    assert rel_fro(a["dW"].cpu().numpy(), ref["dW"]) < GRAD_RTOL
+
+
 def test_kernel_trace_records_every_launch():
     T, V, D, C = 300, 3000, 768, 517
     x, C = _case(T, V, D, C, 4)
