@@ -33,6 +33,7 @@ struct Layout {
 
 constexpr size_t kHdrBytes = 1024;  // int32 status, int32 U, padding, FP8 amax words
 constexpr size_t kHdrAmax = 64;     // byte offset of float amax[2] (max |H|, max |W_c|)
+constexpr size_t kHdrBar = 72;      // uint32 bar[2] of k_h_prep_beside (arrivals, gave up)
 constexpr size_t kHdrQuant = 80;    // ss_quantize_e4m3's own float amax + int32 status
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -219,20 +220,6 @@ __global__ void __launch_bounds__(256) k_amax_bf16(const uint16_t* __restrict__ 
   warp_atomic_max(amax, absmax_slice(x, n8));
 }
 
-// amax[0] = max |x| (as k_amax_bf16) beside the candidate build, launched
-// right after it. Its dependents may start once every CTA of the build has
-// itself started, by which time the build's own predecessors (the producer of
-// x among them) are complete; x is nothing the build writes, so this kernel
-// reads it without waiting. It waits for the build only before it exits, so
-// that the kernels after it, which wait for it, find the build's results. No
-// status check: the build clears the status word while this kernel may run.
-__global__ void __launch_bounds__(256) k_amax_beside(const uint16_t* __restrict__ x, int64_t n8,
-                                                     float* amax) {
-  pdl_launch_dependents();
-  warp_atomic_max(amax, absmax_slice(x, n8));
-  pdl_wait();
-}
-
 // The FP8 head's operands, two tensors in one launch (job 0: H, job 1: W_c):
 // q = e4m3(x * 2^e) and xq = bf16(e4m3 value * 2^-e) (exact), e from the
 // tensor's amax; xq may alias x.
@@ -243,35 +230,45 @@ struct QuantJob {
   const float* amax;
   int64_t n8;  // groups of 8 values
 };
-__global__ void __launch_bounds__(256) k_quantize_e4m3(QuantJob a, QuantJob b, int* status) {
+// Groups i0, i0 + stride, ... of job J (the row-major quantizer's work).
+__device__ __forceinline__ void quantize_rows(const QuantJob& J, int64_t i0, int64_t stride) {
+  const int e = e4m3_exponent(__ldcg(J.amax));
+  const float up = exp2i(e), down = exp2i(-e);
+  for (int64_t i = i0; i < J.n8; i += stride) {
+    const uint4 v = __ldg(reinterpret_cast<const uint4*>(J.x) + i);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t qw[2], out[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float lo = __uint_as_float(w[k] << 16) * up;
+      const float hi = __uint_as_float(w[k] & 0xffff0000u) * up;
+      const uint16_t c = e4m3x2(lo, hi);
+      const uint32_t h2 = e4m3x2_to_f16x2(c);
+      const float dlo = __half2float(__ushort_as_half(static_cast<uint16_t>(h2 & 0xffffu))) * down;
+      const float dhi = __half2float(__ushort_as_half(static_cast<uint16_t>(h2 >> 16))) * down;
+      out[k] = (__float_as_uint(dlo) >> 16) | (__float_as_uint(dhi) & 0xffff0000u);
+      if (k & 1) qw[k >> 1] |= static_cast<uint32_t>(c) << 16;
+      else qw[k >> 1] = c;
+    }
+    reinterpret_cast<uint2*>(J.q)[i] = make_uint2(qw[0], qw[1]);
+    reinterpret_cast<uint4*>(J.xq)[i] = make_uint4(out[0], out[1], out[2], out[3]);
+  }
+}
+
+// beside_fail (nullable): set when H's half, quantized beside the candidate
+// build (k_h_prep_beside), gave up waiting; reported here as SS_ERR_TIMEOUT.
+__global__ void __launch_bounds__(256) k_quantize_e4m3(QuantJob a, QuantJob b, int* status,
+                                                       const uint32_t* beside_fail) {
   pdl_enter();
   if (read_status(status) != 0) return;
-  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-  for (int job = 0; job < 2; ++job) {
-    const QuantJob& J = job == 0 ? a : b;
-    const int e = e4m3_exponent(__ldcg(J.amax));
-    const float up = exp2i(e), down = exp2i(-e);
-    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < J.n8;
-         i += stride) {
-      const uint4 v = __ldg(reinterpret_cast<const uint4*>(J.x) + i);
-      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-      uint32_t qw[2], out[4];
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const float lo = __uint_as_float(w[k] << 16) * up;
-        const float hi = __uint_as_float(w[k] & 0xffff0000u) * up;
-        const uint16_t c = e4m3x2(lo, hi);
-        const uint32_t h2 = e4m3x2_to_f16x2(c);
-        const float dlo = __half2float(__ushort_as_half(static_cast<uint16_t>(h2 & 0xffffu))) * down;
-        const float dhi = __half2float(__ushort_as_half(static_cast<uint16_t>(h2 >> 16))) * down;
-        out[k] = (__float_as_uint(dlo) >> 16) | (__float_as_uint(dhi) & 0xffff0000u);
-        if (k & 1) qw[k >> 1] |= static_cast<uint32_t>(c) << 16;
-        else qw[k >> 1] = c;
-      }
-      reinterpret_cast<uint2*>(J.q)[i] = make_uint2(qw[0], qw[1]);
-      reinterpret_cast<uint4*>(J.xq)[i] = make_uint4(out[0], out[1], out[2], out[3]);
-    }
+  if (beside_fail && __ldcg(beside_fail) != 0u) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) set_status(status, SS_ERR_TIMEOUT);
+    return;
   }
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  const int64_t i0 = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
+  quantize_rows(a, i0, stride);
+  quantize_rows(b, i0, stride);
 }
 
 // FP8 gradients: x [R, D] bf16 (D % 64 == 0) to e4m3 codes twice, q [R, D]
@@ -286,52 +283,109 @@ struct QuantTJob {
   int R, D, ldR, tiles;  // tiles = ceil(R / 64) * (D / 64)
 };
 constexpr int kQtPitch = 72;  // bytes per row of the shared tile (64 + 8 against conflicts)
-__global__ void __launch_bounds__(256) k_quantize_e4m3_t(QuantTJob a, QuantTJob b, int* status) {
-  pdl_enter();
-  if (read_status(status) != 0) return;
-  __shared__ __align__(16) uint8_t tile[64 * kQtPitch];
-  for (int w = blockIdx.x; w < a.tiles + b.tiles; w += gridDim.x) {
-    const bool first = w < a.tiles;
-    const QuantTJob& J = first ? a : b;
-    const int ti = first ? w : w - a.tiles;
-    const int nct = J.D / 64;
-    const int r0 = (ti / nct) * 64, c0 = (ti % nct) * 64;
-    const float up = exp2i(e4m3_exponent(__ldcg(J.amax)));
-    __syncthreads();  // the previous tile's transposed reads are done
-    for (int v = threadIdx.x; v < 512; v += blockDim.x) {
-      const int r = v >> 3, c8 = (v & 7) * 8;  // row r, columns c8 .. c8 + 7 of the tile
-      uint32_t qw[2] = {0u, 0u};
-      if (r0 + r < J.R) {
-        const size_t at = static_cast<size_t>(r0 + r) * J.D + c0 + c8;
-        const uint4 x = __ldg(reinterpret_cast<const uint4*>(J.x + at));
-        const uint32_t xw[4] = {x.x, x.y, x.z, x.w};
+// Tile ti of job J, transposed through the shared tile; every thread of the
+// block calls it (it synchronises the block).
+__device__ __forceinline__ void quantize_t_tile(const QuantTJob& J, int ti, uint8_t* tile) {
+  const int nct = J.D / 64;
+  const int r0 = (ti / nct) * 64, c0 = (ti % nct) * 64;
+  const float up = exp2i(e4m3_exponent(__ldcg(J.amax)));
+  __syncthreads();  // the previous tile's transposed reads are done
+  for (int v = threadIdx.x; v < 512; v += blockDim.x) {
+    const int r = v >> 3, c8 = (v & 7) * 8;  // row r, columns c8 .. c8 + 7 of the tile
+    uint32_t qw[2] = {0u, 0u};
+    if (r0 + r < J.R) {
+      const size_t at = static_cast<size_t>(r0 + r) * J.D + c0 + c8;
+      const uint4 x = __ldg(reinterpret_cast<const uint4*>(J.x + at));
+      const uint32_t xw[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const uint16_t c = e4m3x2(__uint_as_float(xw[k] << 16) * up,
-                                    __uint_as_float(xw[k] & 0xffff0000u) * up);
-          qw[k >> 1] |= static_cast<uint32_t>(c) << (16 * (k & 1));
-        }
-        *reinterpret_cast<uint2*>(J.q + at) = make_uint2(qw[0], qw[1]);
+      for (int k = 0; k < 4; ++k) {
+        const uint16_t c = e4m3x2(__uint_as_float(xw[k] << 16) * up,
+                                  __uint_as_float(xw[k] & 0xffff0000u) * up);
+        qw[k >> 1] |= static_cast<uint32_t>(c) << (16 * (k & 1));
       }
-      *reinterpret_cast<uint2*>(tile + r * kQtPitch + c8) = make_uint2(qw[0], qw[1]);
+      *reinterpret_cast<uint2*>(J.q + at) = make_uint2(qw[0], qw[1]);
     }
-    __syncthreads();
-    for (int v = threadIdx.x; v < 512; v += blockDim.x) {
-      const int c = v >> 3, rg = (v & 7) * 8;  // column c, rows rg .. rg + 7 of the tile
-      const int nr = min(8, J.R - r0 - rg);
-      if (nr <= 0) continue;
-      uint32_t o[2] = {0u, 0u};
+    *reinterpret_cast<uint2*>(tile + r * kQtPitch + c8) = make_uint2(qw[0], qw[1]);
+  }
+  __syncthreads();
+  for (int v = threadIdx.x; v < 512; v += blockDim.x) {
+    const int c = v >> 3, rg = (v & 7) * 8;  // column c, rows rg .. rg + 7 of the tile
+    const int nr = min(8, J.R - r0 - rg);
+    if (nr <= 0) continue;
+    uint32_t o[2] = {0u, 0u};
 #pragma unroll
-      for (int k = 0; k < 8; ++k)
-        o[k >> 2] |= static_cast<uint32_t>(tile[(rg + k) * kQtPitch + c]) << (8 * (k & 3));
-      uint8_t* dst = J.qt + static_cast<size_t>(c0 + c) * J.ldR + r0 + rg;
-      if (nr == 8) {
-        *reinterpret_cast<uint2*>(dst) = make_uint2(o[0], o[1]);
-      } else {
-        for (int k = 0; k < nr; ++k) dst[k] = static_cast<uint8_t>(o[k >> 2] >> (8 * (k & 3)));
-      }
+    for (int k = 0; k < 8; ++k)
+      o[k >> 2] |= static_cast<uint32_t>(tile[(rg + k) * kQtPitch + c]) << (8 * (k & 3));
+    uint8_t* dst = J.qt + static_cast<size_t>(c0 + c) * J.ldR + r0 + rg;
+    if (nr == 8) {
+      *reinterpret_cast<uint2*>(dst) = make_uint2(o[0], o[1]);
+    } else {
+      for (int k = 0; k < nr; ++k) dst[k] = static_cast<uint8_t>(o[k >> 2] >> (8 * (k & 3)));
     }
   }
+}
+
+// beside_fail: as for k_quantize_e4m3.
+__global__ void __launch_bounds__(256) k_quantize_e4m3_t(QuantTJob a, QuantTJob b, int* status,
+                                                         const uint32_t* beside_fail) {
+  pdl_enter();
+  if (read_status(status) != 0) return;
+  if (beside_fail && __ldcg(beside_fail) != 0u) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) set_status(status, SS_ERR_TIMEOUT);
+    return;
+  }
+  __shared__ __align__(16) uint8_t tile[64 * kQtPitch];
+  for (int w = blockIdx.x; w < a.tiles + b.tiles; w += gridDim.x) {
+    if (w < a.tiles) quantize_t_tile(a, w, tile);
+    else quantize_t_tile(b, w - a.tiles, tile);
+  }
+}
+
+// The FP8 head's H beside the candidate build, launched right after it: max
+// |H| into *amax, then, after a barrier over this grid, H's e4m3 operands
+// (mode 1: jr, as k_quantize_e4m3; mode 2: jt, as k_quantize_e4m3_t).
+// - No wait at the start: this grid may start once every CTA of the build has
+//   started, by which time everything the build waited for (H's producer
+//   among it) is complete, and the build writes nothing this kernel reads.
+// - The grid barrier can be waited on: the kernel after this one is launched
+//   only once every block of this grid has started, so all of them are
+//   resident together (the build holds 8 SMs). bar[0] counts arrivals; a
+//   block that gives up (kWaitLimitNs) sets bar[1], which the W_c quantizer
+//   reports as SS_ERR_TIMEOUT. bar[0..1] and *amax are zero at launch.
+// - It waits for the build before it exits, so that the kernels after it,
+//   which wait for it, find the build's results. No status check: the build
+//   clears the status word while this kernel may run.
+__global__ void __launch_bounds__(256) k_h_prep_beside(int64_t n8, float* amax, uint32_t* bar,
+                                                       QuantJob jr, QuantTJob jt, int mode) {
+  pdl_launch_dependents();
+  __shared__ __align__(16) uint8_t tile[64 * kQtPitch];
+  __shared__ int s_go;
+  warp_atomic_max(amax, absmax_slice(jr.x, n8));
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    atomicAdd(bar, 1u);
+    const uint64_t t0 = globaltimer_ns();
+    int go = 1;
+    while (ld_acquire_gpu(bar) < gridDim.x) {
+      if (globaltimer_ns() - t0 > kWaitLimitNs) {
+        atomicExch(bar + 1, 1u);
+        go = 0;
+        break;
+      }
+    }
+    s_go = go;
+  }
+  __syncthreads();
+  if (s_go) {
+    if (mode == 2) {
+      for (int w = blockIdx.x; w < jt.tiles; w += gridDim.x) quantize_t_tile(jt, w, tile);
+    } else {
+      quantize_rows(jr, blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x,
+                    static_cast<int64_t>(gridDim.x) * blockDim.x);
+    }
+  }
+  pdl_wait();
 }
 
 // lse[t] = log sum over tiles of s_c * exp(m_c); loss[t] = lse[t] - tgt[t].
@@ -532,47 +586,63 @@ ss_status enqueue_gather(const uint16_t* W, const int32_t* cand, int64_t C, int6
   return e == cudaSuccess ? SS_OK : fail("launch k_gather_rows", e);
 }
 
+// H's e4m3 jobs: mode 1 (h8 and the rounded bf16 copy hq), mode 2 (h8 and
+// the transposed h8t); tiles = 0 / n8 = 0 give the empty job
+QuantJob h_rows_job(const uint16_t* H, int64_t T, int64_t D, const Layout& L, char* ws,
+                    bool empty) {
+  return QuantJob{H, reinterpret_cast<uint8_t*>(ws + L.h8), reinterpret_cast<uint16_t*>(ws + L.hq),
+                  reinterpret_cast<const float*>(ws + L.hdr + kHdrAmax), empty ? 0 : T * D / 8};
+}
+QuantTJob h_tiles_job(const uint16_t* H, int64_t T, int64_t D, const Layout& L, char* ws,
+                      bool empty) {
+  return QuantTJob{H, reinterpret_cast<uint8_t*>(ws + L.h8),
+                   reinterpret_cast<uint8_t*>(ws + L.h8t),
+                   reinterpret_cast<const float*>(ws + L.hdr + kHdrAmax), static_cast<int>(T),
+                   static_cast<int>(D), static_cast<int>(L.ldT8),
+                   empty ? 0 : static_cast<int>((T + 63) / 64 * (D / 64))};
+}
+
 // W_c = W[cand] and, for the FP8 head, the e4m3 operands: amax of W_c and of
-// H (both in the gather's launch, unless h_amax_done: amax zeroed and max |H|
-// taken beside the candidate build), then H -> (h8, hq) and W_c -> (w8, W_c
-// rounded in place), or (FP8 gradients) the row-major and transposed codes
+// H (both in the gather's launch), then H -> (h8, hq) and W_c -> (w8, W_c
+// rounded in place), or (FP8 gradients) the row-major and transposed codes.
+// h_beside: max |H| and H's codes come from k_h_prep_beside (ss_step), which
+// zeroed nothing itself: amax and its barrier words were cleared before it.
 ss_status enqueue_gather_operands(const uint16_t* W, const int32_t* cand, const uint16_t* H,
                                   int64_t T, int64_t C, int64_t V, int64_t D, int fp8,
                                   const Layout& L, char* ws, int nsm, cudaStream_t s,
-                                  bool h_amax_done = false) {
+                                  bool h_beside = false) {
   int* status = reinterpret_cast<int*>(ws + L.hdr);
   uint16_t* Wc = reinterpret_cast<uint16_t*>(ws + L.wc);
   if (!fp8) return enqueue_gather(W, cand, C, V, D, Wc, status, nsm, s);
   float* amax = reinterpret_cast<float*>(ws + L.hdr + kHdrAmax);
+  const uint32_t* beside_fail =
+      h_beside ? reinterpret_cast<const uint32_t*>(ws + L.hdr + kHdrBar) + 1 : nullptr;
   cudaError_t e = cudaSuccess;
-  if (!h_amax_done) {
+  if (!h_beside) {
     e = cudaMemsetAsync(amax, 0, 2 * sizeof(float), s);
     if (e != cudaSuccess) return fail("cudaMemsetAsync(amax)", e);
   }
-  ss_status r = h_amax_done ? enqueue_gather(W, cand, C, V, D, Wc, status, nsm, s, amax + 1)
-                            : enqueue_gather(W, cand, C, V, D, Wc, status, nsm, s, amax + 1, H,
-                                             T * D / 8, amax);
+  ss_status r = h_beside ? enqueue_gather(W, cand, C, V, D, Wc, status, nsm, s, amax + 1)
+                         : enqueue_gather(W, cand, C, V, D, Wc, status, nsm, s, amax + 1, H,
+                                          T * D / 8, amax);
   if (r != SS_OK) return r;
   if (fp8 == 2) {  // FP8 gradients: row-major and transposed codes, no bf16 copies
     if ((T + 63) / 64 * (D / 64) > INT32_MAX / 2) return SS_ERR_UNSUPPORTED;
-    const QuantTJob th{H, reinterpret_cast<uint8_t*>(ws + L.h8),
-                       reinterpret_cast<uint8_t*>(ws + L.h8t), amax, static_cast<int>(T),
-                       static_cast<int>(D), static_cast<int>(L.ldT8),
-                       static_cast<int>((T + 63) / 64 * (D / 64))};
+    const QuantTJob th = h_tiles_job(H, T, D, L, ws, h_beside);
     const QuantTJob tw{Wc, reinterpret_cast<uint8_t*>(ws + L.w8),
                        reinterpret_cast<uint8_t*>(ws + L.w8t), amax + 1, static_cast<int>(C),
                        static_cast<int>(D), static_cast<int>(L.ldC8),
                        static_cast<int>((C + 63) / 64 * (D / 64))};
     trace_pre(s, "quantize_e4m3");
-    e = launch_pdl(k_quantize_e4m3_t, dim3(nsm * 4), dim3(256), 0, s, th, tw, status);
+    e = launch_pdl(k_quantize_e4m3_t, dim3(nsm * 4), dim3(256), 0, s, th, tw, status,
+                   beside_fail);
     trace_post(s);
     return e == cudaSuccess ? SS_OK : fail("launch k_quantize_e4m3_t", e);
   }
-  const QuantJob jh{H, reinterpret_cast<uint8_t*>(ws + L.h8), reinterpret_cast<uint16_t*>(ws + L.hq),
-                    amax, T * D / 8};
+  const QuantJob jh = h_rows_job(H, T, D, L, ws, h_beside);
   const QuantJob jw{Wc, reinterpret_cast<uint8_t*>(ws + L.w8), Wc, amax + 1, C * D / 8};
   trace_pre(s, "quantize_e4m3");
-  e = launch_pdl(k_quantize_e4m3, dim3(nsm * 4), dim3(256), 0, s, jh, jw, status);
+  e = launch_pdl(k_quantize_e4m3, dim3(nsm * 4), dim3(256), 0, s, jh, jw, status, beside_fail);
   trace_post(s);
   return e == cudaSuccess ? SS_OK : fail("launch k_quantize_e4m3", e);
 }
@@ -895,12 +965,15 @@ static ss_status step_impl(const int32_t* targets, const uint16_t* H, const uint
   const Layout L = make_layout(T, C, D);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   char* ws = static_cast<char*>(workspace);
-  // the FP8 head: max |H| depends on no candidate, so it is taken beside the
-  // candidate build (one cluster of 8 SMs), its accumulators zeroed before
+  // the FP8 head: max |H| and H's e4m3 codes depend on no candidate, so they
+  // are made beside the candidate build (one cluster of 8 SMs); the amax and
+  // barrier words are zeroed before it
   float* amax = reinterpret_cast<float*>(ws + L.hdr + kHdrAmax);
-  const bool h_amax_beside = fp8 != 0 && T > 0;
-  if (h_amax_beside) {
-    const cudaError_t e = cudaMemsetAsync(amax, 0, 2 * sizeof(float), s);
+  const bool h_beside = fp8 != 0 && T > 0;
+  if (h_beside) {
+    if ((T + 63) / 64 * (D / 64) > INT32_MAX / 2) return SS_ERR_UNSUPPORTED;
+    static_assert(kHdrBar == kHdrAmax + 8, "one memset clears amax[2] and bar[2]");
+    const cudaError_t e = cudaMemsetAsync(amax, 0, 16, s);
     if (e != cudaSuccess) return fail("cudaMemsetAsync(amax)", e);
   }
   // the candidate set covers every target of every token (targets [K, T])
@@ -911,16 +984,17 @@ static ss_status step_impl(const int32_t* targets, const uint16_t* H, const uint
   if (nsm <= 0) return fail("cudaGetDevice/cudaDeviceGetAttribute", cudaGetLastError());
   int* status = reinterpret_cast<int*>(ws + L.hdr);
   if (T == 0) return accumulate ? SS_OK : enqueue_zero_rows(cand, C, V, D, dW, status, nsm, s);
-  if (h_amax_beside) {
-    trace_pre(s, "amax_h");
-    const cudaError_t e =
-        launch_pdl(k_amax_beside, dim3(2 * nsm), dim3(256), 0, s, H, T * D / 8, amax);
+  if (h_beside) {
+    trace_pre(s, "prepare_h");
+    const cudaError_t e = launch_pdl(
+        k_h_prep_beside, dim3(4 * nsm), dim3(256), 0, s, T * D / 8, amax,
+        reinterpret_cast<uint32_t*>(ws + L.hdr + kHdrBar), h_rows_job(H, T, D, L, ws, false),
+        h_tiles_job(H, T, D, L, ws, false), fp8);
     trace_post(s);
-    if (e != cudaSuccess) return fail("launch k_amax_beside", e);
+    if (e != cudaSuccess) return fail("launch k_h_prep_beside", e);
   }
   // one gather of W[cand] serves the forward and the backward
-  ss_status r =
-      enqueue_gather_operands(W, cand, H, T, C, V, D, fp8, L, ws, nsm, s, h_amax_beside);
+  ss_status r = enqueue_gather_operands(W, cand, H, T, C, V, D, fp8, L, ws, nsm, s, h_beside);
   if (r != SS_OK) return r;
   // the softmax-gradient GEMM's mainloop beside the LSE merge: measured with
   // the plain bf16 head (one partial per row and logit tile); the heads whose
@@ -1106,7 +1180,8 @@ ss_status ss_quantize_e4m3(const uint16_t* x, int64_t n, uint8_t* q, uint16_t* x
   const QuantJob j{x, q, xq, amax, n / 8};
   const QuantJob none{x, q, xq, amax, 0};
   if (e == cudaSuccess)
-    e = launch_pdl(k_quantize_e4m3, dim3(nsm * 4), dim3(256), 0, s, j, none, status);
+    e = launch_pdl(k_quantize_e4m3, dim3(nsm * 4), dim3(256), 0, s, j, none, status,
+                   static_cast<const uint32_t*>(nullptr));
   return e == cudaSuccess ? SS_OK : fail("ss_quantize_e4m3", e);
 }
 

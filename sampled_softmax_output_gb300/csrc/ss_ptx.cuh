@@ -32,6 +32,13 @@ __device__ __forceinline__ void set_status(int* status, int code) {
   atomicCAS(status, 0, code);
 }
 
+// Device-scope acquire load of a global word, for a spin on a counter.
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
 __device__ __forceinline__ int read_status(const int* status) {
   return *reinterpret_cast<const volatile int*>(status);
 }
