@@ -107,8 +107,16 @@ def test_fp8_head_full_size(orc, mode):
     ws = ss.workspace(w.T, w.V, w.C, w.D)
     scale = 1.0 / w.T
     got = ss.step(H, W, tg, w.C, w.seed, ws, scale=scale, fp8=mode)
+    got = {k: v.clone() for k, v in got.items()}
     torch.cuda.synchronize()
     assert ss.read_status(ws)[0] == 0
+    # ss_step makes H's e4m3 codes beside the candidate build (several tiles
+    # per block at this size); the separate calls make them after the gather
+    sep = ss.step_separate(H, W, tg, w.C, w.seed, ws, scale=scale, fp8=mode)
+    torch.cuda.synchronize()
+    for k in ("cand", "slot", "loss", "lse", "dH", "dW"):
+        assert torch.equal(got[k], sep[k]), k
+    del sep
     cand, slot, _ = orc.build_candidates(x["targets"], w.V, w.C, w.seed)
     np.testing.assert_array_equal(got["cand"].cpu().numpy(), cand)
     Hq, Wq, _, _ = orc.fp8_inputs(x["H"], x["W"], cand)
