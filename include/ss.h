@@ -334,10 +334,16 @@ void ss_step_graph_destroy(ss_step_graph* graph);
  * rejected with SS_ERR_UNSUPPORTED (ss_last_error says by how much).
  *   status_host : NULL, or a host int32 that receives the device status
  *                 word of this call after the stream is synchronised; the
- *                 call then also returns it (e.g. SS_ERR_INDEX).
- * The first call on a device looks up the array's device address (once per
- * device, with that device current); make that first call before any stream
- * capture. The call allocates nothing: no cudaMalloc, no cudaFree, no
+ *                 call then also returns it (e.g. SS_ERR_INDEX). With NULL
+ *                 the call does not synchronise, and a device-side error
+ *                 (a candidate id or slot out of range) cannot be observed
+ *                 afterwards: the status word lives in the library's private
+ *                 array, which ss_read_status cannot reach. loss and lse are
+ *                 then left as they were. Pass a status_host whenever cand
+ *                 and slot are not known to be valid.
+ * The first call on a device looks up the array's device address (with that
+ * device current; again after the device's context is replaced, e.g. by
+ * cudaDeviceReset); make that first call before any stream capture. The call allocates nothing: no cudaMalloc, no cudaFree, no
  * allocating library routine. All calls share the one array, which keeps the
  * previous call's contents; each call clears its status word first and
  * overwrites everything else it reads. Calls whose work overlaps on the GPU

@@ -548,23 +548,55 @@ void trace_post(cudaStream_t s) {
 static __device__ __align__(256) unsigned char g_noalloc_scratch[SS_NOALLOC_SCRATCH_BYTES];
 
 std::mutex g_noalloc_mu;
-void* g_noalloc_addr[kMaxDevices];
+// The array's device address, per device, together with the context it was
+// looked up in: after cudaDeviceReset (or once the primary context is
+// released and created again) the module is loaded anew and the address may
+// change, so a different current context means a fresh lookup.
+struct NoallocAddr {
+  void* ctx;
+  void* addr;
+};
+NoallocAddr g_noalloc_addr[kMaxDevices];
 
-// Device address of g_noalloc_scratch on the current device, looked up once
-// per device (with that device current) and cached.
+using CtxGetCurrentFn = int (*)(void**);  // cuCtxGetCurrent(CUcontext*), CUDA_SUCCESS = 0
+
+CtxGetCurrentFn ctx_get_current_fn() {
+  static CtxGetCurrentFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<CtxGetCurrentFn>(p);
+  });
+  return fn;
+}
+
+// Device address of g_noalloc_scratch on the current device, looked up with
+// that device current and cached per (device, context).
 cudaError_t noalloc_scratch_address(void** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  void* ctx = nullptr;
+  CtxGetCurrentFn get_ctx = ctx_get_current_fn();
+  if (!get_ctx || get_ctx(&ctx) != 0) return cudaErrorDeviceUninitialized;
   std::lock_guard<std::mutex> lock(g_noalloc_mu);
-  if (g_noalloc_addr[dev] == nullptr) {
+  NoallocAddr& a = g_noalloc_addr[dev];
+  if (ctx == nullptr || a.addr == nullptr || a.ctx != ctx) {
+    // (the lookup makes the device's primary context current if no context
+    // was yet)
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
     if (e != cudaSuccess) return e;
-    g_noalloc_addr[dev] = p;
+    if (ctx == nullptr && (get_ctx(&ctx) != 0 || ctx == nullptr)) return cudaErrorDeviceUninitialized;
+    a.ctx = ctx;
+    a.addr = p;
   }
-  *out = g_noalloc_addr[dev];
+  *out = a.addr;
   return cudaSuccess;
 }
 

@@ -8,10 +8,13 @@ needs, so ss_forward_noalloc keeps its scratch in a fixed array inside the
 library's device data instead.
 
 These tests call it through the C ABI and check its loss and lse against the
-ordinary ss_forward, within the tolerance the other parity tests use, on two
-calls in a row with different batch sizes (the shared array keeps the first
-call's contents, so the second call must not depend on them), plus its size
-limit. This file is named to be collected last.
+ordinary ss_forward, within the tolerance the other parity tests use, on calls
+in a row on the shared array: a larger batch first, then a call with a
+candidate id out of range (the gather's bounds check reports SS_ERR_INDEX
+without touching memory outside W), then a smaller valid batch, which must
+return SS_OK (each call clears the status word) and must not read the larger
+call's leftover partials or target logits. Also its size limit. This file is
+named to be collected last.
 """
 import ctypes
 
@@ -44,14 +47,34 @@ def _close(got, ref):
     assert np.all(np.abs(got - ref) <= LOSS_RTOL * np.abs(ref) + 1e-5)
 
 
-def test_noalloc_forward_matches_forward_two_calls():
-    cases = [(300, 3000, 768, 517, 4), (1000, 8000, 768, 2000, 5)]
-    for T, V, D, C, seed in cases:  # two calls in a row on the shared array
-        H, W, cand, slot, ref_loss, ref_lse = _batch(T, V, D, C, seed)
-        loss = torch.full((T,), float("nan"), device="cuda")
-        lse = torch.full((T,), float("nan"), device="cuda")
-        ss.forward_noalloc(H, W, cand, slot, loss, lse, check_status=True)
-        torch.cuda.synchronize()
+def _run(H, W, cand, slot):
+    T = H.shape[0]
+    loss = torch.full((T,), float("nan"), device="cuda")
+    lse = torch.full((T,), float("nan"), device="cuda")
+    ss.forward_noalloc(H, W, cand, slot, loss, lse, check_status=True)
+    torch.cuda.synchronize()
+    return loss, lse
+
+
+def test_noalloc_forward_matches_forward_calls_in_a_row():
+    big = _batch(1000, 8000, 768, 2000, 5)
+    small = _batch(300, 3000, 768, 517, 4)
+    # 1: the larger batch fills more of the shared array
+    H, W, cand, slot, ref_loss, ref_lse = big
+    loss, lse = _run(H, W, cand, slot)
+    _close(loss, ref_loss)
+    _close(lse, ref_lse)
+    # 2: an out-of-range candidate id: the error comes back through status_host
+    H, W, cand, slot, _, _ = small
+    bad = cand.clone()
+    bad[7] = W.shape[0] + 11
+    with pytest.raises(ss.SSError) as e:
+        _run(H, W, bad, slot)
+    assert e.value.name == "SS_ERR_INDEX"
+    # 3, 4: the smaller valid batch, twice: SS_OK again, and the same values
+    H, W, cand, slot, ref_loss, ref_lse = small
+    for _ in range(2):
+        loss, lse = _run(H, W, cand, slot)
         _close(loss, ref_loss)
         _close(lse, ref_lse)
 
