@@ -35,6 +35,7 @@ constexpr size_t kHdrBytes = 1024;  // int32 status, int32 U, padding, FP8 amax 
 constexpr size_t kHdrAmax = 64;     // byte offset of float amax[2] (max |H|, max |W_c|)
 constexpr size_t kHdrBar = 72;      // uint32 bar[2] of k_h_prep_beside (arrivals, gave up)
 constexpr size_t kHdrQuant = 80;    // ss_quantize_e4m3's own float amax + int32 status
+constexpr size_t kHdrFallback = 96;  // int32: ss_step's stored-probability backward falls back
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -469,6 +470,112 @@ __global__ void __launch_bounds__(256) k_lse_merge(const float2* __restrict__ pa
   }
 }
 
+// ss_step's merge when the forward kept the probabilities (EpiFwdP): lse and
+// loss as k_lse_merge (two partials per row per logit tile), then, for the
+// backward, per token t with alpha = exp(r[t] - lse[t]):
+//   rowfac[t] = scale * alpha                        dH   = rowfac * (Pt' . W_c)
+//   Pt[t, slot[t]] = bf16(exp(tgt - r) - exp(lse - r))   so Pt' = (P - Y) / alpha
+//   Hs[t, :] = bf16(alpha * H[t, :])                 dW_c = scale * (Pt'^T . Hs)
+// The target column is recomputed from the fp32 target logit, so (P - 1) keeps
+// its precision when P is close to 1. A row whose lse exceeds r by more than
+// kStoredSpan (or is not finite) raises *fallback: alpha and Pt' would then
+// leave the range where bf16 holds them to full precision, and the backward
+// recomputes G from the logits instead (k_stored_fallback, gated GEMM).
+constexpr float kStoredSpan = 60.f;
+
+__global__ void __launch_bounds__(256) k_lse_merge_p(
+    const float2* __restrict__ part, const float* __restrict__ tgt,
+    const int32_t* __restrict__ slot, const float* __restrict__ ref, int T, int C, int n_parts,
+    const uint16_t* __restrict__ H, int D, float scale, uint16_t* __restrict__ Pt, int64_t ldP,
+    uint16_t* __restrict__ Hs, float* __restrict__ rowfac, int* fallback,
+    float* __restrict__ loss, float* __restrict__ lse, int* status) {
+  pdl_enter();
+  if (read_status(status) != 0) return;
+  const int64_t lanes = static_cast<int64_t>(T) * kMergeLanes;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  const int n8 = D / 8;
+  for (int64_t g0 = static_cast<int64_t>(blockIdx.x) * blockDim.x; g0 < lanes; g0 += stride) {
+    const int64_t gid = g0 + threadIdx.x;
+    const int t = static_cast<int>(gid / kMergeLanes);
+    const int k = static_cast<int>(gid % kMergeLanes);
+    const bool valid = gid < lanes;
+    float M = -INFINITY, S = 0.f;
+    constexpr int kBatch = 8;
+    if (valid)
+      for (int c0 = k; c0 < n_parts; c0 += kMergeLanes * kBatch) {
+        float2 q[kBatch];
+#pragma unroll
+        for (int i = 0; i < kBatch; ++i) {
+          const int c = c0 + i * kMergeLanes;
+          q[i] = c < n_parts ? __ldcg(part + static_cast<size_t>(c) * T + t)
+                             : make_float2(-INFINITY, 0.f);
+        }
+#pragma unroll
+        for (int i = 0; i < kBatch; ++i) lse_fold(M, S, q[i].x, q[i].y);
+      }
+#pragma unroll
+    for (int o = 1; o < kMergeLanes; o <<= 1) {
+      const float m2 = __shfl_xor_sync(0xffffffffu, M, o);
+      const float s2 = __shfl_xor_sync(0xffffffffu, S, o);
+      lse_fold(M, S, m2, s2);
+    }
+    const float l = M + logf(S);
+    const int sl = valid ? __ldg(slot + t) : 0;
+    const bool bad = valid && static_cast<unsigned>(sl) >= static_cast<unsigned>(C);
+    const float r = valid ? __ldcg(ref + t) : 0.f;
+    const float alpha = expf(r - l);
+    if (valid && k == 0) {
+      if (bad) {
+        set_status(status, SS_ERR_INDEX);
+      } else {
+        const float x = __ldcg(tgt + t);
+        lse[t] = l;
+        loss[t] = l - x;
+        rowfac[t] = scale * alpha;
+        if (!(l - r <= kStoredSpan)) {
+          *fallback = 1;
+        } else {
+          Pt[static_cast<int64_t>(t) * ldP + sl] = bf16_bits(expf(x - r) - expf(l - r));
+        }
+      }
+    }
+    if (valid && !bad) {
+      const uint4* src = reinterpret_cast<const uint4*>(H + static_cast<int64_t>(t) * D);
+      uint4* dst = reinterpret_cast<uint4*>(Hs + static_cast<int64_t>(t) * D);
+      for (int i = k; i < n8; i += kMergeLanes) {
+        const uint4 v = __ldg(src + i);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        uint32_t o[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          o[j] = pack_bf16x2(__uint_as_float(w[j] << 16) * alpha,
+                             __uint_as_float(w[j] & 0xffff0000u) * alpha);
+        dst[i] = make_uint4(o[0], o[1], o[2], o[3]);
+      }
+    }
+  }
+}
+
+// ss_step's fallback when k_lse_merge_p raised *fallback: G = P - Y is then
+// recomputed from the logits (the gated softmax-gradient GEMM), so dH's
+// per-row factor becomes plain `scale` and Hs a copy of H. Does nothing when
+// the flag is clear (the usual case).
+__global__ void __launch_bounds__(256) k_stored_fallback(const int* fallback,
+                                                         const uint16_t* __restrict__ H,
+                                                         int64_t n16, int T, float scale,
+                                                         uint16_t* __restrict__ Hs,
+                                                         float* __restrict__ rowfac,
+                                                         int* status) {
+  pdl_enter();
+  if (read_status(status) != 0 || read_status(fallback) == 0) return;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  const int64_t i0 = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const uint4* src = reinterpret_cast<const uint4*>(H);
+  uint4* dst = reinterpret_cast<uint4*>(Hs);
+  for (int64_t i = i0; i < n16; i += stride) dst[i] = __ldg(src + i);
+  for (int64_t i = i0; i < T; i += stride) rowfac[i] = scale;
+}
+
 // dW[cand[j], :] = 0 (the gradient of an empty batch).
 __global__ void __launch_bounds__(256) k_zero_rows(const int32_t* __restrict__ cand, int C, int V,
                                                    int D, float* __restrict__ dW, int* status) {
@@ -815,6 +922,66 @@ ss_status enqueue_backward(const uint16_t* H, const int32_t* cand, const int32_t
   return e == cudaSuccess ? SS_OK : fail("launch gemm_grads", e);
 }
 
+// ss_step with the plain bf16 head and one target: the forward keeps the
+// probabilities exp(S - r) (EpiFwdP) and the gradient GEMMs read them, so
+// the logits are computed once per step. The merge patches the target column
+// and writes the per-row factors; the softmax-gradient GEMM (the recompute)
+// runs only if the merge raised the fallback flag. The regions: Pt in G's
+// place, r and the dH row factors after the target logits, Hs = alpha H in
+// the place of the FP8 head's rounded H.
+ss_status enqueue_step_stored(const uint16_t* H, const int32_t* cand, const int32_t* slot,
+                              int64_t T, int64_t V, int64_t C, int64_t D, float scale,
+                              int accumulate, float* loss, float* lse, uint16_t* dH, float* dW,
+                              const Layout& L, char* ws, int nsm, cudaStream_t s) {
+  int* status = reinterpret_cast<int*>(ws + L.hdr);
+  int* fallback = reinterpret_cast<int*>(ws + L.hdr + kHdrFallback);
+  uint16_t* Wc = reinterpret_cast<uint16_t*>(ws + L.wc);
+  uint16_t* P = reinterpret_cast<uint16_t*>(ws + L.g);
+  float2* part = reinterpret_cast<float2*>(ws + L.part);
+  float* tgt = reinterpret_cast<float*>(ws + L.tgt);
+  float* ref = tgt + T;
+  float* rowfac = tgt + 2 * T;
+  uint16_t* Hs = reinterpret_cast<uint16_t*>(ws + L.hq);
+  const int iT = static_cast<int>(T), iV = static_cast<int>(V), iC = static_cast<int>(C),
+            iD = static_cast<int>(D);
+  const uint64_t pRow = static_cast<uint64_t>(L.ldG) * 2;
+  CUtensorMap tH, tWc, tWc2, tPk, tWcMn, tPmn, tHsMn;
+  const bool ok = make_map(&tH, H, D, T, D * 2, 64, 128) &&
+                  make_map(&tWc, Wc, D, C, D * 2, 64, kBnLogits) &&
+                  make_map(&tWc2, Wc, D, C, D * 2, 64, kBnLogits / 2) &&
+                  make_map(&tPk, P, C, T, pRow, 64, 128) &&
+                  make_map(&tWcMn, Wc, D, C, D * 2, 64, 64) &&
+                  make_map(&tPmn, P, C, T, pRow, 64, 64) &&
+                  make_map(&tHsMn, Hs, D, T, D * 2, 64, 64);
+  if (!ok) return fail("cuTensorMapEncodeTiled", cudaErrorInvalidValue);
+  trace_pre(s, "gemm_forward_lse");
+  cudaError_t e = launch_forward_stored(tH, tWc, tPk, iT, iC, iD, slot, part, tgt, ref, fallback,
+                                        status, nsm, s);
+  trace_post(s);
+  if (e != cudaSuccess) return fail("launch gemm_forward_lse", e);
+  trace_pre(s, "lse_merge");
+  e = launch_pdl(k_lse_merge_p, dim3(static_cast<int>((T * kMergeLanes + 255) / 256)), dim3(256),
+                 0, s, part, tgt, slot, ref, iT, iC, static_cast<int>(L.n_ct * 2), H, iD, scale,
+                 P, static_cast<int64_t>(L.ldG), Hs, rowfac, fallback, loss, lse, status);
+  trace_post(s);
+  if (e != cudaSuccess) return fail("launch k_lse_merge_p", e);
+  trace_pre(s, "stored_fallback");
+  e = launch_pdl(k_stored_fallback, dim3(2 * nsm), dim3(256), 0, s,
+                 static_cast<const int*>(fallback), H, T * D / 8, iT, scale, Hs, rowfac, status);
+  trace_post(s);
+  if (e != cudaSuccess) return fail("launch k_stored_fallback", e);
+  trace_pre(s, "gemm_softmax_grad");
+  e = launch_softmax_grad_gated(tH, tWc, tWc2, tPk, iT, iC, iD, slot, lse, 1.f, fallback, status,
+                                nsm, s);
+  trace_post(s);
+  if (e != cudaSuccess) return fail("launch gemm_softmax_grad", e);
+  trace_pre(s, "gemm_grads");
+  e = launch_grads(tPk, tWcMn, tPmn, tHsMn, iT, iC, iD, iV, accumulate, cand, dH, dW, status, nsm,
+                   s, rowfac, &scale);
+  trace_post(s);
+  return e == cudaSuccess ? SS_OK : fail("launch gemm_grads", e);
+}
+
 ss_status enqueue_zero_rows(const int32_t* cand, int64_t C, int64_t V, int64_t D, float* dW,
                             int* status, int nsm, cudaStream_t s) {
   trace_pre(s, "zero_rows");
@@ -1028,6 +1195,10 @@ static ss_status step_impl(const int32_t* targets, const uint16_t* H, const uint
   // one gather of W[cand] serves the forward and the backward
   ss_status r = enqueue_gather_operands(W, cand, H, T, C, V, D, fp8, L, ws, nsm, s, h_beside);
   if (r != SS_OK) return r;
+  // the plain bf16 head with one target keeps the forward's probabilities
+  if (fp8 == 0 && !(cap > 0.f) && tg.K == 1 && tg.w[0] == 1.f)
+    return enqueue_step_stored(H, cand, slot, T, V, C, D, scale, accumulate, loss, lse, dH, dW, L,
+                               ws, nsm, s);
   // the softmax-gradient GEMM's mainloop beside the LSE merge: measured with
   // the plain bf16 head (one partial per row and logit tile); the heads whose
   // merge folds two per tile keep the wide merge and the full wait, and so do

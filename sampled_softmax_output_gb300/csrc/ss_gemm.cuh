@@ -78,6 +78,11 @@ struct GemmShape {
   // and MMA warps then start at once; the epilogue waits before its first
   // tile. (k_gemm only; the CTA-pair kernel always waits first.)
   int late_wait;
+  // k_gemm only: the units cover the column tiles [n_begin, n_tiles) (0: all)
+  int n_begin;
+  // non-null: the kernel does its work only if *gate != 0, read once the
+  // kernels before it have completed (no late_wait); else every CTA returns
+  int* gate;
 };
 
 // ----------------------------------------------------------------- epilogues
@@ -297,8 +302,9 @@ struct EpiGT {
     float log2_scale;  // log2|scale| (-inf for 0)
     int* status;
     HeadCap head;      // used when CAP: G = scale * (P(z) - Y) * dz/ds
-    Targets tg;        // used when KMAX > 1: G = scale (W P - sum_k w[k] Y_k), W = sum_k w[k];
-                       // log2_scale is then log2(|scale| W)
+    Targets tg;        // the targets' weights: G = scale (W P - sum_k w[k] Y_k), W = sum_k w[k]
+                       // (one target: W = w[0], 1 for the single-target loss); log2_scale is
+                       // log2(|scale| W)
     const float* amax;  // used when F8: logits = accumulator * e4m3_logit_scale(amax)
   };
   __device__ static void begin(const Params& p, EpiState& es) {
@@ -386,12 +392,10 @@ struct EpiGT {
             if constexpr (F8 && !CAP) xt *= sig;  // capped: hz carries the scale
             if (has) {
               // the one-hot weight of this column: every target k2 that falls on it
-              float wt = 1.f;
-              if constexpr (KMAX > 1) {
-                wt = 0.f;
+              // (one target: its own weight, 1 for the single-target loss)
+              float wt = 0.f;
 #pragma unroll
-                for (int k2 = 0; k2 < KMAX; ++k2) wt += (sl[k2] == sl[k]) ? p.tg.w[k2] : 0.f;
-              }
+              for (int k2 = 0; k2 < KMAX; ++k2) wt += (sl[k2] == sl[k]) ? p.tg.w[k2] : 0.f;
               float gt;
               if constexpr (CAP) {
                 const float zt = head_z(xt, hz);
@@ -417,6 +421,154 @@ struct EpiGT {
   }
 };
 using EpiG = EpiGT<false>;
+
+// Forward that keeps the probabilities for the backward (plain bf16 head, one
+// target per token). Besides the per-row softmax partials and the target
+// logit of EpiFwdT, it writes
+//   Pt[t, j] = exp(S[t,j] - r[t])  (bf16, every column of the tile),
+// with r[t] a per-row reference fixed before the tiles after the first: the
+// row's largest logit over the first logit tile. PRE: this launch covers that
+// tile only, finds r[t] itself (every thread of a row reads the row's whole
+// tile from TMEM, so both column groups find the same value) and stores it;
+// otherwise r[t] is read back. exp(S - r) is the partial's own exponential
+// exp(S - m), m the running max, times exp(m - r): one multiply per logit.
+// Once lse is known,
+//   G[t,j] = scale (P - Y) = scale exp(r - lse) (Pt - Y exp(lse - r)),
+// so the backward needs no second pass over the logits (the merge patches
+// the target column and supplies the per-row factor). The staging and the
+// TMA stores are those of EpiGT; two column groups, two partials per row per
+// tile, as in part[(nt * 2 + cg) * T + t].
+template <bool PRE>
+struct EpiFwdP {
+  static constexpr int kStageBytes = 2 * 16384;
+  // Pt streams through L2 once; the H and W_c tiles are re-read by every CTA
+  static constexpr bool kKeepOperands = true;
+  struct Params {
+    CUtensorMap tmP;  // Pt [T, C] bf16 (row pitch ldG), box 64 x 128, 128-byte swizzle
+    int T, C;
+    const int32_t* slot;
+    float2* part;
+    float* tgt;        // [T]: S[t, slot[t]]
+    float* ref;        // [T]: r[t] (PRE writes it, the later tiles read it)
+    int* clear_word;   // PRE: set to 0 once (the merge's fallback flag), or null
+    int* status;
+  };
+  __device__ static void begin(const Params& p, EpiState& es) {
+    if constexpr (PRE)
+      if (p.clear_word && blockIdx.x == 0 && es.ep_tid == 0) *p.clear_word = 0;
+  }
+  __device__ static void finish(const Params&, EpiState& es) {
+    if ((es.ep_tid & 127) == 0) bulk_wait<0>();
+  }
+  template <int BN, int NCG>
+  __device__ static void apply(const Params& p, int mt, int nt, int row, uint32_t taddr,
+                               EpiState& es, int cg) {
+    static_assert(NCG == 2 && BN == 256, "two column groups of two 64-column quarters");
+    const int bar = 1 + 2 * cg;
+    const bool leader = (es.ep_tid & 127) == 0;
+    const int t = mt * BM + row;
+    const bool valid = t < p.T;
+    const int sl = valid ? __ldg(p.slot + t) : -1;
+    if (valid && nt == 0 && static_cast<unsigned>(sl) >= static_cast<unsigned>(p.C))
+      set_status(p.status, SS_ERR_INDEX);
+    const int j0 = nt * BN;
+    const int ncols = min(BN, p.C - j0);
+    float r;
+    if constexpr (PRE) {  // the largest logit of the row over this (first) tile
+      r = -INFINITY;
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
+        if (c * 32 >= ncols) break;  // uniform
+        uint32_t v[32];
+        tmem_ld32(taddr + c * 32, v);
+        tmem_ld_wait();
+        const int nv = min(32, ncols - c * 32);
+#pragma unroll
+        for (int k = 0; k < 32; ++k)
+          if (k < nv) r = fmaxf(r, __uint_as_float(v[k]));
+      }
+      if (valid && cg == 0) p.ref[t] = r;
+    } else {
+      r = valid ? __ldcg(p.ref + t) : 0.f;
+    }
+    const float r2 = r * kLog2e;
+    const uint32_t r7 = static_cast<uint32_t>(row & 7);
+    float m = -INFINITY, s = 0.f, tg = 0.f;
+    bool has_t = false;
+#pragma unroll 1
+    for (int q = 2 * cg; q < 2 * cg + 2; ++q) {
+      const int qc = q * 64;
+      if (qc >= ncols) break;  // uniform: depends on the tile only
+      const uint32_t buf = es.stage + static_cast<uint32_t>(cg) * 16384u;
+      // the store that last used this group's buffer must have read it
+      if (es.rounds >= 1 && leader) bulk_wait_read<0>();
+      named_bar_sync(bar, 128);
+      const uint32_t rowbase = buf + static_cast<uint32_t>(row) * 128u;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int jc = qc + 32 * h;
+        if (jc >= ncols) break;
+        uint32_t v[32];
+        tmem_ld32(taddr + jc, v);
+        tmem_ld_wait();
+        const int nv = min(32, ncols - jc);
+        float cm = -INFINITY;
+#pragma unroll
+        for (int k = 0; k < 32; ++k)
+          if (nv == 32 || k < nv) cm = fmaxf(cm, __uint_as_float(v[k]));
+        const float nm = fmaxf(m, cm);
+        const float nm2 = nm * kLog2e;
+        const float f = ex2_approx(nm2 - r2);  // exp(m - r)
+        float e[32];
+        float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll
+        for (int k = 0; k < 32; k += 4) {
+          e[k + 0] = (nv == 32 || k + 0 < nv) ? ex2_approx(fmaf(__uint_as_float(v[k + 0]), kLog2e, -nm2)) : 0.f;
+          e[k + 1] = (nv == 32 || k + 1 < nv) ? ex2_approx(fmaf(__uint_as_float(v[k + 1]), kLog2e, -nm2)) : 0.f;
+          e[k + 2] = (nv == 32 || k + 2 < nv) ? ex2_approx(fmaf(__uint_as_float(v[k + 2]), kLog2e, -nm2)) : 0.f;
+          e[k + 3] = (nv == 32 || k + 3 < nv) ? ex2_approx(fmaf(__uint_as_float(v[k + 3]), kLog2e, -nm2)) : 0.f;
+          a0 += e[k + 0];
+          a1 += e[k + 1];
+          a2 += e[k + 2];
+          a3 += e[k + 3];
+        }
+        s = s * ex2_approx((m - nm) * kLog2e) + ((a0 + a1) + (a2 + a3));
+        m = nm;
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(e[2 * i] * f, e[2 * i + 1] * f);
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+          const uint32_t ci = static_cast<uint32_t>(h * 4 + w);
+          st_shared_v4(rowbase + ((ci ^ r7) << 4), pk[4 * w], pk[4 * w + 1], pk[4 * w + 2],
+                       pk[4 * w + 3]);
+        }
+        // the target logit: a target falls in a given 32-column chunk for a
+        // few rows of a warp at most
+        const int off = sl - j0 - jc;
+        const bool hit = static_cast<unsigned>(off) < static_cast<unsigned>(nv);
+        if (__any_sync(0xffffffffu, hit)) {
+          const float x = __uint_as_float(select32(v, off));
+          if (hit) {
+            tg = x;
+            has_t = true;
+          }
+        }
+      }
+      fence_proxy_async_smem();
+      named_bar_sync(bar, 128);
+      if (leader) {
+        tma_store_2d_hint(&p.tmP, buf, j0 + qc, mt * BM, l2_evict_first());
+        bulk_commit();
+      }
+      ++es.rounds;
+    }
+    if (valid) {
+      p.part[static_cast<size_t>(nt * 2 + cg) * p.T + t] = make_float2(m, s);
+      if (has_t) p.tgt[t] = tg;
+    }
+  }
+};
 
 // FP8 gradients: G (before `scale`) is scaled by 2^g8e, the largest power of
 // two that keeps its bound -- |P - Y| <= 1, times dz/ds <= cap / (4 tau) with
@@ -568,6 +720,7 @@ struct EpiDhT {
     float scale;         // used when F8G
     const float* amax;   // used when F8G: max |W_c|
     int g8e;             // used when F8G: G8's power of two
+    const float* rowfac;  // bf16: null, or a factor per row of dH (the accumulator times it)
   };
   __device__ static void begin(const Params& p, EpiState& es) {
     if constexpr (F8G) es.f0 = fp8_grad_alpha(p.scale, p.g8e, p.amax);
@@ -585,11 +738,15 @@ struct EpiDhT {
     uint16_t* drow = p.dH + static_cast<size_t>(valid ? t : 0) * p.D + n0;
     float al = 1.f;
     if constexpr (F8G) al = es.f0;
+    const bool rf = !F8G && p.rowfac != nullptr;  // uniform
+    if (rf) al = valid ? __ldg(p.rowfac + t) : 0.f;
     for_tmem_chunks<CPG>(taddr, cg * CPG, [&](const uint32_t(&r)[32], int i) {
       const int jc = i * 32;
       if (jc >= ncols || !valid) return;
       uint4* dst = reinterpret_cast<uint4*>(drow + jc);
-      auto x = [&](int k) { return F8G ? __uint_as_float(r[k]) * al : __uint_as_float(r[k]); };
+      auto x = [&](int k) {
+        return (F8G || rf) ? __uint_as_float(r[k]) * al : __uint_as_float(r[k]);
+      };
 #pragma unroll
       for (int v = 0; v < 4; ++v) {
         const uint32_t q0 = pack_bf16x2(x(8 * v + 0), x(8 * v + 1));
@@ -615,12 +772,14 @@ struct EpiDwT {
     const int32_t* cand;
     float* dW;
     int* status;
-    float scale;         // used when F8G
+    float scale;         // F8G: the gradient's scale; bf16 with out_scale: the factor
     const float* amax;   // used when F8G: max |H|
     int g8e;             // used when F8G: G8's power of two
+    int out_scale;       // bf16: 1 if the accumulator is multiplied by `scale`
   };
   __device__ static void begin(const Params& p, EpiState& es) {
     if constexpr (F8G) es.f0 = fp8_grad_alpha(p.scale, p.g8e, p.amax);
+    else es.f0 = p.out_scale ? p.scale : 1.f;
   }
   __device__ static void finish(const Params&, EpiState&) {}
   template <int BN, int NCG>
@@ -638,13 +797,13 @@ struct EpiDwT {
     const int ncols = min(CPG * 32, p.D - n0);
     if (ncols <= 0) return;
     float* drow = p.dW + static_cast<size_t>(valid ? v : 0) * p.D + n0;
-    float al = 1.f;
-    if constexpr (F8G) al = es.f0;
+    const float al = es.f0;
+    const bool sc = F8G || p.out_scale;  // uniform
     for_tmem_chunks<CPG>(taddr, cg * CPG, [&](const uint32_t(&r)[32], int i) {
       const int jc = i * 32;
       if (jc >= ncols || !valid) return;
       float4* dst = reinterpret_cast<float4*>(drow + jc);
-      auto x = [&](int k) { return F8G ? __uint_as_float(r[k]) * al : __uint_as_float(r[k]); };
+      auto x = [&](int k) { return sc ? __uint_as_float(r[k]) * al : __uint_as_float(r[k]); };
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
         float4 o = make_float4(x(4 * k), x(4 * k + 1), x(4 * k + 2), x(4 * k + 3));
@@ -689,8 +848,10 @@ __global__ void __launch_bounds__(64 + 32 * EPI_WARPS, 1)
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
 
-  // An earlier error of this batch: do nothing (decided once for the CTA).
-  if (threadIdx.x == 0) s_go = (read_status(status) == 0);
+  // An earlier error of this batch, or a gate that is shut: do nothing
+  // (decided once for the CTA).
+  if (threadIdx.x == 0)
+    s_go = read_status(status) == 0 && (shp.gate == nullptr || read_status(shp.gate) != 0);
   __syncthreads();
   if (!s_go) return;
 
@@ -718,7 +879,8 @@ __global__ void __launch_bounds__(64 + 32 * EPI_WARPS, 1)
   tc_fence_after();
   const uint32_t tmem_base = ctrl->tmem_base;
   volatile int* abort_flag = &ctrl->abort_flag;
-  const int num_units = shp.m_tiles * shp.n_tiles;
+  const int n_cols = shp.n_tiles - shp.n_begin;  // column tiles per row block
+  const int num_units = shp.m_tiles * n_cols;
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -727,7 +889,7 @@ __global__ void __launch_bounds__(64 + 32 * EPI_WARPS, 1)
       uint32_t ph = 0, issued = 0, issued_ph = 0;
       bool ok = true;
       for (int u = blockIdx.x; ok && u < num_units; u += gridDim.x) {
-        const int mt = u / shp.n_tiles, nt = u % shp.n_tiles;
+        const int mt = u / n_cols, nt = shp.n_begin + u % n_cols;
         for (int kb = 0; kb < shp.k_blocks; ++kb) {
           if (!mbar_wait(&ctrl->empty[s], ph ^ 1u, abort_flag, status)) {
             ok = false;
@@ -844,7 +1006,7 @@ __global__ void __launch_bounds__(64 + 32 * EPI_WARPS, 1)
       }
       if (!go) break;
       tc_fence_after();
-      const int mt = u / shp.n_tiles, nt = u % shp.n_tiles;
+      const int mt = u / n_cols, nt = shp.n_begin + u % n_cols;
       Epi::template apply<BN, NCG>(ep, mt, nt, row, lane_addr + static_cast<uint32_t>(b * BN), es,
                                    cg);
       tc_fence_before();
@@ -870,8 +1032,9 @@ cudaError_t launch_gemm(const CUtensorMap& tA, const CUtensorMap& tB, GemmShape 
                         cudaStream_t stream) {
   auto kern = k_gemm<BN, STAGES, A_MN, B_MN, Epi, EPI_WARPS, F8>;
   constexpr int smem = GemmSmem<BN, STAGES, Epi::kStageBytes>::TOTAL;
-  const int units = shp.m_tiles * shp.n_tiles;
+  const int units = shp.m_tiles * (shp.n_tiles - shp.n_begin);
   if (units <= 0) return cudaSuccess;
+  if (shp.gate != nullptr && shp.late_wait) return cudaErrorInvalidValue;  // the gate needs the wait
   const int grid = units < num_sms ? units : num_sms;
   return launch_pdl(kern, dim3(grid), dim3(64 + 32 * EPI_WARPS), smem, stream, tA, tB, shp, ep,
                     status);

@@ -65,7 +65,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * EPI_WARPS,
 
   // Both CTAs must take the same decision: each reads the status word, then
   // each combines its own answer with the peer's after a cluster barrier.
-  if (threadIdx.x == 0) s_go = (read_status(status) == 0);
+  if (threadIdx.x == 0)
+    s_go = read_status(status) == 0 && (shp.gate == nullptr || read_status(shp.gate) != 0);
   cluster_sync_all();
   if (threadIdx.x == 0) s_go = s_go && ld_shared_cluster_u32(mapa_shared(smem_u32(&s_go), rank ^ 1u));
   cluster_sync_all();  // the peer has read this CTA's s_go before it changes
@@ -256,6 +257,7 @@ cudaError_t launch_gemm2(const CUtensorMap& tA, const CUtensorMap& tB, GemmShape
   constexpr int smem = Gemm2Smem<BN, STAGES, Epi::kStageBytes>::TOTAL;
   const int units = shp.m_tiles * shp.n_tiles;
   if (units <= 0) return cudaSuccess;
+  if (shp.n_begin != 0) return cudaErrorInvalidValue;  // whole column range only
   const int pairs = units < num_sms / 2 ? units : num_sms / 2;
   return launch_pdl(kern, dim3(2 * pairs), dim3(64 + 32 * EPI_WARPS), smem, stream, tA, tB, shp, ep,
                     status);

@@ -21,18 +21,20 @@ namespace ss {
 
 
 cudaError_t launch_grad_h(const CUtensorMap& tG_kmaj, const CUtensorMap& tWc_mn, int T, int C,
-                          int D, uint16_t* dH, int* status, int num_sms, cudaStream_t stream) {
+                          int D, uint16_t* dH, int* status, int num_sms, cudaStream_t stream,
+                          const float* rowfac) {
   GemmShape shp{(T + 2 * BM - 1) / (2 * BM), (D + kBnGrad - 1) / kBnGrad, (C + BK - 1) / BK};
-  EpiDh::Params ep{T, D, dH};
+  EpiDh::Params ep{T, D, dH, 0.f, nullptr, 0, rowfac};
   return launch_gemm2<kBnGrad, 6, false, true, EpiDh, 8>(tG_kmaj, tWc_mn, shp, ep, status, num_sms,
                                                          stream);
 }
 
 cudaError_t launch_grad_w(const CUtensorMap& tG_mn, const CUtensorMap& tH_mn, int T, int C, int D,
                           int V, int accumulate, const int32_t* cand, float* dW, int* status,
-                          int num_sms, cudaStream_t stream) {
+                          int num_sms, cudaStream_t stream, const float* out_scale) {
   GemmShape shp{(C + 2 * BM - 1) / (2 * BM), (D + kBnGrad - 1) / kBnGrad, (T + BK - 1) / BK};
-  EpiDw::Params ep{C, D, V, accumulate, cand, dW, status};
+  EpiDw::Params ep{C, D, V, accumulate, cand, dW, status, out_scale ? *out_scale : 1.f, nullptr,
+                   0, out_scale ? 1 : 0};
   return launch_gemm2<kBnGrad, 6, true, true, EpiDw, 8>(tG_mn, tH_mn, shp, ep, status, num_sms,
                                                         stream);
 }
@@ -438,7 +440,8 @@ std::shared_ptr<const GradSched> grad_schedule(int n_dw, int kb_dw, int n_dh, in
 cudaError_t launch_grads(const CUtensorMap& tG_kmaj, const CUtensorMap& tWc_mn,
                          const CUtensorMap& tG_mn, const CUtensorMap& tH_mn, int T, int C, int D,
                          int V, int accumulate, const int32_t* cand, uint16_t* dH, float* dW,
-                         int* status, int num_sms, cudaStream_t stream) {
+                         int* status, int num_sms, cudaStream_t stream, const float* rowfac,
+                         const float* out_scale) {
   GradBoth<false> p;
   p.n_nt = (D + kBnGrad - 1) / kBnGrad;
   p.n_dw = (C + 2 * BM - 1) / (2 * BM) * p.n_nt;
@@ -447,8 +450,9 @@ cudaError_t launch_grads(const CUtensorMap& tG_kmaj, const CUtensorMap& tWc_mn,
   p.kb_dh = (C + BK - 1) / BK;
   p.n_units = 0;
   p.rr = 0;
-  p.dh = EpiDh::Params{T, D, dH};
-  p.dw = EpiDw::Params{C, D, V, accumulate, cand, dW, status};
+  p.dh = EpiDh::Params{T, D, dH, 0.f, nullptr, 0, rowfac};
+  p.dw = EpiDw::Params{C, D, V, accumulate, cand, dW, status, out_scale ? *out_scale : 1.f,
+                       nullptr, 0, out_scale ? 1 : 0};
   p.status = status;
   const int pairs = std::min(num_sms / 2, kSchedMaxCtas);
   // Running dW and dH tiles side by side pays when their B operands (H and
@@ -459,9 +463,10 @@ cudaError_t launch_grads(const CUtensorMap& tG_kmaj, const CUtensorMap& tWc_mn,
                  ? grad_schedule(p.n_dw, p.kb_dw, n_dh, p.kb_dh, pairs)
                  : std::shared_ptr<const GradSched>();
   if (!sch) {  // two phase-separated round-robin launches
-    cudaError_t e = launch_grad_h(tG_kmaj, tWc_mn, T, C, D, dH, status, num_sms, stream);
+    cudaError_t e = launch_grad_h(tG_kmaj, tWc_mn, T, C, D, dH, status, num_sms, stream, rowfac);
     if (e != cudaSuccess) return e;
-    return launch_grad_w(tG_mn, tH_mn, T, C, D, V, accumulate, cand, dW, status, num_sms, stream);
+    return launch_grad_w(tG_mn, tH_mn, T, C, D, V, accumulate, cand, dW, status, num_sms, stream,
+                         out_scale);
   }
   return launch_pdl(k_grads<false>, dim3(2 * pairs), dim3(64 + 32 * kGradEpiWarps), LG2::TOTAL,
                     stream, tG_kmaj, tWc_mn, tG_mn, tH_mn, p, *sch);
@@ -480,8 +485,8 @@ cudaError_t launch_grads_fp8(const CUtensorMap& tG8, const CUtensorMap& tW8t,
   p.kb_dw = (T + KB - 1) / KB;
   p.kb_dh = (C + KB - 1) / KB;
   p.n_units = p.n_dw + n_dh;
-  p.dh = EpiDhT<true>::Params{T, D, dH, scale, amax + 1, g8e};
-  p.dw = EpiDwT<true>::Params{C, D, V, accumulate, cand, dW, status, scale, amax, g8e};
+  p.dh = EpiDhT<true>::Params{T, D, dH, scale, amax + 1, g8e, nullptr};
+  p.dw = EpiDwT<true>::Params{C, D, V, accumulate, cand, dW, status, scale, amax, g8e, 0};
   p.status = status;
   const int pairs = std::min(num_sms / 2, kSchedMaxCtas);
   // the balanced schedule where it fits the kernel parameters, else every

@@ -57,6 +57,36 @@ cudaError_t launch_softmax_grad(const CUtensorMap& tH, const CUtensorMap& tWc,
                                             late_wait);
 }
 
+// The first logit tile of every row block finds r and clears *clear_word;
+// the launch over the other tiles starts its mainloop at once (H and W_c are
+// older than the first launch) and its epilogue waits for r.
+cudaError_t launch_forward_stored(const CUtensorMap& tH, const CUtensorMap& tWc,
+                                  const CUtensorMap& tP, int T, int C, int D, const int32_t* slot,
+                                  float2* part, float* tgt, float* ref, int* clear_word,
+                                  int* status, int num_sms, cudaStream_t stream) {
+  const int m_tiles = (T + BM - 1) / BM, n_tiles = (C + kBnLogits - 1) / kBnLogits;
+  EpiFwdP<true>::Params pre{tP, T, C, slot, part, tgt, ref, clear_word, status};
+  GemmShape first{m_tiles, 1, D / BK};
+  cudaError_t e = launch_gemm<kBnLogits, kStagesLogits, false, false, EpiFwdP<true>, 8>(
+      tH, tWc, first, pre, status, num_sms, stream);
+  if (e != cudaSuccess || n_tiles == 1) return e;
+  EpiFwdP<false>::Params rest{tP, T, C, slot, part, tgt, ref, nullptr, status};
+  GemmShape others{m_tiles, n_tiles, D / BK, 1, 1};
+  return launch_gemm<kBnLogits, kStagesLogits, false, false, EpiFwdP<false>, 8>(
+      tH, tWc, others, rest, status, num_sms, stream);
+}
+
+cudaError_t launch_softmax_grad_gated(const CUtensorMap& tH, const CUtensorMap& tWc,
+                                      const CUtensorMap& tWc_half, const CUtensorMap& tG_store,
+                                      int T, int C, int D, const int32_t* slot, const float* lse,
+                                      float scale, int* gate, int* status, int num_sms,
+                                      cudaStream_t stream) {
+  const Targets one = {1, {1.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f}};
+  return softmax_grad<false, 1>(tH, tWc, tWc_half, tG_store, T, C, D, slot, lse, scale,
+                                head_cap(0.f, 1.f), one, nullptr, status, num_sms, stream, false,
+                                gate);
+}
+
 // FP8 gradients: G8 and G8^T in e5m2 from the e4m3 logits (one target)
 template <bool CAP>
 cudaError_t softmax_grad_fp8(const CUtensorMap& tH8, const CUtensorMap& tW8,

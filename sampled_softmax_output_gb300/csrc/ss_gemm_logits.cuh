@@ -41,7 +41,7 @@ cudaError_t softmax_grad(const CUtensorMap& tH, const CUtensorMap& tWc,
                          const CUtensorMap& tWc_half, const CUtensorMap& tG_store, int T, int C,
                          int D, const int32_t* slot, const float* lse, float scale,
                          const HeadCap& head, const Targets& tg, const float* amax, int* status,
-                         int num_sms, cudaStream_t stream, bool late_wait) {
+                         int num_sms, cudaStream_t stream, bool late_wait, int* gate = nullptr) {
   typename EpiGT<CAP, KMAX, F8>::Params ep;
   ep.tmG = tG_store;
   ep.T = T;
@@ -65,12 +65,14 @@ cudaError_t softmax_grad(const CUtensorMap& tH, const CUtensorMap& tWc,
   if constexpr (!F8) {  // the e4m3 operands are half the bytes: single CTAs throughout
     if (operands_exceed_l2(T, C, D)) {
       GemmShape shp{(T + 2 * BM - 1) / (2 * BM), n_tiles, D / BK};
+      shp.gate = gate;
       return launch_gemm2<kBnLogits, 6, false, false, EpiGT<CAP, KMAX>, 8>(tH, tWc_half, shp, ep,
                                                                            status, num_sms,
                                                                            stream);
     }
   }
   GemmShape shp{(T + BM - 1) / BM, n_tiles, D / (F8 ? 2 * BK : BK), late_wait ? 1 : 0};
+  shp.gate = gate;
   return launch_gemm<kBnLogits, F8 ? kStagesGradF8 : kStagesLogits, false, false,
                      EpiGT<CAP, KMAX, F8>, 8, F8>(tH, tWc, shp, ep, status, num_sms, stream);
 }

@@ -111,6 +111,22 @@ cudaError_t launch_softmax_grad_fp8(const CUtensorMap& tH8, const CUtensorMap& t
                                     int T, int C, int D, const int32_t* slot, const float* lse,
                                     float cap, float tau, int g8e, const float* amax, int* status,
                                     int num_sms, cudaStream_t stream, bool late_wait = false);
+// The forward that keeps the probabilities for the backward (plain bf16 head,
+// one target): Pt = exp(S - r) in bf16 through tP (as tG_store above), r[t]
+// the row's largest logit over the first logit tile (stored in ref), the
+// softmax partials (two per row per tile) and the target logit. Two launches:
+// the first logit tile of every row block (which finds r and clears
+// *clear_word), then the others.
+cudaError_t launch_forward_stored(const CUtensorMap& tH, const CUtensorMap& tWc,
+                                  const CUtensorMap& tP, int T, int C, int D, const int32_t* slot,
+                                  float2* part, float* tgt, float* ref, int* clear_word,
+                                  int* status, int num_sms, cudaStream_t stream);
+// launch_softmax_grad (plain bf16 head, one target) that runs only if *gate != 0
+cudaError_t launch_softmax_grad_gated(const CUtensorMap& tH, const CUtensorMap& tWc,
+                                      const CUtensorMap& tWc_half, const CUtensorMap& tG_store,
+                                      int T, int C, int D, const int32_t* slot, const float* lse,
+                                      float scale, int* gate, int* status, int num_sms,
+                                      cudaStream_t stream);
 // the same GEMMs for K > 1 targets per token (ss_gemm_logits_mtp.cu)
 cudaError_t launch_forward_logits_mtp(const CUtensorMap& tH, const CUtensorMap& tWc, int T, int C,
                                       int D, const int32_t* slot, float2* part, float* tgt,
@@ -125,18 +141,22 @@ cudaError_t launch_softmax_grad_mtp(const CUtensorMap& tH, const CUtensorMap& tW
 
 // ---- gradient GEMMs (ss_gemm_grads.cu)
 // dH = G . W_c : A = G [T, C] (K-major), B = W_c [C, D] (MN-major)
+// rowfac: null, or a factor per row of dH that the accumulator is multiplied by
 cudaError_t launch_grad_h(const CUtensorMap& tG_kmaj, const CUtensorMap& tWc_mn, int T, int C,
-                          int D, uint16_t* dH, int* status, int num_sms, cudaStream_t stream);
+                          int D, uint16_t* dH, int* status, int num_sms, cudaStream_t stream,
+                          const float* rowfac = nullptr);
 // dW[cand] (=|+=) G^T . H : A = G (MN-major), B = H [T, D] (MN-major)
+// out_scale: null, or a factor the accumulator is multiplied by
 cudaError_t launch_grad_w(const CUtensorMap& tG_mn, const CUtensorMap& tH_mn, int T, int C, int D,
                           int V, int accumulate, const int32_t* cand, float* dW, int* status,
-                          int num_sms, cudaStream_t stream);
+                          int num_sms, cudaStream_t stream, const float* out_scale = nullptr);
 // Both gradient GEMMs in one launch with a host-computed balanced schedule
 // (falls back to the two launches above for very large problems).
 cudaError_t launch_grads(const CUtensorMap& tG_kmaj, const CUtensorMap& tWc_mn,
                          const CUtensorMap& tG_mn, const CUtensorMap& tH_mn, int T, int C, int D,
                          int V, int accumulate, const int32_t* cand, uint16_t* dH, float* dW,
-                         int* status, int num_sms, cudaStream_t stream);
+                         int* status, int num_sms, cudaStream_t stream,
+                         const float* rowfac = nullptr, const float* out_scale = nullptr);
 
 // FP8 gradients: dH = G8 . W8 and dW[cand] (=|+=) G8^T . H8 on e5m2 x e4m3,
 // all operands K-major in boxes of 128 x 128 bytes: tG8 [T, C], tW8t [D, C],

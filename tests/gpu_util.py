@@ -46,6 +46,30 @@ def run_gpu(ss, x: dict, C: int, seed: int, scale: float = 1.0, dW0: np.ndarray 
             "dH": dH.float().cpu().numpy(), "dW": dW.cpu().numpy(), "status": status}
 
 
+def run_gpu_step(ss, x: dict, C: int, seed: int, scale: float = 1.0,
+                 dW0: np.ndarray | None = None, accumulate: bool = False,
+                 ws: torch.Tensor | None = None, cap: float = 0.0, tau: float = 1.0) -> dict:
+    """The same batch through the one-call entry point ss_step (with the plain
+    head it keeps the forward's probabilities for the backward)."""
+    H = to_dev_bf16(x["H"])
+    W = to_dev_bf16(x["W"])
+    T, D = H.shape
+    V = W.shape[0]
+    targets = torch.from_numpy(np.ascontiguousarray(x["targets"], np.int32)).cuda()
+    if ws is None:
+        ws = ss.workspace(T, V, C, D)
+    dW = (torch.from_numpy(np.ascontiguousarray(dW0, np.float32)).cuda() if dW0 is not None
+          else torch.zeros(V, D, dtype=torch.float32, device="cuda"))
+    out = ss.step(H, W, targets, C, seed, ws, scale=scale, accumulate=accumulate, dW=dW, cap=cap,
+                  tau=tau)
+    torch.cuda.synchronize()
+    status, U = ss.read_status(ws)
+    return {"cand": out["cand"].cpu().numpy(), "slot": out["slot"].cpu().numpy(), "U": U,
+            "loss": out["loss"].cpu().numpy(), "lse": out["lse"].cpu().numpy(),
+            "dH": out["dH"].float().cpu().numpy(), "dW": out["dW"].cpu().numpy(),
+            "status": status}
+
+
 def rel_fro(a: np.ndarray, b: np.ndarray) -> float:
     a = np.asarray(a, np.float64)
     b = np.asarray(b, np.float64)

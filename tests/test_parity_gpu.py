@@ -1,5 +1,10 @@
 """GPU path vs the CPU oracle, through the C ABI.
 
+Both entry-point sequences are checked: the three calls (ss_build_candidates,
+ss_forward, ss_backward, whose backward recomputes the logits) and the
+one-call ss_step (whose plain head keeps the forward's probabilities for the
+backward, with the recompute as its fallback).
+
 * small and ragged sizes (several tiles plus a ragged tail in T, C and D, the
   degenerate cases C = 1, U = C, C = V, T = 1): every output element compared;
 * the five full-size workloads, in the launch configuration the benchmark
@@ -12,7 +17,7 @@ import pytest
 import torch
 
 import synth
-from gpu_util import GRAD_RTOL, assert_loss_close, rel_fro, run_gpu, to_dev_bf16
+from gpu_util import GRAD_RTOL, assert_loss_close, rel_fro, run_gpu, run_gpu_step, to_dev_bf16
 
 pytestmark = pytest.mark.gpu
 
@@ -43,11 +48,15 @@ SMALL = [
 ]
 
 
+RUNS = {"calls": run_gpu, "step": run_gpu_step}
+
+
+@pytest.mark.parametrize("path", ["calls", "step"])
 @pytest.mark.parametrize("T,V,D,C,seed,scale", SMALL)
-def test_small_parity(orc, T, V, D, C, seed, scale):
+def test_small_parity(orc, T, V, D, C, seed, scale, path):
     x, C = _case(T, V, D, C, seed)
     ref = _full_oracle(orc, x, C, seed, scale)
-    got = run_gpu(ss, x, C, seed, scale)
+    got = RUNS[path](ss, x, C, seed, scale)
     assert got["status"] == 0
     assert got["U"] == ref["U"]
     np.testing.assert_array_equal(got["cand"], ref["cand"])
@@ -60,13 +69,14 @@ def test_small_parity(orc, T, V, D, C, seed, scale):
     assert np.all(got["dW"][outside] == 0)
 
 
-def test_accumulate_and_untouched_rows(orc):
+@pytest.mark.parametrize("path", ["calls", "step"])
+def test_accumulate_and_untouched_rows(orc, path):
     T, V, D, C, seed = 300, 2500, 256, 700, 11
     x, C = _case(T, V, D, C, seed)
     dW0 = np.random.default_rng(3).standard_normal((V, D)).astype(np.float32)
     for acc in (False, True):
         ref = _full_oracle(orc, x, C, seed, 0.25, dW0=dW0, accumulate=acc)
-        got = run_gpu(ss, x, C, seed, 0.25, dW0=dW0, accumulate=acc)
+        got = RUNS[path](ss, x, C, seed, 0.25, dW0=dW0, accumulate=acc)
         assert got["status"] == 0
         outside = np.setdiff1d(np.arange(V), ref["cand"])
         np.testing.assert_array_equal(got["dW"][outside], dW0[outside])
@@ -162,18 +172,28 @@ def _check_sampled(orc, x, T, V, D, C, seed, rng_seed, exact_cols, cap=0.0, tau=
     lhs = float((dWc * W64[cand_ref]).sum())
     rhs = float((dH.astype(np.float64) * H64).sum())
     assert abs(lhs - rhs) <= 0.02 * abs(rhs)
-    # the fused entry point (one gather for both passes) gives the same bits
-    # as the three calls
+    # the one-call entry point on the same batch: bit-exact candidates, and
+    # the same oracle checks (with the plain head its backward reads the
+    # forward's stored probabilities instead of recomputing the logits)
     fused = ss.step(H, W, targets, C, seed, ws, scale=scale, cap=cap, tau=tau,
                     dW=torch.full((V, D), canary, dtype=torch.float32, device="cuda"))
     torch.cuda.synchronize()
     assert ss.read_status(ws)[0] == 0
     np.testing.assert_array_equal(fused["cand"].cpu().numpy(), cand_ref)
-    np.testing.assert_array_equal(fused["loss"].cpu().numpy(), loss)
-    np.testing.assert_array_equal(fused["lse"].cpu().numpy(), lse)
-    np.testing.assert_array_equal(fused["dH"].float().cpu().numpy(), dH)
-    np.testing.assert_array_equal(fused["dW"].cpu().numpy(), dW)
+    np.testing.assert_array_equal(fused["slot"].cpu().numpy(), slot_ref)
+    f_loss, f_lse = fused["loss"].cpu().numpy(), fused["lse"].cpu().numpy()
+    f_dH = fused["dH"].float().cpu().numpy()
+    f_dW = fused["dW"].cpu().numpy()
     del fused
+    assert_loss_close(f_loss[rows], l_ref)
+    assert_loss_close(f_lse[rows], s_ref)
+    assert rel_fro(f_dH[rows], dH_ref) < GRAD_RTOL
+    assert np.all(f_dW[outside] == canary)
+    # and it agrees with the three calls over every token and candidate row
+    assert_loss_close(f_loss, loss)
+    assert rel_fro(f_dH, dH) < GRAD_RTOL
+    assert rel_fro(f_dW[cand_ref], dWc) < GRAD_RTOL
+    del f_dH
     if exact_cols:
         _, lse_all = orc.forward(x["H"], x["W"], cand_ref, slot_ref, cap=cap, tau=tau)
         cols = np.unique(np.array([0, U_ref - 1, min(U_ref, C - 1), C - 1, C // 2, 1,
@@ -182,16 +202,50 @@ def _check_sampled(orc, x, T, V, D, C, seed, rng_seed, exact_cols, cap=0.0, tau=
         ref_rows = orc.backward_dWc(x["H"], x["W"], cand_ref, slot_ref, lse_all, scale, cols=cols,
                                     cap=cap, tau=tau)
         assert rel_fro(dW[cand_ref[cols]], ref_rows) < GRAD_RTOL
+        assert rel_fro(f_dW[cand_ref[cols]], ref_rows) < GRAD_RTOL
         assert_loss_close(lse, lse_all)
+        assert_loss_close(f_lse, lse_all)
+    return {"lse": lse, "loss": loss, "dW": dW, "f_lse": f_lse, "f_loss": f_loss, "f_dW": f_dW,
+            "cand": cand_ref, "U": U_ref}
+
+
+def _golden_dw(name):
+    """The stored oracle values of a large workload (tests/golden/, written by
+    tests/golden/make_full_size_dw.py from the CPU oracle alone)."""
+    import importlib.util
+    import os
+    path = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden",
+                        "make_full_size_dw.py")
+    spec = importlib.util.spec_from_file_location("_golden_dw", path)
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    return mod.read(name)
 
 
 @pytest.mark.parametrize("wid", [1, 2, 3, 4, 5])
 def test_full_size_workload(orc, wid):
     w = synth.WORKLOADS[wid]
     x = synth.workload_inputs(w)
-    # exact candidate rows where the oracle's full-batch lse is affordable
-    _check_sampled(orc, x, w.T, w.V, w.D, w.C, w.seed, 100 + wid,
-                   exact_cols=w.T * w.C <= 16384 * 10240)
+    # exact candidate rows computed here where the oracle's full-batch lse is
+    # affordable; for the three large workloads, stored oracle rows instead
+    small = w.T * w.C <= 16384 * 10240
+    got = _check_sampled(orc, x, w.T, w.V, w.D, w.C, w.seed, 100 + wid, exact_cols=small)
+    if small:
+        return
+    g = _golden_dw(w.name)
+    meta = g["meta"]
+    assert int(meta["T"][0]) == w.T and int(meta["C"][0]) == w.C and int(meta["seed"][0]) == w.seed
+    assert int(meta["U"][0]) == got["U"]
+    cols = g["cols"]
+    np.testing.assert_array_equal(got["cand"][cols], [int(c) for c in meta["cand_of_columns"]])
+    # candidate rows of dW (both entry points) against the oracle's, and the
+    # mean loss and lse over every token
+    for dW in (got["dW"], got["f_dW"]):
+        assert rel_fro(dW[got["cand"][cols]], g["rows"]) < GRAD_RTOL
+    for loss, lse in ((got["loss"], got["lse"]), (got["f_loss"], got["f_lse"])):
+        ml, ms = float(np.mean(loss.astype(np.float64))), float(np.mean(lse.astype(np.float64)))
+        assert abs(ml - float(meta["mean_loss"][0])) <= 1e-4 * abs(float(meta["mean_loss"][0]))
+        assert abs(ms - float(meta["mean_lse"][0])) <= 1e-4 * abs(float(meta["mean_lse"][0]))
 
 
 def test_operands_beyond_l2_ragged(orc):
@@ -279,8 +333,9 @@ def test_empty_batch():
     assert np.all(d[np.setdiff1d(np.arange(V), c)] == 3.0)
 
 
-def test_fused_step_equals_separate_calls(orc):
-    # ss_step runs the same kernels on the same data: bit-identical results
+def test_fused_step_against_oracle_and_separate_calls(orc):
+    # ss_step (stored probabilities) and the three calls (recompute) on the
+    # same batch: identical candidates, both within tolerance of the oracle
     T, V, D, C, seed = 700, 6000, 768, 1500, 21
     x, C = _case(T, V, D, C, seed)
     H, W, tg = to_dev_bf16(x["H"]), to_dev_bf16(x["W"]), _dev(x["targets"])
@@ -289,30 +344,82 @@ def test_fused_step_equals_separate_calls(orc):
     a = {k: v.clone() for k, v in a.items()}
     b = ss.step_separate(H, W, tg, C, seed, ws, scale=0.5)
     torch.cuda.synchronize()
-    for k in ("cand", "slot", "loss", "lse", "dH", "dW"):
+    for k in ("cand", "slot"):
         assert torch.equal(a[k], b[k]), k
     ref = _full_oracle(orc, x, C, seed, 0.5)
-    assert_loss_close(a["loss"].cpu().numpy(), ref["loss"])
-    assert rel_fro(a["dW"].cpu().numpy(), ref["dW"]) < GRAD_RTOL
+    for r in (a, b):
+        assert_loss_close(r["loss"].cpu().numpy(), ref["loss"])
+        assert_loss_close(r["lse"].cpu().numpy(), ref["lse"])
+        assert rel_fro(r["dH"].float().cpu().numpy(), ref["dH"]) < GRAD_RTOL
+        assert rel_fro(r["dW"].cpu().numpy(), ref["dW"]) < GRAD_RTOL
 
 
-def test_step_merge_beside_softmax_grad(orc):
-    # ss_step with the plain head runs the LSE merge on two blocks per SM,
-    # several passes of its grid-stride loop at this T, while the
-    # softmax-gradient GEMM's mainloop starts beside it; the separate calls
-    # run the wide merge and wait in full
-    T, V, D, C, seed = 20000, 3000, 64, 2000, 22
+def test_step_is_deterministic():
+    T, V, D, C, seed = 900, 5000, 256, 2100, 23
     x, C = _case(T, V, D, C, seed)
     H, W, tg = to_dev_bf16(x["H"]), to_dev_bf16(x["W"]), _dev(x["targets"])
     ws = ss.workspace(T, V, C, D)
-    a = ss.step(H, W, tg, C, seed, ws, scale=1.0 / T)
-    a = {k: v.clone() for k, v in a.items()}
-    b = ss.step_separate(H, W, tg, C, seed, ws, scale=1.0 / T)
+    a = {k: v.clone() for k, v in ss.step(H, W, tg, C, seed, ws, scale=0.5).items()}
+    b = ss.step(H, W, tg, C, seed, ws, scale=0.5)
     torch.cuda.synchronize()
-    assert ss.read_status(ws)[0] == 0
     for k in ("cand", "slot", "loss", "lse", "dH", "dW"):
         assert torch.equal(a[k], b[k]), k
+
+
+def _stored_fallback_case(T, V, D, C, seed, far):
+    """Inputs on which the first logit tile of every row lies far below the
+    row's largest logits: H = 6 u + noise, W rows of the ids in the first tile
+    (the smallest targets, all below V / 4) = -far/6 u, every other row
+    = +far/6 u plus noise, u a unit vector. Then lse - r is about 2 far."""
+    x = synth.make_inputs(T, V, D, 1.1, seed)
+    rng = np.random.default_rng(seed + 1)
+    u = rng.standard_normal(D)
+    u /= np.linalg.norm(u)
+    H = 6.0 * u[None, :] + 0.3 * rng.standard_normal((T, D))
+    Wf = 0.02 * rng.standard_normal((V, D))
+    Wf[: V // 4] -= (far / 6.0) * u
+    Wf[V // 4:] += (far / 6.0) * u
+    x["H"] = synth.f32_to_bf16_bits(H.astype(np.float32))
+    x["W"] = synth.f32_to_bf16_bits(Wf.astype(np.float32))
+    x["targets"] = np.minimum(x["targets"], V // 4 - 1).astype(np.int32)
+    return x
+
+
+@pytest.mark.parametrize("far", [5.0, 25.0, 40.0, 200.0])
+def test_step_stored_reference_far_below(orc, far):
+    """The per-row reference r (largest logit of the first tile) far below the
+    row's lse: at 2 far = 10, 50 the stored probabilities stay in bf16's
+    range (alpha = exp(r - lse) down to e^-50); at 80 and 400 the merge raises
+    the fallback flag (at 400 exp(S - r) overflows) and the backward
+    recomputes the logits. Every case matches the oracle."""
+    T, V, D, C, seed = 300, 4000, 256, 1700, 31
+    x = _stored_fallback_case(T, V, D, C, seed, far)
+    C = max(C, len(np.unique(x["targets"])))
     ref = _full_oracle(orc, x, C, seed, 1.0 / T)
+    got = run_gpu_step(ss, x, C, seed, 1.0 / T)
+    assert got["status"] == 0
+    np.testing.assert_array_equal(got["cand"], ref["cand"])
+    # the first tile lies below the others: the case does what it says
+    assert np.all(ref["cand"][:256] < V // 4) and ref["U"] <= 256
+    assert_loss_close(got["loss"], ref["loss"])
+    assert_loss_close(got["lse"], ref["lse"])
+    assert rel_fro(got["dH"], ref["dH"]) < GRAD_RTOL
+    assert rel_fro(got["dW"], ref["dW"]) < GRAD_RTOL
+
+
+def test_step_single_target_weight_half_merge_beside_softmax_grad(orc):
+    # one target with weight 1/2 (ss_step_mtp) keeps the recompute, with the
+    # LSE merge on two blocks per SM (several passes of its grid-stride loop
+    # at this T) while the softmax-gradient GEMM's mainloop starts beside it
+    T, V, D, C, seed = 20000, 3000, 64, 2000, 22
+    x, C = _case(T, V, D, C, seed)
+    H, W = to_dev_bf16(x["H"]), to_dev_bf16(x["W"])
+    tg = _dev(x["targets"][None, :].copy())
+    ws = ss.workspace(T, V, C, D)
+    a = ss.step_mtp(H, W, tg, [0.5], C, seed, ws, scale=1.0 / T)
+    torch.cuda.synchronize()
+    assert ss.read_status(ws)[0] == 0
+    ref = orc.loss_and_grads_mtp(x["H"], x["W"], x["targets"][None, :], [0.5], C, seed, 1.0 / T)
     assert_loss_close(a["loss"].cpu().numpy(), ref["loss"])
     assert rel_fro(a["dH"].float().cpu().numpy(), ref["dH"]) < GRAD_RTOL
     assert rel_fro(a["dW"].cpu().numpy(), ref["dW"]) < GRAD_RTOL
@@ -332,9 +439,11 @@ def test_kernel_trace_records_every_launch():
     with ss.KernelTrace(capacity=16) as tr:
         ss.step(H, W, _dev(x["targets"]), C, 4, ws)
     torch.cuda.synchronize()
-    # one gather shared by the forward and the backward
+    # one gather shared by the forward and the backward; the recompute is
+    # launched (as the fallback) but finds its gate shut
     assert [n for n, _ in tr.timings()] == ["build_candidates", "gather_rows", "gemm_forward_lse",
-                                           "lse_merge", "gemm_softmax_grad", "gemm_grads"]
+                                           "lse_merge", "stored_fallback", "gemm_softmax_grad",
+                                           "gemm_grads"]
     assert all(ms > 0 for _, ms in tr.timings())
 
 
