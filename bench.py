@@ -65,6 +65,9 @@ def parse_args():
     # default: the full-vocabulary phase (T=65536, C=V=50304), the largest of
     # the five workloads, which the schedule runs for its final steps
     ap.add_argument("--workload", type=int, default=5, choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--tokens", type=int, default=None,
+                    help="run the workload with this many tokens instead (same seed and "
+                         "distributions; for small profiling captures)")
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
@@ -299,6 +302,9 @@ def run_native(args, world, rank, local):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     w = synth.WORKLOADS[args.workload]
+    if args.tokens is not None:
+        import dataclasses
+        w = dataclasses.replace(w, T=args.tokens, name=f"{w.name}_T{args.tokens}")
     T, V, C, D = w.T, w.V, w.C, w.D
     x = synth.workload_inputs(w)
     H = torch.from_numpy(x["H"].view(np.int16)).to(dev).view(torch.bfloat16)
@@ -592,6 +598,9 @@ def run_reference(args, world, rank):
     import oracle
     oracle.build()
     w = synth.WORKLOADS[args.workload]
+    if args.tokens is not None:
+        import dataclasses
+        w = dataclasses.replace(w, T=args.tokens, name=f"{w.name}_T{args.tokens}")
     x = synth.workload_inputs(w)
     K = args.steps if args.steps is not None else 3
     W_ = max(args.warmup, 0)

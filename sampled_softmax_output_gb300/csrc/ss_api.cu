@@ -480,7 +480,8 @@ __global__ void __launch_bounds__(256) k_lse_merge(const float2* __restrict__ pa
 // its precision when P is close to 1. A row whose lse exceeds r by more than
 // kStoredSpan (or is not finite) raises *fallback: alpha and Pt' would then
 // leave the range where bf16 holds them to full precision, and the backward
-// recomputes G from the logits instead (k_stored_fallback, gated GEMM).
+// recomputes G from the logits instead (the gated softmax-gradient GEMM,
+// which then also resets Hs to H and the row factors to `scale`).
 constexpr float kStoredSpan = 60.f;
 
 __global__ void __launch_bounds__(256) k_lse_merge_p(
@@ -554,26 +555,6 @@ __global__ void __launch_bounds__(256) k_lse_merge_p(
       }
     }
   }
-}
-
-// ss_step's fallback when k_lse_merge_p raised *fallback: G = P - Y is then
-// recomputed from the logits (the gated softmax-gradient GEMM), so dH's
-// per-row factor becomes plain `scale` and Hs a copy of H. Does nothing when
-// the flag is clear (the usual case).
-__global__ void __launch_bounds__(256) k_stored_fallback(const int* fallback,
-                                                         const uint16_t* __restrict__ H,
-                                                         int64_t n16, int T, float scale,
-                                                         uint16_t* __restrict__ Hs,
-                                                         float* __restrict__ rowfac,
-                                                         int* status) {
-  pdl_enter();
-  if (read_status(status) != 0 || read_status(fallback) == 0) return;
-  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-  const int64_t i0 = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  const uint4* src = reinterpret_cast<const uint4*>(H);
-  uint4* dst = reinterpret_cast<uint4*>(Hs);
-  for (int64_t i = i0; i < n16; i += stride) dst[i] = __ldg(src + i);
-  for (int64_t i = i0; i < T; i += stride) rowfac[i] = scale;
 }
 
 // dW[cand[j], :] = 0 (the gradient of an empty batch).
@@ -925,8 +906,9 @@ ss_status enqueue_backward(const uint16_t* H, const int32_t* cand, const int32_t
 // ss_step with the plain bf16 head and one target: the forward keeps the
 // probabilities exp(S - r) (EpiFwdP) and the gradient GEMMs read them, so
 // the logits are computed once per step. The merge patches the target column
-// and writes the per-row factors; the softmax-gradient GEMM (the recompute)
-// runs only if the merge raised the fallback flag. The regions: Pt in G's
+// and writes the per-row factors; the softmax-gradient GEMM (the recompute,
+// G = P - Y) runs only if the merge raised the fallback flag, and then also
+// sets Hs = H and the row factors to `scale`. The regions: Pt in G's
 // place, r and the dH row factors after the target logits, Hs = alpha H in
 // the place of the FP8 head's rounded H.
 ss_status enqueue_step_stored(const uint16_t* H, const int32_t* cand, const int32_t* slot,
@@ -955,8 +937,8 @@ ss_status enqueue_step_stored(const uint16_t* H, const int32_t* cand, const int3
                   make_map(&tHsMn, Hs, D, T, D * 2, 64, 64);
   if (!ok) return fail("cuTensorMapEncodeTiled", cudaErrorInvalidValue);
   trace_pre(s, "gemm_forward_lse");
-  cudaError_t e = launch_forward_stored(tH, tWc, tPk, iT, iC, iD, slot, part, tgt, ref, fallback,
-                                        status, nsm, s);
+  cudaError_t e = launch_forward_stored(tH, tWc, tWc2, tPk, iT, iC, iD, slot, part, tgt, ref,
+                                        fallback, status, nsm, s);
   trace_post(s);
   if (e != cudaSuccess) return fail("launch gemm_forward_lse", e);
   trace_pre(s, "lse_merge");
@@ -965,14 +947,9 @@ ss_status enqueue_step_stored(const uint16_t* H, const int32_t* cand, const int3
                  P, static_cast<int64_t>(L.ldG), Hs, rowfac, fallback, loss, lse, status);
   trace_post(s);
   if (e != cudaSuccess) return fail("launch k_lse_merge_p", e);
-  trace_pre(s, "stored_fallback");
-  e = launch_pdl(k_stored_fallback, dim3(2 * nsm), dim3(256), 0, s,
-                 static_cast<const int*>(fallback), H, T * D / 8, iT, scale, Hs, rowfac, status);
-  trace_post(s);
-  if (e != cudaSuccess) return fail("launch k_stored_fallback", e);
   trace_pre(s, "gemm_softmax_grad");
-  e = launch_softmax_grad_gated(tH, tWc, tWc2, tPk, iT, iC, iD, slot, lse, 1.f, fallback, status,
-                                nsm, s);
+  e = launch_softmax_grad_gated(tH, tWc, tWc2, tPk, iT, iC, iD, slot, lse, fallback, H, Hs, rowfac,
+                                scale, status, nsm, s);
   trace_post(s);
   if (e != cudaSuccess) return fail("launch gemm_softmax_grad", e);
   trace_pre(s, "gemm_grads");

@@ -83,7 +83,27 @@ struct GemmShape {
   // non-null: the kernel does its work only if *gate != 0, read once the
   // kernels before it have completed (no late_wait); else every CTA returns
   int* gate;
+  // > 0: the units walk groups of group_m row tiles column tile by column
+  // tile (the B tile of a column is reused by the group's rows while it is in
+  // L2, and the group's A rows stay in L2 across the columns); 0: row by row
+  int group_m;
 };
+
+// Unit u -> (row tile, column tile) of a GemmShape (column tiles
+// [n_begin, n_tiles)), in the order group_m asks for.
+__device__ __forceinline__ void unit_tile(const GemmShape& shp, int u, int& mt, int& nt) {
+  const int n_cols = shp.n_tiles - shp.n_begin;
+  if (shp.group_m <= 0) {
+    mt = u / n_cols;
+    nt = shp.n_begin + u % n_cols;
+    return;
+  }
+  const int per = shp.group_m * n_cols;
+  const int g = u / per, w = u % per;
+  const int gm = min(shp.group_m, shp.m_tiles - g * shp.group_m);
+  mt = g * shp.group_m + w % gm;
+  nt = shp.n_begin + w / gm;
+}
 
 // ----------------------------------------------------------------- epilogues
 
@@ -306,6 +326,14 @@ struct EpiGT {
                        // (one target: W = w[0], 1 for the single-target loss); log2_scale is
                        // log2(|scale| W)
     const float* amax;  // used when F8: logits = accumulator * e4m3_logit_scale(amax)
+    // non-null: the stored-probability step's fallback also resets, for each
+    // row t (in its first column tile), fix_Hs[t, :] = fix_H[t, :] and
+    // fix_rowfac[t] = fix_scale (D columns, bf16)
+    const uint16_t* fix_H;
+    uint16_t* fix_Hs;
+    float* fix_rowfac;
+    float fix_scale;
+    int D;
   };
   __device__ static void begin(const Params& p, EpiState& es) {
     if constexpr (F8) es.f0 = e4m3_logit_scale(p.amax);
@@ -331,6 +359,12 @@ struct EpiGT {
       sl[k] = (valid && k < K) ? __ldg(p.slot + static_cast<size_t>(k) * p.T + t) : -1;
       if (valid && k < K && nt == 0 && static_cast<unsigned>(sl[k]) >= static_cast<unsigned>(p.C))
         set_status(p.status, SS_ERR_INDEX);
+    }
+    if (p.fix_H != nullptr && nt == 0 && cg == 0 && valid) {
+      const uint4* src = reinterpret_cast<const uint4*>(p.fix_H + static_cast<size_t>(t) * p.D);
+      uint4* dst = reinterpret_cast<uint4*>(p.fix_Hs + static_cast<size_t>(t) * p.D);
+      for (int i = 0; i < p.D / 8; ++i) dst[i] = __ldg(src + i);
+      p.fix_rowfac[t] = p.fix_scale;
     }
     const float asc = fabsf(p.scale);
     float sig = 1.f;
@@ -430,17 +464,23 @@ using EpiG = EpiGT<false>;
 // row's largest logit over the first logit tile. PRE: this launch covers that
 // tile only, finds r[t] itself (every thread of a row reads the row's whole
 // tile from TMEM, so both column groups find the same value) and stores it;
-// otherwise r[t] is read back. exp(S - r) is the partial's own exponential
-// exp(S - m), m the running max, times exp(m - r): one multiply per logit.
-// Once lse is known,
+// otherwise r[t] is read back. Once lse is known,
 //   G[t,j] = scale (P - Y) = scale exp(r - lse) (Pt - Y exp(lse - r)),
 // so the backward needs no second pass over the logits (the merge patches
-// the target column and supplies the per-row factor). The staging and the
-// TMA stores are those of EpiGT; two column groups, two partials per row per
-// tile, as in part[(nt * 2 + cg) * T + t].
-template <bool PRE>
+// the target column and supplies the per-row factor).
+// The partial's reference is r as well: per logit one FMA and one exp give
+// both Pt and the partial's term. Only if a 32-column chunk's sum could
+// overflow (a logit some 59 above r) does that thread move the partial to a
+// running max, as EpiFwdT keeps it; Pt is then out of range, which the merge
+// detects (lse - r too large) and answers with the recompute.
+// The staging and the TMA stores are those of EpiGT; two column groups, two
+// partials per row per tile, part[(nt * 2 + cg) * T + t].
+template <bool PRE, int NBUF = 1>
 struct EpiFwdP {
-  static constexpr int kStageBytes = 2 * 16384;
+  // NBUF 16 KB staging buffers per column group: with two, a group fills one
+  // while the store of the other is still reading it
+  static_assert(NBUF == 1 || NBUF == 2, "staging buffers per column group");
+  static constexpr int kStageBytes = 2 * NBUF * 16384;
   // Pt streams through L2 once; the H and W_c tiles are re-read by every CTA
   static constexpr bool kKeepOperands = true;
   struct Params {
@@ -464,6 +504,7 @@ struct EpiFwdP {
   __device__ static void apply(const Params& p, int mt, int nt, int row, uint32_t taddr,
                                EpiState& es, int cg) {
     static_assert(NCG == 2 && BN == 256, "two column groups of two 64-column quarters");
+    constexpr int CPG = BN / 32 / NCG;  // 32-column chunks per group
     const int bar = 1 + 2 * cg;
     const bool leader = (es.ep_tid & 127) == 0;
     const int t = mt * BM + row;
@@ -476,93 +517,115 @@ struct EpiFwdP {
     float r;
     if constexpr (PRE) {  // the largest logit of the row over this (first) tile
       r = -INFINITY;
-#pragma unroll 1
-      for (int c = 0; c < BN / 32; ++c) {
-        if (c * 32 >= ncols) break;  // uniform
-        uint32_t v[32];
-        tmem_ld32(taddr + c * 32, v);
-        tmem_ld_wait();
-        const int nv = min(32, ncols - c * 32);
+      for_tmem_chunks<BN / 32>(taddr, 0, [&](const uint32_t(&v)[32], int i) {
+        const int nv = min(32, ncols - i * 32);
+        if (nv <= 0) return;
+        if (nv == 32) {
 #pragma unroll
-        for (int k = 0; k < 32; ++k)
-          if (k < nv) r = fmaxf(r, __uint_as_float(v[k]));
-      }
+          for (int k = 0; k < 32; ++k) r = fmaxf(r, __uint_as_float(v[k]));
+        } else {
+#pragma unroll
+          for (int k = 0; k < 32; ++k)
+            if (k < nv) r = fmaxf(r, __uint_as_float(v[k]));
+        }
+      });
       if (valid && cg == 0) p.ref[t] = r;
     } else {
       r = valid ? __ldcg(p.ref + t) : 0.f;
     }
     const float r2 = r * kLog2e;
     const uint32_t r7 = static_cast<uint32_t>(row & 7);
-    float m = -INFINITY, s = 0.f, tg = 0.f;
+    const uint32_t gbuf = es.stage + static_cast<uint32_t>(cg) * (16384u * NBUF);
+    // partial (m, s): sum of exp(S - m) over this group's columns, m = r
+    // unless a chunk moved it up
+    float m = cg * CPG * 32 < ncols ? r : -INFINITY, s = 0.f, tg = 0.f;
     bool has_t = false;
-#pragma unroll 1
-    for (int q = 2 * cg; q < 2 * cg + 2; ++q) {
-      const int qc = q * 64;
-      if (qc >= ncols) break;  // uniform: depends on the tile only
-      const uint32_t buf = es.stage + static_cast<uint32_t>(cg) * 16384u;
-      // the store that last used this group's buffer must have read it
-      if (es.rounds >= 1 && leader) bulk_wait_read<0>();
-      named_bar_sync(bar, 128);
+    for_tmem_chunks<CPG>(taddr, cg * CPG, [&](const uint32_t(&v)[32], int i) {
+      const int jc = (cg * CPG + i) * 32;  // column of the tile
+      if (jc >= ncols) return;             // uniform: depends on the tile only
+      const int h = i & 1;                 // half of the 64-column quarter
+      const uint32_t buf = gbuf + (es.rounds % NBUF) * 16384u;
       const uint32_t rowbase = buf + static_cast<uint32_t>(row) * 128u;
+      if (h == 0) {
+        // the store that last used this buffer must have read it
+        if (es.rounds >= NBUF && leader) bulk_wait_read<NBUF - 1>();
+        named_bar_sync(bar, 128);
+      }
+      const int nv = min(32, ncols - jc);
+      float e[32];
+      float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+      if (nv == 32) {  // every chunk but a ragged tail: no per-column predicates
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int jc = qc + 32 * h;
-        if (jc >= ncols) break;
-        uint32_t v[32];
-        tmem_ld32(taddr + jc, v);
-        tmem_ld_wait();
-        const int nv = min(32, ncols - jc);
+        for (int k = 0; k < 32; k += 4) {
+          e[k + 0] = ex2_approx(fmaf(__uint_as_float(v[k + 0]), kLog2e, -r2));
+          e[k + 1] = ex2_approx(fmaf(__uint_as_float(v[k + 1]), kLog2e, -r2));
+          e[k + 2] = ex2_approx(fmaf(__uint_as_float(v[k + 2]), kLog2e, -r2));
+          e[k + 3] = ex2_approx(fmaf(__uint_as_float(v[k + 3]), kLog2e, -r2));
+          a0 += e[k + 0];
+          a1 += e[k + 1];
+          a2 += e[k + 2];
+          a3 += e[k + 3];
+        }
+      } else {
+#pragma unroll
+        for (int k = 0; k < 32; k += 4) {
+          e[k + 0] = k + 0 < nv ? ex2_approx(fmaf(__uint_as_float(v[k + 0]), kLog2e, -r2)) : 0.f;
+          e[k + 1] = k + 1 < nv ? ex2_approx(fmaf(__uint_as_float(v[k + 1]), kLog2e, -r2)) : 0.f;
+          e[k + 2] = k + 2 < nv ? ex2_approx(fmaf(__uint_as_float(v[k + 2]), kLog2e, -r2)) : 0.f;
+          e[k + 3] = k + 3 < nv ? ex2_approx(fmaf(__uint_as_float(v[k + 3]), kLog2e, -r2)) : 0.f;
+          a0 += e[k + 0];
+          a1 += e[k + 1];
+          a2 += e[k + 2];
+          a3 += e[k + 3];
+        }
+      }
+      const float a = (a0 + a1) + (a2 + a3);
+      if (a <= 0x1p86f && m == r) {
+        s += a;
+      } else {  // rare: the partial takes a running max (robust lse for the fallback)
         float cm = -INFINITY;
 #pragma unroll
         for (int k = 0; k < 32; ++k)
           if (nv == 32 || k < nv) cm = fmaxf(cm, __uint_as_float(v[k]));
         const float nm = fmaxf(m, cm);
         const float nm2 = nm * kLog2e;
-        const float f = ex2_approx(nm2 - r2);  // exp(m - r)
-        float e[32];
-        float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+        float b = 0.f;
 #pragma unroll
-        for (int k = 0; k < 32; k += 4) {
-          e[k + 0] = (nv == 32 || k + 0 < nv) ? ex2_approx(fmaf(__uint_as_float(v[k + 0]), kLog2e, -nm2)) : 0.f;
-          e[k + 1] = (nv == 32 || k + 1 < nv) ? ex2_approx(fmaf(__uint_as_float(v[k + 1]), kLog2e, -nm2)) : 0.f;
-          e[k + 2] = (nv == 32 || k + 2 < nv) ? ex2_approx(fmaf(__uint_as_float(v[k + 2]), kLog2e, -nm2)) : 0.f;
-          e[k + 3] = (nv == 32 || k + 3 < nv) ? ex2_approx(fmaf(__uint_as_float(v[k + 3]), kLog2e, -nm2)) : 0.f;
-          a0 += e[k + 0];
-          a1 += e[k + 1];
-          a2 += e[k + 2];
-          a3 += e[k + 3];
-        }
-        s = s * ex2_approx((m - nm) * kLog2e) + ((a0 + a1) + (a2 + a3));
+        for (int k = 0; k < 32; ++k)
+          if (nv == 32 || k < nv) b += ex2_approx(fmaf(__uint_as_float(v[k]), kLog2e, -nm2));
+        s = s * ex2_approx((m - nm) * kLog2e) + b;
         m = nm;
-        uint32_t pk[16];
+      }
+      uint32_t pk[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(e[2 * i] * f, e[2 * i + 1] * f);
+      for (int k = 0; k < 16; ++k) pk[k] = pack_bf16x2(e[2 * k], e[2 * k + 1]);
 #pragma unroll
-        for (int w = 0; w < 4; ++w) {
-          const uint32_t ci = static_cast<uint32_t>(h * 4 + w);
-          st_shared_v4(rowbase + ((ci ^ r7) << 4), pk[4 * w], pk[4 * w + 1], pk[4 * w + 2],
-                       pk[4 * w + 3]);
-        }
-        // the target logit: a target falls in a given 32-column chunk for a
-        // few rows of a warp at most
-        const int off = sl - j0 - jc;
-        const bool hit = static_cast<unsigned>(off) < static_cast<unsigned>(nv);
-        if (__any_sync(0xffffffffu, hit)) {
-          const float x = __uint_as_float(select32(v, off));
-          if (hit) {
-            tg = x;
-            has_t = true;
-          }
+      for (int w = 0; w < 4; ++w) {
+        const uint32_t ci = static_cast<uint32_t>(h * 4 + w);
+        st_shared_v4(rowbase + ((ci ^ r7) << 4), pk[4 * w], pk[4 * w + 1], pk[4 * w + 2],
+                     pk[4 * w + 3]);
+      }
+      // the target logit: a target falls in a given 32-column chunk for a
+      // few rows of a warp at most
+      const int off = sl - j0 - jc;
+      const bool hit = static_cast<unsigned>(off) < static_cast<unsigned>(nv);
+      if (__any_sync(0xffffffffu, hit)) {
+        const float x = __uint_as_float(select32(v, off));
+        if (hit) {
+          tg = x;
+          has_t = true;
         }
       }
-      fence_proxy_async_smem();
-      named_bar_sync(bar, 128);
-      if (leader) {
-        tma_store_2d_hint(&p.tmP, buf, j0 + qc, mt * BM, l2_evict_first());
-        bulk_commit();
+      if (h == 1 || jc + 32 >= ncols) {  // the quarter is complete: store it
+        fence_proxy_async_smem();
+        named_bar_sync(bar, 128);
+        if (leader) {
+          tma_store_2d_hint(&p.tmP, buf, j0 + jc - 32 * h, mt * BM, l2_evict_first());
+          bulk_commit();
+        }
+        ++es.rounds;
       }
-      ++es.rounds;
-    }
+    });
     if (valid) {
       p.part[static_cast<size_t>(nt * 2 + cg) * p.T + t] = make_float2(m, s);
       if (has_t) p.tgt[t] = tg;
@@ -889,7 +952,8 @@ __global__ void __launch_bounds__(64 + 32 * EPI_WARPS, 1)
       uint32_t ph = 0, issued = 0, issued_ph = 0;
       bool ok = true;
       for (int u = blockIdx.x; ok && u < num_units; u += gridDim.x) {
-        const int mt = u / n_cols, nt = shp.n_begin + u % n_cols;
+        int mt, nt;
+        unit_tile(shp, u, mt, nt);
         for (int kb = 0; kb < shp.k_blocks; ++kb) {
           if (!mbar_wait(&ctrl->empty[s], ph ^ 1u, abort_flag, status)) {
             ok = false;
@@ -1006,7 +1070,8 @@ __global__ void __launch_bounds__(64 + 32 * EPI_WARPS, 1)
       }
       if (!go) break;
       tc_fence_after();
-      const int mt = u / n_cols, nt = shp.n_begin + u % n_cols;
+      int mt, nt;
+      unit_tile(shp, u, mt, nt);
       Epi::template apply<BN, NCG>(ep, mt, nt, row, lane_addr + static_cast<uint32_t>(b * BN), es,
                                    cg);
       tc_fence_before();

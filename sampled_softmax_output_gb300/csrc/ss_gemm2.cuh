@@ -44,7 +44,8 @@ template <int BN, int STAGES, bool A_MN, bool B_MN, class Epi, int EPI_WARPS>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * EPI_WARPS, 1)
     k_gemm2(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
             GemmShape shp, const __grid_constant__ typename Epi::Params ep, int* status) {
-  pdl_enter();
+  if (shp.late_wait) pdl_launch_dependents();
+  else pdl_enter();
   static_assert(BN % 128 == 0 && BN >= 128 && BN <= 256, "BN");
   static_assert(STAGES >= 2 && STAGES <= 8, "STAGES");
   static_assert(EPI_WARPS == 4 || EPI_WARPS == 8, "EPI_WARPS");
@@ -96,7 +97,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * EPI_WARPS,
   tc_fence_after();
   const uint32_t tmem_base = ctrl->tmem_base;
   volatile int* abort_flag = &ctrl->abort_flag;
-  const int num_units = shp.m_tiles * shp.n_tiles;
+  const int num_units = shp.m_tiles * (shp.n_tiles - shp.n_begin);
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -105,7 +106,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * EPI_WARPS,
       uint32_t ph = 0, issued = 0, issued_ph = 0;
       bool ok = true;
       for (int u = pair; ok && u < num_units; u += npairs) {
-        const int mt = u / shp.n_tiles, nt = u % shp.n_tiles;
+        int mt, nt;
+        unit_tile(shp, u, mt, nt);
         const int m0 = mt * 2 * BM + static_cast<int>(rank) * BM;   // this CTA's A rows
         const int n0 = nt * BN + static_cast<int>(rank) * (BN / 2);  // this CTA's half of B
         for (int kb = 0; kb < shp.k_blocks; ++kb) {
@@ -206,6 +208,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * EPI_WARPS,
     const int row = q * 32 + lane;
     const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
     EpiState es{tiles + L::EPI_OFFSET, static_cast<int>(threadIdx.x) - 64, 0u, 0.f};
+    if (shp.late_wait) pdl_wait();
     Epi::begin(ep, es);
     int b = 0;
     uint32_t aph = 0;
@@ -223,7 +226,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * EPI_WARPS,
       }
       if (!go) break;
       tc_fence_after();
-      const int mt = u / shp.n_tiles, nt = u % shp.n_tiles;
+      int mt, nt;
+      unit_tile(shp, u, mt, nt);
       Epi::template apply<BN, NCG>(ep, mt * 2 + static_cast<int>(rank), nt, row,
                                    lane_addr + static_cast<uint32_t>(b * BN), es, cg);
       tc_fence_before();
@@ -255,9 +259,9 @@ cudaError_t launch_gemm2(const CUtensorMap& tA, const CUtensorMap& tB, GemmShape
                          cudaStream_t stream) {
   auto kern = k_gemm2<BN, STAGES, A_MN, B_MN, Epi, EPI_WARPS>;
   constexpr int smem = Gemm2Smem<BN, STAGES, Epi::kStageBytes>::TOTAL;
-  const int units = shp.m_tiles * shp.n_tiles;
+  const int units = shp.m_tiles * (shp.n_tiles - shp.n_begin);
   if (units <= 0) return cudaSuccess;
-  if (shp.n_begin != 0) return cudaErrorInvalidValue;  // whole column range only
+  if (shp.gate != nullptr && shp.late_wait) return cudaErrorInvalidValue;  // the gate needs the wait
   const int pairs = units < num_sms / 2 ? units : num_sms / 2;
   return launch_pdl(kern, dim3(2 * pairs), dim3(64 + 32 * EPI_WARPS), smem, stream, tA, tB, shp, ep,
                     status);

@@ -57,34 +57,67 @@ cudaError_t launch_softmax_grad(const CUtensorMap& tH, const CUtensorMap& tWc,
                                             late_wait);
 }
 
+// The stored-probability forward: on CTA pairs once H and W_c exceed L2
+// (each SM stages its 128 rows of H and half of every W_c tile, a third less
+// operand traffic from L2 than one CTA per 128 x 256 tile), single CTAs
+// below (measured on GB300: pairs 10.20 ms against 10.45 ms per step at
+// T65536_C50304, single CTAs 0.543 ms against 0.556 ms at T16384_C10240).
+// Units walk groups of row tiles column by column (kFwdGroupRows rows per
+// group), so W_c is read from DRAM once per group rather than once per row
+// tile while the Pt stream passes through L2 (10.20 ms against 10.58 ms
+// row by row, on pairs at T65536_C50304).
+constexpr int kFwdGroupRows = 8192;
+// ring stages and staging buffers per column group: CTA pairs, single CTAs
+constexpr int kFwdPairStages = 5, kFwdPairBufs = 2;
+constexpr int kFwdStages = 4, kFwdBufs = 1;
+
 // The first logit tile of every row block finds r and clears *clear_word;
 // the launch over the other tiles starts its mainloop at once (H and W_c are
 // older than the first launch) and its epilogue waits for r.
 cudaError_t launch_forward_stored(const CUtensorMap& tH, const CUtensorMap& tWc,
-                                  const CUtensorMap& tP, int T, int C, int D, const int32_t* slot,
-                                  float2* part, float* tgt, float* ref, int* clear_word,
-                                  int* status, int num_sms, cudaStream_t stream) {
-  const int m_tiles = (T + BM - 1) / BM, n_tiles = (C + kBnLogits - 1) / kBnLogits;
-  EpiFwdP<true>::Params pre{tP, T, C, slot, part, tgt, ref, clear_word, status};
+                                  const CUtensorMap& tWc_half, const CUtensorMap& tP, int T, int C,
+                                  int D, const int32_t* slot, float2* part, float* tgt,
+                                  float* ref, int* clear_word, int* status, int num_sms,
+                                  cudaStream_t stream) {
+  const int n_tiles = (C + kBnLogits - 1) / kBnLogits;
+  if (operands_exceed_l2(T, C, D)) {
+    using Pre = EpiFwdP<true, kFwdPairBufs>;
+    using Rest = EpiFwdP<false, kFwdPairBufs>;
+    typename Pre::Params pre{tP, T, C, slot, part, tgt, ref, clear_word, status};
+    typename Rest::Params rest{tP, T, C, slot, part, tgt, ref, nullptr, status};
+    const int m_tiles = (T + 2 * BM - 1) / (2 * BM);
+    GemmShape first{m_tiles, 1, D / BK};
+    cudaError_t e = launch_gemm2<kBnLogits, kFwdPairStages, false, false, Pre, 8>(
+        tH, tWc_half, first, pre, status, num_sms, stream);
+    if (e != cudaSuccess || n_tiles == 1) return e;
+    GemmShape others{m_tiles, n_tiles, D / BK, 1, 1, nullptr, kFwdGroupRows / (2 * BM)};
+    return launch_gemm2<kBnLogits, kFwdPairStages, false, false, Rest, 8>(
+        tH, tWc_half, others, rest, status, num_sms, stream);
+  }
+  using Pre = EpiFwdP<true, kFwdBufs>;
+  using Rest = EpiFwdP<false, kFwdBufs>;
+  typename Pre::Params pre{tP, T, C, slot, part, tgt, ref, clear_word, status};
+  typename Rest::Params rest{tP, T, C, slot, part, tgt, ref, nullptr, status};
+  const int m_tiles = (T + BM - 1) / BM;
   GemmShape first{m_tiles, 1, D / BK};
-  cudaError_t e = launch_gemm<kBnLogits, kStagesLogits, false, false, EpiFwdP<true>, 8>(
+  cudaError_t e = launch_gemm<kBnLogits, kFwdStages, false, false, Pre, 8>(
       tH, tWc, first, pre, status, num_sms, stream);
   if (e != cudaSuccess || n_tiles == 1) return e;
-  EpiFwdP<false>::Params rest{tP, T, C, slot, part, tgt, ref, nullptr, status};
-  GemmShape others{m_tiles, n_tiles, D / BK, 1, 1};
-  return launch_gemm<kBnLogits, kStagesLogits, false, false, EpiFwdP<false>, 8>(
-      tH, tWc, others, rest, status, num_sms, stream);
+  GemmShape others{m_tiles, n_tiles, D / BK, 1, 1, nullptr, kFwdGroupRows / BM};
+  return launch_gemm<kBnLogits, kFwdStages, false, false, Rest, 8>(tH, tWc, others, rest, status,
+                                                                    num_sms, stream);
 }
 
 cudaError_t launch_softmax_grad_gated(const CUtensorMap& tH, const CUtensorMap& tWc,
                                       const CUtensorMap& tWc_half, const CUtensorMap& tG_store,
                                       int T, int C, int D, const int32_t* slot, const float* lse,
-                                      float scale, int* gate, int* status, int num_sms,
+                                      int* gate, const uint16_t* H, uint16_t* Hs, float* rowfac,
+                                      float scale, int* status, int num_sms,
                                       cudaStream_t stream) {
   const Targets one = {1, {1.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f}};
-  return softmax_grad<false, 1>(tH, tWc, tWc_half, tG_store, T, C, D, slot, lse, scale,
+  return softmax_grad<false, 1>(tH, tWc, tWc_half, tG_store, T, C, D, slot, lse, 1.f,
                                 head_cap(0.f, 1.f), one, nullptr, status, num_sms, stream, false,
-                                gate);
+                                gate, H, Hs, rowfac, scale);
 }
 
 // FP8 gradients: G8 and G8^T in e5m2 from the e4m3 logits (one target)

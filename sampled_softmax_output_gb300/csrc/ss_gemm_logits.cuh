@@ -41,8 +41,15 @@ cudaError_t softmax_grad(const CUtensorMap& tH, const CUtensorMap& tWc,
                          const CUtensorMap& tWc_half, const CUtensorMap& tG_store, int T, int C,
                          int D, const int32_t* slot, const float* lse, float scale,
                          const HeadCap& head, const Targets& tg, const float* amax, int* status,
-                         int num_sms, cudaStream_t stream, bool late_wait, int* gate = nullptr) {
+                         int num_sms, cudaStream_t stream, bool late_wait, int* gate = nullptr,
+                         const uint16_t* fix_H = nullptr, uint16_t* fix_Hs = nullptr,
+                         float* fix_rowfac = nullptr, float fix_scale = 0.f) {
   typename EpiGT<CAP, KMAX, F8>::Params ep;
+  ep.fix_H = fix_H;
+  ep.fix_Hs = fix_Hs;
+  ep.fix_rowfac = fix_rowfac;
+  ep.fix_scale = fix_scale;
+  ep.D = D;
   ep.tmG = tG_store;
   ep.T = T;
   ep.C = C;

@@ -118,14 +118,18 @@ cudaError_t launch_softmax_grad_fp8(const CUtensorMap& tH8, const CUtensorMap& t
 // the first logit tile of every row block (which finds r and clears
 // *clear_word), then the others.
 cudaError_t launch_forward_stored(const CUtensorMap& tH, const CUtensorMap& tWc,
-                                  const CUtensorMap& tP, int T, int C, int D, const int32_t* slot,
-                                  float2* part, float* tgt, float* ref, int* clear_word,
-                                  int* status, int num_sms, cudaStream_t stream);
-// launch_softmax_grad (plain bf16 head, one target) that runs only if *gate != 0
+                                  const CUtensorMap& tWc_half, const CUtensorMap& tP, int T, int C,
+                                  int D, const int32_t* slot, float2* part, float* tgt,
+                                  float* ref, int* clear_word, int* status, int num_sms,
+                                  cudaStream_t stream);
+// The stored-probability step's fallback: launch_softmax_grad (plain bf16
+// head, one target, G = P - Y with scale 1) that runs only if *gate != 0, and
+// then also sets Hs = H and rowfac[t] = scale for every row.
 cudaError_t launch_softmax_grad_gated(const CUtensorMap& tH, const CUtensorMap& tWc,
                                       const CUtensorMap& tWc_half, const CUtensorMap& tG_store,
                                       int T, int C, int D, const int32_t* slot, const float* lse,
-                                      float scale, int* gate, int* status, int num_sms,
+                                      int* gate, const uint16_t* H, uint16_t* Hs, float* rowfac,
+                                      float scale, int* status, int num_sms,
                                       cudaStream_t stream);
 // the same GEMMs for K > 1 targets per token (ss_gemm_logits_mtp.cu)
 cudaError_t launch_forward_logits_mtp(const CUtensorMap& tH, const CUtensorMap& tWc, int T, int C,
