@@ -37,6 +37,18 @@ constexpr size_t kHdrBar = 72;      // uint32 bar[2] of k_h_prep_beside (arrival
 constexpr size_t kHdrQuant = 80;    // ss_quantize_e4m3's own float amax + int32 status
 constexpr size_t kHdrFallback = 96;  // int32: ss_step's stored-probability backward falls back
 
+// The grid barrier of k_h_prep_beside waits for as many arrivals as its grid
+// has blocks, for up to 4 s. A test builds a copy of the library with one
+// more arrival than blocks and a 1 ms limit, so that the wait runs out (the
+// timeout path, with no fault and nothing else in flight); the library
+// itself is built with the defaults.
+#ifndef SS_BESIDE_EXTRA_ARRIVALS
+#define SS_BESIDE_EXTRA_ARRIVALS 0
+#endif
+#ifndef SS_BESIDE_WAIT_NS
+#define SS_BESIDE_WAIT_NS 4000000000ull
+#endif
+
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 Layout make_layout(int64_t T, int64_t C, int64_t D) {
@@ -350,13 +362,15 @@ __global__ void __launch_bounds__(256) k_quantize_e4m3_t(QuantTJob a, QuantTJob 
 //   among it) is complete, and the build writes nothing this kernel reads.
 // - The grid barrier can be waited on: the kernel after this one is launched
 //   only once every block of this grid has started, so all of them are
-//   resident together (the build holds 8 SMs). bar[0] counts arrivals; a
-//   block that gives up (kWaitLimitNs) sets bar[1], which the W_c quantizer
-//   reports as SS_ERR_TIMEOUT. bar[0..1] and *amax are zero at launch.
+//   resident together (the build holds 8 SMs). bar[0] counts arrivals up to
+//   `arrivals` (the grid size); a block that has waited `wait_ns` (4 s) gives
+//   up and sets bar[1], which the W_c quantizer reports as SS_ERR_TIMEOUT.
+//   bar[0..1] and *amax are zero at launch.
 // - It waits for the build before it exits, so that the kernels after it,
 //   which wait for it, find the build's results. No status check: the build
 //   clears the status word while this kernel may run.
 __global__ void __launch_bounds__(256) k_h_prep_beside(int64_t n8, float* amax, uint32_t* bar,
+                                                       uint32_t arrivals, uint64_t wait_ns,
                                                        QuantJob jr, QuantTJob jt, int mode) {
   pdl_launch_dependents();
   __shared__ __align__(16) uint8_t tile[64 * kQtPitch];
@@ -368,8 +382,8 @@ __global__ void __launch_bounds__(256) k_h_prep_beside(int64_t n8, float* amax, 
     atomicAdd(bar, 1u);
     const uint64_t t0 = globaltimer_ns();
     int go = 1;
-    while (ld_acquire_gpu(bar) < gridDim.x) {
-      if (globaltimer_ns() - t0 > kWaitLimitNs) {
+    while (ld_acquire_gpu(bar) < arrivals) {
+      if (globaltimer_ns() - t0 > wait_ns) {
         atomicExch(bar + 1, 1u);
         go = 0;
         break;
@@ -1162,9 +1176,12 @@ static ss_status step_impl(const int32_t* targets, const uint16_t* H, const uint
   if (T == 0) return accumulate ? SS_OK : enqueue_zero_rows(cand, C, V, D, dW, status, nsm, s);
   if (h_beside) {
     trace_pre(s, "prepare_h");
+    const int grid = 4 * nsm;
     const cudaError_t e = launch_pdl(
-        k_h_prep_beside, dim3(4 * nsm), dim3(256), 0, s, T * D / 8, amax,
-        reinterpret_cast<uint32_t*>(ws + L.hdr + kHdrBar), h_rows_job(H, T, D, L, ws, false),
+        k_h_prep_beside, dim3(grid), dim3(256), 0, s, T * D / 8, amax,
+        reinterpret_cast<uint32_t*>(ws + L.hdr + kHdrBar),
+        static_cast<uint32_t>(grid + SS_BESIDE_EXTRA_ARRIVALS),
+        static_cast<uint64_t>(SS_BESIDE_WAIT_NS), h_rows_job(H, T, D, L, ws, false),
         h_tiles_job(H, T, D, L, ws, false), fp8);
     trace_post(s);
     if (e != cudaSuccess) return fail("launch k_h_prep_beside", e);

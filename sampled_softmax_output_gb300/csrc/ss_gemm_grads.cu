@@ -24,6 +24,7 @@ cudaError_t launch_grad_h(const CUtensorMap& tG_kmaj, const CUtensorMap& tWc_mn,
                           int D, uint16_t* dH, int* status, int num_sms, cudaStream_t stream,
                           const float* rowfac) {
   GemmShape shp{(T + 2 * BM - 1) / (2 * BM), (D + kBnGrad - 1) / kBnGrad, (C + BK - 1) / BK};
+  shp.a_stream = 1;  // G
   EpiDh::Params ep{T, D, dH, 0.f, nullptr, 0, rowfac};
   return launch_gemm2<kBnGrad, 6, false, true, EpiDh, 8>(tG_kmaj, tWc_mn, shp, ep, status, num_sms,
                                                          stream);
@@ -33,6 +34,7 @@ cudaError_t launch_grad_w(const CUtensorMap& tG_mn, const CUtensorMap& tH_mn, in
                           int V, int accumulate, const int32_t* cand, float* dW, int* status,
                           int num_sms, cudaStream_t stream, const float* out_scale) {
   GemmShape shp{(C + 2 * BM - 1) / (2 * BM), (D + kBnGrad - 1) / kBnGrad, (T + BK - 1) / BK};
+  shp.a_stream = 1;  // G
   EpiDw::Params ep{C, D, V, accumulate, cand, dW, status, out_scale ? *out_scale : 1.f, nullptr,
                    0, out_scale ? 1 : 0};
   return launch_gemm2<kBnGrad, 6, true, true, EpiDw, 8>(tG_mn, tH_mn, shp, ep, status, num_sms,
@@ -169,15 +171,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * kGradEpiWa
           if constexpr (F8G) {  // one 128 x 128-byte box of A and of B, K-major
             const CUtensorMap* ma = is_dw ? &tmAw : &tmAh;
             const CUtensorMap* mb = is_dw ? &tmBw : &tmBh;
-            tma_load_2d_pair(a_dst, ma, fb, kb * KB, m0);
+            tma_load_2d_pair_hint(a_dst, ma, fb, kb * KB, m0, l2_evict_first());
             tma_load_2d_pair_hint(b_dst, mb, fb, kb * KB, n0, keep);
           } else if (is_dw) {  // A = G columns (MN-major), B = H (MN-major); K = tokens
-            tma_load_2d_pair(a_dst, &tmAw, fb, m0, kb * BK);
-            tma_load_2d_pair(a_dst + 8192, &tmAw, fb, m0 + 64, kb * BK);
+            const uint64_t first = l2_evict_first();  // G streams through
+            tma_load_2d_pair_hint(a_dst, &tmAw, fb, m0, kb * BK, first);
+            tma_load_2d_pair_hint(a_dst + 8192, &tmAw, fb, m0 + 64, kb * BK, first);
             tma_load_2d_pair_hint(b_dst, &tmBw, fb, n0, kb * BK, keep);
             tma_load_2d_pair_hint(b_dst + 8192, &tmBw, fb, n0 + 64, kb * BK, keep);
           } else {      // A = G rows (K-major), B = W_c (MN-major); K = candidates
-            tma_load_2d_pair(a_dst, &tmAh, fb, kb * BK, m0);
+            tma_load_2d_pair_hint(a_dst, &tmAh, fb, kb * BK, m0, l2_evict_first());
             tma_load_2d_pair_hint(b_dst, &tmBh, fb, n0, kb * BK, keep);
             tma_load_2d_pair_hint(b_dst + 8192, &tmBh, fb, n0 + 64, kb * BK, keep);
           }
