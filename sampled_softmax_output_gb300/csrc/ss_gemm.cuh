@@ -87,9 +87,6 @@ struct GemmShape {
   // tile (the B tile of a column is reused by the group's rows while it is in
   // L2, and the group's A rows stay in L2 across the columns); 0: row by row
   int group_m;
-  // k_gemm2 only: 1 if A streams through (each element read by one tile row
-  // at a time): its loads carry the evict-first hint
-  int a_stream;
 };
 
 // Unit u -> (row tile, column tile) of a GemmShape (column tiles

@@ -120,16 +120,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * EPI_WARPS,
           const uint32_t fb = rank == 0 ? fb_local : mapa_shared(fb_local, 0);
           const uint32_t a_dst = tiles + s * L::STAGE_BYTES;
           const uint32_t b_dst = a_dst + L::A_BYTES;
-          if (shp.a_stream) {
-            const uint64_t first = l2_evict_first();
-            if (A_MN) {
-#pragma unroll
-              for (int i = 0; i < BM / 64; ++i)
-                tma_load_2d_pair_hint(a_dst + i * 8192, &tmA, fb, m0 + 64 * i, kb * BK, first);
-            } else {
-              tma_load_2d_pair_hint(a_dst, &tmA, fb, kb * BK, m0, first);
-            }
-          } else if (A_MN) {
+          if (A_MN) {
 #pragma unroll
             for (int i = 0; i < BM / 64; ++i)
               tma_load_2d_pair(a_dst + i * 8192, &tmA, fb, m0 + 64 * i, kb * BK);

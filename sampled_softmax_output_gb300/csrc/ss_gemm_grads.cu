@@ -24,7 +24,6 @@ cudaError_t launch_grad_h(const CUtensorMap& tG_kmaj, const CUtensorMap& tWc_mn,
                           int D, uint16_t* dH, int* status, int num_sms, cudaStream_t stream,
                           const float* rowfac) {
   GemmShape shp{(T + 2 * BM - 1) / (2 * BM), (D + kBnGrad - 1) / kBnGrad, (C + BK - 1) / BK};
-  shp.a_stream = 1;  // G
   EpiDh::Params ep{T, D, dH, 0.f, nullptr, 0, rowfac};
   return launch_gemm2<kBnGrad, 6, false, true, EpiDh, 8>(tG_kmaj, tWc_mn, shp, ep, status, num_sms,
                                                          stream);
@@ -34,7 +33,6 @@ cudaError_t launch_grad_w(const CUtensorMap& tG_mn, const CUtensorMap& tH_mn, in
                           int V, int accumulate, const int32_t* cand, float* dW, int* status,
                           int num_sms, cudaStream_t stream, const float* out_scale) {
   GemmShape shp{(C + 2 * BM - 1) / (2 * BM), (D + kBnGrad - 1) / kBnGrad, (T + BK - 1) / BK};
-  shp.a_stream = 1;  // G
   EpiDw::Params ep{C, D, V, accumulate, cand, dW, status, out_scale ? *out_scale : 1.f, nullptr,
                    0, out_scale ? 1 : 0};
   return launch_gemm2<kBnGrad, 6, true, true, EpiDw, 8>(tG_mn, tH_mn, shp, ep, status, num_sms,
