@@ -76,7 +76,12 @@ struct GemmShape {
   // 1: the operands are older than the kernel just before this one in the
   // stream, and only the epilogue reads what that kernel writes. The producer
   // and MMA warps then start at once; the epilogue waits before its first
-  // tile. (k_gemm only; the CTA-pair kernel always waits first.)
+  // tile.
+  // 2 (k_gemm2): nothing this kernel reads or writes is touched by the kernel
+  // just before it, whose own wait covers everything older: no part waits
+  // before the work, and the kernel's CTAs take SMs as that kernel's last
+  // tiles free them; each CTA waits for it before exiting, so that the kernels
+  // after this one, which wait for this one, also find that one finished.
   int late_wait;
   // k_gemm only: the units cover the column tiles [n_begin, n_tiles) (0: all)
   int n_begin;

@@ -208,7 +208,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * EPI_WARPS,
     const int row = q * 32 + lane;
     const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
     EpiState es{tiles + L::EPI_OFFSET, static_cast<int>(threadIdx.x) - 64, 0u, 0.f};
-    if (shp.late_wait) pdl_wait();
+    if (shp.late_wait == 1) pdl_wait();
     Epi::begin(ep, es);
     int b = 0;
     uint32_t aph = 0;
@@ -243,6 +243,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * EPI_WARPS,
       }
     }
     Epi::finish(ep, es);
+    if (shp.late_wait == 2) pdl_wait();  // the kernel before this one has finished
   }
   __syncthreads();
   cluster_sync_all();  // the leader's MMAs are drained before either CTA frees TMEM

@@ -20,6 +20,9 @@
 namespace ss {
 
 
+// the dW launch of the two-launch path does not wait for the dH launch
+constexpr bool kDwNoWait = true;
+
 cudaError_t launch_grad_h(const CUtensorMap& tG_kmaj, const CUtensorMap& tWc_mn, int T, int C,
                           int D, uint16_t* dH, int* status, int num_sms, cudaStream_t stream,
                           const float* rowfac) {
@@ -32,7 +35,11 @@ cudaError_t launch_grad_h(const CUtensorMap& tG_kmaj, const CUtensorMap& tWc_mn,
 cudaError_t launch_grad_w(const CUtensorMap& tG_mn, const CUtensorMap& tH_mn, int T, int C, int D,
                           int V, int accumulate, const int32_t* cand, float* dW, int* status,
                           int num_sms, cudaStream_t stream, const float* out_scale) {
-  GemmShape shp{(C + 2 * BM - 1) / (2 * BM), (D + kBnGrad - 1) / kBnGrad, (T + BK - 1) / BK};
+  // launched right after the dH GEMM, which it neither reads nor writes: it
+  // need not wait for it (every kernel before dH has finished once dH's CTAs
+  // have started), so its CTAs fill the SMs of dH's ragged last round
+  GemmShape shp{(C + 2 * BM - 1) / (2 * BM), (D + kBnGrad - 1) / kBnGrad, (T + BK - 1) / BK,
+                kDwNoWait ? 2 : 0};
   EpiDw::Params ep{C, D, V, accumulate, cand, dW, status, out_scale ? *out_scale : 1.f, nullptr,
                    0, out_scale ? 1 : 0};
   return launch_gemm2<kBnGrad, 6, true, true, EpiDw, 8>(tG_mn, tH_mn, shp, ep, status, num_sms,
