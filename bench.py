@@ -442,7 +442,8 @@ def run_native(args, world, rank, local):
     per = {}
     for name, ms in trace.timings():
         per.setdefault(name, []).append(ms)
-    launches_per_step = trace.count / Kt
+    # kernels the library launched per step (a traced stage may hold several)
+    launches_per_step = sum(trace.kernels) / Kt
     launches = int(round(launches_per_step * K))
     kern = {n: {"launches": len(v), "avg_ms": sum(v) / len(v), "total_ms": sum(v)}
             for n, v in per.items()}

@@ -373,21 +373,26 @@ const char* ss_status_string(ss_status status);
 const char* ss_last_error(void);
 
 /*
- * Diagnostics: per-kernel timing with CUDA events, for benchmarks.
+ * Diagnostics: per-stage timing with CUDA events, for benchmarks.
  * Between ss_trace_begin and ss_trace_end, on the calling host thread, every
- * kernel that libss launches is bracketed by cudaEventRecord(events[2k]) and
+ * stage of the path that libss launches (one kernel, or a few kernels that
+ * make one stage: the forward's first-tile and other-tile launches, the dH
+ * and dW launches beyond L2) is bracketed by cudaEventRecord(events[2k]) and
  * cudaEventRecord(events[2k + 1]) on the launch stream, for k = 0, 1, ...
- * while k < capacity; later launches are counted but not recorded.
+ * while k < capacity; later stages are counted but not recorded.
  *   events   : host array of 2 * capacity cudaEvent_t created by the caller.
- * ss_trace_end returns the number of launches since ss_trace_begin, or -1 if
+ * ss_trace_end returns the number of stages since ss_trace_begin, or -1 if
  * an event record failed (e.g. an invalid event handle; the launches
  * themselves are unaffected); ss_trace_kernel_name(k) is the static name of
- * launch k (k < capacity and k < that count), or NULL. Tracing adds only the
- * event records.
+ * stage k (k < capacity and k < that count), or NULL;
+ * ss_trace_kernel_launches(k) is the number of kernels stage k launched (0
+ * for a stage with nothing to do), or -1. Tracing adds only the event
+ * records.
  */
 ss_status ss_trace_begin(void** events, int capacity);
 int ss_trace_end(void);
 const char* ss_trace_kernel_name(int k);
+int ss_trace_kernel_launches(int k);
 
 #ifdef __cplusplus
 }

@@ -97,6 +97,8 @@ def _load():
     L.ss_trace_end.argtypes = []
     L.ss_trace_kernel_name.restype = ctypes.c_char_p
     L.ss_trace_kernel_name.argtypes = [ctypes.c_int]
+    L.ss_trace_kernel_launches.restype = ctypes.c_int
+    L.ss_trace_kernel_launches.argtypes = [ctypes.c_int]
     hp = ctypes.POINTER(Head)
     L.ss_forward_head.restype = ctypes.c_int
     L.ss_forward_head.argtypes = [p, p, p, p, i64, i64, i64, i64, hp, p, p, p, sz, p]
@@ -332,7 +334,9 @@ def read_status(ws: torch.Tensor) -> tuple[int, int]:
 
 
 class KernelTrace:
-    """Per-kernel CUDA-event timing of libss launches on this host thread.
+    """Per-stage CUDA-event timing of libss launches on this host thread (a
+    stage is one kernel or the few kernels of one step of the path; .kernels
+    gives the kernel launches of each recorded stage).
 
         with ss.KernelTrace(capacity=64) as tr:
             ...calls...
@@ -362,6 +366,8 @@ class KernelTrace:
             raise RuntimeError("ss_trace: a CUDA event record failed")
         self.names = [(_lib.ss_trace_kernel_name(k) or b"?").decode()
                       for k in range(min(self.count, self.capacity))]
+        self.kernels = [int(_lib.ss_trace_kernel_launches(k))
+                        for k in range(min(self.count, self.capacity))]
         return False
 
     def timings(self) -> list[tuple[str, float]]:

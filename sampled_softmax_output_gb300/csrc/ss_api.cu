@@ -21,6 +21,10 @@
 #include "ss_ptx.cuh"
 
 namespace ss {
+
+// Kernels launched by this host thread (launch_pdl counts them).
+thread_local int g_kernel_launches = 0;
+
 namespace {
 
 // ------------------------------------------------------------ workspace
@@ -615,7 +619,9 @@ struct Trace {
   cudaEvent_t* events = nullptr;
   int capacity = 0;
   int count = 0;
-  std::vector<const char*> names;  // one per recorded launch (host memory)
+  std::vector<const char*> names;  // one per recorded entry (host memory)
+  std::vector<int> kernels;        // kernel launches inside each recorded entry
+  int at_pre = 0;                  // g_kernel_launches when the open entry began
 };
 thread_local Trace g_trace;
 
@@ -630,14 +636,18 @@ void trace_pre(cudaStream_t s, const char* name) {
     }
     t.names.push_back(name);
   }
+  t.at_pre = g_kernel_launches;
 }
 
 void trace_post(cudaStream_t s) {
   Trace& t = g_trace;
   if (!t.on) return;
-  if (t.count < t.capacity && cudaEventRecord(t.events[2 * t.count + 1], s) != cudaSuccess) {
-    (void)cudaGetLastError();
-    t.failed = true;
+  if (t.count < t.capacity) {
+    if (cudaEventRecord(t.events[2 * t.count + 1], s) != cudaSuccess) {
+      (void)cudaGetLastError();
+      t.failed = true;
+    }
+    t.kernels.push_back(g_kernel_launches - t.at_pre);
   }
   ++t.count;
 }
@@ -1498,6 +1508,7 @@ ss_status ss_trace_begin(void** events, int capacity) {
   t.count = 0;
   t.failed = false;
   t.names.clear();
+  t.kernels.clear();
   return SS_OK;
 }
 
@@ -1511,6 +1522,12 @@ const char* ss_trace_kernel_name(int k) {
   const Trace& t = g_trace;
   if (k < 0 || k >= t.count || k >= static_cast<int>(t.names.size())) return nullptr;
   return t.names[k];
+}
+
+int ss_trace_kernel_launches(int k) {
+  const Trace& t = g_trace;
+  if (k < 0 || k >= t.count || k >= static_cast<int>(t.kernels.size())) return -1;
+  return t.kernels[k];
 }
 
 }  // extern "C"

@@ -20,8 +20,12 @@ cudaError_t prepare_kernel(void (*kern)(KArgs...), int dyn_smem_bytes) {
   return prepare_kernel(reinterpret_cast<const void*>(kern), dyn_smem_bytes);
 }
 
+// Kernels launched by this host thread so far (for the launch trace).
+extern thread_local int g_kernel_launches;
+
 // Launch with programmatic stream serialization: the kernel may be scheduled
 // while its predecessor in the stream drains, and waits for it in pdl_enter().
+// Every kernel of the library is launched here.
 template <typename... KArgs, typename... Args>
 cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
                        cudaStream_t stream, Args&&... args) {
@@ -37,7 +41,9 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+  const cudaError_t le = cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+  if (le == cudaSuccess) ++g_kernel_launches;
+  return le;
 }
 
 // Tile widths of the GEMMs (output columns per tile).

@@ -18,6 +18,7 @@ def test_exports_every_declared_symbol():
     assert set(names) == {"ss_workspace_size", "ss_build_candidates", "ss_forward",
                           "ss_backward", "ss_read_status", "ss_status_string",
                           "ss_trace_begin", "ss_trace_end", "ss_trace_kernel_name",
+                          "ss_trace_kernel_launches",
                           "ss_last_error", "ss_forward_noalloc", "ss_step",
                           "ss_schedule_candidates", "ss_clear_rows", "ss_step_graph_create",
                           "ss_step_graph_create_mtp",

@@ -436,6 +436,7 @@ def test_kernel_trace_records_every_launch():
     names = [n for n, _ in tr.timings()]
     assert names == ["build_candidates", "gather_rows", "gemm_forward_lse", "lse_merge",
                      "gather_rows", "gemm_softmax_grad", "gemm_grads"]
+    assert tr.kernels == [1] * 7
     with ss.KernelTrace(capacity=16) as tr:
         ss.step(H, W, _dev(x["targets"]), C, 4, ws)
     torch.cuda.synchronize()
@@ -443,6 +444,8 @@ def test_kernel_trace_records_every_launch():
     # launched (as the fallback) but finds its gate shut
     assert [n for n, _ in tr.timings()] == ["build_candidates", "gather_rows", "gemm_forward_lse",
                                            "lse_merge", "gemm_softmax_grad", "gemm_grads"]
+    # the forward is two launches (first logit tile, the other tiles)
+    assert tr.kernels == [1, 1, 2, 1, 1, 1]
     assert all(ms > 0 for _, ms in tr.timings())
 
 
