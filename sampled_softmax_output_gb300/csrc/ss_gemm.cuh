@@ -560,17 +560,23 @@ struct EpiFwdP {
       float e[32];
       float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
       if (nv == 32) {  // every chunk but a ragged tail: no per-column predicates
+        // two logits per FMA and per add (packed fp32 pairs)
+        const uint64_t k2 = f32x2(kLog2e, kLog2e), nr2 = f32x2(-r2, -r2);
+        uint64_t s01 = f32x2(0.f, 0.f), s23 = s01;
 #pragma unroll
         for (int k = 0; k < 32; k += 4) {
-          e[k + 0] = ex2_approx(fmaf(__uint_as_float(v[k + 0]), kLog2e, -r2));
-          e[k + 1] = ex2_approx(fmaf(__uint_as_float(v[k + 1]), kLog2e, -r2));
-          e[k + 2] = ex2_approx(fmaf(__uint_as_float(v[k + 2]), kLog2e, -r2));
-          e[k + 3] = ex2_approx(fmaf(__uint_as_float(v[k + 3]), kLog2e, -r2));
-          a0 += e[k + 0];
-          a1 += e[k + 1];
-          a2 += e[k + 2];
-          a3 += e[k + 3];
+          float y0, y1, y2, y3;
+          f32x2_split(fma_f32x2(f32x2_bits(v[k], v[k + 1]), k2, nr2), y0, y1);
+          f32x2_split(fma_f32x2(f32x2_bits(v[k + 2], v[k + 3]), k2, nr2), y2, y3);
+          e[k + 0] = ex2_approx(y0);
+          e[k + 1] = ex2_approx(y1);
+          e[k + 2] = ex2_approx(y2);
+          e[k + 3] = ex2_approx(y3);
+          s01 = add_f32x2(s01, f32x2(e[k + 0], e[k + 1]));
+          s23 = add_f32x2(s23, f32x2(e[k + 2], e[k + 3]));
         }
+        f32x2_split(s01, a0, a1);
+        f32x2_split(s23, a2, a3);
       } else {
 #pragma unroll
         for (int k = 0; k < 32; k += 4) {
