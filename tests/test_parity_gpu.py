@@ -258,6 +258,35 @@ def test_operands_beyond_l2_ragged(orc):
     _check_sampled(orc, x, T, V, D, C, seed, 7, exact_cols=True)
 
 
+def test_step_accumulate_beyond_l2():
+    """ss_step with accumulate = 1 where H and W_c exceed L2 (the forward on
+    CTA pairs, dH and dW_c as two launches, dW_c not waiting for dH): every
+    candidate row of dW is the previous row plus what the non-accumulating
+    step writes (to an ulp), and every other row is untouched."""
+    T, V, D, C, seed = 20001, 30000, 2048, 12001, 33
+    assert (T + C) * D * 2 > 96 * 2**20
+    x, C = _case(T, V, D, C, seed)
+    H, W, tg = to_dev_bf16(x["H"]), to_dev_bf16(x["W"]), _dev(x["targets"])
+    ws = ss.workspace(T, V, C, D)
+    dW0 = torch.from_numpy(np.random.default_rng(5).standard_normal((V, D)).astype(np.float32)).cuda()
+    plain = ss.step(H, W, tg, C, seed, ws, scale=1.0 / T, dW=torch.zeros_like(dW0))
+    plain = {k: v.clone() for k, v in plain.items()}
+    acc = ss.step(H, W, tg, C, seed, ws, scale=1.0 / T, dW=dW0.clone(), accumulate=True)
+    torch.cuda.synchronize()
+    assert ss.read_status(ws)[0] == 0
+    c = plain["cand"].long()
+    assert torch.equal(acc["cand"], plain["cand"])
+    # (the epilogue may fuse the scale and the add into one FMA: one rounding
+    # instead of two, so allow an ulp of the operands)
+    want = dW0[c] + plain["dW"][c]
+    tol = 2.0 ** -22 * (dW0[c].abs() + plain["dW"][c].abs()) + 1e-30
+    assert torch.all((acc["dW"][c] - want).abs() <= tol)
+    outside = torch.ones(V, dtype=torch.bool, device="cuda")
+    outside[c] = False
+    assert torch.equal(acc["dW"][outside], dW0[outside])
+    assert torch.equal(acc["dH"], plain["dH"]) and torch.equal(acc["loss"], plain["loss"])
+
+
 # ------------------------------------------------------------ error paths
 
 def _dev(a):

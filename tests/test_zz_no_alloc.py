@@ -8,7 +8,8 @@ needs, so ss_forward_noalloc keeps its scratch in a fixed array inside the
 library's device data instead.
 
 These tests call it through the C ABI and check its loss and lse against the
-ordinary ss_forward, within the tolerance the other parity tests use, on calls
+ordinary ss_forward (itself checked here against the CPU oracle), within the
+tolerance the other parity tests use, on calls
 in a row on the shared array: a larger batch first, then a call with a
 candidate id out of range (the gather's bounds check reports SS_ERR_INDEX
 without touching memory outside W), then a smaller valid batch, which must
@@ -30,7 +31,7 @@ import sampled_softmax_output_gb300 as ss  # noqa: E402  (fails loudly if libss.
 pytestmark = pytest.mark.gpu
 
 
-def _batch(T, V, D, C, seed):
+def _batch(T, V, D, C, seed, orc):
     x = synth.make_inputs(T, V, D, 1.1, seed)
     C = max(C, len(np.unique(x["targets"])))
     H, W = to_dev_bf16(x["H"]), to_dev_bf16(x["W"])
@@ -38,6 +39,10 @@ def _batch(T, V, D, C, seed):
     ws = ss.workspace(T, V, C, D)
     cand, slot = ss.build_candidates(targets, V, C, seed, ws)
     ref_loss, ref_lse = ss.forward(H, W, cand, slot, ws)
+    # the ordinary forward itself against the CPU oracle
+    o_loss, o_lse = orc.forward(x["H"], x["W"], cand.cpu().numpy(), slot.cpu().numpy())
+    _close(ref_loss, torch.from_numpy(o_loss))
+    _close(ref_lse, torch.from_numpy(o_lse))
     return H, W, cand, slot, ref_loss, ref_lse
 
 
@@ -56,9 +61,9 @@ def _run(H, W, cand, slot):
     return loss, lse
 
 
-def test_noalloc_forward_matches_forward_calls_in_a_row():
-    big = _batch(1000, 8000, 768, 2000, 5)
-    small = _batch(300, 3000, 768, 517, 4)
+def test_noalloc_forward_matches_forward_calls_in_a_row(orc):
+    big = _batch(1000, 8000, 768, 2000, 5, orc)
+    small = _batch(300, 3000, 768, 517, 4, orc)
     # 1: the larger batch fills more of the shared array
     H, W, cand, slot, ref_loss, ref_lse = big
     loss, lse = _run(H, W, cand, slot)
