@@ -436,6 +436,39 @@ def test_step_stored_reference_far_below(orc, far):
     assert rel_fro(got["dW"], ref["dW"]) < GRAD_RTOL
 
 
+def test_step_fallback_beyond_l2(orc):
+    """The stored-probability step's fallback where H and W_c exceed L2: the
+    gated recompute runs on CTA pairs and resets Hs and the row factors. The
+    first logit tile lies ~400 below the rest (exp(S - r) overflows), so the
+    fallback must run; the step then matches the three calls (which always
+    recompute) over every token and candidate row, and the oracle on sampled
+    token rows."""
+    T, V, D, C, seed = 20001, 30000, 2048, 12001, 35
+    assert (T + C) * D * 2 > 96 * 2**20
+    x = _stored_fallback_case(T, V, D, C, seed, 200.0)
+    C = max(C, len(np.unique(x["targets"])))
+    H, W, tg = to_dev_bf16(x["H"]), to_dev_bf16(x["W"]), _dev(x["targets"])
+    ws = ss.workspace(T, V, C, D)
+    a = {k: v.clone() for k, v in ss.step(H, W, tg, C, seed, ws, scale=1.0 / T).items()}
+    b = ss.step_separate(H, W, tg, C, seed, ws, scale=1.0 / T)
+    torch.cuda.synchronize()
+    assert ss.read_status(ws)[0] == 0
+    cand = a["cand"].cpu().numpy()
+    assert np.all(cand[:256] < V // 4)
+    assert torch.equal(a["cand"], b["cand"]) and torch.equal(a["slot"], b["slot"])
+    assert_loss_close(a["loss"].cpu().numpy(), b["loss"].cpu().numpy())
+    assert_loss_close(a["lse"].cpu().numpy(), b["lse"].cpu().numpy())
+    assert rel_fro(a["dH"].float().cpu().numpy(), b["dH"].float().cpu().numpy()) < GRAD_RTOL
+    c = a["cand"].long()
+    assert rel_fro(a["dW"][c].cpu().numpy(), b["dW"][c].cpu().numpy()) < GRAD_RTOL
+    rows = np.array([0, 1, T // 2, T - 1])
+    slot = a["slot"].cpu().numpy()
+    l_ref, s_ref = orc.forward(x["H"], x["W"], cand, slot, rows=rows)
+    assert_loss_close(a["loss"].cpu().numpy()[rows], l_ref)
+    dH_ref = orc.backward_dH(x["H"], x["W"], cand, slot, s_ref, 1.0 / T, rows=rows)
+    assert rel_fro(a["dH"].float().cpu().numpy()[rows], dH_ref) < GRAD_RTOL
+
+
 def test_step_single_target_weight_half_merge_beside_softmax_grad(orc):
     # one target with weight 1/2 (ss_step_mtp) keeps the recompute, with the
     # LSE merge on two blocks per SM (several passes of its grid-stride loop
