@@ -25,6 +25,8 @@
 
 #include <math.h>
 
+#include <type_traits>
+
 #include "ss_internal.h"
 #include "ss_ptx.cuh"
 
@@ -114,23 +116,43 @@ __device__ __forceinline__ void unit_tile(const GemmShape& shp, int u, int& mt, 
 
 // Runs fn(r, i) over the 32-column chunks [c_begin, c_begin + n) of this
 // thread's TMEM row, with the load of chunk i + 1 in flight while chunk i is
-// processed.
-template <int N, class F>
-__device__ __forceinline__ void for_tmem_chunks(uint32_t taddr, int c_begin, F&& fn) {
+// processed. on_loaded() runs once, as soon as the last chunk is in registers
+// (before fn processes it): an epilogue that owns its accumulator release
+// hands the TMEM buffer back to the MMA warp there.
+template <int N, class F, class G>
+__device__ __forceinline__ void for_tmem_chunks(uint32_t taddr, int c_begin, F&& fn,
+                                                G&& on_loaded) {
   uint32_t ra[32], rb[32];
   tmem_ld32(taddr + c_begin * 32, ra);
 #pragma unroll
   for (int i = 0; i < N; i += 2) {
     tmem_ld_wait(ra);
     if (i + 1 < N) tmem_ld32(taddr + (c_begin + i + 1) * 32, rb);
+    if (i + 1 == N) on_loaded();
     fn(ra, i);
     if (i + 1 < N) {
       tmem_ld_wait(rb);
       if (i + 2 < N) tmem_ld32(taddr + (c_begin + i + 2) * 32, ra);
+      if (i + 2 == N) on_loaded();
       fn(rb, i + 1);
     }
   }
 }
+template <int N, class F>
+__device__ __forceinline__ void for_tmem_chunks(uint32_t taddr, int c_begin, F&& fn) {
+  for_tmem_chunks<N>(taddr, c_begin, static_cast<F&&>(fn), [] {});
+}
+
+// Epilogues with `static constexpr bool kSelfRelease = true` take a release()
+// functor as the last argument of apply() and call it once, after their last
+// TMEM load of the tile and before their global stores: the MMA warp may then
+// start the tile after next in that buffer while the stores are in flight, and
+// the release-ordered mbarrier arrive does not wait for those stores.
+template <class E, class = void>
+struct EpiSelfRelease : std::false_type {};
+template <class E>
+struct EpiSelfRelease<E, std::void_t<decltype(E::kSelfRelease)>>
+    : std::integral_constant<bool, E::kSelfRelease> {};
 
 // x[off & 31]: a five-level select tree on the bits of off (31 selects,
 // where comparing every index with off takes 32 compares and 32 selects)
@@ -488,6 +510,7 @@ struct EpiFwdP {
   static constexpr int kStageBytes = 2 * NBUF * 16384;
   // Pt streams through L2 once; the H and W_c tiles are re-read by every CTA
   static constexpr bool kKeepOperands = true;
+  static constexpr bool kSelfRelease = true;
   struct Params {
     CUtensorMap tmP;  // Pt [T, C] bf16 (row pitch ldG), box 64 x 128, 128-byte swizzle
     int T, C;
@@ -505,9 +528,9 @@ struct EpiFwdP {
   __device__ static void finish(const Params&, EpiState& es) {
     if ((es.ep_tid & 127) == 0) bulk_wait<0>();
   }
-  template <int BN, int NCG>
+  template <int BN, int NCG, class Rel>
   __device__ static void apply(const Params& p, int mt, int nt, int row, uint32_t taddr,
-                               EpiState& es, int cg) {
+                               EpiState& es, int cg, Rel&& release) {
     static_assert(NCG == 2 && BN == 256, "two column groups of two 64-column quarters");
     constexpr int CPG = BN / 32 / NCG;  // 32-column chunks per group
     const int bar = 1 + 2 * cg;
@@ -636,7 +659,7 @@ struct EpiFwdP {
         }
         ++es.rounds;
       }
-    });
+    }, release);
     if (valid) {
       p.part[static_cast<size_t>(nt * 2 + cg) * p.T + t] = make_float2(m, s);
       if (has_t) p.tgt[t] = tg;
@@ -1083,10 +1106,17 @@ __global__ void __launch_bounds__(64 + 32 * EPI_WARPS, 1)
       tc_fence_after();
       int mt, nt;
       unit_tile(shp, u, mt, nt);
-      Epi::template apply<BN, NCG>(ep, mt, nt, row, lane_addr + static_cast<uint32_t>(b * BN), es,
-                                   cg);
-      tc_fence_before();
-      mbar_arrive(&ctrl->tempty[b]);
+      auto release = [&] {
+        tc_fence_before();
+        mbar_arrive(&ctrl->tempty[b]);
+      };
+      const uint32_t acc = lane_addr + static_cast<uint32_t>(b * BN);
+      if constexpr (EpiSelfRelease<Epi>::value) {
+        Epi::template apply<BN, NCG>(ep, mt, nt, row, acc, es, cg, release);
+      } else {
+        Epi::template apply<BN, NCG>(ep, mt, nt, row, acc, es, cg);
+        release();
+      }
       if (++b == 2) {
         b = 0;
         aph ^= 1u;

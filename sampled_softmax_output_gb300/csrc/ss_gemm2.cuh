@@ -228,14 +228,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * EPI_WARPS,
       tc_fence_after();
       int mt, nt;
       unit_tile(shp, u, mt, nt);
-      Epi::template apply<BN, NCG>(ep, mt * 2 + static_cast<int>(rank), nt, row,
-                                   lane_addr + static_cast<uint32_t>(b * BN), es, cg);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) {
-        const uint32_t te = smem_u32(&ctrl->tempty[b]);
-        if (rank == 0) mbar_arrive(&ctrl->tempty[b]);
-        else mbar_arrive_cluster(mapa_shared(te, 0));
+      auto release = [&] {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          const uint32_t te = smem_u32(&ctrl->tempty[b]);
+          if (rank == 0) mbar_arrive(&ctrl->tempty[b]);
+          else mbar_arrive_cluster(mapa_shared(te, 0));
+        }
+      };
+      const int mrow = mt * 2 + static_cast<int>(rank);
+      const uint32_t acc = lane_addr + static_cast<uint32_t>(b * BN);
+      if constexpr (EpiSelfRelease<Epi>::value) {
+        Epi::template apply<BN, NCG>(ep, mrow, nt, row, acc, es, cg, release);
+      } else {
+        Epi::template apply<BN, NCG>(ep, mrow, nt, row, acc, es, cg);
+        release();
       }
       if (++b == 2) {
         b = 0;

@@ -67,8 +67,13 @@ cudaError_t launch_softmax_grad(const CUtensorMap& tH, const CUtensorMap& tWc,
 // tile while the Pt stream passes through L2 (10.20 ms against 10.58 ms
 // row by row, on pairs at T65536_C50304).
 constexpr int kFwdGroupRows = 8192;
-// ring stages and staging buffers per column group: CTA pairs, single CTAs
-constexpr int kFwdPairStages = 5, kFwdPairBufs = 2;
+// ring stages and staging buffers per column group: CTA pairs, single CTAs.
+// The epilogue hands its accumulator back before its stores, so it has slack
+// and one staging buffer per group is enough; the 32 KB this frees buys a
+// sixth ring stage, which the mainloop (waiting on operands ~15% of the time
+// with five) uses better (measured on GB300 at T65536_C50304: time x SM clock
+// per step 1.8% lower than five stages with two buffers).
+constexpr int kFwdPairStages = 6, kFwdPairBufs = 1;
 constexpr int kFwdStages = 4, kFwdBufs = 1;
 
 // The first logit tile of every row block finds r and clears *clear_word;

@@ -436,10 +436,16 @@ __device__ __forceinline__ uint32_t ld_shared_cluster_u32(uint32_t addr) {
   return v;
 }
 
-// Arrive on an mbarrier of another CTA of the cluster (shared::cluster address).
+// Arrive on an mbarrier of another CTA of the cluster (shared::cluster
+// address), with the default CTA-scope release. The library's only remote
+// arrivals hand a TMEM accumulator back to the peer's MMA warp: the TMEM loads
+// have completed (tcgen05.wait::ld, then tcgen05.fence::before_thread_sync)
+// and the peer reads no memory this thread wrote, so no cluster-scope release
+// is needed -- one would make the arrive wait until this thread's earlier
+// global stores (the epilogue's outputs) are visible across the cluster, a
+// full memory round trip per tile.
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
-               : "memory");
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 
 // 2-D tiled load into this CTA's shared memory whose completion is signalled
