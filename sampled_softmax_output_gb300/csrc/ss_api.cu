@@ -502,76 +502,116 @@ __global__ void __launch_bounds__(256) k_lse_merge(const float2* __restrict__ pa
 // which then also resets Hs to H and the row factors to `scale`).
 constexpr float kStoredSpan = 60.f;
 
+// Partials relative to the row's reference r (the forward's usual case) add
+// without exponentials; a partial with another maximum folds as lse_fold.
+__device__ __forceinline__ void lse_fold_same(float& M, float& S, float m, float s) {
+  if (m == M) {
+    S += s;
+    return;
+  }
+  lse_fold(M, S, m, s);
+}
+
+// One block per kMergeTokens consecutive tokens. Warp w folds the partial rows
+// c = w, w + 8, ... (each row's kMergeTokens entries are contiguous: one
+// 256-byte load per warp and row), the eight warps' (max, sum) pairs meet in
+// shared memory, and then the block scales the tokens' H rows (one contiguous
+// block of kMergeTokens * D values) into Hs.
+constexpr int kMergeTokens = 32;
+
 __global__ void __launch_bounds__(256) k_lse_merge_p(
     const float2* __restrict__ part, const float* __restrict__ tgt,
     const int32_t* __restrict__ slot, const float* __restrict__ ref, int T, int C, int n_parts,
     const uint16_t* __restrict__ H, int D, float scale, uint16_t* __restrict__ Pt, int64_t ldP,
     uint16_t* __restrict__ Hs, float* __restrict__ rowfac, int* fallback,
     float* __restrict__ loss, float* __restrict__ lse, int* status) {
+  static_assert(kMergeTokens == 32, "one lane per token");
+  __shared__ float2 red[8][kMergeTokens];
+  __shared__ float s_alpha[kMergeTokens];
+  __shared__ int s_go;
   pdl_enter();
-  if (read_status(status) != 0) return;
-  const int64_t lanes = static_cast<int64_t>(T) * kMergeLanes;
-  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  // one decision per block: its threads meet at barriers below
+  if (threadIdx.x == 0) s_go = read_status(status) == 0;
+  __syncthreads();
+  if (!s_go) return;
+  const int warp = static_cast<int>(threadIdx.x) >> 5, lane = static_cast<int>(threadIdx.x) & 31;
   const int n8 = D / 8;
-  for (int64_t g0 = static_cast<int64_t>(blockIdx.x) * blockDim.x; g0 < lanes; g0 += stride) {
-    const int64_t gid = g0 + threadIdx.x;
-    const int t = static_cast<int>(gid / kMergeLanes);
-    const int k = static_cast<int>(gid % kMergeLanes);
-    const bool valid = gid < lanes;
+  for (int64_t t0 = static_cast<int64_t>(blockIdx.x) * kMergeTokens; t0 < T;
+       t0 += static_cast<int64_t>(gridDim.x) * kMergeTokens) {
+    const int t = static_cast<int>(t0) + lane;
+    const bool valid = t < T;
     float M = -INFINITY, S = 0.f;
     constexpr int kBatch = 8;
     if (valid)
-      for (int c0 = k; c0 < n_parts; c0 += kMergeLanes * kBatch) {
+      for (int c0 = warp; c0 < n_parts; c0 += 8 * kBatch) {
         float2 q[kBatch];
 #pragma unroll
         for (int i = 0; i < kBatch; ++i) {
-          const int c = c0 + i * kMergeLanes;
-          q[i] = c < n_parts ? __ldcg(part + static_cast<size_t>(c) * T + t)
+          const int c = c0 + 8 * i;
+          q[i] = c < n_parts ? __ldcs(part + static_cast<size_t>(c) * T + t)
                              : make_float2(-INFINITY, 0.f);
         }
 #pragma unroll
-        for (int i = 0; i < kBatch; ++i) lse_fold(M, S, q[i].x, q[i].y);
+        for (int i = 0; i < kBatch; ++i) lse_fold_same(M, S, q[i].x, q[i].y);
       }
+    red[warp][lane] = make_float2(M, S);
+    __syncthreads();
+    if (warp == 0) {
 #pragma unroll
-    for (int o = 1; o < kMergeLanes; o <<= 1) {
-      const float m2 = __shfl_xor_sync(0xffffffffu, M, o);
-      const float s2 = __shfl_xor_sync(0xffffffffu, S, o);
-      lse_fold(M, S, m2, s2);
-    }
-    const float l = M + logf(S);
-    const int sl = valid ? __ldg(slot + t) : 0;
-    const bool bad = valid && static_cast<unsigned>(sl) >= static_cast<unsigned>(C);
-    const float r = valid ? __ldcg(ref + t) : 0.f;
-    const float alpha = expf(r - l);
-    if (valid && k == 0) {
-      if (bad) {
-        set_status(status, SS_ERR_INDEX);
-      } else {
-        const float x = __ldcg(tgt + t);
-        lse[t] = l;
-        loss[t] = l - x;
-        rowfac[t] = scale * alpha;
-        if (!(l - r <= kStoredSpan)) {
-          *fallback = 1;
+      for (int w = 1; w < 8; ++w) lse_fold_same(M, S, red[w][lane].x, red[w][lane].y);
+      const float l = M + logf(S);
+      const int sl = valid ? __ldg(slot + t) : 0;
+      const bool bad = valid && static_cast<unsigned>(sl) >= static_cast<unsigned>(C);
+      const float r = valid ? __ldcg(ref + t) : 0.f;
+      const float alpha = expf(r - l);
+      // 0 marks a token whose H row is not scaled (beyond T, or a bad slot)
+      s_alpha[lane] = valid && !bad ? alpha : 0.f;
+      if (valid) {
+        if (bad) {
+          set_status(status, SS_ERR_INDEX);
         } else {
-          Pt[static_cast<int64_t>(t) * ldP + sl] = bf16_bits(expf(x - r) - expf(l - r));
+          const float x = __ldcg(tgt + t);
+          lse[t] = l;
+          loss[t] = l - x;
+          rowfac[t] = scale * alpha;
+          if (!(l - r <= kStoredSpan)) {
+            *fallback = 1;
+          } else {
+            Pt[static_cast<int64_t>(t) * ldP + sl] = bf16_bits(expf(x - r) - expf(l - r));
+          }
         }
       }
     }
-    if (valid && !bad) {
-      const uint4* src = reinterpret_cast<const uint4*>(H + static_cast<int64_t>(t) * D);
-      uint4* dst = reinterpret_cast<uint4*>(Hs + static_cast<int64_t>(t) * D);
-      for (int i = k; i < n8; i += kMergeLanes) {
-        const uint4 v = __ldg(src + i);
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    __syncthreads();
+    // Hs rows of the block's tokens: 16-byte pieces p of the contiguous block
+    const int nt = T - t0 < kMergeTokens ? static_cast<int>(T - t0) : kMergeTokens;
+    const int pieces = nt * n8;
+    const uint4* src = reinterpret_cast<const uint4*>(H + t0 * D);
+    uint4* dst = reinterpret_cast<uint4*>(Hs + t0 * D);
+    constexpr int kHB = 4;
+    for (int p0 = static_cast<int>(threadIdx.x); p0 < pieces; p0 += 256 * kHB) {
+      uint4 v[kHB];
+#pragma unroll
+      for (int i = 0; i < kHB; ++i) {
+        const int p = p0 + 256 * i;
+        if (p < pieces) v[i] = __ldg(src + p);
+      }
+#pragma unroll
+      for (int i = 0; i < kHB; ++i) {
+        const int p = p0 + 256 * i;
+        if (p >= pieces) continue;
+        const float alpha = s_alpha[p / n8];
+        if (alpha == 0.f) continue;
+        const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
         uint32_t o[4];
 #pragma unroll
         for (int j = 0; j < 4; ++j)
           o[j] = pack_bf16x2(__uint_as_float(w[j] << 16) * alpha,
                              __uint_as_float(w[j] & 0xffff0000u) * alpha);
-        dst[i] = make_uint4(o[0], o[1], o[2], o[3]);
+        dst[p] = make_uint4(o[0], o[1], o[2], o[3]);
       }
     }
+    __syncthreads();  // red and s_alpha are reused by the next group of tokens
   }
 }
 
@@ -966,8 +1006,9 @@ ss_status enqueue_step_stored(const uint16_t* H, const int32_t* cand, const int3
   trace_post(s);
   if (e != cudaSuccess) return fail("launch gemm_forward_lse", e);
   trace_pre(s, "lse_merge");
-  e = launch_pdl(k_lse_merge_p, dim3(static_cast<int>((T * kMergeLanes + 255) / 256)), dim3(256),
-                 0, s, part, tgt, slot, ref, iT, iC, static_cast<int>(L.n_ct * 2), H, iD, scale,
+  e = launch_pdl(k_lse_merge_p, dim3(static_cast<int>((T + kMergeTokens - 1) / kMergeTokens)),
+                 dim3(256), 0, s, part, tgt, slot, ref, iT, iC, static_cast<int>(L.n_ct * 2), H, iD,
+                 scale,
                  P, static_cast<int64_t>(L.ldG), Hs, rowfac, fallback, loss, lse, status);
   trace_post(s);
   if (e != cudaSuccess) return fail("launch k_lse_merge_p", e);
