@@ -57,12 +57,12 @@ cudaError_t launch_softmax_grad(const CUtensorMap& tH, const CUtensorMap& tWc,
                                             late_wait);
 }
 
-// The stored-probability forward: on CTA pairs once H and W_c exceed L2
-// (each SM stages its 128 rows of H and half of every W_c tile, a third less
-// operand traffic from L2 than one CTA per 128 x 256 tile), single CTAs
-// below (measured on GB300: pairs 10.20 ms against 10.45 ms per step at
-// T65536_C50304, single CTAs 0.543 ms against 0.556 ms at T16384_C10240).
-// Units walk groups of row tiles column by column (kFwdGroupRows rows per
+// The stored-probability forward: on CTA pairs whenever every pair gets a
+// tile (each SM stages its 128 rows of H and half of every W_c tile, two
+// thirds of the operand intake per flop of one CTA per 128 x 256 tile;
+// measured on GB300: 0.507 against 0.521 ms per step at T16384_C10240, 1.399
+// against 1.447 ms at T32768_C14336, 10.20 against 10.45 ms at T65536_C50304),
+// single CTAs for small batches. Units walk groups of row tiles column by column (kFwdGroupRows rows per
 // group), so W_c is read from DRAM once per group rather than once per row
 // tile while the Pt stream passes through L2 (10.20 ms against 10.58 ms
 // row by row, on pairs at T65536_C50304).
@@ -70,9 +70,8 @@ constexpr int kFwdGroupRows = 8192;
 // ring stages and staging buffers per column group: CTA pairs, single CTAs.
 // The epilogue hands its accumulator back before its stores, so it has slack
 // and one staging buffer per group is enough; the 32 KB this frees buys a
-// sixth ring stage, which the mainloop (waiting on operands ~15% of the time
-// with five) uses better (measured on GB300 at T65536_C50304: time x SM clock
-// per step 1.8% lower than five stages with two buffers).
+// sixth ring stage (measured on GB300 at T65536_C50304: time x SM clock per
+// step 1.8% lower than five stages with two buffers).
 constexpr int kFwdPairStages = 6, kFwdPairBufs = 1;
 constexpr int kFwdStages = 4, kFwdBufs = 1;
 
@@ -85,7 +84,8 @@ cudaError_t launch_forward_stored(const CUtensorMap& tH, const CUtensorMap& tWc,
                                   float* ref, int* clear_word, int* status, int num_sms,
                                   cudaStream_t stream) {
   const int n_tiles = (C + kBnLogits - 1) / kBnLogits;
-  if (operands_exceed_l2(T, C, D)) {
+  const int pair_units = (T + 2 * BM - 1) / (2 * BM) * (n_tiles - 1);
+  if (pair_units >= num_sms / 2) {
     using Pre = EpiFwdP<true, kFwdPairBufs>;
     using Rest = EpiFwdP<false, kFwdPairBufs>;
     typename Pre::Params pre{tP, T, C, slot, part, tgt, ref, clear_word, status};
