@@ -1247,10 +1247,10 @@ static ss_status step_impl(const int32_t* targets, const uint16_t* H, const uint
   // the softmax-gradient GEMM's mainloop beside the LSE merge: measured with
   // the plain bf16 head (one partial per row and logit tile); the heads whose
   // merge folds two per tile keep the wide merge and the full wait, and so do
-  // operands beyond L2, where that GEMM runs on CTA pairs (always a full wait)
-  const bool overlap_merge = fwd_groups(cap, fp8 != 0, tg.K) == 1 &&
-                             !operands_exceed_l2(static_cast<int>(T), static_cast<int>(C),
-                                                 static_cast<int>(D));
+  // the batches where that GEMM runs on CTA pairs (always a full wait)
+  const bool overlap_merge =
+      fwd_groups(cap, fp8 != 0, tg.K) == 1 &&
+      !softmax_grad_on_pairs(static_cast<int>(T), static_cast<int>(C), nsm);
   r = enqueue_forward(H, slot, T, C, D, cap, tau, tg, fp8, loss, lse, L, ws, nsm, s,
                       overlap_merge);
   if (r != SS_OK) return r;

@@ -340,6 +340,7 @@ struct EpiGT {
   static constexpr int kStageBytes = (F8 ? 4 : 2) * 16384;
   // G streams through L2 once; the H and W_c tiles are re-read by every CTA
   static constexpr bool kKeepOperands = true;
+  static constexpr bool kSelfRelease = true;
   struct Params {
     CUtensorMap tmG;  // G [T, C] bf16 (row pitch ldG), box 64 x 128, 128-byte swizzle
     int T, C;
@@ -371,9 +372,9 @@ struct EpiGT {
   // Column group cg of NCG (four warps each) covers quarters
   // [cg * 4 / NCG, (cg + 1) * 4 / NCG) of the tile with its own staging
   // buffer(s), named barrier (1 + 2 * cg) and storing thread.
-  template <int BN, int NCG>
+  template <int BN, int NCG, class Rel>
   __device__ static void apply(const Params& p, int mt, int nt, int row, uint32_t taddr,
-                               EpiState& es, int cg) {
+                               EpiState& es, int cg, Rel&& release) {
     static_assert(NCG == 1 || NCG == 2, "column groups");
     const int bar = 1 + 2 * cg;
     const bool leader = (es.ep_tid & 127) == 0;
@@ -404,8 +405,14 @@ struct EpiGT {
     const int j0 = nt * BN;
     const int ncols = min(BN, p.C - j0);
     const uint32_t r7 = static_cast<uint32_t>(row & 7);
+    // the last 32-column chunk this group loads from TMEM: the accumulator is
+    // handed back right after it (a group with no columns hands it back now)
+    const int q_begin = cg * (BN / 64) / NCG, q_end = (cg + 1) * (BN / 64) / NCG;
+    const int c_end = min(q_end * 64, ncols);
+    const int jc_last = c_end > q_begin * 64 ? (c_end - 1) / 32 * 32 : -1;
+    if (jc_last < 0) release();
 #pragma unroll 1
-    for (int q = cg * (BN / 64) / NCG; q < (cg + 1) * (BN / 64) / NCG; ++q) {
+    for (int q = q_begin; q < q_end; ++q) {
       const int qc = q * 64;
       if (qc >= ncols) break;  // uniform: depends on the tile only
       constexpr uint32_t kBufs = kStageBytes / 16384 / NCG;  // buffers per column group
@@ -421,7 +428,8 @@ struct EpiGT {
         if (jc >= ncols) break;
         uint32_t r[32];
         tmem_ld32(taddr + jc, r);
-        tmem_ld_wait();
+        tmem_ld_wait(r);
+        if (jc == jc_last) release();
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {

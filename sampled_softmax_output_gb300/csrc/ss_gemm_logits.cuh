@@ -66,11 +66,14 @@ cudaError_t softmax_grad(const CUtensorMap& tH, const CUtensorMap& tWc,
   ep.amax = amax;
   // eight epilogue warps in two column groups, one staging buffer each; CTA
   // pairs (each SM stages half of the W_c tile, a 6-deep ring beside the G
-  // staging) once the operands exceed L2 (measured on GB300: the pair is 5%
-  // slower at (T + C) * D * 2 = 41 MB, 2-3% faster at 138 and 177 MB)
+  // staging) whenever every pair gets a tile. The epilogue hands its
+  // accumulator back before its stores; before it did, pairs were 5% slower
+  // at (T + C) * D * 2 = 41 MB (2-3% faster at 138 and 177 MB); with it,
+  // measured on GB300 at T16384_C10240: the separate calls 0.640 -> 0.624 ms
+  // per step, the capped head's step 0.670 -> 0.658 ms.
   const int n_tiles = (C + kBnLogits - 1) / kBnLogits;
   if constexpr (!F8) {  // the e4m3 operands are half the bytes: single CTAs throughout
-    if (operands_exceed_l2(T, C, D)) {
+    if (softmax_grad_on_pairs(T, C, num_sms)) {
       GemmShape shp{(T + 2 * BM - 1) / (2 * BM), n_tiles, D / BK};
       shp.gate = gate;
       return launch_gemm2<kBnLogits, 6, false, false, EpiGT<CAP, KMAX>, 8>(tH, tWc_half, shp, ep,

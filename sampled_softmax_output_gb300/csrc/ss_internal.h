@@ -77,6 +77,11 @@ constexpr double kL2OperandBytes = 96.0 * (1 << 20);
 inline bool operands_exceed_l2(int T, int C, int D) {
   return (static_cast<double>(T) + C) * D * 2.0 > kL2OperandBytes;
 }
+// The bf16 softmax-gradient GEMM runs on CTA pairs whenever every pair gets a
+// 256 x 256 logit tile (single CTAs for small batches).
+inline bool softmax_grad_on_pairs(int T, int C, int num_sms) {
+  return static_cast<int64_t>((T + 255) / 256) * ((C + 255) / 256) >= num_sms / 2;
+}
 
 // ---- candidate build (ss_candidates.cu)
 size_t build_candidates_smem_bytes(int64_t V);
