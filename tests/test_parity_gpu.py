@@ -70,6 +70,29 @@ def test_small_parity(orc, T, V, D, C, seed, scale, path):
 
 
 @pytest.mark.parametrize("path", ["calls", "step"])
+def test_pair_kernels_ragged(orc, path):
+    """A batch large enough that the logit GEMMs run on CTA pairs (more
+    256 x 256 tiles than SM pairs) while H and W_c stay in L2, with ragged
+    token and candidate tails (the last pair's second CTA holds no valid
+    row, the last logit tile 135 valid columns): every output element
+    against the oracle."""
+    T, V, D, C, seed = 2049, 8000, 128, 4999, 21
+    x, C = _case(T, V, D, C, seed)
+    assert (T + 255) // 256 * ((C + 255) // 256 - 1) >= 76
+    ref = _full_oracle(orc, x, C, seed, 1.0 / T)
+    got = RUNS[path](ss, x, C, seed, 1.0 / T)
+    assert got["status"] == 0
+    np.testing.assert_array_equal(got["cand"], ref["cand"])
+    np.testing.assert_array_equal(got["slot"], ref["slot"])
+    assert_loss_close(got["loss"], ref["loss"])
+    assert_loss_close(got["lse"], ref["lse"])
+    assert rel_fro(got["dH"], ref["dH"]) < GRAD_RTOL
+    assert rel_fro(got["dW"], ref["dW"]) < GRAD_RTOL
+    outside = np.setdiff1d(np.arange(V), ref["cand"])
+    assert np.all(got["dW"][outside] == 0)
+
+
+@pytest.mark.parametrize("path", ["calls", "step"])
 def test_accumulate_and_untouched_rows(orc, path):
     T, V, D, C, seed = 300, 2500, 256, 700, 11
     x, C = _case(T, V, D, C, seed)
