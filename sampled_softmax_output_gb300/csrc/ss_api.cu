@@ -519,12 +519,16 @@ __device__ __forceinline__ void lse_fold_same(float& M, float& S, float m, float
 // block of kMergeTokens * D values) into Hs.
 constexpr int kMergeTokens = 32;
 
+// CAP: the capped head's stored forward (EpiFwdP<false, NBUF, true>): the
+// reference is cap for every row, tgt holds z at the target, and the patched
+// target entry carries dz/ds there; lse - cap <= ln C, so no fallback.
+template <bool CAP>
 __global__ void __launch_bounds__(256) k_lse_merge_p(
     const float2* __restrict__ part, const float* __restrict__ tgt,
     const int32_t* __restrict__ slot, const float* __restrict__ ref, int T, int C, int n_parts,
     const uint16_t* __restrict__ H, int D, float scale, uint16_t* __restrict__ Pt, int64_t ldP,
     uint16_t* __restrict__ Hs, float* __restrict__ rowfac, int* fallback,
-    float* __restrict__ loss, float* __restrict__ lse, int* status) {
+    float* __restrict__ loss, float* __restrict__ lse, int* status, HeadCap head) {
   static_assert(kMergeTokens == 32, "one lane per token");
   __shared__ float2 red[8][kMergeTokens];
   __shared__ float s_alpha[kMergeTokens];
@@ -562,7 +566,7 @@ __global__ void __launch_bounds__(256) k_lse_merge_p(
       const float l = M + logf(S);
       const int sl = valid ? __ldg(slot + t) : 0;
       const bool bad = valid && static_cast<unsigned>(sl) >= static_cast<unsigned>(C);
-      const float r = valid ? __ldcg(ref + t) : 0.f;
+      const float r = CAP ? head.cap : (valid ? __ldcg(ref + t) : 0.f);
       const float alpha = expf(r - l);
       // 0 marks a token whose H row is not scaled (beyond T, or a bad slot)
       s_alpha[lane] = valid && !bad ? alpha : 0.f;
@@ -574,7 +578,10 @@ __global__ void __launch_bounds__(256) k_lse_merge_p(
           lse[t] = l;
           loss[t] = l - x;
           rowfac[t] = scale * alpha;
-          if (!(l - r <= kStoredSpan)) {
+          if (CAP) {  // x = z at the target
+            Pt[static_cast<int64_t>(t) * ldP + sl] =
+                bf16_bits((expf(x - r) - expf(l - r)) * (x * (head.cap - x) * head.icap_tau));
+          } else if (!(l - r <= kStoredSpan)) {
             *fallback = 1;
           } else {
             Pt[static_cast<int64_t>(t) * ldP + sl] = bf16_bits(expf(x - r) - expf(l - r));
@@ -975,10 +982,12 @@ ss_status enqueue_backward(const uint16_t* H, const int32_t* cand, const int32_t
 // sets Hs = H and the row factors to `scale`. The regions: Pt in G's
 // place, r and the dH row factors after the target logits, Hs = alpha H in
 // the place of the FP8 head's rounded H.
+// hc: the capped head (cap <= kStoredCapMax), or cap 0 for the plain head
 ss_status enqueue_step_stored(const uint16_t* H, const int32_t* cand, const int32_t* slot,
-                              int64_t T, int64_t V, int64_t C, int64_t D, float scale,
-                              int accumulate, float* loss, float* lse, uint16_t* dH, float* dW,
-                              const Layout& L, char* ws, int nsm, cudaStream_t s) {
+                              int64_t T, int64_t V, int64_t C, int64_t D, const HeadCap& hc,
+                              float scale, int accumulate, float* loss, float* lse, uint16_t* dH,
+                              float* dW, const Layout& L, char* ws, int nsm, cudaStream_t s) {
+  const bool capped = hc.cap > 0.f;
   int* status = reinterpret_cast<int*>(ws + L.hdr);
   int* fallback = reinterpret_cast<int*>(ws + L.hdr + kHdrFallback);
   uint16_t* Wc = reinterpret_cast<uint16_t*>(ws + L.wc);
@@ -1001,22 +1010,32 @@ ss_status enqueue_step_stored(const uint16_t* H, const int32_t* cand, const int3
                   make_map(&tHsMn, Hs, D, T, D * 2, 64, 64);
   if (!ok) return fail("cuTensorMapEncodeTiled", cudaErrorInvalidValue);
   trace_pre(s, "gemm_forward_lse");
-  cudaError_t e = launch_forward_stored(tH, tWc, tWc2, tPk, iT, iC, iD, slot, part, tgt, ref,
-                                        fallback, status, nsm, s);
+  cudaError_t e = capped ? launch_forward_stored_cap(tH, tWc, tWc2, tPk, iT, iC, iD, slot, part,
+                                                     tgt, hc, status, nsm, s)
+                         : launch_forward_stored(tH, tWc, tWc2, tPk, iT, iC, iD, slot, part, tgt,
+                                                 ref, fallback, status, nsm, s);
   trace_post(s);
   if (e != cudaSuccess) return fail("launch gemm_forward_lse", e);
   trace_pre(s, "lse_merge");
-  e = launch_pdl(k_lse_merge_p, dim3(static_cast<int>((T + kMergeTokens - 1) / kMergeTokens)),
-                 dim3(256), 0, s, part, tgt, slot, ref, iT, iC, static_cast<int>(L.n_ct * 2), H, iD,
-                 scale,
-                 P, static_cast<int64_t>(L.ldG), Hs, rowfac, fallback, loss, lse, status);
+  const dim3 merge_grid(static_cast<unsigned>((T + kMergeTokens - 1) / kMergeTokens));
+  e = capped ? launch_pdl(k_lse_merge_p<true>, merge_grid, dim3(256), 0, s, part, tgt, slot, ref,
+                          iT, iC, static_cast<int>(L.n_ct * 2), H, iD, scale, P,
+                          static_cast<int64_t>(L.ldG), Hs, rowfac, fallback, loss, lse, status,
+                          hc)
+             : launch_pdl(k_lse_merge_p<false>, merge_grid, dim3(256), 0, s, part, tgt, slot, ref,
+                          iT, iC, static_cast<int>(L.n_ct * 2), H, iD, scale, P,
+                          static_cast<int64_t>(L.ldG), Hs, rowfac, fallback, loss, lse, status,
+                          hc);
   trace_post(s);
   if (e != cudaSuccess) return fail("launch k_lse_merge_p", e);
-  trace_pre(s, "gemm_softmax_grad");
-  e = launch_softmax_grad_gated(tH, tWc, tWc2, tPk, iT, iC, iD, slot, lse, fallback, H, Hs, rowfac,
-                                scale, status, nsm, s);
-  trace_post(s);
-  if (e != cudaSuccess) return fail("launch gemm_softmax_grad", e);
+  // the capped head's lse lies within ln C of its reference: no fallback
+  if (!capped) {
+    trace_pre(s, "gemm_softmax_grad");
+    e = launch_softmax_grad_gated(tH, tWc, tWc2, tPk, iT, iC, iD, slot, lse, fallback, H, Hs,
+                                  rowfac, scale, status, nsm, s);
+    trace_post(s);
+    if (e != cudaSuccess) return fail("launch gemm_softmax_grad", e);
+  }
   trace_pre(s, "gemm_grads");
   e = launch_grads(tPk, tWcMn, tPmn, tHsMn, iT, iC, iD, iV, accumulate, cand, dH, dW, status, nsm,
                    s, rowfac, &scale);
@@ -1240,10 +1259,11 @@ static ss_status step_impl(const int32_t* targets, const uint16_t* H, const uint
   // one gather of W[cand] serves the forward and the backward
   ss_status r = enqueue_gather_operands(W, cand, H, T, C, V, D, fp8, L, ws, nsm, s, h_beside);
   if (r != SS_OK) return r;
-  // the plain bf16 head with one target keeps the forward's probabilities
-  if (fp8 == 0 && !(cap > 0.f) && tg.K == 1 && tg.w[0] == 1.f)
-    return enqueue_step_stored(H, cand, slot, T, V, C, D, scale, accumulate, loss, lse, dH, dW, L,
-                               ws, nsm, s);
+  // the bf16 head with one target keeps the forward's probabilities: the
+  // plain head, and the capped head up to kStoredCapMax
+  if (fp8 == 0 && !(cap > kStoredCapMax) && tg.K == 1 && tg.w[0] == 1.f)
+    return enqueue_step_stored(H, cand, slot, T, V, C, D, head_cap(cap, tau), scale, accumulate,
+                               loss, lse, dH, dW, L, ws, nsm, s);
   // the softmax-gradient GEMM's mainloop beside the LSE merge: measured with
   // the plain bf16 head (one partial per row and logit tile); the heads whose
   // merge folds two per tile keep the wide merge and the full wait, and so do

@@ -172,9 +172,6 @@ __device__ __forceinline__ Tv select32(const Tv (&x)[32], int off) {
 
 // The capped head: z = cap / (1 + exp(-s / tau)) = cap * 1 / (1 + 2^(-s k1)),
 // k1 = log2(e) / tau, and dz/ds = z (cap - z) icap_tau, icap_tau = 1 / (cap tau).
-struct HeadCap {
-  float cap, k1, icap_tau;
-};
 __device__ __forceinline__ float head_z(float s, const HeadCap& h) {
   return h.cap * rcp_approx(1.f + ex2_approx(-s * h.k1));
 }
@@ -510,8 +507,15 @@ using EpiG = EpiGT<false>;
 // detects (lse - r too large) and answers with the recompute.
 // The staging and the TMA stores are those of EpiGT; two column groups, two
 // partials per row per tile, part[(nt * 2 + cg) * T + t].
-template <bool PRE, int NBUF = 1>
+// CAP: the capped head z = cap / (1 + exp(-s / tau)). Since z < cap, the
+// reference is r = cap for every row (no first launch; exp(z - cap) stays a
+// normal number for cap <= 64), the partials are of exp(z - cap), and
+//   Pt[t, j] = exp(z[t,j] - cap) dz/ds[t,j],
+// so that G = scale (P - Y) dz/ds = scale exp(cap - lse) (Pt - Y exp(lse - cap) dz/ds);
+// the target logit stored is z.
+template <bool PRE, int NBUF = 1, bool CAP = false>
 struct EpiFwdP {
+  static_assert(!(PRE && CAP), "the capped head's reference is cap: no first launch");
   // NBUF 16 KB staging buffers per column group: with two, a group fills one
   // while the store of the other is still reading it
   static_assert(NBUF == 1 || NBUF == 2, "staging buffers per column group");
@@ -525,9 +529,10 @@ struct EpiFwdP {
     const int32_t* slot;
     float2* part;
     float* tgt;        // [T]: S[t, slot[t]]
-    float* ref;        // [T]: r[t] (PRE writes it, the later tiles read it)
+    float* ref;        // [T]: r[t] (PRE writes it, the later tiles read it); not used with CAP
     int* clear_word;   // PRE: set to 0 once (the merge's fallback flag), or null
     int* status;
+    HeadCap head;      // used when CAP
   };
   __device__ static void begin(const Params& p, EpiState& es) {
     if constexpr (PRE)
@@ -566,6 +571,8 @@ struct EpiFwdP {
         }
       });
       if (valid && cg == 0) p.ref[t] = r;
+    } else if constexpr (CAP) {
+      r = p.head.cap;
     } else {
       r = valid ? __ldcg(p.ref + t) : 0.f;
     }
@@ -590,7 +597,20 @@ struct EpiFwdP {
       const int nv = min(32, ncols - jc);
       float e[32];
       float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
-      if (nv == 32) {  // every chunk but a ragged tail: no per-column predicates
+      if constexpr (CAP) {  // e = exp(z - cap) <= 1 for the partial, e dz/ds into Pt
+        const HeadCap hz = p.head;
+#pragma unroll
+        for (int k = 0; k < 32; k += 2) {
+          const float z0 = head_z(__uint_as_float(v[k]), hz);
+          const float z1 = head_z(__uint_as_float(v[k + 1]), hz);
+          const float x0 = nv == 32 || k < nv ? ex2_approx(fmaf(z0, kLog2e, -r2)) : 0.f;
+          const float x1 = nv == 32 || k + 1 < nv ? ex2_approx(fmaf(z1, kLog2e, -r2)) : 0.f;
+          a0 += x0;
+          a1 += x1;
+          e[k] = x0 * head_dz(z0, hz);
+          e[k + 1] = x1 * head_dz(z1, hz);
+        }
+      } else if (nv == 32) {  // every chunk but a ragged tail: no per-column predicates
         // two logits per FMA and per add (packed fp32 pairs)
         const uint64_t k2 = f32x2(kLog2e, kLog2e), nr2 = f32x2(-r2, -r2);
         uint64_t s01 = f32x2(0.f, 0.f), s23 = s01;
@@ -622,7 +642,7 @@ struct EpiFwdP {
         }
       }
       const float a = (a0 + a1) + (a2 + a3);
-      if (a <= 0x1p86f && m == r) {
+      if (CAP || (a <= 0x1p86f && m == r)) {
         s += a;
       } else {  // rare: the partial takes a running max (robust lse for the fallback)
         float cm = -INFINITY;
@@ -654,7 +674,7 @@ struct EpiFwdP {
       if (__any_sync(0xffffffffu, hit)) {
         const float x = __uint_as_float(select32(v, off));
         if (hit) {
-          tg = x;
+          tg = CAP ? head_z(x, p.head) : x;
           has_t = true;
         }
       }

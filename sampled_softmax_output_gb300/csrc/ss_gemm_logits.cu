@@ -113,6 +113,30 @@ cudaError_t launch_forward_stored(const CUtensorMap& tH, const CUtensorMap& tWc,
                                                                     num_sms, stream);
 }
 
+// The capped head's stored forward: one launch over every logit tile (the
+// reference is cap, known before any tile), on CTA pairs whenever every pair
+// gets a tile.
+cudaError_t launch_forward_stored_cap(const CUtensorMap& tH, const CUtensorMap& tWc,
+                                      const CUtensorMap& tWc_half, const CUtensorMap& tP, int T,
+                                      int C, int D, const int32_t* slot, float2* part, float* tgt,
+                                      const HeadCap& head, int* status, int num_sms,
+                                      cudaStream_t stream) {
+  const int n_tiles = (C + kBnLogits - 1) / kBnLogits;
+  const int pair_m = (T + 2 * BM - 1) / (2 * BM);
+  if (pair_m * n_tiles >= num_sms / 2) {
+    using Epi = EpiFwdP<false, kFwdPairBufs, true>;
+    typename Epi::Params ep{tP, T, C, slot, part, tgt, nullptr, nullptr, status, head};
+    GemmShape shp{pair_m, n_tiles, D / BK, 0, 0, nullptr, kFwdGroupRows / (2 * BM)};
+    return launch_gemm2<kBnLogits, kFwdPairStages, false, false, Epi, 8>(tH, tWc_half, shp, ep,
+                                                                         status, num_sms, stream);
+  }
+  using Epi = EpiFwdP<false, kFwdBufs, true>;
+  typename Epi::Params ep{tP, T, C, slot, part, tgt, nullptr, nullptr, status, head};
+  GemmShape shp{(T + BM - 1) / BM, n_tiles, D / BK, 0, 0, nullptr, kFwdGroupRows / BM};
+  return launch_gemm<kBnLogits, kFwdStages, false, false, Epi, 8>(tH, tWc, shp, ep, status,
+                                                                 num_sms, stream);
+}
+
 cudaError_t launch_softmax_grad_gated(const CUtensorMap& tH, const CUtensorMap& tWc,
                                       const CUtensorMap& tWc_half, const CUtensorMap& tG_store,
                                       int T, int C, int D, const int32_t* slot, const float* lse,

@@ -87,9 +87,4 @@ cudaError_t softmax_grad(const CUtensorMap& tH, const CUtensorMap& tWc,
                      EpiGT<CAP, KMAX, F8>, 8, F8>(tH, tWc, shp, ep, status, num_sms, stream);
 }
 
-inline HeadCap head_cap(float cap, float tau) {
-  const float log2e = 1.4426950408889634f;
-  return cap > 0.f ? HeadCap{cap, log2e / tau, 1.f / (cap * tau)} : HeadCap{0.f, 0.f, 0.f};
-}
-
 }  // namespace ss

@@ -61,6 +61,19 @@ inline int fwd_groups(float cap, bool fp8 = false, int targets = 1) {
 
 struct GemmShape;
 
+// The capped head z = cap / (1 + exp(-s / tau)): cap, log2(e) / tau and
+// 1 / (cap tau) (dz/ds = z (cap - z) / (cap tau)); all zero for the plain head.
+struct HeadCap {
+  float cap, k1, icap_tau;
+};
+inline HeadCap head_cap(float cap, float tau) {
+  const float log2e = 1.4426950408889634f;
+  return cap > 0.f ? HeadCap{cap, log2e / tau, 1.f / (cap * tau)} : HeadCap{0.f, 0.f, 0.f};
+}
+// The stored-probability step takes the capped head up to this cap (exp(z -
+// cap) must stay a normal number); above it the step recomputes the logits.
+constexpr float kStoredCapMax = 64.f;
+
 // Targets per token: K (at most kMaxTargets) target slots per row,
 // slot[k * T + t], with weights w[k] (K = 1, w = 1: the single-target loss).
 constexpr int kMaxTargets = 8;
@@ -133,6 +146,14 @@ cudaError_t launch_forward_stored(const CUtensorMap& tH, const CUtensorMap& tWc,
                                   int D, const int32_t* slot, float2* part, float* tgt,
                                   float* ref, int* clear_word, int* status, int num_sms,
                                   cudaStream_t stream);
+// The capped head's stored forward (cap <= kStoredCapMax): the reference is
+// cap for every row, so one launch covers every logit tile; Pt = exp(z - cap)
+// dz/ds, the partials of exp(z - cap), the target's z in tgt.
+cudaError_t launch_forward_stored_cap(const CUtensorMap& tH, const CUtensorMap& tWc,
+                                      const CUtensorMap& tWc_half, const CUtensorMap& tP, int T,
+                                      int C, int D, const int32_t* slot, float2* part, float* tgt,
+                                      const HeadCap& head, int* status, int num_sms,
+                                      cudaStream_t stream);
 // The stored-probability step's fallback: launch_softmax_grad (plain bf16
 // head, one target, G = P - Y with scale 1) that runs only if *gate != 0, and
 // then also sets Hs = H and rowfac[t] = scale for every row.

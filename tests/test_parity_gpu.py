@@ -542,17 +542,21 @@ CAPPED = [
     (300, 3000, 768, 517, 4, 1.0, 30.0, 7.5),     # ragged T and C tails
     (257, 2000, 192, 1000, 5, 0.5, 6.0, 0.7),     # strongly saturated cap
     (500, 1000, 128, 1000, 6, 1.0 / 500, 15.0, 3.0),  # C = V
+    (300, 3000, 768, 517, 9, 1.0, 80.0, 20.0),    # above the stored step's cap limit
 ]
 
 
+@pytest.mark.parametrize("path", ["calls", "step"])
 @pytest.mark.parametrize("T,V,D,C,seed,scale,cap,tau", CAPPED)
-def test_capped_head_parity(orc, T, V, D, C, seed, scale, cap, tau):
+def test_capped_head_parity(orc, T, V, D, C, seed, scale, cap, tau, path):
     """z = cap / (1 + exp(-s / tau)) before the softmax: every element against
-    the oracle of the same head."""
+    the oracle of the same head, through the three calls (the backward
+    recomputes the logits) and through ss_step (which keeps exp(z - cap) dz/ds
+    from the forward)."""
     x, C = _case(T, V, D, C, seed)
     x["W"] = synth.make_inputs(1, V, D, 1.1, seed + 50, w_std=0.2)["W"]  # wide logits
     ref = _full_oracle(orc, x, C, seed, scale, cap=cap, tau=tau)
-    got = run_gpu(ss, x, C, seed, scale, cap=cap, tau=tau)
+    got = RUNS[path](ss, x, C, seed, scale, cap=cap, tau=tau)
     assert got["status"] == 0
     np.testing.assert_array_equal(got["cand"], ref["cand"])
     assert_loss_close(got["loss"], ref["loss"])
