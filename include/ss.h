@@ -205,6 +205,15 @@ ss_status ss_backward_head(const uint16_t* H, const uint16_t* W, const int32_t* 
  * arguments and results as those three calls. The candidate rows W[cand] are
  * gathered once and serve both passes (the separate ss_backward gathers them
  * again, since it cannot know whether W or cand changed after ss_forward).
+ * With the bf16 head and one target of weight 1 (plain, or capped with
+ * cap <= 64) the logits are computed once: the forward keeps exp(S - r) in
+ * bf16 for the backward (r a per-row reference; with the cap, exp(z - cap)
+ * dz/ds) instead of the backward recomputing them. The results then equal
+ * the three calls' within the library's tolerances (loss and lse 1e-3
+ * relative, dH and dW 2e-2 relative Frobenius) rather than bit for bit; a row
+ * whose logits exceed the reference's range makes the step recompute the
+ * logits for the whole batch, with the same results. Other heads: the three
+ * calls' results exactly.
  * Pages: as for ss_forward and ss_backward.
  */
 ss_status ss_step(const int32_t* targets, const uint16_t* H, const uint16_t* W, int64_t T,
