@@ -597,19 +597,36 @@ struct EpiFwdP {
       const int nv = min(32, ncols - jc);
       float e[32];
       float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
-      if constexpr (CAP) {  // e = exp(z - cap) <= 1 for the partial, e dz/ds into Pt
-        const HeadCap hz = p.head;
+      if constexpr (CAP) {
+        // with w = 1 / (1 + exp(-s / tau)): z = cap w, z - cap = cap (w - 1)
+        // and dz/ds = (cap / tau) w (1 - w); x = exp(z - cap) <= 1 enters the
+        // partial, x dz/ds goes to Pt (two logits per packed operation)
+        const float k1 = p.head.k1, cl2 = r2;  // r = cap
+        const float ct = p.head.cap * p.head.cap * p.head.icap_tau;  // cap / tau
+        const uint64_t nk1 = f32x2(-k1, -k1), one = f32x2(1.f, 1.f), mone = f32x2(-1.f, -1.f);
+        const uint64_t cl = f32x2(cl2, cl2), ncl = f32x2(-cl2, -cl2), ctt = f32x2(ct, ct);
+        uint64_t acc = f32x2(0.f, 0.f);
 #pragma unroll
         for (int k = 0; k < 32; k += 2) {
-          const float z0 = head_z(__uint_as_float(v[k]), hz);
-          const float z1 = head_z(__uint_as_float(v[k + 1]), hz);
-          const float x0 = nv == 32 || k < nv ? ex2_approx(fmaf(z0, kLog2e, -r2)) : 0.f;
-          const float x1 = nv == 32 || k + 1 < nv ? ex2_approx(fmaf(z1, kLog2e, -r2)) : 0.f;
-          a0 += x0;
-          a1 += x1;
-          e[k] = x0 * head_dz(z0, hz);
-          e[k + 1] = x1 * head_dz(z1, hz);
+          float t0, t1;
+          f32x2_split(mul_f32x2(f32x2_bits(v[k], v[k + 1]), nk1), t0, t1);
+          float q0, q1;
+          f32x2_split(add_f32x2(f32x2(ex2_approx(t0), ex2_approx(t1)), one), q0, q1);
+          const uint64_t w = f32x2(rcp_approx(q0), rcp_approx(q1));
+          float y0, y1;
+          f32x2_split(fma_f32x2(w, cl, ncl), y0, y1);
+          float x0 = ex2_approx(y0), x1 = ex2_approx(y1);
+          if (nv < 32) {
+            if (k >= nv) x0 = 0.f;
+            if (k + 1 >= nv) x1 = 0.f;
+          }
+          const uint64_t x = f32x2(x0, x1);
+          acc = add_f32x2(acc, x);
+          // x (cap / tau) w (1 - w)
+          const uint64_t g = mul_f32x2(mul_f32x2(x, ctt), mul_f32x2(w, fma_f32x2(w, mone, one)));
+          f32x2_split(g, e[k], e[k + 1]);
         }
+        f32x2_split(acc, a0, a1);
       } else if (nv == 32) {  // every chunk but a ragged tail: no per-column predicates
         // two logits per FMA and per add (packed fp32 pairs)
         const uint64_t k2 = f32x2(kLog2e, kLog2e), nr2 = f32x2(-r2, -r2);
