@@ -339,7 +339,7 @@ void ss_step_graph_destroy(ss_step_graph* graph);
  * fixed-size array inside the library's own device data, of
  * SS_NOALLOC_SCRATCH_BYTES. Every GPU that loads the library holds that array
  * until the process exits. Sizes whose scratch, 1 KB + C*D*2 +
- * ceil(C/256)*T*16 + T*32 bytes (each term rounded up to 1 KB), exceeds it are
+ * ceil(C/256)*T*16 + T*40 bytes (each term rounded up to 1 KB), exceeds it are
  * rejected with SS_ERR_UNSUPPORTED (ss_last_error says by how much).
  *   status_host : NULL, or a host int32 that receives the device status
  *                 word of this call after the stream is synchronised; the

@@ -66,8 +66,8 @@ Layout make_layout(int64_t T, int64_t C, int64_t D) {
   off = align_up(off + static_cast<size_t>(C) * D * 2, 1024);
   L.part = off;
   off = align_up(off + static_cast<size_t>(L.n_ct) * kFwdGroupsMax * T * sizeof(float2), 1024);
-  L.tgt = off;  // target logits, up to kMaxTargets per token
-  off = align_up(off + static_cast<size_t>(T) * kMaxTargets * sizeof(float), 1024);
+  L.tgt = off;  // target logits, up to kMaxTargets per token; then r and the row factors
+  off = align_up(off + static_cast<size_t>(T) * (kMaxTargets + 2) * sizeof(float), 1024);
   L.ldT8 = (T + 15) / 16 * 16;
   L.ldC8 = (C + 15) / 16 * 16;
   // G in bf16, or (FP8 gradients) G8 [T, ldG] and G8^T [C, ldT8] in e5m2
@@ -528,7 +528,7 @@ __global__ void __launch_bounds__(256) k_lse_merge_p(
     const int32_t* __restrict__ slot, const float* __restrict__ ref, int T, int C, int n_parts,
     const uint16_t* __restrict__ H, int D, float scale, uint16_t* __restrict__ Pt, int64_t ldP,
     uint16_t* __restrict__ Hs, float* __restrict__ rowfac, int* fallback,
-    float* __restrict__ loss, float* __restrict__ lse, int* status, HeadCap head) {
+    float* __restrict__ loss, float* __restrict__ lse, int* status, HeadCap head, Targets tg) {
   static_assert(kMergeTokens == 32, "one lane per token");
   __shared__ float2 red[8][kMergeTokens];
   __shared__ float s_alpha[kMergeTokens];
@@ -564,27 +564,42 @@ __global__ void __launch_bounds__(256) k_lse_merge_p(
 #pragma unroll
       for (int w = 1; w < 8; ++w) lse_fold_same(M, S, red[w][lane].x, red[w][lane].y);
       const float l = M + logf(S);
-      const int sl = valid ? __ldg(slot + t) : 0;
-      const bool bad = valid && static_cast<unsigned>(sl) >= static_cast<unsigned>(C);
       const float r = CAP ? head.cap : (valid ? __ldcg(ref + t) : 0.f);
       const float alpha = expf(r - l);
+      // the targets: tg.K slots and logits (z with the cap) per token
+      int sl[kMaxTargets];
+      float x[kMaxTargets];
+      bool bad = false;
+      float wsum = 0.f, acc = 0.f;
+      for (int k = 0; k < tg.K; ++k) {
+        sl[k] = valid ? __ldg(slot + static_cast<size_t>(k) * T + t) : 0;
+        x[k] = valid ? __ldcg(tgt + static_cast<size_t>(k) * T + t) : 0.f;
+        bad |= valid && static_cast<unsigned>(sl[k]) >= static_cast<unsigned>(C);
+        wsum += tg.w[k];
+        acc += tg.w[k] * (l - x[k]);
+      }
       // 0 marks a token whose H row is not scaled (beyond T, or a bad slot)
       s_alpha[lane] = valid && !bad ? alpha : 0.f;
       if (valid) {
         if (bad) {
           set_status(status, SS_ERR_INDEX);
         } else {
-          const float x = __ldcg(tgt + t);
           lse[t] = l;
-          loss[t] = l - x;
-          rowfac[t] = scale * alpha;
-          if (CAP) {  // x = z at the target
-            Pt[static_cast<int64_t>(t) * ldP + sl] =
-                bf16_bits((expf(x - r) - expf(l - r)) * (x * (head.cap - x) * head.icap_tau));
-          } else if (!(l - r <= kStoredSpan)) {
+          loss[t] = acc;
+          rowfac[t] = scale * wsum * alpha;
+          if (!CAP && !(l - r <= kStoredSpan)) {
             *fallback = 1;
           } else {
-            Pt[static_cast<int64_t>(t) * ldP + sl] = bf16_bits(expf(x - r) - expf(l - r));
+            // each target column: exp(x - r) - (w / W) exp(lse - r), w the summed
+            // weight of every target on that column (times dz/ds with the cap)
+            const float el = expf(l - r);
+            for (int k = 0; k < tg.K; ++k) {
+              float wt = 0.f;
+              for (int k2 = 0; k2 < tg.K; ++k2) wt += sl[k2] == sl[k] ? tg.w[k2] : 0.f;
+              float g = expf(x[k] - r) - wt / wsum * el;
+              if (CAP) g *= x[k] * (head.cap - x[k]) * head.icap_tau;
+              Pt[static_cast<int64_t>(t) * ldP + sl[k]] = bf16_bits(g);
+            }
           }
         }
       }
@@ -982,20 +997,22 @@ ss_status enqueue_backward(const uint16_t* H, const int32_t* cand, const int32_t
 // sets Hs = H and the row factors to `scale`. The regions: Pt in G's
 // place, r and the dH row factors after the target logits, Hs = alpha H in
 // the place of the FP8 head's rounded H.
-// hc: the capped head (cap <= kStoredCapMax), or cap 0 for the plain head
+// hc: the capped head (cap <= kStoredCapMax), or cap 0 for the plain head;
+// tg: the targets per token and their weights
 ss_status enqueue_step_stored(const uint16_t* H, const int32_t* cand, const int32_t* slot,
                               int64_t T, int64_t V, int64_t C, int64_t D, const HeadCap& hc,
-                              float scale, int accumulate, float* loss, float* lse, uint16_t* dH,
-                              float* dW, const Layout& L, char* ws, int nsm, cudaStream_t s) {
+                              const Targets& tg, float scale, int accumulate, float* loss,
+                              float* lse, uint16_t* dH, float* dW, const Layout& L, char* ws,
+                              int nsm, cudaStream_t s) {
   const bool capped = hc.cap > 0.f;
   int* status = reinterpret_cast<int*>(ws + L.hdr);
   int* fallback = reinterpret_cast<int*>(ws + L.hdr + kHdrFallback);
   uint16_t* Wc = reinterpret_cast<uint16_t*>(ws + L.wc);
   uint16_t* P = reinterpret_cast<uint16_t*>(ws + L.g);
   float2* part = reinterpret_cast<float2*>(ws + L.part);
-  float* tgt = reinterpret_cast<float*>(ws + L.tgt);
-  float* ref = tgt + T;
-  float* rowfac = tgt + 2 * T;
+  float* tgt = reinterpret_cast<float*>(ws + L.tgt);  // [K, T]
+  float* ref = tgt + kMaxTargets * T;
+  float* rowfac = ref + T;
   uint16_t* Hs = reinterpret_cast<uint16_t*>(ws + L.hq);
   const int iT = static_cast<int>(T), iV = static_cast<int>(V), iC = static_cast<int>(C),
             iD = static_cast<int>(D);
@@ -1010,10 +1027,8 @@ ss_status enqueue_step_stored(const uint16_t* H, const int32_t* cand, const int3
                   make_map(&tHsMn, Hs, D, T, D * 2, 64, 64);
   if (!ok) return fail("cuTensorMapEncodeTiled", cudaErrorInvalidValue);
   trace_pre(s, "gemm_forward_lse");
-  cudaError_t e = capped ? launch_forward_stored_cap(tH, tWc, tWc2, tPk, iT, iC, iD, slot, part,
-                                                     tgt, hc, status, nsm, s)
-                         : launch_forward_stored(tH, tWc, tWc2, tPk, iT, iC, iD, slot, part, tgt,
-                                                 ref, fallback, status, nsm, s);
+  cudaError_t e = launch_forward_stored(tH, tWc, tWc2, tPk, iT, iC, iD, slot, part, tgt, ref,
+                                        fallback, hc, tg, status, nsm, s);
   trace_post(s);
   if (e != cudaSuccess) return fail("launch gemm_forward_lse", e);
   trace_pre(s, "lse_merge");
@@ -1021,24 +1036,28 @@ ss_status enqueue_step_stored(const uint16_t* H, const int32_t* cand, const int3
   e = capped ? launch_pdl(k_lse_merge_p<true>, merge_grid, dim3(256), 0, s, part, tgt, slot, ref,
                           iT, iC, static_cast<int>(L.n_ct * 2), H, iD, scale, P,
                           static_cast<int64_t>(L.ldG), Hs, rowfac, fallback, loss, lse, status,
-                          hc)
+                          hc, tg)
              : launch_pdl(k_lse_merge_p<false>, merge_grid, dim3(256), 0, s, part, tgt, slot, ref,
                           iT, iC, static_cast<int>(L.n_ct * 2), H, iD, scale, P,
                           static_cast<int64_t>(L.ldG), Hs, rowfac, fallback, loss, lse, status,
-                          hc);
+                          hc, tg);
   trace_post(s);
   if (e != cudaSuccess) return fail("launch k_lse_merge_p", e);
   // the capped head's lse lies within ln C of its reference: no fallback
   if (!capped) {
     trace_pre(s, "gemm_softmax_grad");
     e = launch_softmax_grad_gated(tH, tWc, tWc2, tPk, iT, iC, iD, slot, lse, fallback, H, Hs,
-                                  rowfac, scale, status, nsm, s);
+                                  rowfac, tg, scale, status, nsm, s);
     trace_post(s);
     if (e != cudaSuccess) return fail("launch gemm_softmax_grad", e);
   }
   trace_pre(s, "gemm_grads");
+  // dW_c = scale W (Pt'^T . Hs), W the targets' summed weight
+  float dw_scale = 0.f;
+  for (int k = 0; k < tg.K; ++k) dw_scale += tg.w[k];
+  dw_scale *= scale;
   e = launch_grads(tPk, tWcMn, tPmn, tHsMn, iT, iC, iD, iV, accumulate, cand, dH, dW, status, nsm,
-                   s, rowfac, &scale);
+                   s, rowfac, &dw_scale);
   trace_post(s);
   return e == cudaSuccess ? SS_OK : fail("launch gemm_grads", e);
 }
@@ -1259,11 +1278,11 @@ static ss_status step_impl(const int32_t* targets, const uint16_t* H, const uint
   // one gather of W[cand] serves the forward and the backward
   ss_status r = enqueue_gather_operands(W, cand, H, T, C, V, D, fp8, L, ws, nsm, s, h_beside);
   if (r != SS_OK) return r;
-  // the bf16 head with one target keeps the forward's probabilities: the
-  // plain head, and the capped head up to kStoredCapMax
-  if (fp8 == 0 && !(cap > kStoredCapMax) && tg.K == 1 && tg.w[0] == 1.f)
-    return enqueue_step_stored(H, cand, slot, T, V, C, D, head_cap(cap, tau), scale, accumulate,
-                               loss, lse, dH, dW, L, ws, nsm, s);
+  // the bf16 head keeps the forward's probabilities: the plain head, and
+  // the capped head up to kStoredCapMax, any targets per token
+  if (fp8 == 0 && !(cap > kStoredCapMax))
+    return enqueue_step_stored(H, cand, slot, T, V, C, D, head_cap(cap, tau), tg, scale,
+                               accumulate, loss, lse, dH, dW, L, ws, nsm, s);
   // the softmax-gradient GEMM's mainloop beside the LSE merge: measured with
   // the plain bf16 head (one partial per row and logit tile); the heads whose
   // merge folds two per tile keep the wide merge and the full wait, and so do

@@ -513,7 +513,7 @@ using EpiG = EpiGT<false>;
 //   Pt[t, j] = exp(z[t,j] - cap) dz/ds[t,j],
 // so that G = scale (P - Y) dz/ds = scale exp(cap - lse) (Pt - Y exp(lse - cap) dz/ds);
 // the target logit stored is z.
-template <bool PRE, int NBUF = 1, bool CAP = false>
+template <bool PRE, int NBUF = 1, bool CAP = false, int KMAX = 1>
 struct EpiFwdP {
   static_assert(!(PRE && CAP), "the capped head's reference is cap: no first launch");
   // NBUF 16 KB staging buffers per column group: with two, a group fills one
@@ -526,13 +526,14 @@ struct EpiFwdP {
   struct Params {
     CUtensorMap tmP;  // Pt [T, C] bf16 (row pitch ldG), box 64 x 128, 128-byte swizzle
     int T, C;
-    const int32_t* slot;
+    const int32_t* slot;  // [K, T]
     float2* part;
-    float* tgt;        // [T]: S[t, slot[t]]
+    float* tgt;        // [K, T]: S[t, slot[k T + t]] (z with CAP)
     float* ref;        // [T]: r[t] (PRE writes it, the later tiles read it); not used with CAP
     int* clear_word;   // PRE: set to 0 once (the merge's fallback flag), or null
     int* status;
     HeadCap head;      // used when CAP
+    int K;             // targets per token (KMAX > 1; 1 otherwise)
   };
   __device__ static void begin(const Params& p, EpiState& es) {
     if constexpr (PRE)
@@ -550,9 +551,14 @@ struct EpiFwdP {
     const bool leader = (es.ep_tid & 127) == 0;
     const int t = mt * BM + row;
     const bool valid = t < p.T;
-    const int sl = valid ? __ldg(p.slot + t) : -1;
-    if (valid && nt == 0 && static_cast<unsigned>(sl) >= static_cast<unsigned>(p.C))
-      set_status(p.status, SS_ERR_INDEX);
+    const int K = KMAX > 1 ? p.K : 1;
+    int sl[KMAX];
+#pragma unroll
+    for (int k = 0; k < KMAX; ++k) {
+      sl[k] = valid && k < K ? __ldg(p.slot + static_cast<size_t>(k) * p.T + t) : -1;
+      if (valid && k < K && nt == 0 && static_cast<unsigned>(sl[k]) >= static_cast<unsigned>(p.C))
+        set_status(p.status, SS_ERR_INDEX);
+    }
     const int j0 = nt * BN;
     const int ncols = min(BN, p.C - j0);
     float r;
@@ -581,8 +587,8 @@ struct EpiFwdP {
     const uint32_t gbuf = es.stage + static_cast<uint32_t>(cg) * (16384u * NBUF);
     // partial (m, s): sum of exp(S - m) over this group's columns, m = r
     // unless a chunk moved it up
-    float m = cg * CPG * 32 < ncols ? r : -INFINITY, s = 0.f, tg = 0.f;
-    bool has_t = false;
+    float m = cg * CPG * 32 < ncols ? r : -INFINITY, s = 0.f, tg[KMAX];
+    uint32_t has_t = 0u;  // bit k: target k lies in this group's columns
     for_tmem_chunks<CPG>(taddr, cg * CPG, [&](const uint32_t(&v)[32], int i) {
       const int jc = (cg * CPG + i) * 32;  // column of the tile
       if (jc >= ncols) return;             // uniform: depends on the tile only
@@ -684,15 +690,19 @@ struct EpiFwdP {
         st_shared_v4(rowbase + ((ci ^ r7) << 4), pk[4 * w], pk[4 * w + 1], pk[4 * w + 2],
                      pk[4 * w + 3]);
       }
-      // the target logit: a target falls in a given 32-column chunk for a
+      // the target logits: a target falls in a given 32-column chunk for a
       // few rows of a warp at most
-      const int off = sl - j0 - jc;
-      const bool hit = static_cast<unsigned>(off) < static_cast<unsigned>(nv);
-      if (__any_sync(0xffffffffu, hit)) {
-        const float x = __uint_as_float(select32(v, off));
-        if (hit) {
-          tg = CAP ? head_z(x, p.head) : x;
-          has_t = true;
+#pragma unroll
+      for (int k = 0; k < KMAX; ++k) {
+        if (k >= K) break;  // uniform
+        const int off = sl[k] - j0 - jc;
+        const bool hit = static_cast<unsigned>(off) < static_cast<unsigned>(nv);
+        if (__any_sync(0xffffffffu, hit)) {
+          const float x = __uint_as_float(select32(v, off));
+          if (hit) {
+            tg[k] = CAP ? head_z(x, p.head) : x;
+            has_t |= 1u << k;
+          }
         }
       }
       if (h == 1 || jc + 32 >= ncols) {  // the quarter is complete: store it
@@ -707,7 +717,9 @@ struct EpiFwdP {
     }, release);
     if (valid) {
       p.part[static_cast<size_t>(nt * 2 + cg) * p.T + t] = make_float2(m, s);
-      if (has_t) p.tgt[t] = tg;
+#pragma unroll
+      for (int k = 0; k < KMAX; ++k)
+        if ((has_t >> k) & 1u) p.tgt[static_cast<size_t>(k) * p.T + t] = tg[k];
     }
   }
 };

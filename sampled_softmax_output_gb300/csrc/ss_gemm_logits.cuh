@@ -87,4 +87,94 @@ cudaError_t softmax_grad(const CUtensorMap& tH, const CUtensorMap& tWc,
                      EpiGT<CAP, KMAX, F8>, 8, F8>(tH, tWc, shp, ep, status, num_sms, stream);
 }
 
+// The stored-probability forward: on CTA pairs whenever every pair gets a
+// tile (each SM stages its 128 rows of H and half of every W_c tile, two
+// thirds of the operand intake per flop of one CTA per 128 x 256 tile;
+// measured on GB300: 0.507 against 0.521 ms per step at T16384_C10240, 1.399
+// against 1.447 ms at T32768_C14336, 10.20 against 10.45 ms at T65536_C50304),
+// single CTAs for small batches. Units walk groups of row tiles column by
+// column (kFwdGroupRows rows per group), so W_c is read from DRAM once per
+// group rather than once per row tile while the Pt stream passes through L2
+// (10.20 ms against 10.58 ms row by row, on pairs at T65536_C50304).
+constexpr int kFwdGroupRows = 8192;
+// ring stages and staging buffers per column group: CTA pairs, single CTAs.
+// The epilogue hands its accumulator back before its stores, so it has slack
+// and one staging buffer per group is enough; the 32 KB this frees buys a
+// sixth ring stage (measured on GB300 at T65536_C50304: time x SM clock per
+// step 1.8% lower than five stages with two buffers).
+constexpr int kFwdPairStages = 6, kFwdPairBufs = 1;
+constexpr int kFwdStages = 4, kFwdBufs = 1;
+
+// Plain head: the first logit tile of every row block finds r and clears
+// *clear_word; the launch over the other tiles starts its mainloop at once
+// (H and W_c are older than the first launch) and its epilogue waits for r.
+// CAP: the reference is cap, known before any tile: one launch over every
+// tile. K targets per token (K <= KMAX).
+template <bool CAP, int KMAX>
+cudaError_t forward_stored(const CUtensorMap& tH, const CUtensorMap& tWc,
+                           const CUtensorMap& tWc_half, const CUtensorMap& tP, int T, int C,
+                           int D, const int32_t* slot, float2* part, float* tgt, float* ref,
+                           int* clear_word, const HeadCap& head, int K, int* status, int num_sms,
+                           cudaStream_t stream) {
+  const int n_tiles = (C + kBnLogits - 1) / kBnLogits;
+  const int pair_m = (T + 2 * BM - 1) / (2 * BM);
+  if constexpr (CAP) {
+    if (pair_m * n_tiles >= num_sms / 2) {
+      using Epi = EpiFwdP<false, kFwdPairBufs, true, KMAX>;
+      typename Epi::Params ep{tP, T, C, slot, part, tgt, nullptr, nullptr, status, head, K};
+      GemmShape shp{pair_m, n_tiles, D / BK, 0, 0, nullptr, kFwdGroupRows / (2 * BM)};
+      return launch_gemm2<kBnLogits, kFwdPairStages, false, false, Epi, 8>(
+          tH, tWc_half, shp, ep, status, num_sms, stream);
+    }
+    using Epi = EpiFwdP<false, kFwdBufs, true, KMAX>;
+    typename Epi::Params ep{tP, T, C, slot, part, tgt, nullptr, nullptr, status, head, K};
+    GemmShape shp{(T + BM - 1) / BM, n_tiles, D / BK, 0, 0, nullptr, kFwdGroupRows / BM};
+    return launch_gemm<kBnLogits, kFwdStages, false, false, Epi, 8>(tH, tWc, shp, ep, status,
+                                                                   num_sms, stream);
+  } else {
+    if (pair_m * (n_tiles - 1) >= num_sms / 2) {
+      using Pre = EpiFwdP<true, kFwdPairBufs, false, KMAX>;
+      using Rest = EpiFwdP<false, kFwdPairBufs, false, KMAX>;
+      typename Pre::Params pre{tP, T, C, slot, part, tgt, ref, clear_word, status, head, K};
+      typename Rest::Params rest{tP, T, C, slot, part, tgt, ref, nullptr, status, head, K};
+      GemmShape first{pair_m, 1, D / BK};
+      cudaError_t e = launch_gemm2<kBnLogits, kFwdPairStages, false, false, Pre, 8>(
+          tH, tWc_half, first, pre, status, num_sms, stream);
+      if (e != cudaSuccess || n_tiles == 1) return e;
+      GemmShape others{pair_m, n_tiles, D / BK, 1, 1, nullptr, kFwdGroupRows / (2 * BM)};
+      return launch_gemm2<kBnLogits, kFwdPairStages, false, false, Rest, 8>(
+          tH, tWc_half, others, rest, status, num_sms, stream);
+    }
+    using Pre = EpiFwdP<true, kFwdBufs, false, KMAX>;
+    using Rest = EpiFwdP<false, kFwdBufs, false, KMAX>;
+    typename Pre::Params pre{tP, T, C, slot, part, tgt, ref, clear_word, status, head, K};
+    typename Rest::Params rest{tP, T, C, slot, part, tgt, ref, nullptr, status, head, K};
+    const int m_tiles = (T + BM - 1) / BM;
+    GemmShape first{m_tiles, 1, D / BK};
+    cudaError_t e = launch_gemm<kBnLogits, kFwdStages, false, false, Pre, 8>(
+        tH, tWc, first, pre, status, num_sms, stream);
+    if (e != cudaSuccess || n_tiles == 1) return e;
+    GemmShape others{m_tiles, n_tiles, D / BK, 1, 1, nullptr, kFwdGroupRows / BM};
+    return launch_gemm<kBnLogits, kFwdStages, false, false, Rest, 8>(tH, tWc, others, rest,
+                                                                      status, num_sms, stream);
+  }
+}
+
+// The stored-probability step's fallback: G = P - sum_k (w[k] / W) Y_k (W =
+// sum_k w[k]) from the logits, run only if *gate != 0, which then also resets
+// Hs = H and rowfac = scale W, the factors the stored path's gradient GEMMs
+// apply (rowfac per row of dH, scale W to dW_c).
+template <int KMAX>
+cudaError_t softmax_grad_gated(const CUtensorMap& tH, const CUtensorMap& tWc,
+                               const CUtensorMap& tWc_half, const CUtensorMap& tG_store, int T,
+                               int C, int D, const int32_t* slot, const float* lse, int* gate,
+                               const uint16_t* H, uint16_t* Hs, float* rowfac, const Targets& tg,
+                               float scale, int* status, int num_sms, cudaStream_t stream) {
+  float wsum = 0.f;
+  for (int k = 0; k < tg.K; ++k) wsum += tg.w[k];
+  return softmax_grad<false, KMAX>(tH, tWc, tWc_half, tG_store, T, C, D, slot, lse, 1.f / wsum,
+                                   head_cap(0.f, 1.f), tg, nullptr, status, num_sms, stream,
+                                   false, gate, H, Hs, rowfac, scale * wsum);
+}
+
 }  // namespace ss

@@ -33,4 +33,30 @@ cudaError_t launch_softmax_grad_mtp(const CUtensorMap& tH, const CUtensorMap& tW
                                                       num_sms, stream, late_wait);
 }
 
+cudaError_t launch_forward_stored_mtp(const CUtensorMap& tH, const CUtensorMap& tWc,
+                                      const CUtensorMap& tWc_half, const CUtensorMap& tP, int T,
+                                      int C, int D, const int32_t* slot, float2* part, float* tgt,
+                                      float* ref, int* clear_word, const HeadCap& head,
+                                      const Targets& tg, int* status, int num_sms,
+                                      cudaStream_t stream) {
+  return head.cap > 0.f
+             ? forward_stored<true, kMaxTargets>(tH, tWc, tWc_half, tP, T, C, D, slot, part, tgt,
+                                                 ref, clear_word, head, tg.K, status, num_sms,
+                                                 stream)
+             : forward_stored<false, kMaxTargets>(tH, tWc, tWc_half, tP, T, C, D, slot, part, tgt,
+                                                  ref, clear_word, head, tg.K, status, num_sms,
+                                                  stream);
+}
+
+cudaError_t launch_softmax_grad_gated_mtp(const CUtensorMap& tH, const CUtensorMap& tWc,
+                                          const CUtensorMap& tWc_half,
+                                          const CUtensorMap& tG_store, int T, int C, int D,
+                                          const int32_t* slot, const float* lse, int* gate,
+                                          const uint16_t* H, uint16_t* Hs, float* rowfac,
+                                          const Targets& tg, float scale, int* status,
+                                          int num_sms, cudaStream_t stream) {
+  return softmax_grad_gated<kMaxTargets>(tH, tWc, tWc_half, tG_store, T, C, D, slot, lse, gate,
+                                         H, Hs, rowfac, tg, scale, status, num_sms, stream);
+}
+
 }  // namespace ss

@@ -135,34 +135,43 @@ cudaError_t launch_softmax_grad_fp8(const CUtensorMap& tH8, const CUtensorMap& t
                                     int T, int C, int D, const int32_t* slot, const float* lse,
                                     float cap, float tau, int g8e, const float* amax, int* status,
                                     int num_sms, cudaStream_t stream, bool late_wait = false);
-// The forward that keeps the probabilities for the backward (plain bf16 head,
-// one target): Pt = exp(S - r) in bf16 through tP (as tG_store above), r[t]
-// the row's largest logit over the first logit tile (stored in ref), the
-// softmax partials (two per row per tile) and the target logit. Two launches:
-// the first logit tile of every row block (which finds r and clears
-// *clear_word), then the others.
+// The forward that keeps the probabilities for the backward (bf16 head,
+// plain or capped with cap <= kStoredCapMax, tg.K targets per token): Pt in
+// bf16 through tP (as tG_store above) -- exp(S - r) with r[t] the row's
+// largest logit over the first logit tile (stored in ref), or exp(z - cap)
+// dz/ds with the cap --, the softmax partials (two per row per tile) and the
+// target logits ([K, T]). Plain head: two launches, the first logit tile of
+// every row block (which finds r and clears *clear_word), then the others;
+// capped: one launch. tg.K > 1 runs the instantiations of
+// ss_gemm_logits_mtp.cu.
 cudaError_t launch_forward_stored(const CUtensorMap& tH, const CUtensorMap& tWc,
                                   const CUtensorMap& tWc_half, const CUtensorMap& tP, int T, int C,
                                   int D, const int32_t* slot, float2* part, float* tgt,
-                                  float* ref, int* clear_word, int* status, int num_sms,
+                                  float* ref, int* clear_word, const HeadCap& head,
+                                  const Targets& tg, int* status, int num_sms,
                                   cudaStream_t stream);
-// The capped head's stored forward (cap <= kStoredCapMax): the reference is
-// cap for every row, so one launch covers every logit tile; Pt = exp(z - cap)
-// dz/ds, the partials of exp(z - cap), the target's z in tgt.
-cudaError_t launch_forward_stored_cap(const CUtensorMap& tH, const CUtensorMap& tWc,
+cudaError_t launch_forward_stored_mtp(const CUtensorMap& tH, const CUtensorMap& tWc,
                                       const CUtensorMap& tWc_half, const CUtensorMap& tP, int T,
                                       int C, int D, const int32_t* slot, float2* part, float* tgt,
-                                      const HeadCap& head, int* status, int num_sms,
+                                      float* ref, int* clear_word, const HeadCap& head,
+                                      const Targets& tg, int* status, int num_sms,
                                       cudaStream_t stream);
-// The stored-probability step's fallback: launch_softmax_grad (plain bf16
-// head, one target, G = P - Y with scale 1) that runs only if *gate != 0, and
-// then also sets Hs = H and rowfac[t] = scale for every row.
+// The stored-probability step's fallback (plain bf16 head): launch_softmax_grad
+// with G = P - sum_k (w[k] / W) Y_k, W = sum_k w[k], that runs only if
+// *gate != 0, and then also sets Hs = H and rowfac[t] = scale W for every row.
 cudaError_t launch_softmax_grad_gated(const CUtensorMap& tH, const CUtensorMap& tWc,
                                       const CUtensorMap& tWc_half, const CUtensorMap& tG_store,
                                       int T, int C, int D, const int32_t* slot, const float* lse,
                                       int* gate, const uint16_t* H, uint16_t* Hs, float* rowfac,
-                                      float scale, int* status, int num_sms,
+                                      const Targets& tg, float scale, int* status, int num_sms,
                                       cudaStream_t stream);
+cudaError_t launch_softmax_grad_gated_mtp(const CUtensorMap& tH, const CUtensorMap& tWc,
+                                          const CUtensorMap& tWc_half,
+                                          const CUtensorMap& tG_store, int T, int C, int D,
+                                          const int32_t* slot, const float* lse, int* gate,
+                                          const uint16_t* H, uint16_t* Hs, float* rowfac,
+                                          const Targets& tg, float scale, int* status,
+                                          int num_sms, cudaStream_t stream);
 // the same GEMMs for K > 1 targets per token (ss_gemm_logits_mtp.cu)
 cudaError_t launch_forward_logits_mtp(const CUtensorMap& tH, const CUtensorMap& tWc, int T, int C,
                                       int D, const int32_t* slot, float2* part, float* tgt,

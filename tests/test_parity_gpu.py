@@ -437,6 +437,30 @@ def _stored_fallback_case(T, V, D, C, seed, far):
     return x
 
 
+@pytest.mark.parametrize("far", [5.0, 200.0])
+def test_step_stored_several_targets_far_below(orc, far):
+    """Two weighted targets per token (weights 1 and 0.5, so G carries their
+    sum W = 1.5) on the stored-probability step: with the reference inside
+    the stored range (far 5) and beyond it (far 200, the recompute fallback,
+    whose G is scaled by 1 / W and whose row factors become scale W), every
+    element against the oracle."""
+    T, V, D, C, seed = 300, 4000, 256, 1700, 32
+    x = _stored_fallback_case(T, V, D, C, seed, far)
+    tg = np.stack([x["targets"], np.roll(x["targets"], 1)]).astype(np.int32)
+    weights = [1.0, 0.5]
+    C = max(C, len(np.unique(tg)))
+    ref = orc.loss_and_grads_mtp(x["H"], x["W"], tg, weights, C, seed, 1.0 / T)
+    H, W = to_dev_bf16(x["H"]), to_dev_bf16(x["W"])
+    ws = ss.workspace(T, V, C, D)
+    got = ss.step_mtp(H, W, torch.from_numpy(tg).cuda(), weights, C, seed, ws, scale=1.0 / T)
+    torch.cuda.synchronize()
+    assert ss.read_status(ws)[0] == 0
+    np.testing.assert_array_equal(got["cand"].cpu().numpy(), ref["cand"])
+    assert_loss_close(got["loss"].cpu().numpy(), ref["loss"])
+    assert rel_fro(got["dH"].float().cpu().numpy(), ref["dH"]) < GRAD_RTOL
+    assert rel_fro(got["dW"].cpu().numpy(), ref["dW"]) < GRAD_RTOL
+
+
 @pytest.mark.parametrize("far", [5.0, 25.0, 40.0, 200.0])
 def test_step_stored_reference_far_below(orc, far):
     """The per-row reference r (largest logit of the first tile) far below the
