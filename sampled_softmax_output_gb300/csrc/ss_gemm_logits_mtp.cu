@@ -39,6 +39,14 @@ cudaError_t launch_forward_stored_mtp(const CUtensorMap& tH, const CUtensorMap& 
                                       float* ref, int* clear_word, const HeadCap& head,
                                       const Targets& tg, int* status, int num_sms,
                                       cudaStream_t stream) {
+  // two targets (the next two tokens) have their own instantiation: the
+  // per-chunk target search and registers of eight cost the forward ~10%
+  if (tg.K <= 2)
+    return head.cap > 0.f
+               ? forward_stored<true, 2>(tH, tWc, tWc_half, tP, T, C, D, slot, part, tgt, ref,
+                                         clear_word, head, tg.K, status, num_sms, stream)
+               : forward_stored<false, 2>(tH, tWc, tWc_half, tP, T, C, D, slot, part, tgt, ref,
+                                          clear_word, head, tg.K, status, num_sms, stream);
   return head.cap > 0.f
              ? forward_stored<true, kMaxTargets>(tH, tWc, tWc_half, tP, T, C, D, slot, part, tgt,
                                                  ref, clear_word, head, tg.K, status, num_sms,
