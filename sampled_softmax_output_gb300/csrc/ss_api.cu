@@ -854,12 +854,9 @@ ss_status enqueue_gather_operands(const uint16_t* W, const int32_t* cand, const 
 }
 
 // forward GEMM (LSE partials, target logit) and the LSE merge, from W_c.
-// narrow_merge: at most two merge blocks per SM, for a softmax-gradient GEMM
-// that follows with after_merge (enqueue_backward)
 ss_status enqueue_forward(const uint16_t* H, const int32_t* slot, int64_t T, int64_t C, int64_t D,
                           float cap, float tau, const Targets& tg, int fp8, float* loss,
-                          float* lse, const Layout& L, char* ws, int nsm, cudaStream_t s,
-                          bool narrow_merge = false) {
+                          float* lse, const Layout& L, char* ws, int nsm, cudaStream_t s) {
   int* status = reinterpret_cast<int*>(ws + L.hdr);
   uint16_t* Wc = reinterpret_cast<uint16_t*>(ws + L.wc);
   float2* part = reinterpret_cast<float2*>(ws + L.part);
@@ -881,12 +878,7 @@ ss_status enqueue_forward(const uint16_t* H, const int32_t* slot, int64_t T, int
                                               tg, amax, status, nsm, s);
   trace_post(s);
   if (e != cudaSuccess) return fail("launch gemm_forward_lse", e);
-  // narrow_merge: at most two blocks per SM (40 registers x 256 threads
-  // each), so that the softmax-gradient GEMM after it, whose mainloop starts
-  // while the merge runs, finds room for its CTA beside them
-  const int64_t want = (T * kMergeLanes + 255) / 256;
-  const int blocks =
-      static_cast<int>(narrow_merge ? std::min<int64_t>(want, 2 * int64_t(nsm)) : want);
+  const int blocks = static_cast<int>((T * kMergeLanes + 255) / 256);
   trace_pre(s, "lse_merge");
   const cudaError_t em =
       launch_pdl(k_lse_merge, dim3(blocks), dim3(256), 0, s, part, tgt, slot, static_cast<int>(T),
@@ -911,8 +903,7 @@ int g8_exponent(float cap, float tau) {
 ss_status enqueue_backward_fp8(const int32_t* cand, const int32_t* slot, const float* lse,
                                int64_t T, int64_t V, int64_t C, int64_t D, float cap, float tau,
                                float scale, int accumulate, uint16_t* dH, float* dW,
-                               const Layout& L, char* ws, int nsm, cudaStream_t s,
-                               bool after_merge) {
+                               const Layout& L, char* ws, int nsm, cudaStream_t s) {
   const int g8e = g8_exponent(cap, tau);
   int* status = reinterpret_cast<int*>(ws + L.hdr);
   const float* amax = reinterpret_cast<const float*>(ws + L.hdr + kHdrAmax);
@@ -934,7 +925,7 @@ ss_status enqueue_backward_fp8(const int32_t* cand, const int32_t* slot, const f
             iD = static_cast<int>(D);
   trace_pre(s, "gemm_softmax_grad");
   cudaError_t e = launch_softmax_grad_fp8(tH8, tW8, tG8s, tG8ts, iT, iC, iD, slot, lse, cap, tau,
-                                          g8e, amax, status, nsm, s, after_merge);
+                                          g8e, amax, status, nsm, s);
   trace_post(s);
   if (e != cudaSuccess) return fail("launch gemm_softmax_grad", e);
   trace_pre(s, "gemm_grads");
@@ -944,18 +935,15 @@ ss_status enqueue_backward_fp8(const int32_t* cand, const int32_t* slot, const f
   return e == cudaSuccess ? SS_OK : fail("launch gemm_grads", e);
 }
 
-// softmax-gradient GEMM and the two gradient GEMMs, from W_c. after_merge:
-// the LSE merge is the kernel just before in the stream (ss_step), and W_c,
-// H and slot are older, so the softmax-gradient GEMM's mainloop does not wait
-// for the merge; only its epilogue, which reads lse, does.
+// softmax-gradient GEMM and the two gradient GEMMs, from W_c.
 ss_status enqueue_backward(const uint16_t* H, const int32_t* cand, const int32_t* slot,
                            const float* lse, int64_t T, int64_t V, int64_t C, int64_t D,
                            float cap, float tau, const Targets& tg, int fp8, float scale,
                            int accumulate, uint16_t* dH, float* dW, const Layout& L, char* ws,
-                           int nsm, cudaStream_t s, bool after_merge = false) {
+                           int nsm, cudaStream_t s) {
   if (fp8 == 2)
     return enqueue_backward_fp8(cand, slot, lse, T, V, C, D, cap, tau, scale, accumulate, dH, dW,
-                                L, ws, nsm, s, after_merge);
+                                L, ws, nsm, s);
   int* status = reinterpret_cast<int*>(ws + L.hdr);
   uint16_t* Wc = reinterpret_cast<uint16_t*>(ws + L.wc);
   uint16_t* G = reinterpret_cast<uint16_t*>(ws + L.g);
@@ -979,7 +967,7 @@ ss_status enqueue_backward(const uint16_t* H, const int32_t* cand, const int32_t
   trace_pre(s, "gemm_softmax_grad");
   cudaError_t e =
       launch_softmax_grad(tH, tWc, tWc2, tGk, iT, iC, iD, slot, lse, scale, cap, tau, tg, amax,
-                          status, nsm, s, after_merge);
+                          status, nsm, s);
   trace_post(s);
   if (e != cudaSuccess) return fail("launch gemm_softmax_grad", e);
   trace_pre(s, "gemm_grads");
@@ -1283,18 +1271,10 @@ static ss_status step_impl(const int32_t* targets, const uint16_t* H, const uint
   if (fp8 == 0 && !(cap > kStoredCapMax))
     return enqueue_step_stored(H, cand, slot, T, V, C, D, head_cap(cap, tau), tg, scale,
                                accumulate, loss, lse, dH, dW, L, ws, nsm, s);
-  // the softmax-gradient GEMM's mainloop beside the LSE merge: measured with
-  // the plain bf16 head (one partial per row and logit tile); the heads whose
-  // merge folds two per tile keep the wide merge and the full wait, and so do
-  // the batches where that GEMM runs on CTA pairs (always a full wait)
-  const bool overlap_merge =
-      fwd_groups(cap, fp8 != 0, tg.K) == 1 &&
-      !softmax_grad_on_pairs(static_cast<int>(T), static_cast<int>(C), nsm);
-  r = enqueue_forward(H, slot, T, C, D, cap, tau, tg, fp8, loss, lse, L, ws, nsm, s,
-                      overlap_merge);
+  r = enqueue_forward(H, slot, T, C, D, cap, tau, tg, fp8, loss, lse, L, ws, nsm, s);
   if (r != SS_OK) return r;
   return enqueue_backward(H, cand, slot, lse, T, V, C, D, cap, tau, tg, fp8, scale, accumulate, dH,
-                          dW, L, ws, nsm, s, overlap_merge);
+                          dW, L, ws, nsm, s);
 }
 
 // K targets per token with host weights w[0..K): 1 <= K <= kMaxTargets, each

@@ -35,26 +35,26 @@ cudaError_t launch_softmax_grad(const CUtensorMap& tH, const CUtensorMap& tWc,
                                 const CUtensorMap& tG_store, int T, int C, int D,
                                 const int32_t* slot, const float* lse, float scale, float cap,
                                 float tau, const Targets& tg, const float* amax, int* status,
-                                int num_sms, cudaStream_t stream, bool late_wait) {
+                                int num_sms, cudaStream_t stream) {
   if (amax) {
     const HeadCap h = head_cap(cap, tau);
     return cap > 0.f ? softmax_grad<true, 1, true>(tH, tWc, tWc_half, tG_store, T, C, D, slot,
                                                    lse, scale, h, tg, amax, status, num_sms,
-                                                   stream, late_wait)
+                                                   stream, false)
                      : softmax_grad<false, 1, true>(tH, tWc, tWc_half, tG_store, T, C, D, slot,
                                                     lse, scale, h, tg, amax, status, num_sms,
-                                                    stream, late_wait);
+                                                    stream, false);
   }
   if (tg.K > 1)
     return launch_softmax_grad_mtp(tH, tWc, tWc_half, tG_store, T, C, D, slot, lse, scale, cap,
-                                   tau, tg, status, num_sms, stream, late_wait);
+                                   tau, tg, status, num_sms, stream);
   const HeadCap h = head_cap(cap, tau);
   return cap > 0.f ? softmax_grad<true, 1>(tH, tWc, tWc_half, tG_store, T, C, D, slot, lse,
                                            scale, h, tg, nullptr, status, num_sms, stream,
-                                           late_wait)
+                                           false)
                    : softmax_grad<false, 1>(tH, tWc, tWc_half, tG_store, T, C, D, slot, lse,
                                             scale, h, tg, nullptr, status, num_sms, stream,
-                                            late_wait);
+                                            false);
 }
 
 // The stored-probability forward and its fallback, one target per token
@@ -95,7 +95,7 @@ cudaError_t softmax_grad_fp8(const CUtensorMap& tH8, const CUtensorMap& tW8,
                              const CUtensorMap& tG8_store, const CUtensorMap& tG8t_store, int T,
                              int C, int D, const int32_t* slot, const float* lse, float cap,
                              float tau, int g8e, const float* amax, int* status, int num_sms,
-                             cudaStream_t stream, bool late_wait) {
+                             cudaStream_t stream) {
   typename EpiG8T<CAP>::Params ep;
   ep.tmG = tG8_store;
   ep.tmGt = tG8t_store;
@@ -107,8 +107,7 @@ cudaError_t softmax_grad_fp8(const CUtensorMap& tH8, const CUtensorMap& tW8,
   ep.amax = amax;
   ep.head = head_cap(cap, tau);
   ep.g8e = g8e;
-  GemmShape shp{(T + BM - 1) / BM, (C + kBnLogits - 1) / kBnLogits, D / (2 * BK),
-                late_wait ? 1 : 0};
+  GemmShape shp{(T + BM - 1) / BM, (C + kBnLogits - 1) / kBnLogits, D / (2 * BK)};
   return launch_gemm<kBnLogits, kStagesGradF8, false, false, EpiG8T<CAP>, 8, true>(
       tH8, tW8, shp, ep, status, num_sms, stream);
 }
@@ -117,13 +116,11 @@ cudaError_t launch_softmax_grad_fp8(const CUtensorMap& tH8, const CUtensorMap& t
                                     const CUtensorMap& tG8_store, const CUtensorMap& tG8t_store,
                                     int T, int C, int D, const int32_t* slot, const float* lse,
                                     float cap, float tau, int g8e, const float* amax, int* status,
-                                    int num_sms, cudaStream_t stream, bool late_wait) {
+                                    int num_sms, cudaStream_t stream) {
   return cap > 0.f ? softmax_grad_fp8<true>(tH8, tW8, tG8_store, tG8t_store, T, C, D, slot, lse,
-                                            cap, tau, g8e, amax, status, num_sms, stream,
-                                            late_wait)
+                                            cap, tau, g8e, amax, status, num_sms, stream)
                    : softmax_grad_fp8<false>(tH8, tW8, tG8_store, tG8t_store, T, C, D, slot, lse,
-                                             cap, tau, g8e, amax, status, num_sms, stream,
-                                             late_wait);
+                                             cap, tau, g8e, amax, status, num_sms, stream);
 }
 
 }  // namespace ss

@@ -22,15 +22,14 @@ cudaError_t launch_softmax_grad_mtp(const CUtensorMap& tH, const CUtensorMap& tW
                                     const CUtensorMap& tWc_half, const CUtensorMap& tG_store,
                                     int T, int C, int D, const int32_t* slot, const float* lse,
                                     float scale, float cap, float tau, const Targets& tg,
-                                    int* status, int num_sms, cudaStream_t stream,
-                                    bool late_wait) {
+                                    int* status, int num_sms, cudaStream_t stream) {
   const HeadCap h = head_cap(cap, tau);
   return cap > 0.f ? softmax_grad<true, kMaxTargets>(tH, tWc, tWc_half, tG_store, T, C, D, slot,
                                                      lse, scale, h, tg, nullptr, status, num_sms,
-                                                     stream, late_wait)
+                                                     stream, false)
                    : softmax_grad<false, kMaxTargets>(tH, tWc, tWc_half, tG_store, T, C, D, slot,
                                                       lse, scale, h, tg, nullptr, status,
-                                                      num_sms, stream, late_wait);
+                                                      num_sms, stream, false);
 }
 
 cudaError_t launch_forward_stored_mtp(const CUtensorMap& tH, const CUtensorMap& tWc,

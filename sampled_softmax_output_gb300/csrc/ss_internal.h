@@ -117,15 +117,12 @@ cudaError_t launch_forward_logits(const CUtensorMap& tH, const CUtensorMap& tWc,
 // and 128 x 256 bytes), amax[2] their tensors' max |x|; plain logits, one
 // target per token.
 // G is written through tG_store: G [T, C] bf16, box 64 x 128, 128-byte swizzle.
-// late_wait: the kernel just before this one in the stream writes lse and
-// nothing else this one reads, so the mainloop may start before it has
-// finished (GemmShape::late_wait).
 cudaError_t launch_softmax_grad(const CUtensorMap& tH, const CUtensorMap& tWc,
                                 const CUtensorMap& tWc_half,
                                 const CUtensorMap& tG_store, int T, int C, int D,
                                 const int32_t* slot, const float* lse, float scale, float cap,
                                 float tau, const Targets& tg, const float* amax, int* status,
-                                int num_sms, cudaStream_t stream, bool late_wait = false);
+                                int num_sms, cudaStream_t stream);
 // FP8 gradients (one target; cap > 0: the capped head): tH8 / tW8 as for
 // amax above; G8 = e5m2(2^g8e (P - Y) dz/ds) [T, C] through tG8_store (box
 // 64 x 128 bytes, 64-byte swizzle) and G8^T [C, T] through tG8t_store (box
@@ -134,7 +131,7 @@ cudaError_t launch_softmax_grad_fp8(const CUtensorMap& tH8, const CUtensorMap& t
                                     const CUtensorMap& tG8_store, const CUtensorMap& tG8t_store,
                                     int T, int C, int D, const int32_t* slot, const float* lse,
                                     float cap, float tau, int g8e, const float* amax, int* status,
-                                    int num_sms, cudaStream_t stream, bool late_wait = false);
+                                    int num_sms, cudaStream_t stream);
 // The forward that keeps the probabilities for the backward (bf16 head,
 // plain or capped with cap <= kStoredCapMax, tg.K targets per token): Pt in
 // bf16 through tP (as tG_store above) -- exp(S - r) with r[t] the row's
@@ -181,8 +178,7 @@ cudaError_t launch_softmax_grad_mtp(const CUtensorMap& tH, const CUtensorMap& tW
                                     const CUtensorMap& tWc_half, const CUtensorMap& tG_store,
                                     int T, int C, int D, const int32_t* slot, const float* lse,
                                     float scale, float cap, float tau, const Targets& tg,
-                                    int* status, int num_sms, cudaStream_t stream,
-                                    bool late_wait = false);
+                                    int* status, int num_sms, cudaStream_t stream);
 
 // ---- gradient GEMMs (ss_gemm_grads.cu)
 // dH = G . W_c : A = G [T, C] (K-major), B = W_c [C, D] (MN-major)
