@@ -85,7 +85,7 @@ struct GemmShape {
   // tiles free them; each CTA waits for it before exiting, so that the kernels
   // after this one, which wait for this one, also find that one finished.
   int late_wait;
-  // k_gemm only: the units cover the column tiles [n_begin, n_tiles) (0: all)
+  // the units cover the column tiles [n_begin, n_tiles) (0: all)
   int n_begin;
   // non-null: the kernel does its work only if *gate != 0, read once the
   // kernels before it have completed (no late_wait); else every CTA returns
