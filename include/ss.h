@@ -205,10 +205,11 @@ ss_status ss_backward_head(const uint16_t* H, const uint16_t* W, const int32_t* 
  * arguments and results as those three calls. The candidate rows W[cand] are
  * gathered once and serve both passes (the separate ss_backward gathers them
  * again, since it cannot know whether W or cand changed after ss_forward).
- * With the bf16 head and one target of weight 1 (plain, or capped with
- * cap <= 64) the logits are computed once: the forward keeps exp(S - r) in
- * bf16 for the backward (r a per-row reference; with the cap, exp(z - cap)
- * dz/ds) instead of the backward recomputing them. The results then equal
+ * With bf16 operands (the plain head, or the capped head with cap <= 64;
+ * also in ss_step_mtp, any targets and weights) the logits are computed
+ * once: the forward keeps exp(S - r) in bf16 for the backward (r a per-row
+ * reference; with the cap, exp(z - cap) dz/ds) instead of the backward
+ * recomputing them. The results then equal
  * the three calls' within the library's tolerances (loss and lse 1e-3
  * relative, dH and dW 2e-2 relative Frobenius) rather than bit for bit; a row
  * whose logits exceed the reference's range makes the step recompute the
