@@ -453,22 +453,29 @@ def run_native(args, world, rank, local):
     torch.cuda.synchronize()
     three_calls_ms = sum(a.elapsed_time(b) for a, b in zip(s3, e3)) / K3 if K3 else None
 
-    # the same step replayed from a CUDA graph of ss_step (ss_step_graph_*)
-    graph_ms = None
+    # the same step replayed from a CUDA graph of ss_step (ss_step_graph_*),
+    # alternating with direct ss_step calls (graph first on even k, direct
+    # first on odd k): under the power cap the clock drifts from region to
+    # region, and the two are compared within one region
+    graph_ms = beside_graph_ms = None
     if n_tg == 1:
         graph = ss.StepGraph(H, W, targets, C, ws, scale=scale, cand=cand, slot=slot, loss=loss,
                              lse=lse, dH=dH, dW=dW, cap=cap, tau=tau, fp8=fp8)
         graph.launch(w.seed)
-        sg = [torch.cuda.Event(enable_timing=True) for _ in range(K3)]
-        eg = [torch.cuda.Event(enable_timing=True) for _ in range(K3)]
+        timed = {"graph": [], "direct": []}
         torch.cuda.synchronize()
         for k in range(K3):
-            flush.zero_()
-            sg[k].record()
-            graph.launch(w.seed)
-            eg[k].record()
+            pair = (("graph", lambda: graph.launch(w.seed)), ("direct", step))
+            for name, fn in (pair if k % 2 == 0 else pair[::-1]):
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                flush.zero_()
+                a.record()
+                fn()
+                b.record()
+                timed[name].append((a, b))
         torch.cuda.synchronize()
-        graph_ms = sum(a.elapsed_time(b) for a, b in zip(sg, eg)) / K3
+        graph_ms = sum(a.elapsed_time(b) for a, b in timed["graph"]) / K3
+        beside_graph_ms = sum(a.elapsed_time(b) for a, b in timed["direct"]) / K3
         graph.close()
         st, _ = ss.read_status(ws)
         if st != 0:
@@ -607,6 +614,7 @@ def run_native(args, world, rank, local):
                    **({"target_weights": mtp_weights} if n_tg > 1 else {}),
                    "ms_per_step_three_calls": three_calls_ms,
                    "ms_per_step_graph": graph_ms,
+                   "ms_per_step_beside_graph": beside_graph_ms,
                    "step_tflops_algorithmic_6TCD": step_tflops,
                    "pct_bf16_peak_algorithmic": 100.0 * step_tflops / peaks["bf16_tflops"],
                    "step_flops_executed": executed_flops_step,
