@@ -224,7 +224,7 @@ REJECTING_REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown"
 PINNED_LOW_FRAC = 0.8
 
 
-def clock_verdict(clocks: dict) -> dict:
+def clock_check(clocks: dict) -> dict:
     """Whether the clock record of a timed region voids its number, and why:
     a hardware or thermal slowdown, or the SM clock held well below its
     maximum with no reason active ("pinned_low")."""
@@ -407,15 +407,15 @@ def run_native(args, world, rank, local):
         torch.cuda.synchronize()
         clk = sampler.stop()
         barrier(world)
-        clk["verdict"] = clock_verdict(clk)
+        clk["check"] = clock_check(clk)
         return sum(s.elapsed_time(e) for s, e in zip(starts, ends)), clk
 
     total_ms, clocks = timed_region()
     # a slowdown or a held-down clock on any rank voids the number: every rank
     # takes the region once more (the decision is the same on all of them)
-    if max_over_ranks(float(clocks["verdict"]["rejected"]), world, dev) > 0:
+    if max_over_ranks(float(clocks["check"]["rejected"]), world, dev) > 0:
         first = {"ms_per_step": total_ms / K, "sm_mhz": clocks.get("sm_mhz"),
-                 "reasons": clocks.get("reasons"), "why": clocks["verdict"]["why"]}
+                 "reasons": clocks.get("reasons"), "why": clocks["check"]["why"]}
         total_ms, clocks = timed_region()
         clocks["first_attempt"] = first
     total_ms_max = max_over_ranks(total_ms, world, dev)

@@ -119,18 +119,18 @@ def test_clock_record_parsing(tmp_path):
     assert c["samples"] == 0 and c["sm_mhz"] is None
 
 
-def test_clock_verdict(tmp_path):
+def test_clock_check(tmp_path):
     ok = _sampled(tmp_path, [_row("GPU-aaaa", 2000, 2070, 900.0)])
-    assert bench.clock_verdict(ok) == {"rejected": False, "why": []}
+    assert bench.clock_check(ok) == {"rejected": False, "why": []}
     # the power cap lowers the clock and is kept
     capped = _sampled(tmp_path, [_row("GPU-aaaa", 1400, 2070, 1400.0, ("sw_power_cap",))])
-    assert bench.clock_verdict(capped) == {"rejected": False, "why": []}
+    assert bench.clock_check(capped) == {"rejected": False, "why": []}
     for reason in ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown"):
         c = _sampled(tmp_path, [_row("GPU-aaaa", 1900, 2070, 900.0, (reason, "sw_power_cap"))])
-        assert bench.clock_verdict(c) == {"rejected": True, "why": [reason]}
+        assert bench.clock_check(c) == {"rejected": True, "why": [reason]}
     # held well below the maximum with no reason: a leftover clock lock
     low = _sampled(tmp_path, [_row("GPU-aaaa", 1200, 2070, 600.0)])
-    assert bench.clock_verdict(low) == {"rejected": True, "why": ["pinned_low"]}
+    assert bench.clock_check(low) == {"rejected": True, "why": ["pinned_low"]}
     # no clock record: nothing to reject on
-    assert bench.clock_verdict({"samples": 0, "sm_mhz": None, "sm_max_mhz": None,
+    assert bench.clock_check({"samples": 0, "sm_mhz": None, "sm_max_mhz": None,
                                 "reasons": ["no nvidia-smi"]})["rejected"] is False
