@@ -260,6 +260,12 @@ def max_over_ranks(x: float, world: int, device=None) -> float:
     return float(t.item())
 
 
+def any_rank_rejected(check: dict, world: int, device=None) -> bool:
+    """True on every rank if the clock check of any rank rejected its timed
+    region, so that all ranks take the region again together."""
+    return max_over_ranks(float(check["rejected"]), world, device) > 0
+
+
 def barrier(world: int):
     if world > 1:
         import torch.distributed as dist
@@ -413,7 +419,7 @@ def run_native(args, world, rank, local):
     total_ms, clocks = timed_region()
     # a slowdown or a held-down clock on any rank voids the number: every rank
     # takes the region once more (the decision is the same on all of them)
-    if max_over_ranks(float(clocks["check"]["rejected"]), world, dev) > 0:
+    if any_rank_rejected(clocks["check"], world, dev):
         first = {"ms_per_step": total_ms / K, "sm_mhz": clocks.get("sm_mhz"),
                  "reasons": clocks.get("reasons"), "why": clocks["check"]["why"]}
         total_ms, clocks = timed_region()

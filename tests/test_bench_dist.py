@@ -1,5 +1,6 @@
 """Multi-process host logic of bench.py on CPU with the gloo backend
-(world_size 2): the max-over-ranks timing reduction, the barrier, and the
+(world_size 2): the max-over-ranks timing reduction, the barrier, the
+decision to take a timed region again when any rank's clock record is void, and the
 torchrun launch of the reference arm, where rank 0 alone prints one JSON line.
 The CUDA path itself runs replicas only (no collective on the data path)."""
 import json
@@ -29,7 +30,10 @@ def _worker(rank, world, port, q):
     dist.init_process_group("gloo")
     bench.barrier(world)
     m = bench.max_over_ranks(10.0 * (rank + 1), world)
-    q.put((rank, m))
+    # rank 0's clock record is void, rank 1's is not: both take the region again
+    again = bench.any_rank_rejected({"rejected": rank == 0, "why": []}, world)
+    neither = bench.any_rank_rejected({"rejected": False, "why": []}, world)
+    q.put((rank, m, again, neither))
     dist.destroy_process_group()
 
 
@@ -45,7 +49,7 @@ def test_max_over_ranks_gloo():
         p.join(120)
         assert p.exitcode == 0
     got = sorted(q.get(timeout=10) for _ in range(world))
-    assert got == [(0, 20.0), (1, 20.0)]
+    assert got == [(0, 20.0, True, False), (1, 20.0, True, False)]
 
 
 def test_reference_arm_under_torchrun():
